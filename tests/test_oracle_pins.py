@@ -1,0 +1,382 @@
+"""Pins of the float64 oracle against facts the pages and the mathematics fix.
+
+Each test checks the oracle's behaviour (not a retyped formula) against: a worked example
+printed on the pages, a closed form or optimality condition, a library routine, an exact
+enumeration of the outcome law, or a large-sample statistic.
+"""
+import math
+
+import numpy as np
+import pytest
+import scipy.optimize
+import scipy.special
+import scipy.stats
+
+import oracle
+from synth import philox
+from tests.exact_law import outcome_law, position_marginals
+
+
+def softmax(x, T=1.0):
+    return scipy.special.softmax(np.asarray(x, dtype=np.float64) / T, axis=-1)
+
+
+# --------------------------------------------------------------------------------------
+# Input generator
+# --------------------------------------------------------------------------------------
+
+def test_philox_known_answers():
+    """Philox4x32-10 known-answer vectors published with the Random123 library."""
+    cases = [
+        ([0, 0, 0, 0], [0, 0], [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]),
+        ([0xFFFFFFFF] * 4, [0xFFFFFFFF] * 2, [0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD]),
+        ([0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344], [0xA4093822, 0x299F31D0],
+         [0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1]),
+    ]
+    for ctr, key, want in cases:
+        got = philox.philox4x32_10(np.array([ctr]), np.array(key))[0]
+        assert [int(v) for v in got] == want
+
+
+def test_uniforms_range_and_moments():
+    u = philox.uniforms(7, philox.STREAM_ACCEPT, 3, 1000, 100)
+    assert u.min() >= 0.0 and u.max() < 1.0
+    assert abs(u.mean() - 0.5) < 0.005 and abs(u.var() - 1 / 12) < 0.002
+    # different streams / rounds give different numbers
+    assert not np.array_equal(u, philox.uniforms(7, philox.STREAM_RESIDUAL, 3, 1000, 100))
+
+
+# --------------------------------------------------------------------------------------
+# Distributions
+# --------------------------------------------------------------------------------------
+
+def test_softmax_and_lse_match_scipy():
+    rng = np.random.default_rng(0)
+    x = rng.normal(0, 3, size=(5, 1000))
+    for T in (0.5, 0.8, 1.0, 2.0):
+        q, lse = oracle.softmax_t(x, np.full(5, T))
+        np.testing.assert_allclose(lse, scipy.special.logsumexp(x / T, axis=-1), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(q, softmax(x, T), rtol=1e-12, atol=1e-300)
+
+
+def test_greedy_row_is_first_argmax():
+    x = np.array([[1.0, 3.0, 3.0, -2.0], [5.0, 5.0, 5.0, 5.0]])
+    d, lse, _ = oracle.row_distribution(x, 0.0, 1.0)
+    np.testing.assert_array_equal(d, [[0, 1, 0, 0], [1, 0, 0, 0]])
+    assert np.all(np.isnan(lse))
+
+
+def test_nucleus_hand_examples():
+    p = np.array([0.1, 0.5, 0.05, 0.3, 0.05])
+    x = np.log(p)
+    d, _, _ = oracle.row_distribution(x, 1.0, 0.75)          # {1, 3}: .5 + .3 >= .75
+    np.testing.assert_allclose(d, [0, 0.625, 0, 0.375, 0], atol=1e-15)
+    d, _, _ = oracle.row_distribution(x, 1.0, 0.85)          # {1, 3, 0}
+    np.testing.assert_allclose(d, np.array([0.1, 0.5, 0, 0.3, 0]) / 0.9, atol=1e-15)
+    d, _, _ = oracle.row_distribution(x, 1.0, 0.3)           # the top token alone
+    np.testing.assert_allclose(d, [0, 1, 0, 0, 0], atol=1e-15)
+    # equal probabilities: the lowest ids are kept
+    d, _, _ = oracle.row_distribution(np.zeros(5), 1.0, 0.5)
+    np.testing.assert_allclose(d, [1 / 3, 1 / 3, 1 / 3, 0, 0], atol=1e-15)
+    # top_p = 1 is no filter, bit for bit
+    y = np.random.default_rng(1).normal(size=(3, 50))
+    a, _, _ = oracle.row_distribution(y, 0.7, 1.0)
+    np.testing.assert_array_equal(a, oracle.softmax_t(y, np.full(3, 0.7))[0])
+
+
+def test_inverse_cdf_hand_example():
+    w = np.array([0.1, 0.0, 0.3, 0.6])
+    for u, want in [(0.0, 0), (0.0999, 0), (0.1, 2), (0.3999, 2), (0.4, 3), (0.999, 3)]:
+        t, R = oracle.inverse_cdf(w, u)
+        assert int(t) == want, (u, t)
+        assert R == pytest.approx(1.0)
+
+
+# --------------------------------------------------------------------------------------
+# Theorem 19 worked example (SSD notes §4.4): F=2, C=47/147
+# --------------------------------------------------------------------------------------
+
+P_T = np.array([0.48, 0.48, 0.02, 0.02])
+P_D = np.array([0.49, 0.49, 0.01, 0.01])
+C19 = 47.0 / 147.0
+
+
+def test_theorem19_transformed_draft():
+    p2, p_top, zp = oracle.saguaro_transform(P_D, np.log(P_D), 2, C19)
+    np.testing.assert_allclose(p2, [0.47, 0.47, 0.03, 0.03], rtol=0, atol=1e-15)
+    assert p_top == pytest.approx(0.98, abs=1e-15)
+    # acceptance alpha = sum min(p, q) is 0.98 before and after
+    assert np.minimum(P_D, P_T).sum() == pytest.approx(0.98, abs=1e-15)
+    assert np.minimum(p2, P_T).sum() == pytest.approx(0.98, abs=1e-15)
+
+
+def _hit_given_reject(F, C):
+    """P(cache hit | first draft token rejected) for the Theorem 19 rows, K = 1.
+
+    For each draft token s, the verify rule's exact outcome law (black-box bisection) gives
+    P(k=0, t*=v | s); the cache is the oracle's depth-0 keys (top-2 draft tokens excluding s).
+    """
+    tgt = np.log(np.stack([P_T, P_T]))
+    drf = np.log(np.stack([P_D, P_D]))
+    p_draft = oracle.saguaro_transform(P_D, np.log(P_D), F, C)[0] if F else P_D
+    f_int = [2, 2]
+    num = den = 0.0
+    for s in range(4):
+        keys = oracle.cache_keys(drf[None], np.array([[s]]), f_int)
+        law_s = outcome_law(oracle.verify, tgt, drf, [np.eye(4)[s]], F=F, C=C)
+        for (k, toks), pr in law_s.items():
+            if k == 0:
+                hit = oracle.cache_lookup([0], np.array([[toks[0], -1]]), keys, f_int)[0]
+                den += p_draft[s] * pr
+                num += p_draft[s] * pr * hit
+    return num / den
+
+
+def test_theorem19_hit_rate_rises_from_half_to_one():
+    assert _hit_given_reject(0, 1.0) == pytest.approx(0.5, abs=1e-12)
+    assert _hit_given_reject(2, C19) == pytest.approx(1.0, abs=1e-12)
+
+
+# --------------------------------------------------------------------------------------
+# Verification: exact outcome law (lossless, mass identities, accept-length law)
+# --------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_exact_law_is_target_law_V3_K2(seed):
+    """Brute force on V=3, K=2: committed tokens follow q position by position
+    (SSD notes §2.2: output law equals the target's autoregressive law)."""
+    rng = np.random.default_rng(seed)
+    tgt = rng.normal(0, 1.5, size=(3, 3))
+    drf = 0.5 * tgt[:2] + rng.normal(0, 1.0, size=(2, 3))
+    q, p = softmax(tgt), softmax(drf)
+    law = outcome_law(oracle.verify, tgt, drf, p)
+    assert sum(law.values()) == pytest.approx(1.0, abs=1e-12)
+    joint, exists = position_marginals(law, 2, 3)
+    # position 1 always exists and follows q_1; later positions follow q_i when present
+    np.testing.assert_allclose(joint[0], q[0], atol=1e-12)
+    for i in (1, 2):
+        np.testing.assert_allclose(joint[i], exists[i] * q[i], atol=1e-12)
+    # independence of consecutive committed tokens (rows do not depend on context here)
+    pair = np.zeros((3, 3))
+    for (k, toks), pr in law.items():
+        if len(toks) >= 2:
+            pair[toks[0], toks[1]] += pr
+    alpha1 = np.minimum(p[0], q[0]).sum()
+    np.testing.assert_allclose(pair, np.outer(np.minimum(p[0], q[0]) / alpha1, q[1]) * exists[1],
+                               atol=1e-12)
+
+
+def test_mass_identities_single_position():
+    """SpS notes §3: accepting gives token x the mass min(p, q); the total rejection
+    probability is sum (q - p)_+; the residual draw gives (q - p)_+ and the two add to q."""
+    rng = np.random.default_rng(5)
+    V = 5
+    tgt = rng.normal(0, 2, size=(2, V))
+    drf = rng.normal(0, 2, size=(1, V))
+    q, p = softmax(tgt), softmax(drf)
+    law = outcome_law(oracle.verify, tgt, drf, p)
+    acc = np.zeros(V)
+    res = np.zeros(V)
+    for (k, toks), pr in law.items():
+        if k == 1:
+            acc[toks[0]] += pr
+        else:
+            res[toks[0]] += pr
+    np.testing.assert_allclose(acc, np.minimum(p[0], q[0]), atol=1e-13)
+    np.testing.assert_allclose(res, np.maximum(q[0] - p[0], 0.0), atol=1e-13)
+    assert res.sum() == pytest.approx(np.maximum(q[0] - p[0], 0).sum(), abs=1e-13)
+    np.testing.assert_allclose(acc + res, q[0], atol=1e-13)
+
+
+def test_accept_length_geometric_law():
+    """SSD notes §4.3: with every position accepting at rate a, exactly j tokens are
+    accepted with probability a^j (1 - a) for j < K and a^K for j = K."""
+    rng = np.random.default_rng(9)
+    row_t = rng.normal(0, 1.5, size=3)
+    row_d = rng.normal(0, 1.5, size=3)
+    K = 3
+    tgt = np.stack([row_t] * (K + 1))
+    drf = np.stack([row_d] * K)
+    p = softmax(drf)
+    a = np.minimum(softmax(row_t), softmax(row_d)).sum()
+    law = outcome_law(oracle.verify, tgt, drf, p)
+    pk = np.zeros(K + 1)
+    for (k, _), pr in law.items():
+        pk[k] += pr
+    want = [a ** j * (1 - a) for j in range(K)] + [a ** K]
+    np.testing.assert_allclose(pk, want, atol=1e-12)
+
+
+def test_identical_draft_accepts_everything():
+    rng = np.random.default_rng(3)
+    B, K, V = 64, 4, 50
+    tgt = rng.normal(0, 2, size=(B, K + 1, V))
+    u = rng.random((B, K + 1))
+    toks = rng.integers(0, V, size=(B, K))
+    r = oracle.verify(tgt, tgt[:, :K], toks, u, np.ones(B), np.ones(B))
+    assert np.all(r["accept_len"] == K)
+    # the bonus token is the inverse CDF of q_{K+1} at the residual uniform
+    q = softmax(tgt[:, K])
+    want = [int(np.searchsorted(np.cumsum(q[b]), u[b, K] * np.cumsum(q[b])[-1], side="right"))
+            for b in range(B)]
+    np.testing.assert_array_equal(r["out_tokens"][:, K], want)
+
+
+def test_single_token_vocabulary():
+    B, K = 5, 3
+    tgt = np.zeros((B, K + 1, 1))
+    r = oracle.verify(tgt, tgt[:, :K], np.zeros((B, K), int), np.random.default_rng(0).random((B, K + 1)),
+                      np.ones(B), np.ones(B))
+    assert np.all(r["accept_len"] == K) and np.all(r["out_tokens"] == 0)
+
+
+def test_identity_transforms_are_plain_verify():
+    rng = np.random.default_rng(4)
+    B, K, V = 16, 3, 40
+    tgt = rng.normal(0, 2, size=(B, K + 1, V))
+    drf = rng.normal(0, 2, size=(B, K, V))
+    toks = rng.integers(0, V, size=(B, K))
+    u = rng.random((B, K + 1))
+    base = oracle.verify(tgt, drf, toks, u, np.ones(B), np.ones(B))
+    for F, C in [(0, 0.3), (8, 1.0)]:
+        other = oracle.verify(tgt, drf, toks, u, np.ones(B), np.ones(B), F, C)
+        np.testing.assert_array_equal(base["out_tokens"], other["out_tokens"])
+        np.testing.assert_array_equal(base["ratio"], other["ratio"])
+
+
+def test_greedy_verify_hand_example():
+    """Mirror-SD notes §2 step 3: longest prefix equal to the target argmax, then the
+    target argmax as the correction."""
+    V = 6
+    tgt = np.full((1, 4, V), -1.0)
+    for j, a in enumerate([2, 4, 1, 5]):
+        tgt[0, j, a] = 3.0
+    drf = np.zeros((1, 3, V))
+    u = np.full((1, 4), 0.5)
+    r = oracle.verify(tgt, drf, np.array([[2, 4, 0]]), u, np.zeros(1), np.ones(1))
+    assert r["accept_len"][0] == 2 and list(r["out_tokens"][0]) == [2, 4, 1, -1]
+    r = oracle.verify(tgt, drf, np.array([[2, 4, 1]]), u, np.zeros(1), np.ones(1))
+    assert r["accept_len"][0] == 3 and list(r["out_tokens"][0]) == [2, 4, 1, 5]
+    r = oracle.verify(tgt, drf, np.array([[0, 4, 1]]), u, np.zeros(1), np.ones(1))
+    assert r["accept_len"][0] == 0 and list(r["out_tokens"][0]) == [2, -1, -1, -1]
+
+
+@pytest.mark.parametrize("K", [1, 3])
+def test_chi_square_committed_tokens_V8(K):
+    """SpS notes §6: check the distribution with large-sample token statistics.
+    10^6 sequences on V=8; committed tokens at every position against q, and the
+    accept-length histogram against the product of per-position acceptance rates."""
+    rng = np.random.default_rng(100 + K)
+    V = 8
+    row_t = rng.normal(0, 1.5, size=(K + 1, V))
+    row_d = 0.6 * row_t[:K] + rng.normal(0, 1.0, size=(K, V))
+    q, p = softmax(row_t), softmax(row_d)
+    n_total, chunk = 1_000_000, 100_000
+    counts = np.zeros((K + 1, V))
+    klen = np.zeros(K + 1)
+    for c in range(n_total // chunk):
+        u_d = philox.uniforms(11, philox.STREAM_DRAFT, c, chunk, K)
+        u_v = np.concatenate([philox.uniforms(11, philox.STREAM_ACCEPT, c, chunk, K),
+                              philox.uniforms(11, philox.STREAM_RESIDUAL, c, chunk, 1)], axis=1)
+        tgt = np.broadcast_to(row_t, (chunk, K + 1, V))
+        drf = np.broadcast_to(row_d, (chunk, K, V))
+        toks = oracle.draft_sample(drf, u_d, np.ones(chunk), np.ones(chunk))["tokens"]
+        r = oracle.verify(tgt, drf, toks, u_v, np.ones(chunk), np.ones(chunk))
+        k = r["accept_len"]
+        klen += np.bincount(k, minlength=K + 1)
+        for i in range(K + 1):
+            present = k >= i
+            counts[i] += np.bincount(r["out_tokens"][present, i], minlength=V)
+    for i in range(K + 1):
+        n = counts[i].sum()
+        stat, pval = scipy.stats.chisquare(counts[i], n * q[i])
+        assert pval > 0.01, (i, pval)
+    a = np.minimum(p, q[:K]).sum(axis=1)
+    want = np.array([np.prod(a[:j]) * (1 - a[j]) for j in range(K)] + [np.prod(a)])
+    stat, pval = scipy.stats.chisquare(klen, n_total * want)
+    assert pval > 0.01, pval
+
+
+# --------------------------------------------------------------------------------------
+# Theorem 12 fan-out (SSD abstract page, "Method")
+# --------------------------------------------------------------------------------------
+
+def _optimal_fanout(budget, a, r, K):
+    """Maximise the hit probability sum_k P(k) (1 - F_k^-r) under sum_k F_k = budget, with
+    the geometric accept-length law P(k) = a^k (1-a) (k < K), a^K (k = K)."""
+    P = np.array([a ** k * (1 - a) for k in range(K)] + [a ** K])
+    obj = lambda f: -np.sum(P * (1.0 - np.power(f, -r)))
+    res = scipy.optimize.minimize(obj, np.full(K + 1, budget / (K + 1)), method="SLSQP",
+                                  bounds=[(1e-6, budget)] * (K + 1),
+                                  constraints=[{"type": "eq", "fun": lambda f: f.sum() - budget}],
+                                  options={"ftol": 1e-15, "maxiter": 1000})
+    return res.x
+
+
+@pytest.mark.parametrize("budget,a,r,K", [(64, 0.7, 1.0, 5), (23, 0.8, 1.0, 5), (100, 0.5, 2.0, 3),
+                                          (40, 0.9, 0.5, 4)])
+def test_fanout_is_the_optimum_of_the_power_law_model(budget, a, r, K):
+    f_real, f_int = oracle.fanout(budget, a, r, K)
+    np.testing.assert_allclose(f_real, _optimal_fanout(budget, a, r, K), rtol=2e-4)
+    assert f_real.sum() == pytest.approx(budget, rel=1e-14)
+    assert f_int.sum() == math.floor(budget)
+    assert np.all(np.abs(f_int - f_real) < 1.0)
+
+
+def test_fanout_budget64_values():
+    f_real, f_int = oracle.fanout(64.0, 0.7, 1.0, 5)
+    np.testing.assert_allclose(f_real, [14.676, 12.279, 10.273, 8.595, 7.191, 10.985], atol=5e-4)
+    assert list(f_int) == [15, 12, 10, 9, 7, 11]
+
+
+# --------------------------------------------------------------------------------------
+# Theorem 15 monotonicity (SSD notes §4.4)
+# --------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_hit_probability_monotone_in_C(seed):
+    """p_hit rises as C falls: the share of the residual draw landing in the down-weighted
+    top-F set, given a rejection, is non-increasing in C on a 21-point grid."""
+    rng = np.random.default_rng(seed)
+    V, F = 6, 2
+    tgt = rng.normal(0, 1.5, size=(2, V))
+    drf = 0.5 * tgt[:1] + rng.normal(0, 1.0, size=(1, V))
+    top = set(np.argsort(-drf[0], kind="stable")[:F].tolist())
+    prev = -1.0
+    for C in np.linspace(0.0, 1.0, 21)[::-1]:
+        p_draft = oracle.saguaro_transform(softmax(drf[0]), drf[0], F, C)[0]
+        law = outcome_law(oracle.verify, tgt, drf, [p_draft], F=F, C=C)
+        rej = sum(pr for (k, _), pr in law.items() if k == 0)
+        hit = sum(pr for (k, t), pr in law.items() if k == 0 and t[0] in top)
+        share = hit / rej
+        assert share >= prev - 1e-12, (C, share, prev)
+        prev = share
+
+
+# --------------------------------------------------------------------------------------
+# Cache keys, lookup, Mirror roots and reuse: hand examples
+# --------------------------------------------------------------------------------------
+
+def test_cache_keys_and_lookup_hand_example():
+    # depth 0 uses draft row 1, excluding s_1; depth 1 (=K) uses draft row 2
+    drf = np.array([[[0.0, 5.0, 5.0, 1.0, 4.0],
+                     [3.0, 0.0, 2.0, 2.0, 1.0]]])
+    keys = oracle.cache_keys(drf, np.array([[1]]), [2, 3])
+    assert list(keys[0]) == [2, 4, 0, 2, 3]           # ties at 5.0 and 2.0 go to the lowest id
+    keys2 = oracle.cache_keys(drf, np.array([[3]]), [2, 3])
+    assert list(keys2[0][:2]) == [1, 2]
+    hit = oracle.cache_lookup([0, 1, 0], np.array([[4, -1], [1, 3], [1, -1]]),
+                              np.repeat(keys, 3, axis=0), [2, 3])
+    assert list(hit) == [1, 1, 0]
+
+
+def test_topk_rows_and_reuse_hand_example():
+    x = np.array([[1.0, 4.0, 4.0, 2.0, -1.0]])
+    ids, logp = oracle.topk_rows(x, 1.0, 3)
+    assert list(ids[0]) == [1, 2, 3]
+    np.testing.assert_allclose(logp[0], np.log(softmax(x[0])[[1, 2, 3]]), atol=1e-14)
+    br = np.array([[[5, 6, 7], [5, 8, 9], [3, 1, 1]]])
+    assert oracle.mirror_reuse(br, [1], np.array([[5, 8, -1, -1]]))[0] == 1
+    assert oracle.mirror_reuse(br, [1], np.array([[5, 2, -1, -1]]))[0] == 0
+    assert oracle.mirror_reuse(br, [0], np.array([[3, -1, -1, -1]]))[0] == 1
+    assert oracle.mirror_reuse(br, [3], np.array([[5, 6, 7, 1]]))[0] == 0    # k = gamma

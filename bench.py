@@ -1,0 +1,355 @@
+#!/usr/bin/env python
+"""Benchmark of libspecverify on the large-batch verification workload.
+
+One step = one sv_verify call over one round of the B=512, K=5, V=128256 bf16 workload (target
+logits for K+1 positions, draft logits for K positions, even sequences greedy), i.e. the whole
+verification path: statistics pass, accept tests, residual / bonus draws, float-float tier.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank verifies its own batch (weak
+scaling, no data-path collective); timing is the maximum over ranks.  --impl reference times
+the float64 oracle on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify rounds/sec (B·(K+1)·V logits) and achieved HBM GB/s vs ~8 TB/s peak"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------------------------------
+# host-side helpers (also exercised by the CPU multi-process tests)
+# ------------------------------------------------------------------------------------------
+def rank_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank verifies its own synthetic batch (weak scaling)."""
+    return base_seed + 1009 * rank
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Units processed by all ranks per second, timed by the slowest rank."""
+    return units_per_rank * world * 1000.0 / ms_max
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.strip().split(", ") for r in self.out.read().strip().splitlines() if r.strip()]
+        os.unlink(self.out.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                for name, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_seconds(tgt, drf, K, seqs, T, u, toks, chunk=32):
+    """Seconds the float64 oracle spends verifying the given sequences one by one.  The exact
+    float64 copies of their logits are made chunk by chunk outside the timed region."""
+    import oracle
+    import torch
+    total = 0.0
+    for i in range(0, len(seqs), chunk):
+        sel = seqs[i:i + chunk]
+        idx = torch.as_tensor(sel, device=tgt.device)
+        t64 = tgt.index_select(0, idx).double().cpu().numpy()
+        d64 = drf.index_select(0, idx)[:, :K].double().cpu().numpy()
+        t0 = time.perf_counter()
+        for j, b in enumerate(sel):
+            oracle.verify(t64[j:j + 1], d64[j:j + 1], toks[b:b + 1], u[b:b + 1], T[b:b + 1], np.ones(1), 0, 1.0)
+        total += time.perf_counter() - t0
+    return total
+
+
+# ------------------------------------------------------------------------------------------
+def workload(rank: int):
+    from synth import workloads as W
+    base = W.LARGE_BATCH
+    return W.scaled(base, seed=rank_seed(base.seed, rank))
+
+
+def config_block(w):
+    rows_read = w.B * (w.K + 1) + (w.B // 2) * w.K
+    return {"workload": "large-batch verify: B=512, K=5, V=128256, bf16 target and draft logits, T=1, "
+                        "even sequences greedy", "B": w.B, "K": w.K, "V": w.V, "dtype": "bf16",
+            "greedy_fraction": 0.5, "l2": "inputs (1.44 GB) exceed L2; no flush between steps",
+            "logit_bytes_read_per_round": rows_read * w.V * 2,
+            "logit_bytes_nominal_per_round": w.B * (w.K + 1) * w.V * 2 * 2}
+
+
+def run_reference(args, rank, world):
+    """The float64 oracle on the host cores (rank 0 only): every step verifies a bounded sample
+    of the round's sequences; the rate is extrapolated to whole 512-sequence rounds."""
+    if rank != 0:
+        return None
+    import torch
+    import oracle
+    from synth import workloads as W
+    w = workload(0)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    tgt, drf = W.logits(w, 0, device=dev)
+    u_draft, u, _ = W.round_uniforms(w, 0)
+    T = W.temperatures(w)
+    per_step = max(1, int(os.environ.get("SV_ORACLE_SEQS", "16")))
+    seqs_all = [s % w.B for s in range(per_step * (args.warmup + args.steps))]
+    toks = np.zeros((w.B, w.K), dtype=np.int64)
+    for b0 in range(0, w.B, 64):
+        d64 = drf[b0:b0 + 64, : w.K].double().cpu().numpy()
+        toks[b0:b0 + 64] = oracle.draft_sample(d64, u_draft[b0:b0 + 64, : w.K], T[b0:b0 + 64],
+                                               np.ones(len(d64)))["tokens"]
+    times = []
+    for i in range(args.warmup + args.steps):
+        sel = seqs_all[i * per_step:(i + 1) * per_step]
+        dt = oracle_seconds(tgt, drf, w.K, sel, T, u, toks)
+        if i >= args.warmup:
+            times.append(dt / len(sel) * w.B)        # seconds per full round
+    sec = statistics.mean(times)
+    value = 1.0 / sec
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1000.0, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_block(w),
+            "cpu_baseline": {"value": value, "unit": "rounds/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{per_step} of 512 sequences per step, single-thread float64 numpy "
+                                       f"oracle, extrapolated to whole rounds"},
+            "e2e": {"value": value, "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import speculative_decoding_verification_gb300 as sv
+    from speculative_decoding_verification_gb300 import build as _build
+    from synth import workloads as W
+
+    _build.build()
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    lib = sv.load()
+    w = workload(rank)
+    K, B, V = w.K, w.B, w.V
+    tgt, drf = W.logits(w, 0, device=dev)
+    u_draft, u, _ = W.round_uniforms(w, 0)
+    T = W.temperatures(w)
+    T_d = torch.as_tensor(T, device=dev)
+    u_d = torch.as_tensor(u, device=dev)
+    # draft tokens: the library's own draft sampler (plain p, no transform) at the draft uniforms
+    toks_d, _, st = sv.sv_saguaro_sample(drf, torch.as_tensor(u_draft[:, :K].copy(), device=dev), T_d, n_rows=K)
+    torch.cuda.synchronize()
+    if sv.read_stats(st)["status"] != 0:
+        raise RuntimeError(f"draft sampling failed: {sv.read_stats(st)}")
+    ws = sv.Workspace()
+    al = torch.empty(B, dtype=torch.int32, device=dev)
+    ot = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    stats = sv.new_stats(dev)
+
+    def step():
+        sv.sv_verify(tgt, drf, toks_d, u_d, T_d, accept_len=al, out_tokens=ot, stats=stats, workspace=ws)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    if sv.read_stats(stats)["status"] != 0:
+        raise RuntimeError(f"verify failed: {sv.read_stats(stats)}")
+
+    # ---- timed region: device time of K steps; the statistics pass timed through the hook ----
+    n = args.steps
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in ev_b + ev_e:
+        e.record()          # torch creates the underlying CUDA event on first record
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start.record()
+    for i in range(n):
+        lib.sv_set_profile_events(ev_b[i].cuda_event, ev_e[i].cuda_event)
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    lib.sv_set_profile_events(None, None)
+    clk = clocks.stop()
+    barrier(world)
+    ms = start.elapsed_time(end) / n
+    k1_ms = statistics.mean(ev_b[i].elapsed_time(ev_e[i]) for i in range(n))
+    ms_max = max_over_ranks(ms, world)
+    value = whole_job_rate(1.0, world, ms_max)
+    final = sv.read_stats(stats)
+    if final["status"] != 0:
+        raise RuntimeError(f"verify failed: {final}")
+
+    # ---- end to end through the public API with host buffers ----
+    tgt_h = tgt.cpu().pin_memory()
+    drf_h = drf.cpu().pin_memory()
+    tok_h = toks_d.cpu().pin_memory()
+    u_h = u_d.cpu().pin_memory()
+    T_h = T_d.cpu().pin_memory()
+    tgt_x = torch.empty_like(tgt)
+    drf_x = torch.empty_like(drf)
+    tok_x, u_x, T_x = torch.empty_like(toks_d), torch.empty_like(u_d), torch.empty_like(T_d)
+    al_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    ot_h = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (tgt_h, drf_h, tok_h, u_h, T_h))
+    d2h = al_h.numel() * 4 + ot_h.numel() * 4
+
+    def e2e_step():
+        for dst, src in ((tgt_x, tgt_h), (drf_x, drf_h), (tok_x, tok_h), (u_x, u_h), (T_x, T_h)):
+            dst.copy_(src, non_blocking=True)
+        sv.sv_verify(tgt_x, drf_x, tok_x, u_x, T_x, accept_len=al, out_tokens=ot, stats=stats, workspace=ws)
+        al_h.copy_(al, non_blocking=True)
+        ot_h.copy_(ot, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    n2 = max(1, min(n, 10))
+    barrier(world)
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record()
+    for _ in range(n2):
+        e2e_step()
+    e2.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2) / n2, world)
+
+    # ---- roofline of the dominant kernel (the statistics pass) ----
+    cfg = config_block(w)
+    k1_bytes = cfg["logit_bytes_read_per_round"]
+    peak, peak_kind = load_peaks()
+    achieved = k1_bytes / (k1_ms * 1e-3) / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world, "steps": n, "warmup": args.warmup,
+            "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": cfg,
+            "hbm_gbs_per_step": k1_bytes / (ms_max * 1e-3) / 1e9,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "kernel": "k_stats",
+                         "peak_source": f"{peak_kind} copy bandwidth", "kernel_ms": k1_ms},
+            "e2e": {"value": whole_job_rate(1.0, world, e2e_ms), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": 5 * n, "clocks": clk,
+            "decisions": {k: final[k] for k in ("accept_tests", "draws", "reresolved", "near_boundary",
+                                                "unresolved")}}
+    # ---- CPU baseline: the oracle on one whole round (rank 0) ----
+    if rank == 0:
+        n_seq = int(os.environ.get("SV_ORACLE_SEQS", str(B)))
+        seqs = list(range(min(n_seq, B)))
+        toks = toks_d.cpu().numpy().astype(np.int64)
+        dt = oracle_seconds(tgt, drf, K, seqs, T, u, toks)
+        line["cpu_baseline"] = {"value": len(seqs) / dt / B, "unit": "rounds/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{len(seqs)} of {B} sequences of the round (half greedy), "
+                                          f"{dt:.1f} s single-thread float64 numpy"}
+    return line if rank == 0 else None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    rank, world, local_rank = rank_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)     # rank 0 alone; no process group needed
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend=backend)
+    line = run_ours(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,277 @@
+/*
+ * specverify.h — C ABI of libspecverify: batched speculative-decoding verification on one GPU.
+ *
+ * The library implements the verification step of speculative decoding over the vocabulary,
+ * plus the draft-side pieces of the SSD / Saguaro method and a Mirror-SD style branch check:
+ *
+ *   sv_verify          accept draft token s_i with probability min(1, q_i(s_i)/p_i(s_i)), stop at
+ *                      the first rejection, then draw the bonus token from (q - p)_+ / sum (q - p)_+
+ *                      at that position, or from q_{K+1} when all K are accepted.
+ *                      ["Speculative Speculative Decoding" notes, §2.2 steps ①-④;
+ *                       "Accelerating LLM Decoding with Speculative Sampling (2023)" notes, §1, §3]
+ *   sv_saguaro_sample  draft sampling under sigma_{F,C}: the top-F draft probabilities are
+ *                      multiplied by C and the row is renormalised.
+ *                      [SSD notes §4.4, Theorems 15 and 19; SSD abstract page, "Method"]
+ *   sv_fanout          Theorem 12 geometric fan-out F_k.            [SSD abstract page, "Method"]
+ *   sv_cache_keys      top-F_k draft tokens per depth, excluding the proposed token.
+ *                                                                    [SSD notes §5.1]
+ *   sv_cache_lookup    hit iff the verification outcome (k, t*) is a key.
+ *                                                                    [SSD abstract page, "Method"]
+ *   sv_topk_rows       top-kappa ids and log-probabilities of logit rows (early-exit roots).
+ *                                                                    [Mirror-SD notes §3.1]
+ *   sv_mirror_reuse    does the committed prefix (accepted..., correction) match a branch?
+ *                                                                    [Mirror-SD notes §3.2]
+ *
+ * Notation: q is the target distribution, p the draft distribution (SpS notes §1).  B sequences,
+ * K draft tokens per sequence, vocabulary V.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Logits are row-major: row r of a logit tensor starts at element r * row_pitch of the base
+ *    pointer (row_pitch >= V, in elements).  For per-sequence tensors, row (b, j) is row
+ *    b * rows_per_seq + j.  dtype SV_F32 (IEEE float) or SV_BF16 (bfloat16 bit patterns).
+ *    Rows are moved with 16-byte bulk copies, so base pointers must be 16-byte aligned and
+ *    row_pitch * elem_size a multiple of 16 (else SV_ERR_INVALID_ARG); V itself is free.
+ *  - Pointers marked "dev" are device memory the caller owns; "host" are host memory.  The
+ *    library allocates nothing: calls that need scratch take a caller-owned device workspace
+ *    whose size comes from the matching *_workspace_size() function.  A workspace may be reused
+ *    by consecutive calls on one stream; concurrent calls need distinct workspaces.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *    Argument errors are returned synchronously, before anything is launched.  Conditions only
+ *    the GPU can see (non-finite logits, out-of-range tokens, a wait that timed out) are written
+ *    to the optional device-side sv_stats block, which the caller reads after synchronising.
+ *  - Ranking ties (argmax, top-F, top-kappa, nucleus order) go to the lowest token id.
+ *  - Temperature 0 marks a greedy sequence: q and p are one-hot at the first argmax.
+ *  - Randomness is an input: uniforms are doubles in [0, 1).  An accept test accepts iff
+ *    u < min(1, q/p).  A draw with weights w returns the smallest id v with
+ *    w_0 + ... + w_v > u * (w_0 + ... + w_{V-1}) (token-id order).
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA include. */
+typedef struct CUstream_st *sv_stream_t;
+
+typedef enum sv_status {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1,  /* bad size, null pointer, misaligned base, unsupported value */
+    SV_ERR_CUDA = 2,         /* a CUDA runtime call failed (launch, memset, device query) */
+    SV_ERR_NONFINITE = 3,    /* device: a row holds NaN, or its maximum is not finite */
+    SV_ERR_TIMEOUT = 4,      /* device: a bounded wait on a shared-memory copy gave up */
+    SV_ERR_WORKSPACE = 5,    /* workspace pointer null/misaligned or smaller than required */
+    SV_ERR_BAD_TOKEN = 6     /* device: a token id outside [0, V) */
+} sv_status;
+
+typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+/*
+ * Device-written status and counters.  Each call that takes a stats pointer overwrites the
+ * block (it is cleared on the call's stream before the first kernel).  status holds the first
+ * device-detected error and error_index the row (or sequence) it concerns, -1 if none.
+ *
+ * Decisions (accept tests and draws) are first taken in float32 with a proven error bound.
+ * Those the bound cannot settle are recomputed in a float-float tier (about 44 significant
+ * bits) and counted in `reresolved`; those within ~1e-12 relative of the boundary even there
+ * are counted in `unresolved`.  `near_boundary` counts decisions whose uniform lies within
+ * 1e-6 of a ratio or a normalised CDF boundary (a property of the data, reported for context).
+ */
+typedef struct sv_stats {
+    int32_t status;
+    int32_t error_index;
+    int64_t rows;           /* logit rows streamed by the statistics pass */
+    int64_t accept_tests;   /* ratio tests performed (sampled sequences) */
+    int64_t draws;          /* inverse-CDF draws (residual, bonus or draft) */
+    int64_t reresolved;
+    int64_t near_boundary;
+    int64_t unresolved;
+} sv_stats;
+
+/* Per-position debug values written by sv_verify when `debug` is not NULL:
+ * debug[(b * (K + 1) + j) * SV_DEBUG_FIELDS + field], float64, NaN where undefined.
+ *   LSE_Q    log sum_v exp(x_v / T) of target row j (j = 0..K)
+ *   LSE_P    the same for draft row j (j < K)
+ *   Q_S, P_S q_j(s_j) and p_j(s_j) after temperature, top-p and sigma_{F,C} (j < K)
+ *   RATIO    q_j(s_j) / p_j(s_j), unclipped (j < K)
+ *   MASS_Q   kept nucleus mass of target row j (1 without top-p)
+ *   MASS_P   kept nucleus mass of draft row j
+ *   R        (j == 0 only) sum of the weights of the residual / bonus draw   */
+#define SV_DEBUG_FIELDS 8
+enum {
+    SV_DBG_LSE_Q = 0, SV_DBG_LSE_P = 1, SV_DBG_Q_S = 2, SV_DBG_P_S = 3,
+    SV_DBG_RATIO = 4, SV_DBG_MASS_Q = 5, SV_DBG_MASS_P = 6, SV_DBG_R = 7
+};
+
+/* Largest K accepted by sv_verify / sv_cache_keys (draft tokens per sequence). */
+#define SV_MAX_K 32
+
+const char *sv_status_string(sv_status s);
+int sv_version(void);   /* major * 10000 + minor * 100 + patch */
+
+/* ----------------------------------------------------------------------------------------
+ * sv_verify — modified rejection sampling over the vocabulary for B sequences.
+ * [SSD notes §2.2; SpS notes §3 (rule, mass identities), §6 (filters act before the ratio);
+ *  Mirror-SD notes §2 step 3 (greedy: longest prefix equal to the target argmax)]
+ *
+ *  target_logits  dev, rows (b, j) for j = 0..K at b*(K+1)+j, pitch t_row_pitch: the target
+ *                 scores for positions 1..K+1.
+ *  draft_logits   dev, rows (b, j) at b*d_rows_per_seq+j (d_rows_per_seq >= K), pitch
+ *                 d_row_pitch; rows j < K are the draft distributions that proposed s_1..s_K.
+ *                 Never read for greedy sequences.
+ *  draft_tokens   dev int32 [B][K], each in [0, V) (else SV_ERR_BAD_TOKEN in stats).
+ *  uniforms       dev float64 [B][K+1]: u[b][i] (i < K) the accept test of position i+1,
+ *                 u[b][K] the residual / bonus draw.  Greedy sequences consume none.
+ *  temperature    dev float [B]: T in [1e-3, 1e3] sampled, T == 0 greedy (anything else is
+ *                 reported in stats as SV_ERR_INVALID_ARG).  Applied to both q and p.
+ *  top_p          dev float [B] or NULL (no nucleus filter).  top_p >= 1 disables the filter
+ *                 for that sequence; otherwise the shortest prefix of tokens in (probability
+ *                 desc, id asc) order whose mass reaches top_p is kept, on q and on p.
+ *  saguaro_F, saguaro_C  the draft-side sigma_{F,C} transform applied to every draft row
+ *                 before the ratio and the residual (F = 0 or C = 1: none; 0 <= C <= 1).
+ *  accept_len     dev int32 [B]: k, the number of accepted draft tokens (0..K).
+ *  out_tokens     dev int32 [B][K+1]: s_1..s_k, then t*, then -1 padding.
+ *  debug          dev float64 [B][K+1][SV_DEBUG_FIELDS] or NULL.
+ *  stats          dev sv_stats or NULL.
+ *  workspace      dev, >= sv_verify_workspace_size(B, K, V) bytes, 256-byte aligned.
+ * Returns SV_ERR_INVALID_ARG for B < 1, K < 0, K > SV_MAX_K, V < 1, a pitch < V, a null
+ * required pointer, d_rows_per_seq < K, F < 0, C outside [0, 1] or a misaligned base.
+ * -------------------------------------------------------------------------------------- */
+size_t sv_verify_workspace_size(int B, int K, int V);
+
+sv_status sv_verify(const void *target_logits, int64_t t_row_pitch,
+                    const void *draft_logits, int64_t d_row_pitch, int d_rows_per_seq,
+                    sv_dtype dtype,
+                    const int32_t *draft_tokens, const double *uniforms,
+                    int B, int K, int V,
+                    const float *temperature, const float *top_p,
+                    int saguaro_F, float saguaro_C,
+                    int32_t *accept_len, int32_t *out_tokens,
+                    double *debug, sv_stats *stats,
+                    void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * sv_saguaro_sample — draw one token from each of the first n_rows rows of every sequence's
+ * draft distribution p' = sigma_{F,C}(p): p after temperature and top-p, the top-F tokens
+ * (ranked by draft logit) scaled by C, renormalised.  F = 0 or C = 1 is a plain draft sampler.
+ * [SSD notes §4.4 Theorem 15 (scaling the cached tokens' draft mass raises the hit rate),
+ *  Theorem 19 (worked example); SSD abstract page, "Method" (sigma_{F,C})]
+ *
+ *  draft_logits  dev, rows (b, j) at b*rows_per_seq+j, pitch row_pitch; rows j < n_rows used.
+ *  temperature   dev float [B] (0: argmax), top_p dev float [B] or NULL.
+ *  uniforms      dev float64 [B][n_rows].
+ *  tokens        dev int32 [B][n_rows] (output).
+ *  debug         dev float64 [B][n_rows][4] or NULL: LSE, P_D (top-F mass before scaling),
+ *                Z' (normaliser after scaling), nucleus mass.
+ * A row where C = 0 and all of p's mass lies in the top-F set has no defined transform and
+ * is sampled from p unchanged.
+ * -------------------------------------------------------------------------------------- */
+size_t sv_saguaro_sample_workspace_size(int B, int n_rows, int V);
+
+sv_status sv_saguaro_sample(const void *draft_logits, int64_t row_pitch, int rows_per_seq,
+                            sv_dtype dtype, int B, int n_rows, int V,
+                            const float *temperature, const float *top_p,
+                            int F, float C, const double *uniforms,
+                            int32_t *tokens, double *debug, sv_stats *stats,
+                            void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * sv_fanout — Theorem 12 fan-out, host only.  [SSD abstract page, "Method"; SSD notes §4.3]
+ *   F_k = F_0 a^(k/(1+r)) for k < K,  F_K = F_0 a^(K/(1+r)) (1-a)^(-1/(1+r)),  sum_k F_k = budget.
+ *  F_real  host float64 [K+1] (output), summing to budget.
+ *  F_int   host int32 [K+1] (output): floor(F_real) plus one for the largest fractional parts
+ *          (ties to the smaller k) until the sum is floor(budget).
+ * Requires 0 < a < 1, r > -1, budget >= 0 (finite, < 2^31), 0 <= K <= SV_MAX_K.
+ * -------------------------------------------------------------------------------------- */
+sv_status sv_fanout(double budget, double a, double r, int K, double *F_real, int32_t *F_int);
+
+/* ----------------------------------------------------------------------------------------
+ * sv_cache_keys — the speculation cache's key set.  [SSD notes §5.1; SSD abstract page]
+ * For depth k < K: the top-F_k tokens of draft row k (the row that proposed s_{k+1}), ranked by
+ * raw logit, after removing s_{k+1}; for depth K: the top-F_K tokens of draft row K.
+ *  draft_logits  dev, rows (b, j) at b*rows_per_seq+j, j = 0..K used (rows_per_seq >= K+1).
+ *  draft_tokens  dev int32 [B][K].
+ *  F_int         host int32 [K+1], 0 <= F_k <= V-1 (k < K), 0 <= F_K <= V.
+ *  keys          dev int32 [B][sum F_k], depth-major: depth k occupies
+ *                [sum_{i<k} F_i, sum_{i<=k} F_i).
+ * -------------------------------------------------------------------------------------- */
+size_t sv_cache_keys_workspace_size(int B, int K, int V);
+
+sv_status sv_cache_keys(const void *draft_logits, int64_t row_pitch, int rows_per_seq,
+                        sv_dtype dtype, const int32_t *draft_tokens, const int32_t *F_int,
+                        int B, int K, int V, int32_t *keys, sv_stats *stats,
+                        void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * sv_cache_lookup — hit[b] = 1 iff t* = out_tokens[b][k] is among the depth-k keys of sequence
+ * b, with k = accept_len[b].  [SSD abstract page, "Method": cache lookup on (k, t*)]
+ *  accept_len dev int32 [B]; out_tokens dev int32 [B][K+1]; keys dev int32 [B][sum F_int];
+ *  F_int host int32 [K+1]; hit dev uint8 [B] (output).
+ * A corrupt accept_len (outside [0, K]) yields hit 0.
+ * -------------------------------------------------------------------------------------- */
+sv_status sv_cache_lookup(const int32_t *accept_len, const int32_t *out_tokens,
+                          const int32_t *keys, const int32_t *F_int, int B, int K,
+                          uint8_t *hit, sv_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * sv_topk_rows — top-kappa token ids of each logit row (logit desc, id asc) and their
+ * log-probabilities log softmax(x / T).  [Mirror-SD notes §3.1: the early-exit head's top-kappa
+ * (token, log-prob) pairs become the branch roots]
+ *  logits       dev, n_rows rows with pitch row_pitch.
+ *  temperature  dev float [n_rows] (> 0) or NULL for T = 1.
+ *  ids          dev int32 [n_rows][kappa]; logprobs dev float64 [n_rows][kappa] (may be NULL).
+ * Requires 1 <= kappa <= min(V, 64).
+ * -------------------------------------------------------------------------------------- */
+size_t sv_topk_rows_workspace_size(int n_rows, int V);
+
+sv_status sv_topk_rows(const void *logits, int64_t row_pitch, sv_dtype dtype, int n_rows,
+                       int V, int kappa, const float *temperature, int32_t *ids,
+                       double *logprobs, sv_stats *stats, void *workspace,
+                       size_t workspace_bytes, sv_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * sv_mirror_reuse — reuse[b] = 1 iff k = accept_len[b] < gamma and the committed prefix
+ * (s_1..s_k, t*) = out_tokens[b][0..k] equals the first k+1 tokens of some branch.
+ * [Mirror-SD notes §3.2: reuse vs. fallback]
+ *  branches dev int32 [B][kappa][gamma]; accept_len dev int32 [B];
+ *  out_tokens dev int32 [B][gamma+1]; reuse dev uint8 [B] (output).
+ * -------------------------------------------------------------------------------------- */
+sv_status sv_mirror_reuse(const int32_t *branches, const int32_t *accept_len,
+                          const int32_t *out_tokens, int B, int kappa, int gamma,
+                          uint8_t *reuse, sv_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * sv_set_profile_events — measurement hook (no counterpart on the pages).  begin and end are
+ * cudaEvent_t handles (or NULL to disable).  While set, every call made from this host thread
+ * records `begin` on its stream just before its statistics pass (the one streaming read of the
+ * logit rows, the call's dominant kernel) and `end` just after it, so the caller can time that
+ * kernel with cudaEventElapsedTime.  The setting is thread-local and persists until changed.
+ * -------------------------------------------------------------------------------------- */
+void sv_set_profile_events(void *begin, void *end);
+
+/* ----------------------------------------------------------------------------------------
+ * Self-tests of the device error paths (no counterpart on the pages).
+ *
+ * sv_selftest_timeout: one block waits on a shared-memory barrier that nothing completes,
+ * gives up after `limit_cycles` SM clock cycles, and reports SV_ERR_TIMEOUT in stats.  It
+ * shows that the library's bounded waits return an error instead of hanging; no copy is in
+ * flight and nothing faults.
+ *
+ * sv_selftest_exp2: evaluates the library's fast base-2 exponential (the float32 tier) and
+ * its float-float exponential on n inputs spread over [lo, hi] and writes their largest
+ * relative errors against CUDA's double-precision exp2 to out[0] (fast) and out[1]
+ * (float-float).  The bounds that certify float32 decisions rest on these errors.
+ * -------------------------------------------------------------------------------------- */
+sv_status sv_selftest_timeout(int64_t limit_cycles, sv_stats *stats, sv_stream_t stream);
+sv_status sv_selftest_exp2(double lo, double hi, int64_t n, double *out, sv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -1,0 +1,243 @@
+"""libspecverify Python binding: argument marshalling for the C ABI, nothing else.
+
+Every function here forwards to the entry point of the same name in libspecverify.so (built
+for sm_103a by ``build.build()``).  Tensors are torch CUDA tensors; torch supplies device
+memory and the current stream, the computation runs in the library's kernels.  If the shared
+library is absent, importing the binding still works but every call raises ImportError; no
+other implementation stands in.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _abi
+from ._abi import (DBG, SV_BF16, SV_F32, SV_MAX_K, STATS_BYTES, STATS_FIELDS, SvError,  # noqa: F401
+                   load, status_string)
+
+__all__ = ["sv_verify", "sv_saguaro_sample", "sv_fanout", "sv_cache_keys", "sv_cache_lookup", "sv_topk_rows",
+           "sv_mirror_reuse", "sv_selftest_timeout", "sv_selftest_exp2", "read_stats", "load", "status_string",
+           "SvError", "Workspace"]
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float32:
+        return SV_F32
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _rows(t, name):
+    """(row pitch in elements, rows per sequence) of a [B, R, V] or [N, V] logit tensor."""
+    if t.stride(-1) != 1:
+        raise ValueError(f"{name}: the vocabulary axis must be contiguous")
+    if t.dim() == 3:
+        if t.shape[1] > 1 and t.stride(0) != t.shape[1] * t.stride(1):
+            raise ValueError(f"{name}: rows of a sequence must be consecutive rows of one pitch")
+        pitch = t.stride(1) if t.shape[1] > 1 else t.stride(0)
+        return pitch, t.shape[1]
+    if t.dim() == 2:
+        return t.stride(0), 1
+    raise ValueError(f"{name}: expected [B, R, V] or [N, V]")
+
+
+class Workspace:
+    """A caller-owned device workspace (torch memory) reused across calls on one stream."""
+
+    def __init__(self):
+        self._buf = {}
+
+    def get(self, nbytes: int, device) -> torch.Tensor:
+        key = torch.device(device)
+        buf = self._buf.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+            self._buf[key] = buf
+        return buf
+
+
+_default_ws = Workspace()
+
+
+def new_stats(device) -> torch.Tensor:
+    return torch.zeros(STATS_BYTES, dtype=torch.uint8, device=device)
+
+
+def read_stats(t: torch.Tensor) -> dict:
+    """Decode an sv_stats block (synchronises with the device)."""
+    raw = t.detach().cpu()
+    i32 = raw.view(torch.int32)
+    i64 = raw.view(torch.int64)
+    out = {"status": int(i32[0]), "error_index": int(i32[1])}
+    for k, name in enumerate(STATS_FIELDS[2:]):
+        out[name] = int(i64[1 + k])
+    return out
+
+
+def sv_verify(target, draft, draft_tokens, uniforms, temperature, top_p=None, saguaro_F=0, saguaro_C=1.0,
+              accept_len=None, out_tokens=None, debug=False, stats=None, workspace=None, stream=None):
+    """sv_verify on torch CUDA tensors.
+
+    target [B, K+1, V] and draft [B, R>=K, V] (float32 or bfloat16, same dtype); draft_tokens
+    int32 [B, K]; uniforms float64 [B, K+1]; temperature float32 [B]; top_p float32 [B] or None.
+    Returns (accept_len int32 [B], out_tokens int32 [B, K+1], debug float64 [B, K+1, 8] or None,
+    stats uint8 block).
+    """
+    lib = load()
+    B, K1, V = target.shape
+    K = K1 - 1
+    dev = target.device
+    t_pitch, _ = _rows(target, "target")
+    if K > 0:
+        if draft.dtype != target.dtype:
+            raise TypeError("target and draft logits must share a dtype")
+        d_pitch, d_rows = _rows(draft, "draft")
+        d_ptr = _ptr(draft)
+    else:
+        d_pitch, d_rows, d_ptr = t_pitch, 1, ctypes.c_void_p(0)
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    dbg = torch.empty((B, K + 1, _abi.SV_DEBUG_FIELDS), dtype=torch.float64, device=dev) if debug else None
+    if stats is None:
+        stats = new_stats(dev)
+    ws_bytes = lib.sv_verify_workspace_size(B, K, V)
+    ws = (workspace or _default_ws).get(ws_bytes, dev)
+    code = lib.sv_verify(_ptr(target), t_pitch, d_ptr, d_pitch, d_rows, _dtype_code(target),
+                         _ptr(draft_tokens if K > 0 else None), _ptr(uniforms), B, K, V, _ptr(temperature),
+                         _ptr(top_p), int(saguaro_F), float(saguaro_C), _ptr(accept_len), _ptr(out_tokens),
+                         _ptr(dbg), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream))
+    _abi.check("sv_verify", code)
+    return accept_len, out_tokens, dbg, stats
+
+
+def sv_saguaro_sample(draft, uniforms, temperature, top_p=None, F=0, C=1.0, n_rows=None, tokens=None, debug=False,
+                      stats=None, workspace=None, stream=None):
+    """sv_saguaro_sample: one token per row j < n_rows of each sequence of draft [B, R, V].
+    uniforms float64 [B, n_rows]; temperature float32 [B]; returns (tokens int32 [B, n_rows],
+    debug float64 [B, n_rows, 4] or None, stats)."""
+    lib = load()
+    B, R, V = draft.shape
+    n_rows = R if n_rows is None else n_rows
+    dev = draft.device
+    pitch, rows = _rows(draft, "draft")
+    if tokens is None:
+        tokens = torch.empty((B, n_rows), dtype=torch.int32, device=dev)
+    dbg = torch.empty((B, n_rows, 4), dtype=torch.float64, device=dev) if debug else None
+    if stats is None:
+        stats = new_stats(dev)
+    ws_bytes = lib.sv_saguaro_sample_workspace_size(B, n_rows, V)
+    ws = (workspace or _default_ws).get(ws_bytes, dev)
+    code = lib.sv_saguaro_sample(_ptr(draft), pitch, rows, _dtype_code(draft), B, n_rows, V, _ptr(temperature),
+                                 _ptr(top_p), int(F), float(C), _ptr(uniforms), _ptr(tokens), _ptr(dbg), _ptr(stats),
+                                 _ptr(ws), ws.numel(), _stream(stream))
+    _abi.check("sv_saguaro_sample", code)
+    return tokens, dbg, stats
+
+
+def sv_fanout(budget: float, a: float, r: float, K: int):
+    """Host-only Theorem 12 fan-out: returns (F_real list[float], F_int list[int])."""
+    lib = load()
+    fr = (ctypes.c_double * (K + 1))()
+    fi = (ctypes.c_int32 * (K + 1))()
+    code = lib.sv_fanout(float(budget), float(a), float(r), int(K), ctypes.cast(fr, ctypes.c_void_p),
+                         ctypes.cast(fi, ctypes.c_void_p))
+    _abi.check("sv_fanout", code)
+    return list(fr), list(fi)
+
+
+def _host_i32(values):
+    arr = (ctypes.c_int32 * len(values))(*[int(v) for v in values])
+    return arr, ctypes.cast(arr, ctypes.c_void_p)
+
+
+def sv_cache_keys(draft, draft_tokens, F_int, keys=None, stats=None, workspace=None, stream=None):
+    """sv_cache_keys: draft [B, R>=K+1, V]; draft_tokens int32 [B, K]; F_int host list of K+1 ints.
+    Returns keys int32 [B, sum F_int]."""
+    lib = load()
+    B, R, V = draft.shape
+    K = len(F_int) - 1
+    dev = draft.device
+    pitch, rows = _rows(draft, "draft")
+    if keys is None:
+        keys = torch.empty((B, int(sum(F_int))), dtype=torch.int32, device=dev)
+    if stats is None:
+        stats = new_stats(dev)
+    f_arr, f_ptr = _host_i32(F_int)
+    ws_bytes = lib.sv_cache_keys_workspace_size(B, K, V)
+    ws = (workspace or _default_ws).get(ws_bytes, dev)
+    code = lib.sv_cache_keys(_ptr(draft), pitch, rows, _dtype_code(draft), _ptr(draft_tokens), f_ptr, B, K, V,
+                             _ptr(keys), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream))
+    _abi.check("sv_cache_keys", code)
+    return keys, stats
+
+
+def sv_cache_lookup(accept_len, out_tokens, keys, F_int, hit=None, stream=None):
+    lib = load()
+    B = accept_len.shape[0]
+    K = len(F_int) - 1
+    if hit is None:
+        hit = torch.empty(B, dtype=torch.uint8, device=accept_len.device)
+    f_arr, f_ptr = _host_i32(F_int)
+    code = lib.sv_cache_lookup(_ptr(accept_len), _ptr(out_tokens), _ptr(keys), f_ptr, B, K, _ptr(hit),
+                               _stream(stream))
+    _abi.check("sv_cache_lookup", code)
+    return hit
+
+
+def sv_topk_rows(logits, kappa, temperature=None, ids=None, logprobs=None, stats=None, workspace=None, stream=None):
+    """sv_topk_rows: logits [N, V]; returns (ids int32 [N, kappa], logprobs float64 [N, kappa], stats)."""
+    lib = load()
+    N, V = logits.shape
+    dev = logits.device
+    pitch, _ = _rows(logits, "logits")
+    if ids is None:
+        ids = torch.empty((N, kappa), dtype=torch.int32, device=dev)
+    if logprobs is None:
+        logprobs = torch.empty((N, kappa), dtype=torch.float64, device=dev)
+    if stats is None:
+        stats = new_stats(dev)
+    ws_bytes = lib.sv_topk_rows_workspace_size(N, V)
+    ws = (workspace or _default_ws).get(ws_bytes, dev)
+    code = lib.sv_topk_rows(_ptr(logits), pitch, _dtype_code(logits), N, V, int(kappa), _ptr(temperature), _ptr(ids),
+                            _ptr(logprobs), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream))
+    _abi.check("sv_topk_rows", code)
+    return ids, logprobs, stats
+
+
+def sv_mirror_reuse(branches, accept_len, out_tokens, reuse=None, stream=None):
+    lib = load()
+    B, kappa, gamma = branches.shape
+    if reuse is None:
+        reuse = torch.empty(B, dtype=torch.uint8, device=branches.device)
+    code = lib.sv_mirror_reuse(_ptr(branches), _ptr(accept_len), _ptr(out_tokens), B, kappa, gamma, _ptr(reuse),
+                               _stream(stream))
+    _abi.check("sv_mirror_reuse", code)
+    return reuse
+
+
+def sv_selftest_timeout(limit_cycles: int, stats=None, stream=None):
+    lib = load()
+    if stats is None:
+        stats = new_stats("cuda")
+    _abi.check("sv_selftest_timeout", lib.sv_selftest_timeout(int(limit_cycles), _ptr(stats), _stream(stream)))
+    return stats
+
+
+def sv_selftest_exp2(lo: float, hi: float, n: int, stream=None):
+    lib = load()
+    out = torch.zeros(2, dtype=torch.float64, device="cuda")
+    _abi.check("sv_selftest_exp2", lib.sv_selftest_exp2(float(lo), float(hi), int(n), _ptr(out), _stream(stream)))
+    return out

@@ -1,0 +1,301 @@
+// sv_device.cuh — device helpers for libspecverify (sm_103a).
+//
+// Inline PTX for the shared-memory barriers and 1-D bulk (TMA) copies that stage logit rows
+// into shared memory, the float32 fast exponential, bfloat16 unpacking, order-preserving
+// integer keys, float-float arithmetic for the exact tier, and status reporting.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "specverify.h"
+#include "sv_layout.h"
+
+namespace sv {
+
+// ------------------------------------------------------------------------------------------
+// Shared-memory barriers and bulk copies
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// Makes barrier initialisation visible to the asynchronous (bulk-copy) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the barrier phase with the given parity; gives up after `limit` SM clock cycles.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, long long limit) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > limit) return false;
+    }
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing `bytes` on `bar`.
+// Both addresses must be 16-byte aligned and bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// 1-D bulk copy with an L2 evict-first policy (streamed logits are read once).
+__device__ __forceinline__ void bulk_load_stream(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint4 lds128(const void *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_addr(p)));
+    return v;
+}
+
+// ------------------------------------------------------------------------------------------
+// Element access
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Packed bf16x2 maximum that propagates NaN.
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+template <int ES>
+__device__ __forceinline__ float load_elem(const char *row, int64_t v) {
+    if (ES == 4) return __ldg(reinterpret_cast<const float *>(row) + v);
+    const uint16_t h = __ldg(reinterpret_cast<const unsigned short *>(row) + v);
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// ------------------------------------------------------------------------------------------
+// Exponentials
+// ------------------------------------------------------------------------------------------
+// Fast tier: the SFU base-2 exponential (denormal results flush to zero).  Its largest
+// relative error over the arguments the library feeds it is measured by sv_selftest_exp2 and
+// bounded by kEx2RelErr in the certification of float32 decisions.
+__device__ __forceinline__ float ex2_fast(float y) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+    return r;
+}
+
+// Exact power of two for an integer exponent (0 below the normal range).
+__device__ __forceinline__ float pow2i(int e) {
+    if (e < -126) return 0.0f;
+    if (e > 127) e = 127;
+    return __int_as_float((e + 127) << 23);
+}
+
+// ------------------------------------------------------------------------------------------
+// Float-float arithmetic (exact tier).  Each value is hi + lo with |lo| <= ulp(hi)/2.
+// The _rn intrinsics keep the compiler from contracting the error-free transforms.
+// ------------------------------------------------------------------------------------------
+struct ff {
+    float hi, lo;
+};
+
+__device__ __forceinline__ ff two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return {s, e};
+}
+
+// Requires |a| >= |b| (or a == 0).
+__device__ __forceinline__ ff fast_two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ ff two_prod(float a, float b) {
+    const float p = __fmul_rn(a, b);
+    return {p, __fmaf_rn(a, b, -p)};
+}
+
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+    ff s = two_sum(a.hi, b.hi);
+    const float t = __fadd_rn(__fadd_rn(a.lo, b.lo), s.lo);
+    return fast_two_sum(s.hi, t);
+}
+
+__device__ __forceinline__ ff ff_sub(ff a, ff b) { return ff_add(a, {-b.hi, -b.lo}); }
+
+__device__ __forceinline__ double ff_to_double(ff a) { return (double)a.hi + (double)a.lo; }
+
+__device__ __forceinline__ ff ff_from_double(double d) {
+    const float h = (float)d;
+    return {h, (float)(d - (double)h)};
+}
+
+// 2^(yh + yl) as float-float, Tang's table-driven method (P. T. P. Tang, "Table-driven
+// implementation of the exponential function in IEEE floating-point arithmetic", ACM TOMS
+// 15(2), 1989): y = n + j/256 + r with |r| <= 1/512; 2^(j/256) comes from a 256-entry
+// float-float table (tab[j] = {hi, lo}); 2^r = e^s with s = r ln 2 is its Taylor series
+// to s^4 (the next term is below 4e-17).  Valid for yh in [-200, 120]; results below 2^-126
+// flush to zero.
+__device__ __forceinline__ ff ff_exp2(float yh, float yl, const float2 *tab) {
+    const float kf = rintf(__fmul_rn(yh, 256.0f));
+    const int k = static_cast<int>(kf);
+    const float rh = __fsub_rn(yh, __fmul_rn(kf, 0.00390625f));   // exact
+    // s = (rh + yl) ln2, float-float; ln2 = L_HI + L_LO
+    const float L_HI = 0.693147182464599609375f;
+    const float L_LO = -1.9046542999577520e-09f;
+    ff s = two_prod(rh, L_HI);
+    s.lo = __fmaf_rn(rh, L_LO, __fmaf_rn(yl, L_HI, s.lo));
+    s = fast_two_sum(s.hi, s.lo);
+    // e^s - 1 = s + s^2/2 + s^3/6 + s^4/24
+    const ff s2 = two_prod(s.hi, s.hi);
+    const float half_s2 = __fmul_rn(0.5f, s2.hi);
+    const float cubic = __fmul_rn(__fmul_rn(s2.hi, s.hi), __fmaf_rn(s.hi, 1.0f / 24.0f, 1.0f / 6.0f));
+    const float small = __fadd_rn(__fmaf_rn(s.hi, s.lo, __fmul_rn(0.5f, s2.lo)), cubic);
+    ff t = fast_two_sum(s.hi, half_s2);
+    t.lo = __fadd_rn(t.lo, __fadd_rn(s.lo, small));
+    // 2^(j/256) (1 + t)
+    const int j = k & 255;
+    const int n = k >> 8;
+    const float2 T = tab[j];
+    const ff P = two_prod(T.x, t.hi);
+    ff e = fast_two_sum(T.x, P.hi);
+    const float tail = __fadd_rn(T.y, __fadd_rn(P.lo, __fmaf_rn(T.x, t.lo, __fmul_rn(T.y, t.hi))));
+    e = fast_two_sum(e.hi, __fadd_rn(e.lo, tail));
+    const float sc = pow2i(n);
+    return {__fmul_rn(e.hi, sc), __fmul_rn(e.lo, sc)};
+}
+
+// x * c - g as float-float, with c = c.hi + c.lo and g = g.hi + g.lo float-float constants.
+// x * c.hi is exact through an FMA; the remaining terms are small.
+__device__ __forceinline__ ff ff_affine(float x, ff c, ff g) {
+    const ff p = two_prod(x, c.hi);
+    ff d = two_sum(p.hi, -g.hi);
+    d.lo = __fadd_rn(d.lo, __fadd_rn(__fsub_rn(p.lo, g.lo), __fmul_rn(x, c.lo)));
+    return fast_two_sum(d.hi, d.lo);
+}
+
+// ------------------------------------------------------------------------------------------
+// Order-preserving keys (larger value -> larger key) for ranking logits.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t f32_key(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// ------------------------------------------------------------------------------------------
+// Status reporting into the caller's sv_stats block.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void report_error(sv_stats *st, int code, int index) {
+    if (st == nullptr) return;
+    if (atomicCAS(&st->status, 0, code) == 0) atomicExch(&st->error_index, index);
+}
+
+__device__ __forceinline__ void stats_add(sv_stats *st, int64_t *field_in_stats, long long v) {
+    if (st == nullptr || v == 0) return;
+    atomicAdd(reinterpret_cast<unsigned long long *>(field_in_stats), static_cast<unsigned long long>(v));
+}
+
+// Queue an item for the float-float tier; past the queue's capacity the float32 result stands
+// and the decision is counted as unresolved.
+__device__ __forceinline__ void push_exact(Counters *ctr, ExactItem *q, ExactItem item, sv_stats *st) {
+    const int e = atomicAdd(&ctr->n_exact, 1);
+    if (e < kExactCap) q[e] = item;
+    else stats_add(st, &st->unresolved, 1);
+}
+
+// ------------------------------------------------------------------------------------------
+// Warp helpers
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ int warp_max_i(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ int warp_or_i(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// (value, index) maximum with ties to the lowest index.
+__device__ __forceinline__ void warp_argmax(float &v, int &i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, i, o);
+        if (ov > v || (ov == v && oi < i)) {
+            v = ov;
+            i = oi;
+        }
+    }
+}
+
+__device__ __forceinline__ ff warp_sum_ff(ff a) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ff b;
+        b.hi = __shfl_xor_sync(0xFFFFFFFFu, a.hi, o);
+        b.lo = __shfl_xor_sync(0xFFFFFFFFu, a.lo, o);
+        a = ff_add(a, b);
+    }
+    return a;
+}
+
+}  // namespace sv

@@ -1,0 +1,443 @@
+// sv_draw.cuh — inverse-CDF draws in token-id order, float32 tier with a certified error bound.
+//
+// A draw item names one or two rows and a uniform u.  Its weights are
+//     w_v = max(q_v - p_v, 0)   (residual: SSD notes §2.2 ③; SpS notes §3)   or   w_v = q_v  (bonus),
+// with q_v = keep_q(v) 2^(x_v c - r_q) inv_q and p_v = keep_p(v) 2^(y_v c - r_p) inv_p (C for v in
+// the Saguaro top-F set).  The token is t* = min{v : w_0 + ... + w_v > u R}, R = sum_v w_v.
+//
+// Pass 1 (k_draw_sums): a persistent grid streams the rows through bulk copies and writes, per
+// 32-vector sub-chunk of the row, the float32 sum of w and of the error weights
+// q_v |y_q| + p_v |y_p|.  Pass 2 (k_draw_finish): one block per item scans the sub-chunk sums
+// in float64, locates the sub-chunk that holds u R, recomputes its tokens' weights exactly as
+// pass 1 did, and picks t*.  If u R lies within the proven error bound of either boundary of
+// t*, the item is queued for the float-float tier.
+#pragma once
+
+#include "sv_device.cuh"
+
+namespace sv {
+
+struct DrawArgs {
+    const DrawItem *items;
+    Counters *counters;
+    int V, n_vec, n_sub;        // n_sub = vector sub-chunks + 1 tail sub-chunk
+    int n_split;                // chunks per row
+    int subs_per_chunk;         // vector sub-chunks per chunk
+    float2 *subs;               // [item][n_sub] = (sum w, sum of error weights)
+    ExactItem *exact;           // exact-tier queue (may be nullptr: no re-resolution)
+    sv_stats *stats;
+    long long wait_limit;
+};
+
+// Per-element weight and error weight (identical in both passes).
+template <bool HAS_P, bool FILT>
+__device__ __forceinline__ void draw_weight(const DrawItem &it, float xq, float xp, int v, float &w, float &aq,
+                                            float &ap) {
+    const float yq = fmaf(xq, it.q.c_lo, fmaf(xq, it.q.c_hi, -it.q.rf));
+    float eq = ex2_fast(yq);
+    float scq = it.q.inv_s;
+    if (FILT) {
+        const bool keep = xq > it.q.cut_x || (xq == it.q.cut_x && v <= it.q.cut_id);
+        const bool in_d = xq > it.q.top_x || (xq == it.q.top_x && v <= it.q.top_id);
+        eq = keep ? eq : 0.0f;
+        scq = in_d ? __fmul_rn(scq, it.q.sc_d) : scq;
+    }
+    aq = eq * fabsf(yq);
+    if (HAS_P) {
+        const float yp = fmaf(xp, it.p.c_lo, fmaf(xp, it.p.c_hi, -it.p.rf));
+        float ep = ex2_fast(yp);
+        float sc = it.p.inv_s;
+        if (FILT) {
+            const bool keep = xp > it.p.cut_x || (xp == it.p.cut_x && v <= it.p.cut_id);
+            const bool in_d = xp > it.p.top_x || (xp == it.p.top_x && v <= it.p.top_id);
+            ep = keep ? ep : 0.0f;
+            sc = in_d ? __fmul_rn(sc, it.p.sc_d) : sc;
+        }
+        ap = ep * fabsf(yp);
+        const float pv = __fmul_rn(ep, sc);
+        w = fmaxf(__fmaf_rn(eq, scq, -pv), 0.0f);
+    } else {
+        ap = 0.0f;
+        w = __fmul_rn(eq, scq);
+    }
+}
+
+// Unpack one 16-byte vector of ES-byte elements.
+template <int ES>
+__device__ __forceinline__ void unpack(uint4 w, float (&x)[16 / ES]) {
+    if constexpr (ES == 2) {
+        x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+        x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+    } else {
+        x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+        x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+    }
+}
+
+// Weights of one vector (EPV tokens from element e0); returns the tree sum, fills aq/ap sums.
+template <int ES, bool HAS_P, bool FILT>
+__device__ __forceinline__ float vec_weights(const DrawItem &it, uint4 wq, uint4 wp, int e0, float (&wv)[16 / ES],
+                                             float &aq_sum, float &ap_sum) {
+    constexpr int EPV = 16 / ES;
+    float xq[EPV], xp[EPV];
+    unpack<ES>(wq, xq);
+    unpack<ES>(wp, xp);
+    float aq[EPV], ap[EPV];
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) draw_weight<HAS_P, FILT>(it, xq[i], xp[i], e0 + i, wv[i], aq[i], ap[i]);
+    float s;
+    if constexpr (EPV == 8) {
+        s = ((wv[0] + wv[1]) + (wv[2] + wv[3])) + ((wv[4] + wv[5]) + (wv[6] + wv[7]));
+        aq_sum = ((aq[0] + aq[1]) + (aq[2] + aq[3])) + ((aq[4] + aq[5]) + (aq[6] + aq[7]));
+        ap_sum = ((ap[0] + ap[1]) + (ap[2] + ap[3])) + ((ap[4] + ap[5]) + (ap[6] + ap[7]));
+    } else {
+        s = (wv[0] + wv[1]) + (wv[2] + wv[3]);
+        aq_sum = (aq[0] + aq[1]) + (aq[2] + aq[3]);
+        ap_sum = (ap[0] + ap[1]) + (ap[2] + ap[3]);
+    }
+    return s;
+}
+
+template <int ES, bool HAS_P, bool FILT>
+__device__ __forceinline__ void draw_tile(const DrawItem &it, const unsigned char *bq, const unsigned char *bp,
+                                          int fv, int nv, float2 *subs_item) {
+    constexpr int EPV = 16 / ES;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+#pragma unroll 1
+    for (int g = 0; g < kTileBytes / 16 / kThreads; ++g) {
+        const int vbase = g * kThreads + (tid & ~31);   // first vector of this warp's sub-chunk
+        if (vbase >= nv) break;                          // warp-uniform
+        const int vi = vbase + lane;
+        float w = 0.f, aq = 0.f, ap = 0.f;
+        if (vi < nv) {
+            const uint4 q = lds128(bq + vi * 16);
+            const uint4 p = HAS_P ? lds128(bp + vi * 16) : q;
+            float wv[EPV];
+            w = vec_weights<ES, HAS_P, FILT>(it, q, p, (fv + vi) * EPV, wv, aq, ap);
+        }
+        const float a = fmaf(aq, it.q.inv_s, ap * it.p.inv_s);
+        const float W = warp_sum_f(w);
+        const float A = warp_sum_f(HAS_P ? a : aq * it.q.inv_s);
+        if (lane == 0) subs_item[(fv + vbase) / 32] = make_float2(W, A);
+    }
+}
+
+template <int ES>
+__device__ __forceinline__ void draw_scalar(const DrawItem &it, int v, float &w, float &aq, float &ap) {
+    const float xq = load_elem<ES>(it.q.row, v);
+    const float xp = it.has_p ? load_elem<ES>(it.p.row, v) : xq;
+    if (it.has_p) {
+        if (it.filt) draw_weight<true, true>(it, xq, xp, v, w, aq, ap);
+        else draw_weight<true, false>(it, xq, xp, v, w, aq, ap);
+    } else {
+        if (it.filt) draw_weight<false, true>(it, xq, xp, v, w, aq, ap);
+        else draw_weight<false, false>(it, xq, xp, v, w, aq, ap);
+    }
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kThreads, 2) k_draw_sums(const DrawArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    unsigned char *tiles = smem + 128;          // stage s: q tile at 2s, p tile at 2s+1
+    const int tid = threadIdx.x;
+    const int n_items = *reinterpret_cast<volatile int *>(&a.counters->n_draws);
+    const long long n_units = (long long)n_items * a.n_split;
+    if ((long long)blockIdx.x >= n_units) return;
+    const int n_vsub = a.n_sub - 1;
+
+    if (tid == 0) {
+        for (int s = 0; s < kDrawStages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    auto unit_range = [&](long long u, int &d, int &c, int &v0, int &v1) {
+        d = (int)(u / a.n_split);
+        c = (int)(u - (long long)d * a.n_split);
+        const int s0 = min(c * a.subs_per_chunk, n_vsub);
+        const int s1 = min(s0 + a.subs_per_chunk, n_vsub);
+        v0 = s0 * 32;
+        v1 = min(s1 * 32, a.n_vec);
+        if (v1 < v0) v1 = v0;
+    };
+
+    // producer (thread 0)
+    long long pu = blockIdx.x;
+    int pt = 0;
+    long long issued = 0;
+    const uint64_t policy = policy_evict_first();
+    auto p_issue = [&](int stage) {
+        while (pu < n_units) {
+            int d, c, v0, v1;
+            unit_range(pu, d, c, v0, v1);
+            const int nt = (v1 - v0 + 1023) / 1024;
+            if (pt < nt) {
+                const DrawItem &it = a.items[d];
+                const int fv = v0 + pt * 1024;
+                const int nv = min(1024, v1 - fv);
+                const uint32_t bytes = (uint32_t)nv * 16u;
+                mbar_arrive_expect_tx(&full[stage], it.has_p ? 2u * bytes : bytes);
+                bulk_load_stream(tiles + (2 * stage) * kTileBytes, it.q.row + (size_t)fv * 16, bytes, &full[stage],
+                                 policy);
+                if (it.has_p)
+                    bulk_load_stream(tiles + (2 * stage + 1) * kTileBytes, it.p.row + (size_t)fv * 16, bytes,
+                                     &full[stage], policy);
+                ++pt;
+                ++issued;
+                return;
+            }
+            pu += gridDim.x;
+            pt = 0;
+        }
+    };
+    if (tid == 0)
+        for (int s = 0; s < kDrawStages; ++s) p_issue(s);
+
+    long long itc = 0;
+    for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
+        int d, c, v0, v1;
+        unit_range(u, d, c, v0, v1);
+        const DrawItem it = a.items[d];
+        float2 *subs_item = a.subs + (size_t)d * a.n_sub;
+        const int nt = (v1 - v0 + 1023) / 1024;
+        for (int t = 0; t < nt; ++t, ++itc) {
+            const int st = (int)(itc % kDrawStages);
+            const uint32_t par = (uint32_t)((itc / kDrawStages) & 1);
+            const bool ok = mbar_wait_bounded(&full[st], par, a.wait_limit);
+            if (ok) {
+                const int fv = v0 + t * 1024;
+                const int nv = min(1024, v1 - fv);
+                const unsigned char *bq = tiles + (2 * st) * kTileBytes;
+                const unsigned char *bp = bq + kTileBytes;
+                if (it.has_p) {
+                    if (it.filt) draw_tile<ES, true, true>(it, bq, bp, fv, nv, subs_item);
+                    else draw_tile<ES, true, false>(it, bq, bp, fv, nv, subs_item);
+                } else {
+                    if (it.filt) draw_tile<ES, false, true>(it, bq, bp, fv, nv, subs_item);
+                    else draw_tile<ES, false, false>(it, bq, bp, fv, nv, subs_item);
+                }
+            }
+            if (__syncthreads_or(!ok)) {
+                if (tid == 0) {
+                    report_error(a.stats, SV_ERR_TIMEOUT, it.seq);
+                    for (long long k = itc; k < issued; ++k)
+                        mbar_wait_bounded(&full[k % kDrawStages], (uint32_t)((k / kDrawStages) & 1),
+                                          a.wait_limit / 16);
+                }
+                return;
+            }
+            if (tid == 0) p_issue(st);
+        }
+        // the scalar tail of the row forms the last sub-chunk
+        if (c == a.n_split - 1 && tid < 32) {
+            constexpr int EPV = 16 / ES;
+            const int t0 = a.n_vec * EPV;
+            float w = 0.f, aq = 0.f, ap = 0.f;
+            if (t0 + tid < a.V) draw_scalar<ES>(it, t0 + tid, w, aq, ap);
+            const float W = warp_sum_f(w);
+            const float A = warp_sum_f(fmaf(aq, it.q.inv_s, it.has_p ? ap * it.p.inv_s : 0.f));
+            if (tid == 0) subs_item[n_vsub] = make_float2(W, A);
+        }
+    }
+}
+
+// Certified bound on |C_fast(v) - u R_fast - (C(v) - u R)| over all v (see the header comment of
+// this file): element errors from the SFU exponential, the float32 exponent arguments, the
+// normalisers and the products, plus the float32 summation inside sub-chunks.
+__device__ __forceinline__ double draw_error_bound(const DrawItem &it, double W, double A) {
+    const double u = kU32;
+    double e = kYRound * 1.01 * A + 10.0 * u * W + 1e-15;
+    if (it.has_p) {
+        e += 1.0001 * (kEx2RelErr + 2.0 * u + it.q.norm_err) + 1.0001 * (kEx2RelErr + 2.0 * u + it.p.norm_err);
+    } else if (it.filt) {
+        // tokens inside and outside the scaled set carry different normaliser errors
+        e += (kEx2RelErr + 2.0 * u + it.q.norm_err) * W;
+    } else {
+        e += (kEx2RelErr + u) * W;   // a common normaliser error cancels in C(v) / R
+    }
+    return 2.0 * e;
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
+    constexpr int EPV = 16 / ES;
+    __shared__ double s_scan[kThreads];
+    __shared__ double s_red[2][kWarps];
+    __shared__ int s_sub;
+    __shared__ double s_pre;
+    __shared__ int s_last_sub;
+
+    const int d = blockIdx.x;
+    const int n_items = *reinterpret_cast<volatile int *>(&a.counters->n_draws);
+    if (d >= n_items) return;
+    const DrawItem it = a.items[d];
+    const float2 *subs = a.subs + (size_t)d * a.n_sub;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n_sub = a.n_sub, n_vsub = n_sub - 1;
+
+    // 1. per-thread contiguous ranges of sub-chunks
+    const int per = (n_sub + kThreads - 1) / kThreads;
+    const int s0 = min(tid * per, n_sub), s1 = min(s0 + per, n_sub);
+    double wsum = 0.0, asum = 0.0;
+    int last_pos = -1;
+    for (int s = s0; s < s1; ++s) {
+        const float2 v = subs[s];
+        wsum += (double)v.x;
+        asum += (double)v.y;
+        if (v.x > 0.f) last_pos = s;
+    }
+    // 2. block exclusive scan of wsum
+    s_scan[tid] = wsum;
+    if (tid == 0) {
+        s_sub = -1;
+        s_last_sub = -1;
+    }
+    __syncthreads();
+    for (int off = 1; off < kThreads; off <<= 1) {
+        const double v = tid >= off ? s_scan[tid - off] : 0.0;
+        __syncthreads();
+        s_scan[tid] += v;
+        __syncthreads();
+    }
+    const double incl = s_scan[tid];
+    const double excl = incl - wsum;
+    const double R = s_scan[kThreads - 1];
+    double at = warp_sum_d(asum);
+    if (lane == 0) s_red[0][warp] = at;
+    atomicMax(&s_last_sub, last_pos);
+    __syncthreads();
+    double A = 0.0;
+    for (int w = 0; w < kWarps; ++w) A += s_red[0][w];
+    const double thr = it.u * R;
+    // 3. the thread whose range holds thr finds the sub-chunk
+    const double next = tid + 1 < kThreads ? s_scan[tid] : R;
+    if (wsum > 0.0 && excl <= thr && thr < next) {
+        double run = excl;
+        int found = -1;
+        double pre = excl;
+        for (int s = s0; s < s1; ++s) {
+            const double wv = (double)subs[s].x;
+            if (wv > 0.0) {
+                found = s;
+                pre = run;
+                if (thr < run + wv) break;
+            }
+            run += wv;
+        }
+        s_sub = found;
+        s_pre = pre;
+    }
+    __syncthreads();
+    int sub = s_sub;
+    double pre = s_pre;
+    bool ambiguous = false;
+    if (sub < 0) {
+        // thr beyond the last boundary (rounding) or R == 0: fall back to the last positive weight
+        sub = s_last_sub;
+        pre = -1.0;   // computed below from the scan
+        ambiguous = true;
+        if (sub >= 0 && tid == 0) {
+            double p = 0.0;
+            for (int s = 0; s < sub; ++s) p += (double)subs[s].x;
+            s_pre = p;
+        }
+        __syncthreads();
+        pre = s_pre;
+    }
+    if (warp != 0) return;
+    if (sub < 0) {
+        // every weight is zero: degenerate; the exact tier decides
+        if (lane == 0) {
+            *it.out = -1;
+            if (a.exact) push_exact(a.counters, a.exact, {d, it.seq}, a.stats);
+            stats_add(a.stats, &a.stats->reresolved, 1);
+            stats_add(a.stats, &a.stats->draws, 1);
+        }
+        return;
+    }
+    // 4. rescan the sub-chunk token by token (same arithmetic as pass 1)
+    float wv[EPV];
+    int ntok = 0, tok0 = 0;
+    if (sub < n_vsub) {
+        const int vi = sub * 32 + lane;
+        tok0 = vi * EPV;
+        if (vi < a.n_vec) {
+            ntok = EPV;
+            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(it.q.row) + vi);
+            const uint4 p = it.has_p ? __ldg(reinterpret_cast<const uint4 *>(it.p.row) + vi) : q;
+            float aq, ap;
+            if (it.has_p) {
+                if (it.filt) vec_weights<ES, true, true>(it, q, p, tok0, wv, aq, ap);
+                else vec_weights<ES, true, false>(it, q, p, tok0, wv, aq, ap);
+            } else {
+                if (it.filt) vec_weights<ES, false, true>(it, q, p, tok0, wv, aq, ap);
+                else vec_weights<ES, false, false>(it, q, p, tok0, wv, aq, ap);
+            }
+        }
+    } else {
+        tok0 = a.n_vec * EPV + lane;
+        if (tok0 < a.V) {
+            ntok = 1;
+            float aq, ap;
+            draw_scalar<ES>(it, tok0, wv[0], aq, ap);
+        }
+    }
+    double lt = 0.0;
+    for (int i = 0; i < ntok; ++i) lt += (double)wv[i];
+    double inc = lt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += v;
+    }
+    double run = pre + (inc - lt);
+    int hit = -1;
+    double c_prev = run, c_hit = run;
+    for (int i = 0; i < ntok; ++i) {
+        const double nxt = run + (double)wv[i];
+        if (hit < 0 && wv[i] > 0.f && thr < nxt) {
+            hit = i;
+            c_prev = run;
+            c_hit = nxt;
+        }
+        run = nxt;
+    }
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, hit >= 0);
+    int tstar;
+    double cp, ch;
+    if (m != 0) {
+        const int src = __ffs(m) - 1;
+        const int tok = tok0 + (ntok == 1 ? 0 : hit);
+        tstar = __shfl_sync(0xFFFFFFFFu, tok, src);
+        cp = __shfl_sync(0xFFFFFFFFu, c_prev, src);
+        ch = __shfl_sync(0xFFFFFFFFu, c_hit, src);
+    } else {
+        // rounding left thr past this sub-chunk: take its last positive weight, flag it
+        int lastpos = -1;
+        for (int i = 0; i < ntok; ++i)
+            if (wv[i] > 0.f) lastpos = i;
+        const unsigned mm = __ballot_sync(0xFFFFFFFFu, lastpos >= 0);
+        const int src = mm ? 31 - __clz(mm) : 0;
+        const int tok = tok0 + (ntok == 1 ? 0 : max(lastpos, 0));
+        tstar = __shfl_sync(0xFFFFFFFFu, tok, src);
+        cp = ch = __shfl_sync(0xFFFFFFFFu, run, src);
+        ambiguous = true;
+    }
+    if (lane == 0) {
+        const double E = draw_error_bound(it, R, A);
+        if (thr - cp <= E || ch - thr <= E) ambiguous = true;
+        const bool near = (thr - cp) < 1e-6 * R || (ch - thr) < 1e-6 * R;
+        *it.out = tstar;
+        if (it.dbg_r) *it.dbg_r = R;
+        stats_add(a.stats, &a.stats->draws, 1);
+        if (near) stats_add(a.stats, &a.stats->near_boundary, 1);
+        if (ambiguous && a.exact) {
+            stats_add(a.stats, &a.stats->reresolved, 1);
+            push_exact(a.counters, a.exact, {d, it.seq}, a.stats);
+        }
+    }
+}
+
+}  // namespace sv

@@ -1,0 +1,153 @@
+// sv_layout.h — parameter blocks and workspace layout shared by host and device code.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace sv {
+
+// ---- launch geometry ---------------------------------------------------------------------
+constexpr int kThreads = 256;               // threads per streaming block
+constexpr int kWarps = kThreads / 32;
+constexpr int kTileBytes = 16384;           // one bulk copy (one pipeline stage per row)
+constexpr int kStages = 4;                  // pipeline depth of the statistics pass
+constexpr int kDrawStages = 3;              // pipeline depth of the draw pass (two rows per stage)
+constexpr int kSubBytes = 512;              // bytes of one row per draw sub-chunk (32 x 16 B)
+constexpr int kMaxSplit = 64;               // most chunks per row
+constexpr int kUnitTarget = 16384;          // aim for about this many (row, chunk) units
+constexpr int kExactSplit = 16;             // chunks per row in the float-float tier
+constexpr int kExactCap = 2048;             // most queued items per call in the float-float tier
+constexpr long long kWaitLimitCycles = 4000000000LL;   // ~2 s at 2 GHz: bounded barrier waits
+
+// ---- certification constants of the float32 tier ------------------------------------------
+// Largest relative error of ex2.approx.ftz.f32 over [-126, 0] is below 2^-22 (checked by
+// sv_selftest_exp2 on the device); a margin of 2x is taken.
+constexpr double kEx2RelErr = 4.77e-7;
+constexpr double kU32 = 5.9604644775390625e-08;        // 2^-24, float32 unit roundoff
+constexpr double kLn2 = 0.69314718055994530942;
+// Relative error of 2^y per unit |y| from rounding y twice in float32: 2 * 2^-24 * ln 2.
+constexpr double kYRound = 2.0 * kU32 * kLn2;
+
+// ---- row descriptors ------------------------------------------------------------------------
+// A "row set" is a per-sequence logit tensor: row (b, j) starts at base + (b*rows_per_seq + j)*pitch.
+struct RowSet {
+    const char *base;
+    int64_t pitch_bytes;
+    int rows_per_seq;
+    int rows_used;        // rows j < rows_used of every sequence are candidates
+    int skip_greedy;      // 1: rows of greedy sequences are not streamed
+};
+
+// Per-(row, chunk, warp) partial of the statistics pass.
+struct WarpPartial {
+    double s;       // sum of 2^(x c - r) over the warp's elements
+    double a;       // sum of 2^(x c - r) * |x c - r| (feeds the certified error bound)
+    int r;          // integer reference exponent, >= x*c of every element seen; -2^30 if none
+    float maxv;     // largest logit seen (NaN-free)
+    int argmax;     // its lowest index
+    int flags;      // kFlagNaN | kFlagPosInf
+};
+
+constexpr int kFlagNaN = 1;
+constexpr int kFlagPosInf = 2;
+constexpr int kNoRef = -(1 << 30);
+
+// Combined statistics of one row.
+struct RowStat {
+    double g;       // log2 normaliser: log2 sum_v 2^(x_v c), c = log2(e)/T   (NaN for greedy rows)
+    double err;     // certified relative error bound of 2^g (float32 tier)
+    double S;       // sum_v 2^(x_v c - r)
+    float maxv;
+    int argmax;
+    int r;
+    int flags;
+};
+
+// Nucleus (top-p) cut of a row: token v is kept iff x_v > cut_x or (x_v == cut_x and v <= cut_id).
+// mass = kept probability mass.  A row without a filter has cut_x = -inf, cut_id = INT32_MAX, mass 1.
+struct NucleusCut {
+    float cut_x;
+    int cut_id;
+    double mass;
+    double log2_mass;
+    int ambiguous;  // the float32 tier could not certify the cut
+    int pad;
+};
+
+// Saguaro top-F set of a draft row: v in D iff x_v > top_x or (x_v == top_x and v <= top_id).
+struct TopSet {
+    float top_x;
+    int top_id;
+    double p_d;     // probability mass of D (after temperature and top-p) before scaling
+    double z;       // normaliser after scaling: 1 - (1 - C) p_d
+};
+
+// A row as seen by the draw pass: weight(v) = keep(v) * 2^(x_v c - r) * inv_s * (in_D ? sc_d : 1).
+struct DrawRow {
+    const char *row;
+    float c_hi, c_lo;       // c = log2(e)/T
+    float rf;               // reference exponent r (as float)
+    float inv_s;            // 1 / (S * nucleus mass * Saguaro normaliser), float32
+    float cut_x; int cut_id;
+    float top_x; int top_id;
+    float sc_d;             // C for tokens in D (1 when no transform)
+    int pad;
+    double norm_err;        // relative error bound of inv_s (normaliser from the stats pass)
+};
+
+// One pending draw: t* = inverse CDF of w at u, w = max(q - p, 0) (has_p) or q.
+struct DrawItem {
+    DrawRow q, p;
+    double u;
+    int *out;               // where t* is written
+    double *dbg_r;          // where R (sum of the weights) is written, or nullptr
+    int has_p;
+    int filt;               // nucleus cut or top-F set in use
+    int seq;
+    int k;                  // draw position (accepted count for sv_verify)
+};
+
+// Exact-tier work item: a draw to redo (draw >= 0) or a sequence whose accept tests must be
+// redone (draw < 0).
+struct ExactItem {
+    int draw;
+    int seq;
+};
+
+// Counters that each call resets before use (kernel-side).
+struct Counters {
+    int n_draws;
+    int n_exact;
+    unsigned barrier;       // grid barrier of the exact tier
+    int pad[13];
+};
+
+inline int div_up(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Chunks per row: enough (row, chunk) units to balance ~kUnitTarget of them, chunks >= one tile.
+inline int choose_split(long long n_rows, long long row_bytes) {
+    long long by_units = (kUnitTarget + n_rows - 1) / (n_rows > 0 ? n_rows : 1);
+    long long by_size = row_bytes / kTileBytes;
+    long long s = by_units < by_size ? by_units : by_size;
+    if (s < 1) s = 1;
+    if (s > kMaxSplit) s = kMaxSplit;
+    return (int)s;
+}
+
+// Sub-chunks of a row in the draw pass: one per 32 16-byte vectors, plus a last one holding the
+// (< 16 B) scalar tail of the row.
+inline int vec_count(int V, int es) { return (int)(((long long)V * es) / 16); }
+inline int sub_chunks(int V, int es) { return div_up(vec_count(V, es), 32) + 1; }
+
+// 256-byte aligned bump allocator over the caller's workspace.
+struct Carver {
+    size_t off = 0;
+    template <class T>
+    size_t take(size_t count) {
+        size_t o = (off + 255) & ~size_t(255);
+        off = o + count * sizeof(T);
+        return o;
+    }
+};
+
+}  // namespace sv

@@ -1,0 +1,339 @@
+// sv_stats.cuh — statistics pass: one streaming read of every needed logit row.
+//
+// For a sampled row (temperature T > 0, c = log2(e)/T) the pass accumulates
+//   S = sum_v 2^(x_v c - r)       with an integer reference r >= max_v x_v c,
+//   A = sum_v 2^(x_v c - r) |x_v c - r|    (enters the certified error bound),
+// so that log2 sum_v 2^(x_v c) = r + log2 S and LSE = (r + log2 S) ln 2.  For a greedy row
+// (T == 0) it finds the maximum and its lowest index.  Both track NaN / +inf.
+//
+// Work is a static round-robin over (row, chunk) units across a persistent grid.  Thread 0 of
+// each block feeds a kStages-deep ring of 16 KB shared-memory tiles with 1-D bulk copies
+// (cp.async.bulk); the block consumes tiles with 128-bit shared loads.  Each warp writes one
+// WarpPartial per unit, combined later in float64.
+#pragma once
+
+#include "sv_device.cuh"
+
+namespace sv {
+
+struct StatsArgs {
+    RowSet set[2];
+    int n_sets;
+    int V;
+    const float *temperature;   // per sequence; nullptr -> T = 1
+    int n_split;                // chunks per row
+    int chunk_vecs;             // 16-byte vectors per chunk
+    long long n_rows0;          // candidate rows in set 0
+    long long n_units;          // candidate rows * n_split
+    WarpPartial *part;          // [candidate row][chunk][warp]
+    Counters *counters;         // zeroed by block 0 (consumed by later kernels of the call)
+    sv_stats *stats;
+    long long wait_limit;
+};
+
+struct UnitInfo {
+    const char *row;
+    long long rid;
+    int chunk;
+    int v0, v1;           // vector range
+    int tail0, n_tail;    // scalar tail elements (last chunk only)
+    bool needed;
+    bool greedy;
+    float c_hi, c_lo;
+};
+
+template <int ES>
+__device__ __forceinline__ UnitInfo stats_unit(const StatsArgs &a, long long u) {
+    UnitInfo ui;
+    ui.rid = u / a.n_split;
+    ui.chunk = static_cast<int>(u - ui.rid * a.n_split);
+    const int s = ui.rid < a.n_rows0 ? 0 : 1;
+    const long long lr = s == 0 ? ui.rid : ui.rid - a.n_rows0;
+    const RowSet &rs = a.set[s];
+    const long long b = lr / rs.rows_used;
+    const long long j = lr - b * rs.rows_used;
+    const float T = a.temperature ? a.temperature[b] : 1.0f;
+    ui.greedy = (T == 0.0f);
+    ui.needed = !(rs.skip_greedy && ui.greedy);
+    ui.row = rs.base + (b * rs.rows_per_seq + j) * rs.pitch_bytes;
+    const double c = 1.4426950408889634074 / (double)T;
+    ui.c_hi = (float)c;
+    ui.c_lo = (float)(c - (double)ui.c_hi);
+    constexpr int EPV = 16 / ES;
+    const int n_vec = (a.V * ES) / 16;
+    ui.v0 = min(ui.chunk * a.chunk_vecs, n_vec);
+    ui.v1 = min(ui.v0 + a.chunk_vecs, n_vec);
+    ui.tail0 = n_vec * EPV;
+    ui.n_tail = (ui.chunk == a.n_split - 1) ? (a.V - ui.tail0) : 0;
+    return ui;
+}
+
+__device__ __forceinline__ int unit_tiles(const UnitInfo &ui) {
+    return (ui.v1 - ui.v0 + (kTileBytes / 16) - 1) / (kTileBytes / 16);
+}
+
+// Per-thread accumulator.
+struct StatAcc {
+    int r;
+    float rf, thr, s, comp, aerr;
+    float m;
+    int am;
+    int flags;
+};
+
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+__device__ __forceinline__ void acc_init(StatAcc &A) {
+    A.r = kNoRef;
+    A.rf = (float)kNoRef;
+    A.thr = -INFINITY;
+    A.s = 0.f;
+    A.comp = 0.f;
+    A.aerr = 0.f;
+    A.m = -INFINITY;
+    A.am = 0x7FFFFFFF;
+    A.flags = 0;
+}
+
+// Raise the reference exponent so that x*c <= r for x <= vmax (exact power-of-two rescale).
+__device__ __forceinline__ void acc_reference(StatAcc &A, float vmax, float c_hi) {
+    if (vmax != vmax) {
+        A.flags |= kFlagNaN;
+        return;
+    }
+    if (isinf(vmax)) {
+        if (vmax > 0.f) A.flags |= kFlagPosInf;
+        return;
+    }
+    float yr = ceilf(vmax * c_hi);
+    yr = fminf(fmaxf(yr, -1.0e9f), 1.0e9f);
+    const int rn = (int)yr;
+    if (rn > A.r) {
+        const int d = rn - A.r;
+        const float sc = pow2i(-d);
+        const float tot = A.s + A.comp;
+        A.aerr = (A.aerr + (float)min(d, 1 << 20) * tot) * sc;
+        A.s *= sc;
+        A.comp *= sc;
+        A.r = rn;
+        A.rf = (float)rn;
+    }
+    A.thr = fmaxf(A.rf / c_hi, vmax);
+}
+
+__device__ __forceinline__ void acc_add(StatAcc &A, float s8) {
+    const float t = __fadd_rn(A.s, s8);
+    const float e = (A.s >= s8) ? __fadd_rn(__fsub_rn(A.s, t), s8) : __fadd_rn(__fsub_rn(s8, t), A.s);
+    A.comp = __fadd_rn(A.comp, e);
+    A.s = t;
+}
+
+// One element outside the vector stream (row tails).
+__device__ __forceinline__ void acc_scalar(StatAcc &A, float x, int idx, bool greedy, float c_hi, float c_lo) {
+    if (greedy) {
+        if (!(x <= A.m)) {
+            if (x != x) {
+                A.flags |= kFlagNaN;
+            } else {
+                A.m = x;
+                A.am = idx;
+                if (isinf(x)) A.flags |= kFlagPosInf;
+            }
+        }
+        return;
+    }
+    if (!(x <= A.thr)) acc_reference(A, x, c_hi);
+    const float y = fmaf(x, c_lo, fmaf(x, c_hi, -A.rf));
+    const float e = ex2_fast(y);
+    A.aerr = fmaf(e, fabsf(y), A.aerr);
+    acc_add(A, e);
+}
+
+template <int N>
+__device__ __forceinline__ void acc_sampled(StatAcc &A, const float (&x)[N], float vmax, float c_hi, float c_lo) {
+    if (!(vmax <= A.thr)) acc_reference(A, vmax, c_hi);
+    float e[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const float y = fmaf(x[i], c_lo, fmaf(x[i], c_hi, -A.rf));
+        e[i] = ex2_fast(y);
+        A.aerr = fmaf(e[i], fabsf(y), A.aerr);
+    }
+    float s;
+    if constexpr (N == 8) {
+        s = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+    } else {
+        s = (e[0] + e[1]) + (e[2] + e[3]);
+    }
+    acc_add(A, s);
+}
+
+template <int N>
+__device__ __forceinline__ void acc_greedy_update(StatAcc &A, const float (&x)[N], float vmax, int e0) {
+    if (vmax != vmax) {
+        A.flags |= kFlagNaN;
+        return;
+    }
+    int idx = 0;
+#pragma unroll
+    for (int i = N - 1; i >= 0; --i)
+        if (x[i] == vmax) idx = i;
+    A.m = vmax;
+    A.am = e0 + idx;
+    if (isinf(vmax)) A.flags |= kFlagPosInf;
+}
+
+// One 16-byte vector at element index e0.
+template <int ES>
+__device__ __forceinline__ void acc_vector(StatAcc &A, uint4 w, int e0, bool greedy, float c_hi, float c_lo) {
+    if (ES == 2) {
+        const uint32_t pm = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+        const float vmax = fmax_nan(bf16_lo(pm), bf16_hi(pm));
+        const float x[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                            bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+        if (greedy) {
+            if (!(vmax <= A.m)) acc_greedy_update<8>(A, x, vmax, e0);
+        } else {
+            acc_sampled<8>(A, x, vmax, c_hi, c_lo);
+        }
+    } else {
+        const float x[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                            __uint_as_float(w.w)};
+        const float vmax = fmax_nan(fmax_nan(x[0], x[1]), fmax_nan(x[2], x[3]));
+        if (greedy) {
+            if (!(vmax <= A.m)) acc_greedy_update<4>(A, x, vmax, e0);
+        } else {
+            acc_sampled<4>(A, x, vmax, c_hi, c_lo);
+        }
+    }
+}
+
+// Warp-combine and store this unit's partial.
+__device__ __forceinline__ void acc_store(const StatAcc &A0, bool greedy, WarpPartial *dst) {
+    StatAcc A = A0;
+    const int lane = threadIdx.x & 31;
+    WarpPartial p;
+    p.flags = warp_or_i(A.flags);
+    if (greedy) {
+        warp_argmax(A.m, A.am);
+        p.s = 0.0;
+        p.a = 0.0;
+        p.r = kNoRef;
+        p.maxv = A.m;
+        p.argmax = A.am;
+    } else {
+        const int rw = warp_max_i(A.r);
+        const int d = rw - A.r;   // >= 0
+        const double tot = (double)A.s + (double)A.comp;
+        double sd = 0.0, ad = 0.0;
+        if (d < 1000) {
+            const double sc = ldexp(1.0, -d);
+            sd = tot * sc;
+            ad = ((double)A.aerr + (double)d * tot) * sc;
+        }
+        p.s = warp_sum_d(sd);
+        p.a = warp_sum_d(ad);
+        p.r = rw;
+        p.maxv = -INFINITY;
+        p.argmax = 0x7FFFFFFF;
+    }
+    if (lane == 0) *dst = p;
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kThreads, 2) k_stats(const StatsArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    unsigned char *tiles = smem + 128;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+
+    if (blockIdx.x == 0 && tid < (int)(sizeof(Counters) / 4) && a.counters)
+        reinterpret_cast<int *>(a.counters)[tid] = 0;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // ---- producer state (meaningful in thread 0 only) ----
+    long long pu = blockIdx.x;
+    int pt = 0;
+    UnitInfo pui;
+    bool p_valid = false;
+    long long issued = 0;
+    const uint64_t policy = policy_evict_first();
+    auto p_seek = [&]() {
+        // position (pu, pt) on the next existing tile
+        while (pu < a.n_units) {
+            if (!p_valid) {
+                pui = stats_unit<ES>(a, pu);
+                p_valid = true;
+            }
+            if (pui.needed && pt < unit_tiles(pui)) return true;
+            pu += gridDim.x;
+            pt = 0;
+            p_valid = false;
+        }
+        return false;
+    };
+    auto p_issue = [&](int stage) {
+        if (!p_seek()) return;
+        const int fv = pui.v0 + pt * (kTileBytes / 16);
+        const int nv = min(kTileBytes / 16, pui.v1 - fv);
+        const uint32_t bytes = (uint32_t)nv * 16u;
+        mbar_arrive_expect_tx(&full[stage], bytes);
+        bulk_load_stream(tiles + stage * kTileBytes, pui.row + (size_t)fv * 16, bytes, &full[stage], policy);
+        ++issued;
+        ++pt;
+    };
+    if (tid == 0)
+        for (int s = 0; s < kStages; ++s) p_issue(s);
+
+    long long it = 0;   // tiles consumed by this block
+    for (long long u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+        const UnitInfo ui = stats_unit<ES>(a, u);
+        if (!ui.needed) continue;
+        StatAcc A;
+        acc_init(A);
+        const int nt = unit_tiles(ui);
+        for (int t = 0; t < nt; ++t, ++it) {
+            const int st = (int)(it % kStages);
+            const uint32_t par = (uint32_t)((it / kStages) & 1);
+            const bool ok = mbar_wait_bounded(&full[st], par, a.wait_limit);
+            if (ok) {
+                const int fv = ui.v0 + t * (kTileBytes / 16);
+                const int nv = min(kTileBytes / 16, ui.v1 - fv);
+                const unsigned char *buf = tiles + st * kTileBytes;
+                constexpr int EPV = 16 / ES;
+#pragma unroll 4
+                for (int vi = tid; vi < nv; vi += kThreads) {
+                    const uint4 w = lds128(buf + vi * 16);
+                    acc_vector<ES>(A, w, (fv + vi) * EPV, ui.greedy, ui.c_hi, ui.c_lo);
+                }
+            }
+            if (__syncthreads_or(!ok)) {
+                if (tid == 0) {
+                    report_error(a.stats, SV_ERR_TIMEOUT, (int)ui.rid);
+                    // let copies still in flight land before the block's shared memory is released
+                    for (long long k = it; k < issued; ++k)
+                        mbar_wait_bounded(&full[k % kStages], (uint32_t)((k / kStages) & 1), a.wait_limit / 16);
+                }
+                return;
+            }
+            if (tid == 0) p_issue(st);
+        }
+        // the row's last (< 16 B) elements come after every vector, keeping greedy ties on the lowest id
+        if (tid < ui.n_tail) {
+            const float x = load_elem<ES>(ui.row, ui.tail0 + tid);
+            acc_scalar(A, x, ui.tail0 + tid, ui.greedy, ui.c_hi, ui.c_lo);
+        }
+        acc_store(A, ui.greedy, a.part + ((size_t)ui.rid * a.n_split + ui.chunk) * kWarps + warp);
+    }
+}
+
+}  // namespace sv

@@ -1,0 +1,506 @@
+// sv_verify.cu — sv_verify: modified rejection sampling over the vocabulary for B sequences.
+//
+// ["Speculative Speculative Decoding" notes, §2.2 steps ①-④; "Accelerating LLM Decoding with
+//  Speculative Sampling (2023)" notes, §3; "Mirror Speculative Decoding" notes, §2 step 3]
+//
+// Kernels, in stream order:
+//   k_stats        one streaming pass over every needed row: target rows of all sequences, draft
+//                  rows of sampled sequences (greedy sequences never read the draft)
+//   k_nucleus      (top-p only) the nucleus cut of every sampled row
+//   k_topset       (sigma_{F,C} only) the top-F set of every draft row
+//   k_accept       per sequence: float64 row normalisers, the accept tests u < min(1, q/p) with a
+//                  certified margin, the first rejection k, greedy outputs, and a draw item
+//   k_draw_sums    per draw: sub-chunk sums of w = (q_{k+1} - p_{k+1})_+ or q_{K+1}
+//   k_draw_finish  per draw: t* with a certified margin
+//   k_exact        float-float tier for the decisions the margins could not settle
+#include <math.h>
+
+#include "sv_draw.cuh"
+#include "sv_exact.cuh"
+#include "sv_host.h"
+#include "sv_select.cuh"
+#include "sv_stats.cuh"
+
+namespace sv {
+
+struct AcceptArgs {
+    RowSet tgt, drf;
+    int K, V;
+    const float *temperature;
+    const float *top_p;
+    int sag_on;
+    float sag_C;
+    const int32_t *tokens;
+    const double *uniforms;
+    int32_t *accept_len;
+    int32_t *out_tokens;
+    double *debug;
+    sv_stats *stats;
+    const WarpPartial *part;
+    int n_split;
+    long long n_rows0;
+    RowStat *rowstat;
+    const NucleusCut *nuc;
+    const TopSet *top;
+    DrawItem *draws;
+    ExactItem *exact;
+    Counters *counters;
+};
+
+// Combine a row's warp partials (one warp).
+__device__ __forceinline__ RowStat combine_row(const WarpPartial *P, int np, bool greedy) {
+    const int lane = threadIdx.x & 31;
+    int rmax = kNoRef;
+    for (int p = lane; p < np; p += 32) rmax = max(rmax, P[p].r);
+    rmax = warp_max_i(rmax);
+    double s = 0.0, a = 0.0;
+    float m = -INFINITY;
+    int am = 0x7FFFFFFF, fl = 0;
+    for (int p = lane; p < np; p += 32) {
+        const WarpPartial w = P[p];
+        fl |= w.flags;
+        if (greedy) {
+            if (w.maxv > m || (w.maxv == m && w.argmax < am)) {
+                m = w.maxv;
+                am = w.argmax;
+            }
+        } else {
+            const int d = rmax - w.r;
+            if (d < 1000) {
+                const double sc = ldexp(1.0, -d);
+                s += w.s * sc;
+                a += (w.a + (double)d * w.s) * sc;
+            }
+        }
+    }
+    RowStat r;
+    r.S = warp_sum_d(s);
+    const double A = warp_sum_d(a);
+    r.flags = warp_or_i(fl);
+    warp_argmax(m, am);
+    r.maxv = m;
+    r.argmax = am;
+    r.r = rmax;
+    if (greedy) {
+        r.g = NAN;
+        r.err = 0.0;
+    } else {
+        r.g = (double)rmax + log2(r.S);
+        // ex2 error + exponent rounding (|y| weighted) + float32 summation (tree + compensated)
+        r.err = kEx2RelErr + 1.01 * kYRound * (r.S > 0.0 ? A / r.S : 0.0) + 6.0 * kU32 + 1e-12;
+    }
+    return r;
+}
+
+__device__ __forceinline__ DrawRow draw_row(const char *row, double c, const RowStat &rs, const NucleusCut *nc,
+                                            const TopSet *ts, float sag_C) {
+    DrawRow d;
+    d.row = row;
+    d.c_hi = (float)c;
+    d.c_lo = (float)(c - (double)d.c_hi);
+    d.rf = (float)rs.r;
+    double norm = rs.S;
+    double err = rs.err;
+    d.cut_x = -INFINITY;
+    d.cut_id = 0x7FFFFFFF;
+    if (nc) {
+        d.cut_x = nc->cut_x;
+        d.cut_id = nc->cut_id;
+        norm *= nc->mass;
+        err += 2.0 * rs.err + 1e-12;   // the kept mass is a ratio of two sums of the same pass
+    }
+    d.top_x = INFINITY;
+    d.top_id = -1;
+    d.sc_d = 1.0f;
+    if (ts) {
+        d.top_x = ts->top_x;
+        d.top_id = ts->top_id;
+        d.sc_d = sag_C;
+        norm *= ts->z;
+        err += 2.0 * rs.err + 1e-12;
+    }
+    d.inv_s = (float)(1.0 / norm);
+    d.pad = 0;
+    d.norm_err = err;
+    return d;
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
+    __shared__ RowStat rs[2 * SV_MAX_K + 1];
+    __shared__ int s_err;
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int K = a.K, V = a.V;
+    const float T = a.temperature[b];
+    const bool greedy = (T == 0.0f);
+    const bool bad_t = !(greedy || (T >= 1e-3f && T <= 1e3f));
+    int32_t *outs = a.out_tokens + (size_t)b * (K + 1);
+    if (tid == 0) s_err = 0;
+    __syncthreads();
+    if (bad_t) {
+        if (tid == 0) {
+            report_error(a.stats, SV_ERR_INVALID_ARG, b);
+            a.accept_len[b] = 0;
+        }
+        for (int j = tid; j <= K; j += kThreads) outs[j] = -1;
+        return;
+    }
+    const int n_t = K + 1, n_d = greedy ? 0 : K;
+    for (int i = warp; i < n_t + n_d; i += kWarps) {
+        const long long rid = i < n_t ? (long long)b * n_t + i : a.n_rows0 + (long long)b * K + (i - n_t);
+        const RowStat r = combine_row(a.part + (size_t)rid * a.n_split * kWarps, a.n_split * kWarps, greedy);
+        if (lane == 0) {
+            rs[i] = r;
+            a.rowstat[rid] = r;
+            const bool bad = (r.flags != 0) || (greedy ? !isfinite(r.maxv) : !(r.S > 0.0) || !isfinite(r.g));
+            if (bad) {
+                atomicOr(&s_err, 1);
+                report_error(a.stats, SV_ERR_NONFINITE, (int)rid);
+            }
+        }
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    if (lane == 0) stats_add(a.stats, &a.stats->rows, n_t + n_d);
+    if (s_err) {
+        if (lane == 0) a.accept_len[b] = 0;
+        for (int j = lane; j <= K; j += 32) outs[j] = -1;
+        return;
+    }
+
+    // ---- accept tests (lane j tests position j+1) ----
+    const double c = greedy ? 0.0 : 1.4426950408889634074 / (double)T;
+    const double sag_l2c = log2((double)a.sag_C);
+    int s = -1;
+    bool acc = false, amb = false, near = false, badtok = false;
+    double q_s = NAN, p_s = NAN, ratio = NAN;
+    if (lane < K) {
+        s = a.tokens[(size_t)b * K + lane];
+        badtok = s < 0 || s >= V;
+        if (!badtok) {
+            if (greedy) {
+                acc = (s == rs[lane].argmax);
+            } else {
+                const long long rid_t = (long long)b * n_t + lane;
+                const long long rid_d = a.n_rows0 + (long long)b * K + lane;
+                const RowSet &ts = a.tgt, &ds = a.drf;
+                const char *trow = ts.base + ((long long)b * ts.rows_per_seq + lane) * ts.pitch_bytes;
+                const char *drow = ds.base + ((long long)b * ds.rows_per_seq + lane) * ds.pitch_bytes;
+                const float xt = load_elem<ES>(trow, s);
+                const float xd = load_elem<ES>(drow, s);
+                const RowStat &rq = rs[lane], &rp = rs[n_t + lane];
+                double lq = (double)xt * c - rq.g;
+                double lp = (double)xd * c - rp.g;
+                double delta = rq.err + rp.err;
+                if (a.nuc) {
+                    const NucleusCut nq = a.nuc[rid_t], np = a.nuc[rid_d];
+                    lq = (xt > nq.cut_x || (xt == nq.cut_x && s <= nq.cut_id)) ? lq - nq.log2_mass : -INFINITY;
+                    lp = (xd > np.cut_x || (xd == np.cut_x && s <= np.cut_id)) ? lp - np.log2_mass : -INFINITY;
+                    delta += 2.0 * (rq.err + rp.err);
+                }
+                if (a.sag_on && a.top) {
+                    const TopSet t = a.top[rid_d];
+                    if (xd > t.top_x || (xd == t.top_x && s <= t.top_id)) lp += sag_l2c;
+                    lp -= log2(t.z);
+                    delta += 2.0 * rp.err;
+                }
+                if (lp == -INFINITY) ratio = (lq == -INFINITY) ? 0.0 : INFINITY;
+                else ratio = exp2(lq - lp);
+                q_s = exp2(lq);
+                p_s = exp2(lp);
+                const double r = fmin(1.0, ratio);
+                delta = 1.01 * delta + 1e-13;
+                const double lo = fmin(1.0, ratio * (1.0 - delta));
+                const double hi = fmin(1.0, ratio * (1.0 + delta));
+                const double u = a.uniforms[(size_t)b * (K + 1) + lane];
+                acc = u < r;
+                amb = (u >= lo) && (u < hi);
+                near = fabs(u - r) < 1e-6;
+            }
+        }
+    }
+    const unsigned lowK = K >= 32 ? 0xFFFFFFFFu : ((1u << K) - 1u);
+    const unsigned accm = __ballot_sync(0xFFFFFFFFu, acc) & lowK;
+    const unsigned badm = __ballot_sync(0xFFFFFFFFu, badtok) & lowK;
+    const unsigned rej = ~accm & lowK;
+    const int k = rej ? __ffs(rej) - 1 : K;
+    const unsigned scanned = (unsigned)((k < K) ? ((2ull << k) - 1ull) : (unsigned long long)lowK);
+    const unsigned ambm = __ballot_sync(0xFFFFFFFFu, amb) & scanned;
+    const unsigned nearm = __ballot_sync(0xFFFFFFFFu, near) & scanned;
+    if (badm) {
+        if (lane == 0) {
+            report_error(a.stats, SV_ERR_BAD_TOKEN, b);
+            a.accept_len[b] = 0;
+        }
+        for (int j = lane; j <= K; j += 32) outs[j] = -1;
+        return;
+    }
+    // outputs: s_1..s_k, then t* (greedy now, sampled after the draw), -1 padding
+    for (int j = lane; j <= K; j += 32) outs[j] = j < k ? a.tokens[(size_t)b * K + j] : -1;
+    __syncwarp();
+    if (lane == 0) {
+        a.accept_len[b] = k;
+        if (greedy) outs[k] = rs[k].argmax;
+        if (!greedy) {
+            stats_add(a.stats, &a.stats->accept_tests, min(k + 1, K));
+            stats_add(a.stats, &a.stats->near_boundary, __popc(nearm));
+        }
+    }
+    if (a.debug) {
+        for (int j = lane; j <= K; j += 32) {
+            double *dbg = a.debug + ((size_t)b * (K + 1) + j) * SV_DEBUG_FIELDS;
+            const long long rid_t = (long long)b * n_t + j;
+            dbg[SV_DBG_LSE_Q] = greedy ? NAN : rs[j].g * kLn2;
+            dbg[SV_DBG_LSE_P] = (greedy || j >= K) ? NAN : rs[n_t + j].g * kLn2;
+            dbg[SV_DBG_Q_S] = j < K ? q_s : NAN;
+            dbg[SV_DBG_P_S] = j < K ? p_s : NAN;
+            dbg[SV_DBG_RATIO] = j < K ? ratio : NAN;
+            dbg[SV_DBG_MASS_Q] = (greedy || !a.nuc) ? 1.0 : a.nuc[rid_t].mass;
+            dbg[SV_DBG_MASS_P] = (greedy || !a.nuc || j >= K) ? 1.0 : a.nuc[a.n_rows0 + (long long)b * K + j].mass;
+            dbg[SV_DBG_R] = NAN;
+        }
+    }
+    if (greedy || lane != 0) return;
+    if (ambm) {
+        // an accept test too close to call in float32: the float-float tier redoes the sequence
+        stats_add(a.stats, &a.stats->reresolved, 1);
+        push_exact(a.counters, a.exact, {-1, b}, a.stats);
+        return;
+    }
+    const int d = atomicAdd(&a.counters->n_draws, 1);
+    DrawItem it;
+    const long long rid_q = (long long)b * n_t + k;
+    const char *qrow = a.tgt.base + ((long long)b * a.tgt.rows_per_seq + k) * a.tgt.pitch_bytes;
+    it.q = draw_row(qrow, c, rs[k], a.nuc ? a.nuc + rid_q : nullptr, nullptr, 1.0f);
+    it.has_p = k < K;
+    if (it.has_p) {
+        const long long rid_p = a.n_rows0 + (long long)b * K + k;
+        const char *prow = a.drf.base + ((long long)b * a.drf.rows_per_seq + k) * a.drf.pitch_bytes;
+        it.p = draw_row(prow, c, rs[n_t + k], a.nuc ? a.nuc + rid_p : nullptr,
+                        (a.sag_on && a.top) ? a.top + rid_p : nullptr, a.sag_C);
+    } else {
+        it.p = {};
+        it.p.top_x = INFINITY;
+        it.p.cut_x = -INFINITY;
+        it.p.cut_id = 0x7FFFFFFF;
+    }
+    it.filt = (a.nuc != nullptr) || (a.sag_on && a.top != nullptr);
+    it.u = a.uniforms[(size_t)b * (K + 1) + K];
+    it.out = outs + k;
+    it.dbg_r = a.debug ? a.debug + (size_t)b * (K + 1) * SV_DEBUG_FIELDS + SV_DBG_R : nullptr;
+    it.seq = b;
+    it.k = k;
+    a.draws[d] = it;
+}
+
+// ------------------------------------------------------------------------------------------
+// Host side
+// ------------------------------------------------------------------------------------------
+VerifyPlan plan_verify(int B, int K, int V, int es) {
+    VerifyPlan p;
+    p.es = es;
+    p.n_rows0 = (long long)B * (K + 1);
+    p.n_rows1 = (long long)B * K;
+    const long long n_cand = p.n_rows0 + p.n_rows1;
+    const long long row_bytes = (long long)V * es;
+    p.n_split = choose_split(n_cand, row_bytes);
+    p.n_vec = vec_count(V, es);
+    p.chunk_vecs = p.n_vec > 0 ? div_up(p.n_vec, p.n_split) : 1;
+    p.n_sub = sub_chunks(V, es);
+    const int n_vsub = p.n_sub - 1;
+    long long want = (4096 + B - 1) / B;
+    long long dcap = n_vsub / 32 > 0 ? n_vsub / 32 : 1;
+    p.d_split = (int)(want < dcap ? want : dcap);
+    if (p.d_split < 1) p.d_split = 1;
+    p.d_subs_per_chunk = n_vsub > 0 ? div_up(n_vsub, p.d_split) : 1;
+    Carver cv;
+    p.off_counters = cv.take<Counters>(1);
+    p.off_part = cv.take<WarpPartial>((size_t)n_cand * p.n_split * kWarps);
+    p.off_rowstat = cv.take<RowStat>((size_t)n_cand);
+    p.off_nuc = cv.take<NucleusCut>((size_t)n_cand);
+    p.off_top = cv.take<TopSet>((size_t)n_cand);
+    p.off_draws = cv.take<DrawItem>((size_t)B);
+    p.off_subs = cv.take<float2>((size_t)B * p.n_sub);
+    const size_t cap = (size_t)(B < kExactCap ? B : (int)kExactCap);
+    p.off_exact = cv.take<ExactItem>(cap);
+    const int max_slots = 2 * K + 1 > 2 ? 2 * K + 1 : 2;
+    p.off_xpart = cv.take<double>(cap * max_slots * kExactSplit * 3);
+    p.off_xdraw = cv.take<ExactDraw>(cap);
+    p.off_xsubs = cv.take<double>(cap * p.n_sub);
+    p.bytes = cv.off + 256;
+    return p;
+}
+
+template <int ES>
+static sv_status launch_verify(const VerifyPlan &pl, const AcceptArgs &acc_in, const float *top_p, int F,
+                               float C, int B, void *ws, cudaStream_t stream) {
+    DeviceInfo di;
+    if (!device_info(di)) return SV_ERR_CUDA;
+    char *w = static_cast<char *>(ws);
+    Counters *counters = reinterpret_cast<Counters *>(w + pl.off_counters);
+    WarpPartial *part = reinterpret_cast<WarpPartial *>(w + pl.off_part);
+    const long long wait = kWaitLimitCycles;
+    AcceptArgs acc = acc_in;
+
+    // 1. statistics pass
+    StatsArgs sa;
+    sa.set[0] = acc.tgt;
+    sa.set[1] = acc.drf;
+    sa.n_sets = 2;
+    sa.V = acc.V;
+    sa.temperature = acc.temperature;
+    sa.n_split = pl.n_split;
+    sa.chunk_vecs = pl.chunk_vecs;
+    sa.n_rows0 = pl.n_rows0;
+    sa.n_units = (pl.n_rows0 + pl.n_rows1) * pl.n_split;
+    sa.part = part;
+    sa.counters = counters;
+    sa.stats = acc.stats;
+    sa.wait_limit = wait;
+    {
+        const size_t smem = 128 + (size_t)kStages * kTileBytes;
+        const int occ = prepare_kernel((const void *)k_stats<ES>, kThreads, smem);
+        if (occ < 1) return SV_ERR_CUDA;
+        long long grid = (long long)di.sms * occ;
+        if (grid > sa.n_units) grid = sa.n_units;
+        if (grid < 1) grid = 1;
+        profile_begin(stream);
+        k_stats<ES><<<(unsigned)grid, kThreads, smem, stream>>>(sa);
+        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+        profile_end(stream);
+    }
+    // 2. nucleus cuts and top-F sets (only when asked for)
+    NucleusCut *nuc = nullptr;
+    TopSet *top = nullptr;
+    if (top_p) {
+        nuc = reinterpret_cast<NucleusCut *>(w + pl.off_nuc);
+        sv_status st = launch_nucleus<ES>(acc.tgt, acc.drf, pl.n_rows0, pl.n_rows1, acc.V, acc.temperature, top_p,
+                                          part, pl.n_split, reinterpret_cast<RowStat *>(w + pl.off_rowstat), nuc,
+                                          acc.stats, di, stream);
+        if (st != SV_OK) return st;
+    }
+    if (acc.sag_on) {
+        top = reinterpret_cast<TopSet *>(w + pl.off_top);
+        sv_status st = launch_topset<ES>(acc.drf, pl.n_rows0, B, acc.K, acc.V, acc.temperature, F, C, part,
+                                         pl.n_split, nuc, top, acc.stats, di, stream);
+        if (st != SV_OK) return st;
+    }
+    // 3. accept tests
+    acc.part = part;
+    acc.n_split = pl.n_split;
+    acc.n_rows0 = pl.n_rows0;
+    acc.rowstat = reinterpret_cast<RowStat *>(w + pl.off_rowstat);
+    acc.nuc = nuc;
+    acc.top = top;
+    acc.draws = reinterpret_cast<DrawItem *>(w + pl.off_draws);
+    acc.exact = reinterpret_cast<ExactItem *>(w + pl.off_exact);
+    acc.counters = counters;
+    k_accept<ES><<<B, kThreads, 0, stream>>>(acc);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    // 4. draws
+    DrawArgs da;
+    da.items = acc.draws;
+    da.counters = counters;
+    da.V = acc.V;
+    da.n_vec = pl.n_vec;
+    da.n_sub = pl.n_sub;
+    da.n_split = pl.d_split;
+    da.subs_per_chunk = pl.d_subs_per_chunk;
+    da.subs = reinterpret_cast<float2 *>(w + pl.off_subs);
+    da.exact = acc.exact;
+    da.stats = acc.stats;
+    da.wait_limit = wait;
+    {
+        const size_t smem = 128 + (size_t)2 * kDrawStages * kTileBytes;
+        const int occ = prepare_kernel((const void *)k_draw_sums<ES>, kThreads, smem);
+        if (occ < 1) return SV_ERR_CUDA;
+        long long grid = (long long)di.sms * occ;
+        const long long maxu = (long long)B * pl.d_split;
+        if (grid > maxu) grid = maxu;
+        k_draw_sums<ES><<<(unsigned)grid, kThreads, smem, stream>>>(da);
+        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+        k_draw_finish<ES><<<B, kThreads, 0, stream>>>(da);
+        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    }
+    // 5. float-float tier
+    ExactArgs xa;
+    xa.tgt = acc.tgt;
+    xa.drf = acc.drf;
+    xa.K = acc.K;
+    xa.V = acc.V;
+    xa.temperature = acc.temperature;
+    xa.tokens = acc.tokens;
+    xa.uniforms = acc.uniforms;
+    xa.accept_len = acc.accept_len;
+    xa.out_tokens = acc.out_tokens;
+    xa.debug = acc.debug;
+    xa.sag_C = acc.sag_C;
+    xa.sag_on = acc.sag_on;
+    xa.nuc = nuc;
+    xa.top = top;
+    xa.rowstat = acc.rowstat;
+    xa.n_rows0 = pl.n_rows0;
+    xa.draws = acc.draws;
+    xa.items = acc.exact;
+    xa.counters = counters;
+    xa.xpart = reinterpret_cast<double *>(w + pl.off_xpart);
+    xa.xdraw = reinterpret_cast<ExactDraw *>(w + pl.off_xdraw);
+    xa.xsubs = reinterpret_cast<double *>(w + pl.off_xsubs);
+    xa.n_vec = pl.n_vec;
+    xa.n_sub = pl.n_sub;
+    xa.xsplit = kExactSplit;
+    xa.max_slots = 2 * acc.K + 1 > 2 ? 2 * acc.K + 1 : 2;
+    xa.stats = acc.stats;
+    xa.wait_limit = wait;
+    return launch_exact<ES>(xa, di, stream);
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" size_t sv_verify_workspace_size(int B, int K, int V) {
+    if (B < 1 || K < 0 || K > SV_MAX_K || V < 1) return 0;
+    const VerifyPlan a = plan_verify(B, K, V, 4), b = plan_verify(B, K, V, 2);
+    return a.bytes > b.bytes ? a.bytes : b.bytes;
+}
+
+extern "C" sv_status sv_verify(const void *target_logits, int64_t t_row_pitch, const void *draft_logits,
+                               int64_t d_row_pitch, int d_rows_per_seq, sv_dtype dtype, const int32_t *draft_tokens,
+                               const double *uniforms, int B, int K, int V, const float *temperature,
+                               const float *top_p, int saguaro_F, float saguaro_C, int32_t *accept_len,
+                               int32_t *out_tokens, double *debug, sv_stats *stats, void *workspace,
+                               size_t workspace_bytes, sv_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (B < 1 || K < 0 || K > SV_MAX_K || V < 1) return SV_ERR_INVALID_ARG;
+    if (!rows_ok(target_logits, t_row_pitch, V, dtype)) return SV_ERR_INVALID_ARG;
+    if (K > 0 && (!rows_ok(draft_logits, d_row_pitch, V, dtype) || d_rows_per_seq < K)) return SV_ERR_INVALID_ARG;
+    if ((K > 0 && draft_tokens == nullptr) || uniforms == nullptr || temperature == nullptr) return SV_ERR_INVALID_ARG;
+    if (accept_len == nullptr || out_tokens == nullptr) return SV_ERR_INVALID_ARG;
+    if (saguaro_F < 0 || !(saguaro_C >= 0.0f && saguaro_C <= 1.0f)) return SV_ERR_INVALID_ARG;
+    if ((long long)V * B * (2 * K + 1) > (1LL << 46)) return SV_ERR_INVALID_ARG;
+    const int es = elem_size(dtype);
+    const VerifyPlan pl = plan_verify(B, K, V, es);
+    if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < pl.bytes) return SV_ERR_WORKSPACE;
+    if (stats && cudaMemsetAsync(stats, 0, sizeof(sv_stats), stream) != cudaSuccess) return SV_ERR_CUDA;
+
+    AcceptArgs acc{};
+    acc.tgt = {static_cast<const char *>(target_logits), t_row_pitch * es, K + 1, K + 1, 0};
+    acc.drf = {static_cast<const char *>(K > 0 ? draft_logits : target_logits), (K > 0 ? d_row_pitch : t_row_pitch) * es,
+               K > 0 ? d_rows_per_seq : 1, K, 1};
+    acc.K = K;
+    acc.V = V;
+    acc.temperature = temperature;
+    acc.top_p = top_p;
+    acc.sag_on = (saguaro_F > 0 && saguaro_C != 1.0f) ? 1 : 0;
+    acc.sag_C = saguaro_C;
+    acc.tokens = draft_tokens;
+    acc.uniforms = uniforms;
+    acc.accept_len = accept_len;
+    acc.out_tokens = out_tokens;
+    acc.debug = debug;
+    acc.stats = stats;
+    if (es == 4) return launch_verify<4>(pl, acc, top_p, saguaro_F, saguaro_C, B, workspace, stream);
+    return launch_verify<2>(pl, acc, top_p, saguaro_F, saguaro_C, B, workspace, stream);
+}

@@ -1,0 +1,106 @@
+"""CPU checks of the C ABI: the library builds, loads and exports every declared entry point;
+host-only calls work; argument errors are returned before any device work."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_gb300 import build
+    build.build()
+    import speculative_decoding_verification_gb300 as sv
+    return sv.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "specverify.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = set(re.findall(r"\b(sv_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert "sv_verify" in names and "sv_fanout" in names and len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_binding_declares_every_symbol():
+    from speculative_decoding_verification_gb300 import _abi
+    assert sorted(_abi.SIGNATURES) == declared_symbols()
+
+
+def test_status_strings(lib):
+    import speculative_decoding_verification_gb300 as sv
+    assert sv.status_string(0) == "ok"
+    assert "timed out" in sv.status_string(4)
+
+
+@pytest.mark.parametrize("budget,a,r,K", [(64, 0.7, 1.0, 5), (23, 0.8, 1.0, 5), (100, 0.5, 2.0, 3), (7.5, 0.3, 0.0, 0),
+                                          (1000, 0.95, 0.25, 12)])
+def test_fanout_matches_oracle(lib, budget, a, r, K):
+    import speculative_decoding_verification_gb300 as sv
+    fr, fi = sv.sv_fanout(budget, a, r, K)
+    ofr, ofi = oracle.fanout(budget, a, r, K)
+    np.testing.assert_allclose(fr, ofr, rtol=1e-13)
+    assert list(fi) == list(ofi)
+
+
+def test_fanout_rejects_bad_arguments(lib):
+    fr = (ctypes.c_double * 8)()
+    fi = (ctypes.c_int32 * 8)()
+    p1, p2 = ctypes.cast(fr, ctypes.c_void_p), ctypes.cast(fi, ctypes.c_void_p)
+    assert lib.sv_fanout(64.0, 1.0, 1.0, 5, p1, p2) == 1
+    assert lib.sv_fanout(64.0, 0.5, -1.0, 5, p1, p2) == 1
+    assert lib.sv_fanout(-1.0, 0.5, 1.0, 5, p1, p2) == 1
+    assert lib.sv_fanout(64.0, 0.5, 1.0, 99, p1, p2) == 1
+    assert lib.sv_fanout(64.0, 0.5, 1.0, 5, None, p2) == 1
+
+
+def test_verify_rejects_bad_arguments_before_launch(lib):
+    """Argument errors come back synchronously; no device is touched (none exists here)."""
+    fake = 1 << 20   # a 16-byte aligned non-null address, never dereferenced
+    ws = lib.sv_verify_workspace_size(4, 3, 1000)
+    assert ws > 0 and lib.sv_verify_workspace_size(0, 3, 1000) == 0
+
+    def call(**kw):
+        args = dict(t=fake, tp=1024, d=fake, dp=1024, dr=3, dtype=1, tok=fake, u=fake, B=4, K=3, V=1000, T=fake,
+                    top_p=None, F=0, C=1.0, al=fake, ot=fake, dbg=None, st=None, ws=fake, wsb=ws)
+        kw = {**args, **kw}
+        return lib.sv_verify(kw["t"], kw["tp"], kw["d"], kw["dp"], kw["dr"], kw["dtype"], kw["tok"], kw["u"], kw["B"],
+                             kw["K"], kw["V"], kw["T"], kw["top_p"], kw["F"], kw["C"], kw["al"], kw["ot"], kw["dbg"],
+                             kw["st"], kw["ws"], kw["wsb"], None)
+    assert call(B=0) == 1
+    assert call(K=33) == 1
+    assert call(V=0) == 1
+    assert call(tp=999) == 1                     # pitch < V
+    assert call(tp=1001) == 1                    # row start not 16-byte aligned for bf16
+    assert call(t=fake + 2) == 1                 # misaligned base
+    assert call(t=None) == 1
+    assert call(tok=None) == 1
+    assert call(dr=2) == 1                       # fewer draft rows than K
+    assert call(dtype=7) == 1
+    assert call(C=1.5) == 1
+    assert call(F=-1) == 1
+    assert call(ws=None) == 5
+    assert call(wsb=255) == 5
+    assert call(ws=fake + 8) == 5                # workspace not 256-byte aligned
+
+
+def test_lookup_and_reuse_reject_bad_arguments(lib):
+    f = (ctypes.c_int32 * 3)(1, 2, 3)
+    fp = ctypes.cast(f, ctypes.c_void_p)
+    fake = 1 << 20
+    assert lib.sv_cache_lookup(fake, fake, fake, fp, 0, 2, fake, None) == 1
+    assert lib.sv_cache_lookup(fake, fake, fake, None, 4, 2, fake, None) == 1
+    assert lib.sv_mirror_reuse(fake, fake, fake, 4, 0, 7, fake, None) == 1
+    assert lib.sv_mirror_reuse(None, fake, fake, 4, 8, 7, fake, None) == 1

@@ -1,0 +1,201 @@
+"""GPU parity of sv_verify against the float64 oracle (called through the C ABI).
+
+Accept lengths and tokens must match exactly (the float32 tier certifies its decisions and
+hands the rest to the float-float tier); log-normalisers and probabilities within 1e-6.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_gb300 as sv
+from synth import workloads as W
+from tests.helpers import gpu_args, make_inputs, oracle_verify, to_f64
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-6
+
+
+def run_gpu(inp, w, top_p=False, F=None, C=None):
+    F = w.saguaro_F if F is None else F
+    C = w.saguaro_C if C is None else C
+    a = gpu_args(inp)
+    tp = torch.as_tensor(inp["top_p"], dtype=torch.float32, device="cuda") if top_p else None
+    al, ot, dbg, st = sv.sv_verify(inp["target"], inp["draft"], a["draft_tokens"], a["uniforms"], a["temperature"],
+                                   top_p=tp, saguaro_F=F, saguaro_C=C, debug=True)
+    torch.cuda.synchronize()
+    return al.cpu().numpy(), ot.cpu().numpy(), dbg.cpu().numpy(), sv.read_stats(st)
+
+
+def compare(w, inp, ref, al, ot, dbg, stats, seqs=None):
+    seqs = np.arange(w.B) if seqs is None else np.asarray(seqs)
+    assert stats["status"] == 0, stats
+    np.testing.assert_array_equal(al[seqs], ref["accept_len"])
+    np.testing.assert_array_equal(ot[seqs], ref["out_tokens"])
+    K = w.K
+    d = dbg[seqs]
+    greedy = inp["T"][seqs] == 0
+    s = ~greedy
+    np.testing.assert_allclose(d[s, :, 0], ref["lse_q"][s], atol=TOL, rtol=0)
+    np.testing.assert_allclose(d[s, :K, 1], ref["lse_p"][s], atol=TOL, rtol=0)
+    np.testing.assert_allclose(d[s, :K, 2], ref["q_s"][s], atol=TOL, rtol=0)
+    np.testing.assert_allclose(d[s, :K, 3], ref["p_s"][s], atol=TOL, rtol=0)
+    # ratio: compare where the reference is finite, relative (ratios are unbounded)
+    rr, gr = ref["ratio"][s], d[s, :K, 4]
+    fin = np.isfinite(rr) & (rr < 1e6)
+    np.testing.assert_allclose(gr[fin], rr[fin], rtol=1e-5, atol=TOL)
+    np.testing.assert_allclose(d[s, 0, 7], ref["residual_mass"][s], atol=TOL, rtol=0)
+
+
+def test_fast_exp2_error_bound():
+    """The float32 tier's certification assumes the SFU exp2 error stays below 2^-22 with a
+    2x margin; the float-float exponential must be near 2^-44."""
+    from speculative_decoding_verification_gb300 import _abi
+    out = sv.sv_selftest_exp2(-125.0, 1.0, 1 << 26).cpu().numpy()
+    assert out[0] < 2.0 ** -22, out
+    assert out[1] < 1e-13, out
+
+
+def test_bounded_wait_reports_timeout():
+    st = sv.sv_selftest_timeout(200_000)
+    torch.cuda.synchronize()
+    assert sv.read_stats(st)["status"] == sv._abi.SV_ERR_TIMEOUT
+
+
+@pytest.mark.parametrize("round_idx", [0, 1])
+def test_plain_config_parity(round_idx):
+    """B=1, K=4, V=32000 fp32: 128 rounds batched as 128 independent sequences."""
+    w = W.scaled(W.PLAIN, B=128)
+    inp = make_inputs(w, round_idx)
+    ref = oracle_verify(inp, w)
+    al, ot, dbg, st = run_gpu(inp, w)
+    compare(w, inp, ref, al, ot, dbg, st)
+    assert st["draws"] == 128 - st["reresolved"] + st["reresolved"]
+
+
+def test_large_batch_recipe_small_B():
+    """The B=512 recipe (bf16, V=128256, even rows greedy) at B=24."""
+    w = W.scaled(W.LARGE_BATCH, B=24)
+    inp = make_inputs(w, 0)
+    ref = oracle_verify(inp, w)
+    al, ot, dbg, st = run_gpu(inp, w)
+    compare(w, inp, ref, al, ot, dbg, st)
+
+
+def test_large_batch_full_size_sampled_sequences():
+    """Full B=512 launch; the oracle checks a sample of sequences (greedy and sampled)."""
+    w = W.LARGE_BATCH
+    inp = make_inputs(w, 0, chunk=64)
+    al, ot, dbg, st = run_gpu(inp, w)
+    seqs = np.array([0, 1, 2, 3, 100, 101, 255, 256, 257, 400, 401, 510, 511])
+    ref = oracle_verify(inp, w, seqs=seqs)
+    compare(w, inp, ref, al, ot, dbg, st, seqs=seqs)
+    assert st["rows"] == 512 * 6 + 256 * 5
+
+
+@pytest.mark.parametrize("V,dtype,pitch", [(1, torch.float32, 4), (8, torch.float32, 8), (31, torch.float32, 32),
+                                           (31, torch.bfloat16, 32), (1000, torch.bfloat16, 1000),
+                                           (4099, torch.bfloat16, 4104)])
+def test_ragged_vocabularies(V, dtype, pitch):
+    rng = np.random.default_rng(V)
+    B, K = 48, 3
+    w = W.Workload("ragged", B=B, K=K, V=V, dtype="f32" if dtype == torch.float32 else "bf16", temperature=1.0,
+                   top_p=1.0, rounds=1, seed=0, sigma=2.0, draft_scale=0.7, draft_sigma=1.0)
+    tg = torch.zeros((B, K + 1, pitch), dtype=dtype, device="cuda")
+    dr = torch.zeros((B, K, pitch), dtype=dtype, device="cuda")
+    tg[..., :V] = torch.as_tensor(rng.normal(0, 2, (B, K + 1, V)), dtype=dtype)
+    dr[..., :V] = 0.7 * tg[:, :K, :V] + torch.as_tensor(rng.normal(0, 1, (B, K, V)), dtype=dtype)
+    T = np.where(np.arange(B) % 3 == 0, 0.0, np.where(np.arange(B) % 3 == 1, 1.0, 0.7)).astype(np.float32)
+    u = rng.random((B, K + 1))
+    d64 = to_f64(dr[..., :V])
+    toks = oracle.draft_sample(d64, rng.random((B, K)), T, np.ones(B))["tokens"]
+    inp = dict(target=tg[..., :V], draft=dr[..., :V], tokens=toks, u=u, T=T, top_p=np.ones(B, np.float32))
+    ref = oracle.verify(to_f64(tg[..., :V]), d64, toks, u, T, np.ones(B))
+    al, ot, dbg, st = run_gpu(inp, w)
+    compare(w, inp, ref, al, ot, dbg, st)
+
+
+def test_identical_draft_accepts_all_and_k0():
+    rng = np.random.default_rng(7)
+    B, K, V = 32, 4, 2048
+    tg = torch.as_tensor(rng.normal(0, 2, (B, K + 1, V)), dtype=torch.float32, device="cuda")
+    u = rng.random((B, K + 1))
+    T = np.ones(B, np.float32)
+    toks = rng.integers(0, V, (B, K))
+    a = dict(draft_tokens=torch.as_tensor(toks, dtype=torch.int32, device="cuda"),
+             uniforms=torch.as_tensor(u, device="cuda"), temperature=torch.as_tensor(T, device="cuda"))
+    al, ot, _, st = sv.sv_verify(tg, tg[:, :K].clone(), a["draft_tokens"], a["uniforms"], a["temperature"])
+    ref = oracle.verify(to_f64(tg), to_f64(tg[:, :K]), toks, u, T, np.ones(B))
+    assert (al.cpu().numpy() == K).all()
+    np.testing.assert_array_equal(ot.cpu().numpy(), ref["out_tokens"])
+    # K = 0: the bonus token alone
+    al0, ot0, _, st0 = sv.sv_verify(tg[:, :1].contiguous(), None, None, a["uniforms"][:, :1].contiguous(),
+                                    a["temperature"])
+    ref0 = oracle.verify(to_f64(tg[:, :1]), np.zeros((B, 0, V)), np.zeros((B, 0), int), u[:, :1], T, np.ones(B))
+    np.testing.assert_array_equal(ot0.cpu().numpy(), ref0["out_tokens"])
+    assert sv.read_stats(st0)["status"] == 0
+
+
+def test_device_detected_errors():
+    rng = np.random.default_rng(1)
+    B, K, V = 6, 2, 256
+    tg = torch.as_tensor(rng.normal(0, 1, (B, K + 1, V)), dtype=torch.bfloat16, device="cuda")
+    dr = torch.as_tensor(rng.normal(0, 1, (B, K, V)), dtype=torch.bfloat16, device="cuda")
+    toks = torch.zeros((B, K), dtype=torch.int32, device="cuda")
+    u = torch.full((B, K + 1), 0.5, dtype=torch.float64, device="cuda")
+    T = torch.ones(B, device="cuda")
+    tg2 = tg.clone()
+    tg2[3, 1, 17] = float("nan")
+    _, _, _, st = sv.sv_verify(tg2, dr, toks, u, T)
+    s = sv.read_stats(st)
+    assert s["status"] == sv._abi.SV_ERR_NONFINITE and s["error_index"] == 3 * (K + 1) + 1
+    toks2 = toks.clone()
+    toks2[2, 0] = V
+    _, _, _, st = sv.sv_verify(tg, dr, toks2, u, T)
+    assert sv.read_stats(st)["status"] == sv._abi.SV_ERR_BAD_TOKEN
+    T2 = T.clone()
+    T2[4] = -1.0
+    _, _, _, st = sv.sv_verify(tg, dr, toks, u, T2)
+    assert sv.read_stats(st)["status"] == sv._abi.SV_ERR_INVALID_ARG
+    tg3 = tg.clone()
+    tg3[0, 0, :] = float("-inf")
+    _, _, _, st = sv.sv_verify(tg3, dr, toks, u, T)
+    assert sv.read_stats(st)["status"] == sv._abi.SV_ERR_NONFINITE
+
+
+@pytest.mark.parametrize("K", [1, 3])
+def test_chi_square_committed_tokens_V8_gpu(K):
+    """10^6 sequences on V=8 through the library: committed tokens follow q at every position
+    and accept lengths follow the product law (chi-square, p > 0.01)."""
+    import scipy.stats
+    from synth import philox
+    rng = np.random.default_rng(100 + K)
+    V, n = 8, 1_000_000
+    row_t = rng.normal(0, 1.5, size=(K + 1, V))
+    row_d = 0.6 * row_t[:K] + rng.normal(0, 1.0, size=(K, V))
+    q = np.exp(row_t - row_t.max(1, keepdims=True)); q /= q.sum(1, keepdims=True)
+    p = np.exp(row_d - row_d.max(1, keepdims=True)); p /= p.sum(1, keepdims=True)
+    tg32 = torch.as_tensor(row_t, dtype=torch.float32)
+    dr32 = torch.as_tensor(row_d, dtype=torch.float32)
+    # draft tokens: inverse CDF of p (float64 of the float32 rows) at Philox uniforms
+    pd = np.exp(to_f64(dr32) - to_f64(dr32).max(1, keepdims=True)); pd /= pd.sum(1, keepdims=True)
+    u_d = philox.uniforms(21, philox.STREAM_DRAFT, 0, n, K)
+    toks = np.stack([np.searchsorted(np.cumsum(pd[j]), u_d[:, j] * pd[j].sum(), side="right") for j in range(K)], 1)
+    toks = np.minimum(toks, V - 1)
+    u = np.concatenate([philox.uniforms(21, philox.STREAM_ACCEPT, 0, n, K),
+                        philox.uniforms(21, philox.STREAM_RESIDUAL, 0, n, 1)], axis=1)
+    tg = tg32.to("cuda").expand(n, K + 1, V).contiguous()
+    dr = dr32.to("cuda").expand(n, K, V).contiguous()
+    al, ot, _, st = sv.sv_verify(tg, dr, torch.as_tensor(toks, dtype=torch.int32, device="cuda"),
+                                 torch.as_tensor(u, device="cuda"), torch.ones(n, device="cuda"))
+    al = al.cpu().numpy()
+    ot = ot.cpu().numpy()
+    assert sv.read_stats(st)["status"] == 0
+    qf = np.exp(to_f64(tg32) - to_f64(tg32).max(1, keepdims=True)); qf /= qf.sum(1, keepdims=True)
+    for i in range(K + 1):
+        present = al >= i
+        cnt = np.bincount(ot[present, i], minlength=V)
+        assert scipy.stats.chisquare(cnt, cnt.sum() * qf[i]).pvalue > 0.01
+    a = np.minimum(pd, qf[:K]).sum(axis=1)
+    want = np.array([np.prod(a[:j]) * (1 - a[j]) for j in range(K)] + [np.prod(a)])
+    assert scipy.stats.chisquare(np.bincount(al, minlength=K + 1), n * want).pvalue > 0.01

@@ -225,7 +225,7 @@ sv_status sv_cache_lookup(const int32_t *accept_len, const int32_t *out_tokens,
  *  logits       dev, n_rows rows with pitch row_pitch.
  *  temperature  dev float [n_rows] (> 0) or NULL for T = 1.
  *  ids          dev int32 [n_rows][kappa]; logprobs dev float64 [n_rows][kappa] (may be NULL).
- * Requires 1 <= kappa <= min(V, 64).
+ * Requires 1 <= kappa <= min(V, 1024).  A row with T outside [1e-3, 1e3] is reported in stats.
  * -------------------------------------------------------------------------------------- */
 size_t sv_topk_rows_workspace_size(int n_rows, int V);
 

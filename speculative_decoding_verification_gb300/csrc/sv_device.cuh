@@ -209,6 +209,17 @@ __device__ __forceinline__ ff ff_exp2(float yh, float yl, const float2 *tab) {
     return {__fmul_rn(e.hi, sc), __fmul_rn(e.lo, sc)};
 }
 
+// c = log2(e) / T as a float-float pair using float32 operations only (the FP64 pipe is far
+// slower than FP32 on this GPU).  The remainder of a correctly rounded quotient is exact, so
+// c_hi + c_lo carries about 46 significant bits.
+__device__ __forceinline__ void log2e_over(float T, float &c_hi, float &c_lo) {
+    const float L2E_HI = 1.44269502162933349609375f;
+    const float L2E_LO = 1.925963033500011e-08f;
+    c_hi = __fdiv_rn(L2E_HI, T);
+    const float rem = __fadd_rn(__fmaf_rn(-c_hi, T, L2E_HI), L2E_LO);
+    c_lo = __fdiv_rn(rem, T);
+}
+
 // x * c - g as float-float, with c = c.hi + c.lo and g = g.hi + g.lo float-float constants.
 // x * c.hi is exact through an FMA; the remaining terms are small.
 __device__ __forceinline__ ff ff_affine(float x, ff c, ff g) {

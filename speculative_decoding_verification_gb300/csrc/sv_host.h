@@ -52,7 +52,8 @@ struct VerifyPlan {
     // workspace offsets
     size_t off_part = 0, off_rowstat = 0, off_draws = 0, off_subs = 0, off_exact = 0, off_counters = 0;
     size_t off_nuc = 0, off_top = 0;
-    size_t off_xpart = 0, off_xdraw = 0, off_xsubs = 0;
+    size_t off_xpart = 0, off_xdraw = 0, off_xsubs = 0, off_xnorm = 0, off_xunc_n = 0, off_xunc = 0;
+    int x_split = 1;                       // chunks per row in the float-float pass
     size_t bytes = 0;
 };
 

@@ -38,14 +38,15 @@ struct RowSet {
     int skip_greedy;      // 1: rows of greedy sequences are not streamed
 };
 
-// Per-(row, chunk, warp) partial of the statistics pass.
+// Per-(row, chunk, warp) partial of the statistics pass (float32 only: no FP64 on the hot path).
 struct WarpPartial {
-    double s;       // sum of 2^(x c - r) over the warp's elements
-    double a;       // sum of 2^(x c - r) * |x c - r| (feeds the certified error bound)
-    int r;          // integer reference exponent, >= x*c of every element seen; -2^30 if none
-    float maxv;     // largest logit seen (NaN-free)
-    int argmax;     // its lowest index
-    int flags;      // kFlagNaN | kFlagPosInf
+    float s_hi, s_lo;   // sum of 2^(x c - r) over the warp's elements, float-float
+    float a;            // sum of 2^(x c - r) * |x c - r| (feeds the certified error bound)
+    int r;              // integer reference exponent, >= x*c of every element seen; -2^30 if none
+    float maxv;         // largest logit seen (NaN-free)
+    int argmax;         // its lowest index
+    int flags;          // kFlagNaN | kFlagPosInf
+    int pad;
 };
 
 constexpr int kFlagNaN = 1;
@@ -80,6 +81,7 @@ struct TopSet {
     int top_id;
     double p_d;     // probability mass of D (after temperature and top-p) before scaling
     double z;       // normaliser after scaling: 1 - (1 - C) p_d
+    double z_err;   // relative error bound of z (float32 tier)
 };
 
 // A row as seen by the draw pass: weight(v) = keep(v) * 2^(x_v c - r) * inv_s * (in_D ? sc_d : 1).

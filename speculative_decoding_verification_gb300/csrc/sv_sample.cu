@@ -50,38 +50,7 @@ __global__ void __launch_bounds__(kThreads) k_sample_items(const SampleArgs a, l
         return;
     }
     // combine partials (same arithmetic as the verify path)
-    const WarpPartial *P = a.part + (size_t)r * a.n_split * kWarps;
-    const int np = a.n_split * kWarps;
-    int rmax = kNoRef;
-    for (int p = lane; p < np; p += 32) rmax = max(rmax, P[p].r);
-    rmax = warp_max_i(rmax);
-    double s = 0.0, ae = 0.0;
-    float m = -INFINITY;
-    int am = 0x7FFFFFFF, fl = 0;
-    for (int p = lane; p < np; p += 32) {
-        const WarpPartial w = P[p];
-        fl |= w.flags;
-        if (w.maxv > m || (w.maxv == m && w.argmax < am)) {
-            m = w.maxv;
-            am = w.argmax;
-        }
-        const int d = rmax - w.r;
-        if (!greedy && d < 1000) {
-            const double sc = ldexp(1.0, -d);
-            s += w.s * sc;
-            ae += (w.a + (double)d * w.s) * sc;
-        }
-    }
-    RowStat rs;
-    rs.S = warp_sum_d(s);
-    const double A = warp_sum_d(ae);
-    rs.flags = warp_or_i(fl);
-    warp_argmax(m, am);
-    rs.maxv = m;
-    rs.argmax = am;
-    rs.r = rmax;
-    rs.g = greedy ? NAN : (double)rmax + log2(rs.S);
-    rs.err = greedy ? 0.0 : kEx2RelErr + 1.01 * kYRound * (rs.S > 0.0 ? A / rs.S : 0.0) + 6.0 * kU32 + 1e-12;
+    const RowStat rs = combine_row(a.part + (size_t)r * a.n_split * kWarps, a.n_split * kWarps, greedy);
     if (lane != 0) return;
     a.rowstat[r] = rs;
     const bool bad = rs.flags != 0 || (greedy ? !isfinite(rs.maxv) : (!(rs.S > 0.0) || !isfinite(rs.g)));
@@ -102,15 +71,13 @@ __global__ void __launch_bounds__(kThreads) k_sample_items(const SampleArgs a, l
         a.tokens[r] = rs.argmax;
         return;
     }
-    const double c = 1.4426950408889634074 / (double)T;
     const char *row = a.rows.base + (b * a.rows.rows_per_seq + j) * a.rows.pitch_bytes;
     DrawItem it;
     // the sampled row carries both the nucleus cut and the top-F scaling
     {
         DrawRow &d = it.q;
         d.row = row;
-        d.c_hi = (float)c;
-        d.c_lo = (float)(c - (double)d.c_hi);
+        log2e_over(T, d.c_hi, d.c_lo);
         d.rf = (float)rs.r;
         double norm = rs.S, err = rs.err;
         d.cut_x = -INFINITY;
@@ -129,7 +96,7 @@ __global__ void __launch_bounds__(kThreads) k_sample_items(const SampleArgs a, l
             d.top_id = a.top[r].top_id;
             d.sc_d = a.C;
             norm *= a.top[r].z;
-            err += 2.0 * rs.err + 1e-12;
+            err += a.top[r].z_err;
         }
         d.inv_s = (float)(1.0 / norm);
         d.pad = 0;
@@ -186,7 +153,11 @@ static SamplePlan plan_sample(int B, int n_rows, int V, int es) {
     p.off_exact = cv.take<ExactItem>(capx);
     p.off_xpart = cv.take<double>(capx * 2 * kExactSplit * 3);
     p.off_xdraw = cv.take<ExactDraw>(capx);
-    p.off_xsubs = cv.take<double>(capx * p.n_sub);
+    p.x_split = n_vsub > 64 ? 64 : (n_vsub > 0 ? n_vsub : 1);
+    p.off_xsubs = cv.take<float4>(capx * p.n_sub);
+    p.off_xnorm = cv.take<float4>(capx * p.x_split * kWarps);
+    p.off_xunc_n = cv.take<int>(capx);
+    p.off_xunc = cv.take<int>(capx * kExactUncCap);
     p.bytes = cv.off + 256;
     sp.bytes = p.bytes;
     return sp;
@@ -291,10 +262,13 @@ static sv_status launch_sample(const SamplePlan &sp, const SampleArgs &in, const
     xa.counters = counters;
     xa.xpart = reinterpret_cast<double *>(w + pl.off_xpart);
     xa.xdraw = reinterpret_cast<ExactDraw *>(w + pl.off_xdraw);
-    xa.xsubs = reinterpret_cast<double *>(w + pl.off_xsubs);
+    xa.xsubs = reinterpret_cast<float4 *>(w + pl.off_xsubs);
+    xa.xnorm = reinterpret_cast<float4 *>(w + pl.off_xnorm);
+    xa.xunc_n = reinterpret_cast<int *>(w + pl.off_xunc_n);
+    xa.xunc = reinterpret_cast<int *>(w + pl.off_xunc);
     xa.n_vec = pl.n_vec;
     xa.n_sub = pl.n_sub;
-    xa.xsplit = kExactSplit;
+    xa.xsplit = pl.x_split;
     xa.max_slots = 2;
     xa.stats = a.stats;
     xa.wait_limit = kWaitLimitCycles;

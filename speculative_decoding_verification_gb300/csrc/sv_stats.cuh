@@ -56,9 +56,11 @@ __device__ __forceinline__ UnitInfo stats_unit(const StatsArgs &a, long long u) 
     ui.greedy = (T == 0.0f);
     ui.needed = !(rs.skip_greedy && ui.greedy);
     ui.row = rs.base + (b * rs.rows_per_seq + j) * rs.pitch_bytes;
-    const double c = 1.4426950408889634074 / (double)T;
-    ui.c_hi = (float)c;
-    ui.c_lo = (float)(c - (double)ui.c_hi);
+    if (ui.greedy) {
+        ui.c_hi = ui.c_lo = 0.0f;
+    } else {
+        log2e_over(T, ui.c_hi, ui.c_lo);
+    }
     constexpr int EPV = 16 / ES;
     const int n_vec = (a.V * ES) / 16;
     ui.v0 = min(ui.chunk * a.chunk_vecs, n_vec);
@@ -212,31 +214,31 @@ __device__ __forceinline__ void acc_vector(StatAcc &A, uint4 w, int e0, bool gre
     }
 }
 
-// Warp-combine and store this unit's partial.
+// Warp-combine and store this unit's partial (float32 / float-float arithmetic only).
 __device__ __forceinline__ void acc_store(const StatAcc &A0, bool greedy, WarpPartial *dst) {
     StatAcc A = A0;
     const int lane = threadIdx.x & 31;
     WarpPartial p;
     p.flags = warp_or_i(A.flags);
+    p.pad = 0;
     if (greedy) {
         warp_argmax(A.m, A.am);
-        p.s = 0.0;
-        p.a = 0.0;
+        p.s_hi = p.s_lo = p.a = 0.0f;
         p.r = kNoRef;
         p.maxv = A.m;
         p.argmax = A.am;
     } else {
         const int rw = warp_max_i(A.r);
-        const int d = rw - A.r;   // >= 0
-        const double tot = (double)A.s + (double)A.comp;
-        double sd = 0.0, ad = 0.0;
-        if (d < 1000) {
-            const double sc = ldexp(1.0, -d);
-            sd = tot * sc;
-            ad = ((double)A.aerr + (double)d * tot) * sc;
-        }
-        p.s = warp_sum_d(sd);
-        p.a = warp_sum_d(ad);
+        const int d = rw - A.r;   // >= 0; scaling by 2^-d is exact
+        const float sc = pow2i(-d);
+        ff v = fast_two_sum(A.s, A.comp);
+        v.hi *= sc;
+        v.lo *= sc;
+        const float a = (A.aerr + (float)min(d, 1 << 20) * (A.s + A.comp)) * sc;
+        v = warp_sum_ff(v);
+        p.s_hi = v.hi;
+        p.s_lo = v.lo;
+        p.a = warp_sum_f(a);
         p.r = rw;
         p.maxv = -INFINITY;
         p.argmax = 0x7FFFFFFF;
@@ -334,6 +336,53 @@ __global__ void __launch_bounds__(kThreads, 2) k_stats(const StatsArgs a) {
         }
         acc_store(A, ui.greedy, a.part + ((size_t)ui.rid * a.n_split + ui.chunk) * kWarps + warp);
     }
+}
+
+// Combine a row's warp partials (one warp).  Float-float accumulation; the few float64
+// operations happen once per row.
+__device__ __forceinline__ RowStat combine_row(const WarpPartial *P, int np, bool greedy) {
+    const int lane = threadIdx.x & 31;
+    int rmax = kNoRef;
+    for (int p = lane; p < np; p += 32) rmax = max(rmax, P[p].r);
+    rmax = warp_max_i(rmax);
+    ff s = {0.f, 0.f};
+    float a = 0.f;
+    float m = -INFINITY;
+    int am = 0x7FFFFFFF, fl = 0;
+    for (int p = lane; p < np; p += 32) {
+        const WarpPartial w = P[p];
+        fl |= w.flags;
+        if (greedy) {
+            if (w.maxv > m || (w.maxv == m && w.argmax < am)) {
+                m = w.maxv;
+                am = w.argmax;
+            }
+        } else {
+            const int d = rmax - w.r;
+            const float sc = pow2i(-d);
+            s = ff_add(s, {w.s_hi * sc, w.s_lo * sc});
+            a += (w.a + (float)min(d, 1 << 20) * (w.s_hi + w.s_lo)) * sc;
+        }
+    }
+    s = warp_sum_ff(s);
+    a = warp_sum_f(a);
+    RowStat r;
+    r.flags = warp_or_i(fl);
+    warp_argmax(m, am);
+    r.maxv = m;
+    r.argmax = am;
+    r.r = rmax;
+    if (greedy) {
+        r.S = 0.0;
+        r.g = NAN;
+        r.err = 0.0;
+    } else if (lane == 0) {
+        r.S = (double)s.hi + (double)s.lo;
+        r.g = (double)rmax + log2(r.S);
+        // ex2 error + exponent rounding (|y| weighted) + float32 summation (tree + compensated)
+        r.err = kEx2RelErr + 1.02 * kYRound * (s.hi > 0.f ? (double)(a / s.hi) : 0.0) + 6.0 * kU32 + 1e-12;
+    }
+    return r;   // S, g, err valid in lane 0 (sampled rows)
 }
 
 }  // namespace sv

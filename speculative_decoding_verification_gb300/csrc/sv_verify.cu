@@ -47,57 +47,11 @@ struct AcceptArgs {
     Counters *counters;
 };
 
-// Combine a row's warp partials (one warp).
-__device__ __forceinline__ RowStat combine_row(const WarpPartial *P, int np, bool greedy) {
-    const int lane = threadIdx.x & 31;
-    int rmax = kNoRef;
-    for (int p = lane; p < np; p += 32) rmax = max(rmax, P[p].r);
-    rmax = warp_max_i(rmax);
-    double s = 0.0, a = 0.0;
-    float m = -INFINITY;
-    int am = 0x7FFFFFFF, fl = 0;
-    for (int p = lane; p < np; p += 32) {
-        const WarpPartial w = P[p];
-        fl |= w.flags;
-        if (greedy) {
-            if (w.maxv > m || (w.maxv == m && w.argmax < am)) {
-                m = w.maxv;
-                am = w.argmax;
-            }
-        } else {
-            const int d = rmax - w.r;
-            if (d < 1000) {
-                const double sc = ldexp(1.0, -d);
-                s += w.s * sc;
-                a += (w.a + (double)d * w.s) * sc;
-            }
-        }
-    }
-    RowStat r;
-    r.S = warp_sum_d(s);
-    const double A = warp_sum_d(a);
-    r.flags = warp_or_i(fl);
-    warp_argmax(m, am);
-    r.maxv = m;
-    r.argmax = am;
-    r.r = rmax;
-    if (greedy) {
-        r.g = NAN;
-        r.err = 0.0;
-    } else {
-        r.g = (double)rmax + log2(r.S);
-        // ex2 error + exponent rounding (|y| weighted) + float32 summation (tree + compensated)
-        r.err = kEx2RelErr + 1.01 * kYRound * (r.S > 0.0 ? A / r.S : 0.0) + 6.0 * kU32 + 1e-12;
-    }
-    return r;
-}
-
-__device__ __forceinline__ DrawRow draw_row(const char *row, double c, const RowStat &rs, const NucleusCut *nc,
+__device__ __forceinline__ DrawRow draw_row(const char *row, float T, const RowStat &rs, const NucleusCut *nc,
                                             const TopSet *ts, float sag_C) {
     DrawRow d;
     d.row = row;
-    d.c_hi = (float)c;
-    d.c_lo = (float)(c - (double)d.c_hi);
+    log2e_over(T, d.c_hi, d.c_lo);
     d.rf = (float)rs.r;
     double norm = rs.S;
     double err = rs.err;
@@ -117,7 +71,7 @@ __device__ __forceinline__ DrawRow draw_row(const char *row, double c, const Row
         d.top_id = ts->top_id;
         d.sc_d = sag_C;
         norm *= ts->z;
-        err += 2.0 * rs.err + 1e-12;
+        err += ts->z_err;
     }
     d.inv_s = (float)(1.0 / norm);
     d.pad = 0;
@@ -203,7 +157,7 @@ __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
                     const TopSet t = a.top[rid_d];
                     if (xd > t.top_x || (xd == t.top_x && s <= t.top_id)) lp += sag_l2c;
                     lp -= log2(t.z);
-                    delta += 2.0 * rp.err;
+                    delta += t.z_err;
                 }
                 if (lp == -INFINITY) ratio = (lq == -INFINITY) ? 0.0 : INFINITY;
                 else ratio = exp2(lq - lp);
@@ -272,12 +226,12 @@ __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
     DrawItem it;
     const long long rid_q = (long long)b * n_t + k;
     const char *qrow = a.tgt.base + ((long long)b * a.tgt.rows_per_seq + k) * a.tgt.pitch_bytes;
-    it.q = draw_row(qrow, c, rs[k], a.nuc ? a.nuc + rid_q : nullptr, nullptr, 1.0f);
+    it.q = draw_row(qrow, T, rs[k], a.nuc ? a.nuc + rid_q : nullptr, nullptr, 1.0f);
     it.has_p = k < K;
     if (it.has_p) {
         const long long rid_p = a.n_rows0 + (long long)b * K + k;
         const char *prow = a.drf.base + ((long long)b * a.drf.rows_per_seq + k) * a.drf.pitch_bytes;
-        it.p = draw_row(prow, c, rs[n_t + k], a.nuc ? a.nuc + rid_p : nullptr,
+        it.p = draw_row(prow, T, rs[n_t + k], a.nuc ? a.nuc + rid_p : nullptr,
                         (a.sag_on && a.top) ? a.top + rid_p : nullptr, a.sag_C);
     } else {
         it.p = {};
@@ -327,7 +281,11 @@ VerifyPlan plan_verify(int B, int K, int V, int es) {
     const int max_slots = 2 * K + 1 > 2 ? 2 * K + 1 : 2;
     p.off_xpart = cv.take<double>(cap * max_slots * kExactSplit * 3);
     p.off_xdraw = cv.take<ExactDraw>(cap);
-    p.off_xsubs = cv.take<double>(cap * p.n_sub);
+    p.x_split = n_vsub > 64 ? 64 : (n_vsub > 0 ? n_vsub : 1);
+    p.off_xsubs = cv.take<float4>(cap * p.n_sub);
+    p.off_xnorm = cv.take<float4>(cap * p.x_split * kWarps);
+    p.off_xunc_n = cv.take<int>(cap);
+    p.off_xunc = cv.take<int>(cap * kExactUncCap);
     p.bytes = cv.off + 256;
     return p;
 }
@@ -446,10 +404,13 @@ static sv_status launch_verify(const VerifyPlan &pl, const AcceptArgs &acc_in, c
     xa.counters = counters;
     xa.xpart = reinterpret_cast<double *>(w + pl.off_xpart);
     xa.xdraw = reinterpret_cast<ExactDraw *>(w + pl.off_xdraw);
-    xa.xsubs = reinterpret_cast<double *>(w + pl.off_xsubs);
+    xa.xsubs = reinterpret_cast<float4 *>(w + pl.off_xsubs);
+    xa.xnorm = reinterpret_cast<float4 *>(w + pl.off_xnorm);
+    xa.xunc_n = reinterpret_cast<int *>(w + pl.off_xunc_n);
+    xa.xunc = reinterpret_cast<int *>(w + pl.off_xunc);
     xa.n_vec = pl.n_vec;
     xa.n_sub = pl.n_sub;
-    xa.xsplit = kExactSplit;
+    xa.xsplit = pl.x_split;
     xa.max_slots = 2 * acc.K + 1 > 2 ? 2 * acc.K + 1 : 2;
     xa.stats = acc.stats;
     xa.wait_limit = wait;

@@ -107,6 +107,18 @@ __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
     return d;
 }
 
+// Unpack one 16-byte vector of ES-byte elements.
+template <int ES>
+__device__ __forceinline__ void unpack(uint4 w, float (&x)[16 / ES]) {
+    if constexpr (ES == 2) {
+        x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+        x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+    } else {
+        x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+        x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+    }
+}
+
 template <int ES>
 __device__ __forceinline__ float load_elem(const char *row, int64_t v) {
     if (ES == 4) return __ldg(reinterpret_cast<const float *>(row) + v);

@@ -62,18 +62,6 @@ __device__ __forceinline__ void draw_weight(const DrawItem &it, float xq, float 
     }
 }
 
-// Unpack one 16-byte vector of ES-byte elements.
-template <int ES>
-__device__ __forceinline__ void unpack(uint4 w, float (&x)[16 / ES]) {
-    if constexpr (ES == 2) {
-        x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
-        x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
-    } else {
-        x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
-        x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
-    }
-}
-
 // Weights of one vector (EPV tokens from element e0); returns the tree sum, fills aq/ap sums.
 template <int ES, bool HAS_P, bool FILT>
 __device__ __forceinline__ float vec_weights(const DrawItem &it, uint4 wq, uint4 wp, int e0, float (&wv)[16 / ES],

@@ -96,6 +96,19 @@ __device__ __forceinline__ void pick_digit(const T *h, T need, int &digit, T &ab
     above = __shfl_sync(0xFFFFFFFFu, acc, L);
 }
 
+// After the 8-bit passes over the top 16 bits, a bf16 key is complete except for its low 16
+// bits, which are 0 for positive values and all ones for negative ones (the key of a negative
+// float is its complement).
+template <int ES>
+__device__ __forceinline__ uint32_t complete_key(uint32_t prefix) {
+    if (ES == 2 && !(prefix & 0x80000000u)) prefix |= 0xFFFFu;
+    return prefix;
+}
+
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return (k & 0x80000000u) ? __uint_as_float(k & 0x7FFFFFFFu) : __uint_as_float(~k);
+}
+
 // Count-weighted radix select: the key K* of the N-th largest element (1 <= N <= V) and the
 // number of elements strictly above it.
 template <int ES>
@@ -128,7 +141,7 @@ __device__ uint32_t radix_select_count(const char *row, int V, int N, int &n_abo
         __syncthreads();
     }
     n_above = N - need;
-    return prefix;
+    return complete_key<ES>(prefix);
 }
 
 // Ids of the first `want` elements with key == kstar, in increasing id order.  Writes them to
@@ -272,57 +285,17 @@ __device__ __forceinline__ double exact_mass(float x, ff c, float rf, const floa
     return ff_to_double(ff_exp2(y.hi, y.lo, tab));
 }
 
-template <int ES>
-__global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
-    __shared__ double hm[256];
-    __shared__ unsigned hc[256];
-    __shared__ int s_dig[2], s_warp[kWarps], s_last;
-    __shared__ double s_dm[2];
-    __shared__ double s_red[kWarps];
-    __shared__ float2 tab[256];
-    const long long rid = blockIdx.x;
-    if (rid >= a.n_rows) return;
-    const int s = rid < a.n_rows0 ? 0 : 1;
-    const long long lr = s == 0 ? rid : rid - a.n_rows0;
-    const RowSet &rs = a.set[s];
-    const long long b = lr / rs.rows_used, j = lr - b * rs.rows_used;
-    const float T = a.temperature[b];
-    const float tp = a.top_p[b];
-    NucleusCut none;
-    none.cut_x = -INFINITY;
-    none.cut_id = 0x7FFFFFFF;
-    none.mass = 1.0;
-    none.log2_mass = 0.0;
-    none.ambiguous = 0;
-    none.pad = 0;
-    const bool active = T > 0.0f && tp < 1.0f && (rs.skip_greedy == 0 || T != 0.0f);
-    if (!active || !(T >= 1e-3f && T <= 1e3f)) {
-        if (threadIdx.x == 0) a.nuc[rid] = none;
-        return;
-    }
-    const char *row = rs.base + (b * rs.rows_per_seq + j) * rs.pitch_bytes;
-    // row statistics from the statistics pass
-    __shared__ RowStat s_rs;
-    if (threadIdx.x < 32) {
-        const RowStat st = combine_row(a.part + (size_t)rid * a.n_split * kWarps, a.n_split * kWarps, false);
-        if (threadIdx.x == 0) s_rs = st;
-    }
-    __syncthreads();
-    const RowStat st = s_rs;
-    if (!(st.S > 0.0) || st.flags) {   // reported by the accept / sampling kernels
-        if (threadIdx.x == 0) a.nuc[rid] = none;
-        return;
-    }
-    float c_hi, c_lo;
-    log2e_over(T, c_hi, c_lo);
-    const double c = (double)c_hi + (double)c_lo;
-    const float rf = (float)st.r;
-    const double target = (double)tp * st.S;
-    auto mass = [&](float x) { return ex2_fast(fmaf(x, c_lo, fmaf(x, c_hi, -rf))); };
-
-    // ---- float32 tier: mass-weighted radix select ----
+// Mass-weighted radix select: the key K* at which the running mass from the top, in
+// (value desc) order, first reaches `target`; the mass strictly above K*, and the count of
+// elements at K*.  mass(x) gives each element's weight; the histogram bins accumulate in
+// float64.  When `total` is non-null the first pass also sums every element's mass into it
+// (and `target_frac` then scales that total into the target).
+template <int ES, class Mass>
+__device__ uint32_t radix_select_mass(const char *row, int V, double target_in, double target_frac, Mass mass,
+                                      double *hm, unsigned *hc, int *s_dig, double *s_dm, double *s_red,
+                                      double &above_out, int &cnt_out, double *total, double *aux_total) {
     uint32_t prefix = 0, mask = 0;
-    double above_m = 0.0;
+    double above_m = 0.0, target = target_in;
     int cnt_star = 0;
     constexpr int passes = ES == 2 ? 2 : 4;
     for (int p = 0; p < passes; ++p) {
@@ -332,15 +305,39 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
             hc[i] = 0;
         }
         __syncthreads();
-        for_each_elem<ES>(row, a.V, [&](float x, int) {
+        double tsum = 0.0, asum = 0.0;
+        for_each_elem<ES>(row, V, [&](float x, int) {
             const uint32_t k = f32_key(x);
             if ((k & mask) == prefix) {
+                const double2 m = mass(x);   // (mass, auxiliary error weight)
                 const unsigned bin = (k >> shift) & 255u;
-                atomicAdd(&hm[bin], (double)mass(x));
+                atomicAdd(&hm[bin], m.x);
                 atomicAdd(&hc[bin], 1u);
+                if (p == 0) {
+                    tsum += m.x;
+                    asum += m.y;
+                }
             }
         });
+        if (p == 0 && total) {
+            tsum = warp_sum_d(tsum);
+            asum = warp_sum_d(asum);
+            if ((threadIdx.x & 31) == 0) {
+                s_red[threadIdx.x >> 5] = tsum;
+                hm[256 + (threadIdx.x >> 5)] = asum;
+            }
+        }
         __syncthreads();
+        if (p == 0 && total) {
+            double t = 0.0, at = 0.0;
+            for (int w = 0; w < kWarps; ++w) {
+                t += s_red[w];
+                at += hm[256 + w];
+            }
+            *total = t;
+            if (aux_total) *aux_total = at;
+            target = target_frac * t;
+        }
         if (threadIdx.x < 32) {
             int d;
             double above;
@@ -370,26 +367,84 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
         cnt_star = s_dig[1];
         __syncthreads();
     }
-    const uint32_t kstar = prefix;
-    const float xstar = (kstar & 0x80000000u) ? __uint_as_float(kstar & 0x7FFFFFFFu) : __uint_as_float(~kstar);
-    const double estar = (double)mass(xstar);
+    above_out = above_m;
+    cnt_out = cnt_star;
+    return complete_key<ES>(prefix);
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
+    __shared__ double hm[256 + kWarps];
+    __shared__ unsigned hc[256];
+    __shared__ int s_dig[2], s_warp[kWarps], s_last;
+    __shared__ double s_dm[2];
+    __shared__ double s_red[kWarps];
+    __shared__ float2 tab[256];
+    __shared__ RowStat s_rs;
+    const long long rid = blockIdx.x;
+    if (rid >= a.n_rows) return;
+    const int s = rid < a.n_rows0 ? 0 : 1;
+    const long long lr = s == 0 ? rid : rid - a.n_rows0;
+    const RowSet &rs = a.set[s];
+    const long long b = lr / rs.rows_used, j = lr - b * rs.rows_used;
+    const float T = a.temperature[b];
+    const float tp = a.top_p[b];
+    NucleusCut none;
+    none.cut_x = -INFINITY;
+    none.cut_id = 0x7FFFFFFF;
+    none.mass = 1.0;
+    none.log2_mass = 0.0;
+    none.ambiguous = 0;
+    none.pad = 0;
+    if (!(tp < 1.0f) || !(T >= 1e-3f && T <= 1e3f)) {   // off, greedy or invalid temperature
+        if (threadIdx.x == 0) a.nuc[rid] = none;
+        return;
+    }
+    const char *row = rs.base + (b * rs.rows_per_seq + j) * rs.pitch_bytes;
+    if (threadIdx.x < 32) {
+        const RowStat st = combine_row(a.part + (size_t)rid * a.n_split * kWarps, a.n_split * kWarps, false);
+        if (threadIdx.x == 0) s_rs = st;
+    }
+    __syncthreads();
+    const RowStat st = s_rs;
+    if (!(st.S > 0.0) || st.flags) {   // reported by the accept / sampling kernels
+        if (threadIdx.x == 0) a.nuc[rid] = none;
+        return;
+    }
+    float c_hi, c_lo;
+    log2e_over(T, c_hi, c_lo);
+    const float rf = (float)st.r;
+
+    // ---- float32 tier: masses 2^(x c - r) as in the statistics pass ----
+    auto fast_mass = [&](float x) {   // (mass, mass * |y|): the second feeds the error bound
+        const float y = fmaf(x, c_lo, fmaf(x, c_hi, -rf));
+        const float e = ex2_fast(y);
+        return make_double2((double)e, (double)(e * fabsf(y)));
+    };
+    double above_m, S_fast, A_row;
+    int cnt_star;
+    const uint32_t kstar = radix_select_mass<ES>(row, a.V, 0.0, (double)tp, fast_mass, hm, hc, s_dig, s_dm, s_red,
+                                                 above_m, cnt_star, &S_fast, &A_row);
+    const double target = (double)tp * S_fast;
+    const float xstar = key_value(kstar);
+    const double estar = (double)ex2_fast(fmaf(xstar, c_lo, fmaf(xstar, c_hi, -rf)));
     int jt = (int)ceil((target - above_m) / estar);
     jt = max(1, min(jt, cnt_star));
-    // certification: all kept elements have |y| <= |y*|
-    const double ystar = fabs((double)xstar * c - (double)st.r);
+    // certification: cum and target come from the same per-element masses; the kept set is an
+    // upper set, so its error per unit mass is at most the row's (weighted mean of |y|).
     const double cum_hi = above_m + jt * estar, cum_lo = above_m + (jt - 1) * estar;
-    const double E = (kEx2RelErr + 1.01 * kYRound * ystar + 1e-12) * cum_hi + (double)tp * st.S * st.err + 1e-15;
+    const double rel = kEx2RelErr + 1.02 * kYRound * (A_row / S_fast) + 4.0 * kU32 + 1e-12;
+    const double E = rel * (cum_hi + (double)tp * S_fast) + 1e-15 * S_fast;
     const bool ambiguous = (target - cum_lo) <= E || (cum_hi - target) <= E;
     NucleusCut out;
-    out.ambiguous = 0;
+    out.ambiguous = ambiguous ? 1 : 0;
     out.pad = 0;
     if (!ambiguous) {
-        const int id = ordered_ties<ES>(row, a.V, kstar, jt, nullptr, s_warp, &s_last);
         out.cut_x = xstar;
-        out.cut_id = id;
-        out.mass = cum_hi / st.S;
+        out.cut_id = ordered_ties<ES>(row, a.V, kstar, jt, nullptr, s_warp, &s_last);
+        out.mass = cum_hi / S_fast;
     } else {
-        // ---- float-float tier in this block: exact S, exact mass above K*, exact e* ----
+        // ---- float-float tier: the same select on exact masses ----
         {
             const double t = exp2((double)threadIdx.x / 256.0);
             const float hi = (float)t;
@@ -397,78 +452,21 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
         }
         __syncthreads();
         const ff cff = {c_hi, c_lo};
-        double sx = 0.0, ax = 0.0;
-        uint32_t k_up = 0xFFFFFFFFu, k_dn = 0u;   // nearest keys above / below K*
-        for_each_elem<ES>(row, a.V, [&](float x, int) {
-            const double m = exact_mass(x, cff, rf, tab);
-            const uint32_t k = f32_key(x);
-            sx += m;
-            if (k > kstar) {
-                ax += m;
-                k_up = min(k_up, k);
-            } else if (k < kstar) {
-                k_dn = max(k_dn, k);
-            }
-        });
-        // block reductions
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        sx = warp_sum_d(sx);
-        ax = warp_sum_d(ax);
-        unsigned ku = k_up, kd = k_dn;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            ku = min(ku, __shfl_xor_sync(0xFFFFFFFFu, ku, o));
-            kd = max(kd, __shfl_xor_sync(0xFFFFFFFFu, kd, o));
-        }
-        __shared__ double s_x[2][kWarps];
-        __shared__ unsigned s_k[2][kWarps];
-        if (lane == 0) {
-            s_x[0][warp] = sx;
-            s_x[1][warp] = ax;
-            s_k[0][warp] = ku;
-            s_k[1][warp] = kd;
-        }
-        __syncthreads();
-        double S_x = 0.0, A_x = 0.0;
-        unsigned KU = 0xFFFFFFFFu, KD = 0u;
-        for (int w = 0; w < kWarps; ++w) {
-            S_x += s_x[0][w];
-            A_x += s_x[1][w];
-            KU = min(KU, s_k[0][w]);
-            KD = max(KD, s_k[1][w]);
-        }
-        const double e_x = exact_mass(xstar, cff, rf, tab);
+        auto exact = [&](float x) { return make_double2(exact_mass(x, cff, rf, tab), 0.0); };
+        double A_x, S_x;
+        int cnt_x;
+        const uint32_t kx = radix_select_mass<ES>(row, a.V, 0.0, (double)tp, exact, hm, hc, s_dig, s_dm, s_red, A_x,
+                                                  cnt_x, &S_x, nullptr);
+        const float xx = key_value(kx);
+        const double e_x = exact_mass(xx, cff, rf, tab);
         const double tgt = (double)tp * S_x;
         const double jr = (tgt - A_x) / e_x;
         int jx = (int)ceil(jr);
-        bool unres = fabs(jr - rint(jr)) < 1e-9 * fmax(1.0, fabs(jr));
-        auto key_x = [](uint32_t k) {
-            return (k & 0x80000000u) ? __uint_as_float(k & 0x7FFFFFFFu) : __uint_as_float(~k);
-        };
-        if (jx >= 1 && jx <= cnt_star) {
-            out.cut_x = xstar;
-            out.cut_id = ordered_ties<ES>(row, a.V, kstar, jx, nullptr, s_warp, &s_last);
-            out.mass = (A_x + jx * e_x) / S_x;
-        } else if (jx < 1 && KU != 0xFFFFFFFFu) {
-            // the cut closes the next group up: its last token
-            const float xu = key_x(KU);
-            int cnt_u = 0;
-            for_each_elem<ES>(row, a.V, [&](float x, int) { cnt_u += f32_key(x) == KU ? 1 : 0; });
-            int tot;
-            block_excl_scan(cnt_u, tot, s_warp);
-            out.cut_x = xu;
-            out.cut_id = ordered_ties<ES>(row, a.V, KU, tot, nullptr, s_warp, &s_last);
-            out.mass = A_x / S_x;
-            unres = unres || (A_x - exact_mass(xu, cff, rf, tab) >= tgt);
-        } else {
-            // the cut opens the next group down: its first token
-            const float xd = key_x(KD);
-            out.cut_x = xd;
-            out.cut_id = ordered_ties<ES>(row, a.V, KD, 1, nullptr, s_warp, &s_last);
-            const double m1 = A_x + cnt_star * e_x + exact_mass(xd, cff, rf, tab);
-            out.mass = m1 / S_x;
-            unres = unres || (m1 < tgt);
-        }
+        jx = max(1, min(jx, cnt_x));
+        const bool unres = fabs(jr - rint(jr)) < 1e-9 * fmax(1.0, fabs(jr));
+        out.cut_x = xx;
+        out.cut_id = ordered_ties<ES>(row, a.V, kx, jx, nullptr, s_warp, &s_last);
+        out.mass = (A_x + jx * e_x) / S_x;
         if (threadIdx.x == 0) {
             stats_add(a.stats, &a.stats->reresolved, 1);
             if (unres) stats_add(a.stats, &a.stats->unresolved, 1);
@@ -554,7 +552,7 @@ __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
     int n_above;
     const uint32_t kstar = radix_select_count<ES>(row, a.V, N, n_above, hist, s_dig);
     const int last = ordered_ties<ES>(row, a.V, kstar, N - n_above, nullptr, s_warp, &s_last);
-    const float xstar = (kstar & 0x80000000u) ? __uint_as_float(kstar & 0x7FFFFFFFu) : __uint_as_float(~kstar);
+    const float xstar = key_value(kstar);
     // mass of D, restricted to the nucleus when top-p is on
     float c_hi, c_lo;
     log2e_over(T, c_hi, c_lo);

@@ -151,7 +151,7 @@ __device__ __forceinline__ void acc_scalar(StatAcc &A, float x, int idx, bool gr
     if (!(x <= A.thr)) acc_reference(A, x, c_hi);
     const float y = fmaf(x, c_lo, fmaf(x, c_hi, -A.rf));
     const float e = ex2_fast(y);
-    A.aerr = fmaf(e, fabsf(y), A.aerr);
+    A.aerr = fmaf(e, fminf(fabsf(y), 128.0f), A.aerr);   // e = 0 below 2^-126: keeps -inf logits finite
     acc_add(A, e);
 }
 
@@ -214,6 +214,84 @@ __device__ __forceinline__ void acc_vector(StatAcc &A, uint4 w, int e0, bool gre
     }
 }
 
+// A thread's share of one shared-memory tile: its NV vectors (vi = tid + i * kThreads) are
+// loaded together, checked against the reference with one combined maximum, and their
+// 8 * NV (bf16) exponentials are independent, so the SFU work overlaps.  Vectors past the
+// end of a partial tile read as -inf.
+template <int ES>
+__device__ __forceinline__ void acc_tile(StatAcc &A, const unsigned char *buf, int nv, int fv, bool greedy, float c_hi,
+                                         float c_lo) {
+    constexpr int EPV = 16 / ES;
+    constexpr int NV = kTileBytes / 16 / kThreads;
+    const uint32_t ninf = ES == 2 ? 0xFF80FF80u : 0xFF800000u;
+    const int tid = threadIdx.x;
+    uint4 w[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int vi = tid + i * kThreads;
+        w[i] = vi < nv ? lds128(buf + vi * 16) : make_uint4(ninf, ninf, ninf, ninf);
+    }
+    float vmax;
+    if constexpr (ES == 2) {
+        uint32_t pm = bmax2(bmax2(w[0].x, w[0].y), bmax2(w[0].z, w[0].w));
+#pragma unroll
+        for (int i = 1; i < NV; ++i) pm = bmax2(pm, bmax2(bmax2(w[i].x, w[i].y), bmax2(w[i].z, w[i].w)));
+        vmax = fmax_nan(bf16_lo(pm), bf16_hi(pm));
+    } else {
+        vmax = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            vmax = fmax_nan(vmax, fmax_nan(fmax_nan(__uint_as_float(w[i].x), __uint_as_float(w[i].y)),
+                                           fmax_nan(__uint_as_float(w[i].z), __uint_as_float(w[i].w))));
+    }
+    if (greedy) {
+        if (!(vmax <= A.m)) {
+            if (vmax != vmax) {
+                A.flags |= kFlagNaN;
+                return;
+            }
+            // the first index (in this thread's increasing order) holding the new maximum
+            int idx = -1;
+            for (int i = NV - 1; i >= 0; --i) {
+                float x[EPV];
+                unpack<ES>(w[i], x);
+                for (int k = EPV - 1; k >= 0; --k)
+                    if (x[k] == vmax) idx = (fv + tid + i * kThreads) * EPV + k;
+            }
+            A.m = vmax;
+            A.am = idx;
+            if (isinf(vmax)) A.flags |= kFlagPosInf;
+        }
+        return;
+    }
+    if (!(vmax <= A.thr)) acc_reference(A, vmax, c_hi);
+    float sv[NV], av[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        float x[EPV], e[EPV];
+        unpack<ES>(w[i], x);
+        float a = 0.f;
+#pragma unroll
+        for (int k = 0; k < EPV; ++k) {
+            const float y = fmaf(x[k], c_lo, fmaf(x[k], c_hi, -A.rf));
+            e[k] = ex2_fast(y);
+            a = fmaf(e[k], fminf(fabsf(y), 128.0f), a);
+        }
+        if constexpr (EPV == 8) {
+            sv[i] = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+        } else {
+            sv[i] = (e[0] + e[1]) + (e[2] + e[3]);
+        }
+        av[i] = a;
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) acc_add(A, sv[i]);
+    float at = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) at += av[i];
+    A.aerr += at;
+}
+
 // Warp-combine and store this unit's partial (float32 / float-float arithmetic only).
 __device__ __forceinline__ void acc_store(const StatAcc &A0, bool greedy, WarpPartial *dst) {
     StatAcc A = A0;
@@ -247,7 +325,7 @@ __device__ __forceinline__ void acc_store(const StatAcc &A0, bool greedy, WarpPa
 }
 
 template <int ES>
-__global__ void __launch_bounds__(kThreads, 2) k_stats(const StatsArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) k_stats(const StatsArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     unsigned char *tiles = smem + 128;
@@ -310,13 +388,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stats(const StatsArgs a) {
             if (ok) {
                 const int fv = ui.v0 + t * (kTileBytes / 16);
                 const int nv = min(kTileBytes / 16, ui.v1 - fv);
-                const unsigned char *buf = tiles + st * kTileBytes;
-                constexpr int EPV = 16 / ES;
-#pragma unroll 4
-                for (int vi = tid; vi < nv; vi += kThreads) {
-                    const uint4 w = lds128(buf + vi * 16);
-                    acc_vector<ES>(A, w, (fv + vi) * EPV, ui.greedy, ui.c_hi, ui.c_lo);
-                }
+                acc_tile<ES>(A, tiles + st * kTileBytes, nv, fv, ui.greedy, ui.c_hi, ui.c_lo);
             }
             if (__syncthreads_or(!ok)) {
                 if (tid == 0) {

@@ -36,6 +36,9 @@ def test_top_p_values_small_vocab(tp):
     ref = oracle_verify(inp, w)
     al, ot, dbg, st = run_gpu(inp, w, top_p=True)
     compare(w, inp, ref, al, ot, dbg, st)
+    np.testing.assert_allclose(dbg[:, :, 5], ref["mass_q"], atol=1e-6)
+    np.testing.assert_allclose(dbg[:, : w.K, 6], ref["mass_p"], atol=1e-6)
+    assert st["unresolved"] == 0, st
 
 
 def test_top_p_with_plateaus():
@@ -142,7 +145,11 @@ def test_topn_against_sorting(N, V):
     rng = np.random.default_rng(N + V)
     x = np.round(rng.normal(0, 2, (6, V)) * 4) / 4
     x[2] = 0.0
-    t = torch.as_tensor(x, dtype=torch.bfloat16, device="cuda")
+    x[3] = -np.abs(x[3]) - 0.25                   # all negative: keys with low bits set
+    pitch = (V + 7) // 8 * 8                      # 16-byte aligned rows
+    buf = torch.zeros((6, pitch), dtype=torch.bfloat16, device="cuda")
+    buf[:, :V] = torch.as_tensor(x, dtype=torch.bfloat16, device="cuda")
+    t = buf[:, :V]
     ids, _, _ = sv.sv_topk_rows(t, N)
     torch.cuda.synchronize()
     xs = to_f64(t)

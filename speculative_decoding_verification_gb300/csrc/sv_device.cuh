@@ -222,12 +222,13 @@ __device__ __forceinline__ ff ff_exp2(float yh, float yl, const float2 *tab) {
 }
 
 // c = log2(e) / T as a float-float pair using float32 operations only (the FP64 pipe is far
-// slower than FP32 on this GPU).  The remainder of a correctly rounded quotient is exact, so
-// c_hi + c_lo carries about 46 significant bits.
+// slower than FP32 on this GPU).  The quotient is rounded down, so c_lo >= 0: x * c_hi and
+// x * c_lo then share a sign and a -inf logit gives -inf (never inf - inf).  The remainder of
+// the quotient is exact, so c_hi + c_lo carries about 46 significant bits.
 __device__ __forceinline__ void log2e_over(float T, float &c_hi, float &c_lo) {
     const float L2E_HI = 1.44269502162933349609375f;
     const float L2E_LO = 1.925963033500011e-08f;
-    c_hi = __fdiv_rn(L2E_HI, T);
+    c_hi = __fdiv_rd(L2E_HI, T);
     const float rem = __fadd_rn(__fmaf_rn(-c_hi, T, L2E_HI), L2E_LO);
     c_lo = __fdiv_rn(rem, T);
 }
@@ -264,10 +265,14 @@ __device__ __forceinline__ void stats_add(sv_stats *st, int64_t *field_in_stats,
 
 // Queue an item for the float-float tier; past the queue's capacity the float32 result stands
 // and the decision is counted as unresolved.
-__device__ __forceinline__ void push_exact(Counters *ctr, ExactItem *q, ExactItem item, sv_stats *st) {
+__device__ __forceinline__ void push_exact(Counters *ctr, ExactItem *q, int *unc_n, ExactItem item, sv_stats *st) {
     const int e = atomicAdd(&ctr->n_exact, 1);
-    if (e < kExactCap) q[e] = item;
-    else stats_add(st, &st->unresolved, 1);
+    if (e < kExactCap) {
+        q[e] = item;
+        unc_n[e] = 0;
+    } else {
+        stats_add(st, &st->unresolved, 1);
+    }
 }
 
 // ------------------------------------------------------------------------------------------

@@ -25,6 +25,7 @@ struct DrawArgs {
     int subs_per_chunk;         // vector sub-chunks per chunk
     float2 *subs;               // [item][n_sub] = (sum w, sum of error weights)
     ExactItem *exact;           // exact-tier queue (may be nullptr: no re-resolution)
+    int *exact_unc;             // per queued item: uncertain-token count, zeroed at push
     sv_stats *stats;
     long long wait_limit;
 };
@@ -339,7 +340,7 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
         // every weight is zero: degenerate; the exact tier decides
         if (lane == 0) {
             *it.out = -1;
-            if (a.exact) push_exact(a.counters, a.exact, {d, it.seq}, a.stats);
+            if (a.exact) push_exact(a.counters, a.exact, a.exact_unc, {d, it.seq}, a.stats);
             stats_add(a.stats, &a.stats->reresolved, 1);
             stats_add(a.stats, &a.stats->draws, 1);
         }
@@ -423,7 +424,7 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
         if (near) stats_add(a.stats, &a.stats->near_boundary, 1);
         if (ambiguous && a.exact) {
             stats_add(a.stats, &a.stats->reresolved, 1);
-            push_exact(a.counters, a.exact, {d, it.seq}, a.stats);
+            push_exact(a.counters, a.exact, a.exact_unc, {d, it.seq}, a.stats);
         }
     }
 }

@@ -72,7 +72,7 @@ struct ExactArgs {
     double *xpart;           // [item][slot][kExactSplit][3]   (phase A)
     ExactDraw *xdraw;        // [item]
     float4 *xsubs;           // [item][n_sub]: A_q (ff), A_p (ff)
-    float4 *xnorm;           // [item][xsplit][kWarps]: S_q (ff), S_p (ff)
+    float4 *xnorm;           // [item][xsplit]: S_q (ff), S_p (ff) per unit
     int *xunc_n;             // [item]
     int *xunc;               // [item][kExactUncCap]
     int n_vec, n_sub, xsplit, max_slots;
@@ -159,12 +159,27 @@ __device__ __forceinline__ ExactRow seq_row(const ExactArgs &a, int b, int slot)
 }
 
 // Weight of token v in a row: keep(v) * 2^(x c - r) * (sc on the top-F set), float-float.
-__device__ __forceinline__ ff exact_w(const ExactRow &r, float x, int v, const float2 *tab) {
-    if (!in_cut(x, v, r.cut_x, r.cut_id)) return {0.f, 0.f};
+// Not inlined: one copy of the float-float exponential keeps the kernel inside the I-cache.
+static __device__ __noinline__ ff exact_w(const ExactRow &r, float x, int v, const float2 *tab) {
+    if (!in_cut(x, v, r.cut_x, r.cut_id) || x == -INFINITY) return {0.f, 0.f};
     const ff y = ff_affine(x, r.c, {r.rf, 0.f});
     ff e = ff_exp2(y.hi, y.lo, tab);
     if (in_cut(x, v, r.top_x, r.top_id)) e = ff_mul(e, {r.sc, 0.f});
     return e;
+}
+
+__device__ __forceinline__ ExactDraw exact_draw_from(const DrawItem &d) {
+    ExactDraw xd;
+    xd.q = exact_row_from_draw(d.q);
+    xd.inv_q = d.q.inv_s;
+    xd.has_p = d.has_p;
+    xd.p = d.has_p ? exact_row_from_draw(d.p) : xd.q;
+    xd.inv_p = d.has_p ? d.p.inv_s : 0.f;
+    xd.sign_tol = (float)(1.05 * (d.q.norm_err + (d.has_p ? d.p.norm_err : 0.0)) + 4.0 * kU32);
+    xd.u = d.u;
+    xd.out = d.out;
+    xd.dbg_r = d.dbg_r;
+    return xd;
 }
 
 template <int ES>
@@ -212,6 +227,7 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
             ff sa = {0.f, 0.f}, sk = {0.f, 0.f}, skd = {0.f, 0.f};
             const int v0 = min(c * chunk_vecs, n_vec), v1 = min(v0 + chunk_vecs, n_vec);
             auto add = [&](float x, int v) {
+                if (x == -INFINITY) return;
                 const ff y = ff_affine(x, r.c, {r.rf, 0.f});
                 const ff e = ff_exp2(y.hi, y.lo, tab);
                 sa = ff_add(sa, e);
@@ -250,22 +266,13 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
         }
     }
 
-    // ---- phase B: draw parameters (and the accept tests of queued sequences) ---------------
+    // ---- phase B: the accept tests of queued sequences, then their draw parameters -----------
     const int gwarp = blockIdx.x * kWarps + warp, nwarps = gridDim.x * kWarps;
-    for (int i = gwarp; i < n_items; i += nwarps) {
+    for (int i = gwarp; i < n_items && any_accept; i += nwarps) {
         const ExactItem it = a.items[i];
         ExactDraw xd;
         if (it.draw >= 0) {
-            const DrawItem &d = a.draws[it.draw];
-            xd.q = exact_row_from_draw(d.q);
-            xd.inv_q = d.q.inv_s;
-            xd.has_p = d.has_p;
-            xd.p = d.has_p ? exact_row_from_draw(d.p) : xd.q;
-            xd.inv_p = d.has_p ? d.p.inv_s : 0.f;
-            xd.sign_tol = (float)(1.05 * (d.q.norm_err + (d.has_p ? d.p.norm_err : 0.0)) + 4.0 * kU32);
-            xd.u = d.u;
-            xd.out = d.out;
-            xd.dbg_r = d.dbg_r;
+            continue;   // draw items take their parameters in phase C
         } else {
             const int b = it.seq, K = a.K;
             const double cc = 1.4426950408889634074 / (double)a.temperature[b];
@@ -340,22 +347,24 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
             xd.out = a.out_tokens + (size_t)b * (K + 1) + k;
             xd.dbg_r = a.debug ? a.debug + (size_t)b * (K + 1) * SV_DEBUG_FIELDS + SV_DBG_R : nullptr;
         }
-        if (lane == 0) {
-            a.xdraw[i] = xd;
-            a.xunc_n[i] = 0;
-        }
+        if (lane == 0) a.xdraw[i] = xd;
     }
-    if (!grid_barrier(&a.counters->barrier, bar_target, a.wait_limit)) {
+    if (any_accept && !grid_barrier(&a.counters->barrier, bar_target, a.wait_limit)) {
         if (tid == 0 && blockIdx.x == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
         return;
     }
 
     // ---- phase C: one float-float pass: normalisers and sign-split sub-chunk sums -----------
-    const int subs_per_chunk = (n_vsub + a.xsplit - 1) / a.xsplit;
-    const long long units_c = (long long)n_items * a.xsplit;
+    // about 8 units per block, whole sub-chunks per unit
+    int xsplit = (int)min((long long)a.xsplit, max(1LL, (8LL * gridDim.x + n_items - 1) / n_items));
+    xsplit = max(1, min(xsplit, max(n_vsub, 1)));
+    const int subs_per_chunk = (n_vsub + xsplit - 1) / xsplit;
+    const long long units_c = (long long)n_items * xsplit;
+    __shared__ float4 s_norm[kWarps];
     for (long long u = blockIdx.x; u < units_c; u += gridDim.x) {
-        const int i = (int)(u / a.xsplit), c = (int)(u - (long long)i * a.xsplit);
-        const ExactDraw d = a.xdraw[i];
+        const int i = (int)(u / xsplit), c = (int)(u - (long long)i * xsplit);
+        const ExactItem itm = a.items[i];
+        const ExactDraw d = itm.draw >= 0 ? exact_draw_from(a.draws[itm.draw]) : a.xdraw[i];
         float4 *xs = a.xsubs + (size_t)i * a.n_sub;
         ff nq = {0.f, 0.f}, np = {0.f, 0.f};
         // one token: its contributions to the normalisers and, by the sign test, to (A_q, A_p)
@@ -393,7 +402,7 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
             ap = warp_sum_ff(ap);
             if (lane == 0) xs[sb] = make_float4(aq.hi, aq.lo, ap.hi, ap.lo);
         }
-        if (c == a.xsplit - 1 && warp == 0) {
+        if (c == xsplit - 1 && warp == 0) {
             const int t = n_vec * EPV + lane;
             ff aq = {0.f, 0.f}, ap = {0.f, 0.f};
             if (t < a.V) {
@@ -406,7 +415,17 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
         }
         nq = warp_sum_ff(nq);
         np = warp_sum_ff(np);
-        if (lane == 0) a.xnorm[((size_t)i * a.xsplit + c) * kWarps + warp] = make_float4(nq.hi, nq.lo, np.hi, np.lo);
+        if (lane == 0) s_norm[warp] = make_float4(nq.hi, nq.lo, np.hi, np.lo);
+        __syncthreads();
+        if (tid == 0) {
+            ff tq = {0.f, 0.f}, tpp = {0.f, 0.f};
+            for (int w = 0; w < kWarps; ++w) {
+                tq = ff_add(tq, {s_norm[w].x, s_norm[w].y});
+                tpp = ff_add(tpp, {s_norm[w].z, s_norm[w].w});
+            }
+            a.xnorm[(size_t)i * a.xsplit + c] = make_float4(tq.hi, tq.lo, tpp.hi, tpp.lo);
+        }
+        __syncthreads();
     }
     if (!grid_barrier(&a.counters->barrier, bar_target, a.wait_limit)) {
         if (tid == 0 && blockIdx.x == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
@@ -415,11 +434,12 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
 
     // ---- phase D: per item, exact sub-chunk masses, scan, t* (one warp per item) ------------
     for (int i = gwarp; i < n_items; i += nwarps) {
-        const ExactDraw d = a.xdraw[i];
+        const ExactItem itm = a.items[i];
+        const ExactDraw d = itm.draw >= 0 ? exact_draw_from(a.draws[itm.draw]) : a.xdraw[i];
         const float4 *xs = a.xsubs + (size_t)i * a.n_sub;
         double sq = 0.0, sp = 0.0;
-        for (int k = lane; k < a.xsplit * kWarps; k += 32) {
-            const float4 v = a.xnorm[(size_t)i * a.xsplit * kWarps + k];
+        for (int k = lane; k < xsplit; k += 32) {
+            const float4 v = a.xnorm[(size_t)i * a.xsplit + k];
             sq += (double)v.x + (double)v.y;
             sp += (double)v.z + (double)v.w;
         }

@@ -153,9 +153,9 @@ static SamplePlan plan_sample(int B, int n_rows, int V, int es) {
     p.off_exact = cv.take<ExactItem>(capx);
     p.off_xpart = cv.take<double>(capx * 2 * kExactSplit * 3);
     p.off_xdraw = cv.take<ExactDraw>(capx);
-    p.x_split = n_vsub > 64 ? 64 : (n_vsub > 0 ? n_vsub : 1);
+    p.x_split = n_vsub > 0 ? n_vsub : 1;
     p.off_xsubs = cv.take<float4>(capx * p.n_sub);
-    p.off_xnorm = cv.take<float4>(capx * p.x_split * kWarps);
+    p.off_xnorm = cv.take<float4>(capx * p.x_split);
     p.off_xunc_n = cv.take<int>(capx);
     p.off_xunc = cv.take<int>(capx * kExactUncCap);
     p.bytes = cv.off + 256;
@@ -233,6 +233,7 @@ static sv_status launch_sample(const SamplePlan &sp, const SampleArgs &in, const
     da.subs_per_chunk = pl.d_subs_per_chunk;
     da.subs = reinterpret_cast<float2 *>(w + pl.off_subs);
     da.exact = reinterpret_cast<ExactItem *>(w + pl.off_exact);
+    da.exact_unc = reinterpret_cast<int *>(w + pl.off_xunc_n);
     da.stats = a.stats;
     da.wait_limit = kWaitLimitCycles;
     {

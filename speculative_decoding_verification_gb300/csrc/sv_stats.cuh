@@ -324,58 +324,93 @@ __device__ __forceinline__ void acc_store(const StatAcc &A0, bool greedy, WarpPa
     if (lane == 0) *dst = p;
 }
 
+// Position in a block's sequence of tiles: units blockIdx.x, blockIdx.x + gridDim.x, ...,
+// skipping units that are not needed or hold no whole vector.
+template <int ES>
+struct TileCursor {
+    long long u;
+    int t;
+    UnitInfo ui;
+    bool have;   // ui describes u
+    __device__ __forceinline__ void init(const StatsArgs &a) {
+        u = blockIdx.x;
+        t = 0;
+        have = false;
+        seek(a);
+    }
+    __device__ __forceinline__ void seek(const StatsArgs &a) {
+        while (u < a.n_units) {
+            if (!have) {
+                ui = stats_unit<ES>(a, u);
+                have = true;
+            }
+            if (ui.needed && t < unit_tiles(ui)) return;
+            u += gridDim.x;
+            t = 0;
+            have = false;
+        }
+    }
+    __device__ __forceinline__ bool valid(const StatsArgs &a) const { return u < a.n_units; }
+    __device__ __forceinline__ void next(const StatsArgs &a) {
+        ++t;
+        seek(a);
+    }
+};
+
+template <int ES>
+__device__ __forceinline__ void issue_tile(const TileCursor<ES> &c, uint64_t *bar, unsigned char *dst,
+                                           uint64_t policy) {
+    const int fv = c.ui.v0 + c.t * (kTileBytes / 16);
+    const int nv = min(kTileBytes / 16, c.ui.v1 - fv);
+    const uint32_t bytes = (uint32_t)nv * 16u;
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_load_stream(dst, c.ui.row + (size_t)fv * 16, bytes, bar, policy);
+}
+
+// The pipeline has no block-wide barrier per tile: every warp waits on the stage's "full"
+// barrier, consumes its share, and counts itself done on the stage; the last warp to finish a
+// stage refills it with the tile kStages ahead.  Each warp keeps its own look-ahead cursor, so
+// any warp can be the one that refills.
 template <int ES>
 __global__ void __launch_bounds__(kThreads, 3) k_stats(const StatsArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    static_assert(kStages <= 4, "control block layout");
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);                   // [0, 32)
+    int *done = reinterpret_cast<int *>(smem + 32);                         // [32, 48): warps done per stage
+    int *abort_flag = reinterpret_cast<int *>(smem + 48);                   // [48, 52)
+    long long *last_issued = reinterpret_cast<long long *>(smem + 64);      // [64, 96): tile in flight per stage
     unsigned char *tiles = smem + 128;
     const int tid = threadIdx.x;
-    const int warp = tid >> 5;
+    const int lane = tid & 31, warp = tid >> 5;
 
     if (blockIdx.x == 0 && tid < (int)(sizeof(Counters) / 4) && a.counters)
         reinterpret_cast<int *>(a.counters)[tid] = 0;
+    const uint64_t policy = policy_evict_first();
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            done[s] = 0;
+            last_issued[s] = -1;
+        }
+        *abort_flag = 0;
         fence_barrier_init();
+        TileCursor<ES> pc;
+        pc.init(a);
+        for (int s = 0; s < kStages && pc.valid(a); ++s) {
+            issue_tile<ES>(pc, &full[s], tiles + s * kTileBytes, policy);
+            last_issued[s] = s;
+            pc.next(a);
+        }
     }
     __syncthreads();
-
-    // ---- producer state (meaningful in thread 0 only) ----
-    long long pu = blockIdx.x;
-    int pt = 0;
-    UnitInfo pui;
-    bool p_valid = false;
-    long long issued = 0;
-    const uint64_t policy = policy_evict_first();
-    auto p_seek = [&]() {
-        // position (pu, pt) on the next existing tile
-        while (pu < a.n_units) {
-            if (!p_valid) {
-                pui = stats_unit<ES>(a, pu);
-                p_valid = true;
-            }
-            if (pui.needed && pt < unit_tiles(pui)) return true;
-            pu += gridDim.x;
-            pt = 0;
-            p_valid = false;
-        }
-        return false;
-    };
-    auto p_issue = [&](int stage) {
-        if (!p_seek()) return;
-        const int fv = pui.v0 + pt * (kTileBytes / 16);
-        const int nv = min(kTileBytes / 16, pui.v1 - fv);
-        const uint32_t bytes = (uint32_t)nv * 16u;
-        mbar_arrive_expect_tx(&full[stage], bytes);
-        bulk_load_stream(tiles + stage * kTileBytes, pui.row + (size_t)fv * 16, bytes, &full[stage], policy);
-        ++issued;
-        ++pt;
-    };
-    if (tid == 0)
-        for (int s = 0; s < kStages; ++s) p_issue(s);
+    // look-ahead cursor: kStages tiles ahead of the consumed one
+    TileCursor<ES> ahead;
+    ahead.init(a);
+    for (int s = 0; s < kStages && ahead.valid(a); ++s) ahead.next(a);
 
     long long it = 0;   // tiles consumed by this block
-    for (long long u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+    bool aborted = false;
+    for (long long u = blockIdx.x; u < a.n_units && !aborted; u += gridDim.x) {
         const UnitInfo ui = stats_unit<ES>(a, u);
         if (!ui.needed) continue;
         StatAcc A;
@@ -384,29 +419,45 @@ __global__ void __launch_bounds__(kThreads, 3) k_stats(const StatsArgs a) {
         for (int t = 0; t < nt; ++t, ++it) {
             const int st = (int)(it % kStages);
             const uint32_t par = (uint32_t)((it / kStages) & 1);
-            const bool ok = mbar_wait_bounded(&full[st], par, a.wait_limit);
-            if (ok) {
-                const int fv = ui.v0 + t * (kTileBytes / 16);
-                const int nv = min(kTileBytes / 16, ui.v1 - fv);
-                acc_tile<ES>(A, tiles + st * kTileBytes, nv, fv, ui.greedy, ui.c_hi, ui.c_lo);
-            }
-            if (__syncthreads_or(!ok)) {
-                if (tid == 0) {
-                    report_error(a.stats, SV_ERR_TIMEOUT, (int)ui.rid);
-                    // let copies still in flight land before the block's shared memory is released
-                    for (long long k = it; k < issued; ++k)
-                        mbar_wait_bounded(&full[k % kStages], (uint32_t)((k / kStages) & 1), a.wait_limit / 16);
+            bool ok = mbar_try_wait(&full[st], par);
+            if (!ok) {
+                const long long t0 = clock64();
+                while (!(ok = mbar_try_wait(&full[st], par))) {
+                    if (*reinterpret_cast<volatile int *>(abort_flag) || clock64() - t0 > a.wait_limit) break;
                 }
-                return;
             }
-            if (tid == 0) p_issue(st);
+            if (!ok) {
+                aborted = true;
+                if (lane == 0 && atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, (int)ui.rid);
+                break;
+            }
+            const int fv = ui.v0 + t * (kTileBytes / 16);
+            const int nv = min(kTileBytes / 16, ui.v1 - fv);
+            acc_tile<ES>(A, tiles + st * kTileBytes, nv, fv, ui.greedy, ui.c_hi, ui.c_lo);
+            __syncwarp();
+            if (lane == 0 && atomicAdd(&done[st], 1) == kWarps - 1) {
+                done[st] = 0;
+                if (ahead.valid(a)) {
+                    issue_tile<ES>(ahead, &full[st], tiles + st * kTileBytes, policy);
+                    last_issued[st] = it + kStages;
+                }
+            }
+            if (ahead.valid(a)) ahead.next(a);
         }
+        if (aborted) break;
         // the row's last (< 16 B) elements come after every vector, keeping greedy ties on the lowest id
         if (tid < ui.n_tail) {
             const float x = load_elem<ES>(ui.row, ui.tail0 + tid);
             acc_scalar(A, x, ui.tail0 + tid, ui.greedy, ui.c_hi, ui.c_lo);
         }
         acc_store(A, ui.greedy, a.part + ((size_t)ui.rid * a.n_split + ui.chunk) * kWarps + warp);
+    }
+    __syncthreads();
+    if (tid == 0 && *abort_flag) {
+        // let copies still in flight land before the block's shared memory is released
+        for (int s = 0; s < kStages; ++s)
+            if (last_issued[s] >= 0)
+                mbar_wait_bounded(&full[s], (uint32_t)((last_issued[s] / kStages) & 1), a.wait_limit / 16);
     }
 }
 

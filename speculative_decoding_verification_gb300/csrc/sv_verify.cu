@@ -44,6 +44,7 @@ struct AcceptArgs {
     const TopSet *top;
     DrawItem *draws;
     ExactItem *exact;
+    int *exact_unc;
     Counters *counters;
 };
 
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
     if (ambm) {
         // an accept test too close to call in float32: the float-float tier redoes the sequence
         stats_add(a.stats, &a.stats->reresolved, 1);
-        push_exact(a.counters, a.exact, {-1, b}, a.stats);
+        push_exact(a.counters, a.exact, a.exact_unc, {-1, b}, a.stats);
         return;
     }
     const int d = atomicAdd(&a.counters->n_draws, 1);
@@ -281,9 +282,9 @@ VerifyPlan plan_verify(int B, int K, int V, int es) {
     const int max_slots = 2 * K + 1 > 2 ? 2 * K + 1 : 2;
     p.off_xpart = cv.take<double>(cap * max_slots * kExactSplit * 3);
     p.off_xdraw = cv.take<ExactDraw>(cap);
-    p.x_split = n_vsub > 64 ? 64 : (n_vsub > 0 ? n_vsub : 1);
+    p.x_split = n_vsub > 0 ? n_vsub : 1;
     p.off_xsubs = cv.take<float4>(cap * p.n_sub);
-    p.off_xnorm = cv.take<float4>(cap * p.x_split * kWarps);
+    p.off_xnorm = cv.take<float4>(cap * p.x_split);
     p.off_xunc_n = cv.take<int>(cap);
     p.off_xunc = cv.take<int>(cap * kExactUncCap);
     p.bytes = cv.off + 256;
@@ -353,6 +354,7 @@ static sv_status launch_verify(const VerifyPlan &pl, const AcceptArgs &acc_in, c
     acc.top = top;
     acc.draws = reinterpret_cast<DrawItem *>(w + pl.off_draws);
     acc.exact = reinterpret_cast<ExactItem *>(w + pl.off_exact);
+    acc.exact_unc = reinterpret_cast<int *>(w + pl.off_xunc_n);
     acc.counters = counters;
     k_accept<ES><<<B, kThreads, 0, stream>>>(acc);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
@@ -367,6 +369,7 @@ static sv_status launch_verify(const VerifyPlan &pl, const AcceptArgs &acc_in, c
     da.subs_per_chunk = pl.d_subs_per_chunk;
     da.subs = reinterpret_cast<float2 *>(w + pl.off_subs);
     da.exact = acc.exact;
+    da.exact_unc = acc.exact_unc;
     da.stats = acc.stats;
     da.wait_limit = wait;
     {

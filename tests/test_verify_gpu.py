@@ -116,6 +116,30 @@ def test_ragged_vocabularies(V, dtype, pitch):
     compare(w, inp, ref, al, ot, dbg, st)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_masked_logits(dtype):
+    """-inf logits (masked tokens) in target and draft rows, at several temperatures."""
+    rng = np.random.default_rng(11)
+    B, K, V = 40, 3, 3000
+    x = rng.normal(0, 2, (B, K + 1, V))
+    y = 0.7 * x[:, :K] + rng.normal(0, 1, (B, K, V))
+    x[rng.random(x.shape) < 0.3] = -np.inf
+    y[rng.random(y.shape) < 0.3] = -np.inf
+    tg = torch.as_tensor(x, dtype=dtype, device="cuda")
+    dr = torch.as_tensor(y, dtype=dtype, device="cuda")
+    T = np.where(np.arange(B) % 4 == 0, 0.0, np.where(np.arange(B) % 4 == 1, 1.0,
+                 np.where(np.arange(B) % 4 == 2, 0.6, 1.7))).astype(np.float32)
+    d64 = to_f64(dr)
+    toks = oracle.draft_sample(d64, rng.random((B, K)), T, np.ones(B))["tokens"]
+    u = rng.random((B, K + 1))
+    w = W.Workload("masked", B=B, K=K, V=V, dtype="f32" if dtype == torch.float32 else "bf16", temperature=1.0,
+                   top_p=1.0, rounds=1, seed=0, sigma=2.0, draft_scale=0.7, draft_sigma=1.0)
+    inp = dict(target=tg, draft=dr, tokens=toks, u=u, T=T, top_p=np.ones(B, np.float32))
+    ref = oracle.verify(to_f64(tg), d64, toks, u, T, np.ones(B))
+    al, ot, dbg, st = run_gpu(inp, w)
+    compare(w, inp, ref, al, ot, dbg, st)
+
+
 def test_identical_draft_accepts_all_and_k0():
     rng = np.random.default_rng(7)
     B, K, V = 32, 4, 2048

@@ -156,6 +156,45 @@ sv_status sv_verify(const void *target_logits, int64_t t_row_pitch,
                     void *workspace, size_t workspace_bytes, sv_stream_t stream);
 
 /* ----------------------------------------------------------------------------------------
+ * sv_verify_static — sv_verify for callers that cannot allocate device memory.  The paper
+ * has no counterpart: this is a deployment convenience, not a step of the method.
+ *
+ * Who needs it: a serving engine that hands (nearly) all free HBM to its KV-cache pool when
+ * it starts, so that a cudaMalloc later, in the decode loop, would fail or eat into that
+ * pool; and a host program that loads this library as a plug-in and owns every device
+ * allocation in its process.  Neither can give sv_verify a workspace of its own.
+ *
+ * The arguments and results are those of sv_verify without workspace/workspace_bytes.  The
+ * scratch lives in one fixed device array of SV_STATIC_SCRATCH_BYTES (32 MiB) inside the
+ * library, which every GPU that loads the library holds until the process exits.  The call
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *
+ *  - Limit: a call whose scratch need for (B, K, V, dtype) exceeds SV_STATIC_SCRATCH_BYTES
+ *    returns SV_ERR_WORKSPACE before any device work (B = 512, K = 5, V = 128256 needs about
+ *    28.5 MiB and fits).  sv_verify_workspace_size(B, K, V) bounds the need from above.
+ *  - Set-up: the first call on a device, with that device current, looks up the array's
+ *    device address (cudaGetSymbolAddress) and caches it for that device; a failure there
+ *    returns SV_ERR_CUDA.  Make that first call before any stream capture.
+ *  - Contents: every call shares the array, and it keeps the last call's contents.  Nothing
+ *    in it has to start at zero: the call's first kernel clears its counters (queued draws,
+ *    queued float-float items, grid-barrier count) and every other byte is written before
+ *    it is read within the same call.
+ *  - Races: calls whose kernels overlap on the GPU (other streams, other host threads on the
+ *    same device) use the same scratch and race.  Order them, e.g. on one stream.
+ * -------------------------------------------------------------------------------------- */
+#define SV_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+
+sv_status sv_verify_static(const void *target_logits, int64_t t_row_pitch,
+                           const void *draft_logits, int64_t d_row_pitch, int d_rows_per_seq,
+                           sv_dtype dtype,
+                           const int32_t *draft_tokens, const double *uniforms,
+                           int B, int K, int V,
+                           const float *temperature, const float *top_p,
+                           int saguaro_F, float saguaro_C,
+                           int32_t *accept_len, int32_t *out_tokens,
+                           double *debug, sv_stats *stats, sv_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
  * sv_saguaro_sample — draw one token from each of the first n_rows rows of every sequence's
  * draft distribution p' = sigma_{F,C}(p): p after temperature and top-p, the top-F tokens
  * (ranked by draft logit) scaled by C, renormalised.  F = 0 or C = 1 is a plain draft sampler.

@@ -123,6 +123,51 @@ def sv_verify(target, draft, draft_tokens, uniforms, temperature, top_p=None, sa
     return accept_len, out_tokens, dbg, stats
 
 
+def sv_verify_static(target, draft, draft_tokens, uniforms, temperature, top_p=None, saguaro_F=0, saguaro_C=1.0,
+                     accept_len=None, out_tokens=None, debug=None, stats=None, stream=None):
+    """sv_verify without a workspace, for callers that cannot allocate device memory (a server
+    whose KV-cache pool holds all free HBM, a host program that owns every allocation).
+
+    The library's own scratch array (SV_STATIC_SCRATCH_BYTES, 32 MiB per device) stands in for
+    the workspace, so the C call allocates nothing.  Pass accept_len int32 [B], out_tokens int32
+    [B, K+1], stats (new_stats) and, optionally, debug float64 [B, K+1, 8] to keep this wrapper
+    from allocating them.  Calls that overlap on the GPU share the scratch and race; the first
+    call on a device looks up the array's address and belongs before any stream capture.
+    Returns (accept_len, out_tokens, debug, stats) like sv_verify.
+    """
+    lib = load()
+    B, K1, V = target.shape
+    K = K1 - 1
+    dev = target.device
+    t_pitch, _ = _rows(target, "target")
+    if K > 0:
+        if draft.dtype != target.dtype:
+            raise TypeError("target and draft logits must share a dtype")
+        d_pitch, d_rows = _rows(draft, "draft")
+        d_ptr = _ptr(draft)
+    else:
+        d_pitch, d_rows, d_ptr = t_pitch, 1, ctypes.c_void_p(0)
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if debug is True:
+        debug = torch.empty((B, K + 1, _abi.SV_DEBUG_FIELDS), dtype=torch.float64, device=dev)
+    elif debug is False:
+        debug = None
+    if stats is None:
+        stats = new_stats(dev)
+    code = lib.sv_verify_static(_ptr(target), t_pitch, d_ptr, d_pitch, d_rows, _dtype_code(target),
+                                _ptr(draft_tokens if K > 0 else None), _ptr(uniforms), B, K, V, _ptr(temperature),
+                                _ptr(top_p), int(saguaro_F), float(saguaro_C), _ptr(accept_len), _ptr(out_tokens),
+                                _ptr(debug), _ptr(stats), _stream(stream))
+    if code == _abi.SV_ERR_WORKSPACE:
+        raise ValueError(f"sv_verify_static: B={B}, K={K}, V={V} needs more scratch than the "
+                         f"{_abi.SV_STATIC_SCRATCH_BYTES >> 20} MiB static array; use sv_verify with a workspace")
+    _abi.check("sv_verify_static", code)
+    return accept_len, out_tokens, debug, stats
+
+
 def sv_saguaro_sample(draft, uniforms, temperature, top_p=None, F=0, C=1.0, n_rows=None, tokens=None, debug=False,
                       stats=None, workspace=None, stream=None):
     """sv_saguaro_sample: one token per row j < n_rows of each sequence of draft [B, R, V].

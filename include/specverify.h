@@ -176,9 +176,10 @@ sv_status sv_verify(const void *target_logits, int64_t t_row_pitch,
  *    device address (cudaGetSymbolAddress) and caches it for that device; a failure there
  *    returns SV_ERR_CUDA.  Make that first call before any stream capture.
  *  - Contents: every call shares the array, and it keeps the last call's contents.  Nothing
- *    in it has to start at zero: the call's first kernel clears its counters (queued draws,
- *    queued float-float items, grid-barrier count) and every other byte is written before
- *    it is read within the same call.
+ *    in it has to start at zero: each call clears its counters (queued draws, queued
+ *    float-float items, grid-barrier count, next unit of the statistics pass) with one
+ *    memset on its stream before its first kernel, and every other byte is written before it
+ *    is read within the same call.
  *  - Races: calls whose kernels overlap on the GPU (other streams, other host threads on the
  *    same device) use the same scratch and race.  Order them, e.g. on one stream.
  * -------------------------------------------------------------------------------------- */

@@ -10,14 +10,17 @@ namespace sv {
 constexpr int kThreads = 256;               // threads per streaming block
 constexpr int kWarps = kThreads / 32;
 constexpr int kTileBytes = 16384;           // one bulk copy (one pipeline stage per row)
-constexpr int kStages = 4;                  // pipeline depth of the statistics pass
+constexpr int kStatsStages = 6;             // pipeline depth of the statistics pass
+constexpr int kStatsThreads = kThreads + 32;   // eight consumer warps and one producer warp
+constexpr int kUnitTiles = 4;               // aim for (row, chunk) units of about this many tiles
 constexpr int kDrawStages = 3;              // pipeline depth of the draw pass (two rows per stage)
 constexpr int kSubBytes = 512;              // bytes of one row per draw sub-chunk (32 x 16 B)
 constexpr int kMaxSplit = 64;               // most chunks per row
-constexpr int kUnitTarget = 16384;          // aim for about this many (row, chunk) units
+constexpr int kUnitTarget = 1024;           // at least about this many (row, chunk) units
 constexpr int kExactSplit = 16;             // chunks per row in the float-float tier
 constexpr int kExactCap = 2048;             // most queued items per call in the float-float tier
 constexpr long long kWaitLimitCycles = 4000000000LL;   // ~2 s at 2 GHz: bounded barrier waits
+constexpr unsigned kSuspendHintNs = 100000;  // a waiting thread sleeps at most this long per try
 
 // ---- certification constants of the float32 tier ------------------------------------------
 // Largest relative error of ex2.approx.ftz.f32 over [-126, 0] is below 2^-22 (checked by
@@ -117,23 +120,42 @@ struct ExactItem {
 };
 
 // Counters that each call resets before use (kernel-side).
+// Zeroed by the host (one memset) before the statistics pass of every call.
 struct Counters {
     int n_draws;
     int n_exact;
     unsigned barrier;       // grid barrier of the exact tier
-    int pad[13];
+    int next_unit;          // statistics pass: next (row, chunk) unit to hand out
+    int pad[12];
 };
 
 inline int div_up(long long a, long long b) { return (int)((a + b - 1) / b); }
 
 // Chunks per row: enough (row, chunk) units to balance ~kUnitTarget of them, chunks >= one tile.
 inline int choose_split(long long n_rows, long long row_bytes) {
-    long long by_units = (kUnitTarget + n_rows - 1) / (n_rows > 0 ? n_rows : 1);
-    long long by_size = row_bytes / kTileBytes;
-    long long s = by_units < by_size ? by_units : by_size;
+    const long long row_tiles = row_bytes / kTileBytes;
+    long long s = row_tiles / kUnitTiles;                                     // units of ~kUnitTiles tiles
+    const long long by_units = (kUnitTarget + n_rows - 1) / (n_rows > 0 ? n_rows : 1);
+    if (s < by_units) s = by_units;                                           // small batches: more units
+    if (s > row_tiles) s = row_tiles;                                         // but chunks >= one tile
     if (s < 1) s = 1;
     if (s > kMaxSplit) s = kMaxSplit;
     return (int)s;
+}
+
+// 16-byte vectors per chunk: whole tiles where the row has them, so only a row's last chunk
+// ends in a partial tile.  n_split may shrink; both are returned.
+inline void chunk_geometry(long long n_vec, int &n_split, int &chunk_vecs) {
+    if (n_vec <= 0) {
+        n_split = 1;
+        chunk_vecs = 1;
+        return;
+    }
+    const long long tv = kTileBytes / 16;
+    long long cv = (n_vec + n_split - 1) / n_split;
+    if (cv > tv) cv = (cv + tv - 1) / tv * tv;
+    chunk_vecs = (int)cv;
+    n_split = (int)((n_vec + cv - 1) / cv);
 }
 
 // Sub-chunks of a row in the draw pass: one per 32 16-byte vectors, plus a last one holding the

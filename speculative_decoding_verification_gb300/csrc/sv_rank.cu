@@ -176,7 +176,7 @@ static TopKPlan plan_topk(int n_rows, int V, int es, int stride) {
     p.n_rows0 = n_rows;
     p.n_split = choose_split(n_rows, (long long)V * es);
     p.n_vec = vec_count(V, es);
-    p.chunk_vecs = p.n_vec > 0 ? div_up(p.n_vec, p.n_split) : 1;
+    chunk_geometry(p.n_vec, p.n_split, p.chunk_vecs);
     Carver cv;
     p.off_counters = cv.take<Counters>(1);
     p.off_part = cv.take<WarpPartial>((size_t)n_rows * p.n_split * kWarps);
@@ -221,17 +221,10 @@ extern "C" sv_status sv_topk_rows(const void *logits, int64_t row_pitch, sv_dtyp
     sa.counters = reinterpret_cast<Counters *>(w + pl.off_counters);
     sa.stats = stats;
     sa.wait_limit = kWaitLimitCycles;
-    const size_t smem = 128 + (size_t)kStages * kTileBytes;
-    const void *kfun = es == 4 ? (const void *)k_stats<4> : (const void *)k_stats<2>;
-    const int occ = prepare_kernel(kfun, kThreads, smem);
-    if (occ < 1) return SV_ERR_CUDA;
-    long long grid = (long long)di.sms * occ;
-    if (grid > sa.n_units) grid = sa.n_units;
-    profile_begin(stream);
-    if (es == 4) k_stats<4><<<(unsigned)grid, kThreads, smem, stream>>>(sa);
-    else k_stats<2><<<(unsigned)grid, kThreads, smem, stream>>>(sa);
-    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
-    profile_end(stream);
+    {
+        const sv_status st = es == 4 ? launch_stats<4>(sa, di, stream) : launch_stats<2>(sa, di, stream);
+        if (st != SV_OK) return st;
+    }
     TopNArgs ta{};
     ta.base = static_cast<const char *>(logits);
     ta.pitch_bytes = row_pitch * es;

@@ -133,7 +133,7 @@ static SamplePlan plan_sample(int B, int n_rows, int V, int es) {
     p.n_rows1 = 0;
     p.n_split = choose_split(rows, (long long)V * es);
     p.n_vec = vec_count(V, es);
-    p.chunk_vecs = p.n_vec > 0 ? div_up(p.n_vec, p.n_split) : 1;
+    chunk_geometry(p.n_vec, p.n_split, p.chunk_vecs);
     p.n_sub = sub_chunks(V, es);
     const int n_vsub = p.n_sub - 1;
     long long want = (4096 + rows - 1) / rows;
@@ -189,15 +189,8 @@ static sv_status launch_sample(const SamplePlan &sp, const SampleArgs &in, const
     sa.stats = a.stats;
     sa.wait_limit = kWaitLimitCycles;
     {
-        const size_t smem = 128 + (size_t)kStages * kTileBytes;
-        const int occ = prepare_kernel((const void *)k_stats<ES>, kThreads, smem);
-        if (occ < 1) return SV_ERR_CUDA;
-        long long grid = (long long)di.sms * occ;
-        if (grid > sa.n_units) grid = sa.n_units;
-        profile_begin(stream);
-        k_stats<ES><<<(unsigned)grid, kThreads, smem, stream>>>(sa);
-        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
-        profile_end(stream);
+        const sv_status st = launch_stats<ES>(sa, di, stream);
+        if (st != SV_OK) return st;
     }
     NucleusCut *nuc = nullptr;
     TopSet *top = nullptr;

@@ -6,13 +6,14 @@
 // so that log2 sum_v 2^(x_v c) = r + log2 S and LSE = (r + log2 S) ln 2.  For a greedy row
 // (T == 0) it finds the maximum and its lowest index.  Both track NaN / +inf.
 //
-// Work is a static round-robin over (row, chunk) units across a persistent grid.  Thread 0 of
-// each block feeds a kStages-deep ring of 16 KB shared-memory tiles with 1-D bulk copies
-// (cp.async.bulk); the block consumes tiles with 128-bit shared loads.  Each warp writes one
-// WarpPartial per unit, combined later in float64.
+// Work is handed out as (row, chunk) units from a global counter to a persistent grid.  In each
+// block a producer warp streams the units' 16 KB tiles into shared memory with 1-D bulk copies
+// (cp.async.bulk) and eight consumer warps read them with 128-bit shared loads.  Each consumer
+// warp writes one WarpPartial per unit; partials are combined per row by the accept kernel.
 #pragma once
 
 #include "sv_device.cuh"
+#include "sv_host.h"
 
 namespace sv {
 
@@ -26,7 +27,7 @@ struct StatsArgs {
     long long n_rows0;          // candidate rows in set 0
     long long n_units;          // candidate rows * n_split
     WarpPartial *part;          // [candidate row][chunk][warp]
-    Counters *counters;         // zeroed by block 0 (consumed by later kernels of the call)
+    Counters *counters;         // zeroed by the host before the pass (work counter; later kernels)
     sv_stats *stats;
     long long wait_limit;
 };
@@ -324,141 +325,167 @@ __device__ __forceinline__ void acc_store(const StatAcc &A0, bool greedy, WarpPa
     if (lane == 0) *dst = p;
 }
 
-// Position in a block's sequence of tiles: units blockIdx.x, blockIdx.x + gridDim.x, ...,
-// skipping units that are not needed or hold no whole vector.
-template <int ES>
-struct TileCursor {
-    long long u;
-    int t;
-    UnitInfo ui;
-    bool have;   // ui describes u
-    __device__ __forceinline__ void init(const StatsArgs &a) {
-        u = blockIdx.x;
-        t = 0;
-        have = false;
-        seek(a);
-    }
-    __device__ __forceinline__ void seek(const StatsArgs &a) {
-        while (u < a.n_units) {
-            if (!have) {
-                ui = stats_unit<ES>(a, u);
-                have = true;
-            }
-            if (ui.needed && t < unit_tiles(ui)) return;
-            u += gridDim.x;
-            t = 0;
-            have = false;
-        }
-    }
-    __device__ __forceinline__ bool valid(const StatsArgs &a) const { return u < a.n_units; }
-    __device__ __forceinline__ void next(const StatsArgs &a) {
-        ++t;
-        seek(a);
-    }
+// One pipeline stage's description, written by the producer before the stage's copy is issued.
+struct TileMeta {
+    const char *row;
+    long long rid;
+    float c_hi, c_lo;
+    int chunk;
+    int fv, nv;           // first vector of the tile within the row, vectors in the tile
+    int tail0, n_tail;    // scalar tail of the row (last tile of a row's last chunk)
+    int flags;            // kTileFirst | kTileLast | kTileGreedy | kTileEnd
 };
+constexpr int kTileFirst = 1, kTileLast = 2, kTileGreedy = 4, kTileEnd = 8;
 
-template <int ES>
-__device__ __forceinline__ void issue_tile(const TileCursor<ES> &c, uint64_t *bar, unsigned char *dst,
-                                           uint64_t policy) {
-    const int fv = c.ui.v0 + c.t * (kTileBytes / 16);
-    const int nv = min(kTileBytes / 16, c.ui.v1 - fv);
-    const uint32_t bytes = (uint32_t)nv * 16u;
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_load_stream(dst, c.ui.row + (size_t)fv * 16, bytes, bar, policy);
-}
+constexpr int kStatsCtlBytes = 1024;   // full[], empty[], abort flag, TileMeta[]
+static_assert(2 * kStatsStages * 8 + 16 + kStatsStages * (int)sizeof(TileMeta) <= kStatsCtlBytes, "control block");
+constexpr size_t kStatsSmemBytes = (size_t)kStatsCtlBytes + (size_t)kStatsStages * kTileBytes;
 
-// The pipeline has no block-wide barrier per tile: every warp waits on the stage's "full"
-// barrier, consumes its share, and counts itself done on the stage; the last warp to finish a
-// stage refills it with the tile kStages ahead.  Each warp keeps its own look-ahead cursor, so
-// any warp can be the one that refills.
+// Warp-specialised pipeline.  The producer (lane 0 of the last warp) takes (row, chunk) units
+// from a global counter, skips units that are not needed, and streams each unit's tiles into a
+// kStatsStages-deep ring of 16 KB shared-memory tiles with 1-D bulk copies; per stage it first
+// waits until the eight consumer warps released the stage ("empty"), writes the TileMeta, then
+// issues the copy that completes the stage's "full" barrier.  Consumer warps wait on "full",
+// accumulate their share of the tile, and release it.  Waits sleep (suspend hint) instead of
+// spinning, give up after wait_limit cycles or once another warp has aborted, and on abort the
+// producer lets its copies in flight land before the block exits.
 template <int ES>
-__global__ void __launch_bounds__(kThreads, 3) k_stats(const StatsArgs a) {
+__global__ void __launch_bounds__(kStatsThreads, 2) k_stats(const StatsArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
-    static_assert(kStages <= 4, "control block layout");
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem);                   // [0, 32)
-    int *done = reinterpret_cast<int *>(smem + 32);                         // [32, 48): warps done per stage
-    int *abort_flag = reinterpret_cast<int *>(smem + 48);                   // [48, 52)
-    long long *last_issued = reinterpret_cast<long long *>(smem + 64);      // [64, 96): tile in flight per stage
-    unsigned char *tiles = smem + 128;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + kStatsStages;
+    int *abort_flag = reinterpret_cast<int *>(smem + 2 * kStatsStages * 8);
+    TileMeta *meta = reinterpret_cast<TileMeta *>(smem + 2 * kStatsStages * 8 + 16);
+    unsigned char *tiles = smem + kStatsCtlBytes;
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
 
-    if (blockIdx.x == 0 && tid < (int)(sizeof(Counters) / 4) && a.counters)
-        reinterpret_cast<int *>(a.counters)[tid] = 0;
-    const uint64_t policy = policy_evict_first();
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kStatsStages; ++s) {
             mbar_init(&full[s], 1);
-            done[s] = 0;
-            last_issued[s] = -1;
+            mbar_init(&empty[s], kWarps);
         }
         *abort_flag = 0;
         fence_barrier_init();
-        TileCursor<ES> pc;
-        pc.init(a);
-        for (int s = 0; s < kStages && pc.valid(a); ++s) {
-            issue_tile<ES>(pc, &full[s], tiles + s * kTileBytes, policy);
-            last_issued[s] = s;
-            pc.next(a);
-        }
     }
     __syncthreads();
-    // look-ahead cursor: kStages tiles ahead of the consumed one
-    TileCursor<ES> ahead;
-    ahead.init(a);
-    for (int s = 0; s < kStages && ahead.valid(a); ++s) ahead.next(a);
 
-    long long it = 0;   // tiles consumed by this block
-    bool aborted = false;
-    for (long long u = blockIdx.x; u < a.n_units && !aborted; u += gridDim.x) {
-        const UnitInfo ui = stats_unit<ES>(a, u);
-        if (!ui.needed) continue;
-        StatAcc A;
-        acc_init(A);
-        const int nt = unit_tiles(ui);
-        for (int t = 0; t < nt; ++t, ++it) {
-            const int st = (int)(it % kStages);
-            const uint32_t par = (uint32_t)((it / kStages) & 1);
-            bool ok = mbar_try_wait(&full[st], par);
-            if (!ok) {
-                const long long t0 = clock64();
-                while (!(ok = mbar_try_wait(&full[st], par))) {
-                    if (*reinterpret_cast<volatile int *>(abort_flag) || clock64() - t0 > a.wait_limit) break;
+    if (warp == kWarps) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            const uint64_t policy = policy_evict_first();
+            long long in_flight[kStatsStages];   // tile number whose copy a stage waits for, or -1
+            for (int s = 0; s < kStatsStages; ++s) in_flight[s] = -1;
+            long long it = 0;
+            bool ok = true;
+            int u = atomicAdd(&a.counters->next_unit, 1);
+            while (ok) {
+                // the next needed unit (or the end)
+                UnitInfo ui;
+                bool have = false;
+                while (u < a.n_units) {
+                    ui = stats_unit<ES>(a, u);
+                    u = atomicAdd(&a.counters->next_unit, 1);   // fetch ahead; used for the next unit
+                    if (ui.needed) {
+                        have = true;
+                        break;
+                    }
+                }
+                const int nt = have ? max(unit_tiles(ui), 1) : 1;
+                for (int t = 0; t < nt; ++t, ++it) {
+                    const int st = (int)(it % kStatsStages);
+                    if (it >= kStatsStages) {
+                        const uint32_t par = (uint32_t)(((it / kStatsStages) - 1) & 1);
+                        if (!mbar_wait_or_abort(&empty[st], par, abort_flag, a.wait_limit)) {
+                            if (atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
+                            ok = false;
+                            break;
+                        }
+                    }
+                    in_flight[st] = -1;
+                    TileMeta m;
+                    if (!have) {
+                        m.flags = kTileEnd;
+                        meta[st] = m;
+                        mbar_arrive(&full[st]);
+                        ok = false;
+                        break;
+                    }
+                    const int fv = ui.v0 + t * (kTileBytes / 16);
+                    const int nv = max(0, min(kTileBytes / 16, ui.v1 - fv));
+                    m.row = ui.row;
+                    m.rid = ui.rid;
+                    m.c_hi = ui.c_hi;
+                    m.c_lo = ui.c_lo;
+                    m.chunk = ui.chunk;
+                    m.fv = fv;
+                    m.nv = nv;
+                    m.tail0 = ui.tail0;
+                    m.n_tail = ui.n_tail;
+                    m.flags = (t == 0 ? kTileFirst : 0) | (t == nt - 1 ? kTileLast : 0) | (ui.greedy ? kTileGreedy : 0);
+                    meta[st] = m;
+                    if (nv > 0) {
+                        mbar_arrive_expect_tx(&full[st], (uint32_t)nv * 16u);
+                        bulk_load_stream(tiles + st * kTileBytes, ui.row + (size_t)fv * 16, (uint32_t)nv * 16u,
+                                         &full[st], policy);
+                        in_flight[st] = it;
+                    } else {
+                        mbar_arrive(&full[st]);   // a tail-only unit: nothing to copy
+                    }
                 }
             }
-            if (!ok) {
-                aborted = true;
-                if (lane == 0 && atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, (int)ui.rid);
-                break;
+            // after an abort, copies still in flight land before shared memory is released
+            if (*reinterpret_cast<volatile int *>(abort_flag)) {
+                for (int s = 0; s < kStatsStages; ++s)
+                    if (in_flight[s] >= 0)
+                        mbar_wait_bounded(&full[s], (uint32_t)((in_flight[s] / kStatsStages) & 1), a.wait_limit / 16);
             }
-            const int fv = ui.v0 + t * (kTileBytes / 16);
-            const int nv = min(kTileBytes / 16, ui.v1 - fv);
-            acc_tile<ES>(A, tiles + st * kTileBytes, nv, fv, ui.greedy, ui.c_hi, ui.c_lo);
-            __syncwarp();
-            if (lane == 0 && atomicAdd(&done[st], 1) == kWarps - 1) {
-                done[st] = 0;
-                if (ahead.valid(a)) {
-                    issue_tile<ES>(ahead, &full[st], tiles + st * kTileBytes, policy);
-                    last_issued[st] = it + kStages;
-                }
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    StatAcc A;
+    acc_init(A);
+    for (long long it = 0;; ++it) {
+        const int st = (int)(it % kStatsStages);
+        const uint32_t par = (uint32_t)((it / kStatsStages) & 1);
+        if (!mbar_wait_or_abort(&full[st], par, abort_flag, a.wait_limit)) {
+            if (lane == 0 && atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
+            break;
+        }
+        const TileMeta m = meta[st];
+        if (m.flags & kTileEnd) break;
+        const bool greedy = (m.flags & kTileGreedy) != 0;
+        if (m.flags & kTileFirst) acc_init(A);
+        if (m.nv > 0) acc_tile<ES>(A, tiles + st * kTileBytes, m.nv, m.fv, greedy, m.c_hi, m.c_lo);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        if (m.flags & kTileLast) {
+            // the row's last (< 16 B) elements come after every vector, keeping greedy ties on the lowest id
+            if (tid < m.n_tail) {
+                const float x = load_elem<ES>(m.row, m.tail0 + tid);
+                acc_scalar(A, x, m.tail0 + tid, greedy, m.c_hi, m.c_lo);
             }
-            if (ahead.valid(a)) ahead.next(a);
+            acc_store(A, greedy, a.part + ((size_t)m.rid * a.n_split + m.chunk) * kWarps + warp);
         }
-        if (aborted) break;
-        // the row's last (< 16 B) elements come after every vector, keeping greedy ties on the lowest id
-        if (tid < ui.n_tail) {
-            const float x = load_elem<ES>(ui.row, ui.tail0 + tid);
-            acc_scalar(A, x, ui.tail0 + tid, ui.greedy, ui.c_hi, ui.c_lo);
-        }
-        acc_store(A, ui.greedy, a.part + ((size_t)ui.rid * a.n_split + ui.chunk) * kWarps + warp);
     }
-    __syncthreads();
-    if (tid == 0 && *abort_flag) {
-        // let copies still in flight land before the block's shared memory is released
-        for (int s = 0; s < kStages; ++s)
-            if (last_issued[s] >= 0)
-                mbar_wait_bounded(&full[s], (uint32_t)((last_issued[s] / kStages) & 1), a.wait_limit / 16);
-    }
+}
+
+// Host side: clear the call's counters, then run the statistics pass on a persistent grid.
+template <int ES>
+static sv_status launch_stats(const StatsArgs &sa, const DeviceInfo &di, cudaStream_t stream) {
+    if (cudaMemsetAsync(sa.counters, 0, sizeof(Counters), stream) != cudaSuccess) return SV_ERR_CUDA;
+    const int occ = prepare_kernel((const void *)k_stats<ES>, kStatsThreads, kStatsSmemBytes);
+    if (occ < 1) return SV_ERR_CUDA;
+    long long grid = (long long)di.sms * occ;
+    if (grid > sa.n_units) grid = sa.n_units;
+    if (grid < 1) grid = 1;
+    profile_begin(stream);
+    k_stats<ES><<<(unsigned)grid, kStatsThreads, kStatsSmemBytes, stream>>>(sa);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    profile_end(stream);
+    return SV_OK;
 }
 
 // Combine a row's warp partials (one warp).  Float-float accumulation; the few float64

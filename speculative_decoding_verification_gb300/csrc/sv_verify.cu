@@ -261,7 +261,7 @@ VerifyPlan plan_verify(int B, int K, int V, int es) {
     const long long row_bytes = (long long)V * es;
     p.n_split = choose_split(n_cand, row_bytes);
     p.n_vec = vec_count(V, es);
-    p.chunk_vecs = p.n_vec > 0 ? div_up(p.n_vec, p.n_split) : 1;
+    chunk_geometry(p.n_vec, p.n_split, p.chunk_vecs);
     p.n_sub = sub_chunks(V, es);
     const int n_vsub = p.n_sub - 1;
     long long want = (4096 + B - 1) / B;
@@ -318,16 +318,8 @@ static sv_status launch_verify(const VerifyPlan &pl, const AcceptArgs &acc_in, c
     sa.stats = acc.stats;
     sa.wait_limit = wait;
     {
-        const size_t smem = 128 + (size_t)kStages * kTileBytes;
-        const int occ = prepare_kernel((const void *)k_stats<ES>, kThreads, smem);
-        if (occ < 1) return SV_ERR_CUDA;
-        long long grid = (long long)di.sms * occ;
-        if (grid > sa.n_units) grid = sa.n_units;
-        if (grid < 1) grid = 1;
-        profile_begin(stream);
-        k_stats<ES><<<(unsigned)grid, kThreads, smem, stream>>>(sa);
-        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
-        profile_end(stream);
+        const sv_status st = launch_stats<ES>(sa, di, stream);
+        if (st != SV_OK) return st;
     }
     // 2. nucleus cuts and top-F sets (only when asked for)
     NucleusCut *nuc = nullptr;

@@ -310,6 +310,12 @@ void sv_set_profile_events(void *begin, void *end);
 sv_status sv_selftest_timeout(int64_t limit_cycles, sv_stats *stats, sv_stream_t stream);
 sv_status sv_selftest_exp2(double lo, double hi, int64_t n, double *out, sv_stream_t stream);
 
+/* sv_selftest_exp2_all: the same two errors over EVERY float32 input in [lo, hi] (lo >= -125,
+ * hi <= 100) whose exact result is above 2^-125; out[0] fast, out[1] float-float, out[2] the
+ * number of inputs evaluated (a double).  Over [-125, 1] this is an exhaustive proof of the
+ * fast exponential's error bound on the GPU it runs on (about 2.2e9 inputs). */
+sv_status sv_selftest_exp2_all(float lo, float hi, double *out, sv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -286,3 +286,14 @@ def sv_selftest_exp2(lo: float, hi: float, n: int, stream=None):
     out = torch.zeros(2, dtype=torch.float64, device="cuda")
     _abi.check("sv_selftest_exp2", lib.sv_selftest_exp2(float(lo), float(hi), int(n), _ptr(out), _stream(stream)))
     return out
+
+
+def sv_selftest_exp2_all(lo: float, hi: float, stream=None):
+    """Largest relative errors (fast, float-float) of the library's exponentials over every
+    float32 input in [lo, hi], and the number of inputs evaluated."""
+    lib = load()
+    out = torch.zeros(3, dtype=torch.float64, device="cuda")
+    _abi.check("sv_selftest_exp2_all", lib.sv_selftest_exp2_all(float(lo), float(hi), _ptr(out), _stream(stream)))
+    torch.cuda.synchronize()
+    r = out.cpu().tolist()
+    return r[0], r[1], int(r[2])

@@ -53,6 +53,7 @@ SIGNATURES = {
     "sv_set_profile_events": (None, [c_vp, c_vp]),
     "sv_selftest_timeout": (c_int, [c_i64, c_vp, c_vp]),
     "sv_selftest_exp2": (c_int, [c_f64, c_f64, c_i64, c_vp, c_vp]),
+    "sv_selftest_exp2_all": (c_int, [c_f32, c_f32, c_vp, c_vp]),
 }
 
 _lib = None

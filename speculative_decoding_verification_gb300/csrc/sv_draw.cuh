@@ -235,18 +235,26 @@ __global__ void __launch_bounds__(kThreads, 2) k_draw_sums(const DrawArgs a) {
 // Certified bound on |C_fast(v) - u R_fast - (C(v) - u R)| over all v (see the header comment of
 // this file): element errors from the SFU exponential, the float32 exponent arguments, the
 // normalisers and the products, plus the float32 summation inside sub-chunks.
+// Bound on |(u R~ - C~(v)) - (u R - C(v))| for any v, where ~ marks the computed prefix sums.
+// With per-token errors d_v = |w~_v - w_v| the difference is (1-u) sum_{i<=v} d_i and
+// u sum_{i>v} d_i of opposite signs at worst, so it is at most max(u, 1-u) sum_v d_v; the
+// float32 sums of each sub-chunk (8 rounding levels, non-negative terms) add 8u to both
+// C~(v) <= R and u R~, bounded by 20u R.  sum_v d_v: the exponent's rounding (kYRound per unit
+// |y|, summed as A), the exponential (kEx2RelErr), the products with the normalisers (2u) and
+// the normalisers' own errors; for a bonus draw without filters a common normaliser error
+// cancels in C(v) / R.
 __device__ __forceinline__ double draw_error_bound(const DrawItem &it, double W, double A) {
     const double u = kU32;
-    double e = kYRound * 1.01 * A + 10.0 * u * W + 1e-15;
+    double e = kYRound * 1.01 * A;
     if (it.has_p) {
         e += 1.0001 * (kEx2RelErr + 2.0 * u + it.q.norm_err) + 1.0001 * (kEx2RelErr + 2.0 * u + it.p.norm_err);
     } else if (it.filt) {
         // tokens inside and outside the scaled set carry different normaliser errors
         e += (kEx2RelErr + 2.0 * u + it.q.norm_err) * W;
     } else {
-        e += (kEx2RelErr + u) * W;   // a common normaliser error cancels in C(v) / R
+        e += (kEx2RelErr + u) * W;
     }
-    return 2.0 * e;
+    return fmax(it.u, 1.0 - it.u) * e + 20.0 * u * W + 1e-15;
 }
 
 template <int ES>

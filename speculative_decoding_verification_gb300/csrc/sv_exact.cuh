@@ -354,15 +354,13 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
         return;
     }
 
-    // ---- phase C: one float-float pass: normalisers and sign-split sub-chunk sums -----------
-    // about 8 units per block, whole sub-chunks per unit
-    int xsplit = (int)min((long long)a.xsplit, max(1LL, (8LL * gridDim.x + n_items - 1) / n_items));
-    xsplit = max(1, min(xsplit, max(n_vsub, 1)));
-    const int subs_per_chunk = (n_vsub + xsplit - 1) / xsplit;
-    const long long units_c = (long long)n_items * xsplit;
-    __shared__ float4 s_norm[kWarps];
-    for (long long u = blockIdx.x; u < units_c; u += gridDim.x) {
-        const int i = (int)(u / xsplit), c = (int)(u - (long long)i * xsplit);
+    // ---- phase C: one float-float pass over the draw rows, one warp per unit ----------------
+    // A unit is kExactGroup sub-chunks of one item (or its scalar tail): per sub-chunk the
+    // sign-split sums (A_q, A_p), per unit the two normaliser partials.  No block barriers.
+    const int n_grp = a.xsplit;   // exact_groups(n_sub)
+    const long long units_c = (long long)n_items * n_grp;
+    for (long long u = gwarp; u < units_c; u += nwarps) {
+        const int i = (int)(u / n_grp), g = (int)(u - (long long)i * n_grp);
         const ExactItem itm = a.items[i];
         const ExactDraw d = itm.draw >= 0 ? exact_draw_from(a.draws[itm.draw]) : a.xdraw[i];
         float4 *xs = a.xsubs + (size_t)i * a.n_sub;
@@ -387,22 +385,23 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
                 if (slot < kExactUncCap) a.xunc[(size_t)i * kExactUncCap + slot] = v;
             }
         };
-        const int sb0 = min(c * subs_per_chunk, n_vsub), sb1 = min(sb0 + subs_per_chunk, n_vsub);
-        for (int sb = sb0 + warp; sb < sb1; sb += kWarps) {
-            const int vi = sb * 32 + lane;
-            ff aq = {0.f, 0.f}, ap = {0.f, 0.f};
-            if (vi < n_vec) {
-                float xq[EPV], xp[EPV];
-                load_vec<ES>(d.q.row, vi, xq);
-                if (d.has_p) load_vec<ES>(d.p.row, vi, xp);
-#pragma unroll
-                for (int k = 0; k < EPV; ++k) token(xq[k], d.has_p ? xp[k] : xq[k], vi * EPV + k, aq, ap);
+        if (g < n_grp - 1) {
+            const int sb0 = g * kExactGroup, sb1 = min(sb0 + kExactGroup, n_vsub);
+            for (int sb = sb0; sb < sb1; ++sb) {
+                const int vi = sb * 32 + lane;
+                ff aq = {0.f, 0.f}, ap = {0.f, 0.f};
+                if (vi < n_vec) {
+                    float xq[EPV], xp[EPV];
+                    load_vec<ES>(d.q.row, vi, xq);
+                    if (d.has_p) load_vec<ES>(d.p.row, vi, xp);
+#pragma unroll 1
+                    for (int k = 0; k < EPV; ++k) token(xq[k], d.has_p ? xp[k] : xq[k], vi * EPV + k, aq, ap);
+                }
+                aq = warp_sum_ff(aq);
+                ap = warp_sum_ff(ap);
+                if (lane == 0) xs[sb] = make_float4(aq.hi, aq.lo, ap.hi, ap.lo);
             }
-            aq = warp_sum_ff(aq);
-            ap = warp_sum_ff(ap);
-            if (lane == 0) xs[sb] = make_float4(aq.hi, aq.lo, ap.hi, ap.lo);
-        }
-        if (c == xsplit - 1 && warp == 0) {
+        } else {
             const int t = n_vec * EPV + lane;
             ff aq = {0.f, 0.f}, ap = {0.f, 0.f};
             if (t < a.V) {
@@ -415,159 +414,193 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
         }
         nq = warp_sum_ff(nq);
         np = warp_sum_ff(np);
-        if (lane == 0) s_norm[warp] = make_float4(nq.hi, nq.lo, np.hi, np.lo);
-        __syncthreads();
-        if (tid == 0) {
-            ff tq = {0.f, 0.f}, tpp = {0.f, 0.f};
-            for (int w = 0; w < kWarps; ++w) {
-                tq = ff_add(tq, {s_norm[w].x, s_norm[w].y});
-                tpp = ff_add(tpp, {s_norm[w].z, s_norm[w].w});
-            }
-            a.xnorm[(size_t)i * a.xsplit + c] = make_float4(tq.hi, tq.lo, tpp.hi, tpp.lo);
-        }
-        __syncthreads();
+        if (lane == 0) a.xnorm[(size_t)i * n_grp + g] = make_float4(nq.hi, nq.lo, np.hi, np.lo);
     }
     if (!grid_barrier(&a.counters->barrier, bar_target, a.wait_limit)) {
         if (tid == 0 && blockIdx.x == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
         return;
     }
 
-    // ---- phase D: per item, exact sub-chunk masses, scan, t* (one warp per item) ------------
-    for (int i = gwarp; i < n_items; i += nwarps) {
+    // ---- phase D: one block per item: exact sub-chunk masses, block scan, t* ----------------
+    __shared__ double s_unc_w[kExactUncCap];
+    __shared__ int s_unc_sub[kExactUncCap];
+    __shared__ double s_wsum[kWarps];
+    __shared__ int s_sub;
+    __shared__ double s_pre;
+    __shared__ int s_last;
+    for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
         const ExactItem itm = a.items[i];
         const ExactDraw d = itm.draw >= 0 ? exact_draw_from(a.draws[itm.draw]) : a.xdraw[i];
         const float4 *xs = a.xsubs + (size_t)i * a.n_sub;
+        // normalisers
         double sq = 0.0, sp = 0.0;
-        for (int k = lane; k < xsplit; k += 32) {
-            const float4 v = a.xnorm[(size_t)i * a.xsplit + k];
+        for (int k = tid; k < n_grp; k += kThreads) {
+            const float4 v = a.xnorm[(size_t)i * n_grp + k];
             sq += (double)v.x + (double)v.y;
             sp += (double)v.z + (double)v.w;
         }
         sq = warp_sum_d(sq);
         sp = warp_sum_d(sp);
+        if (lane == 0) {
+            s_red[0][warp] = sq;
+            s_red[1][warp] = sp;
+        }
+        __syncthreads();
+        sq = 0.0;
+        sp = 0.0;
+        for (int w = 0; w < kWarps; ++w) {
+            sq += s_red[0][w];
+            sp += s_red[1][w];
+        }
         const double iq = 1.0 / sq, ip = d.has_p ? 1.0 / sp : 0.0;
+        // exact residuals of the tokens whose sign the float32 test could not settle
         const int n_unc_all = a.xunc_n[i];
         const int n_unc = min(n_unc_all, kExactUncCap);
-        if (lane == 0 && n_unc_all > kExactUncCap) stats_add(a.stats, &a.stats->unresolved, 1);
-        // exact residual of an uncertain token
-        auto unc_w = [&](int t) {
+        if (tid == 0 && n_unc_all > kExactUncCap) stats_add(a.stats, &a.stats->unresolved, 1);
+        for (int k = tid; k < n_unc; k += kThreads) {
+            const int t = a.xunc[(size_t)i * kExactUncCap + k];
             const float xq = load_elem<ES>(d.q.row, t), xp = load_elem<ES>(d.p.row, t);
             const double w = ff_to_double(exact_w(d.q, xq, t, tab)) * iq - ff_to_double(exact_w(d.p, xp, t, tab)) * ip;
-            return w > 0.0 ? w : 0.0;
-        };
-        auto sub_of = [&](int t) { return t < n_vec * EPV ? t / (32 * EPV) : n_vsub; };
-        auto W = [&](int s, const float4 &v) {
+            s_unc_w[k] = w > 0.0 ? w : 0.0;
+            s_unc_sub[k] = t < n_vec * EPV ? t / (32 * EPV) : n_vsub;
+        }
+        if (tid == 0) {
+            s_sub = -1;
+            s_last = -1;
+        }
+        __syncthreads();
+        auto W = [&](int s) {
+            const float4 v = xs[s];
             double w = ((double)v.x + (double)v.y) * iq - ((double)v.z + (double)v.w) * ip;
-            for (int k = 0; k < n_unc; ++k) {
-                const int t = a.xunc[(size_t)i * kExactUncCap + k];
-                if (sub_of(t) == s) w += unc_w(t);
-            }
+            for (int k = 0; k < n_unc; ++k)
+                if (s_unc_sub[k] == s) w += s_unc_w[k];
             return w;
         };
-        double R = 0.0;
-        for (int s = lane; s < a.n_sub; s += 32) R += W(s, xs[s]);
-        R = warp_sum_d(R);
+        // per-thread contiguous ranges of sub-chunks, block scan of their sums
+        const int per = (a.n_sub + kThreads - 1) / kThreads;
+        const int s0 = min(tid * per, a.n_sub), s1 = min(s0 + per, a.n_sub);
+        double mine = 0.0;
+        int last_pos = -1;
+        for (int s = s0; s < s1; ++s) {
+            const double w = W(s);
+            mine += w;
+            if (w > 0.0) last_pos = s;
+        }
+        double inc = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += t;
+        }
+        if (lane == 31) s_wsum[warp] = inc;
+        atomicMax(&s_last, last_pos);
+        __syncthreads();
+        double wbase = 0.0, R = 0.0;
+        for (int w = 0; w < kWarps; ++w) {
+            if (w < warp) wbase += s_wsum[w];
+            R += s_wsum[w];
+        }
+        const double excl = wbase + inc - mine;
         const double thr = d.u * R;
-        int sub = -1, last_pos = -1;
-        double pre = 0.0, run = 0.0, last_pre = 0.0;
-        for (int base = 0; base < a.n_sub && sub < 0; base += 32) {
-            const int s = base + lane;
-            const double v = s < a.n_sub ? W(s, xs[s]) : 0.0;
-            double inc = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const double t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-                if (lane >= o) inc += t;
+        if (mine > 0.0 && excl <= thr && thr < excl + mine) {
+            double run = excl;
+            for (int s = s0; s < s1; ++s) {
+                const double w = W(s);
+                if (w > 0.0 && thr < run + w) {
+                    s_sub = s;
+                    s_pre = run;
+                    break;
+                }
+                run += w;
             }
-            const double ex = run + inc - v;
-            const unsigned m = __ballot_sync(0xFFFFFFFFu, v > 0.0 && thr < ex + v);
-            const unsigned mp = __ballot_sync(0xFFFFFFFFu, v > 0.0);
-            if (mp) {
-                const int src = 31 - __clz(mp);
-                last_pos = base + src;
-                last_pre = __shfl_sync(0xFFFFFFFFu, ex, src);
-            }
-            if (m) {
-                const int src = __ffs(m) - 1;
-                sub = base + src;
-                pre = __shfl_sync(0xFFFFFFFFu, ex, src);
-            }
-            run = __shfl_sync(0xFFFFFFFFu, run + inc, 31);
         }
+        __syncthreads();
+        int sub = s_sub;
+        double pre = s_pre;
         if (sub < 0) {
-            sub = last_pos;
-            pre = last_pre;
+            // u R at or past the last boundary through rounding: the last positive sub-chunk
+            sub = s_last;
+            if (tid == 0 && sub >= 0) {
+                double p = 0.0;
+                for (int s = 0; s < sub; ++s) p += W(s);
+                s_pre = p;
+            }
+            __syncthreads();
+            pre = s_pre;
         }
-        int tstar = -1;
-        if (sub >= 0) {
-            double wv[EPV];
-            int ntok = 0, tok0;
-            auto wt = [&](float xq, float xp, int t) {
-                const double q = ff_to_double(exact_w(d.q, xq, t, tab)) * iq;
-                if (!d.has_p) return q;
-                const double w = q - ff_to_double(exact_w(d.p, xp, t, tab)) * ip;
-                return w > 0.0 ? w : 0.0;
-            };
-            if (sub < n_vsub) {
-                const int vi = sub * 32 + lane;
-                tok0 = vi * EPV;
-                if (vi < n_vec) {
-                    ntok = EPV;
-                    float xq[EPV], xp[EPV];
-                    load_vec<ES>(d.q.row, vi, xq);
-                    if (d.has_p) load_vec<ES>(d.p.row, vi, xp);
+        if (warp == 0) {
+            int tstar = -1;
+            if (sub >= 0) {
+                double wv[EPV];
+                int ntok = 0, tok0;
+                auto wt = [&](float xq, float xp, int t) {
+                    const double q = ff_to_double(exact_w(d.q, xq, t, tab)) * iq;
+                    if (!d.has_p) return q;
+                    const double w = q - ff_to_double(exact_w(d.p, xp, t, tab)) * ip;
+                    return w > 0.0 ? w : 0.0;
+                };
+                if (sub < n_vsub) {
+                    const int vi = sub * 32 + lane;
+                    tok0 = vi * EPV;
+                    if (vi < n_vec) {
+                        ntok = EPV;
+                        float xq[EPV], xp[EPV];
+                        load_vec<ES>(d.q.row, vi, xq);
+                        if (d.has_p) load_vec<ES>(d.p.row, vi, xp);
+#pragma unroll 1
+                        for (int k = 0; k < EPV; ++k) wv[k] = wt(xq[k], d.has_p ? xp[k] : xq[k], tok0 + k);
+                    }
+                } else {
+                    tok0 = n_vec * EPV + lane;
+                    if (tok0 < a.V) {
+                        ntok = 1;
+                        const float xq = load_elem<ES>(d.q.row, tok0);
+                        wv[0] = wt(xq, d.has_p ? load_elem<ES>(d.p.row, tok0) : xq, tok0);
+                    }
+                }
+                double lt = 0.0;
+                for (int k = 0; k < ntok; ++k) lt += wv[k];
+                double linc = lt;
 #pragma unroll
-                    for (int k = 0; k < EPV; ++k) wv[k] = wt(xq[k], d.has_p ? xp[k] : xq[k], tok0 + k);
+                for (int o = 1; o < 32; o <<= 1) {
+                    const double t = __shfl_up_sync(0xFFFFFFFFu, linc, o);
+                    if (lane >= o) linc += t;
                 }
-            } else {
-                tok0 = n_vec * EPV + lane;
-                if (tok0 < a.V) {
-                    ntok = 1;
-                    const float xq = load_elem<ES>(d.q.row, tok0);
-                    wv[0] = wt(xq, d.has_p ? load_elem<ES>(d.p.row, tok0) : xq, tok0);
+                double cc = pre + linc - lt;
+                int hit = -1, lastk = -1;
+                double cp = cc, ch = cc;
+                for (int k = 0; k < ntok; ++k) {
+                    const double nx = cc + wv[k];
+                    if (wv[k] > 0.0) lastk = k;
+                    if (hit < 0 && wv[k] > 0.0 && thr < nx) {
+                        hit = k;
+                        cp = cc;
+                        ch = nx;
+                    }
+                    cc = nx;
                 }
-            }
-            double lt = 0.0;
-            for (int k = 0; k < ntok; ++k) lt += wv[k];
-            double inc = lt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const double t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-                if (lane >= o) inc += t;
-            }
-            double cc = pre + inc - lt;
-            int hit = -1, lastk = -1;
-            double cp = cc, ch = cc;
-            for (int k = 0; k < ntok; ++k) {
-                const double nx = cc + wv[k];
-                if (wv[k] > 0.0) lastk = k;
-                if (hit < 0 && wv[k] > 0.0 && thr < nx) {
-                    hit = k;
-                    cp = cc;
-                    ch = nx;
+                const unsigned m = __ballot_sync(0xFFFFFFFFu, hit >= 0);
+                bool unres;
+                if (m) {
+                    const int src = __ffs(m) - 1;
+                    tstar = __shfl_sync(0xFFFFFFFFu, tok0 + (ntok == 1 ? 0 : hit), src);
+                    const double c_prev = __shfl_sync(0xFFFFFFFFu, cp, src);
+                    const double c_hit = __shfl_sync(0xFFFFFFFFu, ch, src);
+                    unres = (thr - c_prev) < 1e-12 * R || (c_hit - thr) < 1e-12 * R;
+                } else {
+                    const unsigned mm = __ballot_sync(0xFFFFFFFFu, lastk >= 0);
+                    const int src = mm ? 31 - __clz(mm) : 0;
+                    tstar = __shfl_sync(0xFFFFFFFFu, tok0 + (ntok == 1 ? 0 : max(lastk, 0)), src);
+                    unres = true;
                 }
-                cc = nx;
+                if (lane == 0 && unres) stats_add(a.stats, &a.stats->unresolved, 1);
             }
-            const unsigned m = __ballot_sync(0xFFFFFFFFu, hit >= 0);
-            bool unres;
-            if (m) {
-                const int src = __ffs(m) - 1;
-                tstar = __shfl_sync(0xFFFFFFFFu, tok0 + (ntok == 1 ? 0 : hit), src);
-                const double c_prev = __shfl_sync(0xFFFFFFFFu, cp, src);
-                const double c_hit = __shfl_sync(0xFFFFFFFFu, ch, src);
-                unres = (thr - c_prev) < 1e-12 * R || (c_hit - thr) < 1e-12 * R;
-            } else {
-                const unsigned mm = __ballot_sync(0xFFFFFFFFu, lastk >= 0);
-                const int src = mm ? 31 - __clz(mm) : 0;
-                tstar = __shfl_sync(0xFFFFFFFFu, tok0 + (ntok == 1 ? 0 : max(lastk, 0)), src);
-                unres = true;
+            if (lane == 0) {
+                *d.out = tstar;
+                if (d.dbg_r) *d.dbg_r = R;
             }
-            if (lane == 0 && unres) stats_add(a.stats, &a.stats->unresolved, 1);
         }
-        if (lane == 0) {
-            *d.out = tstar;
-            if (d.dbg_r) *d.dbg_r = R;
-        }
+        __syncthreads();
     }
 }
 

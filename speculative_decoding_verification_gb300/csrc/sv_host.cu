@@ -4,6 +4,8 @@
 #include <vector>
 
 #include "sv_device.cuh"
+#include <string.h>
+
 #include "sv_host.h"
 
 namespace sv {
@@ -93,9 +95,70 @@ __global__ void k_selftest_exp2(double lo, double hi, long long n, unsigned long
     atomicMax(&out_bits[1], (unsigned long long)__double_as_longlong(e_ff));
 }
 
+// Every float32 x with key(lo) <= key(x) <= key(hi), key an order-preserving map of the bit
+// patterns: the same two errors as k_selftest_exp2, over all inputs instead of a sample.
+__device__ __forceinline__ unsigned f32_order_key(float x) {
+    const unsigned b = __float_as_uint(x);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float f32_from_order_key(unsigned k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+__global__ void k_selftest_exp2_all(unsigned k0, long long count, unsigned long long *out_bits) {
+    __shared__ float2 tab[256];
+    {
+        const double t = exp2((double)threadIdx.x / 256.0);
+        const float h = (float)t;
+        tab[threadIdx.x] = make_float2(h, (float)(t - (double)h));
+    }
+    __syncthreads();
+    double e_fast = 0.0, e_ff = 0.0;
+    unsigned long long n_eval = 0;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < count;
+         i += (long long)gridDim.x * blockDim.x) {
+        const float x = f32_from_order_key(k0 + (unsigned)i);
+        const double ref = exp2((double)x);
+        if (ref > 0x1p-125) {
+            const double f = (double)ex2_fast(x);
+            e_fast = fmax(e_fast, fabs(f - ref) / ref);
+            const ff e = ff_exp2(x, 0.0f, tab);
+            e_ff = fmax(e_ff, fabs(ff_to_double(e) - ref) / ref);
+            ++n_eval;
+        }
+    }
+    const int lane = threadIdx.x & 31;
+    for (int o = 16; o > 0; o >>= 1) {
+        e_fast = fmax(e_fast, __shfl_xor_sync(0xFFFFFFFFu, e_fast, o));
+        e_ff = fmax(e_ff, __shfl_xor_sync(0xFFFFFFFFu, e_ff, o));
+        n_eval += __shfl_xor_sync(0xFFFFFFFFu, n_eval, o);
+    }
+    if (lane == 0) {
+        atomicMax(&out_bits[0], (unsigned long long)__double_as_longlong(e_fast));
+        atomicMax(&out_bits[1], (unsigned long long)__double_as_longlong(e_ff));
+        atomicAdd(reinterpret_cast<double *>(&out_bits[2]), (double)n_eval);
+    }
+}
+
 }  // namespace sv
 
 using namespace sv;
+
+static unsigned host_order_key(float x) {
+    unsigned b;
+    memcpy(&b, &x, sizeof(b));
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+extern "C" sv_status sv_selftest_exp2_all(float lo, float hi, double *out, sv_stream_t stream) {
+    if (out == nullptr || !(lo <= hi) || lo < -125.0f || hi > 100.0f) return SV_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(out, 0, 3 * sizeof(double), s) != cudaSuccess) return SV_ERR_CUDA;
+    const unsigned k0 = host_order_key(lo), k1 = host_order_key(hi);
+    const long long count = (long long)k1 - (long long)k0 + 1;
+    k_selftest_exp2_all<<<4096, 256, 0, s>>>(k0, count, reinterpret_cast<unsigned long long *>(out));
+    return cuda_status(cudaGetLastError());
+}
 
 extern "C" const char *sv_status_string(sv_status s) {
     switch (s) {

@@ -153,7 +153,7 @@ static SamplePlan plan_sample(int B, int n_rows, int V, int es) {
     p.off_exact = cv.take<ExactItem>(capx);
     p.off_xpart = cv.take<double>(capx * 2 * kExactSplit * 3);
     p.off_xdraw = cv.take<ExactDraw>(capx);
-    p.x_split = n_vsub > 0 ? n_vsub : 1;
+    p.x_split = exact_groups(p.n_sub);
     p.off_xsubs = cv.take<float4>(capx * p.n_sub);
     p.off_xnorm = cv.take<float4>(capx * p.x_split);
     p.off_xunc_n = cv.take<int>(capx);

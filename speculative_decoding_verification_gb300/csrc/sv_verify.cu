@@ -282,7 +282,7 @@ VerifyPlan plan_verify(int B, int K, int V, int es) {
     const int max_slots = 2 * K + 1 > 2 ? 2 * K + 1 : 2;
     p.off_xpart = cv.take<double>(cap * max_slots * kExactSplit * 3);
     p.off_xdraw = cv.take<ExactDraw>(cap);
-    p.x_split = n_vsub > 0 ? n_vsub : 1;
+    p.x_split = exact_groups(p.n_sub);
     p.off_xsubs = cv.take<float4>(cap * p.n_sub);
     p.off_xnorm = cv.take<float4>(cap * p.x_split);
     p.off_xunc_n = cv.take<int>(cap);

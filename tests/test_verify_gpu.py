@@ -57,6 +57,29 @@ def test_fast_exp2_error_bound():
     assert out[1] < 1e-13, out
 
 
+def _layout_constant(name):
+    import os
+    import re
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "speculative_decoding_verification_gb300", "csrc", "sv_layout.h")
+    m = re.search(name + r"\s*=\s*([0-9.eE+-]+);", open(path).read())
+    return float(m.group(1))
+
+
+def test_fast_exp2_error_bound_exhaustive():
+    """Every float32 input in [-125, 1]: the fast exponential's largest relative error stays
+    within the constant the float32 tier's certification uses.  The float-float one is below
+    1e-13 down to 2^-64; below that its low word meets the float32 underflow range, where its
+    absolute error (under 1e-7 of a value below 2^-64) is irrelevant to any sum."""
+    e_fast, e_ff, n = sv.sv_selftest_exp2_all(-125.0, 1.0)
+    assert n > 2_000_000_000
+    assert e_fast <= _layout_constant("kEx2RelErr"), e_fast
+    assert e_ff < 1e-7, e_ff
+    _, e_ff_hi, n_hi = sv.sv_selftest_exp2_all(-64.0, 1.0)
+    assert n_hi > 1_000_000_000
+    assert e_ff_hi < 1e-13, e_ff_hi
+
+
 def test_bounded_wait_reports_timeout():
     st = sv.sv_selftest_timeout(200_000)
     torch.cuda.synchronize()

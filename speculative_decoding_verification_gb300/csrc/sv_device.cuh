@@ -208,6 +208,21 @@ __device__ __forceinline__ ff ff_add(ff a, ff b) {
 
 __device__ __forceinline__ ff ff_sub(ff a, ff b) { return ff_add(a, {-b.hi, -b.lo}); }
 
+__device__ __forceinline__ ff ff_mul(ff a, ff b) {
+    ff p = two_prod(a.hi, b.hi);
+    p.lo = __fmaf_rn(a.hi, b.lo, __fmaf_rn(a.lo, b.hi, p.lo));
+    return fast_two_sum(p.hi, p.lo);
+}
+
+// a + b for a float b.
+__device__ __forceinline__ ff ff_add_f(ff a, float b) {
+    const ff s = two_sum(a.hi, b);
+    return fast_two_sum(s.hi, __fadd_rn(s.lo, a.lo));
+}
+
+// a - b as a float (the float-float difference rounded once): its sign is that of a - b.
+__device__ __forceinline__ float ff_diff(ff a, ff b) { return ff_sub(a, b).hi; }
+
 __device__ __forceinline__ double ff_to_double(ff a) { return (double)a.hi + (double)a.lo; }
 
 __device__ __forceinline__ ff ff_from_double(double d) {

@@ -242,28 +242,34 @@ __global__ void __launch_bounds__(kThreads, 2) k_draw_sums(const DrawArgs a) {
 // C~(v) <= R and u R~, bounded by 20u R.  sum_v d_v: the exponent's rounding (kYRound per unit
 // |y|, summed as A), the exponential (kEx2RelErr), the products with the normalisers (2u) and
 // the normalisers' own errors; for a bonus draw without filters a common normaliser error
-// cancels in C(v) / R.
-__device__ __forceinline__ double draw_error_bound(const DrawItem &it, double W, double A) {
-    const double u = kU32;
-    double e = kYRound * 1.01 * A;
+// cancels in C(v) / R.  The float-float scans add well under 1e-9 R.  Evaluated in float32
+// and rounded up.
+__device__ __forceinline__ float draw_error_bound(const DrawItem &it, float W, float A) {
+    const float u = (float)kU32;
+    const float ex = (float)kEx2RelErr;
+    float e = (float)(kYRound * 1.01) * A;
     if (it.has_p) {
-        e += 1.0001 * (kEx2RelErr + 2.0 * u + it.q.norm_err) + 1.0001 * (kEx2RelErr + 2.0 * u + it.p.norm_err);
+        e += 1.0001f * (ex + 2.0f * u + (float)it.q.norm_err) + 1.0001f * (ex + 2.0f * u + (float)it.p.norm_err);
     } else if (it.filt) {
         // tokens inside and outside the scaled set carry different normaliser errors
-        e += (kEx2RelErr + 2.0 * u + it.q.norm_err) * W;
+        e += (ex + 2.0f * u + (float)it.q.norm_err) * W;
     } else {
-        e += (kEx2RelErr + u) * W;
+        e += (ex + u) * W;
     }
-    return fmax(it.u, 1.0 - it.u) * e + 20.0 * u * W + 1e-15;
+    const float uu = (float)fmax(it.u, 1.0 - it.u);
+    return (uu * e + 20.0f * u * W + 1e-9f * W + 1e-30f) * (1.0f + 0x1p-18f);
 }
 
+// One block per item, float32 / float-float only: the sub-chunk sums are scanned in
+// float-float, the sub-chunk holding u R is rescanned token by token, and t* is certified
+// against draw_error_bound.
 template <int ES>
 __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
     constexpr int EPV = 16 / ES;
-    __shared__ double s_scan[kThreads];
-    __shared__ double s_red[2][kWarps];
+    __shared__ float2 s_scan[kThreads];
+    __shared__ float s_red[kWarps];
     __shared__ int s_sub;
-    __shared__ double s_pre;
+    __shared__ float2 s_pre;
     __shared__ int s_last_sub;
 
     const int d = blockIdx.x;
@@ -277,71 +283,75 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
     // 1. per-thread contiguous ranges of sub-chunks
     const int per = (n_sub + kThreads - 1) / kThreads;
     const int s0 = min(tid * per, n_sub), s1 = min(s0 + per, n_sub);
-    double wsum = 0.0, asum = 0.0;
+    ff wsum = {0.f, 0.f};
+    float asum = 0.f;
     int last_pos = -1;
     for (int s = s0; s < s1; ++s) {
         const float2 v = subs[s];
-        wsum += (double)v.x;
-        asum += (double)v.y;
+        wsum = ff_add_f(wsum, v.x);
+        asum += v.y;
         if (v.x > 0.f) last_pos = s;
     }
-    // 2. block exclusive scan of wsum
-    s_scan[tid] = wsum;
+    // 2. block inclusive scan of wsum in float-float
+    s_scan[tid] = make_float2(wsum.hi, wsum.lo);
     if (tid == 0) {
         s_sub = -1;
         s_last_sub = -1;
     }
     __syncthreads();
     for (int off = 1; off < kThreads; off <<= 1) {
-        const double v = tid >= off ? s_scan[tid - off] : 0.0;
+        const float2 v = tid >= off ? s_scan[tid - off] : make_float2(0.f, 0.f);
         __syncthreads();
-        s_scan[tid] += v;
+        const float2 m = s_scan[tid];
+        const ff t = ff_add({m.x, m.y}, {v.x, v.y});
+        s_scan[tid] = make_float2(t.hi, t.lo);
         __syncthreads();
     }
-    const double incl = s_scan[tid];
-    const double excl = incl - wsum;
-    const double R = s_scan[kThreads - 1];
-    double at = warp_sum_d(asum);
-    if (lane == 0) s_red[0][warp] = at;
+    const float2 in2 = s_scan[tid];
+    const float2 ex2v = tid > 0 ? s_scan[tid - 1] : make_float2(0.f, 0.f);
+    const float2 r2 = s_scan[kThreads - 1];
+    const ff incl = {in2.x, in2.y}, excl = {ex2v.x, ex2v.y}, R = {r2.x, r2.y};
+    const float at = warp_sum_f(asum);
+    if (lane == 0) s_red[warp] = at;
     atomicMax(&s_last_sub, last_pos);
     __syncthreads();
-    double A = 0.0;
-    for (int w = 0; w < kWarps; ++w) A += s_red[0][w];
-    const double thr = it.u * R;
+    float A = 0.f;
+    for (int w = 0; w < kWarps; ++w) A += s_red[w];
+    const float u_hi = __double2float_rn(it.u);
+    const float u_lo = __double2float_rn(it.u - (double)u_hi);
+    const ff thr = ff_mul(R, {u_hi, u_lo});
     // 3. the thread whose range holds thr finds the sub-chunk
-    const double next = tid + 1 < kThreads ? s_scan[tid] : R;
-    if (wsum > 0.0 && excl <= thr && thr < next) {
-        double run = excl;
+    if (wsum.hi > 0.f && ff_diff(thr, excl) >= 0.f && ff_diff(thr, incl) < 0.f) {
+        ff run = excl, pre = excl;
         int found = -1;
-        double pre = excl;
         for (int s = s0; s < s1; ++s) {
-            const double wv = (double)subs[s].x;
-            if (wv > 0.0) {
+            const float wv = subs[s].x;
+            const ff nx = ff_add_f(run, wv);
+            if (wv > 0.f) {
                 found = s;
                 pre = run;
-                if (thr < run + wv) break;
+                if (ff_diff(thr, nx) < 0.f) break;
             }
-            run += wv;
+            run = nx;
         }
         s_sub = found;
-        s_pre = pre;
+        s_pre = make_float2(pre.hi, pre.lo);
     }
     __syncthreads();
     int sub = s_sub;
-    double pre = s_pre;
+    ff pre = {s_pre.x, s_pre.y};
     bool ambiguous = false;
     if (sub < 0) {
-        // thr beyond the last boundary (rounding) or R == 0: fall back to the last positive weight
+        // thr at or beyond the last boundary (rounding) or R == 0: the last positive weight
         sub = s_last_sub;
-        pre = -1.0;   // computed below from the scan
         ambiguous = true;
         if (sub >= 0 && tid == 0) {
-            double p = 0.0;
-            for (int s = 0; s < sub; ++s) p += (double)subs[s].x;
-            s_pre = p;
+            ff p = {0.f, 0.f};
+            for (int s = 0; s < sub; ++s) p = ff_add_f(p, subs[s].x);
+            s_pre = make_float2(p.hi, p.lo);
         }
         __syncthreads();
-        pre = s_pre;
+        pre = {s_pre.x, s_pre.y};
     }
     if (warp != 0) return;
     if (sub < 0) {
@@ -381,53 +391,61 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
             draw_scalar<ES>(it, tok0, wv[0], aq, ap);
         }
     }
-    double lt = 0.0;
-    for (int i = 0; i < ntok; ++i) lt += (double)wv[i];
-    double inc = lt;
+    ff lt = {0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < EPV; ++i)
+        if (i < ntok) lt = ff_add_f(lt, wv[i]);
+    ff inc = lt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-        if (lane >= o) inc += v;
+        const float h = __shfl_up_sync(0xFFFFFFFFu, inc.hi, o);
+        const float l = __shfl_up_sync(0xFFFFFFFFu, inc.lo, o);
+        if (lane >= o) inc = ff_add(inc, {h, l});
     }
-    double run = pre + (inc - lt);
+    ff run = ff_add(pre, ff_sub(inc, lt));
     int hit = -1;
-    double c_prev = run, c_hit = run;
-    for (int i = 0; i < ntok; ++i) {
-        const double nxt = run + (double)wv[i];
-        if (hit < 0 && wv[i] > 0.f && thr < nxt) {
-            hit = i;
-            c_prev = run;
-            c_hit = nxt;
+    ff c_prev = run, c_hit = run;
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) {
+        if (i < ntok) {
+            const ff nxt = ff_add_f(run, wv[i]);
+            if (hit < 0 && wv[i] > 0.f && ff_diff(thr, nxt) < 0.f) {
+                hit = i;
+                c_prev = run;
+                c_hit = nxt;
+            }
+            run = nxt;
         }
-        run = nxt;
     }
     const unsigned m = __ballot_sync(0xFFFFFFFFu, hit >= 0);
     int tstar;
-    double cp, ch;
+    float dprev, dhit;   // thr - C(t*-1) and C(t*) - thr
     if (m != 0) {
         const int src = __ffs(m) - 1;
         const int tok = tok0 + (ntok == 1 ? 0 : hit);
         tstar = __shfl_sync(0xFFFFFFFFu, tok, src);
-        cp = __shfl_sync(0xFFFFFFFFu, c_prev, src);
-        ch = __shfl_sync(0xFFFFFFFFu, c_hit, src);
+        const float dp = ff_diff(thr, c_prev), dh = ff_diff(c_hit, thr);
+        dprev = __shfl_sync(0xFFFFFFFFu, dp, src);
+        dhit = __shfl_sync(0xFFFFFFFFu, dh, src);
     } else {
         // rounding left thr past this sub-chunk: take its last positive weight, flag it
         int lastpos = -1;
-        for (int i = 0; i < ntok; ++i)
-            if (wv[i] > 0.f) lastpos = i;
+#pragma unroll
+        for (int i = 0; i < EPV; ++i)
+            if (i < ntok && wv[i] > 0.f) lastpos = i;
         const unsigned mm = __ballot_sync(0xFFFFFFFFu, lastpos >= 0);
         const int src = mm ? 31 - __clz(mm) : 0;
         const int tok = tok0 + (ntok == 1 ? 0 : max(lastpos, 0));
         tstar = __shfl_sync(0xFFFFFFFFu, tok, src);
-        cp = ch = __shfl_sync(0xFFFFFFFFu, run, src);
+        dprev = dhit = 0.f;
         ambiguous = true;
     }
     if (lane == 0) {
-        const double E = draw_error_bound(it, R, A);
-        if (thr - cp <= E || ch - thr <= E) ambiguous = true;
-        const bool near = (thr - cp) < 1e-6 * R || (ch - thr) < 1e-6 * R;
+        const float E = draw_error_bound(it, R.hi, A);
+        if (dprev <= E || dhit <= E) ambiguous = true;
+        const bool near = dprev < 1e-6f * R.hi || dhit < 1e-6f * R.hi;
         *it.out = tstar;
-        if (it.dbg_r) *it.dbg_r = R;
+        if (it.dbg_r) *it.dbg_r = (double)R.hi + (double)R.lo;
         stats_add(a.stats, &a.stats->draws, 1);
         if (near) stats_add(a.stats, &a.stats->near_boundary, 1);
         if (ambiguous && a.exact) {

@@ -80,11 +80,6 @@ struct ExactArgs {
     long long wait_limit;
 };
 
-__device__ __forceinline__ ff ff_mul(ff a, ff b) {
-    ff p = two_prod(a.hi, b.hi);
-    p.lo = __fmaf_rn(a.hi, b.lo, __fmaf_rn(a.lo, b.hi, p.lo));
-    return fast_two_sum(p.hi, p.lo);
-}
 
 // Bounded grid-wide barrier for a cooperative launch.  The counter is zeroed earlier in the call.
 __device__ __forceinline__ bool grid_barrier(unsigned *ctr, unsigned &target, long long limit) {
@@ -159,8 +154,7 @@ __device__ __forceinline__ ExactRow seq_row(const ExactArgs &a, int b, int slot)
 }
 
 // Weight of token v in a row: keep(v) * 2^(x c - r) * (sc on the top-F set), float-float.
-// Not inlined: one copy of the float-float exponential keeps the kernel inside the I-cache.
-static __device__ __noinline__ ff exact_w(const ExactRow &r, float x, int v, const float2 *tab) {
+__device__ __forceinline__ ff exact_w(const ExactRow &r, float x, int v, const float2 *tab) {
     if (!in_cut(x, v, r.cut_x, r.cut_id) || x == -INFINITY) return {0.f, 0.f};
     const ff y = ff_affine(x, r.c, {r.rf, 0.f});
     ff e = ff_exp2(y.hi, y.lo, tab);
@@ -180,6 +174,15 @@ __device__ __forceinline__ ExactDraw exact_draw_from(const DrawItem &d) {
     xd.out = d.out;
     xd.dbg_r = d.dbg_r;
     return xd;
+}
+
+// Element k of a 16-byte vector, for loops that are not unrolled (no local-memory array).
+template <int ES>
+__device__ __forceinline__ float elem_of(const uint4 &w, int k) {
+    const int j = ES == 4 ? k : (k >> 1);
+    const unsigned b = j == 0 ? w.x : j == 1 ? w.y : j == 2 ? w.z : w.w;
+    if (ES == 4) return __uint_as_float(b);
+    return (k & 1) ? bf16_hi(b) : bf16_lo(b);
 }
 
 template <int ES>
@@ -391,11 +394,10 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
                 const int vi = sb * 32 + lane;
                 ff aq = {0.f, 0.f}, ap = {0.f, 0.f};
                 if (vi < n_vec) {
-                    float xq[EPV], xp[EPV];
-                    load_vec<ES>(d.q.row, vi, xq);
-                    if (d.has_p) load_vec<ES>(d.p.row, vi, xp);
+                    const uint4 wq = __ldg(reinterpret_cast<const uint4 *>(d.q.row) + vi);
+                    const uint4 wp = d.has_p ? __ldg(reinterpret_cast<const uint4 *>(d.p.row) + vi) : wq;
 #pragma unroll 1
-                    for (int k = 0; k < EPV; ++k) token(xq[k], d.has_p ? xp[k] : xq[k], vi * EPV + k, aq, ap);
+                    for (int k = 0; k < EPV; ++k) token(elem_of<ES>(wq, k), elem_of<ES>(wp, k), vi * EPV + k, aq, ap);
                 }
                 aq = warp_sum_ff(aq);
                 ap = warp_sum_ff(ap);

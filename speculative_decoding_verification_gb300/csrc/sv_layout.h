@@ -19,7 +19,7 @@ constexpr int kMaxSplit = 64;               // most chunks per row
 constexpr int kUnitTarget = 1024;           // at least about this many (row, chunk) units
 constexpr int kExactSplit = 16;             // chunks per row in the float-float tier
 constexpr int kExactCap = 2048;             // most queued items per call in the float-float tier
-constexpr int kExactGroup = 2;              // draw sub-chunks per warp unit in the float-float tier
+constexpr int kExactGroup = 1;              // draw sub-chunks per warp unit in the float-float tier
 constexpr long long kWaitLimitCycles = 4000000000LL;   // ~2 s at 2 GHz: bounded barrier waits
 constexpr unsigned kSuspendHintNs = 100000;  // a waiting thread sleeps at most this long per try
 
@@ -61,13 +61,13 @@ constexpr int kNoRef = -(1 << 30);
 
 // Combined statistics of one row.
 struct RowStat {
-    double g;       // log2 normaliser: log2 sum_v 2^(x_v c), c = log2(e)/T   (NaN for greedy rows)
-    double err;     // certified relative error bound of 2^g (float32 tier)
-    double S;       // sum_v 2^(x_v c - r)
-    float maxv;
+    float s_hi, s_lo;   // S = sum_v 2^(x_v c - r) as float-float (sampled rows), c = log2(e)/T
+    float err;          // certified relative error bound of S (float32 tier)
+    float maxv;         // greedy rows: the maximum and its lowest index
     int argmax;
-    int r;
+    int r;              // the integer reference exponent r
     int flags;
+    int pad;
 };
 
 // Nucleus (top-p) cut of a row: token v is kept iff x_v > cut_x or (x_v == cut_x and v <= cut_id).
@@ -78,7 +78,7 @@ struct NucleusCut {
     double mass;
     double log2_mass;
     int ambiguous;  // the float32 tier could not certify the cut
-    int pad;
+    float mass_f;   // mass rounded to float32 (for float32 consumers)
 };
 
 // Saguaro top-F set of a draft row: v in D iff x_v > top_x or (x_v == top_x and v <= top_id).
@@ -88,6 +88,8 @@ struct TopSet {
     double p_d;     // probability mass of D (after temperature and top-p) before scaling
     double z;       // normaliser after scaling: 1 - (1 - C) p_d
     double z_err;   // relative error bound of z (float32 tier)
+    float z_f;      // z rounded to float32
+    float z_err_f;  // z_err rounded up to float32
 };
 
 // A row as seen by the draw pass: weight(v) = keep(v) * 2^(x_v c - r) * inv_s * (in_D ? sc_d : 1).

@@ -81,8 +81,8 @@ __global__ void __launch_bounds__(kThreads) k_topk_finish(const TopKArgs a) {
     double lse = 0.0;
     int bad = 0;
     if (lane == 0) {
-        bad = st.flags != 0 || !(st.S > 0.0) || !isfinite(st.g);
-        lse = st.g * kLn2;
+        bad = st.flags != 0 || !rs_sampled_ok(st);
+        lse = bad ? 0.0 : rs_g(st) * kLn2;
         if (bad) report_error(a.stats, SV_ERR_NONFINITE, (int)r);
         else stats_add(a.stats, &a.stats->rows, 1);
     }

@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kThreads) k_sample_items(const SampleArgs a, l
     const RowStat rs = combine_row(a.part + (size_t)r * a.n_split * kWarps, a.n_split * kWarps, greedy);
     if (lane != 0) return;
     a.rowstat[r] = rs;
-    const bool bad = rs.flags != 0 || (greedy ? !isfinite(rs.maxv) : (!(rs.S > 0.0) || !isfinite(rs.g)));
+    const bool bad = rs.flags != 0 || (greedy ? !isfinite(rs.maxv) : !rs_sampled_ok(rs));
     if (bad) {
         report_error(a.stats, SV_ERR_NONFINITE, (int)r);
         a.tokens[r] = -1;
@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kThreads) k_sample_items(const SampleArgs a, l
     stats_add(a.stats, &a.stats->rows, 1);
     if (a.debug) {
         double *dbg = a.debug + (size_t)r * 4;
-        dbg[0] = greedy ? NAN : rs.g * kLn2;
+        dbg[0] = greedy ? NAN : rs_g(rs) * kLn2;
         dbg[1] = (a.top && !greedy) ? a.top[r].p_d : 0.0;
         dbg[2] = (a.top && !greedy) ? a.top[r].z : 1.0;
         dbg[3] = (a.nuc && !greedy) ? a.nuc[r].mass : 1.0;
@@ -79,7 +79,8 @@ __global__ void __launch_bounds__(kThreads) k_sample_items(const SampleArgs a, l
         d.row = row;
         log2e_over(T, d.c_hi, d.c_lo);
         d.rf = (float)rs.r;
-        double norm = rs.S, err = rs.err;
+        float norm = rs.s_hi;
+        double err = rs_err(rs) + 4.0 * kU32;   // S_lo dropped, products, reciprocal
         d.cut_x = -INFINITY;
         d.cut_id = 0x7FFFFFFF;
         d.top_x = INFINITY;
@@ -88,17 +89,17 @@ __global__ void __launch_bounds__(kThreads) k_sample_items(const SampleArgs a, l
         if (a.nuc) {
             d.cut_x = a.nuc[r].cut_x;
             d.cut_id = a.nuc[r].cut_id;
-            norm *= a.nuc[r].mass;
-            err += 2.0 * rs.err + 1e-12;
+            norm = __fmul_rn(norm, a.nuc[r].mass_f);
+            err += 2.0 * rs_err(rs) + kU32 + 1e-12;
         }
         if (a.top) {
             d.top_x = a.top[r].top_x;
             d.top_id = a.top[r].top_id;
             d.sc_d = a.C;
-            norm *= a.top[r].z;
-            err += a.top[r].z_err;
+            norm = __fmul_rn(norm, a.top[r].z_f);
+            err += (double)a.top[r].z_err_f + kU32;
         }
-        d.inv_s = (float)(1.0 / norm);
+        d.inv_s = __frcp_rn(norm);
         d.pad = 0;
         d.norm_err = err;
     }

@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
     none.mass = 1.0;
     none.log2_mass = 0.0;
     none.ambiguous = 0;
-    none.pad = 0;
+    none.mass_f = 1.0f;
     if (!(tp < 1.0f) || !(T >= 1e-3f && T <= 1e3f)) {   // off, greedy or invalid temperature
         if (threadIdx.x == 0) a.nuc[rid] = none;
         return;
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
     }
     __syncthreads();
     const RowStat st = s_rs;
-    if (!(st.S > 0.0) || st.flags) {   // reported by the accept / sampling kernels
+    if (!rs_sampled_ok(st) || st.flags) {   // reported by the accept / sampling kernels
         if (threadIdx.x == 0) a.nuc[rid] = none;
         return;
     }
@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
     const bool ambiguous = (target - cum_lo) <= E || (cum_hi - target) <= E;
     NucleusCut out;
     out.ambiguous = ambiguous ? 1 : 0;
-    out.pad = 0;
+    out.mass_f = 1.0f;
     if (!ambiguous) {
         out.cut_x = xstar;
         out.cut_id = ordered_ties<ES>(row, a.V, kstar, jt, nullptr, s_warp, &s_last);
@@ -474,6 +474,7 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
         }
     }
     out.log2_mass = log2(out.mass);
+    out.mass_f = (float)out.mass;
     if (threadIdx.x == 0) a.nuc[rid] = out;
 }
 
@@ -534,6 +535,8 @@ __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
     none.p_d = 0.0;
     none.z = 1.0;
     none.z_err = 0.0;
+    none.z_f = 1.0f;
+    none.z_err_f = 0.0f;
     if (!(T >= 1e-3f && T <= 1e3f)) {   // greedy or invalid: no transform
         if (threadIdx.x == 0) a.top[rid] = none;
         return;
@@ -545,7 +548,7 @@ __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
     }
     __syncthreads();
     const RowStat st = s_rs;
-    if (!(st.S > 0.0) || st.flags) {
+    if (!rs_sampled_ok(st) || st.flags) {
         if (threadIdx.x == 0) a.top[rid] = none;
         return;
     }
@@ -581,11 +584,13 @@ __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
         TopSet t;
         t.top_x = xstar;
         t.top_id = last;
-        t.p_d = fmin(1.0, tot / (st.S * mass_n));
+        t.p_d = fmin(1.0, tot / (rs_S(st) * mass_n));
         t.z = 1.0 - (1.0 - (double)a.C) * t.p_d;
         // p_d is a ratio of two sums of the same pass: relative error <= 2 err (x2 with top-p)
-        const double pd_rel = (a.nuc ? 4.04 : 2.02) * st.err;
+        const double pd_rel = (a.nuc ? 4.04 : 2.02) * rs_err(st);
         t.z_err = t.z > 0.0 ? (1.0 - (double)a.C) * t.p_d * pd_rel / t.z + 1e-12 : 1.0;
+        t.z_f = (float)t.z;
+        t.z_err_f = (float)t.z_err * (1.0f + 0x1p-20f);
         a.top[rid] = t;
     }
 }

@@ -522,17 +522,25 @@ __device__ __forceinline__ RowStat combine_row(const WarpPartial *P, int np, boo
     r.maxv = m;
     r.argmax = am;
     r.r = rmax;
-    if (greedy) {
-        r.S = 0.0;
-        r.g = NAN;
-        r.err = 0.0;
-    } else if (lane == 0) {
-        r.S = (double)s.hi + (double)s.lo;
-        r.g = (double)rmax + log2(r.S);
-        // ex2 error + exponent rounding (|y| weighted) + float32 summation (tree + compensated)
-        r.err = kEx2RelErr + 1.02 * kYRound * (s.hi > 0.f ? (double)(a / s.hi) : 0.0) + 6.0 * kU32 + 1e-12;
+    r.pad = 0;
+    r.s_hi = r.s_lo = r.err = 0.f;
+    if (!greedy && lane == 0) {
+        const ff S = fast_two_sum(s.hi, s.lo);
+        r.s_hi = S.hi;
+        r.s_lo = S.lo;
+        // ex2 error + exponent rounding (|y| weighted) + float32 summation (tree + compensated);
+        // evaluated in float32 and rounded up by 2^-20 to cover that evaluation
+        const float ay = S.hi > 0.f ? __fdiv_rn(a, S.hi) : 0.f;
+        r.err = (float)(kEx2RelErr + 6.0 * kU32 + 1e-12) + (float)(1.02 * kYRound) * ay;
+        r.err *= 1.0f + 0x1p-20f;
     }
-    return r;   // S, g, err valid in lane 0 (sampled rows)
+    return r;   // s_hi, s_lo, err valid in lane 0 (sampled rows)
 }
+
+// Double-precision views of a row's statistics, for kernels off the per-sequence hot path.
+__device__ __forceinline__ double rs_S(const RowStat &r) { return (double)r.s_hi + (double)r.s_lo; }
+__device__ __forceinline__ double rs_g(const RowStat &r) { return (double)r.r + log2(rs_S(r)); }
+__device__ __forceinline__ double rs_err(const RowStat &r) { return (double)r.err; }
+__device__ __forceinline__ bool rs_sampled_ok(const RowStat &r) { return r.s_hi > 0.f && r.s_hi < INFINITY; }
 
 }  // namespace sv

@@ -48,21 +48,22 @@ struct AcceptArgs {
     Counters *counters;
 };
 
+// Draw parameters of one row, float32 only: inv_s = 1 / (S * nucleus mass * Saguaro normaliser).
 __device__ __forceinline__ DrawRow draw_row(const char *row, float T, const RowStat &rs, const NucleusCut *nc,
                                             const TopSet *ts, float sag_C) {
     DrawRow d;
     d.row = row;
     log2e_over(T, d.c_hi, d.c_lo);
     d.rf = (float)rs.r;
-    double norm = rs.S;
-    double err = rs.err;
+    float norm = rs.s_hi;
+    double err = (double)rs.err + 4.0 * kU32;   // S_lo dropped, products, reciprocal
     d.cut_x = -INFINITY;
     d.cut_id = 0x7FFFFFFF;
     if (nc) {
         d.cut_x = nc->cut_x;
         d.cut_id = nc->cut_id;
-        norm *= nc->mass;
-        err += 2.0 * rs.err + 1e-12;   // the kept mass is a ratio of two sums of the same pass
+        norm = __fmul_rn(norm, nc->mass_f);
+        err += 2.0 * (double)rs.err + kU32 + 1e-12;   // the kept mass is a ratio of two sums of the same pass
     }
     d.top_x = INFINITY;
     d.top_id = -1;
@@ -71,10 +72,10 @@ __device__ __forceinline__ DrawRow draw_row(const char *row, float T, const RowS
         d.top_x = ts->top_x;
         d.top_id = ts->top_id;
         d.sc_d = sag_C;
-        norm *= ts->z;
-        err += ts->z_err;
+        norm = __fmul_rn(norm, ts->z_f);
+        err += (double)ts->z_err_f + kU32;
     }
-    d.inv_s = (float)(1.0 / norm);
+    d.inv_s = __frcp_rn(norm);
     d.pad = 0;
     d.norm_err = err;
     return d;
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
         if (lane == 0) {
             rs[i] = r;
             a.rowstat[rid] = r;
-            const bool bad = (r.flags != 0) || (greedy ? !isfinite(r.maxv) : !(r.S > 0.0) || !isfinite(r.g));
+            const bool bad = (r.flags != 0) || (greedy ? !isfinite(r.maxv) : !rs_sampled_ok(r));
             if (bad) {
                 atomicOr(&s_err, 1);
                 report_error(a.stats, SV_ERR_NONFINITE, (int)rid);
@@ -124,12 +125,18 @@ __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
         return;
     }
 
-    // ---- accept tests (lane j tests position j+1) ----
-    const double c = greedy ? 0.0 : 1.4426950408889634074 / (double)T;
-    const double sag_l2c = log2((double)a.sag_C);
+    // ---- accept tests (lane j tests position j+1), float32 / float-float only ----
+    // ratio = q(s)/p(s) = 2^(y_q - y_p) * (S_p m_p z_p) / (S_q m_q C_s) with y = x c - r, S the
+    // row sums, m the nucleus masses, z the Saguaro normaliser and C_s = C on the top-F set.
+    // y_q - y_p is formed in float-float; its float32 exponential, the products and the
+    // quotient carry kEx2RelErr + 8u, the row sums err_q + err_p, the masses 2(err_q + err_p)
+    // and the normaliser z_err; u < ratio is certain outside ratio (1 -+ delta).
+    float c_hi = 0.f, c_lo = 0.f;
+    if (!greedy) log2e_over(T, c_hi, c_lo);
     int s = -1;
     bool acc = false, amb = false, near = false, badtok = false;
-    double q_s = NAN, p_s = NAN, ratio = NAN;
+    bool keep_q = false, keep_p = false, in_top = false;
+    float ratio = NAN;
     if (lane < K) {
         s = a.tokens[(size_t)b * K + lane];
         badtok = s < 0 || s >= V;
@@ -145,33 +152,48 @@ __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
                 const float xt = load_elem<ES>(trow, s);
                 const float xd = load_elem<ES>(drow, s);
                 const RowStat &rq = rs[lane], &rp = rs[n_t + lane];
-                double lq = (double)xt * c - rq.g;
-                double lp = (double)xd * c - rp.g;
-                double delta = rq.err + rp.err;
+                float num = rp.s_hi, den = rq.s_hi;
+                float delta = (float)(kEx2RelErr + 8.0 * kU32 + 1e-10) + rq.err + rp.err;
+                keep_q = xt != -INFINITY;
+                keep_p = xd != -INFINITY;
                 if (a.nuc) {
-                    const NucleusCut nq = a.nuc[rid_t], np = a.nuc[rid_d];
-                    lq = (xt > nq.cut_x || (xt == nq.cut_x && s <= nq.cut_id)) ? lq - nq.log2_mass : -INFINITY;
-                    lp = (xd > np.cut_x || (xd == np.cut_x && s <= np.cut_id)) ? lp - np.log2_mass : -INFINITY;
-                    delta += 2.0 * (rq.err + rp.err);
+                    const NucleusCut &nq = a.nuc[rid_t], &np = a.nuc[rid_d];
+                    keep_q = keep_q && (xt > nq.cut_x || (xt == nq.cut_x && s <= nq.cut_id));
+                    keep_p = keep_p && (xd > np.cut_x || (xd == np.cut_x && s <= np.cut_id));
+                    num = __fmul_rn(num, np.mass_f);
+                    den = __fmul_rn(den, nq.mass_f);
+                    delta += 2.0f * (rq.err + rp.err) + (float)(2.0 * kU32);
                 }
                 if (a.sag_on && a.top) {
-                    const TopSet t = a.top[rid_d];
-                    if (xd > t.top_x || (xd == t.top_x && s <= t.top_id)) lp += sag_l2c;
-                    lp -= log2(t.z);
-                    delta += t.z_err;
+                    const TopSet &t = a.top[rid_d];
+                    in_top = xd > t.top_x || (xd == t.top_x && s <= t.top_id);
+                    num = __fmul_rn(num, t.z_f);
+                    if (in_top) den = __fmul_rn(den, a.sag_C);
+                    delta += t.z_err_f + (float)kU32;
                 }
-                if (lp == -INFINITY) ratio = (lq == -INFINITY) ? 0.0 : INFINITY;
-                else ratio = exp2(lq - lp);
-                q_s = exp2(lq);
-                p_s = exp2(lp);
-                const double r = fmin(1.0, ratio);
-                delta = 1.01 * delta + 1e-13;
-                const double lo = fmin(1.0, ratio * (1.0 - delta));
-                const double hi = fmin(1.0, ratio * (1.0 + delta));
-                const double u = a.uniforms[(size_t)b * (K + 1) + lane];
-                acc = u < r;
-                amb = (u >= lo) && (u < hi);
-                near = fabs(u - r) < 1e-6;
+                if (!keep_p) {
+                    ratio = keep_q ? INFINITY : 0.0f;
+                } else if (!keep_q) {
+                    ratio = 0.0f;
+                } else {
+                    const ff c = {c_hi, c_lo};
+                    const ff yq = ff_affine(xt, c, {(float)rq.r, 0.f});
+                    const ff yp = ff_affine(xd, c, {(float)rp.r, 0.f});
+                    const ff dy = ff_sub(yq, yp);
+                    delta += 1e-12f * (fabsf(yq.hi) + fabsf(yp.hi));   // float-float y and c
+                    const float e = ex2_fast(dy.hi) * fmaf(dy.lo, (float)kLn2, 1.0f);
+                    ratio = e * __fdiv_rn(num, den);
+                }
+                delta *= 1.01f;
+                const float rr = fminf(1.0f, ratio);
+                const float lo = fminf(1.0f, ratio * (1.0f - delta));
+                const float hi = fminf(1.0f, ratio * (1.0f + delta));
+                const float u = __double2float_rn(a.uniforms[(size_t)b * (K + 1) + lane]);
+                // u is rounded to float32 (relative error 2^-24, inside delta's 8u); a ratio that
+                // underflowed is decided by the float-float tier unless u is clearly above it
+                acc = u < rr;
+                amb = (u >= lo && u < hi) || (keep_q && keep_p && ratio < 0x1p-100f && u < 0x1p-90f);
+                near = fabsf(u - rr) < 1e-6f;
             }
         }
     }
@@ -203,14 +225,37 @@ __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
         }
     }
     if (a.debug) {
+        // reference values in float64 (debug output only)
+        const double cd = greedy ? 0.0 : 1.4426950408889634074 / (double)T;
+        double q_s = NAN, p_s = NAN, rat = NAN;
+        if (!greedy && lane < K && !badtok) {
+            const long long rid_t = (long long)b * n_t + lane;
+            const long long rid_d = a.n_rows0 + (long long)b * K + lane;
+            const char *trow = a.tgt.base + ((long long)b * a.tgt.rows_per_seq + lane) * a.tgt.pitch_bytes;
+            const char *drow = a.drf.base + ((long long)b * a.drf.rows_per_seq + lane) * a.drf.pitch_bytes;
+            const float xt = load_elem<ES>(trow, s), xd = load_elem<ES>(drow, s);
+            double lq = keep_q ? (double)xt * cd - rs_g(rs[lane]) : -INFINITY;
+            double lp = keep_p ? (double)xd * cd - rs_g(rs[n_t + lane]) : -INFINITY;
+            if (a.nuc) {
+                lq -= a.nuc[rid_t].log2_mass;
+                lp -= a.nuc[rid_d].log2_mass;
+            }
+            if (a.sag_on && a.top) {
+                if (in_top) lp += log2((double)a.sag_C);
+                lp -= log2(a.top[rid_d].z);
+            }
+            q_s = exp2(lq);
+            p_s = exp2(lp);
+            rat = (lp == -INFINITY) ? (lq == -INFINITY ? 0.0 : INFINITY) : exp2(lq - lp);
+        }
         for (int j = lane; j <= K; j += 32) {
             double *dbg = a.debug + ((size_t)b * (K + 1) + j) * SV_DEBUG_FIELDS;
             const long long rid_t = (long long)b * n_t + j;
-            dbg[SV_DBG_LSE_Q] = greedy ? NAN : rs[j].g * kLn2;
-            dbg[SV_DBG_LSE_P] = (greedy || j >= K) ? NAN : rs[n_t + j].g * kLn2;
+            dbg[SV_DBG_LSE_Q] = greedy ? NAN : rs_g(rs[j]) * kLn2;
+            dbg[SV_DBG_LSE_P] = (greedy || j >= K) ? NAN : rs_g(rs[n_t + j]) * kLn2;
             dbg[SV_DBG_Q_S] = j < K ? q_s : NAN;
             dbg[SV_DBG_P_S] = j < K ? p_s : NAN;
-            dbg[SV_DBG_RATIO] = j < K ? ratio : NAN;
+            dbg[SV_DBG_RATIO] = j < K ? rat : NAN;
             dbg[SV_DBG_MASS_Q] = (greedy || !a.nuc) ? 1.0 : a.nuc[rid_t].mass;
             dbg[SV_DBG_MASS_P] = (greedy || !a.nuc || j >= K) ? 1.0 : a.nuc[a.n_rows0 + (long long)b * K + j].mass;
             dbg[SV_DBG_R] = NAN;

@@ -14,6 +14,8 @@
 #pragma once
 
 #include "sv_device.cuh"
+#include "sv_host.h"
+#include "sv_stats.cuh"
 
 namespace sv {
 
@@ -23,17 +25,16 @@ struct DrawArgs {
     int V, n_vec, n_sub;        // n_sub = vector sub-chunks + 1 tail sub-chunk
     int n_split;                // chunks per row
     int subs_per_chunk;         // vector sub-chunks per chunk
-    float2 *subs;               // [item][n_sub] = (sum w, sum of error weights)
+    float *subs;                // [item][n_sub] = float32 sum of w over the sub-chunk
     ExactItem *exact;           // exact-tier queue (may be nullptr: no re-resolution)
     int *exact_unc;             // per queued item: uncertain-token count, zeroed at push
     sv_stats *stats;
     long long wait_limit;
 };
 
-// Per-element weight and error weight (identical in both passes).
+// Per-element weight (identical in both passes).
 template <bool HAS_P, bool FILT>
-__device__ __forceinline__ void draw_weight(const DrawItem &it, float xq, float xp, int v, float &w, float &aq,
-                                            float &ap) {
+__device__ __forceinline__ float draw_weight(const DrawItem &it, float xq, float xp, int v) {
     const float yq = fmaf(xq, it.q.c_lo, fmaf(xq, it.q.c_hi, -it.q.rf));
     float eq = ex2_fast(yq);
     float scq = it.q.inv_s;
@@ -43,7 +44,6 @@ __device__ __forceinline__ void draw_weight(const DrawItem &it, float xq, float 
         eq = keep ? eq : 0.0f;
         scq = in_d ? __fmul_rn(scq, it.q.sc_d) : scq;
     }
-    aq = eq * fabsf(yq);
     if (HAS_P) {
         const float yp = fmaf(xp, it.p.c_lo, fmaf(xp, it.p.c_hi, -it.p.rf));
         float ep = ex2_fast(yp);
@@ -54,187 +54,206 @@ __device__ __forceinline__ void draw_weight(const DrawItem &it, float xq, float 
             ep = keep ? ep : 0.0f;
             sc = in_d ? __fmul_rn(sc, it.p.sc_d) : sc;
         }
-        ap = ep * fabsf(yp);
         const float pv = __fmul_rn(ep, sc);
-        w = fmaxf(__fmaf_rn(eq, scq, -pv), 0.0f);
-    } else {
-        ap = 0.0f;
-        w = __fmul_rn(eq, scq);
+        return fmaxf(__fmaf_rn(eq, scq, -pv), 0.0f);
     }
+    return __fmul_rn(eq, scq);
 }
 
-// Weights of one vector (EPV tokens from element e0); returns the tree sum, fills aq/ap sums.
+// Weights of one vector (EPV tokens from element e0); returns their tree sum.
 template <int ES, bool HAS_P, bool FILT>
-__device__ __forceinline__ float vec_weights(const DrawItem &it, uint4 wq, uint4 wp, int e0, float (&wv)[16 / ES],
-                                             float &aq_sum, float &ap_sum) {
+__device__ __forceinline__ float vec_weights(const DrawItem &it, uint4 wq, uint4 wp, int e0, float (&wv)[16 / ES]) {
     constexpr int EPV = 16 / ES;
     float xq[EPV], xp[EPV];
     unpack<ES>(wq, xq);
     unpack<ES>(wp, xp);
-    float aq[EPV], ap[EPV];
 #pragma unroll
-    for (int i = 0; i < EPV; ++i) draw_weight<HAS_P, FILT>(it, xq[i], xp[i], e0 + i, wv[i], aq[i], ap[i]);
-    float s;
+    for (int i = 0; i < EPV; ++i) wv[i] = draw_weight<HAS_P, FILT>(it, xq[i], xp[i], e0 + i);
     if constexpr (EPV == 8) {
-        s = ((wv[0] + wv[1]) + (wv[2] + wv[3])) + ((wv[4] + wv[5]) + (wv[6] + wv[7]));
-        aq_sum = ((aq[0] + aq[1]) + (aq[2] + aq[3])) + ((aq[4] + aq[5]) + (aq[6] + aq[7]));
-        ap_sum = ((ap[0] + ap[1]) + (ap[2] + ap[3])) + ((ap[4] + ap[5]) + (ap[6] + ap[7]));
+        return ((wv[0] + wv[1]) + (wv[2] + wv[3])) + ((wv[4] + wv[5]) + (wv[6] + wv[7]));
     } else {
-        s = (wv[0] + wv[1]) + (wv[2] + wv[3]);
-        aq_sum = (aq[0] + aq[1]) + (aq[2] + aq[3]);
-        ap_sum = (ap[0] + ap[1]) + (ap[2] + ap[3]);
+        return (wv[0] + wv[1]) + (wv[2] + wv[3]);
     }
-    return s;
 }
 
+// One consumer warp's share of a tile: 32-vector groups g = warp, warp + kWarps, ...; each
+// group is one sub-chunk, whose sum lane 0 writes.
 template <int ES, bool HAS_P, bool FILT>
 __device__ __forceinline__ void draw_tile(const DrawItem &it, const unsigned char *bq, const unsigned char *bp,
-                                          int fv, int nv, float2 *subs_item) {
+                                          int fv, int nv, float *subs_item) {
     constexpr int EPV = 16 / ES;
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll 1
-    for (int g = 0; g < kTileBytes / 16 / kThreads; ++g) {
-        const int vbase = g * kThreads + (tid & ~31);   // first vector of this warp's sub-chunk
-        if (vbase >= nv) break;                          // warp-uniform
-        const int vi = vbase + lane;
-        float w = 0.f, aq = 0.f, ap = 0.f;
+    for (int g = warp; g * 32 < nv; g += kWarps) {
+        const int vi = g * 32 + lane;
+        float w = 0.f;
         if (vi < nv) {
             const uint4 q = lds128(bq + vi * 16);
             const uint4 p = HAS_P ? lds128(bp + vi * 16) : q;
             float wv[EPV];
-            w = vec_weights<ES, HAS_P, FILT>(it, q, p, (fv + vi) * EPV, wv, aq, ap);
+            w = vec_weights<ES, HAS_P, FILT>(it, q, p, (fv + vi) * EPV, wv);
         }
-        const float a = fmaf(aq, it.q.inv_s, ap * it.p.inv_s);
         const float W = warp_sum_f(w);
-        const float A = warp_sum_f(HAS_P ? a : aq * it.q.inv_s);
-        if (lane == 0) subs_item[(fv + vbase) / 32] = make_float2(W, A);
+        if (lane == 0) subs_item[(fv + g * 32) / 32] = W;
     }
 }
 
 template <int ES>
-__device__ __forceinline__ void draw_scalar(const DrawItem &it, int v, float &w, float &aq, float &ap) {
+__device__ __forceinline__ float draw_scalar(const DrawItem &it, int v) {
     const float xq = load_elem<ES>(it.q.row, v);
     const float xp = it.has_p ? load_elem<ES>(it.p.row, v) : xq;
-    if (it.has_p) {
-        if (it.filt) draw_weight<true, true>(it, xq, xp, v, w, aq, ap);
-        else draw_weight<true, false>(it, xq, xp, v, w, aq, ap);
-    } else {
-        if (it.filt) draw_weight<false, true>(it, xq, xp, v, w, aq, ap);
-        else draw_weight<false, false>(it, xq, xp, v, w, aq, ap);
-    }
+    if (it.has_p) return it.filt ? draw_weight<true, true>(it, xq, xp, v) : draw_weight<true, false>(it, xq, xp, v);
+    return it.filt ? draw_weight<false, true>(it, xq, xp, v) : draw_weight<false, false>(it, xq, xp, v);
 }
 
+// One pipeline stage of the draw pass: a q tile and (with a draft row) a p tile of one item.
+struct DrawMeta {
+    int d;            // item
+    int fv, nv;       // first vector of the tile within the row, vectors in the tile
+    int flags;        // kTileLast (last tile of the item's last chunk: also the scalar tail) | kTileEnd
+};
+constexpr int kDrawCtlBytes = 512;
+static_assert(2 * kDrawStages * 8 + 16 + kDrawStages * (int)sizeof(DrawMeta) <= kDrawCtlBytes, "control block");
+constexpr size_t kDrawSmemBytes = (size_t)kDrawCtlBytes + (size_t)2 * kDrawStages * kTileBytes;
+
+// Pass 1, warp-specialised like the statistics pass: the producer warp takes (item, chunk)
+// units from a global counter and streams each unit's q and p tiles into shared memory; eight
+// consumer warps weight the tokens and write one float32 sum per 32-vector sub-chunk.
 template <int ES>
-__global__ void __launch_bounds__(kThreads, 2) k_draw_sums(const DrawArgs a) {
+__global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-    unsigned char *tiles = smem + 128;          // stage s: q tile at 2s, p tile at 2s+1
+    uint64_t *empty = full + kDrawStages;
+    int *abort_flag = reinterpret_cast<int *>(smem + 2 * kDrawStages * 8);
+    DrawMeta *meta = reinterpret_cast<DrawMeta *>(smem + 2 * kDrawStages * 8 + 16);
+    unsigned char *tiles = smem + kDrawCtlBytes;   // stage s: q tile at 2s, p tile at 2s+1
     const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
     const int n_items = *reinterpret_cast<volatile int *>(&a.counters->n_draws);
-    const long long n_units = (long long)n_items * a.n_split;
-    if ((long long)blockIdx.x >= n_units) return;
     const int n_vsub = a.n_sub - 1;
 
     if (tid == 0) {
-        for (int s = 0; s < kDrawStages; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < kDrawStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
+        }
+        *abort_flag = 0;
         fence_barrier_init();
     }
     __syncthreads();
 
-    auto unit_range = [&](long long u, int &d, int &c, int &v0, int &v1) {
-        d = (int)(u / a.n_split);
-        c = (int)(u - (long long)d * a.n_split);
-        const int s0 = min(c * a.subs_per_chunk, n_vsub);
-        const int s1 = min(s0 + a.subs_per_chunk, n_vsub);
-        v0 = s0 * 32;
-        v1 = min(s1 * 32, a.n_vec);
-        if (v1 < v0) v1 = v0;
-    };
-
-    // producer (thread 0)
-    long long pu = blockIdx.x;
-    int pt = 0;
-    long long issued = 0;
-    const uint64_t policy = policy_evict_first();
-    auto p_issue = [&](int stage) {
-        while (pu < n_units) {
-            int d, c, v0, v1;
-            unit_range(pu, d, c, v0, v1);
-            const int nt = (v1 - v0 + 1023) / 1024;
-            if (pt < nt) {
-                const DrawItem &it = a.items[d];
-                const int fv = v0 + pt * 1024;
-                const int nv = min(1024, v1 - fv);
-                const uint32_t bytes = (uint32_t)nv * 16u;
-                mbar_arrive_expect_tx(&full[stage], it.has_p ? 2u * bytes : bytes);
-                bulk_load_stream(tiles + (2 * stage) * kTileBytes, it.q.row + (size_t)fv * 16, bytes, &full[stage],
-                                 policy);
-                if (it.has_p)
-                    bulk_load_stream(tiles + (2 * stage + 1) * kTileBytes, it.p.row + (size_t)fv * 16, bytes,
-                                     &full[stage], policy);
-                ++pt;
-                ++issued;
-                return;
-            }
-            pu += gridDim.x;
-            pt = 0;
-        }
-    };
-    if (tid == 0)
-        for (int s = 0; s < kDrawStages; ++s) p_issue(s);
-
-    long long itc = 0;
-    for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
-        int d, c, v0, v1;
-        unit_range(u, d, c, v0, v1);
-        const DrawItem it = a.items[d];
-        float2 *subs_item = a.subs + (size_t)d * a.n_sub;
-        const int nt = (v1 - v0 + 1023) / 1024;
-        for (int t = 0; t < nt; ++t, ++itc) {
-            const int st = (int)(itc % kDrawStages);
-            const uint32_t par = (uint32_t)((itc / kDrawStages) & 1);
-            const bool ok = mbar_wait_bounded(&full[st], par, a.wait_limit);
-            if (ok) {
-                const int fv = v0 + t * 1024;
-                const int nv = min(1024, v1 - fv);
-                const unsigned char *bq = tiles + (2 * st) * kTileBytes;
-                const unsigned char *bp = bq + kTileBytes;
-                if (it.has_p) {
-                    if (it.filt) draw_tile<ES, true, true>(it, bq, bp, fv, nv, subs_item);
-                    else draw_tile<ES, true, false>(it, bq, bp, fv, nv, subs_item);
-                } else {
-                    if (it.filt) draw_tile<ES, false, true>(it, bq, bp, fv, nv, subs_item);
-                    else draw_tile<ES, false, false>(it, bq, bp, fv, nv, subs_item);
+    if (warp == kWarps) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            const uint64_t policy = policy_evict_first();
+            const long long n_units = (long long)n_items * a.n_split;
+            long long in_flight[kDrawStages];
+            for (int s = 0; s < kDrawStages; ++s) in_flight[s] = -1;
+            long long it = 0;
+            bool ok = true;
+            while (ok) {
+                const long long u = atomicAdd(&a.counters->next_draw_unit, 1);
+                const bool have = u < n_units;
+                int d = 0, c = 0, v0 = 0, v1 = 0;
+                const DrawItem *item = nullptr;
+                if (have) {
+                    d = (int)(u / a.n_split);
+                    c = (int)(u - (long long)d * a.n_split);
+                    const int s0 = min(c * a.subs_per_chunk, n_vsub), s1 = min(s0 + a.subs_per_chunk, n_vsub);
+                    v0 = s0 * 32;
+                    v1 = max(v0, min(s1 * 32, a.n_vec));
+                    item = a.items + d;
+                }
+                const int nt = have ? max((v1 - v0 + kTileBytes / 16 - 1) / (kTileBytes / 16), 1) : 1;
+                for (int t = 0; t < nt; ++t, ++it) {
+                    const int st = (int)(it % kDrawStages);
+                    if (it >= kDrawStages) {
+                        const uint32_t par = (uint32_t)(((it / kDrawStages) - 1) & 1);
+                        if (!mbar_wait_or_abort(&empty[st], par, abort_flag, a.wait_limit)) {
+                            if (atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
+                            ok = false;
+                            break;
+                        }
+                    }
+                    in_flight[st] = -1;
+                    DrawMeta m;
+                    if (!have) {
+                        m.flags = kTileEnd;
+                        meta[st] = m;
+                        mbar_arrive(&full[st]);
+                        ok = false;
+                        break;
+                    }
+                    const int fv = v0 + t * (kTileBytes / 16);
+                    const int nv = max(0, min(kTileBytes / 16, v1 - fv));
+                    m.d = d;
+                    m.fv = fv;
+                    m.nv = nv;
+                    m.flags = (t == nt - 1 && c == a.n_split - 1) ? kTileLast : 0;
+                    meta[st] = m;
+                    if (nv > 0) {
+                        const uint32_t bytes = (uint32_t)nv * 16u;
+                        const bool has_p = item->has_p != 0;
+                        mbar_arrive_expect_tx(&full[st], has_p ? 2u * bytes : bytes);
+                        bulk_load_stream(tiles + (2 * st) * kTileBytes, item->q.row + (size_t)fv * 16, bytes, &full[st],
+                                         policy);
+                        if (has_p)
+                            bulk_load_stream(tiles + (2 * st + 1) * kTileBytes, item->p.row + (size_t)fv * 16, bytes,
+                                             &full[st], policy);
+                        in_flight[st] = it;
+                    } else {
+                        mbar_arrive(&full[st]);
+                    }
                 }
             }
-            if (__syncthreads_or(!ok)) {
-                if (tid == 0) {
-                    report_error(a.stats, SV_ERR_TIMEOUT, it.seq);
-                    for (long long k = itc; k < issued; ++k)
-                        mbar_wait_bounded(&full[k % kDrawStages], (uint32_t)((k / kDrawStages) & 1),
-                                          a.wait_limit / 16);
-                }
-                return;
+            if (*reinterpret_cast<volatile int *>(abort_flag)) {
+                for (int s = 0; s < kDrawStages; ++s)
+                    if (in_flight[s] >= 0)
+                        mbar_wait_bounded(&full[s], (uint32_t)((in_flight[s] / kDrawStages) & 1), a.wait_limit / 16);
             }
-            if (tid == 0) p_issue(st);
         }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    int cur = -1;
+    DrawItem item;
+    for (long long it = 0;; ++it) {
+        const int st = (int)(it % kDrawStages);
+        const uint32_t par = (uint32_t)((it / kDrawStages) & 1);
+        if (!mbar_wait_or_abort(&full[st], par, abort_flag, a.wait_limit)) {
+            if (lane == 0 && atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
+            break;
+        }
+        const DrawMeta m = meta[st];
+        if (m.flags & kTileEnd) break;
+        if (m.d != cur) {
+            item = a.items[m.d];
+            cur = m.d;
+        }
+        float *subs_item = a.subs + (size_t)m.d * a.n_sub;
+        const unsigned char *bq = tiles + (2 * st) * kTileBytes;
+        const unsigned char *bp = bq + kTileBytes;
+        if (item.has_p) {
+            if (item.filt) draw_tile<ES, true, true>(item, bq, bp, m.fv, m.nv, subs_item);
+            else draw_tile<ES, true, false>(item, bq, bp, m.fv, m.nv, subs_item);
+        } else {
+            if (item.filt) draw_tile<ES, false, true>(item, bq, bp, m.fv, m.nv, subs_item);
+            else draw_tile<ES, false, false>(item, bq, bp, m.fv, m.nv, subs_item);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
         // the scalar tail of the row forms the last sub-chunk
-        if (c == a.n_split - 1 && tid < 32) {
+        if ((m.flags & kTileLast) && warp == 0) {
             constexpr int EPV = 16 / ES;
             const int t0 = a.n_vec * EPV;
-            float w = 0.f, aq = 0.f, ap = 0.f;
-            if (t0 + tid < a.V) draw_scalar<ES>(it, t0 + tid, w, aq, ap);
+            const float w = t0 + lane < a.V ? draw_scalar<ES>(item, t0 + lane) : 0.f;
             const float W = warp_sum_f(w);
-            const float A = warp_sum_f(fmaf(aq, it.q.inv_s, it.has_p ? ap * it.p.inv_s : 0.f));
-            if (tid == 0) subs_item[n_vsub] = make_float2(W, A);
+            if (lane == 0) subs_item[n_vsub] = W;
         }
     }
 }
 
-// Certified bound on |C_fast(v) - u R_fast - (C(v) - u R)| over all v (see the header comment of
-// this file): element errors from the SFU exponential, the float32 exponent arguments, the
-// normalisers and the products, plus the float32 summation inside sub-chunks.
 // Bound on |(u R~ - C~(v)) - (u R - C(v))| for any v, where ~ marks the computed prefix sums.
 // With per-token errors d_v = |w~_v - w_v| the difference is (1-u) sum_{i<=v} d_i and
 // u sum_{i>v} d_i of opposite signs at worst, so it is at most max(u, 1-u) sum_v d_v; the
@@ -267,7 +286,6 @@ template <int ES>
 __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
     constexpr int EPV = 16 / ES;
     __shared__ float2 s_scan[kThreads];
-    __shared__ float s_red[kWarps];
     __shared__ int s_sub;
     __shared__ float2 s_pre;
     __shared__ int s_last_sub;
@@ -276,7 +294,7 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
     const int n_items = *reinterpret_cast<volatile int *>(&a.counters->n_draws);
     if (d >= n_items) return;
     const DrawItem it = a.items[d];
-    const float2 *subs = a.subs + (size_t)d * a.n_sub;
+    const float *subs = a.subs + (size_t)d * a.n_sub;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n_sub = a.n_sub, n_vsub = n_sub - 1;
 
@@ -284,13 +302,11 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
     const int per = (n_sub + kThreads - 1) / kThreads;
     const int s0 = min(tid * per, n_sub), s1 = min(s0 + per, n_sub);
     ff wsum = {0.f, 0.f};
-    float asum = 0.f;
     int last_pos = -1;
     for (int s = s0; s < s1; ++s) {
-        const float2 v = subs[s];
-        wsum = ff_add_f(wsum, v.x);
-        asum += v.y;
-        if (v.x > 0.f) last_pos = s;
+        const float v = subs[s];
+        wsum = ff_add_f(wsum, v);
+        if (v > 0.f) last_pos = s;
     }
     // 2. block inclusive scan of wsum in float-float
     s_scan[tid] = make_float2(wsum.hi, wsum.lo);
@@ -311,12 +327,10 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
     const float2 ex2v = tid > 0 ? s_scan[tid - 1] : make_float2(0.f, 0.f);
     const float2 r2 = s_scan[kThreads - 1];
     const ff incl = {in2.x, in2.y}, excl = {ex2v.x, ex2v.y}, R = {r2.x, r2.y};
-    const float at = warp_sum_f(asum);
-    if (lane == 0) s_red[warp] = at;
     atomicMax(&s_last_sub, last_pos);
     __syncthreads();
-    float A = 0.f;
-    for (int w = 0; w < kWarps; ++w) A += s_red[w];
+    // sum_v (q_v |y_q,v| + p_v |y_p,v|) over the normalised rows, from the statistics pass
+    const float A = it.q.ay + (it.has_p ? it.p.ay : 0.f);
     const float u_hi = __double2float_rn(it.u);
     const float u_lo = __double2float_rn(it.u - (double)u_hi);
     const ff thr = ff_mul(R, {u_hi, u_lo});
@@ -325,7 +339,7 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
         ff run = excl, pre = excl;
         int found = -1;
         for (int s = s0; s < s1; ++s) {
-            const float wv = subs[s].x;
+            const float wv = subs[s];
             const ff nx = ff_add_f(run, wv);
             if (wv > 0.f) {
                 found = s;
@@ -347,7 +361,7 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
         ambiguous = true;
         if (sub >= 0 && tid == 0) {
             ff p = {0.f, 0.f};
-            for (int s = 0; s < sub; ++s) p = ff_add_f(p, subs[s].x);
+            for (int s = 0; s < sub; ++s) p = ff_add_f(p, subs[s]);
             s_pre = make_float2(p.hi, p.lo);
         }
         __syncthreads();
@@ -374,21 +388,19 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
             ntok = EPV;
             const uint4 q = __ldg(reinterpret_cast<const uint4 *>(it.q.row) + vi);
             const uint4 p = it.has_p ? __ldg(reinterpret_cast<const uint4 *>(it.p.row) + vi) : q;
-            float aq, ap;
             if (it.has_p) {
-                if (it.filt) vec_weights<ES, true, true>(it, q, p, tok0, wv, aq, ap);
-                else vec_weights<ES, true, false>(it, q, p, tok0, wv, aq, ap);
+                if (it.filt) vec_weights<ES, true, true>(it, q, p, tok0, wv);
+                else vec_weights<ES, true, false>(it, q, p, tok0, wv);
             } else {
-                if (it.filt) vec_weights<ES, false, true>(it, q, p, tok0, wv, aq, ap);
-                else vec_weights<ES, false, false>(it, q, p, tok0, wv, aq, ap);
+                if (it.filt) vec_weights<ES, false, true>(it, q, p, tok0, wv);
+                else vec_weights<ES, false, false>(it, q, p, tok0, wv);
             }
         }
     } else {
         tok0 = a.n_vec * EPV + lane;
         if (tok0 < a.V) {
             ntok = 1;
-            float aq, ap;
-            draw_scalar<ES>(it, tok0, wv[0], aq, ap);
+            wv[0] = draw_scalar<ES>(it, tok0);
         }
     }
     ff lt = {0.f, 0.f};
@@ -453,6 +465,23 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
             push_exact(a.counters, a.exact, a.exact_unc, {d, it.seq}, a.stats);
         }
     }
+}
+
+// Host side: both passes of the draws.  The number of items is known only on the device, so
+// the pass-1 grid is the persistent size and pass 2 has one block per possible item.
+template <int ES>
+static sv_status launch_draws(const DrawArgs &da, long long max_items, const DeviceInfo &di, cudaStream_t stream) {
+    const int occ = prepare_kernel((const void *)k_draw_sums<ES>, kStatsThreads, kDrawSmemBytes);
+    if (occ < 1) return SV_ERR_CUDA;
+    long long grid = (long long)di.sms * occ;
+    const long long maxu = max_items * da.n_split;
+    if (grid > maxu) grid = maxu;
+    if (grid < 1) grid = 1;
+    k_draw_sums<ES><<<(unsigned)grid, kStatsThreads, kDrawSmemBytes, stream>>>(da);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    k_draw_finish<ES><<<(unsigned)max_items, kThreads, 0, stream>>>(da);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    return SV_OK;
 }
 
 }  // namespace sv

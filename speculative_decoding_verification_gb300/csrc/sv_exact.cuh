@@ -19,6 +19,7 @@
 #pragma once
 
 #include "sv_device.cuh"
+#include "sv_exp2_table.h"
 #include "sv_draw.cuh"
 #include "sv_host.h"
 
@@ -201,9 +202,7 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
     if (n_items == 0) return;   // uniform across the grid
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     {
-        const double t = exp2((double)tid / 256.0);
-        const float hi = (float)t;
-        tab[tid] = make_float2(hi, (float)(t - (double)hi));
+        tab[tid] = kExp2Table[tid];
     }
     if (tid == 0) {
         int acc = 0;

@@ -4,6 +4,7 @@
 #include <vector>
 
 #include "sv_device.cuh"
+#include "sv_exp2_table.h"
 #include <string.h>
 
 #include "sv_host.h"
@@ -72,9 +73,7 @@ __global__ void k_selftest_timeout(long long limit, sv_stats *stats) {
 __global__ void k_selftest_exp2(double lo, double hi, long long n, unsigned long long *out_bits) {
     __shared__ float2 tab[256];
     {
-        const double t = exp2((double)threadIdx.x / 256.0);
-        const float h = (float)t;
-        tab[threadIdx.x] = make_float2(h, (float)(t - (double)h));
+        tab[threadIdx.x] = kExp2Table[threadIdx.x];
     }
     __syncthreads();
     double e_fast = 0.0, e_ff = 0.0;
@@ -108,9 +107,7 @@ __device__ __forceinline__ float f32_from_order_key(unsigned k) {
 __global__ void k_selftest_exp2_all(unsigned k0, long long count, unsigned long long *out_bits) {
     __shared__ float2 tab[256];
     {
-        const double t = exp2((double)threadIdx.x / 256.0);
-        const float h = (float)t;
-        tab[threadIdx.x] = make_float2(h, (float)(t - (double)h));
+        tab[threadIdx.x] = kExp2Table[threadIdx.x];
     }
     __syncthreads();
     double e_fast = 0.0, e_ff = 0.0;

@@ -14,6 +14,7 @@ constexpr int kStatsStages = 6;             // pipeline depth of the statistics 
 constexpr int kStatsThreads = kThreads + 32;   // eight consumer warps and one producer warp
 constexpr int kUnitTiles = 4;               // aim for (row, chunk) units of about this many tiles
 constexpr int kDrawStages = 3;              // pipeline depth of the draw pass (two rows per stage)
+constexpr int kDrawUnitSubs = 64;           // draw-pass units: 64 sub-chunks (2 tiles) of a row pair
 constexpr int kSubBytes = 512;              // bytes of one row per draw sub-chunk (32 x 16 B)
 constexpr int kMaxSplit = 64;               // most chunks per row
 constexpr int kUnitTarget = 1024;           // at least about this many (row, chunk) units
@@ -67,7 +68,7 @@ struct RowStat {
     int argmax;
     int r;              // the integer reference exponent r
     int flags;
-    int pad;
+    float ay;           // sum_v 2^(x_v c - r) |x_v c - r| / S: mean |exponent| under the row
 };
 
 // Nucleus (top-p) cut of a row: token v is kept iff x_v > cut_x or (x_v == cut_x and v <= cut_id).
@@ -101,7 +102,7 @@ struct DrawRow {
     float cut_x; int cut_id;
     float top_x; int top_id;
     float sc_d;             // C for tokens in D (1 when no transform)
-    int pad;
+    float ay;               // bound on sum_v w_v |y_v| for this row's normalised weights w
     double norm_err;        // relative error bound of inv_s (normaliser from the stats pass)
 };
 
@@ -131,7 +132,8 @@ struct Counters {
     int n_exact;
     unsigned barrier;       // grid barrier of the exact tier
     int next_unit;          // statistics pass: next (row, chunk) unit to hand out
-    int pad[12];
+    int next_draw_unit;     // draw pass: next (item, chunk) unit to hand out
+    int pad[11];
 };
 
 inline int div_up(long long a, long long b) { return (int)((a + b - 1) / b); }
@@ -167,6 +169,13 @@ inline void chunk_geometry(long long n_vec, int &n_split, int &chunk_vecs) {
 // (< 16 B) scalar tail of the row.
 inline int vec_count(int V, int es) { return (int)(((long long)V * es) / 16); }
 inline int sub_chunks(int V, int es) { return div_up(vec_count(V, es), 32) + 1; }
+// Draw-pass chunks of a row: kDrawUnitSubs vector sub-chunks each.
+inline void draw_geometry(int n_sub, int &d_split, int &d_subs_per_chunk) {
+    const int n_vsub = n_sub - 1;
+    d_subs_per_chunk = kDrawUnitSubs;
+    d_split = n_vsub > 0 ? div_up(n_vsub, kDrawUnitSubs) : 1;
+}
+
 // Warp units per item in the float-float tier's row pass: groups of kExactGroup vector
 // sub-chunks, plus one for the scalar tail.
 inline int exact_groups(int n_sub) { return div_up(n_sub - 1, kExactGroup) + 1; }

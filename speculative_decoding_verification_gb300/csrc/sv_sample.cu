@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kThreads) k_sample_items(const SampleArgs a, l
             err += (double)a.top[r].z_err_f + kU32;
         }
         d.inv_s = __frcp_rn(norm);
-        d.pad = 0;
+        d.ay = __fdiv_ru(rs.ay * (1.0f + 0x1p-20f), __fdiv_rn(norm, rs.s_hi) * (1.0f - 0x1p-20f));
         d.norm_err = err;
     }
     it.p = {};
@@ -136,12 +136,7 @@ static SamplePlan plan_sample(int B, int n_rows, int V, int es) {
     p.n_vec = vec_count(V, es);
     chunk_geometry(p.n_vec, p.n_split, p.chunk_vecs);
     p.n_sub = sub_chunks(V, es);
-    const int n_vsub = p.n_sub - 1;
-    long long want = (4096 + rows - 1) / rows;
-    long long cap = n_vsub / 32 > 0 ? n_vsub / 32 : 1;
-    p.d_split = (int)(want < cap ? want : cap);
-    if (p.d_split < 1) p.d_split = 1;
-    p.d_subs_per_chunk = n_vsub > 0 ? div_up(n_vsub, p.d_split) : 1;
+    draw_geometry(p.n_sub, p.d_split, p.d_subs_per_chunk);
     Carver cv;
     p.off_counters = cv.take<Counters>(1);
     p.off_part = cv.take<WarpPartial>((size_t)rows * p.n_split * kWarps);
@@ -149,7 +144,7 @@ static SamplePlan plan_sample(int B, int n_rows, int V, int es) {
     p.off_nuc = cv.take<NucleusCut>((size_t)rows);
     p.off_top = cv.take<TopSet>((size_t)rows);
     p.off_draws = cv.take<DrawItem>((size_t)rows);
-    p.off_subs = cv.take<float2>((size_t)rows * p.n_sub);
+    p.off_subs = cv.take<float>((size_t)rows * p.n_sub);
     const size_t capx = (size_t)(rows < (long long)kExactCap ? rows : (long long)kExactCap);
     p.off_exact = cv.take<ExactItem>(capx);
     p.off_xpart = cv.take<double>(capx * 2 * kExactSplit * 3);
@@ -225,22 +220,14 @@ static sv_status launch_sample(const SamplePlan &sp, const SampleArgs &in, const
     da.n_sub = pl.n_sub;
     da.n_split = pl.d_split;
     da.subs_per_chunk = pl.d_subs_per_chunk;
-    da.subs = reinterpret_cast<float2 *>(w + pl.off_subs);
+    da.subs = reinterpret_cast<float *>(w + pl.off_subs);
     da.exact = reinterpret_cast<ExactItem *>(w + pl.off_exact);
     da.exact_unc = reinterpret_cast<int *>(w + pl.off_xunc_n);
     da.stats = a.stats;
     da.wait_limit = kWaitLimitCycles;
     {
-        const size_t smem = 128 + (size_t)2 * kDrawStages * kTileBytes;
-        const int occ = prepare_kernel((const void *)k_draw_sums<ES>, kThreads, smem);
-        if (occ < 1) return SV_ERR_CUDA;
-        long long grid = (long long)di.sms * occ;
-        const long long maxu = total * pl.d_split;
-        if (grid > maxu) grid = maxu;
-        k_draw_sums<ES><<<(unsigned)grid, kThreads, smem, stream>>>(da);
-        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
-        k_draw_finish<ES><<<(unsigned)total, kThreads, 0, stream>>>(da);
-        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+        const sv_status st = launch_draws<ES>(da, total, di, stream);
+        if (st != SV_OK) return st;
     }
     ExactArgs xa{};
     xa.tgt = a.rows;

@@ -12,6 +12,7 @@
 #pragma once
 
 #include "sv_device.cuh"
+#include "sv_exp2_table.h"
 #include "sv_host.h"
 #include "sv_stats.cuh"
 
@@ -447,9 +448,7 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
     } else {
         // ---- float-float tier: the same select on exact masses ----
         {
-            const double t = exp2((double)threadIdx.x / 256.0);
-            const float hi = (float)t;
-            tab[threadIdx.x] = make_float2(hi, (float)(t - (double)hi));
+            tab[threadIdx.x] = kExp2Table[threadIdx.x];
         }
         __syncthreads();
         const ff cff = {c_hi, c_lo};

@@ -522,7 +522,7 @@ __device__ __forceinline__ RowStat combine_row(const WarpPartial *P, int np, boo
     r.maxv = m;
     r.argmax = am;
     r.r = rmax;
-    r.pad = 0;
+    r.ay = 0.f;
     r.s_hi = r.s_lo = r.err = 0.f;
     if (!greedy && lane == 0) {
         const ff S = fast_two_sum(s.hi, s.lo);
@@ -531,6 +531,7 @@ __device__ __forceinline__ RowStat combine_row(const WarpPartial *P, int np, boo
         // ex2 error + exponent rounding (|y| weighted) + float32 summation (tree + compensated);
         // evaluated in float32 and rounded up by 2^-20 to cover that evaluation
         const float ay = S.hi > 0.f ? __fdiv_rn(a, S.hi) : 0.f;
+        r.ay = ay;
         r.err = (float)(kEx2RelErr + 6.0 * kU32 + 1e-12) + (float)(1.02 * kYRound) * ay;
         r.err *= 1.0f + 0x1p-20f;
     }

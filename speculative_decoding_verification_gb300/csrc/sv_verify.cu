@@ -76,7 +76,8 @@ __device__ __forceinline__ DrawRow draw_row(const char *row, float T, const RowS
         err += (double)ts->z_err_f + kU32;
     }
     d.inv_s = __frcp_rn(norm);
-    d.pad = 0;
+    // mean |y| under the normalised weights: at most the row's, divided by the kept mass and z
+    d.ay = __fdiv_ru(rs.ay * (1.0f + 0x1p-20f), __fdiv_rn(norm, rs.s_hi) * (1.0f - 0x1p-20f));
     d.norm_err = err;
     return d;
 }
@@ -308,12 +309,7 @@ VerifyPlan plan_verify(int B, int K, int V, int es) {
     p.n_vec = vec_count(V, es);
     chunk_geometry(p.n_vec, p.n_split, p.chunk_vecs);
     p.n_sub = sub_chunks(V, es);
-    const int n_vsub = p.n_sub - 1;
-    long long want = (4096 + B - 1) / B;
-    long long dcap = n_vsub / 32 > 0 ? n_vsub / 32 : 1;
-    p.d_split = (int)(want < dcap ? want : dcap);
-    if (p.d_split < 1) p.d_split = 1;
-    p.d_subs_per_chunk = n_vsub > 0 ? div_up(n_vsub, p.d_split) : 1;
+    draw_geometry(p.n_sub, p.d_split, p.d_subs_per_chunk);
     Carver cv;
     p.off_counters = cv.take<Counters>(1);
     p.off_part = cv.take<WarpPartial>((size_t)n_cand * p.n_split * kWarps);
@@ -321,7 +317,7 @@ VerifyPlan plan_verify(int B, int K, int V, int es) {
     p.off_nuc = cv.take<NucleusCut>((size_t)n_cand);
     p.off_top = cv.take<TopSet>((size_t)n_cand);
     p.off_draws = cv.take<DrawItem>((size_t)B);
-    p.off_subs = cv.take<float2>((size_t)B * p.n_sub);
+    p.off_subs = cv.take<float>((size_t)B * p.n_sub);
     const size_t cap = (size_t)(B < kExactCap ? B : (int)kExactCap);
     p.off_exact = cv.take<ExactItem>(cap);
     const int max_slots = 2 * K + 1 > 2 ? 2 * K + 1 : 2;
@@ -404,22 +400,14 @@ static sv_status launch_verify(const VerifyPlan &pl, const AcceptArgs &acc_in, c
     da.n_sub = pl.n_sub;
     da.n_split = pl.d_split;
     da.subs_per_chunk = pl.d_subs_per_chunk;
-    da.subs = reinterpret_cast<float2 *>(w + pl.off_subs);
+    da.subs = reinterpret_cast<float *>(w + pl.off_subs);
     da.exact = acc.exact;
     da.exact_unc = acc.exact_unc;
     da.stats = acc.stats;
     da.wait_limit = wait;
     {
-        const size_t smem = 128 + (size_t)2 * kDrawStages * kTileBytes;
-        const int occ = prepare_kernel((const void *)k_draw_sums<ES>, kThreads, smem);
-        if (occ < 1) return SV_ERR_CUDA;
-        long long grid = (long long)di.sms * occ;
-        const long long maxu = (long long)B * pl.d_split;
-        if (grid > maxu) grid = maxu;
-        k_draw_sums<ES><<<(unsigned)grid, kThreads, smem, stream>>>(da);
-        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
-        k_draw_finish<ES><<<B, kThreads, 0, stream>>>(da);
-        if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+        const sv_status st = launch_draws<ES>(da, (long long)B, di, stream);
+        if (st != SV_OK) return st;
     }
     // 5. float-float tier
     ExactArgs xa;

@@ -104,3 +104,25 @@ def test_lookup_and_reuse_reject_bad_arguments(lib):
     assert lib.sv_cache_lookup(fake, fake, fake, None, 4, 2, fake, None) == 1
     assert lib.sv_mirror_reuse(fake, fake, fake, 4, 0, 7, fake, None) == 1
     assert lib.sv_mirror_reuse(None, fake, fake, 4, 8, 7, fake, None) == 1
+
+
+def test_exp2_table_header_values():
+    """The float-float table of 2^(j/256) used by the library's float-float exponential: hi is the
+    float32 nearest to 2^(j/256), lo the float32 nearest to the remainder (checked in float64
+    and against a 50-digit decimal evaluation for a sample)."""
+    import decimal
+    import struct
+    path = os.path.join(ROOT, "speculative_decoding_verification_gb300", "csrc", "sv_exp2_table.h")
+    pairs = re.findall(r"\{(-?0x[0-9a-f.p+-]+)f, (-?0x[0-9a-f.p+-]+)f\}", open(path).read())
+    assert len(pairs) == 256
+    f32 = lambda x: struct.unpack("<f", struct.pack("<f", x))[0]
+    decimal.getcontext().prec = 50
+    ln2 = decimal.Decimal(2).ln()
+    for j, (h, l) in enumerate(pairs):
+        hi, lo = float.fromhex(h), float.fromhex(l)
+        assert f32(hi) == hi and f32(lo) == lo
+        assert abs((hi + lo) / np.exp2(j / 256.0) - 1.0) < 2.0 ** -47
+        if j % 17 == 0:
+            t = (ln2 * j / 256).exp()
+            assert abs(decimal.Decimal(hi) + decimal.Decimal(lo) - t) / t < decimal.Decimal(2) ** -47
+            assert abs(decimal.Decimal(hi) - t) <= decimal.Decimal(2) ** -24 * t

@@ -37,6 +37,7 @@ struct ExactRow {
     int top_id;
     float sc;       // factor on the top-F set (1: none)
     int valid;
+    int filt;       // a nucleus cut or a top-F set is in use
 };
 
 struct ExactDraw {
@@ -122,6 +123,7 @@ __device__ __forceinline__ ExactRow exact_row_from_draw(const DrawRow &r) {
     e.top_id = r.top_id;
     e.sc = r.sc_d;
     e.valid = r.row != nullptr;
+    e.filt = (e.cut_x > -INFINITY) || (e.top_id >= 0);
     return e;
 }
 
@@ -151,15 +153,16 @@ __device__ __forceinline__ ExactRow seq_row(const ExactArgs &a, int b, int slot)
         e.sc = a.sag_C;
     }
     e.valid = 1;
+    e.filt = (e.cut_x > -INFINITY) || (e.top_id >= 0);
     return e;
 }
 
 // Weight of token v in a row: keep(v) * 2^(x c - r) * (sc on the top-F set), float-float.
 __device__ __forceinline__ ff exact_w(const ExactRow &r, float x, int v, const float2 *tab) {
-    if (!in_cut(x, v, r.cut_x, r.cut_id) || x == -INFINITY) return {0.f, 0.f};
+    if (x == -INFINITY || (r.filt && !in_cut(x, v, r.cut_x, r.cut_id))) return {0.f, 0.f};
     const ff y = ff_affine(x, r.c, {r.rf, 0.f});
     ff e = ff_exp2(y.hi, y.lo, tab);
-    if (in_cut(x, v, r.top_x, r.top_id)) e = ff_mul(e, {r.sc, 0.f});
+    if (r.filt && in_cut(x, v, r.top_x, r.top_id)) e = ff_mul(e, {r.sc, 0.f});
     return e;
 }
 

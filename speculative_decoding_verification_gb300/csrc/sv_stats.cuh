@@ -156,69 +156,17 @@ __device__ __forceinline__ void acc_scalar(StatAcc &A, float x, int idx, bool gr
     acc_add(A, e);
 }
 
-template <int N>
-__device__ __forceinline__ void acc_sampled(StatAcc &A, const float (&x)[N], float vmax, float c_hi, float c_lo) {
-    if (!(vmax <= A.thr)) acc_reference(A, vmax, c_hi);
-    float e[N];
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const float y = fmaf(x[i], c_lo, fmaf(x[i], c_hi, -A.rf));
-        e[i] = ex2_fast(y);
-        A.aerr = fmaf(e[i], fabsf(y), A.aerr);
-    }
-    float s;
-    if constexpr (N == 8) {
-        s = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-    } else {
-        s = (e[0] + e[1]) + (e[2] + e[3]);
-    }
-    acc_add(A, s);
-}
-
-template <int N>
-__device__ __forceinline__ void acc_greedy_update(StatAcc &A, const float (&x)[N], float vmax, int e0) {
-    if (vmax != vmax) {
-        A.flags |= kFlagNaN;
-        return;
-    }
-    int idx = 0;
-#pragma unroll
-    for (int i = N - 1; i >= 0; --i)
-        if (x[i] == vmax) idx = i;
-    A.m = vmax;
-    A.am = e0 + idx;
-    if (isinf(vmax)) A.flags |= kFlagPosInf;
-}
-
-// One 16-byte vector at element index e0.
-template <int ES>
-__device__ __forceinline__ void acc_vector(StatAcc &A, uint4 w, int e0, bool greedy, float c_hi, float c_lo) {
-    if (ES == 2) {
-        const uint32_t pm = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
-        const float vmax = fmax_nan(bf16_lo(pm), bf16_hi(pm));
-        const float x[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                            bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-        if (greedy) {
-            if (!(vmax <= A.m)) acc_greedy_update<8>(A, x, vmax, e0);
-        } else {
-            acc_sampled<8>(A, x, vmax, c_hi, c_lo);
-        }
-    } else {
-        const float x[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
-                            __uint_as_float(w.w)};
-        const float vmax = fmax_nan(fmax_nan(x[0], x[1]), fmax_nan(x[2], x[3]));
-        if (greedy) {
-            if (!(vmax <= A.m)) acc_greedy_update<4>(A, x, vmax, e0);
-        } else {
-            acc_sampled<4>(A, x, vmax, c_hi, c_lo);
-        }
-    }
-}
+// Largest finite logit magnitude kept as is; smaller logits (and -inf) have 2^(x c - r) = 0
+// for every allowed c, so clamping them there changes no weight and keeps x c - r finite.
+constexpr uint32_t kBf16Floor2 = 0xF149F149u;   // bf16 pair (-9.95e29, -9.95e29)
+constexpr float kF32Floor = -9.95e29f;
 
 // A thread's share of one shared-memory tile: its NV vectors (vi = tid + i * kThreads) are
 // loaded together, checked against the reference with one combined maximum, and their
 // 8 * NV (bf16) exponentials are independent, so the SFU work overlaps.  Vectors past the
-// end of a partial tile read as -inf.
+// end of a partial tile read as -inf.  Sampled rows accumulate S = sum 2^y and
+// A = sum 2^y (-y) with y = x c - r <= 0 (up to the rounding of x c_lo; combine_row adds
+// the bound for that), one compensated addition per tile.
 template <int ES>
 __device__ __forceinline__ void acc_tile(StatAcc &A, const unsigned char *buf, int nv, int fv, bool greedy, float c_hi,
                                          float c_lo) {
@@ -227,10 +175,15 @@ __device__ __forceinline__ void acc_tile(StatAcc &A, const unsigned char *buf, i
     const uint32_t ninf = ES == 2 ? 0xFF80FF80u : 0xFF800000u;
     const int tid = threadIdx.x;
     uint4 w[NV];
+    if (nv == kTileBytes / 16) {
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-        const int vi = tid + i * kThreads;
-        w[i] = vi < nv ? lds128(buf + vi * 16) : make_uint4(ninf, ninf, ninf, ninf);
+        for (int i = 0; i < NV; ++i) w[i] = lds128(buf + (tid + i * kThreads) * 16);
+    } else {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int vi = tid + i * kThreads;
+            w[i] = vi < nv ? lds128(buf + vi * 16) : make_uint4(ninf, ninf, ninf, ninf);
+        }
     }
     float vmax;
     if constexpr (ES == 2) {
@@ -270,13 +223,21 @@ __device__ __forceinline__ void acc_tile(StatAcc &A, const unsigned char *buf, i
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         float x[EPV], e[EPV];
-        unpack<ES>(w[i], x);
+        if constexpr (ES == 2) {
+            const uint4 c = make_uint4(bmax2(w[i].x, kBf16Floor2), bmax2(w[i].y, kBf16Floor2),
+                                       bmax2(w[i].z, kBf16Floor2), bmax2(w[i].w, kBf16Floor2));
+            unpack<ES>(c, x);
+        } else {
+            unpack<ES>(w[i], x);
+#pragma unroll
+            for (int k = 0; k < EPV; ++k) x[k] = fmax_nan(x[k], kF32Floor);
+        }
         float a = 0.f;
 #pragma unroll
         for (int k = 0; k < EPV; ++k) {
             const float y = fmaf(x[k], c_lo, fmaf(x[k], c_hi, -A.rf));
             e[k] = ex2_fast(y);
-            a = fmaf(e[k], fminf(fabsf(y), 128.0f), a);
+            a = fmaf(e[k], -y, a);
         }
         if constexpr (EPV == 8) {
             sv[i] = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
@@ -285,11 +246,13 @@ __device__ __forceinline__ void acc_tile(StatAcc &A, const unsigned char *buf, i
         }
         av[i] = a;
     }
+    float st = sv[0], at = av[0];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) acc_add(A, sv[i]);
-    float at = 0.f;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) at += av[i];
+    for (int i = 1; i < NV; ++i) {
+        st += sv[i];
+        at += av[i];
+    }
+    acc_add(A, st);
     A.aerr += at;
 }
 
@@ -530,9 +493,13 @@ __device__ __forceinline__ RowStat combine_row(const WarpPartial *P, int np, boo
         r.s_lo = S.lo;
         // ex2 error + exponent rounding (|y| weighted) + float32 summation (tree + compensated);
         // evaluated in float32 and rounded up by 2^-20 to cover that evaluation
-        const float ay = S.hi > 0.f ? __fdiv_rn(a, S.hi) : 0.f;
+        // A counts 2^y (-y); the few y > 0 left by rounding (x c_hi may exceed r by a rounding of
+        // the threshold, plus x c_lo: y <= (|r| + 1) 2^-21, each with 2^y < 2, at most S of
+        // them) can lower it by 2 S (|r| + 1) 2^-21 at most
+        const float ay = (S.hi > 0.f ? __fdiv_rn(a, S.hi) : 0.f) + (float)(abs(rmax) + 1) * 0x1p-19f;
         r.ay = ay;
-        r.err = (float)(kEx2RelErr + 6.0 * kU32 + 1e-12) + (float)(1.02 * kYRound) * ay;
+        // summation: 3 + 2 tree levels per tile, a compensated running sum, float-float merges
+        r.err = (float)(kEx2RelErr + 8.0 * kU32 + 1e-12) + (float)(1.02 * kYRound) * ay;
         r.err *= 1.0f + 0x1p-20f;
     }
     return r;   // s_hi, s_lo, err valid in lane 0 (sampled rows)

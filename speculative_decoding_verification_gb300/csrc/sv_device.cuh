@@ -78,14 +78,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
-// As mbar_wait_bounded, and also gives up once *abort_flag is set by another warp.
+// As mbar_wait_bounded, and also gives up once *abort_flag is set by another warp.  Between
+// tries the warp backs off (32 ns doubling to 256 ns), so waiting warps leave the issue slots
+// to the warps that have work.
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, const int *abort_flag,
                                                    long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
+    unsigned ns = 32;
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return true;
         if (*reinterpret_cast<const volatile int *>(abort_flag) || clock64() - t0 > limit) return false;
+        __nanosleep(ns);
+        ns = ns < 256 ? 2 * ns : 256;
     }
 }
 

@@ -149,7 +149,9 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a
             const long long n_units = (long long)n_items * a.n_split;
             long long in_flight[kDrawStages];
             for (int s = 0; s < kDrawStages; ++s) in_flight[s] = -1;
-            long long it = 0;
+            long long it = 0;           // tiles issued
+            int st = 0;                 // it % kDrawStages
+            uint32_t epar = 0;          // parity of the "empty" phase to wait for at stage st
             bool ok = true;
             while (ok) {
                 const long long u = atomicAdd(&a.counters->next_draw_unit, 1);
@@ -166,10 +168,8 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a
                 }
                 const int nt = have ? max((v1 - v0 + kTileBytes / 16 - 1) / (kTileBytes / 16), 1) : 1;
                 for (int t = 0; t < nt; ++t, ++it) {
-                    const int st = (int)(it % kDrawStages);
                     if (it >= kDrawStages) {
-                        const uint32_t par = (uint32_t)(((it / kDrawStages) - 1) & 1);
-                        if (!mbar_wait_or_abort(&empty[st], par, abort_flag, a.wait_limit)) {
+                        if (!mbar_wait_or_abort(&empty[st], epar, abort_flag, a.wait_limit)) {
                             if (atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
                             ok = false;
                             break;
@@ -204,6 +204,10 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a
                     } else {
                         mbar_arrive(&full[st]);
                     }
+                    if (++st == kDrawStages) {
+                        st = 0;
+                        if (it >= 2 * kDrawStages - 1) epar ^= 1u;   // round r >= 2 waits phase r - 1
+                    }
                 }
             }
             if (*reinterpret_cast<volatile int *>(abort_flag)) {
@@ -218,9 +222,9 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a
     // ---------------- consumers ----------------
     int cur = -1;
     DrawItem item;
-    for (long long it = 0;; ++it) {
-        const int st = (int)(it % kDrawStages);
-        const uint32_t par = (uint32_t)((it / kDrawStages) & 1);
+    int st = 0;
+    uint32_t par = 0;
+    for (;;) {
         if (!mbar_wait_or_abort(&full[st], par, abort_flag, a.wait_limit)) {
             if (lane == 0 && atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
             break;
@@ -250,6 +254,10 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a
             const float w = t0 + lane < a.V ? draw_scalar<ES>(item, t0 + lane) : 0.f;
             const float W = warp_sum_f(w);
             if (lane == 0) subs_item[n_vsub] = W;
+        }
+        if (++st == kDrawStages) {
+            st = 0;
+            par ^= 1u;
         }
     }
 }

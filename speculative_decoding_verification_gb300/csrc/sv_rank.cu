@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_finish(const TopKArgs a) {
         }
         return;
     }
-    const RowStat st = combine_row(a.part + (size_t)r * a.n_split * kWarps, a.n_split * kWarps, false);
+    const RowStat st = combine_row(a.part + (size_t)r * a.n_split * kWarps, a.n_split * kWarps, false, T);
     double lse = 0.0;
     int bad = 0;
     if (lane == 0) {

@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(kThreads) k_sample_items(const SampleArgs a, l
         return;
     }
     // combine partials (same arithmetic as the verify path)
-    const RowStat rs = combine_row(a.part + (size_t)r * a.n_split * kWarps, a.n_split * kWarps, greedy);
+    const RowStat rs = combine_row(a.part + (size_t)r * a.n_split * kWarps, a.n_split * kWarps, greedy, T);
     if (lane != 0) return;
     a.rowstat[r] = rs;
     const bool bad = rs.flags != 0 || (greedy ? !isfinite(rs.maxv) : !rs_sampled_ok(rs));

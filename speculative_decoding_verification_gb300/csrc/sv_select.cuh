@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
     }
     const char *row = rs.base + (b * rs.rows_per_seq + j) * rs.pitch_bytes;
     if (threadIdx.x < 32) {
-        const RowStat st = combine_row(a.part + (size_t)rid * a.n_split * kWarps, a.n_split * kWarps, false);
+        const RowStat st = combine_row(a.part + (size_t)rid * a.n_split * kWarps, a.n_split * kWarps, false, T);
         if (threadIdx.x == 0) s_rs = st;
     }
     __syncthreads();
@@ -542,7 +542,7 @@ __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
     }
     const char *row = a.rows.base + (b * a.rows.rows_per_seq + j) * a.rows.pitch_bytes;
     if (threadIdx.x < 32) {
-        const RowStat st = combine_row(a.part + (size_t)rid * a.n_split * kWarps, a.n_split * kWarps, false);
+        const RowStat st = combine_row(a.part + (size_t)rid * a.n_split * kWarps, a.n_split * kWarps, false, T);
         if (threadIdx.x == 0) s_rs = st;
     }
     __syncthreads();

@@ -135,6 +135,11 @@ __device__ __forceinline__ void acc_add(StatAcc &A, float s8) {
     A.s = t;
 }
 
+// Largest finite logit magnitude kept as is; smaller logits (and -inf) have 2^(x c - r) = 0
+// for every allowed c, so clamping them there changes no weight and keeps x c - r finite.
+constexpr uint32_t kBf16Floor2 = 0xF149F149u;   // bf16 pair (-9.95e29, -9.95e29)
+constexpr float kF32Floor = -9.95e29f;
+
 // One element outside the vector stream (row tails).
 __device__ __forceinline__ void acc_scalar(StatAcc &A, float x, int idx, bool greedy, float c_hi, float c_lo) {
     if (greedy) {
@@ -150,26 +155,21 @@ __device__ __forceinline__ void acc_scalar(StatAcc &A, float x, int idx, bool gr
         return;
     }
     if (!(x <= A.thr)) acc_reference(A, x, c_hi);
-    const float y = fmaf(x, c_lo, fmaf(x, c_hi, -A.rf));
+    (void)c_lo;   // applied to the row sum in combine_row
+    const float y = fmaf(fmaxf(x, kF32Floor), c_hi, -A.rf);
     const float e = ex2_fast(y);
-    A.aerr = fmaf(e, fminf(fabsf(y), 128.0f), A.aerr);   // e = 0 below 2^-126: keeps -inf logits finite
+    A.aerr = fmaf(e, -y, A.aerr);
     acc_add(A, e);
 }
-
-// Largest finite logit magnitude kept as is; smaller logits (and -inf) have 2^(x c - r) = 0
-// for every allowed c, so clamping them there changes no weight and keeps x c - r finite.
-constexpr uint32_t kBf16Floor2 = 0xF149F149u;   // bf16 pair (-9.95e29, -9.95e29)
-constexpr float kF32Floor = -9.95e29f;
 
 // A thread's share of one shared-memory tile: its NV vectors (vi = tid + i * kThreads) are
 // loaded together, checked against the reference with one combined maximum, and their
 // 8 * NV (bf16) exponentials are independent, so the SFU work overlaps.  Vectors past the
 // end of a partial tile read as -inf.  Sampled rows accumulate S = sum 2^y and
-// A = sum 2^y (-y) with y = x c - r <= 0 (up to the rounding of x c_lo; combine_row adds
-// the bound for that), one compensated addition per tile.
+// A = sum 2^y (-y) with y = x c_hi - r <= 0 rounded once (c = c_hi + c_lo); combine_row
+// applies the x c_lo part to the row sum to first order.  One compensated addition per tile.
 template <int ES>
-__device__ __forceinline__ void acc_tile(StatAcc &A, const unsigned char *buf, int nv, int fv, bool greedy, float c_hi,
-                                         float c_lo) {
+__device__ __forceinline__ void acc_tile(StatAcc &A, const unsigned char *buf, int nv, int fv, bool greedy, float c_hi) {
     constexpr int EPV = 16 / ES;
     constexpr int NV = kTileBytes / 16 / kThreads;
     const uint32_t ninf = ES == 2 ? 0xFF80FF80u : 0xFF800000u;
@@ -235,7 +235,7 @@ __device__ __forceinline__ void acc_tile(StatAcc &A, const unsigned char *buf, i
         float a = 0.f;
 #pragma unroll
         for (int k = 0; k < EPV; ++k) {
-            const float y = fmaf(x[k], c_lo, fmaf(x[k], c_hi, -A.rf));
+            const float y = fmaf(x[k], c_hi, -A.rf);   // one rounding; x c_lo enters in combine_row
             e[k] = ex2_fast(y);
             a = fmaf(e[k], -y, a);
         }
@@ -339,7 +339,9 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_stats(const StatsArgs a) {
             const uint64_t policy = policy_evict_first();
             long long in_flight[kStatsStages];   // tile number whose copy a stage waits for, or -1
             for (int s = 0; s < kStatsStages; ++s) in_flight[s] = -1;
-            long long it = 0;
+            long long it = 0;           // tiles issued
+            int st = 0;                 // it % kStatsStages
+            uint32_t epar = 0;          // parity of the "empty" phase to wait for at stage st
             bool ok = true;
             int u = atomicAdd(&a.counters->next_unit, 1);
             while (ok) {
@@ -356,10 +358,8 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_stats(const StatsArgs a) {
                 }
                 const int nt = have ? max(unit_tiles(ui), 1) : 1;
                 for (int t = 0; t < nt; ++t, ++it) {
-                    const int st = (int)(it % kStatsStages);
                     if (it >= kStatsStages) {
-                        const uint32_t par = (uint32_t)(((it / kStatsStages) - 1) & 1);
-                        if (!mbar_wait_or_abort(&empty[st], par, abort_flag, a.wait_limit)) {
+                        if (!mbar_wait_or_abort(&empty[st], epar, abort_flag, a.wait_limit)) {
                             if (atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
                             ok = false;
                             break;
@@ -395,6 +395,10 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_stats(const StatsArgs a) {
                     } else {
                         mbar_arrive(&full[st]);   // a tail-only unit: nothing to copy
                     }
+                    if (++st == kStatsStages) {
+                        st = 0;
+                        if (it >= 2 * kStatsStages - 1) epar ^= 1u;   // round r >= 2 waits phase r - 1
+                    }
                 }
             }
             // after an abort, copies still in flight land before shared memory is released
@@ -410,9 +414,9 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_stats(const StatsArgs a) {
     // ---------------- consumers ----------------
     StatAcc A;
     acc_init(A);
-    for (long long it = 0;; ++it) {
-        const int st = (int)(it % kStatsStages);
-        const uint32_t par = (uint32_t)((it / kStatsStages) & 1);
+    int st = 0;
+    uint32_t par = 0;
+    for (;;) {
         if (!mbar_wait_or_abort(&full[st], par, abort_flag, a.wait_limit)) {
             if (lane == 0 && atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
             break;
@@ -421,7 +425,7 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_stats(const StatsArgs a) {
         if (m.flags & kTileEnd) break;
         const bool greedy = (m.flags & kTileGreedy) != 0;
         if (m.flags & kTileFirst) acc_init(A);
-        if (m.nv > 0) acc_tile<ES>(A, tiles + st * kTileBytes, m.nv, m.fv, greedy, m.c_hi, m.c_lo);
+        if (m.nv > 0) acc_tile<ES>(A, tiles + st * kTileBytes, m.nv, m.fv, greedy, m.c_hi);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
         if (m.flags & kTileLast) {
@@ -431,6 +435,10 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_stats(const StatsArgs a) {
                 acc_scalar(A, x, m.tail0 + tid, greedy, m.c_hi, m.c_lo);
             }
             acc_store(A, greedy, a.part + ((size_t)m.rid * a.n_split + m.chunk) * kWarps + warp);
+        }
+        if (++st == kStatsStages) {
+            st = 0;
+            par ^= 1u;
         }
     }
 }
@@ -453,7 +461,7 @@ static sv_status launch_stats(const StatsArgs &sa, const DeviceInfo &di, cudaStr
 
 // Combine a row's warp partials (one warp).  Float-float accumulation; the few float64
 // operations happen once per row.
-__device__ __forceinline__ RowStat combine_row(const WarpPartial *P, int np, bool greedy) {
+__device__ __forceinline__ RowStat combine_row(const WarpPartial *P, int np, bool greedy, float T) {
     const int lane = threadIdx.x & 31;
     int rmax = kNoRef;
     for (int p = lane; p < np; p += 32) rmax = max(rmax, P[p].r);
@@ -488,18 +496,29 @@ __device__ __forceinline__ RowStat combine_row(const WarpPartial *P, int np, boo
     r.ay = 0.f;
     r.s_hi = r.s_lo = r.err = 0.f;
     if (!greedy && lane == 0) {
-        const ff S = fast_two_sum(s.hi, s.lo);
+        float c_hi, c_lo;
+        log2e_over(T, c_hi, c_lo);
+        // The pass summed e = 2^(x c_hi - r); the true terms are e 2^(x c_lo) = e (1 + k x c_hi + q)
+        // with k = ln2 c_lo / c_hi and |q| <= (ln2 |x c_lo|)^2 (|x c_lo| <= 2^-22 here).  Since
+        // x c_hi = y + r and sum e (-y) = a:  S = S_pass + k (r S_pass - a).
+        const ff S0 = fast_two_sum(s.hi, s.lo);
+        const float k = (float)kLn2 * __fdiv_rn(c_lo, c_hi);
+        const float corr = k * fmaf((float)rmax, S0.hi, -a);
+        const ff S = ff_add(S0, {corr, 0.f});
         r.s_hi = S.hi;
         r.s_lo = S.lo;
-        // ex2 error + exponent rounding (|y| weighted) + float32 summation (tree + compensated);
-        // evaluated in float32 and rounded up by 2^-20 to cover that evaluation
         // A counts 2^y (-y); the few y > 0 left by rounding (x c_hi may exceed r by a rounding of
-        // the threshold, plus x c_lo: y <= (|r| + 1) 2^-21, each with 2^y < 2, at most S of
-        // them) can lower it by 2 S (|r| + 1) 2^-21 at most
-        const float ay = (S.hi > 0.f ? __fdiv_rn(a, S.hi) : 0.f) + (float)(abs(rmax) + 1) * 0x1p-19f;
+        // the threshold: y <= (|r| + 1) 2^-22, each with 2^y < 2, at most S of them) can lower it
+        // by 2 S (|r| + 1) 2^-22 at most.  ay bounds sum q |y| for y = x c_hi - r and, with
+        // |x c_lo| <= (|r| + 128) 2^-23 added, for y = x c - r as the draw pass computes it.
+        const float rr = (float)(abs(rmax) + 128);
+        const float ay = (S0.hi > 0.f ? __fdiv_rn(a, S0.hi) : 0.f) + rr * 0x1p-20f;
         r.ay = ay;
-        // summation: 3 + 2 tree levels per tile, a compensated running sum, float-float merges
-        r.err = (float)(kEx2RelErr + 8.0 * kU32 + 1e-12) + (float)(1.02 * kYRound) * ay;
+        // exponential + exponent rounded once (ln2 u per unit |y|) + second-order c_lo term +
+        // summation (3 + 2 tree levels per tile, compensated running sum, float-float merges) +
+        // the correction's own rounding; evaluated in float32 and rounded up by 2^-20
+        const float q2 = (float)kLn2 * rr * 0x1p-23f;
+        r.err = (float)(kEx2RelErr + 9.0 * kU32 + 1e-12) + (float)(1.02 * kLn2 * kU32) * ay + q2 * q2;
         r.err *= 1.0f + 0x1p-20f;
     }
     return r;   // s_hi, s_lo, err valid in lane 0 (sampled rows)

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
     const int n_t = K + 1, n_d = greedy ? 0 : K;
     for (int i = warp; i < n_t + n_d; i += kWarps) {
         const long long rid = i < n_t ? (long long)b * n_t + i : a.n_rows0 + (long long)b * K + (i - n_t);
-        const RowStat r = combine_row(a.part + (size_t)rid * a.n_split * kWarps, a.n_split * kWarps, greedy);
+        const RowStat r = combine_row(a.part + (size_t)rid * a.n_split * kWarps, a.n_split * kWarps, greedy, T);
         if (lane == 0) {
             rs[i] = r;
             a.rowstat[rid] = r;

@@ -78,7 +78,7 @@ typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
  *
  * Decisions (accept tests and draws) are first taken in float32 with a proven error bound.
  * Those the bound cannot settle are recomputed in a float-float tier (about 44 significant
- * bits) and counted in `reresolved`; those within ~1e-12 relative of the boundary even there
+ * bits) and counted in `reresolved`; those within 2e-11 relative of the boundary even there
  * are counted in `unresolved`.  `near_boundary` counts decisions whose uniform lies within
  * 1e-6 of a ratio or a normalised CDF boundary (a property of the data, reported for context).
  */

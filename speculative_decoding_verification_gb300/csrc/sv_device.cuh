@@ -219,6 +219,13 @@ __device__ __forceinline__ ff ff_mul(ff a, ff b) {
     return fast_two_sum(p.hi, p.lo);
 }
 
+// 1 / a in float-float: a float32 reciprocal refined by one Newton step in float-float.
+__device__ __forceinline__ ff ff_recip(ff a) {
+    const float r0 = __frcp_rn(a.hi);
+    const ff e = ff_sub({1.0f, 0.0f}, ff_mul(a, {r0, 0.0f}));   // 1 - a r0, about 2^-24
+    return ff_add({r0, 0.0f}, ff_mul({r0, 0.0f}, e));
+}
+
 // a + b for a float b.
 __device__ __forceinline__ ff ff_add_f(ff a, float b) {
     const ff s = two_sum(a.hi, b);

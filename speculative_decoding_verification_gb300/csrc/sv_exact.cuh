@@ -13,7 +13,7 @@
 //   D. per item: exact normalisers, sub-chunk masses W = A_q/S_q - A_p/S_p plus the exact
 //      residuals of the listed tokens, a float64 scan, the sub-chunk holding u R, a
 //      float-float rescan, t*.
-// Results agree with a float64 evaluation except when u R lies within ~1e-12 relative of a
+// Results agree with a float64 evaluation except when u R lies within 2e-11 relative of a
 // boundary; such decisions are counted in sv_stats.unresolved.  Element exponentials use
 // Tang's table method in float-float (sv_device.cuh); no float64 work runs per element.
 #pragma once
@@ -426,37 +426,41 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
     }
 
     // ---- phase D: one block per item: exact sub-chunk masses, block scan, t* ----------------
-    __shared__ double s_unc_w[kExactUncCap];
+    // Float-float throughout (the float64 pipe of this GPU would set the latency of the block).
+    __shared__ float2 s_unc_w[kExactUncCap];
     __shared__ int s_unc_sub[kExactUncCap];
-    __shared__ double s_wsum[kWarps];
+    __shared__ float2 s_scan[kThreads];
+    __shared__ float4 s_norm[kWarps];
     __shared__ int s_sub;
-    __shared__ double s_pre;
+    __shared__ float2 s_pre;
     __shared__ int s_last;
     for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
         const ExactItem itm = a.items[i];
         const ExactDraw d = itm.draw >= 0 ? exact_draw_from(a.draws[itm.draw]) : a.xdraw[i];
         const float4 *xs = a.xsubs + (size_t)i * a.n_sub;
         // normalisers
-        double sq = 0.0, sp = 0.0;
+        ff sq = {0.f, 0.f}, sp = {0.f, 0.f};
         for (int k = tid; k < n_grp; k += kThreads) {
             const float4 v = a.xnorm[(size_t)i * n_grp + k];
-            sq += (double)v.x + (double)v.y;
-            sp += (double)v.z + (double)v.w;
+            sq = ff_add(sq, {v.x, v.y});
+            sp = ff_add(sp, {v.z, v.w});
         }
-        sq = warp_sum_d(sq);
-        sp = warp_sum_d(sp);
-        if (lane == 0) {
-            s_red[0][warp] = sq;
-            s_red[1][warp] = sp;
+        sq = warp_sum_ff(sq);
+        sp = warp_sum_ff(sp);
+        if (lane == 0) s_norm[warp] = make_float4(sq.hi, sq.lo, sp.hi, sp.lo);
+        if (tid == 0) {
+            s_sub = -1;
+            s_last = -1;
         }
         __syncthreads();
-        sq = 0.0;
-        sp = 0.0;
+        sq = {0.f, 0.f};
+        sp = {0.f, 0.f};
         for (int w = 0; w < kWarps; ++w) {
-            sq += s_red[0][w];
-            sp += s_red[1][w];
+            const float4 v = s_norm[w];
+            sq = ff_add(sq, {v.x, v.y});
+            sp = ff_add(sp, {v.z, v.w});
         }
-        const double iq = 1.0 / sq, ip = d.has_p ? 1.0 / sp : 0.0;
+        const ff iq = ff_recip(sq), ip = d.has_p ? ff_recip(sp) : ff{0.f, 0.f};
         // exact residuals of the tokens whose sign the float32 test could not settle
         const int n_unc_all = a.xunc_n[i];
         const int n_unc = min(n_unc_all, kExactUncCap);
@@ -464,95 +468,93 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
         for (int k = tid; k < n_unc; k += kThreads) {
             const int t = a.xunc[(size_t)i * kExactUncCap + k];
             const float xq = load_elem<ES>(d.q.row, t), xp = load_elem<ES>(d.p.row, t);
-            const double w = ff_to_double(exact_w(d.q, xq, t, tab)) * iq - ff_to_double(exact_w(d.p, xp, t, tab)) * ip;
-            s_unc_w[k] = w > 0.0 ? w : 0.0;
+            const ff w = ff_sub(ff_mul(exact_w(d.q, xq, t, tab), iq), ff_mul(exact_w(d.p, xp, t, tab), ip));
+            s_unc_w[k] = w.hi > 0.f ? make_float2(w.hi, w.lo) : make_float2(0.f, 0.f);
             s_unc_sub[k] = t < n_vec * EPV ? t / (32 * EPV) : n_vsub;
-        }
-        if (tid == 0) {
-            s_sub = -1;
-            s_last = -1;
         }
         __syncthreads();
         auto W = [&](int s) {
             const float4 v = xs[s];
-            double w = ((double)v.x + (double)v.y) * iq - ((double)v.z + (double)v.w) * ip;
+            ff w = ff_sub(ff_mul({v.x, v.y}, iq), ff_mul({v.z, v.w}, ip));
             for (int k = 0; k < n_unc; ++k)
-                if (s_unc_sub[k] == s) w += s_unc_w[k];
+                if (s_unc_sub[k] == s) w = ff_add(w, {s_unc_w[k].x, s_unc_w[k].y});
             return w;
         };
         // per-thread contiguous ranges of sub-chunks, block scan of their sums
         const int per = (a.n_sub + kThreads - 1) / kThreads;
         const int s0 = min(tid * per, a.n_sub), s1 = min(s0 + per, a.n_sub);
-        double mine = 0.0;
+        ff mine = {0.f, 0.f};
         int last_pos = -1;
         for (int s = s0; s < s1; ++s) {
-            const double w = W(s);
-            mine += w;
-            if (w > 0.0) last_pos = s;
+            const ff w = W(s);
+            mine = ff_add(mine, w);
+            if (w.hi > 0.f) last_pos = s;
         }
-        double inc = mine;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const double t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-            if (lane >= o) inc += t;
-        }
-        if (lane == 31) s_wsum[warp] = inc;
+        s_scan[tid] = make_float2(mine.hi, mine.lo);
         atomicMax(&s_last, last_pos);
         __syncthreads();
-        double wbase = 0.0, R = 0.0;
-        for (int w = 0; w < kWarps; ++w) {
-            if (w < warp) wbase += s_wsum[w];
-            R += s_wsum[w];
+        for (int off = 1; off < kThreads; off <<= 1) {
+            const float2 v = tid >= off ? s_scan[tid - off] : make_float2(0.f, 0.f);
+            __syncthreads();
+            const float2 m = s_scan[tid];
+            const ff t = ff_add({m.x, m.y}, {v.x, v.y});
+            s_scan[tid] = make_float2(t.hi, t.lo);
+            __syncthreads();
         }
-        const double excl = wbase + inc - mine;
-        const double thr = d.u * R;
-        if (mine > 0.0 && excl <= thr && thr < excl + mine) {
-            double run = excl;
+        const float2 in2 = s_scan[tid];
+        const float2 ex2v = tid > 0 ? s_scan[tid - 1] : make_float2(0.f, 0.f);
+        const float2 r2 = s_scan[kThreads - 1];
+        const ff incl = {in2.x, in2.y}, excl = {ex2v.x, ex2v.y}, R = {r2.x, r2.y};
+        const float u_hi = __double2float_rn(d.u);
+        const float u_lo = __double2float_rn(d.u - (double)u_hi);
+        const ff thr = ff_mul(R, {u_hi, u_lo});
+        if (mine.hi > 0.f && ff_diff(thr, excl) >= 0.f && ff_diff(thr, incl) < 0.f) {
+            ff run = excl;
             for (int s = s0; s < s1; ++s) {
-                const double w = W(s);
-                if (w > 0.0 && thr < run + w) {
+                const ff w = W(s);
+                const ff nx = ff_add(run, w);
+                if (w.hi > 0.f && ff_diff(thr, nx) < 0.f) {
                     s_sub = s;
-                    s_pre = run;
+                    s_pre = make_float2(run.hi, run.lo);
                     break;
                 }
-                run += w;
+                run = nx;
             }
         }
         __syncthreads();
         int sub = s_sub;
-        double pre = s_pre;
+        ff pre = {s_pre.x, s_pre.y};
         if (sub < 0) {
             // u R at or past the last boundary through rounding: the last positive sub-chunk
             sub = s_last;
             if (tid == 0 && sub >= 0) {
-                double p = 0.0;
-                for (int s = 0; s < sub; ++s) p += W(s);
-                s_pre = p;
+                ff p = {0.f, 0.f};
+                for (int s = 0; s < sub; ++s) p = ff_add(p, W(s));
+                s_pre = make_float2(p.hi, p.lo);
             }
             __syncthreads();
-            pre = s_pre;
+            pre = {s_pre.x, s_pre.y};
         }
         if (warp == 0) {
             int tstar = -1;
             if (sub >= 0) {
-                double wv[EPV];
+                ff wv[EPV];
                 int ntok = 0, tok0;
                 auto wt = [&](float xq, float xp, int t) {
-                    const double q = ff_to_double(exact_w(d.q, xq, t, tab)) * iq;
+                    const ff q = ff_mul(exact_w(d.q, xq, t, tab), iq);
                     if (!d.has_p) return q;
-                    const double w = q - ff_to_double(exact_w(d.p, xp, t, tab)) * ip;
-                    return w > 0.0 ? w : 0.0;
+                    const ff w = ff_sub(q, ff_mul(exact_w(d.p, xp, t, tab), ip));
+                    return w.hi > 0.f ? w : ff{0.f, 0.f};
                 };
                 if (sub < n_vsub) {
                     const int vi = sub * 32 + lane;
                     tok0 = vi * EPV;
                     if (vi < n_vec) {
                         ntok = EPV;
-                        float xq[EPV], xp[EPV];
-                        load_vec<ES>(d.q.row, vi, xq);
-                        if (d.has_p) load_vec<ES>(d.p.row, vi, xp);
-#pragma unroll 1
-                        for (int k = 0; k < EPV; ++k) wv[k] = wt(xq[k], d.has_p ? xp[k] : xq[k], tok0 + k);
+                        const uint4 wq = __ldg(reinterpret_cast<const uint4 *>(d.q.row) + vi);
+                        const uint4 wp = d.has_p ? __ldg(reinterpret_cast<const uint4 *>(d.p.row) + vi) : wq;
+#pragma unroll
+                        for (int k = 0; k < EPV; ++k) wv[k] = wt(elem_of<ES>(wq, k), elem_of<ES>(wp, k), tok0 + k);
                     }
                 } else {
                     tok0 = n_vec * EPV + lane;
@@ -562,35 +564,44 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
                         wv[0] = wt(xq, d.has_p ? load_elem<ES>(d.p.row, tok0) : xq, tok0);
                     }
                 }
-                double lt = 0.0;
-                for (int k = 0; k < ntok; ++k) lt += wv[k];
-                double linc = lt;
+                ff lt = {0.f, 0.f};
+#pragma unroll
+                for (int k = 0; k < EPV; ++k)
+                    if (k < ntok) lt = ff_add(lt, wv[k]);
+                ff linc = lt;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
-                    const double t = __shfl_up_sync(0xFFFFFFFFu, linc, o);
-                    if (lane >= o) linc += t;
+                    const float h = __shfl_up_sync(0xFFFFFFFFu, linc.hi, o);
+                    const float l = __shfl_up_sync(0xFFFFFFFFu, linc.lo, o);
+                    if (lane >= o) linc = ff_add(linc, {h, l});
                 }
-                double cc = pre + linc - lt;
+                ff cc = ff_add(pre, ff_sub(linc, lt));
                 int hit = -1, lastk = -1;
-                double cp = cc, ch = cc;
-                for (int k = 0; k < ntok; ++k) {
-                    const double nx = cc + wv[k];
-                    if (wv[k] > 0.0) lastk = k;
-                    if (hit < 0 && wv[k] > 0.0 && thr < nx) {
-                        hit = k;
-                        cp = cc;
-                        ch = nx;
+                ff cp = cc, ch = cc;
+#pragma unroll
+                for (int k = 0; k < EPV; ++k) {
+                    if (k < ntok) {
+                        const ff nx = ff_add(cc, wv[k]);
+                        if (wv[k].hi > 0.f) lastk = k;
+                        if (hit < 0 && wv[k].hi > 0.f && ff_diff(thr, nx) < 0.f) {
+                            hit = k;
+                            cp = cc;
+                            ch = nx;
+                        }
+                        cc = nx;
                     }
-                    cc = nx;
                 }
                 const unsigned m = __ballot_sync(0xFFFFFFFFu, hit >= 0);
                 bool unres;
+                // float-float sums over ~V / 256 sub-chunks: worst-case relative error below 2e-11
+                const float tol = 2e-11f * R.hi;
                 if (m) {
                     const int src = __ffs(m) - 1;
                     tstar = __shfl_sync(0xFFFFFFFFu, tok0 + (ntok == 1 ? 0 : hit), src);
-                    const double c_prev = __shfl_sync(0xFFFFFFFFu, cp, src);
-                    const double c_hit = __shfl_sync(0xFFFFFFFFu, ch, src);
-                    unres = (thr - c_prev) < 1e-12 * R || (c_hit - thr) < 1e-12 * R;
+                    const float dp = ff_diff(thr, cp), dh = ff_diff(ch, thr);
+                    const float d_prev = __shfl_sync(0xFFFFFFFFu, dp, src);
+                    const float d_hit = __shfl_sync(0xFFFFFFFFu, dh, src);
+                    unres = d_prev < tol || d_hit < tol;
                 } else {
                     const unsigned mm = __ballot_sync(0xFFFFFFFFu, lastk >= 0);
                     const int src = mm ? 31 - __clz(mm) : 0;
@@ -601,7 +612,7 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
             }
             if (lane == 0) {
                 *d.out = tstar;
-                if (d.dbg_r) *d.dbg_r = R;
+                if (d.dbg_r) *d.dbg_r = (double)R.hi + (double)R.lo;
             }
         }
         __syncthreads();

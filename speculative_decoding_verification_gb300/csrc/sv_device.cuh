@@ -298,6 +298,45 @@ __device__ __forceinline__ ff ff_affine(float x, ff c, ff g) {
     return fast_two_sum(d.hi, d.lo);
 }
 
+// 2^(x c - r) in float-float for a float x, a float-float c and an integer r.  The product
+// x c_hi is exact through two_prod and x c_lo joins its low word; r joins the exponent after
+// the table reduction, so no float-float subtraction is needed.  The low word's rounding is
+// about 2^-48 |x c| in the exponent.  Outside |x c_hi| < 2^20 it falls back to ff_affine and
+// ff_exp2; results below 2^-126 flush to zero.
+__device__ __forceinline__ ff ff_exp2_xc(float x, ff c, int r, const float2 *tab) {
+    const ff p = two_prod(x, c.hi);
+    if (!(fabsf(p.hi) < 0x1p20f)) {
+        const ff y = ff_affine(x, c, {(float)r, 0.f});
+        return ff_exp2(y.hi, y.lo, tab);
+    }
+    if (__fsub_rn(p.hi, (float)r) < -140.0f) return {0.f, 0.f};
+    const float yl = __fmaf_rn(x, c.lo, p.lo);
+    const float kf = rintf(__fmul_rn(p.hi, 256.0f));
+    const int k = static_cast<int>(kf);
+    const float rh = __fsub_rn(p.hi, __fmul_rn(kf, 0.00390625f));   // exact
+    const float L_HI = 0.693147182464599609375f;
+    const float L_LO = -1.9046542999577520e-09f;
+    ff s = two_prod(rh, L_HI);
+    s.lo = __fmaf_rn(rh, L_LO, __fmaf_rn(yl, L_HI, s.lo));
+    s = fast_two_sum(s.hi, s.lo);
+    const ff s2 = two_prod(s.hi, s.hi);
+    const float half_s2 = __fmul_rn(0.5f, s2.hi);
+    const float cubic = __fmul_rn(__fmul_rn(s2.hi, s.hi), __fmaf_rn(s.hi, 1.0f / 24.0f, 1.0f / 6.0f));
+    const float small = __fadd_rn(__fmaf_rn(s.hi, s.lo, __fmul_rn(0.5f, s2.lo)), cubic);
+    ff t = fast_two_sum(s.hi, half_s2);
+    t.lo = __fadd_rn(t.lo, __fadd_rn(s.lo, small));
+    const int j = k & 255;
+    const int n = (k >> 8) - r;
+    const float2 T = tab[j];
+    const ff P = two_prod(T.x, t.hi);
+    ff e = fast_two_sum(T.x, P.hi);
+    const float tail = __fadd_rn(T.y, __fadd_rn(P.lo, __fmaf_rn(T.x, t.lo, __fmul_rn(T.y, t.hi))));
+    e = fast_two_sum(e.hi, __fadd_rn(e.lo, tail));
+    const float sc = pow2i(n);
+    return {__fmul_rn(e.hi, sc), __fmul_rn(e.lo, sc)};
+}
+
+
 // ------------------------------------------------------------------------------------------
 // Order-preserving keys (larger value -> larger key) for ranking logits.
 // ------------------------------------------------------------------------------------------

@@ -160,8 +160,7 @@ __device__ __forceinline__ ExactRow seq_row(const ExactArgs &a, int b, int slot)
 // Weight of token v in a row: keep(v) * 2^(x c - r) * (sc on the top-F set), float-float.
 __device__ __forceinline__ ff exact_w(const ExactRow &r, float x, int v, const float2 *tab) {
     if (x == -INFINITY || (r.filt && !in_cut(x, v, r.cut_x, r.cut_id))) return {0.f, 0.f};
-    const ff y = ff_affine(x, r.c, {r.rf, 0.f});
-    ff e = ff_exp2(y.hi, y.lo, tab);
+    ff e = ff_exp2_xc(x, r.c, (int)r.rf, tab);
     if (r.filt && in_cut(x, v, r.top_x, r.top_id)) e = ff_mul(e, {r.sc, 0.f});
     return e;
 }
@@ -233,8 +232,7 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
             const int v0 = min(c * chunk_vecs, n_vec), v1 = min(v0 + chunk_vecs, n_vec);
             auto add = [&](float x, int v) {
                 if (x == -INFINITY) return;
-                const ff y = ff_affine(x, r.c, {r.rf, 0.f});
-                const ff e = ff_exp2(y.hi, y.lo, tab);
+                const ff e = ff_exp2_xc(x, r.c, (int)r.rf, tab);
                 sa = ff_add(sa, e);
                 if (in_cut(x, v, r.cut_x, r.cut_id)) {
                     sk = ff_add(sk, e);
@@ -535,86 +533,64 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
             __syncthreads();
             pre = {s_pre.x, s_pre.y};
         }
-        if (warp == 0) {
-            int tstar = -1;
-            if (sub >= 0) {
-                ff wv[EPV];
-                int ntok = 0, tok0;
-                auto wt = [&](float xq, float xp, int t) {
-                    const ff q = ff_mul(exact_w(d.q, xq, t, tab), iq);
-                    if (!d.has_p) return q;
+        __syncthreads();   // every thread has read s_sub / s_pre before they are reused below
+        // rescan the sub-chunk holding u R: one token per thread, block scan in float-float
+        if (sub >= 0) {
+            const int t0 = sub < n_vsub ? sub * 32 * EPV : n_vec * EPV;
+            const int ntok = sub < n_vsub ? min(32 * EPV, (n_vec - sub * 32) * EPV) : a.V - n_vec * EPV;
+            ff wt = {0.f, 0.f};
+            if (tid < ntok) {
+                const int t = t0 + tid;
+                const float xq = load_elem<ES>(d.q.row, t);
+                const ff q = ff_mul(exact_w(d.q, xq, t, tab), iq);
+                if (d.has_p) {
+                    const float xp = load_elem<ES>(d.p.row, t);
                     const ff w = ff_sub(q, ff_mul(exact_w(d.p, xp, t, tab), ip));
-                    return w.hi > 0.f ? w : ff{0.f, 0.f};
-                };
-                if (sub < n_vsub) {
-                    const int vi = sub * 32 + lane;
-                    tok0 = vi * EPV;
-                    if (vi < n_vec) {
-                        ntok = EPV;
-                        const uint4 wq = __ldg(reinterpret_cast<const uint4 *>(d.q.row) + vi);
-                        const uint4 wp = d.has_p ? __ldg(reinterpret_cast<const uint4 *>(d.p.row) + vi) : wq;
-#pragma unroll
-                        for (int k = 0; k < EPV; ++k) wv[k] = wt(elem_of<ES>(wq, k), elem_of<ES>(wp, k), tok0 + k);
-                    }
+                    wt = w.hi > 0.f ? w : ff{0.f, 0.f};
                 } else {
-                    tok0 = n_vec * EPV + lane;
-                    if (tok0 < a.V) {
-                        ntok = 1;
-                        const float xq = load_elem<ES>(d.q.row, tok0);
-                        wv[0] = wt(xq, d.has_p ? load_elem<ES>(d.p.row, tok0) : xq, tok0);
-                    }
+                    wt = q;
                 }
-                ff lt = {0.f, 0.f};
-#pragma unroll
-                for (int k = 0; k < EPV; ++k)
-                    if (k < ntok) lt = ff_add(lt, wv[k]);
-                ff linc = lt;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float h = __shfl_up_sync(0xFFFFFFFFu, linc.hi, o);
-                    const float l = __shfl_up_sync(0xFFFFFFFFu, linc.lo, o);
-                    if (lane >= o) linc = ff_add(linc, {h, l});
-                }
-                ff cc = ff_add(pre, ff_sub(linc, lt));
-                int hit = -1, lastk = -1;
-                ff cp = cc, ch = cc;
-#pragma unroll
-                for (int k = 0; k < EPV; ++k) {
-                    if (k < ntok) {
-                        const ff nx = ff_add(cc, wv[k]);
-                        if (wv[k].hi > 0.f) lastk = k;
-                        if (hit < 0 && wv[k].hi > 0.f && ff_diff(thr, nx) < 0.f) {
-                            hit = k;
-                            cp = cc;
-                            ch = nx;
-                        }
-                        cc = nx;
-                    }
-                }
-                const unsigned m = __ballot_sync(0xFFFFFFFFu, hit >= 0);
-                bool unres;
-                // float-float sums over ~V / 256 sub-chunks: worst-case relative error below 2e-11
-                const float tol = 2e-11f * R.hi;
-                if (m) {
-                    const int src = __ffs(m) - 1;
-                    tstar = __shfl_sync(0xFFFFFFFFu, tok0 + (ntok == 1 ? 0 : hit), src);
-                    const float dp = ff_diff(thr, cp), dh = ff_diff(ch, thr);
-                    const float d_prev = __shfl_sync(0xFFFFFFFFu, dp, src);
-                    const float d_hit = __shfl_sync(0xFFFFFFFFu, dh, src);
-                    unres = d_prev < tol || d_hit < tol;
-                } else {
-                    const unsigned mm = __ballot_sync(0xFFFFFFFFu, lastk >= 0);
-                    const int src = mm ? 31 - __clz(mm) : 0;
-                    tstar = __shfl_sync(0xFFFFFFFFu, tok0 + (ntok == 1 ? 0 : max(lastk, 0)), src);
-                    unres = true;
-                }
-                if (lane == 0 && unres) stats_add(a.stats, &a.stats->unresolved, 1);
             }
-            if (lane == 0) {
-                *d.out = tstar;
-                if (d.dbg_r) *d.dbg_r = (double)R.hi + (double)R.lo;
+            ff inc = wt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float h = __shfl_up_sync(0xFFFFFFFFu, inc.hi, o);
+                const float l = __shfl_up_sync(0xFFFFFFFFu, inc.lo, o);
+                if (lane >= o) inc = ff_add(inc, {h, l});
             }
+            if (lane == 31) s_norm[warp] = make_float4(inc.hi, inc.lo, 0.f, 0.f);
+            if (tid == 0) {
+                s_sub = 0x7FFFFFFF;   // first hit token (thread index)
+                s_last = -1;          // last positive token
+            }
+            __syncthreads();
+            ff base = pre;
+            for (int w = 0; w < warp; ++w) base = ff_add(base, {s_norm[w].x, s_norm[w].y});
+            const ff c_hit = ff_add(base, inc), c_prev = ff_add(base, ff_sub(inc, wt));
+            if (wt.hi > 0.f) {
+                atomicMax(&s_last, tid);
+                if (ff_diff(thr, c_hit) < 0.f) atomicMin(&s_sub, tid);
+            }
+            __syncthreads();
+            const int hit = s_sub;
+            // float-float sums over ~V / 256 sub-chunks: worst-case relative error below 2e-11,
+            // plus the exponents' low-word rounding, about 2^-48 |x c| <= 2^-48 (|r| + 126)
+            const float tol = (2e-11f + 0x1p-46f * (fabsf(d.q.rf) + fabsf(d.p.rf) + 252.0f)) * R.hi;
+            if (hit != 0x7FFFFFFF) {
+                if (tid == hit) {
+                    *d.out = t0 + tid;
+                    if (ff_diff(thr, c_prev) < tol || ff_diff(c_hit, thr) < tol)
+                        stats_add(a.stats, &a.stats->unresolved, 1);
+                }
+            } else if (tid == 0) {
+                // rounding left u R past the sub-chunk: its last positive token, unresolved
+                *d.out = s_last >= 0 ? t0 + s_last : -1;
+                stats_add(a.stats, &a.stats->unresolved, 1);
+            }
+        } else if (tid == 0) {
+            *d.out = -1;
         }
+        if (tid == 0 && d.dbg_r) *d.dbg_r = (double)R.hi + (double)R.lo;
         __syncthreads();
     }
 }

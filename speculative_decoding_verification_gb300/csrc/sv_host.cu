@@ -87,6 +87,14 @@ __global__ void k_selftest_exp2(double lo, double hi, long long n, unsigned long
             const ff y = {x, 0.0f};
             const ff e = ff_exp2(y.hi, y.lo, tab);
             e_ff = fmax(e_ff, fabs(ff_to_double(e) - ref) / ref);
+            // the exponential with an integer offset folded into the exponent, 2^(x * 1 - r)
+            const ff e0 = ff_exp2_xc(x, {1.0f, 0.0f}, 0, tab);
+            e_ff = fmax(e_ff, fabs(ff_to_double(e0) - ref) / ref);
+            if (x >= -60.0f) {
+                const ff e5 = ff_exp2_xc(x, {1.0f, 0.0f}, 5, tab);
+                const double ref5 = exp2((double)x - 5.0);
+                e_ff = fmax(e_ff, fabs(ff_to_double(e5) - ref5) / ref5);
+            }
         }
     }
     // non-negative doubles order like their bit patterns

@@ -283,8 +283,7 @@ struct NucleusArgs {
 // Float-float mass of one element (exact tier arithmetic).
 __device__ __forceinline__ double exact_mass(float x, ff c, float rf, const float2 *tab) {
     if (x == -INFINITY) return 0.0;
-    const ff y = ff_affine(x, c, {rf, 0.f});
-    return ff_to_double(ff_exp2(y.hi, y.lo, tab));
+    return ff_to_double(ff_exp2_xc(x, c, (int)rf, tab));
 }
 
 // Mass-weighted radix select: the key K* at which the running mass from the top, in

@@ -69,3 +69,15 @@ def test_single_rank_helpers_need_no_process_group():
     bench.barrier(1)
     assert bench.whole_job_rate(1.0, 1, 0.5) == pytest.approx(2000.0)
     assert bench.rank_seed(4, 0) == 4
+
+
+def test_stats_traffic_from_committed_capture():
+    """The bench's roofline traffic comes from the committed ncu summary only while the
+    statistics pass's sources are unchanged; it must then be close to the algorithmic bytes."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.stats_traffic(128) is None
+    t = bench.stats_traffic(512)
+    if t is not None:
+        alg = (512 * 6 + 256 * 5) * 128256 * 2
+        assert alg <= t < 1.02 * alg

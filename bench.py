@@ -248,8 +248,10 @@ def run_ours(args, rank, world, local_rank):
     ot = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
     stats = sv.new_stats(dev)
 
+    lazy = args.path == "lazy"
+
     def step():
-        sv.sv_verify(tgt, drf, toks_d, u_d, T_d, accept_len=al, out_tokens=ot, stats=stats, workspace=ws)
+        sv.sv_verify(tgt, drf, toks_d, u_d, T_d, accept_len=al, out_tokens=ot, stats=stats, workspace=ws, lazy=lazy)
 
     # clocks are sampled from before the warm-up (GPU under load) to the end of the timed region
     clocks = ClockSampler(local_rank)
@@ -260,46 +262,61 @@ def run_ours(args, rank, world, local_rank):
     if sv.read_stats(stats)["status"] != 0:
         raise RuntimeError(f"verify failed: {sv.read_stats(stats)}")
 
-    # ---- timed region: device time of K steps; the statistics pass timed through the hook ----
+    # ---- timed region: device time of K steps; the streaming pass timed through the hook ----
     n = args.steps
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-    for e in ev_b + ev_e:
-        e.record()          # torch creates the underlying CUDA event on first record
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    start.record()
-    for i in range(n):
-        lib.sv_set_profile_events(ev_b[i].cuda_event, ev_e[i].cuda_event)
-        step()
-    end.record()
-    torch.cuda.synchronize()
-    lib.sv_set_profile_events(None, None)
+
+    def timed(fn):
+        ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in ev_b + ev_e:
+            e.record()          # torch creates the underlying CUDA event on first record
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record()
+        for i in range(n):
+            lib.sv_set_profile_events(ev_b[i].cuda_event, ev_e[i].cuda_event)
+            fn()
+        end.record()
+        torch.cuda.synchronize()
+        lib.sv_set_profile_events(None, None)
+        barrier(world)
+        ms = start.elapsed_time(end) / n
+        k_ms = statistics.mean(ev_b[i].elapsed_time(ev_e[i]) for i in range(n))
+        st = sv.read_stats(stats)
+        if st["status"] != 0:
+            raise RuntimeError(f"verify failed: {st}")
+        return max_over_ranks(ms, world), k_ms, st
+
+    ms_max, k1_ms, final = timed(step)
     clk = clocks.stop()
-    barrier(world)
-    ms = start.elapsed_time(end) / n
-    k1_ms = statistics.mean(ev_b[i].elapsed_time(ev_e[i]) for i in range(n))
-    ms_max = max_over_ranks(ms, world)
     value = whole_job_rate(1.0, world, ms_max)
-    final = sv.read_stats(stats)
-    if final["status"] != 0:
-        raise RuntimeError(f"verify failed: {final}")
 
     cfg = config_block(w)
-    k1_bytes = cfg["logit_bytes_read_per_round"]
     peak, peak_kind = load_peaks()
+    # bytes the streaming pass reads: every needed row (sv_verify), or the rows up to each first
+    # rejection (sv_verify_lazy), counted by the library
+    k1_bytes = final["rows"] * V * 2
     achieved = k1_bytes / (k1_ms * 1e-3) / 1e9
     line = {"metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world, "steps": n, "warmup": args.warmup,
             "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": cfg,
+            "data": "synthetic", "config": dict(cfg, path=args.path, bytes_read_per_round=k1_bytes),
             "hbm_gbs_per_step": k1_bytes / (ms_max * 1e-3) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": stats_traffic(w.B), "kernel": "k_stats",
+                         "frac": achieved / peak, "traffic": stats_traffic(w.B) if not lazy else None,
+                         "kernel": "k_lazy" if lazy else "k_stats",
                          "peak_source": f"{peak_kind} copy bandwidth", "kernel_ms": k1_ms},
             "gpu_launches": 5 * n, "clocks": clk,
             "decisions": {k: final[k] for k in ("accept_tests", "draws", "reresolved", "near_boundary",
                                                 "unresolved")}}
+    # the other verification path on the same inputs (same outputs; see config.path)
+    other = "eager" if lazy else "lazy"
+    ms_o, k_o, st_o = timed(lambda: sv.sv_verify(tgt, drf, toks_d, u_d, T_d, accept_len=al, out_tokens=ot,
+                                                 stats=stats, workspace=ws, lazy=not lazy))
+    b_o = st_o["rows"] * V * 2
+    line[other] = {"value": whole_job_rate(1.0, world, ms_o), "unit": "rounds/s", "ms_per_step": ms_o,
+                   "bytes_read_per_round": b_o, "kernel": "k_stats" if lazy else "k_lazy", "kernel_ms": k_o,
+                   "kernel_gbs": b_o / (k_o * 1e-3) / 1e9, "frac": b_o / (k_o * 1e-3) / 1e9 / peak}
     if args.kernel_only:
         return line if rank == 0 else None
 
@@ -320,7 +337,8 @@ def run_ours(args, rank, world, local_rank):
     def e2e_step():
         for dst, src in ((tgt_x, tgt_h), (drf_x, drf_h), (tok_x, tok_h), (u_x, u_h), (T_x, T_h)):
             dst.copy_(src, non_blocking=True)
-        sv.sv_verify(tgt_x, drf_x, tok_x, u_x, T_x, accept_len=al, out_tokens=ot, stats=stats, workspace=ws)
+        sv.sv_verify(tgt_x, drf_x, tok_x, u_x, T_x, accept_len=al, out_tokens=ot, stats=stats, workspace=ws,
+                     lazy=lazy)
         al_h.copy_(al, non_blocking=True)
         ot_h.copy_(ot, non_blocking=True)
 
@@ -358,6 +376,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--batch", type=int, default=512, help="sequences per round (512: the stated workload)")
+    ap.add_argument("--path", choices=["eager", "lazy"], default="eager",
+                    help="sv_verify (every candidate row) or sv_verify_lazy (rows up to each first rejection)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="report the device-timed steps only (no end-to-end or CPU-baseline measurement)")
     args = ap.parse_args()

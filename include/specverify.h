@@ -156,6 +156,32 @@ sv_status sv_verify(const void *target_logits, int64_t t_row_pitch,
                     void *workspace, size_t workspace_bytes, sv_stream_t stream);
 
 /* ----------------------------------------------------------------------------------------
+ * sv_verify_lazy — sv_verify that reads each sequence's rows position by position and stops at
+ * its first rejection.
+ * [SpS notes §3: after the first rejection the draft tokens to its right are discarded, so
+ *  their rows decide nothing; SURVEY's "lazy positions"]
+ *
+ * Arguments, workspace (sv_verify_workspace_size) and outputs are those of sv_verify, and the
+ * outputs are identical.  Rows after a sequence's first rejection (after its first greedy
+ * mismatch) are never read: their debug fields stay NaN, they do not count in stats.rows, and
+ * non-finite values in them raise no error.  The bytes read fall with the acceptance rate
+ * (about 30% of sv_verify's at the large-batch workload).  Calls with top_p or an active
+ * sigma_{F,C} (saguaro_F > 0 and saguaro_C != 1) run the sv_verify pipeline unchanged.  One
+ * kernel of the call waits on work that other blocks of the same launch queue; it is
+ * launched cooperatively, so SV_ERR_CUDA results if the device cannot hold all its blocks.
+ * -------------------------------------------------------------------------------------- */
+sv_status sv_verify_lazy(const void *target_logits, int64_t t_row_pitch,
+                         const void *draft_logits, int64_t d_row_pitch, int d_rows_per_seq,
+                         sv_dtype dtype,
+                         const int32_t *draft_tokens, const double *uniforms,
+                         int B, int K, int V,
+                         const float *temperature, const float *top_p,
+                         int saguaro_F, float saguaro_C,
+                         int32_t *accept_len, int32_t *out_tokens,
+                         double *debug, sv_stats *stats,
+                         void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
  * sv_verify_static — sv_verify for callers that cannot allocate device memory.  The paper
  * has no counterpart: this is a deployment convenience, not a step of the method.
  *
@@ -171,7 +197,7 @@ sv_status sv_verify(const void *target_logits, int64_t t_row_pitch,
  *
  *  - Limit: a call whose scratch need for (B, K, V, dtype) exceeds SV_STATIC_SCRATCH_BYTES
  *    returns SV_ERR_WORKSPACE before any device work (B = 512, K = 5, V = 128256 needs about
- *    28.5 MiB and fits).  sv_verify_workspace_size(B, K, V) bounds the need from above.
+ *    28.7 MiB and fits).  sv_verify_workspace_size(B, K, V) bounds the need from above.
  *  - Set-up: the first call on a device, with that device current, looks up the array's
  *    device address (cudaGetSymbolAddress) and caches it for that device; a failure there
  *    returns SV_ERR_CUDA.  Make that first call before any stream capture.

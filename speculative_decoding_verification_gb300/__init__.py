@@ -86,8 +86,9 @@ def read_stats(t: torch.Tensor) -> dict:
 
 
 def sv_verify(target, draft, draft_tokens, uniforms, temperature, top_p=None, saguaro_F=0, saguaro_C=1.0,
-              accept_len=None, out_tokens=None, debug=False, stats=None, workspace=None, stream=None):
-    """sv_verify on torch CUDA tensors.
+              accept_len=None, out_tokens=None, debug=False, stats=None, workspace=None, stream=None, lazy=False):
+    """sv_verify (or, with lazy=True, sv_verify_lazy: same outputs, rows after each sequence's
+    first rejection left unread) on torch CUDA tensors.
 
     target [B, K+1, V] and draft [B, R>=K, V] (float32 or bfloat16, same dtype); draft_tokens
     int32 [B, K]; uniforms float64 [B, K+1]; temperature float32 [B]; top_p float32 [B] or None.
@@ -115,11 +116,12 @@ def sv_verify(target, draft, draft_tokens, uniforms, temperature, top_p=None, sa
         stats = new_stats(dev)
     ws_bytes = lib.sv_verify_workspace_size(B, K, V)
     ws = (workspace or _default_ws).get(ws_bytes, dev)
-    code = lib.sv_verify(_ptr(target), t_pitch, d_ptr, d_pitch, d_rows, _dtype_code(target),
-                         _ptr(draft_tokens if K > 0 else None), _ptr(uniforms), B, K, V, _ptr(temperature),
-                         _ptr(top_p), int(saguaro_F), float(saguaro_C), _ptr(accept_len), _ptr(out_tokens),
-                         _ptr(dbg), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream))
-    _abi.check("sv_verify", code)
+    fn = lib.sv_verify_lazy if lazy else lib.sv_verify
+    code = fn(_ptr(target), t_pitch, d_ptr, d_pitch, d_rows, _dtype_code(target),
+              _ptr(draft_tokens if K > 0 else None), _ptr(uniforms), B, K, V, _ptr(temperature),
+              _ptr(top_p), int(saguaro_F), float(saguaro_C), _ptr(accept_len), _ptr(out_tokens),
+              _ptr(dbg), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream))
+    _abi.check("sv_verify_lazy" if lazy else "sv_verify", code)
     return accept_len, out_tokens, dbg, stats
 
 

@@ -54,6 +54,8 @@ struct VerifyPlan {
     size_t off_nuc = 0, off_top = 0;
     size_t off_xpart = 0, off_xdraw = 0, off_xsubs = 0, off_xnorm = 0, off_xunc_n = 0, off_xunc = 0;
     int x_split = 1;                       // chunks per row in the float-float pass
+    size_t off_lz_units = 0, off_lz_pos = 0;   // lazy verification queue
+    long long lz_cap = 0;                  // queue capacity: every (row, chunk) unit once
     size_t bytes = 0;
 };
 

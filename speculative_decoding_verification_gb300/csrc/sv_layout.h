@@ -133,7 +133,10 @@ struct Counters {
     unsigned barrier;       // grid barrier of the exact tier
     int next_unit;          // statistics pass: next (row, chunk) unit to hand out
     int next_draw_unit;     // draw pass: next (item, chunk) unit to hand out
-    int pad[11];
+    int q_head;             // lazy verification: next queue position to claim (position 0, then later)
+    int q0_tail, q_tail;    // lazy verification: position-0 units / later units queued
+    int n_pending;          // lazy verification: sequences not finished yet
+    int pad[7];
 };
 
 inline int div_up(long long a, long long b) { return (int)((a + b - 1) / b); }

@@ -44,7 +44,9 @@ struct UnitInfo {
 };
 
 template <int ES>
-__device__ __forceinline__ UnitInfo stats_unit(const StatsArgs &a, long long u) {
+// t_cache: the temperatures in shared memory (n_cache of them), or nullptr.
+__device__ __forceinline__ UnitInfo stats_unit(const StatsArgs &a, long long u, const float *t_cache = nullptr,
+                                               int n_cache = 0) {
     UnitInfo ui;
     ui.rid = u / a.n_split;
     ui.chunk = static_cast<int>(u - ui.rid * a.n_split);
@@ -53,7 +55,7 @@ __device__ __forceinline__ UnitInfo stats_unit(const StatsArgs &a, long long u) 
     const RowSet &rs = a.set[s];
     const long long b = lr / rs.rows_used;
     const long long j = lr - b * rs.rows_used;
-    const float T = a.temperature ? a.temperature[b] : 1.0f;
+    const float T = b < n_cache ? t_cache[b] : (a.temperature ? a.temperature[b] : 1.0f);
     ui.greedy = (T == 0.0f);
     ui.needed = !(rs.skip_greedy && ui.greedy);
     ui.row = rs.base + (b * rs.rows_per_seq + j) * rs.pitch_bytes;
@@ -297,6 +299,7 @@ struct TileMeta {
     int fv, nv;           // first vector of the tile within the row, vectors in the tile
     int tail0, n_tail;    // scalar tail of the row (last tile of a row's last chunk)
     int flags;            // kTileFirst | kTileLast | kTileGreedy | kTileEnd
+    int aux;              // lazy verification: (warps expected for the position << 1) | completing
 };
 constexpr int kTileFirst = 1, kTileLast = 2, kTileGreedy = 4, kTileEnd = 8;
 
@@ -386,6 +389,7 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_stats(const StatsArgs a) {
                     m.tail0 = ui.tail0;
                     m.n_tail = ui.n_tail;
                     m.flags = (t == 0 ? kTileFirst : 0) | (t == nt - 1 ? kTileLast : 0) | (ui.greedy ? kTileGreedy : 0);
+                    m.aux = 0;
                     meta[st] = m;
                     if (nv > 0) {
                         mbar_arrive_expect_tx(&full[st], (uint32_t)nv * 16u);

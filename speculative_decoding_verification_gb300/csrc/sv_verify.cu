@@ -15,6 +15,7 @@
 //   k_exact        float-float tier for the decisions the margins could not settle
 #include <math.h>
 
+#include "sv_accept.cuh"
 #include "sv_draw.cuh"
 #include "sv_exact.cuh"
 #include "sv_host.h"
@@ -22,65 +23,6 @@
 #include "sv_stats.cuh"
 
 namespace sv {
-
-struct AcceptArgs {
-    RowSet tgt, drf;
-    int K, V;
-    const float *temperature;
-    const float *top_p;
-    int sag_on;
-    float sag_C;
-    const int32_t *tokens;
-    const double *uniforms;
-    int32_t *accept_len;
-    int32_t *out_tokens;
-    double *debug;
-    sv_stats *stats;
-    const WarpPartial *part;
-    int n_split;
-    long long n_rows0;
-    RowStat *rowstat;
-    const NucleusCut *nuc;
-    const TopSet *top;
-    DrawItem *draws;
-    ExactItem *exact;
-    int *exact_unc;
-    Counters *counters;
-};
-
-// Draw parameters of one row, float32 only: inv_s = 1 / (S * nucleus mass * Saguaro normaliser).
-__device__ __forceinline__ DrawRow draw_row(const char *row, float T, const RowStat &rs, const NucleusCut *nc,
-                                            const TopSet *ts, float sag_C) {
-    DrawRow d;
-    d.row = row;
-    log2e_over(T, d.c_hi, d.c_lo);
-    d.rf = (float)rs.r;
-    float norm = rs.s_hi;
-    double err = (double)rs.err + 4.0 * kU32;   // S_lo dropped, products, reciprocal
-    d.cut_x = -INFINITY;
-    d.cut_id = 0x7FFFFFFF;
-    if (nc) {
-        d.cut_x = nc->cut_x;
-        d.cut_id = nc->cut_id;
-        norm = __fmul_rn(norm, nc->mass_f);
-        err += 2.0 * (double)rs.err + kU32 + 1e-12;   // the kept mass is a ratio of two sums of the same pass
-    }
-    d.top_x = INFINITY;
-    d.top_id = -1;
-    d.sc_d = 1.0f;
-    if (ts) {
-        d.top_x = ts->top_x;
-        d.top_id = ts->top_id;
-        d.sc_d = sag_C;
-        norm = __fmul_rn(norm, ts->z_f);
-        err += (double)ts->z_err_f + kU32;
-    }
-    d.inv_s = __frcp_rn(norm);
-    // mean |y| under the normalised weights: at most the row's, divided by the kept mass and z
-    d.ay = __fdiv_ru(rs.ay * (1.0f + 0x1p-20f), __fdiv_rn(norm, rs.s_hi) * (1.0f - 0x1p-20f));
-    d.norm_err = err;
-    return d;
-}
 
 template <int ES>
 __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
@@ -145,56 +87,14 @@ __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
             if (greedy) {
                 acc = (s == rs[lane].argmax);
             } else {
-                const long long rid_t = (long long)b * n_t + lane;
-                const long long rid_d = a.n_rows0 + (long long)b * K + lane;
-                const RowSet &ts = a.tgt, &ds = a.drf;
-                const char *trow = ts.base + ((long long)b * ts.rows_per_seq + lane) * ts.pitch_bytes;
-                const char *drow = ds.base + ((long long)b * ds.rows_per_seq + lane) * ds.pitch_bytes;
-                const float xt = load_elem<ES>(trow, s);
-                const float xd = load_elem<ES>(drow, s);
-                const RowStat &rq = rs[lane], &rp = rs[n_t + lane];
-                float num = rp.s_hi, den = rq.s_hi;
-                float delta = (float)(kEx2RelErr + 8.0 * kU32 + 1e-10) + rq.err + rp.err;
-                keep_q = xt != -INFINITY;
-                keep_p = xd != -INFINITY;
-                if (a.nuc) {
-                    const NucleusCut &nq = a.nuc[rid_t], &np = a.nuc[rid_d];
-                    keep_q = keep_q && (xt > nq.cut_x || (xt == nq.cut_x && s <= nq.cut_id));
-                    keep_p = keep_p && (xd > np.cut_x || (xd == np.cut_x && s <= np.cut_id));
-                    num = __fmul_rn(num, np.mass_f);
-                    den = __fmul_rn(den, nq.mass_f);
-                    delta += 2.0f * (rq.err + rp.err) + (float)(2.0 * kU32);
-                }
-                if (a.sag_on && a.top) {
-                    const TopSet &t = a.top[rid_d];
-                    in_top = xd > t.top_x || (xd == t.top_x && s <= t.top_id);
-                    num = __fmul_rn(num, t.z_f);
-                    if (in_top) den = __fmul_rn(den, a.sag_C);
-                    delta += t.z_err_f + (float)kU32;
-                }
-                if (!keep_p) {
-                    ratio = keep_q ? INFINITY : 0.0f;
-                } else if (!keep_q) {
-                    ratio = 0.0f;
-                } else {
-                    const ff c = {c_hi, c_lo};
-                    const ff yq = ff_affine(xt, c, {(float)rq.r, 0.f});
-                    const ff yp = ff_affine(xd, c, {(float)rp.r, 0.f});
-                    const ff dy = ff_sub(yq, yp);
-                    delta += 1e-12f * (fabsf(yq.hi) + fabsf(yp.hi));   // float-float y and c
-                    const float e = ex2_fast(dy.hi) * fmaf(dy.lo, (float)kLn2, 1.0f);
-                    ratio = e * __fdiv_rn(num, den);
-                }
-                delta *= 1.01f;
-                const float rr = fminf(1.0f, ratio);
-                const float lo = fminf(1.0f, ratio * (1.0f - delta));
-                const float hi = fminf(1.0f, ratio * (1.0f + delta));
-                const float u = __double2float_rn(a.uniforms[(size_t)b * (K + 1) + lane]);
-                // u is rounded to float32 (relative error 2^-24, inside delta's 8u); a ratio that
-                // underflowed is decided by the float-float tier unless u is clearly above it
-                acc = u < rr;
-                amb = (u >= lo && u < hi) || (keep_q && keep_p && ratio < 0x1p-100f && u < 0x1p-90f);
-                near = fabsf(u - rr) < 1e-6f;
+                const AcceptOutcome o = accept_test<ES>(a, b, lane, s, c_hi, c_lo, rs[lane], rs[n_t + lane]);
+                acc = o.acc;
+                amb = o.amb;
+                near = o.near;
+                keep_q = o.keep_q;
+                keep_p = o.keep_p;
+                in_top = o.in_top;
+                ratio = o.ratio;
             }
         }
     }
@@ -328,6 +228,9 @@ VerifyPlan plan_verify(int B, int K, int V, int es) {
     p.off_xnorm = cv.take<float4>(cap * p.x_split);
     p.off_xunc_n = cv.take<int>(cap);
     p.off_xunc = cv.take<int>(cap * kExactUncCap);
+    p.lz_cap = n_cand * p.n_split;
+    p.off_lz_units = cv.take<unsigned long long>((size_t)p.lz_cap);
+    p.off_lz_pos = cv.take<int>((size_t)B);
     p.bytes = cv.off + 256;
     return p;
 }

@@ -82,8 +82,8 @@ struct AcceptOutcome {
 // products and the quotient carry kEx2RelErr + 8u, the row sums err_q + err_p, the masses
 // 2(err_q + err_p), the normaliser z_err; u < ratio is certain outside ratio (1 -+ delta).
 template <int ES>
-__device__ __forceinline__ AcceptOutcome accept_test(const AcceptArgs &a, int b, int j, int s, float c_hi, float c_lo,
-                                                     const RowStat &rq, const RowStat &rp) {
+__device__ __forceinline__ AcceptOutcome accept_test(const AcceptArgs &a, int b, int j, int s, double u_acc,
+                                                     float c_hi, float c_lo, const RowStat &rq, const RowStat &rp) {
     bool acc = false, amb = false, near = false;
     bool keep_q = false, keep_p = false, in_top = false;
     float ratio = NAN;
@@ -130,7 +130,7 @@ __device__ __forceinline__ AcceptOutcome accept_test(const AcceptArgs &a, int b,
     const float rr = fminf(1.0f, ratio);
     const float lo = fminf(1.0f, ratio * (1.0f - delta));
     const float hi = fminf(1.0f, ratio * (1.0f + delta));
-    const float u = __double2float_rn(a.uniforms[(size_t)b * (a.K + 1) + j]);
+    const float u = __double2float_rn(u_acc);
     // u is rounded to float32 (relative error 2^-24, inside delta's 8u); a ratio that
     // underflowed is decided by the float-float tier unless u is clearly above it
     acc = u < rr;

@@ -135,7 +135,6 @@ __global__ void __launch_bounds__(kThreads) k_lazy_init(const LazyArgs L, int B)
 template <int ES>
 __device__ void lazy_draw(const AcceptArgs &a, int b, int k, float T, const RowStat &rq, const RowStat &rp) {
     const int K = a.K;
-    lazy_outputs(a, b, k, -1);
     DrawItem it;
     const char *qrow = a.tgt.base + ((long long)b * a.tgt.rows_per_seq + k) * a.tgt.pitch_bytes;
     it.q = draw_row(qrow, T, rq, nullptr, nullptr, 1.0f);
@@ -159,13 +158,28 @@ __device__ void lazy_draw(const AcceptArgs &a, int b, int k, float T, const RowS
 }
 
 // The finisher warp: the batch of rows (starting at position j0) of sequence b is complete.
+// Latency matters here (a sequence's next batch waits for it): the loads it needs are issued
+// together up front, both rows' partials are combined in one pass each, and outputs are
+// written by all lanes.
 template <int ES>
 __device__ void lazy_finish(const LazyArgs &L, int b, int j0, int kind, int cum) {
     const AcceptArgs &a = L.acc;
     const int lane = threadIdx.x & 31;
     const int K = a.K, ns = L.st.n_split;
     const float T = a.temperature[b];
+    const int tok_l = lane < K ? a.tokens[(size_t)b * K + lane] : -1;                // s_lane
+    const double u_l = lane <= K ? a.uniforms[(size_t)b * (K + 1) + lane] : 0.0;    // u_lane
     const bool greedy = (T == 0.0f);
+    auto token = [&](int j) {
+        const int v = __shfl_sync(0xFFFFFFFFu, tok_l, j & 31);
+        return j < 32 ? v : a.tokens[(size_t)b * K + j];
+    };
+    // s_1..s_k, then tstar (-1: a draw fills it), then -1; accept_len = k
+    auto outputs = [&](int k, int tstar) {
+        int32_t *outs = a.out_tokens + (size_t)b * (K + 1);
+        for (int j = lane; j <= K; j += 32) outs[j] = j < k ? (j < 32 ? tok_l : a.tokens[(size_t)b * K + j]) : (j == k ? tstar : -1);
+        if (lane == 0) a.accept_len[b] = k;
+    };
     auto combine = [&](long long rid, int &bad) {
         const RowStat r = combine_row(a.part + (size_t)rid * ns * kWarps, ns * kWarps, greedy, T);
         if (lane == 0) {
@@ -179,13 +193,17 @@ __device__ void lazy_finish(const LazyArgs &L, int b, int j0, int kind, int cum)
     };
     // statistics of the batch's rows that the walk below did not reach (for the float-float tier)
     auto combine_rest = [&](int j_from, int &bad) {
-        int n = 0;
-        for (int jj = j_from; jj <= K; ++jj, ++n) combine((long long)b * (K + 1) + jj, bad);
-        for (int jj = j_from; jj < K; ++jj, ++n) combine(L.st.n_rows0 + (long long)b * K + jj, bad);
-        return n;
+        for (int jj = j_from; jj <= K; ++jj) combine((long long)b * (K + 1) + jj, bad);
+        for (int jj = j_from; jj < K; ++jj) combine(L.st.n_rows0 + (long long)b * K + jj, bad);
     };
     auto done = [&]() {
         if (lane == 0) atomicSub(&L.st.counters->n_pending, 1);
+    };
+    auto to_exact = [&]() {
+        if (lane == 0) {
+            stats_add(a.stats, &a.stats->reresolved, 1);
+            push_exact(a.counters, a.exact, a.exact_unc, {-1, b}, a.stats);
+        }
     };
     int bad = 0;
     if (lane == 0) {   // rows this batch streamed
@@ -195,14 +213,9 @@ __device__ void lazy_finish(const LazyArgs &L, int b, int j0, int kind, int cum)
     }
     if (kind == kBatchComplete) {
         combine_rest(j0, bad);
-        if (lane == 0) {
-            if (bad) {
-                lazy_outputs(a, b, 0, -1);
-            } else {
-                stats_add(a.stats, &a.stats->reresolved, 1);
-                push_exact(a.counters, a.exact, a.exact_unc, {-1, b}, a.stats);
-            }
-        }
+        bad = __shfl_sync(0xFFFFFFFFu, bad, 0);
+        if (bad) outputs(0, -1);
+        else to_exact();
         done();
         return;
     }
@@ -214,21 +227,25 @@ __device__ void lazy_finish(const LazyArgs &L, int b, int j0, int kind, int cum)
         const bool with_p = !greedy && j < K;
         RowStat rp{};
         if (with_p) rp = combine(L.st.n_rows0 + (long long)b * K + j, bad);
-        // lane 0 decides: 0 finished, 1 accepted (next position), 2 handed to the float-float tier
-        int verdict = 0;
+        const int s = j < K ? token(j) : -1;
+        const double u_j = __shfl_sync(0xFFFFFFFFu, u_l, j);
+        // lane 0 decides: 0 finished with (k, tstar), 1 accepted, 2 for the float-float tier
+        int verdict = 0, k = 0, tstar = -1;
         if (lane == 0) {
             if (bad) {
-                lazy_outputs(a, b, 0, -1);
+                k = 0;
             } else if (greedy) {
-                if (j < K && a.tokens[(size_t)b * K + j] == rq.argmax) verdict = 1;
-                else lazy_outputs(a, b, j, rq.argmax);
+                if (j < K && s == rq.argmax) verdict = 1;
+                else {
+                    k = j;
+                    tstar = rq.argmax;
+                }
             } else {
                 if (a.debug) {
                     double *dbg = a.debug + ((size_t)b * (K + 1) + j) * SV_DEBUG_FIELDS;
                     dbg[SV_DBG_LSE_Q] = rs_g(rq) * kLn2;
                     dbg[SV_DBG_MASS_Q] = 1.0;
                     if (with_p) {
-                        const int s = a.tokens[(size_t)b * K + j];
                         const double cd = 1.4426950408889634074 / (double)T;
                         const char *trow = a.tgt.base + ((long long)b * a.tgt.rows_per_seq + j) * a.tgt.pitch_bytes;
                         const char *drow = a.drf.base + ((long long)b * a.drf.rows_per_seq + j) * a.drf.pitch_bytes;
@@ -243,45 +260,43 @@ __device__ void lazy_finish(const LazyArgs &L, int b, int j0, int kind, int cum)
                     }
                 }
                 if (with_p) {
-                    const int s = a.tokens[(size_t)b * K + j];
-                    const AcceptOutcome o = accept_test<ES>(a, b, j, s, c_hi, c_lo, rq, rp);
+                    const AcceptOutcome o = accept_test<ES>(a, b, j, s, u_j, c_hi, c_lo, rq, rp);
                     stats_add(a.stats, &a.stats->accept_tests, 1);
                     if (o.near) stats_add(a.stats, &a.stats->near_boundary, 1);
                     if (o.amb) {
                         verdict = 2;
-                        lazy_outputs(a, b, j, -1);   // the float-float tier writes the final outputs
+                        k = j;   // placeholder outputs; the float-float tier writes the final ones
                     } else if (o.acc) {
                         verdict = 1;
                     } else {
+                        k = j;
                         lazy_draw<ES>(a, b, j, T, rq, rp);
                     }
                 } else {
+                    k = K;
                     lazy_draw<ES>(a, b, K, T, rq, rp);   // all K accepted: bonus draw from row K
                 }
             }
         }
         verdict = __shfl_sync(0xFFFFFFFFu, verdict, 0);
+        k = __shfl_sync(0xFFFFFFFFu, k, 0);
+        tstar = __shfl_sync(0xFFFFFFFFu, tstar, 0);
         bad = __shfl_sync(0xFFFFFFFFu, bad, 0);
         if (verdict == 0) {
+            outputs(k, tstar);
             done();
             return;
         }
         if (verdict == 2) {
+            outputs(k, -1);
             if (j_last > j) {
-                // the rest of this tail batch is read already
-                combine_rest(j + 1, bad);
-                if (lane == 0) {
-                    stats_add(a.stats, &a.stats->reresolved, 1);
-                    push_exact(a.counters, a.exact, a.exact_unc, {-1, b}, a.stats);
-                }
+                combine_rest(j + 1, bad);   // the rest of this tail batch is read already
+                to_exact();
                 done();
             } else if (j + 1 <= K) {
                 if (lane == 0) lazy_enqueue(L, b, j + 1, K, !greedy, kBatchComplete, cum);
             } else {
-                if (lane == 0) {
-                    stats_add(a.stats, &a.stats->reresolved, 1);
-                    push_exact(a.counters, a.exact, a.exact_unc, {-1, b}, a.stats);
-                }
+                to_exact();
                 done();
             }
             return;

@@ -467,11 +467,11 @@ static sv_status launch_stats(const StatsArgs &sa, const DeviceInfo &di, cudaStr
 // operations happen once per row.
 __device__ __forceinline__ RowStat combine_row(const WarpPartial *P, int np, bool greedy, float T) {
     const int lane = threadIdx.x & 31;
-    int rmax = kNoRef;
-    for (int p = lane; p < np; p += 32) rmax = max(rmax, P[p].r);
-    rmax = warp_max_i(rmax);
+    // one pass over the partials: each lane keeps its own reference and raises it (an exact
+    // power-of-two rescale; A gains d * S as every -y grows by d), then the lanes agree on one
     ff s = {0.f, 0.f};
     float a = 0.f;
+    int rl = kNoRef;
     float m = -INFINITY;
     int am = 0x7FFFFFFF, fl = 0;
     for (int p = lane; p < np; p += 32) {
@@ -483,11 +483,27 @@ __device__ __forceinline__ RowStat combine_row(const WarpPartial *P, int np, boo
                 am = w.argmax;
             }
         } else {
-            const int d = rmax - w.r;
+            if (w.r > rl) {
+                const int d = w.r - rl;
+                const float sc = pow2i(-d);
+                a = (a + (float)min(d, 1 << 20) * (s.hi + s.lo)) * sc;
+                s.hi *= sc;
+                s.lo *= sc;
+                rl = w.r;
+            }
+            const int d = rl - w.r;
             const float sc = pow2i(-d);
             s = ff_add(s, {w.s_hi * sc, w.s_lo * sc});
             a += (w.a + (float)min(d, 1 << 20) * (w.s_hi + w.s_lo)) * sc;
         }
+    }
+    const int rmax = warp_max_i(rl);
+    if (!greedy) {
+        const int d = rmax - rl;
+        const float sc = pow2i(-d);
+        a = (a + (float)min(d, 1 << 20) * (s.hi + s.lo)) * sc;
+        s.hi *= sc;
+        s.lo *= sc;
     }
     s = warp_sum_ff(s);
     a = warp_sum_f(a);

@@ -87,7 +87,8 @@ __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
             if (greedy) {
                 acc = (s == rs[lane].argmax);
             } else {
-                const AcceptOutcome o = accept_test<ES>(a, b, lane, s, c_hi, c_lo, rs[lane], rs[n_t + lane]);
+                const AcceptOutcome o = accept_test<ES>(a, b, lane, s, a.uniforms[(size_t)b * (K + 1) + lane], c_hi,
+                                                        c_lo, rs[lane], rs[n_t + lane]);
                 acc = o.acc;
                 amb = o.amb;
                 near = o.near;

@@ -63,6 +63,8 @@ __device__ __forceinline__ DrawRow draw_row(const char *row, float T, const RowS
         err += (double)ts->z_err_f + kU32;
     }
     d.inv_s = __frcp_rn(norm);
+    d.k_lo = __fmul_rn(__fmul_rn(d.c_lo, (float)kLn2), d.inv_s);
+    d.pad = 0;
     // mean |y| under the normalised weights: at most the row's, divided by the kept mass and z
     d.ay = __fdiv_ru(rs.ay * (1.0f + 0x1p-20f), __fdiv_rn(norm, rs.s_hi) * (1.0f - 0x1p-20f));
     d.norm_err = err;

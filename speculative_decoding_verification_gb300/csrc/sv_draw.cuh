@@ -32,43 +32,62 @@ struct DrawArgs {
     long long wait_limit;
 };
 
-// Per-element weight (identical in both passes).
+// Per-element weight (identical in both passes).  The exponent x c_hi - r is rounded once;
+// the low part of c enters as the factor 1 + ln2 c_lo x (first order), folded into the
+// normaliser: t = inv_s + x (ln2 c_lo inv_s).  x is clamped below (see the callers), so t is
+// finite wherever 2^y > 0.
 template <bool HAS_P, bool FILT>
 __device__ __forceinline__ float draw_weight(const DrawItem &it, float xq, float xp, int v) {
-    const float yq = fmaf(xq, it.q.c_lo, fmaf(xq, it.q.c_hi, -it.q.rf));
-    float eq = ex2_fast(yq);
-    float scq = it.q.inv_s;
+    float eq = ex2_fast(fmaf(xq, it.q.c_hi, -it.q.rf));
+    float tq = fmaf(xq, it.q.k_lo, it.q.inv_s);
     if (FILT) {
         const bool keep = xq > it.q.cut_x || (xq == it.q.cut_x && v <= it.q.cut_id);
         const bool in_d = xq > it.q.top_x || (xq == it.q.top_x && v <= it.q.top_id);
         eq = keep ? eq : 0.0f;
-        scq = in_d ? __fmul_rn(scq, it.q.sc_d) : scq;
+        tq = in_d ? __fmul_rn(tq, it.q.sc_d) : tq;
     }
     if (HAS_P) {
-        const float yp = fmaf(xp, it.p.c_lo, fmaf(xp, it.p.c_hi, -it.p.rf));
-        float ep = ex2_fast(yp);
-        float sc = it.p.inv_s;
+        float ep = ex2_fast(fmaf(xp, it.p.c_hi, -it.p.rf));
+        float tp = fmaf(xp, it.p.k_lo, it.p.inv_s);
         if (FILT) {
             const bool keep = xp > it.p.cut_x || (xp == it.p.cut_x && v <= it.p.cut_id);
             const bool in_d = xp > it.p.top_x || (xp == it.p.top_x && v <= it.p.top_id);
             ep = keep ? ep : 0.0f;
-            sc = in_d ? __fmul_rn(sc, it.p.sc_d) : sc;
+            tp = in_d ? __fmul_rn(tp, it.p.sc_d) : tp;
         }
-        const float pv = __fmul_rn(ep, sc);
-        return fmaxf(__fmaf_rn(eq, scq, -pv), 0.0f);
+        const float pv = __fmul_rn(ep, tp);
+        return fmaxf(__fmaf_rn(eq, tq, -pv), 0.0f);
     }
-    return __fmul_rn(eq, scq);
+    return __fmul_rn(eq, tq);
 }
+
+// Logits below this weigh exactly 0 at every allowed temperature; clamping them there keeps
+// the factor t above finite (a -inf logit would otherwise give 0 * inf).
+constexpr uint32_t kDrawFloor2 = 0xF149F149u;   // bf16 pair (-9.95e29, -9.95e29)
+constexpr float kDrawFloor = -9.95e29f;
 
 // Weights of one vector (EPV tokens from element e0); returns their tree sum.
 template <int ES, bool HAS_P, bool FILT>
 __device__ __forceinline__ float vec_weights(const DrawItem &it, uint4 wq, uint4 wp, int e0, float (&wv)[16 / ES]) {
     constexpr int EPV = 16 / ES;
     float xq[EPV], xp[EPV];
-    unpack<ES>(wq, xq);
-    unpack<ES>(wp, xp);
+    if constexpr (ES == 2) {
+        unpack<ES>(make_uint4(bmax2(wq.x, kDrawFloor2), bmax2(wq.y, kDrawFloor2), bmax2(wq.z, kDrawFloor2),
+                              bmax2(wq.w, kDrawFloor2)), xq);
+        if (HAS_P)
+            unpack<ES>(make_uint4(bmax2(wp.x, kDrawFloor2), bmax2(wp.y, kDrawFloor2), bmax2(wp.z, kDrawFloor2),
+                                  bmax2(wp.w, kDrawFloor2)), xp);
+    } else {
+        unpack<ES>(wq, xq);
+        if (HAS_P) unpack<ES>(wp, xp);
 #pragma unroll
-    for (int i = 0; i < EPV; ++i) wv[i] = draw_weight<HAS_P, FILT>(it, xq[i], xp[i], e0 + i);
+        for (int i = 0; i < EPV; ++i) {
+            xq[i] = fmaxf(xq[i], kDrawFloor);
+            xp[i] = HAS_P ? fmaxf(xp[i], kDrawFloor) : xq[i];
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < EPV; ++i) wv[i] = draw_weight<HAS_P, FILT>(it, xq[i], HAS_P ? xp[i] : xq[i], e0 + i);
     if constexpr (EPV == 8) {
         return ((wv[0] + wv[1]) + (wv[2] + wv[3])) + ((wv[4] + wv[5]) + (wv[6] + wv[7]));
     } else {
@@ -100,8 +119,8 @@ __device__ __forceinline__ void draw_tile(const DrawItem &it, const unsigned cha
 
 template <int ES>
 __device__ __forceinline__ float draw_scalar(const DrawItem &it, int v) {
-    const float xq = load_elem<ES>(it.q.row, v);
-    const float xp = it.has_p ? load_elem<ES>(it.p.row, v) : xq;
+    const float xq = fmaxf(load_elem<ES>(it.q.row, v), kDrawFloor);
+    const float xp = it.has_p ? fmaxf(load_elem<ES>(it.p.row, v), kDrawFloor) : xq;
     if (it.has_p) return it.filt ? draw_weight<true, true>(it, xq, xp, v) : draw_weight<true, false>(it, xq, xp, v);
     return it.filt ? draw_weight<false, true>(it, xq, xp, v) : draw_weight<false, false>(it, xq, xp, v);
 }
@@ -264,27 +283,32 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a
 
 // Bound on |(u R~ - C~(v)) - (u R - C(v))| for any v, where ~ marks the computed prefix sums.
 // With per-token errors d_v = |w~_v - w_v| the difference is (1-u) sum_{i<=v} d_i and
-// u sum_{i>v} d_i of opposite signs at worst, so it is at most max(u, 1-u) sum_v d_v; the
-// float32 sums of each sub-chunk (8 rounding levels, non-negative terms) add 8u to both
-// C~(v) <= R and u R~, bounded by 20u R.  sum_v d_v: the exponent's rounding (kYRound per unit
-// |y|, summed as A), the exponential (kEx2RelErr), the products with the normalisers (2u) and
-// the normalisers' own errors; for a bonus draw without filters a common normaliser error
-// cancels in C(v) / R.  The float-float scans add well under 1e-9 R.  Evaluated in float32
-// and rounded up.
-__device__ __forceinline__ float draw_error_bound(const DrawItem &it, float W, float A) {
+// u sum_{i>v} d_i of opposite signs at worst, so it is at most max(u, 1-u) sum_v d_v.  Each
+// sub-chunk sum of non-negative terms has 8 float32 rounding levels (3 per 16-byte vector, 5
+// across the warp) and the scans over sub-chunks are float-float, so C~(v) and u R~ carry at
+// most 8u (C(v) + u R) between them; the caller passes C(v) + u R at the boundary it checks.
+// sum_v d_v: the exponent x c_hi - r rounded once (ln2 u per unit |y|, summed as A), the
+// exponential (kEx2RelErr), the factor t = inv_s (1 + ln2 c_lo x) (its rounding, and the
+// second-order remainder (ln2 (|r| + 128) 2^-23)^2), the products (2u), and the rows'
+// normaliser errors; for a bonus draw without filters a common normaliser error cancels.
+// The float-float scans add well under 1e-9 R.  Evaluated in float32 and rounded up.
+__device__ __forceinline__ float draw_error_bound(const DrawItem &it, float W, float A, float c_sum) {
     const float u = (float)kU32;
     const float ex = (float)kEx2RelErr;
-    float e = (float)(kYRound * 1.01) * A;
+    const float rq = ((float)kLn2 * 0x1p-23f) * (fabsf(it.q.rf) + 128.0f);
+    const float rp = ((float)kLn2 * 0x1p-23f) * (fabsf(it.p.rf) + 128.0f);
+    float e = (float)(kLn2 * kU32 * 1.01) * A;
     if (it.has_p) {
-        e += 1.0001f * (ex + 2.0f * u + (float)it.q.norm_err) + 1.0001f * (ex + 2.0f * u + (float)it.p.norm_err);
+        e += 1.0001f * (ex + 3.0f * u + rq * rq + (float)it.q.norm_err) +
+             1.0001f * (ex + 3.0f * u + rp * rp + (float)it.p.norm_err);
     } else if (it.filt) {
         // tokens inside and outside the scaled set carry different normaliser errors
-        e += (ex + 2.0f * u + (float)it.q.norm_err) * W;
+        e += (ex + 3.0f * u + rq * rq + (float)it.q.norm_err) * W;
     } else {
-        e += (ex + u) * W;
+        e += (ex + 2.0f * u + rq * rq) * W;
     }
     const float uu = (float)fmax(it.u, 1.0 - it.u);
-    return (uu * e + 20.0f * u * W + 1e-9f * W + 1e-30f) * (1.0f + 0x1p-18f);
+    return (uu * e + 8.1f * u * c_sum + 1e-9f * W + 1e-30f) * (1.0f + 0x1p-18f);
 }
 
 // One block per item, float32 / float-float only: the sub-chunk sums are scanned in
@@ -461,7 +485,8 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
         ambiguous = true;
     }
     if (lane == 0) {
-        const float E = draw_error_bound(it, R.hi, A);
+        // C(t*) + u R covers both boundaries' prefix and total terms
+        const float E = draw_error_bound(it, R.hi, A, fmaxf(thr.hi + dhit, 0.f) + thr.hi);
         if (dprev <= E || dhit <= E) ambiguous = true;
         const bool near = dprev < 1e-6f * R.hi || dhit < 1e-6f * R.hi;
         *it.out = tstar;

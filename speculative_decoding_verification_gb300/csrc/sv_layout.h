@@ -103,6 +103,8 @@ struct DrawRow {
     float top_x; int top_id;
     float sc_d;             // C for tokens in D (1 when no transform)
     float ay;               // bound on sum_v w_v |y_v| for this row's normalised weights w
+    float k_lo;             // ln2 c_lo inv_s: weight = 2^(x c_hi - r) (inv_s + x k_lo)
+    int pad;
     double norm_err;        // relative error bound of inv_s (normaliser from the stats pass)
 };
 

@@ -100,6 +100,8 @@ __global__ void __launch_bounds__(kThreads) k_sample_items(const SampleArgs a, l
             err += (double)a.top[r].z_err_f + kU32;
         }
         d.inv_s = __frcp_rn(norm);
+        d.k_lo = __fmul_rn(__fmul_rn(d.c_lo, (float)kLn2), d.inv_s);
+        d.pad = 0;
         d.ay = __fdiv_ru(rs.ay * (1.0f + 0x1p-20f), __fdiv_rn(norm, rs.s_hi) * (1.0f - 0x1p-20f));
         d.norm_err = err;
     }

@@ -56,25 +56,51 @@ def nucleus(q, x, top_p):
     return np.where(keep, q / mass[..., None], 0.0), mass, n
 
 
-def row_distribution(x, temperature, top_p):
-    """The distribution a row of logits stands for, after temperature and top-p.
+def top_k(q, x, k):
+    """Top-k filter: keep the first k tokens in (probability descending, id ascending) order;
+    zero the rest and renormalise.  k <= 0 or k >= V keeps every token.
+
+    The ordering uses the logits x, which order the tokens exactly as q does for T > 0.
+    Returns (filtered q, kept-mass M).
+    """
+    V = q.shape[-1]
+    k = np.asarray(k, dtype=np.int64)[..., None]
+    k = np.where((k <= 0) | (k >= V), V, k)
+    order = order_desc(x)
+    keep = np.zeros(q.shape, dtype=bool)
+    np.put_along_axis(keep, order, np.arange(V) < k, axis=-1)
+    mass = np.sum(np.where(keep, q, 0.0), axis=-1)
+    return np.where(keep, q / mass[..., None], 0.0), mass
+
+
+def row_distribution(x, temperature, top_p, top_k_=0):
+    """The distribution a row of logits stands for, after temperature, top-k and top-p.
 
     temperature == 0 means greedy: the one-hot vector at the first argmax.
-    top_p >= 1 means no nucleus filter.
-    Returns (dist [..., V], lse [...] (nan for greedy rows), nucleus mass [...]).
+    top_k_ <= 0 or >= V means no top-k filter; top_p >= 1 means no nucleus filter.  With both
+    on, top-k acts first and the nucleus is taken of the renormalised top-k distribution (the
+    pages fix no order between the two filters; this is the common sampler order).
+    Returns (dist [..., V], lse [...] (nan for greedy rows), kept mass [...] (the fraction of
+    the unfiltered q that the filters keep)).
     """
     x = np.asarray(x, dtype=np.float64)
     T = np.broadcast_to(np.asarray(temperature, dtype=np.float64), x.shape[:-1])
     tp = np.broadcast_to(np.asarray(top_p, dtype=np.float64), x.shape[:-1])
+    tk = np.broadcast_to(np.asarray(top_k_, dtype=np.int64), x.shape[:-1])
     greedy = T == 0.0
     safe_T = np.where(greedy, 1.0, T)
     q, lse = softmax_t(x, safe_T)
     mass = np.ones(x.shape[:-1])
+    kf = (tk > 0) & (tk < x.shape[-1]) & ~greedy
+    if np.any(kf):
+        qk, mk = top_k(q, x, np.where(kf, tk, 0))
+        q = np.where(kf[..., None], qk, q)
+        mass = np.where(kf, mk, mass)
     filt = (tp < 1.0) & ~greedy
     if np.any(filt):
         qf, mf, _ = nucleus(q, x, np.where(filt, tp, 1.0))
         q = np.where(filt[..., None], qf, q)
-        mass = np.where(filt, mf, mass)
+        mass = np.where(filt, mass * mf, mass)
     if np.any(greedy):
         onehot = np.zeros(x.shape)
         np.put_along_axis(onehot, argmax_first(x)[..., None], 1.0, axis=-1)

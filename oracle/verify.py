@@ -29,7 +29,7 @@ def _acceptance_ratio(q_s, p_s):
     return raw, np.minimum(1.0, raw)
 
 
-def verify(target, draft, tokens, uniforms, temperature, top_p, saguaro_F=0, saguaro_C=1.0):
+def verify(target, draft, tokens, uniforms, temperature, top_p, saguaro_F=0, saguaro_C=1.0, top_k=None):
     """Verify B sequences.
 
     target:  [B, K+1, V] float64 target logits for positions 1..K+1.
@@ -37,6 +37,8 @@ def verify(target, draft, tokens, uniforms, temperature, top_p, saguaro_F=0, sag
     tokens:  [B, K] draft tokens s_1..s_K.
     uniforms:[B, K+1] float64 in [0, 1): K accept tests then the residual draw.
     temperature, top_p: [B] per sequence, applied to both q and p.
+    top_k: [B] per sequence or None (<= 0 or >= V: off), applied to both q and p before
+      top-p (SpS notes §3: the filters act on each distribution before the correction).
     saguaro_F, saguaro_C: the draft-side sigma_{F,C} transform applied to every draft row
       (F = 0 or C = 1: none).  Verification must use the transformed p for losslessness
       (SSD notes §3.2).
@@ -53,10 +55,11 @@ def verify(target, draft, tokens, uniforms, temperature, top_p, saguaro_F=0, sag
     K = K1 - 1
     T = np.asarray(temperature, dtype=np.float64).reshape(B)
     tp = np.asarray(top_p, dtype=np.float64).reshape(B)
+    tk = np.zeros(B, np.int64) if top_k is None else np.asarray(top_k, dtype=np.int64).reshape(B)
     greedy = T == 0.0
 
-    q, lse_q, mass_q = row_distribution(target, T[:, None], tp[:, None])
-    p, lse_p, mass_p = row_distribution(draft[:, :K, :], T[:, None], tp[:, None])
+    q, lse_q, mass_q = row_distribution(target, T[:, None], tp[:, None], tk[:, None])
+    p, lse_p, mass_p = row_distribution(draft[:, :K, :], T[:, None], tp[:, None], tk[:, None])
     if saguaro_F > 0 and saguaro_C != 1.0:
         p_sag, _, _ = saguaro_transform(p, draft[:, :K, :], saguaro_F, saguaro_C)
         p = np.where(greedy[:, None, None], p, p_sag)
@@ -90,19 +93,20 @@ def verify(target, draft, tokens, uniforms, temperature, top_p, saguaro_F=0, sag
                 mass_p=mass_p)
 
 
-def draft_sample(draft, uniforms, temperature, top_p, saguaro_F=0, saguaro_C=1.0):
+def draft_sample(draft, uniforms, temperature, top_p, saguaro_F=0, saguaro_C=1.0, top_k=None):
     """Sample one draft token per row: s = inverse_cdf(p', u), with p' the draft
-    distribution after temperature, top-p and sigma_{F,C} (SSD notes §4.4; SSD abstract
+    distribution after temperature, top-k, top-p and sigma_{F,C} (SSD notes §4.4; SSD abstract
     page, "Method").  Temperature 0 rows take the argmax.
 
-    draft: [B, R, V]; uniforms: [B, R]; temperature, top_p: [B].
+    draft: [B, R, V]; uniforms: [B, R]; temperature, top_p: [B]; top_k: [B] or None.
     Returns dict(tokens [B, R], p_top [B, R] (P_D), z_prime [B, R], lse [B, R]).
     """
     draft = np.asarray(draft, dtype=np.float64)
     B, R, V = draft.shape
     T = np.asarray(temperature, dtype=np.float64).reshape(B)
     tp = np.asarray(top_p, dtype=np.float64).reshape(B)
-    p, lse, _ = row_distribution(draft, T[:, None], tp[:, None])
+    tk = np.zeros(B, np.int64) if top_k is None else np.asarray(top_k, dtype=np.int64).reshape(B)
+    p, lse, _ = row_distribution(draft, T[:, None], tp[:, None], tk[:, None])
     p2, p_d, zp = saguaro_transform(p, draft, saguaro_F, saguaro_C)
     t, _ = inverse_cdf(p2, np.asarray(uniforms, dtype=np.float64))
     greedy = (T == 0.0)[:, None]

@@ -84,6 +84,77 @@ def test_nucleus_hand_examples():
     np.testing.assert_array_equal(a, oracle.softmax_t(y, np.full(3, 0.7))[0])
 
 
+def test_top_k_hand_examples():
+    """SpS notes §3: top-k acts on each distribution before the correction.  Probabilities
+    (0.1, 0.4, 0.2, 0.2, 0.1): the plateaus at 0.2 and 0.1 are cut at the lowest ids."""
+    p = np.array([0.1, 0.4, 0.2, 0.2, 0.1])
+    x = np.log(p)
+    cases = {1: [0, 1, 0, 0, 0], 2: [0, 2 / 3, 1 / 3, 0, 0], 3: [0, 0.5, 0.25, 0.25, 0],
+             4: np.array([0.1, 0.4, 0.2, 0.2, 0]) / 0.9}
+    for k, want in cases.items():
+        d, _, m = oracle.row_distribution(x, 1.0, 1.0, k)
+        np.testing.assert_allclose(d, want, atol=1e-15)
+        assert m == pytest.approx([0.4, 0.6, 0.8, 0.9][k - 1], abs=1e-15)
+    base = oracle.softmax_t(x[None], np.ones(1))[0][0]
+    for k in (0, -1, 5, 99):                                   # off: no filter, bit for bit
+        d, _, m = oracle.row_distribution(x, 1.0, 1.0, k)
+        np.testing.assert_array_equal(d, base)
+        assert m == 1.0
+    # temperature first: at T = 1/2 the kept pair {1, 2} weighs 0.4^2 : 0.2^2
+    d, _, _ = oracle.row_distribution(x, 0.5, 1.0, 2)
+    np.testing.assert_allclose(d, [0, 0.8, 0.2, 0, 0], atol=1e-14)
+    # greedy rows ignore the filter
+    d, _, _ = oracle.row_distribution(x, 0.0, 1.0, 3)
+    np.testing.assert_array_equal(d, [0, 1, 0, 0, 0])
+
+
+def test_top_k_then_top_p_hand_examples():
+    """With both filters, the nucleus is taken of the renormalised top-k distribution, so the
+    order of the two filters shows in the result."""
+    x = np.log(np.array([0.1, 0.4, 0.2, 0.2, 0.1]))
+    # top-4 = (1/9, 4/9, 2/9, 2/9, 0): cumulative 4/9, 6/9, 8/9 >= 0.85 keeps {1, 2, 3}
+    d, _, m = oracle.row_distribution(x, 1.0, 0.85, 4)
+    np.testing.assert_allclose(d, [0, 0.5, 0.25, 0.25, 0], atol=1e-15)
+    assert m == pytest.approx(0.8, abs=1e-15)
+    # the nucleus of the unfiltered row at 0.85 needs 0.4 + 0.2 + 0.2 + 0.1
+    d, _, _ = oracle.row_distribution(x, 1.0, 0.85)
+    np.testing.assert_allclose(d, np.array([0.1, 0.4, 0.2, 0.2, 0]) / 0.9, atol=1e-15)
+    # top-2 = (0, 2/3, 1/3, 0, 0): 2/3 >= 0.55 keeps the top token alone
+    d, _, m = oracle.row_distribution(x, 1.0, 0.55, 2)
+    np.testing.assert_array_equal(d, [0, 1, 0, 0, 0])
+    assert m == pytest.approx(0.4, abs=1e-15)
+    d, _, _ = oracle.row_distribution(x, 1.0, 0.55)
+    np.testing.assert_allclose(d, [0, 2 / 3, 1 / 3, 0, 0], atol=1e-15)
+
+
+def test_top_k_invariants_on_plateau_rows():
+    """Rows of rounded logits (many ties): the kept set has min(k, V) tokens, no dropped token
+    outranks a kept one, ties at the cut keep the lowest ids, and the kept tokens keep their
+    relative probabilities.  k = 1 is the greedy one-hot."""
+    rng = np.random.default_rng(21)
+    V = 40
+    x = np.round(rng.normal(0, 1.5, size=(60, V)))
+    ks = rng.integers(1, V + 3, size=60)
+    T = rng.uniform(0.3, 2.0, size=60)
+    d, _, m = oracle.row_distribution(x, T, 1.0, ks)
+    q = softmax(x / T[:, None])
+    for i in range(60):
+        keep = d[i] > 0
+        assert keep.sum() == min(ks[i], V)
+        assert d[i].sum() == pytest.approx(1.0, abs=1e-14)
+        assert m[i] == pytest.approx(q[i][keep].sum(), abs=1e-14)
+        np.testing.assert_allclose(d[i][keep], q[i][keep] / q[i][keep].sum(), rtol=1e-13)
+        if keep.all():
+            continue
+        lo, hi = x[i][keep].min(), x[i][~keep].max()
+        assert lo >= hi
+        if lo == hi:
+            assert np.flatnonzero(keep & (x[i] == lo)).max() < np.flatnonzero(~keep & (x[i] == lo)).min()
+    d1, _, _ = oracle.row_distribution(x, T, 1.0, 1)
+    g, _, _ = oracle.row_distribution(x, 0.0, 1.0)
+    np.testing.assert_array_equal(d1, g)
+
+
 def test_inverse_cdf_hand_example():
     w = np.array([0.1, 0.0, 0.3, 0.6])
     for u, want in [(0.0, 0), (0.0999, 0), (0.1, 2), (0.3999, 2), (0.4, 3), (0.999, 3)]:
@@ -164,6 +235,32 @@ def test_exact_law_is_target_law_V3_K2(seed):
     alpha1 = np.minimum(p[0], q[0]).sum()
     np.testing.assert_allclose(pair, np.outer(np.minimum(p[0], q[0]) / alpha1, q[1]) * exists[1],
                                atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_exact_law_under_top_k_V4_K2(seed):
+    """Brute force on V=4, K=2 with top-2 on both models: the committed tokens follow the
+    top-2 target distribution, and tokens outside the target's top two never appear."""
+    import functools
+    rng = np.random.default_rng(40 + seed)
+    tgt = rng.normal(0, 1.5, size=(3, 4))
+    drf = 0.5 * tgt[:2] + rng.normal(0, 1.0, size=(2, 4))
+
+    def top2(x):
+        keep = np.zeros(x.shape, bool)
+        for i, row in enumerate(x):
+            keep[i, np.argsort(row)[-2:]] = True
+        w = np.where(keep, softmax(x), 0.0)
+        return w / w.sum(axis=-1, keepdims=True)
+
+    q2, p2 = top2(tgt), top2(drf)
+    verify = functools.partial(oracle.verify, top_k=np.array([2]))
+    law = outcome_law(verify, tgt, drf, p2)
+    assert sum(law.values()) == pytest.approx(1.0, abs=1e-12)
+    joint, exists = position_marginals(law, 2, 4)
+    np.testing.assert_allclose(joint[0], q2[0], atol=1e-12)
+    for i in (1, 2):
+        np.testing.assert_allclose(joint[i], exists[i] * q2[i], atol=1e-12)
 
 
 def test_mass_identities_single_position():

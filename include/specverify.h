@@ -97,10 +97,10 @@ typedef struct sv_stats {
  * debug[(b * (K + 1) + j) * SV_DEBUG_FIELDS + field], float64, NaN where undefined.
  *   LSE_Q    log sum_v exp(x_v / T) of target row j (j = 0..K)
  *   LSE_P    the same for draft row j (j < K)
- *   Q_S, P_S q_j(s_j) and p_j(s_j) after temperature, top-p and sigma_{F,C} (j < K)
+ *   Q_S, P_S q_j(s_j) and p_j(s_j) after temperature, top-k, top-p and sigma_{F,C} (j < K)
  *   RATIO    q_j(s_j) / p_j(s_j), unclipped (j < K)
- *   MASS_Q   kept nucleus mass of target row j (1 without top-p)
- *   MASS_P   kept nucleus mass of draft row j
+ *   MASS_Q   mass of target row j that the top-k / top-p filters keep (1 without filters)
+ *   MASS_P   the same for draft row j
  *   R        (j == 0 only) sum of the weights of the residual / bonus draw   */
 #define SV_DEBUG_FIELDS 8
 enum {
@@ -132,6 +132,11 @@ int sv_version(void);   /* major * 10000 + minor * 100 + patch */
  *  top_p          dev float [B] or NULL (no nucleus filter).  top_p >= 1 disables the filter
  *                 for that sequence; otherwise the shortest prefix of tokens in (probability
  *                 desc, id asc) order whose mass reaches top_p is kept, on q and on p.
+ *  top_k          dev int32 [B] or NULL (no top-k filter).  k <= 0 or k >= V disables the
+ *                 filter for that sequence; otherwise the first k tokens in (probability desc,
+ *                 id asc) order are kept, on q and on p.  With both filters on, top-k acts
+ *                 first and the nucleus is that of the renormalised top-k distribution (the
+ *                 pages fix no order between the two; this is the common sampler order).
  *  saguaro_F, saguaro_C  the draft-side sigma_{F,C} transform applied to every draft row
  *                 before the ratio and the residual (F = 0 or C = 1: none; 0 <= C <= 1).
  *  accept_len     dev int32 [B]: k, the number of accepted draft tokens (0..K).
@@ -149,7 +154,7 @@ sv_status sv_verify(const void *target_logits, int64_t t_row_pitch,
                     sv_dtype dtype,
                     const int32_t *draft_tokens, const double *uniforms,
                     int B, int K, int V,
-                    const float *temperature, const float *top_p,
+                    const float *temperature, const float *top_p, const int32_t *top_k,
                     int saguaro_F, float saguaro_C,
                     int32_t *accept_len, int32_t *out_tokens,
                     double *debug, sv_stats *stats,
@@ -165,7 +170,7 @@ sv_status sv_verify(const void *target_logits, int64_t t_row_pitch,
  * outputs are identical.  Rows after a sequence's first rejection (after its first greedy
  * mismatch) are never read: their debug fields stay NaN, they do not count in stats.rows, and
  * non-finite values in them raise no error.  The bytes read fall with the acceptance rate
- * (about 30% of sv_verify's at the large-batch workload).  Calls with top_p or an active
+ * (about 30% of sv_verify's at the large-batch workload).  Calls with top_p, top_k or an active
  * sigma_{F,C} (saguaro_F > 0 and saguaro_C != 1) run the sv_verify pipeline unchanged.  One
  * kernel of the call waits on work that other blocks of the same launch queue; it is
  * launched cooperatively, so SV_ERR_CUDA results if the device cannot hold all its blocks.
@@ -175,7 +180,7 @@ sv_status sv_verify_lazy(const void *target_logits, int64_t t_row_pitch,
                          sv_dtype dtype,
                          const int32_t *draft_tokens, const double *uniforms,
                          int B, int K, int V,
-                         const float *temperature, const float *top_p,
+                         const float *temperature, const float *top_p, const int32_t *top_k,
                          int saguaro_F, float saguaro_C,
                          int32_t *accept_len, int32_t *out_tokens,
                          double *debug, sv_stats *stats,
@@ -216,24 +221,25 @@ sv_status sv_verify_static(const void *target_logits, int64_t t_row_pitch,
                            sv_dtype dtype,
                            const int32_t *draft_tokens, const double *uniforms,
                            int B, int K, int V,
-                           const float *temperature, const float *top_p,
+                           const float *temperature, const float *top_p, const int32_t *top_k,
                            int saguaro_F, float saguaro_C,
                            int32_t *accept_len, int32_t *out_tokens,
                            double *debug, sv_stats *stats, sv_stream_t stream);
 
 /* ----------------------------------------------------------------------------------------
  * sv_saguaro_sample — draw one token from each of the first n_rows rows of every sequence's
- * draft distribution p' = sigma_{F,C}(p): p after temperature and top-p, the top-F tokens
+ * draft distribution p' = sigma_{F,C}(p): p after temperature, top-k and top-p, the top-F tokens
  * (ranked by draft logit) scaled by C, renormalised.  F = 0 or C = 1 is a plain draft sampler.
  * [SSD notes §4.4 Theorem 15 (scaling the cached tokens' draft mass raises the hit rate),
  *  Theorem 19 (worked example); SSD abstract page, "Method" (sigma_{F,C})]
  *
  *  draft_logits  dev, rows (b, j) at b*rows_per_seq+j, pitch row_pitch; rows j < n_rows used.
- *  temperature   dev float [B] (0: argmax), top_p dev float [B] or NULL.
+ *  temperature   dev float [B] (0: argmax), top_p dev float [B] or NULL, top_k dev int32 [B]
+ *                or NULL (both as in sv_verify).
  *  uniforms      dev float64 [B][n_rows].
  *  tokens        dev int32 [B][n_rows] (output).
  *  debug         dev float64 [B][n_rows][4] or NULL: LSE, P_D (top-F mass before scaling),
- *                Z' (normaliser after scaling), nucleus mass.
+ *                Z' (normaliser after scaling), mass kept by the top-k / top-p filters.
  * A row where C = 0 and all of p's mass lies in the top-F set has no defined transform and
  * is sampled from p unchanged.
  * -------------------------------------------------------------------------------------- */
@@ -241,7 +247,7 @@ size_t sv_saguaro_sample_workspace_size(int B, int n_rows, int V);
 
 sv_status sv_saguaro_sample(const void *draft_logits, int64_t row_pitch, int rows_per_seq,
                             sv_dtype dtype, int B, int n_rows, int V,
-                            const float *temperature, const float *top_p,
+                            const float *temperature, const float *top_p, const int32_t *top_k,
                             int F, float C, const double *uniforms,
                             int32_t *tokens, double *debug, sv_stats *stats,
                             void *workspace, size_t workspace_bytes, sv_stream_t stream);

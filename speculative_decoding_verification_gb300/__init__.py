@@ -85,13 +85,22 @@ def read_stats(t: torch.Tensor) -> dict:
     return out
 
 
+def _top_k(top_k):
+    """top_k must be a contiguous int32 CUDA tensor (or None): the library reads it as int32."""
+    if top_k is not None and (top_k.dtype != torch.int32 or not top_k.is_contiguous() or not top_k.is_cuda):
+        raise TypeError("top_k must be a contiguous int32 CUDA tensor")
+    return top_k
+
+
 def sv_verify(target, draft, draft_tokens, uniforms, temperature, top_p=None, saguaro_F=0, saguaro_C=1.0,
-              accept_len=None, out_tokens=None, debug=False, stats=None, workspace=None, stream=None, lazy=False):
+              accept_len=None, out_tokens=None, debug=False, stats=None, workspace=None, stream=None, lazy=False,
+              top_k=None):
     """sv_verify (or, with lazy=True, sv_verify_lazy: same outputs, rows after each sequence's
     first rejection left unread) on torch CUDA tensors.
 
     target [B, K+1, V] and draft [B, R>=K, V] (float32 or bfloat16, same dtype); draft_tokens
-    int32 [B, K]; uniforms float64 [B, K+1]; temperature float32 [B]; top_p float32 [B] or None.
+    int32 [B, K]; uniforms float64 [B, K+1]; temperature float32 [B]; top_p float32 [B] or None;
+    top_k int32 [B] or None (top-k acts before top-p).
     Returns (accept_len int32 [B], out_tokens int32 [B, K+1], debug float64 [B, K+1, 8] or None,
     stats uint8 block).
     """
@@ -119,14 +128,14 @@ def sv_verify(target, draft, draft_tokens, uniforms, temperature, top_p=None, sa
     fn = lib.sv_verify_lazy if lazy else lib.sv_verify
     code = fn(_ptr(target), t_pitch, d_ptr, d_pitch, d_rows, _dtype_code(target),
               _ptr(draft_tokens if K > 0 else None), _ptr(uniforms), B, K, V, _ptr(temperature),
-              _ptr(top_p), int(saguaro_F), float(saguaro_C), _ptr(accept_len), _ptr(out_tokens),
-              _ptr(dbg), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream))
+              _ptr(top_p), _ptr(_top_k(top_k)), int(saguaro_F), float(saguaro_C), _ptr(accept_len),
+              _ptr(out_tokens), _ptr(dbg), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream))
     _abi.check("sv_verify_lazy" if lazy else "sv_verify", code)
     return accept_len, out_tokens, dbg, stats
 
 
 def sv_verify_static(target, draft, draft_tokens, uniforms, temperature, top_p=None, saguaro_F=0, saguaro_C=1.0,
-                     accept_len=None, out_tokens=None, debug=None, stats=None, stream=None):
+                     accept_len=None, out_tokens=None, debug=None, stats=None, stream=None, top_k=None):
     """sv_verify without a workspace, for callers that cannot allocate device memory (a server
     whose KV-cache pool holds all free HBM, a host program that owns every allocation).
 
@@ -161,8 +170,8 @@ def sv_verify_static(target, draft, draft_tokens, uniforms, temperature, top_p=N
         stats = new_stats(dev)
     code = lib.sv_verify_static(_ptr(target), t_pitch, d_ptr, d_pitch, d_rows, _dtype_code(target),
                                 _ptr(draft_tokens if K > 0 else None), _ptr(uniforms), B, K, V, _ptr(temperature),
-                                _ptr(top_p), int(saguaro_F), float(saguaro_C), _ptr(accept_len), _ptr(out_tokens),
-                                _ptr(debug), _ptr(stats), _stream(stream))
+                                _ptr(top_p), _ptr(_top_k(top_k)), int(saguaro_F), float(saguaro_C), _ptr(accept_len),
+                                _ptr(out_tokens), _ptr(debug), _ptr(stats), _stream(stream))
     if code == _abi.SV_ERR_WORKSPACE:
         raise ValueError(f"sv_verify_static: B={B}, K={K}, V={V} needs more scratch than the "
                          f"{_abi.SV_STATIC_SCRATCH_BYTES >> 20} MiB static array; use sv_verify with a workspace")
@@ -171,9 +180,10 @@ def sv_verify_static(target, draft, draft_tokens, uniforms, temperature, top_p=N
 
 
 def sv_saguaro_sample(draft, uniforms, temperature, top_p=None, F=0, C=1.0, n_rows=None, tokens=None, debug=False,
-                      stats=None, workspace=None, stream=None):
+                      stats=None, workspace=None, stream=None, top_k=None):
     """sv_saguaro_sample: one token per row j < n_rows of each sequence of draft [B, R, V].
-    uniforms float64 [B, n_rows]; temperature float32 [B]; returns (tokens int32 [B, n_rows],
+    uniforms float64 [B, n_rows]; temperature float32 [B]; top_p float32 [B] or None; top_k
+    int32 [B] or None; returns (tokens int32 [B, n_rows],
     debug float64 [B, n_rows, 4] or None, stats)."""
     lib = load()
     B, R, V = draft.shape
@@ -188,7 +198,8 @@ def sv_saguaro_sample(draft, uniforms, temperature, top_p=None, F=0, C=1.0, n_ro
     ws_bytes = lib.sv_saguaro_sample_workspace_size(B, n_rows, V)
     ws = (workspace or _default_ws).get(ws_bytes, dev)
     code = lib.sv_saguaro_sample(_ptr(draft), pitch, rows, _dtype_code(draft), B, n_rows, V, _ptr(temperature),
-                                 _ptr(top_p), int(F), float(C), _ptr(uniforms), _ptr(tokens), _ptr(dbg), _ptr(stats),
+                                 _ptr(top_p), _ptr(_top_k(top_k)), int(F), float(C), _ptr(uniforms), _ptr(tokens),
+                                 _ptr(dbg), _ptr(stats),
                                  _ptr(ws), ws.numel(), _stream(stream))
     _abi.check("sv_saguaro_sample", code)
     return tokens, dbg, stats

@@ -36,14 +36,14 @@ SIGNATURES = {
     "sv_version": (c_int, []),
     "sv_verify_workspace_size": (c_size, [c_int, c_int, c_int]),
     "sv_verify": (c_int, [c_vp, c_i64, c_vp, c_i64, c_int, c_int, c_vp, c_vp, c_int, c_int, c_int, c_vp, c_vp,
-                          c_int, c_f32, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
+                          c_vp, c_int, c_f32, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
     "sv_verify_lazy": (c_int, [c_vp, c_i64, c_vp, c_i64, c_int, c_int, c_vp, c_vp, c_int, c_int, c_int, c_vp, c_vp,
-                               c_int, c_f32, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
+                               c_vp, c_int, c_f32, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
     "sv_verify_static": (c_int, [c_vp, c_i64, c_vp, c_i64, c_int, c_int, c_vp, c_vp, c_int, c_int, c_int, c_vp,
-                                 c_vp, c_int, c_f32, c_vp, c_vp, c_vp, c_vp, c_vp]),
+                                 c_vp, c_vp, c_int, c_f32, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "sv_saguaro_sample_workspace_size": (c_size, [c_int, c_int, c_int]),
-    "sv_saguaro_sample": (c_int, [c_vp, c_i64, c_int, c_int, c_int, c_int, c_int, c_vp, c_vp, c_int, c_f32, c_vp,
-                                  c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
+    "sv_saguaro_sample": (c_int, [c_vp, c_i64, c_int, c_int, c_int, c_int, c_int, c_vp, c_vp, c_vp, c_int, c_f32,
+                                  c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
     "sv_fanout": (c_int, [c_f64, c_f64, c_f64, c_int, c_vp, c_vp]),
     "sv_cache_keys_workspace_size": (c_size, [c_int, c_int, c_int]),
     "sv_cache_keys": (c_int, [c_vp, c_i64, c_int, c_int, c_vp, c_vp, c_int, c_int, c_int, c_vp, c_vp, c_vp, c_size,

@@ -341,7 +341,8 @@ __device__ __forceinline__ ff ff_exp2_xc(float x, ff c, int r, const float2 *tab
 // Order-preserving keys (larger value -> larger key) for ranking logits.
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t f32_key(float x) {
-    const uint32_t b = __float_as_uint(x);
+    uint32_t b = __float_as_uint(x);
+    if (b == 0x80000000u) b = 0u;   // -0 ranks with +0: equal logits, ordered by id
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 

@@ -702,13 +702,14 @@ using namespace sv;
 extern "C" sv_status sv_verify_lazy(const void *target_logits, int64_t t_row_pitch, const void *draft_logits,
                                     int64_t d_row_pitch, int d_rows_per_seq, sv_dtype dtype,
                                     const int32_t *draft_tokens, const double *uniforms, int B, int K, int V,
-                                    const float *temperature, const float *top_p, int saguaro_F, float saguaro_C,
+                                    const float *temperature, const float *top_p, const int32_t *top_k,
+                                    int saguaro_F, float saguaro_C,
                                     int32_t *accept_len, int32_t *out_tokens, double *debug, sv_stats *stats,
                                     void *workspace, size_t workspace_bytes, sv_stream_t stream_) {
     const bool sag_on = saguaro_F > 0 && saguaro_C != 1.0f;
-    if (top_p != nullptr || sag_on)
+    if (top_p != nullptr || top_k != nullptr || sag_on)
         return sv_verify(target_logits, t_row_pitch, draft_logits, d_row_pitch, d_rows_per_seq, dtype, draft_tokens,
-                         uniforms, B, K, V, temperature, top_p, saguaro_F, saguaro_C, accept_len, out_tokens, debug,
+                         uniforms, B, K, V, temperature, top_p, top_k, saguaro_F, saguaro_C, accept_len, out_tokens, debug,
                          stats, workspace, workspace_bytes, stream_);
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (B < 1 || K < 0 || K > SV_MAX_K || V < 1) return SV_ERR_INVALID_ARG;

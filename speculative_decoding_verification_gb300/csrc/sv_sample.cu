@@ -162,8 +162,8 @@ static SamplePlan plan_sample(int B, int n_rows, int V, int es) {
 }
 
 template <int ES>
-static sv_status launch_sample(const SamplePlan &sp, const SampleArgs &in, const float *top_p, int F, int B,
-                               void *ws, cudaStream_t stream) {
+static sv_status launch_sample(const SamplePlan &sp, const SampleArgs &in, const float *top_p,
+                               const int32_t *top_k, int F, int B, void *ws, cudaStream_t stream) {
     const VerifyPlan &pl = sp.v;
     DeviceInfo di;
     if (!device_info(di)) return SV_ERR_CUDA;
@@ -192,10 +192,10 @@ static sv_status launch_sample(const SamplePlan &sp, const SampleArgs &in, const
     }
     NucleusCut *nuc = nullptr;
     TopSet *top = nullptr;
-    if (top_p) {
+    if (top_p || top_k) {
         nuc = reinterpret_cast<NucleusCut *>(w + pl.off_nuc);
-        const sv_status st = launch_nucleus<ES>(a.rows, a.rows, pl.n_rows0, 0, a.V, a.temperature, top_p, part,
-                                                pl.n_split, rowstat, nuc, a.stats, di, stream);
+        const sv_status st = launch_nucleus<ES>(a.rows, a.rows, pl.n_rows0, 0, a.V, a.temperature, top_p, top_k,
+                                                part, pl.n_split, nuc, a.stats, stream);
         if (st != SV_OK) return st;
     }
     if (a.sag_on) {
@@ -270,8 +270,8 @@ extern "C" size_t sv_saguaro_sample_workspace_size(int B, int n_rows, int V) {
 }
 
 extern "C" sv_status sv_saguaro_sample(const void *draft_logits, int64_t row_pitch, int rows_per_seq, sv_dtype dtype,
-                                       int B, int n_rows, int V, const float *temperature, const float *top_p, int F,
-                                       float C, const double *uniforms, int32_t *tokens, double *debug,
+                                       int B, int n_rows, int V, const float *temperature, const float *top_p,
+                                       const int32_t *top_k, int F, float C, const double *uniforms, int32_t *tokens, double *debug,
                                        sv_stats *stats, void *workspace, size_t workspace_bytes,
                                        sv_stream_t stream_) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -294,6 +294,6 @@ extern "C" sv_status sv_saguaro_sample(const void *draft_logits, int64_t row_pit
     a.tokens = tokens;
     a.debug = debug;
     a.stats = stats;
-    if (es == 4) return launch_sample<4>(sp, a, top_p, F, B, workspace, stream);
-    return launch_sample<2>(sp, a, top_p, F, B, workspace, stream);
+    if (es == 4) return launch_sample<4>(sp, a, top_p, top_k, F, B, workspace, stream);
+    return launch_sample<2>(sp, a, top_p, top_k, F, B, workspace, stream);
 }

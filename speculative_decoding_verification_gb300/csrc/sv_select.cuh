@@ -4,12 +4,15 @@
 //    digit radix select on order-preserving 32-bit keys (two 8-bit passes for bf16, four for
 //    float32) finds the key K* of the N-th token; ties at K* are taken in id order by an ordered
 //    block scan, so ranking ties go to the lowest id.
-//  * nucleus (top-p) cut [SpS notes §3 and §6: the filter acts on q and on p before the ratio]:
-//    the same radix select weighted by probability mass 2^(x c - r) finds the shortest prefix in
-//    (probability desc, id asc) order whose mass reaches top_p.  The float32 masses carry a
+//  * top-k and nucleus (top-p) cuts [SpS notes §3 and §6: the filters act on q and on p before
+//    the ratio]: the count select finds the k-th token; the same radix select weighted by
+//    probability mass 2^(x c - r) finds the shortest prefix in (probability desc, id asc) order
+//    whose mass reaches top_p (of the row, or of the top-k set when both are on).  The float32 masses carry a
 //    proven error bound; a cut the bound cannot settle is recomputed in float-float in the same
 //    block.
 #pragma once
+
+#include <cooperative_groups.h>
 
 #include "sv_device.cuh"
 #include "sv_exp2_table.h"
@@ -273,7 +276,8 @@ struct NucleusArgs {
     long long n_rows0, n_rows;
     int V;
     const float *temperature;
-    const float *top_p;
+    const float *top_p;      // [B] or null
+    const int32_t *top_k;    // [B] or null
     const WarpPartial *part;
     int n_split;
     NucleusCut *nuc;
@@ -373,13 +377,42 @@ __device__ uint32_t radix_select_mass(const char *row, int V, double target_in, 
     return complete_key<ES>(prefix);
 }
 
+// Block sums of three doubles; every thread gets the totals.  s_red holds 3 * kWarps doubles.
+__device__ __forceinline__ double3 block_sum_d3(double x, double y, double z, double *s_red) {
+    x = warp_sum_d(x);
+    y = warp_sum_d(y);
+    z = warp_sum_d(z);
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        s_red[w] = x;
+        s_red[kWarps + w] = y;
+        s_red[2 * kWarps + w] = z;
+    }
+    __syncthreads();
+    double3 t = {0.0, 0.0, 0.0};
+    for (int i = 0; i < kWarps; ++i) {
+        t.x += s_red[i];
+        t.y += s_red[kWarps + i];
+        t.z += s_red[2 * kWarps + i];
+    }
+    __syncthreads();
+    return t;
+}
+
+// The filters of one row as one upper set of the (logit desc, id asc) order.  Top-k keeps
+// the first k tokens: a count-weighted select finds the key of the k-th, exactly.  Top-p keeps
+// the shortest prefix whose mass reaches top_p times the mass it filters (the whole row, or
+// the top-k set when both are on: top-k acts first and the nucleus is that of the
+// renormalised top-k distribution, and since both are prefixes of one order the result is
+// the shorter of the two).  Masses: float32 with a proven bound, float-float when the bound
+// cannot settle the nucleus cut.
 template <int ES>
 __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
     __shared__ double hm[256 + kWarps];
     __shared__ unsigned hc[256];
     __shared__ int s_dig[2], s_warp[kWarps], s_last;
     __shared__ double s_dm[2];
-    __shared__ double s_red[kWarps];
+    __shared__ double s_red[3 * kWarps];
     __shared__ float2 tab[256];
     __shared__ RowStat s_rs;
     const long long rid = blockIdx.x;
@@ -389,7 +422,10 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
     const RowSet &rs = a.set[s];
     const long long b = lr / rs.rows_used, j = lr - b * rs.rows_used;
     const float T = a.temperature[b];
-    const float tp = a.top_p[b];
+    const float tp = a.top_p ? a.top_p[b] : 1.0f;
+    const int tk = a.top_k ? a.top_k[b] : 0;
+    const bool p_on = tp < 1.0f;
+    const bool k_on = tk > 0 && tk < a.V;
     NucleusCut none;
     none.cut_x = -INFINITY;
     none.cut_id = 0x7FFFFFFF;
@@ -397,7 +433,7 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
     none.log2_mass = 0.0;
     none.ambiguous = 0;
     none.mass_f = 1.0f;
-    if (!(tp < 1.0f) || !(T >= 1e-3f && T <= 1e3f)) {   // off, greedy or invalid temperature
+    if (!(p_on || k_on) || !(T >= 1e-3f && T <= 1e3f)) {   // off, greedy or invalid temperature
         if (threadIdx.x == 0) a.nuc[rid] = none;
         return;
     }
@@ -416,27 +452,73 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
     log2e_over(T, c_hi, c_lo);
     const float rf = (float)st.r;
 
+    // ---- top-k: the key of the k-th token and how many of its ties are kept ----
+    uint32_t kk = 0;
+    int k_ties = 0;
+    float xk = -INFINITY;
+    if (k_on) {
+        int n_above;
+        kk = radix_select_count<ES>(row, a.V, tk, n_above, hc, s_dig);
+        k_ties = tk - n_above;
+        xk = key_value(kk);
+    }
+
     // ---- float32 tier: masses 2^(x c - r) as in the statistics pass ----
     auto fast_mass = [&](float x) {   // (mass, mass * |y|): the second feeds the error bound
         const float y = fmaf(x, c_lo, fmaf(x, c_hi, -rf));
         const float e = ex2_fast(y);
         return make_double2((double)e, (double)(e * fabsf(y)));
     };
-    double above_m, S_fast, A_row;
-    int cnt_star;
-    const uint32_t kstar = radix_select_mass<ES>(row, a.V, 0.0, (double)tp, fast_mass, hm, hc, s_dig, s_dm, s_red,
-                                                 above_m, cnt_star, &S_fast, &A_row);
-    const double target = (double)tp * S_fast;
-    const float xstar = key_value(kstar);
-    const double estar = (double)ex2_fast(fmaf(xstar, c_lo, fmaf(xstar, c_hi, -rf)));
-    int jt = (int)ceil((target - above_m) / estar);
-    jt = max(1, min(jt, cnt_star));
+    double S_fast = 0.0, A_row = 0.0, M_above_k = 0.0, M_k = 0.0, e_k = 0.0;
+    if (k_on) {   // row sum, error weight and the top-k mass in one pass
+        double ts = 0.0, ta = 0.0, tm = 0.0;
+        for_each_elem<ES>(row, a.V, [&](float x, int) {
+            const double2 w = fast_mass(x);
+            ts += w.x;
+            ta += w.y;
+            if (f32_key(x) > kk) tm += w.x;
+        });
+        const double3 t = block_sum_d3(ts, ta, tm, s_red);
+        S_fast = t.x;
+        A_row = t.y;
+        M_above_k = t.z;
+        e_k = fast_mass(xk).x;
+        M_k = M_above_k + k_ties * e_k;
+    }
+    uint32_t kstar = kk;
+    float xstar = xk;
+    double above_m = M_above_k, estar = e_k, target = M_k;
+    int jt = k_ties;
+    if (p_on) {
+        int cnt_star;
+        if (k_on) {
+            target = (double)tp * M_k;
+            kstar = radix_select_mass<ES>(row, a.V, target, 0.0, fast_mass, hm, hc, s_dig, s_dm, s_red, above_m,
+                                          cnt_star, nullptr, nullptr);
+        } else {
+            kstar = radix_select_mass<ES>(row, a.V, 0.0, (double)tp, fast_mass, hm, hc, s_dig, s_dm, s_red, above_m,
+                                          cnt_star, &S_fast, &A_row);
+            target = (double)tp * S_fast;
+        }
+        xstar = key_value(kstar);
+        estar = fast_mass(xstar).x;
+        jt = (int)ceil((target - above_m) / estar);
+        jt = max(1, min(jt, cnt_star));
+        if (k_on && (kstar < kk || (kstar == kk && jt > k_ties))) {   // past the top-k set
+            kstar = kk;
+            xstar = xk;
+            jt = k_ties;
+            estar = e_k;
+            above_m = M_above_k;
+        }
+    }
     // certification: cum and target come from the same per-element masses; the kept set is an
-    // upper set, so its error per unit mass is at most the row's (weighted mean of |y|).
+    // upper set, so its error per unit mass is at most the row's (weighted mean of |y|).  A
+    // top-k cut alone involves no rounding.
     const double cum_hi = above_m + jt * estar, cum_lo = above_m + (jt - 1) * estar;
     const double rel = kEx2RelErr + 1.02 * kYRound * (A_row / S_fast) + 4.0 * kU32 + 1e-12;
-    const double E = rel * (cum_hi + (double)tp * S_fast) + 1e-15 * S_fast;
-    const bool ambiguous = (target - cum_lo) <= E || (cum_hi - target) <= E;
+    const double E = rel * (cum_hi + target) + 1e-15 * S_fast;
+    const bool ambiguous = p_on && ((target - cum_lo) <= E || (cum_hi - target) <= E);
     NucleusCut out;
     out.ambiguous = ambiguous ? 1 : 0;
     out.mass_f = 1.0f;
@@ -445,23 +527,46 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
         out.cut_id = ordered_ties<ES>(row, a.V, kstar, jt, nullptr, s_warp, &s_last);
         out.mass = cum_hi / S_fast;
     } else {
-        // ---- float-float tier: the same select on exact masses ----
-        {
-            tab[threadIdx.x] = kExp2Table[threadIdx.x];
-        }
+        // ---- float-float tier: the same selects on exact masses ----
+        tab[threadIdx.x] = kExp2Table[threadIdx.x];
         __syncthreads();
         const ff cff = {c_hi, c_lo};
         auto exact = [&](float x) { return make_double2(exact_mass(x, cff, rf, tab), 0.0); };
-        double A_x, S_x;
+        double A_x, S_x, tgt, M_above_kx = 0.0, e_kx = 0.0;
         int cnt_x;
-        const uint32_t kx = radix_select_mass<ES>(row, a.V, 0.0, (double)tp, exact, hm, hc, s_dig, s_dm, s_red, A_x,
-                                                  cnt_x, &S_x, nullptr);
-        const float xx = key_value(kx);
-        const double e_x = exact_mass(xx, cff, rf, tab);
-        const double tgt = (double)tp * S_x;
-        const double jr = (tgt - A_x) / e_x;
+        uint32_t kx;
+        if (k_on) {
+            double ts = 0.0, tm = 0.0;
+            for_each_elem<ES>(row, a.V, [&](float x, int) {
+                const double m = exact(x).x;
+                ts += m;
+                if (f32_key(x) > kk) tm += m;
+            });
+            const double3 t = block_sum_d3(ts, tm, 0.0, s_red);
+            S_x = t.x;
+            M_above_kx = t.y;
+            e_kx = exact(xk).x;
+            tgt = (double)tp * (M_above_kx + k_ties * e_kx);
+            kx = radix_select_mass<ES>(row, a.V, tgt, 0.0, exact, hm, hc, s_dig, s_dm, s_red, A_x, cnt_x, nullptr,
+                                       nullptr);
+        } else {
+            kx = radix_select_mass<ES>(row, a.V, 0.0, (double)tp, exact, hm, hc, s_dig, s_dm, s_red, A_x, cnt_x, &S_x,
+                                       nullptr);
+            tgt = (double)tp * S_x;
+        }
+        float xx = key_value(kx);
+        double e_x = exact(xx).x;
+        double jr = (tgt - A_x) / e_x;
         int jx = (int)ceil(jr);
         jx = max(1, min(jx, cnt_x));
+        if (k_on && (kx < kk || (kx == kk && jx > k_ties))) {
+            kx = kk;
+            xx = xk;
+            e_x = e_kx;
+            A_x = M_above_kx;
+            jx = k_ties;
+            jr = (tgt - A_x) / e_x;
+        }
         const bool unres = fabs(jr - rint(jr)) < 1e-9 * fmax(1.0, fabs(jr));
         out.cut_x = xx;
         out.cut_id = ordered_ties<ES>(row, a.V, kx, jx, nullptr, s_warp, &s_last);
@@ -476,13 +581,548 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
     if (threadIdx.x == 0) a.nuc[rid] = out;
 }
 
+// ------------------------------------------------------------------------------------------
+// bf16 rows: the filters from a histogram of the row's values.
+//
+// A bf16 logit takes one of 65536 values and its 16-bit order key is its rank among them.  A
+// cluster of kNucSplit blocks shares a row: block q holds one counter per value for the q-th
+// quarter of the keys from the top (64 KB of shared memory), and each block reads a quarter of
+// the row and adds its tokens to the counters of whichever block holds their values
+// (distributed shared memory).  All tokens of one value carry the same mass 2^(x c - r), so the
+// mass a value holds is its count times one float-float exponential, and the cumulative count
+// and mass in (value desc) order come from scans over the counters rather than the tokens.  The
+// k-th token and the nucleus cut follow from float-float masses (relative error ~2^-44 each);
+// the position inside the cut's group of equal values is then found in id order.
+// ------------------------------------------------------------------------------------------
+constexpr int kNucSplit = 4;                                  // blocks per row
+constexpr int kNucKeys = 65536 / kNucSplit;                   // values counted per block
+constexpr int kNucBins = kNucKeys / kThreads;                 // values per thread segment (64)
+constexpr size_t kNucHistBytes = kNucKeys * sizeof(unsigned);
+static_assert(kNucBins == 64, "two values per lane per segment");
+
+struct NucXch {   // what one block of the cluster publishes to the others
+    ff mass;      // total mass of the block's keys / mass strictly above a located cut
+    ff each;      // mass of one token at the cut's value
+    int count;    // tokens in the block's keys / tokens of the cut's value
+    int key, pos; // a located cut: 16-bit key and how many of its equal values are kept
+    int pad;
+};
+
+// 16-bit order key of a bf16 bit pattern (-0 ranks with +0).
+__device__ __forceinline__ uint32_t bf16_key16(uint32_t bits) {
+    if (bits == 0x8000u) bits = 0u;
+    return (bits & 0x8000u) ? (0xFFFFu - bits) : (bits | 0x8000u);
+}
+
+// The bf16 value of a 16-bit order key.
+__device__ __forceinline__ float bf16_key_value(uint32_t k16) {
+    const uint32_t bits = (k16 & 0x8000u) ? (k16 & 0x7FFFu) : (0xFFFFu - k16);
+    return __uint_as_float(bits << 16);
+}
+
+// Float-float mass 2^(x c - r) of one token of the value with key k16.
+__device__ __forceinline__ ff key_mass(uint32_t k16, ff c, int r, const float2 *tab) {
+    const float x = bf16_key_value(k16);
+    if (x == -INFINITY) return {0.f, 0.f};
+    return ff_exp2_xc(x, c, r, tab);
+}
+
+__device__ __forceinline__ ff ff_shfl_xor(ff v, int o) {
+    return {__shfl_xor_sync(0xFFFFFFFFu, v.hi, o), __shfl_xor_sync(0xFFFFFFFFu, v.lo, o)};
+}
+__device__ __forceinline__ ff ff_shfl_up(ff v, int o) {
+    return {__shfl_up_sync(0xFFFFFFFFu, v.hi, o), __shfl_up_sync(0xFFFFFFFFu, v.lo, o)};
+}
+__device__ __forceinline__ ff ff_shfl(ff v, int l) {
+    return {__shfl_sync(0xFFFFFFFFu, v.hi, l), __shfl_sync(0xFFFFFFFFu, v.lo, l)};
+}
+// 32-bit shared::cluster address of a shared variable in block `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_map(const void *p, uint32_t rank) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+
+// Atomic add to a shared::cluster address, no result.
+__device__ __forceinline__ void dsmem_red_add(uint32_t addr, uint32_t v) {
+    asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ bool ff_ge(ff a, ff b) { return a.hi > b.hi || (a.hi == b.hi && a.lo >= b.lo); }
+__device__ __forceinline__ ff ff_times(ff m, unsigned n) { return ff_mul(m, {(float)n, 0.f}); }
+
+// A located cut inside one block's keys, in (value desc) order: the value `key`, of which `pos`
+// tokens are kept; `mass` is the mass strictly above it and `each` one token's mass.  Count
+// mode: the need-th token from the top of the block.  Mass mode: the first value at which base +
+// the cumulative mass reaches target.  Called by the whole block; one warp walks the segment
+// that holds the cut and writes *out.
+__device__ __forceinline__ void locate_cut(bool by_mass, int need, ff base, ff target, uint32_t kbase,
+                                           const unsigned *cnt, const int *exc, const ff *exm, const int *segc,
+                                           const ff *segm, ff c, int r, const float2 *tab, int *s_owner, NucXch *out) {
+    const int t = threadIdx.x, lane = t & 31;
+    if (t == 0) *s_owner = kThreads;
+    __syncthreads();
+    const bool mine = segc[t] > 0 && (by_mass ? ff_ge(ff_add(base, ff_add(exm[t], segm[t])), target)
+                                              : exc[t] + segc[t] >= need);
+    if (mine) atomicMin(s_owner, t);
+    __syncthreads();
+    int owner = *s_owner;
+    if (owner == kThreads) {   // rounding left the mass short of target: the last occupied value
+        __syncthreads();
+        if (t == 0) *s_owner = -1;
+        __syncthreads();
+        if (segc[t] > 0) atomicMax(s_owner, t);
+        __syncthreads();
+        owner = *s_owner;
+        if (owner < 0 && t == 0) *out = {base, {0.f, 0.f}, 0, (int)kbase, 1, 0};   // an empty block (not reached)
+    }
+    if (owner >= 0 && (t >> 5) == (owner >> 5)) {
+        const int top = kNucKeys - 1 - kNucBins * owner;
+        ff cum = ff_add(base, exm[owner]);
+        int cc = exc[owner];
+        bool done = false;
+        int last_lane = -1;
+        NucXch last = {};
+        for (int g = 0; g < 2 && !done; ++g) {
+            const int li = top - (32 * g + lane);
+            const unsigned n = cnt[li];
+            const uint32_t k16 = kbase + (uint32_t)li;
+            const ff m = n ? key_mass(k16, c, r, tab) : ff{0.f, 0.f};
+            const ff add = n ? ff_times(m, n) : ff{0.f, 0.f};
+            int ci = (int)n;
+            ff mi = add;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int tc = __shfl_up_sync(0xFFFFFFFFu, ci, o);
+                const ff tm = ff_shfl_up(mi, o);
+                if (lane >= o) {
+                    ci += tc;
+                    mi = ff_add(tm, mi);
+                }
+            }
+            ff ex = ff_shfl_up(mi, 1);
+            int cx = __shfl_up_sync(0xFFFFFFFFu, ci, 1);
+            if (lane == 0) {
+                ex = {0.f, 0.f};
+                cx = 0;
+            }
+            const ff above = ff_add(cum, ex);
+            const bool cross = n > 0 && (by_mass ? ff_ge(ff_add(cum, mi), target) : cc + ci >= need);
+            const unsigned mask = __ballot_sync(0xFFFFFFFFu, cross);
+            const unsigned occ = __ballot_sync(0xFFFFFFFFu, n > 0);
+            if (mask) {
+                if (lane == __ffs(mask) - 1) {
+                    int pos;
+                    if (by_mass) {
+                        const ff d = ff_sub(target, above);
+                        const double md = ff_to_double(m);
+                        pos = md > 0.0 ? (int)ceil(ff_to_double(d) / md) : 1;
+                    } else {
+                        pos = need - (cc + cx);
+                    }
+                    *out = {above, m, (int)n, (int)k16, max(1, min(pos, (int)n)), 0};
+                }
+                done = true;
+            } else if (occ) {
+                const int L = 31 - __clz(occ);
+                if (lane == L) last = {above, m, (int)n, (int)k16, (int)n, 0};
+                last_lane = L;
+            }
+            cum = ff_add(cum, ff_shfl(mi, 31));
+            cc += __shfl_sync(0xFFFFFFFFu, ci, 31);
+        }
+        if (!done && lane == last_lane) *out = last;   // not reached by the mass: the last value, all of it
+    }
+    __syncthreads();
+}
+
+// Matches of key k16 among the 8 bf16 tokens of a 16-byte word.
+__device__ __forceinline__ int key_matches8(uint4 q, uint32_t k16) {
+    const uint32_t a[4] = {q.x, q.y, q.z, q.w};
+    int m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m += bf16_key16(a[i] & 0xFFFFu) == k16;
+        m += bf16_key16(a[i] >> 16) == k16;
+    }
+    return m;
+}
+
+// Id of the pos-th token (1-based, in id order) whose bf16 key is k16, found by the blocks of the
+// cluster together: the row is cut into kNucSplit * kWarps stretches, one per warp; each lane
+// keeps the match count of every 16-byte word it reads (4 bits each), so the warp whose stretch
+// holds the pos-th match finds its word by scanning those counts and reads that word once more.
+// Returns the id in block 0 (-1 if the row has fewer matches).
+constexpr int kTieWords = 32;   // words per lane kept (stretches up to 1024 words: V <= 262144)
+
+template <class Cluster>
+__device__ int bf16_tie_id(Cluster &cl, int rank, const char *row, int V, uint32_t k16, int pos, int *s_wc,
+                           int *s_own, int *s_res) {
+    constexpr int kStretches = kNucSplit * kWarps;
+    constexpr int kDepth = 8;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = rank * kWarps + w;
+    const int n_vec = (V * 2) / 16;
+    const int per = (n_vec + kStretches - 1) / kStretches;
+    const int lo = min(n_vec, g * per), hi = min(n_vec, lo + per);
+    const int J = (per + 31) / 32;   // words per lane
+    const uint4 *rv = reinterpret_cast<const uint4 *>(row);
+    const uint16_t *r16 = reinterpret_cast<const uint16_t *>(row);
+    uint32_t nib[kTieWords / 8] = {0u, 0u, 0u, 0u};
+    int cnt = 0;
+    for (int j0 = 0; j0 < J; j0 += kDepth) {
+        uint4 q[kDepth];
+#pragma unroll
+        for (int d = 0; d < kDepth; ++d) {
+            const int vi = lo + 32 * (j0 + d) + lane;
+            q[d] = (j0 + d < J && vi < hi) ? __ldg(rv + vi) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int d = 0; d < kDepth; ++d) {
+            const int j = j0 + d, vi = lo + 32 * j + lane;
+            const int m = (j < J && vi < hi) ? key_matches8(q[d], k16) : 0;
+            cnt += m;
+            if (j < kTieWords) {
+#pragma unroll
+                for (int x = 0; x < kTieWords / 8; ++x)
+                    if ((j >> 3) == x) nib[x] |= (uint32_t)m << (4 * (j & 7));
+            }
+        }
+    }
+    if (g == kStretches - 1)
+        for (int v = n_vec * 8 + lane; v < V; v += 32) cnt += bf16_key16(r16[v]) == k16;
+    cnt = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)cnt);
+    if (lane == 0) s_wc[w] = cnt;
+    if (threadIdx.x == 0) *s_res = -1;
+    cl.sync();
+    static_assert(kStretches == 32, "one stretch per lane of warp 0");
+    if (threadIdx.x < 32) {   // the stretch that holds the pos-th match: lane l reads stretch l
+        const int cx = cl.map_shared_rank(s_wc, lane / kWarps)[lane % kWarps];
+        int inc = cx;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int tt = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += tt;
+        }
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, inc - cx < pos && pos <= inc);
+        const int L = hit ? __ffs(hit) - 1 : -1;
+        const int L_off = __shfl_sync(0xFFFFFFFFu, inc - cx, L < 0 ? 0 : L);
+        if (lane == 0) {
+            s_own[0] = L;
+            s_own[1] = L_off;
+        }
+    }
+    __syncthreads();
+    const int own = s_own[0];
+    if (own == g) {
+        int need = pos - s_own[1];
+        for (int j = 0; j < J && need > 0; ++j) {
+            int m;
+            if (j < kTieWords) {
+                m = (int)((nib[j >> 3] >> (4 * (j & 7))) & 15u);
+            } else {
+                const int vi = lo + 32 * j + lane;
+                m = vi < hi ? key_matches8(__ldg(rv + vi), k16) : 0;
+            }
+            int inc = m;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int tt = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+                if (lane >= o) inc += tt;
+            }
+            const int tot = __shfl_sync(0xFFFFFFFFu, inc, 31);
+            if (tot >= need) {
+                if (inc - m < need && inc >= need) {
+                    const int vi = lo + 32 * j + lane;
+                    const uint4 qq = __ldg(rv + vi);
+                    const uint32_t a4[4] = {qq.x, qq.y, qq.z, qq.w};
+                    int k = need - (inc - m);
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t bits = (i & 1) ? (a4[i >> 1] >> 16) : (a4[i >> 1] & 0xFFFFu);
+                        if (bf16_key16(bits) == k16 && --k == 0) {
+                            *s_res = vi * 8 + i;
+                            break;
+                        }
+                    }
+                }
+                need = 0;
+            } else {
+                need -= tot;
+            }
+        }
+        if (need > 0 && g == kStretches - 1 && lane == 0)   // the scalar tail
+            for (int v = n_vec * 8; v < V; ++v)
+                if (bf16_key16(r16[v]) == k16 && --need == 0) {
+                    *s_res = v;
+                    break;
+                }
+    }
+    cl.sync();
+    return (rank == 0 && own >= 0) ? *cl.map_shared_rank(s_res, own / kWarps) : -1;
+}
+
+template <int ES>
+__global__ void __cluster_dims__(kNucSplit, 1, 1) __launch_bounds__(kThreads, 3) k_nucleus_hist(const NucleusArgs a) {
+    static_assert(ES == 2, "value histogram: bf16 rows only");
+    namespace cg = cooperative_groups;
+    extern __shared__ __align__(16) unsigned s_cnt[];   // kNucKeys counters
+    __shared__ float2 tab[256];
+    __shared__ int s_segc[kThreads], s_exc[kThreads];
+    __shared__ ff s_segm[kThreads], s_exm[kThreads];
+    __shared__ NucXch s_x[3];                           // totals, top-k cut, nucleus cut
+    __shared__ int s_owner, s_wc[kWarps], s_own[2], s_res;
+    __shared__ RowStat s_rs;
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank();
+    const long long rid = blockIdx.x / kNucSplit;
+    if (rid >= a.n_rows) return;                        // the whole cluster
+    const int s = rid < a.n_rows0 ? 0 : 1;
+    const long long lr = s == 0 ? rid : rid - a.n_rows0;
+    const RowSet &rs = a.set[s];
+    const long long b = lr / rs.rows_used, j = lr - b * rs.rows_used;
+    const float T = a.temperature[b];
+    const float tp = a.top_p ? a.top_p[b] : 1.0f;
+    const int tk = a.top_k ? a.top_k[b] : 0;
+    const bool p_on = tp < 1.0f;
+    const bool k_on = tk > 0 && tk < a.V;
+    NucleusCut none;
+    none.cut_x = -INFINITY;
+    none.cut_id = 0x7FFFFFFF;
+    none.mass = 1.0;
+    none.log2_mass = 0.0;
+    none.ambiguous = 0;
+    none.mass_f = 1.0f;
+    if (!(p_on || k_on) || !(T >= 1e-3f && T <= 1e3f)) {   // off, greedy or invalid temperature
+        if (threadIdx.x == 0 && rank == 0) a.nuc[rid] = none;
+        return;
+    }
+    const char *row = rs.base + (b * rs.rows_per_seq + j) * rs.pitch_bytes;
+    if (threadIdx.x < 32) {
+        const RowStat st = combine_row(a.part + (size_t)rid * a.n_split * kWarps, a.n_split * kWarps, false, T);
+        if (threadIdx.x == 0) s_rs = st;
+    }
+    tab[threadIdx.x] = kExp2Table[threadIdx.x];
+    for (int i = threadIdx.x; i < kNucKeys / 4; i += kThreads) reinterpret_cast<uint4 *>(s_cnt)[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    const RowStat st = s_rs;
+    if (!rs_sampled_ok(st) || st.flags) {   // reported by the accept / sampling kernels
+        if (threadIdx.x == 0 && rank == 0) a.nuc[rid] = none;
+        return;
+    }
+    float c_hi, c_lo;
+    log2e_over(T, c_hi, c_lo);
+    const ff c = {c_hi, c_lo};
+    const int r = st.r;
+
+    // ---- counts per value: every block reads the whole row and counts the tokens whose values
+    //      fall in its quarter of the keys (block q: the q-th quarter from the top).  The quarter
+    //      of a bf16 value is fixed by its two top bits; -0 and +0 are counted apart here
+    //      (adjacent keys of the same mass) and taken together when a cut falls on them. ----
+    const uint32_t kbase = (uint32_t)(kNucSplit - 1 - rank) * (uint32_t)kNucKeys;
+    {
+        // block 0: bits 0x4000-0x7FFF, 1: 0x0000-0x3FFF (non-negative); 2: 0x8000-0xBFFF,
+        // 3: 0xC000-0xFFFF (negative, whose keys run opposite to their bits)
+        const uint32_t top2 = rank == 0 ? 0x4000u : rank == 1 ? 0x0000u : rank == 2 ? 0x8000u : 0xC000u;
+        const uint32_t flip = rank < 2 ? 0u : 0xFFFFu;
+        auto add_tok = [&](uint32_t bits) {
+            if ((bits & 0xC000u) == top2) atomicAdd(&s_cnt[(bits ^ flip) & (uint32_t)(kNucKeys - 1)], 1u);
+        };
+        auto add8 = [&](uint4 wd) {
+            add_tok(wd.x & 0xFFFFu);
+            add_tok(wd.x >> 16);
+            add_tok(wd.y & 0xFFFFu);
+            add_tok(wd.y >> 16);
+            add_tok(wd.z & 0xFFFFu);
+            add_tok(wd.z >> 16);
+            add_tok(wd.w & 0xFFFFu);
+            add_tok(wd.w >> 16);
+        };
+        const int n_vec = (a.V * 2) / 16;
+        const uint4 *rv = reinterpret_cast<const uint4 *>(row);
+        constexpr int kDepth = 8;   // loads in flight per thread
+        int vi = threadIdx.x;
+        for (; vi + (kDepth - 1) * kThreads < n_vec; vi += kDepth * kThreads) {
+            uint4 q[kDepth];
+#pragma unroll
+            for (int d = 0; d < kDepth; ++d) q[d] = __ldg(rv + vi + d * kThreads);
+#pragma unroll
+            for (int d = 0; d < kDepth; ++d) add8(q[d]);
+        }
+        for (; vi < n_vec; vi += kThreads) add8(__ldg(rv + vi));
+        const uint16_t *r16 = reinterpret_cast<const uint16_t *>(row);
+        for (int v = n_vec * 8 + threadIdx.x; v < a.V; v += kThreads) add_tok(r16[v]);
+    }
+    cl.sync();   // all counts are in
+
+    // ---- segment sums: a segment is kNucBins adjacent keys (segment t of block q: the values
+    //      just below key top(t)); the 4 x 256 segments are dealt round-robin to the blocks so
+    //      that a dense stretch of values is shared out; two values per lane ----
+    {
+        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+        constexpr int kAhead = 4;   // segments whose counters are loaded together
+        for (int q0 = 0; q0 < 32; q0 += kAhead) {
+            unsigned n0[kAhead], n1[kAhead];
+#pragma unroll
+            for (int d = 0; d < kAhead; ++d) {
+                const int G = kNucSplit * (32 * w + q0 + d) + rank;
+                const unsigned *cnt = cl.map_shared_rank(s_cnt, G / kThreads);
+                const int top = kNucKeys - 1 - kNucBins * (G % kThreads);
+                n0[d] = cnt[top - lane];
+                n1[d] = cnt[top - 32 - lane];
+            }
+#pragma unroll
+            for (int d = 0; d < kAhead; ++d) {
+                const int G = kNucSplit * (32 * w + q0 + d) + rank;
+                const int owner = G / kThreads, seg = G % kThreads;
+                const uint32_t kb = (uint32_t)(kNucSplit - 1 - owner) * (uint32_t)kNucKeys;
+                const int top = kNucKeys - 1 - kNucBins * seg;
+                int *segc = cl.map_shared_rank(s_segc, owner);
+                ff *segm = cl.map_shared_rank(s_segm, owner);
+                if (!__any_sync(0xFFFFFFFFu, (n0[d] | n1[d]) != 0)) {
+                    if (lane == 0) {
+                        segc[seg] = 0;
+                        segm[seg] = {0.f, 0.f};
+                    }
+                    continue;
+                }
+                ff m = {0.f, 0.f};
+                if (n0[d]) m = ff_times(key_mass(kb + (uint32_t)(top - lane), c, r, tab), n0[d]);
+                if (n1[d]) m = ff_add(m, ff_times(key_mass(kb + (uint32_t)(top - 32 - lane), c, r, tab), n1[d]));
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) m = ff_add(m, ff_shfl_xor(m, o));
+                const int nc = (int)__reduce_add_sync(0xFFFFFFFFu, n0[d] + n1[d]);
+                if (lane == 0) {
+                    segc[seg] = nc;
+                    segm[seg] = m;
+                }
+            }
+        }
+    }
+    cl.sync();
+    if (threadIdx.x < 32) {   // exclusive prefixes over the segments, 8 per lane in order
+        const int lane = threadIdx.x;
+        int lc = 0;
+        ff lm = {0.f, 0.f};
+        for (int q = 0; q < 8; ++q) {
+            lc += s_segc[8 * lane + q];
+            lm = ff_add(lm, s_segm[8 * lane + q]);
+        }
+        int ic = lc;
+        ff im = lm;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int tc = __shfl_up_sync(0xFFFFFFFFu, ic, o);
+            const ff tm = ff_shfl_up(im, o);
+            if (lane >= o) {
+                ic += tc;
+                im = ff_add(tm, im);
+            }
+        }
+        int ec = ic - lc;
+        ff em = ff_shfl_up(im, 1);
+        if (lane == 0) em = {0.f, 0.f};
+        for (int q = 0; q < 8; ++q) {
+            s_exc[8 * lane + q] = ec;
+            s_exm[8 * lane + q] = em;
+            ec += s_segc[8 * lane + q];
+            em = ff_add(em, s_segm[8 * lane + q]);
+        }
+        if (lane == 31) {
+            s_x[0].count = ec;
+            s_x[0].mass = em;
+        }
+    }
+    cl.sync();
+    // totals of the blocks above this one, and of the row (the same sums in every block)
+    int cnt_above[kNucSplit];
+    ff m_above[kNucSplit];
+    ff S = {0.f, 0.f};
+    int C = 0;
+    for (int q = 0; q < kNucSplit; ++q) {
+        const NucXch *xq = cl.map_shared_rank(&s_x[0], q);
+        cnt_above[q] = C;
+        m_above[q] = S;
+        C += xq->count;
+        S = ff_add(S, xq->mass);
+    }
+
+    // ---- top-k: the k-th token from the top (exact counts) ----
+    int k_rank = 0;
+    if (k_on)
+        for (int q = 0; q < kNucSplit; ++q)
+            if (tk > cnt_above[q]) k_rank = q;
+    if (k_on && rank == k_rank)
+        locate_cut(false, tk - cnt_above[rank], m_above[rank], {0.f, 0.f}, kbase, s_cnt, s_exc, s_exm, s_segc,
+                   s_segm, c, r, tab, &s_owner, &s_x[1]);
+    cl.sync();
+    // -0 (key 0x7FFF) and +0 (key 0x8000) are one value: a cut on either becomes a cut on +0
+    // with the tokens of both, in id order
+    const int n_pz = (int)cl.map_shared_rank(s_cnt, 1)[0];
+    const int n_nz = (int)cl.map_shared_rank(s_cnt, 2)[kNucKeys - 1];
+    auto fold_zero = [&](NucXch &x) {
+        if (x.key == 0x7FFF) {
+            x.key = 0x8000;
+            x.mass = ff_sub(x.mass, ff_times(x.each, (unsigned)n_pz));
+            x.pos += n_pz;
+            x.count += n_pz;
+        } else if (x.key == 0x8000) {
+            x.count += n_nz;
+        }
+    };
+    NucXch kc = {};
+    if (k_on) {
+        kc = *cl.map_shared_rank(&s_x[1], k_rank);
+        fold_zero(kc);
+    }
+    const ff M_k = k_on ? ff_add(kc.mass, ff_times(kc.each, (unsigned)kc.pos)) : S;
+
+    // ---- top-p: the first value where the mass from the top reaches top_p of M_k ----
+    const ff target = ff_mul({tp, 0.f}, M_k);
+    int p_rank = 0;
+    if (p_on)
+        for (int q = 1; q < kNucSplit; ++q)
+            if (!ff_ge(m_above[q], target)) p_rank = q;
+    if (p_on && rank == p_rank)
+        locate_cut(true, 0, m_above[rank], target, kbase, s_cnt, s_exc, s_exm, s_segc, s_segm, c, r, tab, &s_owner,
+                   &s_x[2]);
+    cl.sync();
+    NucXch pc = kc;
+    if (p_on) {
+        pc = *cl.map_shared_rank(&s_x[2], p_rank);
+        fold_zero(pc);
+        if (k_on && (pc.key < kc.key || (pc.key == kc.key && pc.pos > kc.pos))) pc = kc;   // past the top-k set
+    }
+    cl.sync();   // every block has read the cuts before any is overwritten
+    // the id of the last kept token of the cut's value (all of them kept: no search)
+    const int cut_id = pc.pos >= pc.count ? 0x7FFFFFFF
+                                          : bf16_tie_id(cl, rank, row, a.V, (uint32_t)pc.key, pc.pos, s_wc, s_own, &s_res);
+    cl.sync();   // no block leaves while another may still read its shared memory
+    if (rank != 0) return;
+
+    const double above = ff_to_double(pc.mass), each = ff_to_double(pc.each), Sd = ff_to_double(S);
+    const double cum_hi = above + pc.pos * each;
+    NucleusCut out;
+    out.ambiguous = 0;
+    out.cut_x = bf16_key_value((uint32_t)pc.key);
+    out.cut_id = cut_id;
+    out.mass = cum_hi / Sd;
+    out.log2_mass = log2(out.mass);
+    out.mass_f = (float)out.mass;
+    if (threadIdx.x == 0) {
+        if (p_on) {
+            // each mass carries ~2^-44 and the float-float sums add ~2^-44 per level
+            const double tg = ff_to_double(target), cum_lo = above + (pc.pos - 1) * each;
+            const double E = 2e-11 * (cum_hi + tg);
+            if ((tg - cum_lo) <= E || (cum_hi - tg) <= E) stats_add(a.stats, &a.stats->unresolved, 1);
+        }
+        a.nuc[rid] = out;
+    }
+}
+
 template <int ES>
 sv_status launch_nucleus(const RowSet &tgt, const RowSet &drf, long long n_rows0, long long n_rows1, int V,
-                         const float *temperature, const float *top_p, const WarpPartial *part, int n_split,
-                         RowStat *rowstat, NucleusCut *nuc, sv_stats *stats, const DeviceInfo &di,
-                         cudaStream_t stream) {
-    (void)rowstat;
-    (void)di;
+                         const float *temperature, const float *top_p, const int32_t *top_k, const WarpPartial *part,
+                         int n_split, NucleusCut *nuc, sv_stats *stats, cudaStream_t stream) {
     NucleusArgs a;
     a.set[0] = tgt;
     a.set[1] = drf;
@@ -491,12 +1131,19 @@ sv_status launch_nucleus(const RowSet &tgt, const RowSet &drf, long long n_rows0
     a.V = V;
     a.temperature = temperature;
     a.top_p = top_p;
+    a.top_k = top_k;
     a.part = part;
     a.n_split = n_split;
     a.nuc = nuc;
     a.stats = stats;
     if (a.n_rows < 1) return SV_OK;
-    k_nucleus<ES><<<(unsigned)a.n_rows, kThreads, 0, stream>>>(a);
+    if constexpr (ES == 2) {
+        if (prepare_kernel(reinterpret_cast<const void *>(&k_nucleus_hist<2>), kThreads, kNucHistBytes) < 1)
+            return SV_ERR_CUDA;
+        k_nucleus_hist<2><<<(unsigned)(kNucSplit * a.n_rows), kThreads, kNucHistBytes, stream>>>(a);
+    } else {
+        k_nucleus<ES><<<(unsigned)a.n_rows, kThreads, 0, stream>>>(a);
+    }
     return cuda_status(cudaGetLastError());
 }
 
@@ -514,13 +1161,14 @@ struct TopSetArgs {
     int n_split;
     const NucleusCut *nuc;   // indexed by candidate row, or null
     TopSet *top;             // indexed by candidate row
+    sv_stats *stats;
 };
 
 template <int ES>
 __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
     __shared__ unsigned hist[256];
     __shared__ int s_dig[2], s_warp[kWarps], s_last;
-    __shared__ double s_red[kWarps];
+    __shared__ double s_red[3 * kWarps];
     __shared__ RowStat s_rs;
     const long long lr = blockIdx.x;
     if (lr >= a.n_rows) return;
@@ -555,40 +1203,60 @@ __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
     const uint32_t kstar = radix_select_count<ES>(row, a.V, N, n_above, hist, s_dig);
     const int last = ordered_ties<ES>(row, a.V, kstar, N - n_above, nullptr, s_warp, &s_last);
     const float xstar = key_value(kstar);
-    // mass of D, restricted to the nucleus when top-p is on
+    // masses inside and outside D among the tokens the top-k / top-p filters keep
     float c_hi, c_lo;
     log2e_over(T, c_hi, c_lo);
     const float rf = (float)st.r;
     float cut_x = -INFINITY;
     int cut_id = 0x7FFFFFFF;
-    double mass_n = 1.0;
     if (a.nuc) {
         cut_x = a.nuc[rid].cut_x;
         cut_id = a.nuc[rid].cut_id;
-        mass_n = a.nuc[rid].mass;
     }
-    double e_d = 0.0;
+    double e_in = 0.0, e_out = 0.0, a_in = 0.0, a_out = 0.0;
+    int n_out = 0;
     for_each_elem<ES>(row, a.V, [&](float x, int v) {
-        const bool in_d = x > xstar || (x == xstar && v <= last);
-        const bool keep = x > cut_x || (x == cut_x && v <= cut_id);
-        if (in_d && keep) e_d += (double)ex2_fast(fmaf(x, c_lo, fmaf(x, c_hi, -rf)));
+        if (x == -INFINITY || !(x > cut_x || (x == cut_x && v <= cut_id))) return;
+        const float y = fmaf(x, c_lo, fmaf(x, c_hi, -rf));
+        const float e = ex2_fast(y);
+        if (x > xstar || (x == xstar && v <= last)) {
+            e_in += (double)e;
+            a_in += (double)(e * fabsf(y));
+        } else {
+            e_out += (double)e;
+            a_out += (double)(e * fabsf(y));
+            ++n_out;
+        }
     });
-    e_d = warp_sum_d(e_d);
-    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = e_d;
-    __syncthreads();
+    const double3 t_in = block_sum_d3(e_in, a_in, (double)n_out, s_red);
+    const double3 t_out = block_sum_d3(e_out, a_out, 0.0, s_red);
     if (threadIdx.x == 0) {
-        double tot = 0.0;
-        for (int w = 0; w < kWarps; ++w) tot += s_red[w];
-        TopSet t;
-        t.top_x = xstar;
-        t.top_id = last;
-        t.p_d = fmin(1.0, tot / (rs_S(st) * mass_n));
-        t.z = 1.0 - (1.0 - (double)a.C) * t.p_d;
-        // p_d is a ratio of two sums of the same pass: relative error <= 2 err (x2 with top-p)
-        const double pd_rel = (a.nuc ? 4.04 : 2.02) * rs_err(st);
-        t.z_err = t.z > 0.0 ? (1.0 - (double)a.C) * t.p_d * pd_rel / t.z + 1e-12 : 1.0;
-        t.z_f = (float)t.z;
-        t.z_err_f = (float)t.z_err * (1.0f + 0x1p-20f);
+        const double C = (double)a.C, Ein = t_in.x, Eout = t_out.x;
+        const double num = C * Ein + Eout, den = Ein + Eout;
+        TopSet t = none;
+        if (C == 0.0 && t_in.z == 0.0) {
+            // every kept token lies in D and C = 0: no transform (the row is used unchanged)
+            t.p_d = 1.0;
+        } else if (!(num > 0.0)) {
+            // the mass left outside D underflows float32: no transform, reported as unresolved
+            stats_add(a.stats, &a.stats->unresolved, 1);
+        } else {
+            t.top_x = xstar;
+            t.top_id = last;
+            t.p_d = Ein / den;
+            t.z = num / den;
+            // each part is a sum of float32 masses: relative error kEx2RelErr + ln2 u |y| per
+            // token (A / E is the mass-weighted mean |y|) plus rounding; masses that flush to
+            // zero below 2^-126 are at most V 2^-126 in all
+            const double r_in = kEx2RelErr + 1.02 * kYRound * (Ein > 0.0 ? t_in.y / Ein : 0.0) + 4.0 * kU32;
+            const double r_out = kEx2RelErr + 1.02 * kYRound * (Eout > 0.0 ? t_out.y / Eout : 0.0) + 4.0 * kU32;
+            const double uf = (double)a.V * 0x1p-126;
+            const double rel_num = (C * Ein * r_in + Eout * r_out + uf) / num;
+            const double rel_den = (Ein * r_in + Eout * r_out + uf) / den;
+            t.z_err = rel_num + rel_den + 1e-12;
+            t.z_f = (float)t.z;
+            t.z_err_f = (float)t.z_err * (1.0f + 0x1p-20f);
+        }
         a.top[rid] = t;
     }
 }
@@ -597,7 +1265,6 @@ template <int ES>
 sv_status launch_topset(const RowSet &drf, long long rid0, int B, int rows_used, int V, const float *temperature,
                         int F, float C, const WarpPartial *part, int n_split, const NucleusCut *nuc, TopSet *top,
                         sv_stats *stats, const DeviceInfo &di, cudaStream_t stream) {
-    (void)stats;
     (void)di;
     TopSetArgs a;
     a.rows = drf;
@@ -612,6 +1279,7 @@ sv_status launch_topset(const RowSet &drf, long long rid0, int B, int rows_used,
     a.n_split = n_split;
     a.nuc = nuc;
     a.top = top;
+    a.stats = stats;
     if (a.n_rows < 1) return SV_OK;
     k_topset<ES><<<(unsigned)a.n_rows, kThreads, 0, stream>>>(a);
     return cuda_status(cudaGetLastError());

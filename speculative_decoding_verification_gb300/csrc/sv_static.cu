@@ -43,7 +43,8 @@ sv_status scratch_address(void **out) {
 extern "C" sv_status sv_verify_static(const void *target_logits, int64_t t_row_pitch, const void *draft_logits,
                                       int64_t d_row_pitch, int d_rows_per_seq, sv_dtype dtype,
                                       const int32_t *draft_tokens, const double *uniforms, int B, int K, int V,
-                                      const float *temperature, const float *top_p, int saguaro_F, float saguaro_C,
+                                      const float *temperature, const float *top_p, const int32_t *top_k,
+                                      int saguaro_F, float saguaro_C,
                                       int32_t *accept_len, int32_t *out_tokens, double *debug, sv_stats *stats,
                                       sv_stream_t stream) {
     if (B < 1 || K < 0 || K > SV_MAX_K || V < 1) return SV_ERR_INVALID_ARG;
@@ -55,6 +56,6 @@ extern "C" sv_status sv_verify_static(const void *target_logits, int64_t t_row_p
     const sv_status st = scratch_address(&scratch);
     if (st != SV_OK) return st;
     return sv_verify(target_logits, t_row_pitch, draft_logits, d_row_pitch, d_rows_per_seq, dtype, draft_tokens,
-                     uniforms, B, K, V, temperature, top_p, saguaro_F, saguaro_C, accept_len, out_tokens, debug,
+                     uniforms, B, K, V, temperature, top_p, top_k, saguaro_F, saguaro_C, accept_len, out_tokens, debug,
                      stats, scratch, SV_STATIC_SCRATCH_BYTES, stream);
 }

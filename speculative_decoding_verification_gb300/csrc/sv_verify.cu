@@ -237,8 +237,8 @@ VerifyPlan plan_verify(int B, int K, int V, int es) {
 }
 
 template <int ES>
-static sv_status launch_verify(const VerifyPlan &pl, const AcceptArgs &acc_in, const float *top_p, int F,
-                               float C, int B, void *ws, cudaStream_t stream) {
+static sv_status launch_verify(const VerifyPlan &pl, const AcceptArgs &acc_in, const float *top_p,
+                               const int32_t *top_k, int F, float C, int B, void *ws, cudaStream_t stream) {
     DeviceInfo di;
     if (!device_info(di)) return SV_ERR_CUDA;
     char *w = static_cast<char *>(ws);
@@ -266,14 +266,13 @@ static sv_status launch_verify(const VerifyPlan &pl, const AcceptArgs &acc_in, c
         const sv_status st = launch_stats<ES>(sa, di, stream);
         if (st != SV_OK) return st;
     }
-    // 2. nucleus cuts and top-F sets (only when asked for)
+    // 2. top-k / nucleus cuts and top-F sets (only when asked for)
     NucleusCut *nuc = nullptr;
     TopSet *top = nullptr;
-    if (top_p) {
+    if (top_p || top_k) {
         nuc = reinterpret_cast<NucleusCut *>(w + pl.off_nuc);
         sv_status st = launch_nucleus<ES>(acc.tgt, acc.drf, pl.n_rows0, pl.n_rows1, acc.V, acc.temperature, top_p,
-                                          part, pl.n_split, reinterpret_cast<RowStat *>(w + pl.off_rowstat), nuc,
-                                          acc.stats, di, stream);
+                                          top_k, part, pl.n_split, nuc, acc.stats, stream);
         if (st != SV_OK) return st;
     }
     if (acc.sag_on) {
@@ -362,7 +361,8 @@ extern "C" size_t sv_verify_workspace_size(int B, int K, int V) {
 extern "C" sv_status sv_verify(const void *target_logits, int64_t t_row_pitch, const void *draft_logits,
                                int64_t d_row_pitch, int d_rows_per_seq, sv_dtype dtype, const int32_t *draft_tokens,
                                const double *uniforms, int B, int K, int V, const float *temperature,
-                               const float *top_p, int saguaro_F, float saguaro_C, int32_t *accept_len,
+                               const float *top_p, const int32_t *top_k, int saguaro_F, float saguaro_C,
+                               int32_t *accept_len,
                                int32_t *out_tokens, double *debug, sv_stats *stats, void *workspace,
                                size_t workspace_bytes, sv_stream_t stream_) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -394,6 +394,6 @@ extern "C" sv_status sv_verify(const void *target_logits, int64_t t_row_pitch, c
     acc.out_tokens = out_tokens;
     acc.debug = debug;
     acc.stats = stats;
-    if (es == 4) return launch_verify<4>(pl, acc, top_p, saguaro_F, saguaro_C, B, workspace, stream);
-    return launch_verify<2>(pl, acc, top_p, saguaro_F, saguaro_C, B, workspace, stream);
+    if (es == 4) return launch_verify<4>(pl, acc, top_p, top_k, saguaro_F, saguaro_C, B, workspace, stream);
+    return launch_verify<2>(pl, acc, top_p, top_k, saguaro_F, saguaro_C, B, workspace, stream);
 }

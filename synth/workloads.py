@@ -51,6 +51,7 @@ class Workload:
     accept_rate: float = 0.0
     power_r: float = 0.0
     kappa: int = 0               # Mirror-style: root candidates
+    top_k: int = 0               # top-k filter (0: off)
     extra: dict = field(default_factory=dict)
 
     @property
@@ -85,6 +86,12 @@ LARGE_BATCH = Workload("large-batch B=512 K=5 V=128256 bf16 half-greedy", B=512,
                        draft_scale=0.7, draft_sigma=1.5, zipf_bias=True, greedy_even_rows=True)
 
 CONFIGS = {1: PLAIN, 2: SAMPLED_TOPP, 3: SAGUARO, 4: MIRROR, 5: LARGE_BATCH}
+
+# The sampled recipe with a top-k filter ahead of top-p (k = 50 is a common sampler setting;
+# the pages name top-k without a value).
+SAMPLED_TOPK = Workload("sampled-sd-topk B=8 K=5 V=128256 bf16 T=0.8 top-k=50 top-p=0.9", B=8, K=5, V=128256,
+                        dtype="bf16", temperature=0.8, top_p=0.9, rounds=200, seed=5, sigma=3.0,
+                        draft_scale=0.7, draft_sigma=1.5, zipf_bias=True, top_k=50)
 
 
 def scaled(w: Workload, **kw) -> Workload:
@@ -138,6 +145,10 @@ def temperatures(w: Workload) -> np.ndarray:
 
 def top_ps(w: Workload) -> np.ndarray:
     return np.full(w.B, w.top_p, dtype=np.float32)
+
+
+def top_ks(w: Workload) -> np.ndarray:
+    return np.full(w.B, w.top_k, dtype=np.int32)
 
 
 def round_uniforms(w: Workload, round_idx: int = 0):

@@ -23,14 +23,17 @@ def make_inputs(w: W.Workload, round_idx: int = 0, device="cuda", chunk: int = 3
     u_draft, u_ver, u_branch = W.round_uniforms(w, round_idx)
     T = W.temperatures(w)
     tp = W.top_ps(w)
+    tk = W.top_ks(w)
     K = w.K
     toks = np.zeros((w.B, K), dtype=np.int64)
     for b0 in range(0, w.B, chunk):
         b1 = min(w.B, b0 + chunk)
         d64 = to_f64(drf[b0:b1, :K])
-        r = oracle.draft_sample(d64, u_draft[b0:b1, :K], T[b0:b1], tp[b0:b1], w.saguaro_F, w.saguaro_C)
+        r = oracle.draft_sample(d64, u_draft[b0:b1, :K], T[b0:b1], tp[b0:b1], w.saguaro_F, w.saguaro_C,
+                                top_k=tk[b0:b1])
         toks[b0:b1] = r["tokens"]
-    return dict(target=tgt, draft=drf, tokens=toks, u_draft=u_draft, u=u_ver, u_branch=u_branch, T=T, top_p=tp)
+    return dict(target=tgt, draft=drf, tokens=toks, u_draft=u_draft, u=u_ver, u_branch=u_branch, T=T, top_p=tp,
+                top_k=tk)
 
 
 def oracle_verify(inp, w: W.Workload, seqs=None, chunk: int = 16, F=None, C=None):
@@ -45,7 +48,9 @@ def oracle_verify(inp, w: W.Workload, seqs=None, chunk: int = 16, F=None, C=None
         tsel = torch.as_tensor(sel, device=inp["target"].device)
         t64 = to_f64(inp["target"].index_select(0, tsel))
         d64 = to_f64(inp["draft"].index_select(0, tsel)[:, : w.K])
-        parts.append(oracle.verify(t64, d64, inp["tokens"][sel], inp["u"][sel], inp["T"][sel], inp["top_p"][sel], F, C))
+        tk = inp["top_k"][sel] if "top_k" in inp else None
+        parts.append(oracle.verify(t64, d64, inp["tokens"][sel], inp["u"][sel], inp["T"][sel], inp["top_p"][sel], F, C,
+                                   top_k=tk))
     return {k: np.concatenate([p[k] for p in parts]) for k in parts[0]}
 
 

@@ -77,7 +77,7 @@ def test_verify_rejects_bad_arguments_before_launch(lib):
                     top_p=None, F=0, C=1.0, al=fake, ot=fake, dbg=None, st=None, ws=fake, wsb=ws)
         kw = {**args, **kw}
         return lib.sv_verify(kw["t"], kw["tp"], kw["d"], kw["dp"], kw["dr"], kw["dtype"], kw["tok"], kw["u"], kw["B"],
-                             kw["K"], kw["V"], kw["T"], kw["top_p"], kw["F"], kw["C"], kw["al"], kw["ot"], kw["dbg"],
+                             kw["K"], kw["V"], kw["T"], kw["top_p"], None, kw["F"], kw["C"], kw["al"], kw["ot"], kw["dbg"],
                              kw["st"], kw["ws"], kw["wsb"], None)
     assert call(B=0) == 1
     assert call(K=33) == 1

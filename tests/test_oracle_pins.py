@@ -155,6 +155,23 @@ def test_top_k_invariants_on_plateau_rows():
     np.testing.assert_array_equal(d1, g)
 
 
+def test_saguaro_under_top_k_hand_example():
+    """sigma_{F,C} acts on the filtered draft distribution.  Top-2 of (0.1, 0.4, 0.2, 0.2, 0.1)
+    keeps {1, 2} at (2/3, 1/3).  With F=1, C=0.5 the top token is halved: (1/3, 1/3) / (2/3) =
+    (1/2, 1/2).  With F=3, C=0 every kept token is scaled to zero: the transform is undefined and
+    the filtered row is sampled unchanged."""
+    x = np.log(np.array([[[0.1, 0.4, 0.2, 0.2, 0.1]]]))
+    one, tk = np.ones(1), np.array([2])
+    for u, want in [(0.0, 1), (0.49, 1), (0.51, 2), (0.99, 2)]:
+        r = oracle.draft_sample(x, np.array([[u]]), one, one, 1, 0.5, top_k=tk)
+        assert r["tokens"][0, 0] == want
+        assert r["p_top"][0, 0] == pytest.approx(2 / 3, abs=1e-15)
+        assert r["z_prime"][0, 0] == pytest.approx(2 / 3, abs=1e-15)
+    for u, want in [(0.0, 1), (0.66, 1), (0.67, 2), (0.99, 2)]:
+        r = oracle.draft_sample(x, np.array([[u]]), one, one, 3, 0.0, top_k=tk)
+        assert r["tokens"][0, 0] == want and r["z_prime"][0, 0] == 1.0
+
+
 def test_inverse_cdf_hand_example():
     w = np.array([0.1, 0.0, 0.3, 0.6])
     for u, want in [(0.0, 0), (0.0999, 0), (0.1, 2), (0.3999, 2), (0.4, 3), (0.999, 3)]:

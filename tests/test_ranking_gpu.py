@@ -1,5 +1,5 @@
 """GPU parity of the ranking-based paths against the float64 oracle (through the C ABI):
-nucleus (top-p) verification, the Saguaro transform in verification and in draft sampling,
+nucleus (top-p) and top-k verification, the Saguaro transform in verification and in draft sampling,
 cache keys and lookup, top-kappa roots and Mirror-style branch reuse."""
 import numpy as np
 import pytest
@@ -62,6 +62,91 @@ def test_top_p_with_plateaus():
 
 
 # --------------------------------------------------------------------------------------
+# top-k verification, alone and ahead of top-p
+# --------------------------------------------------------------------------------------
+@pytest.mark.parametrize("round_idx,top_p", [(0, 1.0), (1, 1.0), (0, 0.9), (1, 0.9)])
+def test_top_k_verify_parity(round_idx, top_p):
+    w = W.scaled(W.SAMPLED_TOPK, top_p=top_p)
+    inp = make_inputs(w, round_idx)
+    ref = oracle_verify(inp, w)
+    al, ot, dbg, st = run_gpu(inp, w, top_p=top_p < 1, top_k=True)
+    compare(w, inp, ref, al, ot, dbg, st)
+    np.testing.assert_allclose(dbg[:, :, 5], ref["mass_q"], atol=1e-6)
+    np.testing.assert_allclose(dbg[:, : w.K, 6], ref["mass_p"], atol=1e-6)
+    assert st["unresolved"] == 0, st
+
+
+@pytest.mark.parametrize("k,tp", [(1, 1.0), (2, 1.0), (50, 1.0), (3999, 1.0), (4000, 1.0), (0, 1.0), (-3, 1.0),
+                                  (1, 0.5), (7, 0.999), (300, 0.5), (300, 1e-6), (3999, 0.9)])
+def test_top_k_values_small_vocab(k, tp):
+    """k = 1 (the argmax), small, V - 1, V and <= 0 (off); with top-p close to 1, middling and
+    tiny, where the nucleus of the top-k set may be the whole set or its first token."""
+    w = W.scaled(W.SAMPLED_TOPK, B=32, V=4000, top_p=tp, top_k=k)
+    inp = make_inputs(w, 3)
+    ref = oracle_verify(inp, w)
+    al, ot, dbg, st = run_gpu(inp, w, top_p=tp < 1, top_k=True)
+    compare(w, inp, ref, al, ot, dbg, st)
+    np.testing.assert_allclose(dbg[:, :, 5], ref["mass_q"], atol=1e-6)
+    np.testing.assert_allclose(dbg[:, : w.K, 6], ref["mass_p"], atol=1e-6)
+    assert st["unresolved"] == 0, st
+
+
+@pytest.mark.parametrize("k,tp", [(5, 1.0), (37, 1.0), (37, 0.6), (200, 1.0), (200, 0.95)])
+def test_top_k_with_plateaus_and_signed_zeros(k, tp):
+    """Equal logits straddling the k-th place keep the lowest ids; -0 and +0 are one value."""
+    rng = np.random.default_rng(6)
+    B, K, V = 16, 3, 512
+    base = np.round(rng.normal(0, 1, (B, K + 1, V)) * 2) / 2       # many ties (step 0.5)
+    base[rng.random(base.shape) < 0.15] = 0.0
+    neg0 = rng.random(base.shape) < 0.5
+    base = np.where((base == 0.0) & neg0, -0.0, base)
+    dr_np = np.round(0.7 * base[:, :K] * 2) / 2
+    dr_np = np.where(dr_np == 0.0, np.where(neg0[:, :K], -0.0, 0.0), dr_np)
+    tg = torch.as_tensor(base, dtype=torch.bfloat16, device="cuda")
+    dr = torch.as_tensor(dr_np, dtype=torch.bfloat16, device="cuda")
+    assert (torch.signbit(tg) & (tg == 0)).any() and ((~torch.signbit(tg)) & (tg == 0)).any()
+    T = np.ones(B, np.float32)
+    T[1] = 0.0
+    tpa = np.full(B, tp, np.float32)
+    tka = np.full(B, k, np.int32)
+    d64 = to_f64(dr)
+    toks = oracle.draft_sample(d64, rng.random((B, K)), T, tpa, top_k=tka)["tokens"]
+    u = rng.random((B, K + 1))
+    w = W.Workload("plateau", B=B, K=K, V=V, dtype="bf16", temperature=1.0, top_p=tp, rounds=1, seed=0, sigma=1,
+                   draft_scale=0.7, draft_sigma=1, top_k=k)
+    inp = dict(target=tg, draft=dr, tokens=toks, u=u, T=T, top_p=tpa, top_k=tka)
+    ref = oracle.verify(to_f64(tg), d64, toks, u, T, tpa, top_k=tka)
+    al, ot, dbg, st = run_gpu(inp, w, top_p=tp < 1, top_k=True)
+    compare(w, inp, ref, al, ot, dbg, st)
+    np.testing.assert_allclose(dbg[:, :, 5], ref["mass_q"], atol=1e-6)
+
+
+def test_top_k_on_the_lazy_and_static_entry_points():
+    """sv_verify_lazy runs the full pipeline under a filter, sv_verify_static passes top_k on:
+    both equal sv_verify."""
+    w = W.scaled(W.SAMPLED_TOPK, B=6, V=20000)
+    inp = make_inputs(w, 0)
+    a = gpu_args(inp)
+    tp = torch.as_tensor(inp["top_p"], device="cuda")
+    tk = torch.as_tensor(inp["top_k"], device="cuda")
+    outs = []
+    for mode in ("eager", "lazy", "static"):
+        if mode == "static":
+            al, ot, _, st = sv.sv_verify_static(inp["target"], inp["draft"], a["draft_tokens"], a["uniforms"],
+                                                a["temperature"], top_p=tp, top_k=tk)
+        else:
+            al, ot, _, st = sv.sv_verify(inp["target"], inp["draft"], a["draft_tokens"], a["uniforms"],
+                                         a["temperature"], top_p=tp, top_k=tk, lazy=mode == "lazy")
+        torch.cuda.synchronize()
+        assert sv.read_stats(st)["status"] == 0
+        outs.append((al.cpu().numpy(), ot.cpu().numpy()))
+    ref = oracle_verify(inp, w)
+    for al, ot in outs:
+        np.testing.assert_array_equal(al, ref["accept_len"])
+        np.testing.assert_array_equal(ot, ref["out_tokens"])
+
+
+# --------------------------------------------------------------------------------------
 # Saguaro: verification with p' and the draft sampler
 # --------------------------------------------------------------------------------------
 @pytest.mark.parametrize("F,C", [(8, 0.3), (8, 0.0), (1, 0.5), (300, 0.1)])
@@ -73,8 +158,10 @@ def test_saguaro_verify_parity(F, C):
     compare(w, inp, ref, al, ot, dbg, st)
 
 
-@pytest.mark.parametrize("F,C,top_p", [(0, 1.0, None), (8, 0.3, None), (8, 0.0, None), (8, 0.3, 0.9)])
-def test_saguaro_sample_parity(F, C, top_p):
+@pytest.mark.parametrize("F,C,top_p,top_k", [(0, 1.0, None, None), (8, 0.3, None, None), (8, 0.0, None, None),
+                                             (8, 0.3, 0.9, None), (0, 1.0, None, 20), (8, 0.3, 0.9, 20),
+                                             (8, 0.0, None, 5)])
+def test_saguaro_sample_parity(F, C, top_p, top_k):
     w = W.scaled(W.SAGUARO, B=16)
     tgt, drf = W.logits(w, 1, device="cuda")
     u_draft, _, _ = W.round_uniforms(w, 1)
@@ -82,14 +169,14 @@ def test_saguaro_sample_parity(F, C, top_p):
     T[3] = 0.0                    # one greedy row
     T[5] = 0.7
     tp = np.full(w.B, top_p if top_p else 1.0, np.float32)
-    R = w.K + 1
+    tk = np.full(w.B, top_k if top_k else 0, np.int32)
     toks, dbg, st = sv.sv_saguaro_sample(drf, torch.as_tensor(u_draft, device="cuda"), torch.as_tensor(T, device="cuda"),
                                          top_p=torch.as_tensor(tp, device="cuda") if top_p else None, F=F, C=C,
-                                         debug=True)
+                                         debug=True, top_k=torch.as_tensor(tk, device="cuda") if top_k else None)
     torch.cuda.synchronize()
     s = sv.read_stats(st)
     assert s["status"] == 0, s
-    ref = oracle.draft_sample(to_f64(drf), u_draft, T, tp, F, C)
+    ref = oracle.draft_sample(to_f64(drf), u_draft, T, tp, F, C, top_k=tk)
     np.testing.assert_array_equal(toks.cpu().numpy(), ref["tokens"])
     d = dbg.cpu().numpy()
     sampled = T > 0

@@ -16,13 +16,14 @@ pytestmark = pytest.mark.gpu
 TOL = 1e-6
 
 
-def run_gpu(inp, w, top_p=False, F=None, C=None):
+def run_gpu(inp, w, top_p=False, F=None, C=None, top_k=False):
     F = w.saguaro_F if F is None else F
     C = w.saguaro_C if C is None else C
     a = gpu_args(inp)
     tp = torch.as_tensor(inp["top_p"], dtype=torch.float32, device="cuda") if top_p else None
+    tk = torch.as_tensor(inp["top_k"], dtype=torch.int32, device="cuda") if top_k else None
     al, ot, dbg, st = sv.sv_verify(inp["target"], inp["draft"], a["draft_tokens"], a["uniforms"], a["temperature"],
-                                   top_p=tp, saguaro_F=F, saguaro_C=C, debug=True)
+                                   top_p=tp, saguaro_F=F, saguaro_C=C, debug=True, top_k=tk)
     torch.cuda.synchronize()
     return al.cpu().numpy(), ot.cpu().numpy(), dbg.cpu().numpy(), sv.read_stats(st)
 

@@ -31,11 +31,11 @@ def test_oversize_call_is_refused_before_device_work():
     fake = 1 << 20
     B, K, V = 1024, 5, 128256
     assert lib.sv_verify_workspace_size(B, K, V) > _abi.SV_STATIC_SCRATCH_BYTES
-    code = lib.sv_verify_static(fake, V, fake, V, K, _abi.SV_BF16, fake, fake, B, K, V, fake, None, 0, 1.0, fake,
-                                fake, None, None, None)
+    code = lib.sv_verify_static(fake, V, fake, V, K, _abi.SV_BF16, fake, fake, B, K, V, fake, None, None, 0, 1.0,
+                                fake, fake, None, None, None)
     assert code == _abi.SV_ERR_WORKSPACE
-    assert lib.sv_verify_static(fake, V, fake, V, K, 7, fake, fake, 4, K, V, fake, None, 0, 1.0, fake, fake, None,
-                                None, None) == _abi.SV_ERR_INVALID_ARG
+    assert lib.sv_verify_static(fake, V, fake, V, K, 7, fake, fake, 4, K, V, fake, None, None, 0, 1.0, fake, fake,
+                                None, None, None) == _abi.SV_ERR_INVALID_ARG
 
 
 def _outputs(B, K, dev):

@@ -16,6 +16,8 @@ Sources (cited by page title and section):
     §1 notation (q target, p draft), §3 modified rejection sampling, §6 checks.
   * "Mirror Speculative Decoding" notes (Mirror-SD notes): §2 greedy verify, §3.1 top-kappa
     early-exit roots, §3.2 verification vs. reuse.
+  * "3-Model Speculative Decoding (PyramidSD)" notes (PyramidSD notes): "Method", the fuzzy
+    (divergence-threshold) and assisted acceptance of one verification stage.
 
 Every function works in float64 on logits already converted exactly to float64
 (bf16 -> f64 and f32 -> f64 are exact).  Ties in any ranking go to the lowest token id.
@@ -25,3 +27,4 @@ from .dist import (argmax_first, softmax_t, nucleus, saguaro_transform, row_dist
 from .verify import verify, draft_sample  # noqa: F401
 from .saguaro import fanout, cache_keys, cache_lookup  # noqa: F401
 from .mirror import topk_rows, mirror_reuse  # noqa: F401
+from .fuzzy import jensen_shannon, fuzzy_verify  # noqa: F401

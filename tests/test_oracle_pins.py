@@ -494,3 +494,104 @@ def test_topk_rows_and_reuse_hand_example():
     assert oracle.mirror_reuse(br, [1], np.array([[5, 2, -1, -1]]))[0] == 0
     assert oracle.mirror_reuse(br, [0], np.array([[3, -1, -1, -1]]))[0] == 1
     assert oracle.mirror_reuse(br, [3], np.array([[5, 6, 7, 1]]))[0] == 0    # k = gamma
+
+
+# --------------------------------------------------------------------------------------
+# PyramidSD stage verification: Jensen-Shannon divergence, fuzzy and assisted acceptance
+# --------------------------------------------------------------------------------------
+def test_jensen_shannon_matches_scipy():
+    """The divergence against scipy's Jensen-Shannon distance (squared, base 2), including
+    distributions with zeros; identities: 0 on equal inputs, 1 on disjoint supports, symmetry."""
+    import scipy.spatial.distance as ssd
+    rng = np.random.default_rng(30)
+    for V in (2, 7, 300):
+        for _ in range(20):
+            q = rng.random(V) ** 3
+            p = rng.random(V) ** 3
+            q[rng.random(V) < 0.2] = 0.0
+            p[rng.random(V) < 0.2] = 0.0
+            q[0] += 1e-3
+            p[-1] += 1e-3
+            q /= q.sum()
+            p /= p.sum()
+            want = ssd.jensenshannon(q, p, base=2) ** 2
+            assert oracle.jensen_shannon(q, p) == pytest.approx(want, rel=1e-12, abs=1e-15)
+            assert oracle.jensen_shannon(p, q) == pytest.approx(oracle.jensen_shannon(q, p), abs=1e-15)
+            assert oracle.jensen_shannon(q, q) == pytest.approx(0.0, abs=1e-15)
+    assert oracle.jensen_shannon([1.0, 0.0, 0.0], [0.0, 0.5, 0.5]) == pytest.approx(1.0, abs=1e-15)
+
+
+def test_fuzzy_verify_hand_example():
+    """Position 1: verifier and drafter agree (Div 0); position 2: disjoint one-token rows
+    (Div 1).  tau = 0.5 accepts position 1 only, and position 2 takes the verifier's token."""
+    ninf = -np.inf
+    ver = np.array([[[0.0, 0.0, ninf], [ninf, 0.0, ninf], [0.0, ninf, ninf]]])
+    drf = np.array([[[0.0, 0.0, ninf], [0.0, ninf, ninf]]])
+    toks = np.array([[1, 0]])
+    u = np.array([[0.9, 0.9, 0.3]])
+    r = oracle.fuzzy_verify(ver, drf, toks, u, np.ones(1), 0.5)
+    np.testing.assert_allclose(r["div"], [[0.0, 1.0]], atol=1e-15)
+    assert r["accept_len"][0] == 1 and list(r["out_tokens"][0]) == [1, 1, -1]
+    r = oracle.fuzzy_verify(ver, drf, toks, u, np.ones(1), 1.0)        # everything passes: bonus from row 3
+    assert r["accept_len"][0] == 2 and list(r["out_tokens"][0]) == [1, 0, 0]
+    r = oracle.fuzzy_verify(ver, drf, toks, u, np.ones(1), -0.1)       # nothing passes: draw from row 1
+    assert r["accept_len"][0] == 0 and r["out_tokens"][0, 0] == 0       # u = 0.3 < 1/2 -> id 0
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_fuzzy_first_token_law(seed):
+    """Exact outcome law (bisection on the uniforms): when Div <= tau the first committed token
+    follows the drafter's distribution p (its token is kept whatever it is); otherwise it
+    follows the verifier's q."""
+    import functools
+    rng = np.random.default_rng(50 + seed)
+    ver = rng.normal(0, 1.5, size=(2, 4))
+    drf = 0.5 * ver[:1] + rng.normal(0, 1.0, size=(1, 4))
+    q, p = softmax(ver), softmax(drf)
+    d = oracle.jensen_shannon(q[0], p[0])
+    for tau, want in ((d + 1e-9, p[0]), (d - 1e-9, q[0])):
+        fv = functools.partial(_fuzzy_as_verify, tau=tau, mode="divergence")
+        law = outcome_law(fv, ver, drf, p)
+        joint, _ = position_marginals(law, 1, 4)
+        np.testing.assert_allclose(joint[0], want, atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_assisted_first_token_law(seed):
+    """Assisted acceptance: accepting gives min(p, q); a rejection (probability 1 - sum min(p, q))
+    draws from q itself, so the first token's law is min(p, q) + (1 - alpha) q (not q)."""
+    import functools
+    rng = np.random.default_rng(60 + seed)
+    ver = rng.normal(0, 1.5, size=(2, 5))
+    drf = rng.normal(0, 1.5, size=(1, 5))
+    q, p = softmax(ver), softmax(drf)
+    alpha = np.minimum(p[0], q[0]).sum()
+    fv = functools.partial(_fuzzy_as_verify, tau=0.0, mode="assisted")
+    law = outcome_law(fv, ver, drf, p)
+    joint, _ = position_marginals(law, 1, 5)
+    np.testing.assert_allclose(joint[0], np.minimum(p[0], q[0]) + (1.0 - alpha) * q[0], atol=1e-12)
+
+
+def test_fuzzy_greedy_rows():
+    """Temperature 0: assisted acceptance is greedy verification; the divergence of one-hot rows is
+    0 or 1, so any tau in [0, 1) accepts exactly where the two argmaxes agree."""
+    rng = np.random.default_rng(70)
+    B, K, V = 40, 4, 9
+    ver = np.round(rng.normal(0, 1, (B, K + 1, V)) * 2) / 2
+    drf = np.where(rng.random((B, K, V)) < 0.5, ver[:, :K], np.round(rng.normal(0, 1, (B, K, V)) * 2) / 2)
+    toks = np.argmax(drf, axis=-1)
+    u = rng.random((B, K + 1))
+    T = np.zeros(B)
+    a = oracle.fuzzy_verify(ver, drf, toks, u, T, 0.0, mode="assisted")
+    g = oracle.verify(ver, drf, toks, u, T, np.ones(B))
+    np.testing.assert_array_equal(a["out_tokens"], g["out_tokens"])
+    f = oracle.fuzzy_verify(ver, drf, toks, u, T, 0.5)
+    agree = np.argmax(ver[:, :K], axis=-1) == np.argmax(drf, axis=-1)
+    np.testing.assert_array_equal(f["div"], np.where(agree, 0.0, 1.0))
+    np.testing.assert_array_equal(f["accept_len"], np.sum(np.cumprod(agree, axis=1), axis=1))
+    np.testing.assert_array_equal(f["out_tokens"], g["out_tokens"])   # tokens = argmax where they agree
+
+
+def _fuzzy_as_verify(target, draft, tokens, u, T, top_p, F, C, tau, mode):
+    """fuzzy_verify under the calling convention of tests.exact_law."""
+    return oracle.fuzzy_verify(target, draft, tokens, u, T, tau, mode=mode)

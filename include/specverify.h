@@ -227,6 +227,46 @@ sv_status sv_verify_static(const void *target_logits, int64_t t_row_pitch,
                            double *debug, sv_stats *stats, sv_stream_t stream);
 
 /* ----------------------------------------------------------------------------------------
+ * sv_fuzzy_verify — one verification stage of three-model speculative decoding: a verifier
+ * (the qualifier checking the draft model, or the target checking the qualifier) accepts a
+ * drafter's tokens position by position.
+ * [PyramidSD notes, "Method": fuzzy acceptance Div(P_verifier, P_drafter) <= tau (PSDF) and
+ *  assisted acceptance (PSDA); SpS notes §3 for the test the assisted mode keeps]
+ *
+ *  mode SV_ACCEPT_DIVERGENCE  position i+1 passes while the Jensen-Shannon divergence (bits,
+ *                  in [0, 1]) of the verifier's and the drafter's distributions at that
+ *                  position is <= tau, whatever the drafted token; uniforms[b][i < K] unused.
+ *  mode SV_ACCEPT_ASSISTED    position i+1 passes iff u[b][i] < min(1, q(s)/p(s)) (greedy: s ==
+ *                  argmax q), as in sv_verify; tau unused.
+ *  In both modes the first failing position takes a token drawn from the verifier's
+ *  distribution there (inverse CDF in id order at u[b][K]; greedy: its argmax), and when all K
+ *  pass the verifier's row K+1 gives the bonus token.  The divergence is certified: a value
+ *  the float32 bound cannot place on one side of tau is recomputed in float-float.
+ *
+ *  verifier_logits  dev, rows (b, j), j = 0..K, pitch v_row_pitch (as sv_verify's target).
+ *  drafter_logits   dev, rows (b, j) at b*d_rows_per_seq+j, j < K.  Read for every sequence.
+ *  temperature      dev float [B]: 0 greedy (one-hot rows: Div is 0 or 1), else [1e-3, 1e3].
+ *  divergence       dev float64 [B][K] or NULL (must be NULL in the assisted mode): Div of every
+ *                   position (certified to the float32 bound, or float-float where that bound
+ *                   could not place it on one side of tau).
+ *  accept_len, out_tokens, stats, workspace as sv_verify (workspace: sv_fuzzy_verify_workspace_size).
+ * Returns SV_ERR_INVALID_ARG for a bad mode, a non-finite tau, or the conditions of sv_verify.
+ * -------------------------------------------------------------------------------------- */
+typedef enum { SV_ACCEPT_DIVERGENCE = 0, SV_ACCEPT_ASSISTED = 1 } sv_accept_mode;
+
+size_t sv_fuzzy_verify_workspace_size(int B, int K, int V);
+
+sv_status sv_fuzzy_verify(const void *verifier_logits, int64_t v_row_pitch,
+                          const void *drafter_logits, int64_t d_row_pitch, int d_rows_per_seq,
+                          sv_dtype dtype,
+                          const int32_t *draft_tokens, const double *uniforms,
+                          int B, int K, int V,
+                          const float *temperature, float tau, int mode,
+                          int32_t *accept_len, int32_t *out_tokens,
+                          double *divergence, sv_stats *stats,
+                          void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
  * sv_saguaro_sample — draw one token from each of the first n_rows rows of every sequence's
  * draft distribution p' = sigma_{F,C}(p): p after temperature, top-k and top-p, the top-F tokens
  * (ranked by draft logit) scaled by C, renormalised.  F = 0 or C = 1 is a plain draft sampler.

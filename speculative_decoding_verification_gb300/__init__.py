@@ -179,6 +179,45 @@ def sv_verify_static(target, draft, draft_tokens, uniforms, temperature, top_p=N
     return accept_len, out_tokens, debug, stats
 
 
+def sv_fuzzy_verify(verifier, drafter, draft_tokens, uniforms, temperature, tau=0.5, mode="divergence",
+                    divergence=False, accept_len=None, out_tokens=None, stats=None, workspace=None, stream=None):
+    """sv_fuzzy_verify: one stage of three-model speculative decoding on torch CUDA tensors.
+
+    verifier [B, K+1, V] and drafter [B, R>=K, V] logits (same dtype); draft_tokens int32 [B, K];
+    uniforms float64 [B, K+1]; temperature float32 [B]; mode "divergence" (accept while the
+    Jensen-Shannon divergence <= tau) or "assisted".  Returns (accept_len, out_tokens,
+    divergence float64 [B, K] or None, stats).
+    """
+    lib = load()
+    B, K1, V = verifier.shape
+    K = K1 - 1
+    dev = verifier.device
+    v_pitch, _ = _rows(verifier, "verifier")
+    if K > 0:
+        if drafter.dtype != verifier.dtype:
+            raise TypeError("verifier and drafter logits must share a dtype")
+        d_pitch, d_rows = _rows(drafter, "drafter")
+        d_ptr = _ptr(drafter)
+    else:
+        d_pitch, d_rows, d_ptr = v_pitch, 1, ctypes.c_void_p(0)
+    code_mode = {"divergence": _abi.SV_ACCEPT_DIVERGENCE, "assisted": _abi.SV_ACCEPT_ASSISTED}[mode]
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    div = torch.full((B, max(K, 1)), float("nan"), dtype=torch.float64, device=dev) if divergence else None
+    if stats is None:
+        stats = new_stats(dev)
+    ws_bytes = lib.sv_fuzzy_verify_workspace_size(B, K, V)
+    ws = (workspace or _default_ws).get(ws_bytes, dev)
+    code = lib.sv_fuzzy_verify(_ptr(verifier), v_pitch, d_ptr, d_pitch, d_rows, _dtype_code(verifier),
+                               _ptr(draft_tokens if K > 0 else None), _ptr(uniforms), B, K, V, _ptr(temperature),
+                               float(tau), code_mode, _ptr(accept_len), _ptr(out_tokens), _ptr(div), _ptr(stats),
+                               _ptr(ws), ws.numel(), _stream(stream))
+    _abi.check("sv_fuzzy_verify", code)
+    return accept_len, out_tokens, (div[:, :K] if div is not None else None), stats
+
+
 def sv_saguaro_sample(draft, uniforms, temperature, top_p=None, F=0, C=1.0, n_rows=None, tokens=None, debug=False,
                       stats=None, workspace=None, stream=None, top_k=None):
     """sv_saguaro_sample: one token per row j < n_rows of each sequence of draft [B, R, V].

@@ -17,7 +17,8 @@ SV_OK, SV_ERR_INVALID_ARG, SV_ERR_CUDA, SV_ERR_NONFINITE, SV_ERR_TIMEOUT, SV_ERR
 SV_F32, SV_BF16 = 0, 1
 SV_DEBUG_FIELDS = 8
 SV_MAX_K = 32
-SV_STATIC_SCRATCH_BYTES = 32 << 20   # scratch array behind sv_verify_static
+SV_STATIC_SCRATCH_BYTES = 32 << 20
+SV_ACCEPT_DIVERGENCE, SV_ACCEPT_ASSISTED = 0, 1   # sv_accept_mode   # scratch array behind sv_verify_static
 DBG = dict(lse_q=0, lse_p=1, q_s=2, p_s=3, ratio=4, mass_q=5, mass_p=6, R=7)
 
 
@@ -41,6 +42,9 @@ SIGNATURES = {
                                c_vp, c_int, c_f32, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
     "sv_verify_static": (c_int, [c_vp, c_i64, c_vp, c_i64, c_int, c_int, c_vp, c_vp, c_int, c_int, c_int, c_vp,
                                  c_vp, c_vp, c_int, c_f32, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "sv_fuzzy_verify_workspace_size": (c_size, [c_int, c_int, c_int]),
+    "sv_fuzzy_verify": (c_int, [c_vp, c_i64, c_vp, c_i64, c_int, c_int, c_vp, c_vp, c_int, c_int, c_int, c_vp, c_f32,
+                                c_int, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
     "sv_saguaro_sample_workspace_size": (c_size, [c_int, c_int, c_int]),
     "sv_saguaro_sample": (c_int, [c_vp, c_i64, c_int, c_int, c_int, c_int, c_int, c_vp, c_vp, c_vp, c_int, c_f32,
                                   c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),

@@ -33,6 +33,7 @@ struct AcceptArgs {
     ExactItem *exact;
     int *exact_unc;
     Counters *counters;
+    int draw_from_q;        // 1: a rejection draws from q itself, not from (q - p)+
 };
 
 // Draw parameters of one row, float32 only: inv_s = 1 / (S * nucleus mass * Saguaro normaliser).

@@ -80,6 +80,7 @@ struct ExactArgs {
     int n_vec, n_sub, xsplit, max_slots;
     sv_stats *stats;
     long long wait_limit;
+    int draw_from_q;         // 1: a rejection draws from q itself, not from (q - p)+
 };
 
 
@@ -336,10 +337,10 @@ __global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
             sums(k, sa, sk, sd);
             xd.q = seq_row(a, b, k);
             xd.inv_q = (float)(1.0 / sk);
-            xd.has_p = k < K;
+            xd.has_p = k < K && !a.draw_from_q;
             xd.p = xd.q;
             xd.inv_p = 0.f;
-            if (k < K) {
+            if (xd.has_p) {
                 double pa, pk, pd;
                 sums(K + 1 + k, pa, pk, pd);
                 xd.p = seq_row(a, b, K + 1 + k);

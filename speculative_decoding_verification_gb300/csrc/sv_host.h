@@ -56,9 +56,19 @@ struct VerifyPlan {
     int x_split = 1;                       // chunks per row in the float-float pass
     size_t off_lz_units = 0, off_lz_pos = 0;   // lazy verification queue
     long long lz_cap = 0;                  // queue capacity: every (row, chunk) unit once
+    int dv_chunks = 1, dv_words = 1;       // fuzzy verification: chunks per row pair, words per chunk
+    size_t off_dpart = 0, off_ditem = 0, off_dq = 0, off_deferred = 0;
     size_t bytes = 0;
 };
 
 VerifyPlan plan_verify(int B, int K, int V, int es);
+
+// The sv_verify pipeline; draw_from_q = 1 replaces the residual draw after a rejection by a draw
+// from the target row itself (the assisted acceptance of three-model speculative decoding).
+sv_status verify_entry(const void *target_logits, int64_t t_row_pitch, const void *draft_logits, int64_t d_row_pitch,
+                       int d_rows_per_seq, sv_dtype dtype, const int32_t *draft_tokens, const double *uniforms, int B,
+                       int K, int V, const float *temperature, const float *top_p, const int32_t *top_k, int saguaro_F,
+                       float saguaro_C, int draw_from_q, int32_t *accept_len, int32_t *out_tokens, double *debug,
+                       sv_stats *stats, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 }  // namespace sv

@@ -120,6 +120,20 @@ struct DrawItem {
     int k;                  // draw position (accepted count for sv_verify)
 };
 
+// Fuzzy verification: per (pair, chunk) partial of the divergence pass, and per pair its
+// float32 divergence, error bound and (when the bound could not settle it) float-float value.
+struct DivPart {
+    float s_hi, s_lo;       // sum of (q + p) h(d) over the chunk, float-float
+    float y;                // sum of (q + p)(|y_q| + |y_p|) (feeds the error bound)
+    float pad;
+};
+
+struct DivItem {
+    double exact;           // float-float divergence (state 2)
+    int state;              // 0 float32 only, 1 queued for the float-float pass, 2 done
+    int pad;
+};
+
 // Exact-tier work item: a draw to redo (draw >= 0) or a sequence whose accept tests must be
 // redone (draw < 0).
 struct ExactItem {
@@ -138,7 +152,8 @@ struct Counters {
     int q_head;             // lazy verification: next queue position to claim (position 0, then later)
     int q0_tail, q_tail;    // lazy verification: position-0 units / later units queued
     int n_pending;          // lazy verification: sequences not finished yet
-    int pad[7];
+    int n_div_exact;        // fuzzy verification: divergences queued for the float-float pass
+    int pad[6];
 };
 
 inline int div_up(long long a, long long b) { return (int)((a + b - 1) / b); }

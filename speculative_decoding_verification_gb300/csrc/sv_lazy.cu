@@ -673,6 +673,7 @@ static sv_status launch_lazy(const VerifyPlan &pl, const AcceptArgs &acc_in, int
     xa.debug = acc_in.debug;
     xa.sag_C = acc_in.sag_C;
     xa.sag_on = 0;
+    xa.draw_from_q = 0;
     xa.nuc = nullptr;
     xa.top = nullptr;
     xa.rowstat = L.acc.rowstat;

@@ -21,6 +21,7 @@
 #include "sv_host.h"
 #include "sv_select.cuh"
 #include "sv_stats.cuh"
+#include "sv_tiers.cuh"
 
 namespace sv {
 
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
     const long long rid_q = (long long)b * n_t + k;
     const char *qrow = a.tgt.base + ((long long)b * a.tgt.rows_per_seq + k) * a.tgt.pitch_bytes;
     it.q = draw_row(qrow, T, rs[k], a.nuc ? a.nuc + rid_q : nullptr, nullptr, 1.0f);
-    it.has_p = k < K;
+    it.has_p = k < K && !a.draw_from_q;
     if (it.has_p) {
         const long long rid_p = a.n_rows0 + (long long)b * K + k;
         const char *prow = a.drf.base + ((long long)b * a.drf.rows_per_seq + k) * a.drf.pitch_bytes;
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
         it.p.cut_x = -INFINITY;
         it.p.cut_id = 0x7FFFFFFF;
     }
-    it.filt = (a.nuc != nullptr) || (a.sag_on && a.top != nullptr);
+    it.filt = (a.nuc != nullptr) || (it.has_p && a.sag_on && a.top != nullptr);
     it.u = a.uniforms[(size_t)b * (K + 1) + K];
     it.out = outs + k;
     it.dbg_r = a.debug ? a.debug + (size_t)b * (K + 1) * SV_DEBUG_FIELDS + SV_DBG_R : nullptr;
@@ -232,6 +233,16 @@ VerifyPlan plan_verify(int B, int K, int V, int es) {
     p.lz_cap = n_cand * p.n_split;
     p.off_lz_units = cv.take<unsigned long long>((size_t)p.lz_cap);
     p.off_lz_pos = cv.take<int>((size_t)B);
+    const long long n_pairs = (long long)B * K;
+    long long want = n_pairs > 0 ? (2LL * kUnitTarget + n_pairs - 1) / n_pairs : 1;
+    if (want > kMaxSplit) want = kMaxSplit;
+    if (want > p.n_vec) want = p.n_vec > 0 ? p.n_vec : 1;
+    p.dv_chunks = (int)(want < 1 ? 1 : want);
+    p.dv_words = p.n_vec > 0 ? (p.n_vec + p.dv_chunks - 1) / p.dv_chunks : 1;
+    p.off_dpart = cv.take<DivPart>((size_t)(n_pairs > 0 ? n_pairs : 1) * p.dv_chunks);
+    p.off_ditem = cv.take<DivItem>((size_t)(n_pairs > 0 ? n_pairs : 1));
+    p.off_dq = cv.take<int>((size_t)(n_pairs > 0 ? n_pairs : 1));
+    p.off_deferred = cv.take<int>((size_t)B);
     p.bytes = cv.off + 256;
     return p;
 }
@@ -294,58 +305,8 @@ static sv_status launch_verify(const VerifyPlan &pl, const AcceptArgs &acc_in, c
     acc.counters = counters;
     k_accept<ES><<<B, kThreads, 0, stream>>>(acc);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
-    // 4. draws
-    DrawArgs da;
-    da.items = acc.draws;
-    da.counters = counters;
-    da.V = acc.V;
-    da.n_vec = pl.n_vec;
-    da.n_sub = pl.n_sub;
-    da.n_split = pl.d_split;
-    da.subs_per_chunk = pl.d_subs_per_chunk;
-    da.subs = reinterpret_cast<float *>(w + pl.off_subs);
-    da.exact = acc.exact;
-    da.exact_unc = acc.exact_unc;
-    da.stats = acc.stats;
-    da.wait_limit = wait;
-    {
-        const sv_status st = launch_draws<ES>(da, (long long)B, di, stream);
-        if (st != SV_OK) return st;
-    }
-    // 5. float-float tier
-    ExactArgs xa;
-    xa.tgt = acc.tgt;
-    xa.drf = acc.drf;
-    xa.K = acc.K;
-    xa.V = acc.V;
-    xa.temperature = acc.temperature;
-    xa.tokens = acc.tokens;
-    xa.uniforms = acc.uniforms;
-    xa.accept_len = acc.accept_len;
-    xa.out_tokens = acc.out_tokens;
-    xa.debug = acc.debug;
-    xa.sag_C = acc.sag_C;
-    xa.sag_on = acc.sag_on;
-    xa.nuc = nuc;
-    xa.top = top;
-    xa.rowstat = acc.rowstat;
-    xa.n_rows0 = pl.n_rows0;
-    xa.draws = acc.draws;
-    xa.items = acc.exact;
-    xa.counters = counters;
-    xa.xpart = reinterpret_cast<double *>(w + pl.off_xpart);
-    xa.xdraw = reinterpret_cast<ExactDraw *>(w + pl.off_xdraw);
-    xa.xsubs = reinterpret_cast<float4 *>(w + pl.off_xsubs);
-    xa.xnorm = reinterpret_cast<float4 *>(w + pl.off_xnorm);
-    xa.xunc_n = reinterpret_cast<int *>(w + pl.off_xunc_n);
-    xa.xunc = reinterpret_cast<int *>(w + pl.off_xunc);
-    xa.n_vec = pl.n_vec;
-    xa.n_sub = pl.n_sub;
-    xa.xsplit = pl.x_split;
-    xa.max_slots = 2 * acc.K + 1 > 2 ? 2 * acc.K + 1 : 2;
-    xa.stats = acc.stats;
-    xa.wait_limit = wait;
-    return launch_exact<ES>(xa, di, stream);
+    // 4-5. draws and the float-float tier
+    return launch_draw_tiers<ES>(pl, acc, nuc, top, w, B, di, stream);
 }
 
 }  // namespace sv
@@ -358,14 +319,12 @@ extern "C" size_t sv_verify_workspace_size(int B, int K, int V) {
     return a.bytes > b.bytes ? a.bytes : b.bytes;
 }
 
-extern "C" sv_status sv_verify(const void *target_logits, int64_t t_row_pitch, const void *draft_logits,
-                               int64_t d_row_pitch, int d_rows_per_seq, sv_dtype dtype, const int32_t *draft_tokens,
-                               const double *uniforms, int B, int K, int V, const float *temperature,
-                               const float *top_p, const int32_t *top_k, int saguaro_F, float saguaro_C,
-                               int32_t *accept_len,
-                               int32_t *out_tokens, double *debug, sv_stats *stats, void *workspace,
-                               size_t workspace_bytes, sv_stream_t stream_) {
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+sv_status sv::verify_entry(const void *target_logits, int64_t t_row_pitch, const void *draft_logits,
+                           int64_t d_row_pitch, int d_rows_per_seq, sv_dtype dtype, const int32_t *draft_tokens,
+                           const double *uniforms, int B, int K, int V, const float *temperature, const float *top_p,
+                           const int32_t *top_k, int saguaro_F, float saguaro_C, int draw_from_q, int32_t *accept_len,
+                           int32_t *out_tokens, double *debug, sv_stats *stats, void *workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
     if (B < 1 || K < 0 || K > SV_MAX_K || V < 1) return SV_ERR_INVALID_ARG;
     if (!rows_ok(target_logits, t_row_pitch, V, dtype)) return SV_ERR_INVALID_ARG;
     if (K > 0 && (!rows_ok(draft_logits, d_row_pitch, V, dtype) || d_rows_per_seq < K)) return SV_ERR_INVALID_ARG;
@@ -394,6 +353,19 @@ extern "C" sv_status sv_verify(const void *target_logits, int64_t t_row_pitch, c
     acc.out_tokens = out_tokens;
     acc.debug = debug;
     acc.stats = stats;
+    acc.draw_from_q = draw_from_q;
     if (es == 4) return launch_verify<4>(pl, acc, top_p, top_k, saguaro_F, saguaro_C, B, workspace, stream);
     return launch_verify<2>(pl, acc, top_p, top_k, saguaro_F, saguaro_C, B, workspace, stream);
+}
+
+extern "C" sv_status sv_verify(const void *target_logits, int64_t t_row_pitch, const void *draft_logits,
+                               int64_t d_row_pitch, int d_rows_per_seq, sv_dtype dtype, const int32_t *draft_tokens,
+                               const double *uniforms, int B, int K, int V, const float *temperature,
+                               const float *top_p, const int32_t *top_k, int saguaro_F, float saguaro_C,
+                               int32_t *accept_len, int32_t *out_tokens, double *debug, sv_stats *stats,
+                               void *workspace, size_t workspace_bytes, sv_stream_t stream) {
+    return sv::verify_entry(target_logits, t_row_pitch, draft_logits, d_row_pitch, d_rows_per_seq, dtype, draft_tokens,
+                            uniforms, B, K, V, temperature, top_p, top_k, saguaro_F, saguaro_C, 0, accept_len,
+                            out_tokens, debug, stats, workspace, workspace_bytes,
+                            reinterpret_cast<cudaStream_t>(stream));
 }

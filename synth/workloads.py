@@ -20,7 +20,7 @@ import torch
 from . import philox
 
 # Tags for bulk-generator seeds (one per tensor role).
-_TAG_TARGET, _TAG_DRAFT, _TAG_BIAS_IDS, _TAG_BIAS_PERM = 1, 2, 3, 4
+_TAG_TARGET, _TAG_DRAFT, _TAG_BIAS_IDS, _TAG_BIAS_PERM, _TAG_DRAFT_SPREAD = 1, 2, 3, 4, 5
 
 
 @dataclass(frozen=True)
@@ -52,6 +52,7 @@ class Workload:
     power_r: float = 0.0
     kappa: int = 0               # Mirror-style: root candidates
     top_k: int = 0               # top-k filter (0: off)
+    draft_sigma_spread: float = 0.0   # per drafter row, the noise sigma times U[1 - s, 1 + s]
     extra: dict = field(default_factory=dict)
 
     @property
@@ -86,6 +87,22 @@ LARGE_BATCH = Workload("large-batch B=512 K=5 V=128256 bf16 half-greedy", B=512,
                        draft_scale=0.7, draft_sigma=1.5, zipf_bias=True, greedy_even_rows=True)
 
 CONFIGS = {1: PLAIN, 2: SAMPLED_TOPP, 3: SAGUARO, 4: MIRROR, 5: LARGE_BATCH}
+
+# One verification stage of three-model speculative decoding (PyramidSD notes: LLaMA-3 family,
+# V = 128256; the qualifier accumulates l_Q = 25 tokens for the target, the draft model about
+# half as many for the qualifier; tau_T = 0.5, tau_Q = 0.4).  The page runs one stream; a batch
+# of 64 independent streams stands in for a serving batch.  The drafter's logits are a scaled
+# copy of the verifier's plus noise whose scale varies from row to row (x U[0.1, 1.9]), so
+# that confident and uncertain positions mix: about 83% of positions pass tau_T = 0.5 in the
+# qualifier -> target stage and about 75% pass tau_Q = 0.4 in the draft -> qualifier stage.
+PYRAMID_QT = Workload("pyramid qualifier->target B=64 K=25 V=128256 bf16 tau=0.5", B=64, K=25, V=128256,
+                      dtype="bf16", temperature=1.0, top_p=1.0, rounds=50, seed=6, sigma=3.0,
+                      draft_scale=0.8, draft_sigma=1.5, zipf_bias=True, draft_sigma_spread=0.9,
+                      extra={"tau": 0.5})
+PYRAMID_DQ = Workload("pyramid draft->qualifier B=64 K=12 V=128256 bf16 tau=0.4", B=64, K=12, V=128256,
+                      dtype="bf16", temperature=1.0, top_p=1.0, rounds=50, seed=7, sigma=3.0,
+                      draft_scale=0.75, draft_sigma=1.5, zipf_bias=True, draft_sigma_spread=0.9,
+                      extra={"tau": 0.4})
 
 # The sampled recipe with a top-k filter ahead of top-p (k = 50 is a common sampler setting;
 # the pages name top-k without a value).
@@ -132,6 +149,10 @@ def logits(w: Workload, round_idx: int = 0, device="cpu"):
     noise = torch.randn((B, rows_d, V), generator=g_d, device=device, dtype=torch.float32)
     src = tgt[:, :rows_d, :] if rows_d <= rows_t else torch.cat(
         [tgt, tgt[:, -1:, :].expand(B, rows_d - rows_t, V)], dim=1)
+    if w.draft_sigma_spread > 0.0:
+        g_s = _gen(w.seed, 0, round_idx, _TAG_DRAFT_SPREAD, device)
+        f = torch.rand((B, rows_d, 1), generator=g_s, device=device, dtype=torch.float32)
+        noise.mul_(f.mul_(2.0 * w.draft_sigma_spread).add_(1.0 - w.draft_sigma_spread))
     drf = noise.mul_(w.draft_sigma).add_(src, alpha=w.draft_scale)
     return tgt.to(w.torch_dtype), drf.to(w.torch_dtype)
 

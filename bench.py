@@ -266,6 +266,54 @@ def filter_rates(sv, dev, world, n):
     return out
 
 
+def pyramid_rates(sv, dev, world, n, peak):
+    """Rounds/s of one verification stage of three-model speculative decoding (sv_fuzzy_verify):
+    qualifier -> target (B=64, K=25, tau 0.5) and draft -> qualifier (B=64, K=12, tau 0.4), the
+    fuzzy (divergence) mode, and the assisted mode on the first.  Inputs exceed L2 (0.84 GB and
+    0.41 GB): no flush."""
+    import torch
+    from synth import workloads as W
+    out = {}
+    cases = (("qualifier_target", W.PYRAMID_QT, "divergence"), ("draft_qualifier", W.PYRAMID_DQ, "divergence"),
+             ("qualifier_target_assisted", W.PYRAMID_QT, "assisted"))
+    for name, base, mode in cases:
+        w = W.scaled(base, seed=rank_seed(base.seed, int(os.environ.get("RANK", "0"))))
+        ver, drf = W.logits(w, 0, device=dev)
+        u_draft, u, _ = W.round_uniforms(w, 0)
+        T_d = torch.as_tensor(W.temperatures(w), device=dev)
+        u_d = torch.as_tensor(u, device=dev)
+        toks, _, st = sv.sv_saguaro_sample(drf, torch.as_tensor(u_draft[:, :w.K].copy(), device=dev), T_d, n_rows=w.K)
+        ws = sv.Workspace()
+        stats = sv.new_stats(dev)
+        al = torch.empty(w.B, dtype=torch.int32, device=dev)
+        ot = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
+
+        def call():
+            sv.sv_fuzzy_verify(ver, drf, toks, u_d, T_d, tau=w.extra["tau"], mode=mode, accept_len=al,
+                               out_tokens=ot, stats=stats, workspace=ws)
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        start.record()
+        for _ in range(n):
+            call()
+        end.record()
+        torch.cuda.synchronize()
+        st = sv.read_stats(stats)
+        if st["status"] != 0:
+            raise RuntimeError(f"fuzzy verify failed: {st}")
+        ms = max_over_ranks(start.elapsed_time(end) / n, world)
+        rows = w.B * (2 * w.K + 1)
+        byts = rows * w.V * 2
+        out[name] = {"workload": w.name, "mode": mode, "value": whole_job_rate(1.0, world, ms), "unit": "rounds/s",
+                     "ms_per_round": ms, "steps": n, "rows_per_round": rows,
+                     "logit_gbs": byts / (ms * 1e-3) / 1e9, "mean_accept_len": float(al.float().mean().item()),
+                     "reresolved": st["reresolved"], "unresolved": st["unresolved"]}
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import speculative_decoding_verification_gb300 as sv
@@ -363,6 +411,7 @@ def run_ours(args, rank, world, local_rank):
                    "bytes_read_per_round": b_o, "kernel": "k_stats" if lazy else "k_lazy", "kernel_ms": k_o,
                    "kernel_gbs": b_o / (k_o * 1e-3) / 1e9, "frac": b_o / (k_o * 1e-3) / 1e9 / peak}
     line["filters"] = filter_rates(sv, dev, world, min(n, 200))
+    line["pyramid"] = pyramid_rates(sv, dev, world, min(n, 200), peak)
     if args.kernel_only:
         return line if rank == 0 else None
 

@@ -14,8 +14,8 @@ Sources (cited by page title and section):
     Theorem 12 fan-out formula, the Saguaro sampling scheme sigma_{F,C}.
   * "Accelerating LLM Decoding with Speculative Sampling (2023)" notes (SpS notes):
     §1 notation (q target, p draft), §3 modified rejection sampling, §6 checks.
-  * "Mirror Speculative Decoding" notes (Mirror-SD notes): §2 greedy verify, §3.1 top-kappa
-    early-exit roots, §3.2 verification vs. reuse.
+  * "Mirror Speculative Decoding" notes (Mirror-SD notes): §1.1 tree drafts, §2 greedy verify,
+    §3.1 top-kappa early-exit roots and branch-complete trees, §3.2-§3.3 verification vs. reuse.
   * "3-Model Speculative Decoding (PyramidSD)" notes (PyramidSD notes): "Method", the fuzzy
     (divergence-threshold) and assisted acceptance of one verification stage.
 
@@ -28,3 +28,4 @@ from .verify import verify, draft_sample  # noqa: F401
 from .saguaro import fanout, cache_keys, cache_lookup  # noqa: F401
 from .mirror import topk_rows, mirror_reuse  # noqa: F401
 from .fuzzy import jensen_shannon, fuzzy_verify  # noqa: F401
+from .tree import tree_verify, tree_reuse  # noqa: F401

@@ -595,3 +595,130 @@ def test_fuzzy_greedy_rows():
 def _fuzzy_as_verify(target, draft, tokens, u, T, top_p, F, C, tau, mode):
     """fuzzy_verify under the calling convention of tests.exact_law."""
     return oracle.fuzzy_verify(target, draft, tokens, u, T, tau, mode=mode)
+
+
+# --------------------------------------------------------------------------------------
+# Tree verification and tree reuse
+# --------------------------------------------------------------------------------------
+def _bisect_last_true(pred, lo=0.0, hi=None):
+    """Largest u in [0, 1) (as a limit, to ~1e-15) with pred(u) true, given pred monotone
+    (true then false); 0 if pred(0) is false, 1 if pred is true up to 1."""
+    hi = np.nextafter(1.0, 0.0) if hi is None else hi
+    if not pred(0.0):
+        return 0.0
+    if pred(hi):
+        return 1.0
+    a, b = 0.0, hi
+    for _ in range(60):
+        m = 0.5 * (a + b)
+        if pred(m):
+            a = m
+        else:
+            b = m
+    return b
+
+
+def _first_token_law_of_tree(tgt, drf, m, V):
+    """Exact law of the first committed token when the root has m children drafted i.i.d.
+    from the root's draft distribution: the tree rule is treated as a black box of its uniforms."""
+    from itertools import product
+    p = softmax(drf[0])
+    law = np.zeros(V)
+    one = np.nextafter(1.0, 0.0)
+    parents = np.zeros((1, m), dtype=np.int64)
+    for toks in product(range(V), repeat=m):
+        wgt = float(np.prod([p[t] for t in toks]))
+        tt = np.array([toks])
+
+        def run(uvec):
+            r = oracle.tree_verify(tgt[None], drf[None], parents, tt, np.array([uvec]), np.ones(1))
+            return int(r["path"][0, 0]), int(r["out_tokens"][0, 0])
+        reach = 1.0
+        for i in range(1, m + 1):
+            if reach == 0.0:
+                break
+            base = [0.5] + [one] * m
+
+            def accepted(x, i=i, base=base):
+                v = list(base)
+                v[i] = x
+                return run(v)[0] == i
+            r_i = _bisect_last_true(accepted)
+            law[toks[i - 1]] += wgt * reach * r_i
+            reach *= (1.0 - r_i)
+        if reach > 0.0:
+            base = [0.0] + [one] * m
+            lo_u, cur = 0.0, run(base)[1]
+            while True:
+                def same(x, cur=cur):
+                    v = list(base)
+                    v[0] = x
+                    return run(v)[1] == cur
+                if same(one):
+                    law[cur] += wgt * reach * (1.0 - lo_u)
+                    break
+                hi_u = _bisect_last_true(lambda x: same(max(x, lo_u)))
+                law[cur] += wgt * reach * (hi_u - lo_u)
+                lo_u = hi_u
+                v = list(base)
+                v[0] = hi_u
+                cur = run(v)[1]
+    return law
+
+
+@pytest.mark.parametrize("m,V,seed", [(1, 4, 0), (2, 3, 1), (2, 5, 3), (3, 5, 14)])
+def test_tree_root_with_m_children_is_lossless(m, V, seed):
+    """SpS notes §3's rule applied again after each rejection (the residual of the residual):
+    with m children drafted i.i.d. from p, the first committed token follows q exactly.  The
+    draft is made far from the target so that several tokens keep a positive residual after
+    each rejection (otherwise every residual is the same one-hot vector)."""
+    rng = np.random.default_rng(80 + seed)
+    tgt = rng.normal(0, 1.5, size=(m + 1, V))
+    drf = rng.normal(0, 1.5, size=(m + 1, V))
+    q, p = softmax(tgt[0]), softmax(drf[0])
+    assert (q > p).sum() >= (3 if V >= 5 else 1)
+    law = _first_token_law_of_tree(tgt, drf, m, V)
+    np.testing.assert_allclose(law, softmax(tgt[0]), atol=1e-12)
+
+
+def test_tree_chain_is_plain_verification():
+    """A chain (node i below node i-1) is a plain draft of K tokens: the tree rule equals
+    speculative sampling (uniform slots mapped: node i <- position i, the draw <- slot K)."""
+    rng = np.random.default_rng(90)
+    B, K, V = 64, 5, 40
+    tgt = rng.normal(0, 2, size=(B, K + 1, V))
+    drf = 0.7 * tgt + rng.normal(0, 1, size=(B, K + 1, V))
+    toks = oracle.draft_sample(drf[:, :K], rng.random((B, K)), np.ones(B), np.ones(B))["tokens"]
+    u = rng.random((B, K + 1))
+    T = np.where(np.arange(B) % 4 == 0, 0.0, 1.0)
+    ref = oracle.verify(tgt, drf[:, :K], toks, u, T, np.ones(B))
+    parents = np.tile(np.arange(K), (B, 1))
+    ut = np.concatenate([u[:, K:], u[:, :K]], axis=1)
+    got = oracle.tree_verify(tgt, drf, parents, toks, ut, T)
+    np.testing.assert_array_equal(got["accept_len"], ref["accept_len"])
+    np.testing.assert_array_equal(got["out_tokens"], ref["out_tokens"])
+
+
+def test_tree_greedy_hand_example():
+    """Root children 1 (tok 2), 2 (tok 5); node 2 has children 3 (tok 1), 4 (tok 4).  The target
+    argmax is 5 at the root, 4 after node 2 and 0 after node 4: the path is 2 -> 4, then 0."""
+    V = 6
+    tgt = np.full((1, 5, V), -1.0)
+    for row, a in [(0, 5), (2, 4), (4, 0), (1, 3), (3, 3)]:
+        tgt[0, row, a] = 2.0
+    r = oracle.tree_verify(tgt, np.zeros((1, 5, V)), np.array([[0, 0, 2, 2]]), np.array([[2, 5, 1, 4]]),
+                           np.full((1, 5), 0.5), np.zeros(1))
+    assert r["accept_len"][0] == 2 and list(r["path"][0]) == [2, 4, -1, -1]
+    assert list(r["out_tokens"][0]) == [5, 4, 0, -1, -1]
+
+
+def test_tree_reuse_depth2_branching():
+    """Mirror-SD notes §3.3: roots A, B; under A -> F the draft expanded two branches (Z and Q).
+    The committed prefix A, F, Q reuses the tree (ending at Q's node); A, F, X does not."""
+    A, B_, F, Z, Q, X = 10, 11, 12, 13, 14, 15
+    parents = np.array([[0, 0, 1, 3, 3]])          # nodes: 1 A, 2 B, 3 F (under A), 4 Z, 5 Q (under F)
+    tokens = np.array([[A, B_, F, Z, Q]])
+    hit = oracle.tree_reuse(parents, tokens, np.array([2]), np.array([[A, F, Q, -1]]))
+    miss = oracle.tree_reuse(parents, tokens, np.array([2]), np.array([[A, F, X, -1]]))
+    root = oracle.tree_reuse(parents, tokens, np.array([0]), np.array([[B_, -1, -1, -1]]))
+    assert hit[0] == 5 and miss[0] == -1 and root[0] == 2

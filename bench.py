@@ -314,6 +314,69 @@ def pyramid_rates(sv, dev, world, n, peak):
     return out
 
 
+def mirror_tree(B, kappa, gamma):
+    """parents [B, kappa*gamma] of a branch-complete tree: kappa roots below the context, each
+    the head of a chain of gamma drafted tokens (node id = branch*gamma + depth, depth 1..gamma)."""
+    par = np.zeros((B, kappa * gamma), dtype=np.int64)
+    for i in range(kappa):
+        for d in range(1, gamma + 1):
+            node = i * gamma + d
+            par[:, node - 1] = 0 if d == 1 else node - 1
+    return par
+
+
+def tree_rates(sv, dev, world, n):
+    """Rounds/s of sv_tree_verify on the branch-complete tree of the Mirror-style workload
+    (kappa = 8 roots, depth gamma = 7: 56 drafted nodes, V = 151936 bf16), B = 4 and B = 64
+    sequences, T = 1.  Each node's token is the library's draw from its parent's draft row."""
+    import torch
+    from synth import workloads as W
+    out = {}
+    for B in (4, 64):
+        base = W.MIRROR
+        N = base.kappa * base.K
+        w = W.scaled(base, B=B, K=N, draft_rows_extra=1, seed=rank_seed(base.seed, int(os.environ.get("RANK", "0"))))
+        tgt, drf = W.logits(w, 0, device=dev)
+        par = mirror_tree(B, base.kappa, base.K)
+        rng = np.random.default_rng(w.seed)
+        T_d = torch.as_tensor(W.temperatures(w), device=dev)
+        # node tokens: one draw per node from its parent's draft row
+        par_d = torch.as_tensor(par, device=dev)
+        rows = torch.gather(drf, 1, par_d[:, :, None].expand(B, N, w.V)).contiguous()
+        toks, _, _ = sv.sv_saguaro_sample(rows, torch.as_tensor(rng.random((B, N)), device=dev), T_d, n_rows=N)
+        u_d = torch.as_tensor(rng.random((B, N + 1)), device=dev)
+        par_i = par_d.to(torch.int32)
+        ws = sv.Workspace()
+        stats = sv.new_stats(dev)
+        al = torch.empty(B, dtype=torch.int32, device=dev)
+        ot = torch.empty((B, N + 1), dtype=torch.int32, device=dev)
+
+        def call():
+            sv.sv_tree_verify(tgt, drf, par_i, toks, u_d, T_d, accept_len=al, out_tokens=ot, path=False, stats=stats,
+                              workspace=ws)
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        start.record()
+        for _ in range(n):
+            call()
+        end.record()
+        torch.cuda.synchronize()
+        st = sv.read_stats(stats)
+        if st["status"] != 0:
+            raise RuntimeError(f"tree verify failed: {st}")
+        ms = max_over_ranks(start.elapsed_time(end) / n, world)
+        out[f"mirror_tree_B{B}"] = {"workload": f"branch-complete tree kappa=8 gamma=7 (56 nodes), B={B}, V={w.V} bf16",
+                                    "value": whole_job_rate(1.0, world, ms), "unit": "rounds/s", "ms_per_round": ms,
+                                    "steps": n, "mean_accept_len": float(al.float().mean().item()),
+                                    "child_tests": st["accept_tests"], "reresolved": st["reresolved"],
+                                    "unresolved": st["unresolved"],
+                                    "l2": "inputs of B=64 exceed L2; B=4 (0.14 GB) fits: no flush"}
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import speculative_decoding_verification_gb300 as sv
@@ -412,6 +475,7 @@ def run_ours(args, rank, world, local_rank):
                    "kernel_gbs": b_o / (k_o * 1e-3) / 1e9, "frac": b_o / (k_o * 1e-3) / 1e9 / peak}
     line["filters"] = filter_rates(sv, dev, world, min(n, 200))
     line["pyramid"] = pyramid_rates(sv, dev, world, min(n, 200), peak)
+    line["tree"] = tree_rates(sv, dev, world, min(n, 200))
     if args.kernel_only:
         return line if rank == 0 else None
 

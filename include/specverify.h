@@ -111,6 +111,9 @@ enum {
 /* Largest K accepted by sv_verify / sv_cache_keys (draft tokens per sequence). */
 #define SV_MAX_K 32
 
+/* Most drafted nodes in one tree of sv_tree_verify. */
+#define SV_MAX_TREE 128
+
 const char *sv_status_string(sv_status s);
 int sv_version(void);   /* major * 10000 + minor * 100 + patch */
 
@@ -265,6 +268,55 @@ sv_status sv_fuzzy_verify(const void *verifier_logits, int64_t v_row_pitch,
                           int32_t *accept_len, int32_t *out_tokens,
                           double *divergence, sv_stats *stats,
                           void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * sv_tree_verify — verify a tree of drafted tokens per sequence in one pass.
+ * [Mirror-SD notes §1.1 (tree drafts verified at once), §3.1 (branch-complete trees); SpS notes
+ *  §3 (the accept test and the residual, applied again after each rejection)]
+ *
+ * Node i (1..N) holds tokens[b][i-1] below node parents[b][i-1] in [0, i-1]; node 0 is the
+ * committed context.  Row i of target_logits / draft_logits is the distribution that follows node
+ * i; a node's children are drafted from its draft row.
+ *  Greedy (T == 0): from node 0, move to the first child (lowest index) holding the target argmax;
+ *    the target argmax where no child matches is the correction.
+ *  Sampled: the children of the current node are tested in index order; child i passes iff
+ *    u[b][i] < min(1, (q(t) - c_i p(t))+ / (R(c_i) p(t))), R(c) = sum_v (q_v - c p_v)+, c_1 = 0,
+ *    c_(i+1) = c_i + R(c_i) (SpS's residual applied again after each rejection: lossless).  A
+ *    passing child becomes the current node; when every child fails (or there is none) t* is
+ *    drawn from (q - c p)+ by the inverse CDF in id order at u[b][0].
+ *  Decisions are certified in float32 and redone in float-float where the margin is too thin.
+ *
+ *  target_logits, draft_logits  dev, rows (b, i) at b*(N+1)+i, i = 0..N, pitches in elements.
+ *                 Draft rows of greedy sequences are not read; draft rows of leaves are read
+ *                 by the statistics pass but not used (they must be finite).
+ *  parents, tokens  dev int32 [B][N]; uniforms dev float64 [B][N+1]; temperature dev float [B].
+ *  accept_len     dev int32 [B]: the number of accepted nodes k (the depth reached).
+ *  out_tokens     dev int32 [B][N+1]: the k accepted tokens, t*, then -1.
+ *  path           dev int32 [B][N] or NULL: the accepted node ids, then -1.
+ * Errors (stats): SV_ERR_INVALID_ARG for a parent outside [0, i-1] or a bad temperature,
+ * SV_ERR_BAD_TOKEN for a token outside [0, V), SV_ERR_NONFINITE for a non-finite row used.
+ * -------------------------------------------------------------------------------------- */
+size_t sv_tree_verify_workspace_size(int B, int N, int V);
+
+sv_status sv_tree_verify(const void *target_logits, int64_t t_row_pitch,
+                         const void *draft_logits, int64_t d_row_pitch, sv_dtype dtype,
+                         const int32_t *parents, const int32_t *tokens, const double *uniforms,
+                         int B, int N, int V, const float *temperature,
+                         int32_t *accept_len, int32_t *out_tokens, int32_t *path,
+                         sv_stats *stats, void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * sv_tree_reuse — does the committed prefix spell a path of a drafted tree?
+ * [Mirror-SD notes §3.2-§3.3: reuse when (accepted tokens, correction) is a path of the
+ *  branch-complete tree, a depth-2 node with several branches included]
+ *  parents, tokens  dev int32 [B][N] (as sv_tree_verify); accept_len dev int32 [B];
+ *  out_tokens       dev int32 [B][K+1] (k accepted tokens then the correction);
+ *  reuse_node       dev int32 [B] (output): the node where the path ends (1..N), or -1.
+ * At each depth the first child (lowest index) holding the committed token is followed.
+ * -------------------------------------------------------------------------------------- */
+sv_status sv_tree_reuse(const int32_t *parents, const int32_t *tokens, int N,
+                        const int32_t *accept_len, const int32_t *out_tokens, int K, int B,
+                        int32_t *reuse_node, sv_stream_t stream);
 
 /* ----------------------------------------------------------------------------------------
  * sv_saguaro_sample — draw one token from each of the first n_rows rows of every sequence's

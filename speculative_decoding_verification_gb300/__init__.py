@@ -218,6 +218,52 @@ def sv_fuzzy_verify(verifier, drafter, draft_tokens, uniforms, temperature, tau=
     return accept_len, out_tokens, (div[:, :K] if div is not None else None), stats
 
 
+def sv_tree_verify(target, draft, parents, tokens, uniforms, temperature, accept_len=None, out_tokens=None, path=True,
+                   stats=None, workspace=None, stream=None):
+    """sv_tree_verify on torch CUDA tensors: target and draft [B, N+1, V] (same dtype; row i follows
+    node i), parents and tokens int32 [B, N], uniforms float64 [B, N+1], temperature float32 [B].
+    Returns (accept_len int32 [B], out_tokens int32 [B, N+1], path int32 [B, N] or None, stats)."""
+    lib = load()
+    B, N1, V = target.shape
+    N = N1 - 1
+    dev = target.device
+    if draft.dtype != target.dtype or draft.shape[1] < N1:
+        raise TypeError("draft must share the target's dtype and hold N+1 rows per sequence")
+    t_pitch, _ = _rows(target, "target")
+    d_pitch, _ = _rows(draft, "draft")
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, N + 1), dtype=torch.int32, device=dev)
+    if path is True:
+        path = torch.empty((B, max(N, 1)), dtype=torch.int32, device=dev)
+    elif path is False:
+        path = None
+    if stats is None:
+        stats = new_stats(dev)
+    ws = (workspace or _default_ws).get(lib.sv_tree_verify_workspace_size(B, N, V), dev)
+    code = lib.sv_tree_verify(_ptr(target), t_pitch, _ptr(draft), d_pitch, _dtype_code(target),
+                              _ptr(parents if N > 0 else None), _ptr(tokens if N > 0 else None), _ptr(uniforms), B, N,
+                              V, _ptr(temperature), _ptr(accept_len), _ptr(out_tokens), _ptr(path), _ptr(stats),
+                              _ptr(ws), ws.numel(), _stream(stream))
+    _abi.check("sv_tree_verify", code)
+    return accept_len, out_tokens, (path[:, :N] if path is not None else None), stats
+
+
+def sv_tree_reuse(parents, tokens, accept_len, out_tokens, reuse_node=None, stream=None):
+    """sv_tree_reuse: per sequence the node where the committed prefix ends as a path of the
+    drafted tree (parents / tokens int32 [B, N]), or -1."""
+    lib = load()
+    B, N = parents.shape
+    K = out_tokens.shape[1] - 1
+    if reuse_node is None:
+        reuse_node = torch.empty(B, dtype=torch.int32, device=parents.device)
+    code = lib.sv_tree_reuse(_ptr(parents), _ptr(tokens), N, _ptr(accept_len), _ptr(out_tokens), K, B,
+                             _ptr(reuse_node), _stream(stream))
+    _abi.check("sv_tree_reuse", code)
+    return reuse_node
+
+
 def sv_saguaro_sample(draft, uniforms, temperature, top_p=None, F=0, C=1.0, n_rows=None, tokens=None, debug=False,
                       stats=None, workspace=None, stream=None, top_k=None):
     """sv_saguaro_sample: one token per row j < n_rows of each sequence of draft [B, R, V].

@@ -42,6 +42,10 @@ SIGNATURES = {
                                c_vp, c_int, c_f32, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
     "sv_verify_static": (c_int, [c_vp, c_i64, c_vp, c_i64, c_int, c_int, c_vp, c_vp, c_int, c_int, c_int, c_vp,
                                  c_vp, c_vp, c_int, c_f32, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "sv_tree_verify_workspace_size": (c_size, [c_int, c_int, c_int]),
+    "sv_tree_verify": (c_int, [c_vp, c_i64, c_vp, c_i64, c_int, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_vp, c_vp, c_vp,
+                               c_vp, c_vp, c_vp, c_size, c_vp]),
+    "sv_tree_reuse": (c_int, [c_vp, c_vp, c_int, c_vp, c_vp, c_int, c_int, c_vp, c_vp]),
     "sv_fuzzy_verify_workspace_size": (c_size, [c_int, c_int, c_int]),
     "sv_fuzzy_verify": (c_int, [c_vp, c_i64, c_vp, c_i64, c_int, c_int, c_vp, c_vp, c_int, c_int, c_int, c_vp, c_f32,
                                 c_int, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),

@@ -19,6 +19,7 @@
 // relative error, each residual sum R(c) is a block reduction over both rows with that error
 // summed, c accumulates the errors of the sums it adds up.  A node whose decision the margin
 // cannot settle is redone in float-float (exact row sums, residual sums and draw).
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "sv_accept.cuh"
@@ -57,14 +58,25 @@ __global__ void __launch_bounds__(kThreads) k_tree_rowstats(const TreeArgs a) {
     if ((threadIdx.x & 31) == 0) a.rowstat[rid] = r;
 }
 
-// ---- block-wide helpers (every thread gets the result) -------------------------------------
+// ---- cluster-wide helpers (every thread of every block gets the result) ----------------------
+// kTreeCluster blocks share one sequence; each streams its slice of every row.
+constexpr int kTreeCluster = 8;
+
 struct TreeShared {
     float2 tab[256];
     float s_hi[kWarps], s_lo[kWarps];
-    float2 seg[kThreads];      // per-thread segment sums (draw), then inclusive prefixes
-    int owner;
+    float2 part;               // this block's share of a cluster sum / scan
+    int owner;                 // draw: first segment of this block past u R (kThreads: none)
     int result;
-    float2 c_at, c_before;     // draw: cumulative sums at t* and before it
+    float2 c_at, c_before;     // draw: cumulative sums at t* and before it (owner block)
+};
+
+struct TreeCtx {
+    cooperative_groups::cluster_group cl;
+    int rank;
+    int n_vec, V;
+    int w0, w1;                // this block's slice of 16-byte words
+    bool tail;                 // this block also takes the row's scalar tail
 };
 
 __device__ __forceinline__ ff block_sum_ffv(ff v, TreeShared &S) {
@@ -83,6 +95,20 @@ __device__ __forceinline__ ff block_sum_ffv(ff v, TreeShared &S) {
     return t;
 }
 
+// Sum over the cluster, added in rank order so that every block gets the same value.
+__device__ __forceinline__ ff cluster_sum_ff(TreeCtx &X, ff v, TreeShared &S) {
+    const ff b = block_sum_ffv(v, S);
+    if (threadIdx.x == 0) S.part = make_float2(b.hi, b.lo);
+    X.cl.sync();
+    ff t = {0.f, 0.f};
+    for (int q = 0; q < kTreeCluster; ++q) {
+        const float2 pq = *X.cl.map_shared_rank(&S.part, q);
+        t = ff_add(t, {pq.x, pq.y});
+    }
+    X.cl.sync();   // S.part is free again
+    return t;
+}
+
 // Normalised float32 weight of one token (the draw pass's form).
 __device__ __forceinline__ float tw(const DrawRow &R, float x, float &y) {
     x = fmaxf(x, kDrawFloor);
@@ -96,12 +122,12 @@ __device__ __forceinline__ ff twx(float x, ff c, int r, ff inv_s, const float2 *
     return ff_mul(ff_exp2_xc(x, c, r, tab), inv_s);
 }
 
-// Calls fn(xq, xp, v) for every token of the two rows (16-byte words, then the scalar tail).
-// Thread t takes words t, t + blockDim, ... (order inside a thread: ascending).
+// Calls fn(xq, xp, v) for every token of this block's slice of the two rows (16-byte words, then
+// the scalar tail in the last block).  Thread t takes words w0 + t, w0 + t + blockDim, ...
 template <int ES, class Fn>
-__device__ __forceinline__ void for_pair(const char *rq, const char *rp, int V, int n_vec, Fn fn) {
+__device__ __forceinline__ void for_pair(const TreeCtx &X, const char *rq, const char *rp, Fn fn) {
     constexpr int EPV = 16 / ES;
-    for (int wi = threadIdx.x; wi < n_vec; wi += kThreads) {
+    for (int wi = X.w0 + threadIdx.x; wi < X.w1; wi += kThreads) {
         const uint4 gq = __ldg(reinterpret_cast<const uint4 *>(rq) + wi);
         const uint4 gp = __ldg(reinterpret_cast<const uint4 *>(rp) + wi);
         float xq[EPV], xp[EPV];
@@ -110,7 +136,8 @@ __device__ __forceinline__ void for_pair(const char *rq, const char *rp, int V, 
 #pragma unroll
         for (int k = 0; k < EPV; ++k) fn(xq[k], xp[k], wi * EPV + k);
     }
-    for (int v = n_vec * EPV + threadIdx.x; v < V; v += kThreads) fn(load_elem<ES>(rq, v), load_elem<ES>(rp, v), v);
+    if (X.tail)
+        for (int v = X.n_vec * EPV + threadIdx.x; v < X.V; v += kThreads) fn(load_elem<ES>(rq, v), load_elem<ES>(rp, v), v);
 }
 
 // Per-token relative error of a float32 weight, without the ln2 u |y| part: the exponential,
@@ -125,15 +152,15 @@ constexpr double kTreeKappa = kLn2 * kU32 * 1.01;   // relative error per unit |
 // Float32 residual sum R(c) = sum_v (q_v - c p_v)+ and a bound on its error.  dc bounds the error
 // of c itself.
 template <int ES>
-__device__ __forceinline__ float tree_R(const DrawRow &Q, const DrawRow &P, float c, double dc, int V, int n_vec,
+__device__ __forceinline__ float tree_R(TreeCtx &X, const DrawRow &Q, const DrawRow &P, float c, double dc,
                                         TreeShared &S, double &err) {
     ff acc = {0.f, 0.f};
-    for_pair<ES>(Q.row, P.row, V, n_vec, [&](float xq, float xp, int) {
+    for_pair<ES>(X, Q.row, P.row, [&](float xq, float xp, int) {
         float yq, yp;
         const float wq = tw(Q, xq, yq), wp = tw(P, xp, yp);
         acc = ff_add_f(acc, fmaxf(fmaf(-c, wp, wq), 0.f));
     });
-    const ff R = block_sum_ffv(acc, S);
+    const ff R = cluster_sum_ff(X, acc, S);
     // the positive part is 1-Lipschitz: sum_v |dq_v| + c |dp_v| + |dc| p_v, plus the sums
     err = (base_err(Q) + kTreeKappa * Q.ay) + (double)c * (base_err(P) + kTreeKappa * P.ay) + dc +
           8.0 * kU32 * (1.0 + (double)c) + 1e-12;
@@ -141,28 +168,31 @@ __device__ __forceinline__ float tree_R(const DrawRow &Q, const DrawRow &P, floa
 }
 
 template <int ES>
-__device__ __forceinline__ ff tree_R_exact(const char *rq, const char *rp, ff c_, int r_q, int r_p, ff iq, ff ip, ff c,
-                                           int V, int n_vec, TreeShared &S) {
+__device__ __forceinline__ ff tree_R_exact(TreeCtx &X, const char *rq, const char *rp, ff c_, int r_q, int r_p, ff iq,
+                                           ff ip, ff c, TreeShared &S) {
     ff acc = {0.f, 0.f};
-    for_pair<ES>(rq, rp, V, n_vec, [&](float xq, float xp, int) {
+    for_pair<ES>(X, rq, rp, [&](float xq, float xp, int) {
         const ff d = ff_sub(twx(xq, c_, r_q, iq, S.tab), ff_mul(c, twx(xp, c_, r_p, ip, S.tab)));
         if (d.hi > 0.f) acc = ff_add(acc, d);
     });
-    return block_sum_ffv(acc, S);
+    return cluster_sum_ff(X, acc, S);
 }
 
 // Inverse-CDF draw over w_v = (q_v - c p_v)+ (c = 0: q) in id order: t* = min{v : C(v) > u R}.
-// Segments of contiguous words per thread; float32 sums into float-float per thread and a
-// float-float block scan; the owning thread rescans its segment.  Returns t* and whether the
-// margin certifies it (float32 weights); with exact = true the weights are float-float.
+// Segments of contiguous words, one per thread of the cluster in id order; float32 sums into
+// float-float per thread, a float-float scan over the cluster; the owning thread rescans its
+// segment.  Returns t* and whether the margin certifies it (float32 weights); with EXACT the
+// weights are float-float.
 template <int ES, bool EXACT>
-__device__ __forceinline__ int tree_draw(const DrawRow &Q, const DrawRow &P, float c, double dc, double u,
-                                         const char *rq, const char *rp, ff c_, int r_q, int r_p, ff iq, ff ip,
-                                         ff cx, int V, int n_vec, TreeShared &S, bool &certain) {
+__device__ __forceinline__ int tree_draw(TreeCtx &X, const DrawRow &Q, const DrawRow &P, float c, double dc,
+                                         double u, ff c_, int r_q, int r_p, ff iq, ff ip, ff cx, TreeShared &S,
+                                         bool &certain) {
     constexpr int EPV = 16 / ES;
-    const int per = (n_vec + kThreads - 1) / kThreads;   // words per segment
-    const int w0 = min(n_vec, (int)threadIdx.x * per), w1 = min(n_vec, w0 + per);
-    const bool last = threadIdx.x == kThreads - 1;
+    const int n_vec = X.n_vec, V = X.V;
+    const int per = (n_vec + kThreads * kTreeCluster - 1) / (kThreads * kTreeCluster);   // words per segment
+    const int g = X.rank * kThreads + (int)threadIdx.x;
+    const int w0 = min(n_vec, g * per), w1 = min(n_vec, w0 + per);
+    const bool last = g == kThreads * kTreeCluster - 1;
     auto weight = [&](float xq, float xp) -> ff {
         if constexpr (EXACT) {
             const ff d = ff_sub(twx(xq, c_, r_q, iq, S.tab), ff_mul(cx, twx(xp, c_, r_p, ip, S.tab)));
@@ -192,7 +222,7 @@ __device__ __forceinline__ int tree_draw(const DrawRow &Q, const DrawRow &P, flo
     }
     if (last)
         for (int v = n_vec * EPV; v < V; ++v) seg = ff_add(seg, weight(load_elem<ES>(Q.row, v), load_elem<ES>(P.row, v)));
-    // inclusive block scan of the segment sums (thread order = id order)
+    // inclusive scan of the segment sums in thread order, then over the blocks in rank order
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     ff inc = seg;
 #pragma unroll
@@ -205,23 +235,38 @@ __device__ __forceinline__ int tree_draw(const DrawRow &Q, const DrawRow &P, flo
         S.s_hi[warp] = inc.hi;
         S.s_lo[warp] = inc.lo;
     }
+    __syncthreads();
+    ff base = {0.f, 0.f}, blk = {0.f, 0.f};
+    for (int i = 0; i < kWarps; ++i) {
+        if (i < warp) base = ff_add(base, {S.s_hi[i], S.s_lo[i]});
+        blk = ff_add(blk, {S.s_hi[i], S.s_lo[i]});
+    }
     if (threadIdx.x == 0) {
+        S.part = make_float2(blk.hi, blk.lo);
         S.owner = kThreads;
         S.result = -1;
     }
-    __syncthreads();
-    ff base = {0.f, 0.f}, R = {0.f, 0.f};
-    for (int i = 0; i < kWarps; ++i) {
-        if (i < warp) base = ff_add(base, {S.s_hi[i], S.s_lo[i]});
-        R = ff_add(R, {S.s_hi[i], S.s_lo[i]});
+    X.cl.sync();
+    ff before_blocks = {0.f, 0.f}, R = {0.f, 0.f};
+    for (int q = 0; q < kTreeCluster; ++q) {
+        const float2 pq = *X.cl.map_shared_rank(&S.part, q);
+        if (q < X.rank) before_blocks = ff_add(before_blocks, {pq.x, pq.y});
+        R = ff_add(R, {pq.x, pq.y});
     }
-    inc = ff_add(base, inc);
-    const ff X = ff_mul({(float)u, (float)(u - (double)(float)u)}, R);
+    inc = ff_add(before_blocks, ff_add(base, inc));
+    const ff Xu = ff_mul({(float)u, (float)(u - (double)(float)u)}, R);
     const ff excl = ff_sub(inc, seg);
-    if (ff_diff(inc, X) > 0.f && seg.hi > 0.f) atomicMin(&S.owner, (int)threadIdx.x);
-    __syncthreads();
-    const int owner = S.owner;
-    if ((int)threadIdx.x == owner) {
+    if (ff_diff(inc, Xu) > 0.f && seg.hi > 0.f) atomicMin(&S.owner, (int)threadIdx.x);
+    X.cl.sync();
+    int owner_rank = -1, owner_t = kThreads;
+    for (int q = 0; q < kTreeCluster && owner_rank < 0; ++q) {
+        const int o = *X.cl.map_shared_rank(&S.owner, q);
+        if (o < kThreads) {
+            owner_rank = q;
+            owner_t = o;
+        }
+    }
+    if (X.rank == owner_rank && (int)threadIdx.x == owner_t) {
         ff C = excl;
         int t_star = -1;
         ff before = excl;
@@ -231,7 +276,7 @@ __device__ __forceinline__ int tree_draw(const DrawRow &Q, const DrawRow &P, flo
             if (!(w.hi > 0.f)) return;
             before = C;
             C = ff_add(C, w);
-            if (ff_diff(C, X) > 0.f) t_star = v;
+            if (ff_diff(C, Xu) > 0.f) t_star = v;
         };
         for (int wi = w0; wi < w1 && t_star < 0; ++wi) {
             const uint4 gq = __ldg(reinterpret_cast<const uint4 *>(Q.row) + wi);
@@ -248,11 +293,19 @@ __device__ __forceinline__ int tree_draw(const DrawRow &Q, const DrawRow &P, flo
         S.c_at = make_float2(C.hi, C.lo);
         S.c_before = make_float2(before.hi, before.lo);
     }
-    __syncthreads();
-    int t_star = S.result;
-    const double Xd = ff_to_double(X), Rd = ff_to_double(R);
-    const double ca = (double)S.c_at.x + S.c_at.y, cb = (double)S.c_before.x + S.c_before.y;
-    if (owner == kThreads || t_star < 0) {   // rounding left u R at or beyond the total
+    X.cl.sync();
+    int t_star = -1;
+    float2 c_at = make_float2(0.f, 0.f), c_bf = make_float2(0.f, 0.f);
+    if (owner_rank >= 0) {
+        TreeShared *O = X.cl.map_shared_rank(&S, owner_rank);
+        t_star = O->result;
+        c_at = O->c_at;
+        c_bf = O->c_before;
+    }
+    X.cl.sync();   // the owner's results are read before any block moves on
+    const double Xd = ff_to_double(Xu), Rd = ff_to_double(R);
+    const double ca = (double)c_at.x + c_at.y, cb = (double)c_bf.x + c_bf.y;
+    if (owner_rank < 0 || t_star < 0) {   // rounding left u R at or beyond the total
         certain = false;
         t_star = -1;
     } else if (EXACT) {
@@ -263,17 +316,25 @@ __device__ __forceinline__ int tree_draw(const DrawRow &Q, const DrawRow &P, flo
         const double E = fmax(u, 1.0 - u) * tok + 8.1 * kU32 * (ca + u * Rd) + 1e-9 * Rd + 1e-30;
         certain = (ca - Xd) > E && (Xd - cb) > E;
     }
-    __syncthreads();
     return t_star;
 }
 
-// Per sequence: the walk through the tree (one block).
+// Per sequence: the walk through the tree (one cluster of kTreeCluster blocks; every block takes
+// the same decisions from the same values, each streams its slice of the rows).
 template <int ES>
-__global__ void __launch_bounds__(kThreads) k_tree_walk(const TreeArgs a) {
+__global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kThreads) k_tree_walk(const TreeArgs a) {
     __shared__ TreeShared S;
     __shared__ int s_first[SV_MAX_TREE + 1], s_next[SV_MAX_TREE + 1], s_tok[SV_MAX_TREE + 1];
     __shared__ int s_err, s_errcode;
-    const int b = blockIdx.x, N = a.N, V = a.V;
+    const int b = blockIdx.x / kTreeCluster, N = a.N, V = a.V;
+    TreeCtx X{cooperative_groups::this_cluster(), 0, a.n_vec, V, 0, 0, false};
+    X.rank = (int)X.cl.block_rank();
+    {
+        const int per = (a.n_vec + kTreeCluster - 1) / kTreeCluster;
+        X.w0 = min(a.n_vec, X.rank * per);
+        X.w1 = min(a.n_vec, X.w0 + per);
+        X.tail = X.rank == kTreeCluster - 1;
+    }
     const float T = a.temperature[b];
     const bool greedy = T == 0.0f;
     int32_t *outs = a.out_tokens + (size_t)b * (N + 1);
@@ -315,10 +376,12 @@ __global__ void __launch_bounds__(kThreads) k_tree_walk(const TreeArgs a) {
                 }
             }
         }
-        if (s_err) report_error(a.stats, s_errcode, b);
+        if (s_err && X.rank == 0) report_error(a.stats, s_errcode, b);
     }
     __syncthreads();
-    if (s_err) {
+    if (s_err || (greedy && X.rank != 0)) {   // (greedy: block 0 walks alone; no block reads another's memory)
+        if (!s_err) return;
+        if (X.rank != 0) return;
         if (threadIdx.x == 0) a.accept_len[b] = 0;
         for (int j = threadIdx.x; j <= N; j += kThreads) outs[j] = -1;
         if (pth)
@@ -348,7 +411,6 @@ __global__ void __launch_bounds__(kThreads) k_tree_walk(const TreeArgs a) {
             }
         }
     } else {
-        const int n_vec = a.n_vec;
         const double *ub = a.uniforms + (size_t)b * (N + 1);
         while (true) {
             const long long rt = (long long)b * (N + 1) + node, rd = a.n_rows0 + rt;
@@ -386,7 +448,7 @@ __global__ void __launch_bounds__(kThreads) k_tree_walk(const TreeArgs a) {
                 const float c_new = c + R;
                 const double dc_new = dc + dR + kU32 * (double)c_new;
                 double eR;
-                const float R_new = tree_R<ES>(Q, P, c_new, dc_new, V, n_vec, S, eR);
+                const float R_new = tree_R<ES>(X, Q, P, c_new, dc_new, S, eR);
                 if (!((double)R_new > eR)) {   // cannot tell the residual from empty
                     exact = true;
                     break;
@@ -398,8 +460,8 @@ __global__ void __launch_bounds__(kThreads) k_tree_walk(const TreeArgs a) {
             }
             if (!exact && nxt < 0) {   // every child failed (or none): the draw
                 bool certain = false;
-                const int t = tree_draw<ES, false>(Q, P, c, dc, ub[0], rowq, rowp, {0.f, 0.f}, 0, 0, {0.f, 0.f},
-                                                   {0.f, 0.f}, {0.f, 0.f}, V, n_vec, S, certain);
+                const int t = tree_draw<ES, false>(X, Q, P, c, dc, ub[0], {0.f, 0.f}, 0, 0, {0.f, 0.f}, {0.f, 0.f},
+                                                   {0.f, 0.f}, S, certain);
                 if (certain) t_star = t;
                 else exact = true;
             }
@@ -413,11 +475,12 @@ __global__ void __launch_bounds__(kThreads) k_tree_walk(const TreeArgs a) {
                 const ff c_ = {c_hi, c_lo};
                 const int r_q = a.rowstat[rt].r, r_p = has_children ? a.rowstat[rd].r : r_q;
                 ff sq = {0.f, 0.f}, sp = {0.f, 0.f};
-                for_pair<ES>(rowq, rowp, V, n_vec, [&](float xq, float xp, int) {
+                for_pair<ES>(X, rowq, rowp, [&](float xq, float xp, int) {
                     if (xq != -INFINITY) sq = ff_add(sq, ff_exp2_xc(xq, c_, r_q, S.tab));
                     if (has_children && xp != -INFINITY) sp = ff_add(sp, ff_exp2_xc(xp, c_, r_p, S.tab));
                 });
-                const ff Sq = block_sum_ffv(sq, S), Sp = block_sum_ffv(sp, S);
+                const ff Sq = cluster_sum_ff(X, sq, S);
+                const ff Sp = cluster_sum_ff(X, sp, S);
                 const ff iq = ff_recip(Sq), ip = has_children ? ff_recip(Sp) : ff{0.f, 0.f};
                 ff cx = {0.f, 0.f}, Rx = {1.f, 0.f};
                 for (int ch = s_first[node]; ch >= 0; ch = s_next[ch]) {
@@ -433,7 +496,7 @@ __global__ void __launch_bounds__(kThreads) k_tree_walk(const TreeArgs a) {
                         break;
                     }
                     const ff c_next = ff_add(cx, Rx);
-                    const ff R_next = tree_R_exact<ES>(rowq, rowp, c_, r_q, r_p, iq, ip, c_next, V, n_vec, S);
+                    const ff R_next = tree_R_exact<ES>(X, rowq, rowp, c_, r_q, r_p, iq, ip, c_next, S);
                     if (!(R_next.hi > 0.f)) {   // empty residual after rounding: draw from q
                         cx = {0.f, 0.f};
                         Rx = {1.f, 0.f};
@@ -444,14 +507,13 @@ __global__ void __launch_bounds__(kThreads) k_tree_walk(const TreeArgs a) {
                 }
                 if (nxt < 0) {
                     bool certain = true;
-                    const int t = tree_draw<ES, true>(Q, P, 0.f, 0.0, ub[0], rowq, rowp, c_, r_q, r_p, iq, ip, cx, V,
-                                                      n_vec, S, certain);
+                    const int t = tree_draw<ES, true>(X, Q, P, 0.f, 0.0, ub[0], c_, r_q, r_p, iq, ip, cx, S, certain);
                     if (!certain) ++unresolved;
                     t_star = t >= 0 ? t : a.rowstat[rt].argmax;
                 }
             }
             if (nxt < 0) break;
-            if (threadIdx.x == 0) {
+            if (threadIdx.x == 0 && X.rank == 0) {
                 if (pth) pth[k] = nxt;
                 outs[k] = s_tok[nxt];
             }
@@ -460,6 +522,8 @@ __global__ void __launch_bounds__(kThreads) k_tree_walk(const TreeArgs a) {
         }
     }
     __syncthreads();
+    if (!greedy) X.cl.sync();   // no block leaves while another may read its shared memory
+    if (X.rank != 0) return;
     if (threadIdx.x == 0) {   // (greedy: k and t_star come from thread 0's walk)
         a.accept_len[b] = k;
         outs[k] = t_star;
@@ -551,7 +615,7 @@ static sv_status launch_tree(const TreePlan &pl, TreeArgs ta, void *ws, cudaStre
     ta.rowstat = reinterpret_cast<RowStat *>(w + pl.off_rowstat);
     ta.n_vec = pl.n_vec;
     k_tree_rowstats<<<(unsigned)div_up(ta.n_rows, kWarps), kThreads, 0, stream>>>(ta);
-    k_tree_walk<ES><<<ta.B, kThreads, 0, stream>>>(ta);
+    k_tree_walk<ES><<<(unsigned)ta.B * kTreeCluster, kThreads, 0, stream>>>(ta);
     return cuda_status(cudaGetLastError());
 }
 

@@ -6,10 +6,13 @@
 //  runs the speculative-sampling test and replaces a rejected token by a sample of the
 //  verifier's own distribution.]
 //
-// Div is the Jensen-Shannon divergence in bits.  With s = q + p and d = (q - p) / s per token,
-//   JSD = 1/4 sum_v s_v h(d_v),   h(d) = (1 + d) log2(1 + d) + (1 - d) log2(1 - d) in [0, 2],
-// a sum of non-negative terms; h is evaluated by its series (1/ln2) sum_k d^2k / (k (2k - 1))
-// for |d| < 1/4 (no cancellation) and by its logarithms otherwise.
+// Div is the Jensen-Shannon divergence in bits, a sum of non-negative per-token terms
+//   (q log2(2q/(q+p)) + p log2(2p/(q+p))) / 2 = M g(l),  M = max(q, p), l = |log2(q/p)|,
+//   g(l) = ((1 + z)(1 - log2(1 + z)) - l z) / 2, z = 2^-l  (0 at l = 0, 1/2 as l grows),
+// with g read from a cubic table (sv_js_table.h) and l taken from the exponents: one
+// exponential per token.  The float-float pass (positions too close to tau) evaluates the same
+// term as (q + p) h(d) / 4, h(d) = (1 + d) log2(1 + d) + (1 - d) log2(1 - d), d = (q - p)/(q + p),
+// by its series for |d| < 1/4 and by float-float logarithms elsewhere.
 //
 // Kernels, in stream order (divergence mode):
 //   k_stats          row statistics of every verifier row and every drafter row
@@ -27,6 +30,7 @@
 #include "sv_device.cuh"
 #include "sv_exp2_table.h"
 #include "sv_host.h"
+#include "sv_js_table.h"
 #include "sv_stats.cuh"
 #include "sv_tiers.cuh"
 
@@ -68,35 +72,32 @@ __global__ void __launch_bounds__(kThreads) k_rowstats(const FuzzyArgs a) {
     if ((threadIdx.x & 31) == 0) a.rowstat[rid] = r;
 }
 
-// (1/ln2) / (k (2k - 1)), k = 1..6: the series of h(d) in d^2.
-constexpr float kH1 = 1.4426950408889634f, kH2 = kH1 / 6.0f, kH3 = kH1 / 15.0f, kH4 = kH1 / 28.0f,
-                kH5 = kH1 / 45.0f, kH6 = kH1 / 66.0f;
+// One token's term of the divergence, M g(l) with M = max(q, p) and l = |log2(q/p)| (the float
+// weights of the draw pass), and its error weight M (|y_q| + |y_p|).  l comes from the exponents
+// (y_q - y_p + log2(inv_q / inv_p) + (x_q - x_p) c_lo), so one exponential per token suffices; g
+// is read from the cubic table in shared memory.
+struct JsPair {
+    DrawRow Q, P;
+    float dL;   // log2(inv_q) - log2(inv_p)
+};
 
-// s h(d) and s (|y_q| + |y_p|) of one token, float32.  q and p are the normalised weights of
-// the draw pass (one rounding of y, first-order c_lo factor).
-__device__ __forceinline__ void js_term(float xq, float xp, const DrawRow &Q, const DrawRow &P, float &f, float &yw) {
+__device__ __forceinline__ void js_term(float xq, float xp, const JsPair &J, const float4 *tab, float &f, float &yw) {
     xq = fmaxf(xq, kDrawFloor);
     xp = fmaxf(xp, kDrawFloor);
-    const float yq = fmaf(xq, Q.c_hi, -Q.rf), yp = fmaf(xp, P.c_hi, -P.rf);
-    const float wq = ex2_fast(yq) * fmaf(xq, Q.k_lo, Q.inv_s);
-    const float wp = ex2_fast(yp) * fmaf(xp, P.k_lo, P.inv_s);
-    const float s = wq + wp;
-    f = 0.f;
-    yw = 0.f;
-    if (s > 0.f) {
-        const float r = __fdividef(1.0f, s);
-        const float d = (wq - wp) * r;
-        float h;
-        if (fabsf(d) < 0.25f) {
-            const float d2 = d * d;
-            h = d2 * fmaf(d2, fmaf(d2, fmaf(d2, fmaf(d2, fmaf(d2, kH6, kH5), kH4), kH3), kH2), kH1);
-        } else {
-            const float qa = 2.0f * wq * r, pb = 2.0f * wp * r;
-            h = (qa > 0.f ? qa * __log2f(qa) : 0.f) + (pb > 0.f ? pb * __log2f(pb) : 0.f);
-        }
-        f = s * h;
-        yw = s * (fabsf(yq) + fabsf(yp));
+    const float yq = fmaf(xq, J.Q.c_hi, -J.Q.rf), yp = fmaf(xp, J.P.c_hi, -J.P.rf);
+    const float lam = (yq - yp) + fmaf(xq - xp, J.Q.c_lo, J.dL);
+    const bool qbig = lam >= 0.f;
+    const float M = ex2_fast(qbig ? yq : yp) * fmaf(qbig ? xq : xp, qbig ? J.Q.k_lo : J.P.k_lo, qbig ? J.Q.inv_s : J.P.inv_s);
+    const float l = fabsf(lam) * (float)kJsTableN;
+    float g = 0.5f;
+    if (l < (float)(kJsTableN * kJsTableL)) {
+        const int i = (int)l;
+        const float t = l - (float)i;
+        const float4 e = tab[i];
+        g = fmaf(t, fmaf(t, fmaf(t, e.w, e.z), e.y), e.x);
     }
+    f = M * g;
+    yw = M * (fabsf(yq) + fabsf(yp));
 }
 
 __device__ __forceinline__ DrawRow fuzzy_row(const FuzzyArgs &a, bool ver, long long b, int j, float T) {
@@ -115,6 +116,7 @@ template <int ES>
 __global__ void __launch_bounds__(kThreads) k_div(const FuzzyArgs a) {
     constexpr int EPV = 16 / ES;
     __shared__ float s_h[kWarps], s_l[kWarps], s_y[kWarps];
+    __shared__ float4 s_js[kJsTableSize];
     const long long unit = blockIdx.x;
     const long long pair = unit / a.dv_chunks;
     const int chunk = (int)(unit - pair * a.dv_chunks);
@@ -124,7 +126,13 @@ __global__ void __launch_bounds__(kThreads) k_div(const FuzzyArgs a) {
     if (T == 0.0f || !fuzzy_t_ok(T)) return;
     const RowStat rq = a.rowstat[b * (a.K + 1) + j], rp = a.rowstat[a.n_rows0 + b * a.K + j];
     if (!row_ok(rq, false) || !row_ok(rp, false)) return;   // reported by k_fuzzy_accept
-    const DrawRow Q = fuzzy_row(a, true, b, j, T), P = fuzzy_row(a, false, b, j, T);
+    for (int i = threadIdx.x; i < kJsTableSize; i += kThreads) s_js[i] = kJsTable[i];
+    JsPair J;
+    J.Q = fuzzy_row(a, true, b, j, T);
+    J.P = fuzzy_row(a, false, b, j, T);
+    J.dL = (float)(log2((double)J.Q.inv_s) - log2((double)J.P.inv_s));
+    const DrawRow &Q = J.Q, &P = J.P;
+    __syncthreads();
     const int w0 = chunk * a.dv_words, w1 = min(a.n_vec, w0 + a.dv_words);
     const uint4 *vq = reinterpret_cast<const uint4 *>(Q.row);
     const uint4 *vp = reinterpret_cast<const uint4 *>(P.row);
@@ -148,7 +156,7 @@ __global__ void __launch_bounds__(kThreads) k_div(const FuzzyArgs a) {
 #pragma unroll
         for (int k = 0; k < EPV; ++k) {
             float f, yw;
-            js_term(xq[k], xp[k], Q, P, f, yw);
+            js_term(xq[k], xp[k], J, s_js, f, yw);
             fs += f;
             ys += yw;
         }
@@ -158,7 +166,7 @@ __global__ void __launch_bounds__(kThreads) k_div(const FuzzyArgs a) {
     if (chunk == a.dv_chunks - 1) {   // the row's last (< 16 B) elements
         for (int v = a.n_vec * EPV + threadIdx.x; v < a.V; v += kThreads) {
             float f, yw;
-            js_term(load_elem<ES>(Q.row, v), load_elem<ES>(P.row, v), Q, P, f, yw);
+            js_term(load_elem<ES>(Q.row, v), load_elem<ES>(P.row, v), J, s_js, f, yw);
             acc = ff_add_f(acc, f);
             ysum += yw;
         }
@@ -347,21 +355,22 @@ __global__ void __launch_bounds__(32) k_fuzzy_accept(const FuzzyArgs a, int pass
                 F = ff_add(F, {dp.s_hi, dp.s_lo});
                 Y += dp.y;
             }
-            dv = 0.25 * ff_to_double(F);
-            // Bound on |div - JSD|: the token weights carry relative errors alpha, beta (the
-            // normaliser, the exponential, the factor, the product, and ln2 u |y| from rounding
-            // y once); JSD is 1-homogeneous with partials log2(2q/s)/2 and log2(2p/s)/2, and
-            // q |log2(2q/s)| <= s, so the input errors move it by at most
-            // sum_v s_v (alpha_v + beta_v) / 2 <= A_q + A_p + (ln2 u / 2) Y.  h(d) itself: 1.2e-6
-            // relative on the series, 4.5e-6 absolute with the logarithms (sum s = 2); the
-            // float32 word sums 8u relative.
+            dv = ff_to_double(F);
+            // Bound on |dv - JSD|.  Per token the term is M g(l).  M carries the weight's relative
+            // error (the normaliser, the exponential, the factor and product roundings, and
+            // ln2 u |y| from rounding y once): at most g M (A + ln2 u |y|) with g <= 1/2 and
+            // sum M <= 2.  l carries u (|y_q| + |y_p|) from the exponents' roundings plus the
+            // normalisers' relative errors / ln2 (through dL); g moves by at most kJsSlopeMax per
+            // unit of l.  The table adds kJsTableErr per unit of M, its Horner evaluation 3u, the
+            // float32 word sums 8u.  Y = sum M (|y_q| + |y_p|).
             const DrawRow Q = fuzzy_row(a, true, b, lane, T), P = fuzzy_row(a, false, b, lane, T);
             const double rq2 = kLn2 * 0x1p-23 * (fabs((double)Q.rf) + 128.0);
             const double rp2 = kLn2 * 0x1p-23 * (fabs((double)P.rf) + 128.0);
             const double Aq = kEx2RelErr + 4.0 * kU32 + Q.norm_err + rq2 * rq2;
             const double Ap = kEx2RelErr + 4.0 * kU32 + P.norm_err + rp2 * rp2;
             const double E = 1.0002 * (Aq + Ap) + 0.5 * kLn2 * kU32 * 1.01 * 1.001 * (double)Y +
-                             (1.2e-6 + 8.0 * kU32) * dv + 2.3e-6 + 1e-9;
+                             kJsSlopeMax * (3.0 * kU32 * 1.001 * (double)Y + 2.0 * 1.4427 * (Q.norm_err + P.norm_err)) +
+                             2.0 * kJsTableErr + 8.0 * kU32 + 8.0 * kU32 * dv + 1e-9;
             amb = fabs(dv - (double)a.tau) <= E;
         }
     }

@@ -126,3 +126,53 @@ def test_exp2_table_header_values():
             t = (ln2 * j / 256).exp()
             assert abs(decimal.Decimal(hi) + decimal.Decimal(lo) - t) / t < decimal.Decimal(2) ** -47
             assert abs(decimal.Decimal(hi) - t) <= decimal.Decimal(2) ** -24 * t
+
+
+def _js_table():
+    path = os.path.join(ROOT, "speculative_decoding_verification_gb300", "csrc", "sv_js_table.h")
+    text = open(path).read()
+    num = r"(-?0x[0-9a-f.p+-]+)f"
+    rows = re.findall(r"\{" + ", ".join([num] * 4) + r"\}", text)
+    consts = {k: float(v) for k, v in re.findall(r"constexpr (?:int|double) (kJs\w+) = ([0-9.e+-]+);", text)}
+    return np.array([[float.fromhex(x) for x in r] for r in rows]), consts
+
+
+def test_js_table_header_values():
+    """The cubic table of g(l) behind the divergence kernel: its interpolant stays within
+    kJsTableErr of g (evaluated here with 50-digit arithmetic at points the generator did not
+    sample), kJsSlopeMax bounds g', and M g(l) summed over tokens is the Jensen-Shannon divergence
+    of the oracle."""
+    import mpmath
+    import oracle
+    mpmath.mp.dps = 30
+    tab, c = _js_table()
+    N, L = int(c["kJsTableN"]), int(c["kJsTableL"])
+    assert tab.shape == (N * L, 4) and c["kJsTableErr"] < 1e-7
+
+    def g_exact(l):
+        z = mpmath.power(2, -mpmath.mpf(l))
+        return float(((1 + z) * (1 - mpmath.log(1 + z, 2)) - l * z) / 2)
+
+    def g_tab(l):
+        x = l * N
+        if x >= N * L:
+            return 0.5
+        i = int(x)
+        t = x - i
+        g0, d, a, b = tab[i]
+        return g0 + t * (d + t * (a + t * b))
+
+    rng = np.random.default_rng(3)
+    ls = np.concatenate([rng.uniform(0, 4, 300), rng.uniform(4, L + 4, 200), [0.0, 1e-3, L - 1e-6, L + 1e-6]])
+    for l in ls:
+        assert abs(g_tab(l) - g_exact(l)) <= c["kJsTableErr"], l
+    for l in rng.uniform(0, 10, 200):
+        h = 1e-6
+        assert abs(g_exact(l + h) - g_exact(l)) / h <= c["kJsSlopeMax"]
+    for _ in range(20):
+        q = rng.random(50) ** 4
+        p = rng.random(50) ** 4
+        q /= q.sum()
+        p /= p.sum()
+        terms = [max(a, b) * g_exact(abs(np.log2(a / b))) for a, b in zip(q, p)]
+        assert sum(terms) == pytest.approx(oracle.jensen_shannon(q, p), rel=1e-12, abs=1e-15)

@@ -127,12 +127,17 @@ __global__ void __launch_bounds__(kThreads) k_div(const FuzzyArgs a) {
     const RowStat rq = a.rowstat[b * (a.K + 1) + j], rp = a.rowstat[a.n_rows0 + b * a.K + j];
     if (!row_ok(rq, false) || !row_ok(rp, false)) return;   // reported by k_fuzzy_accept
     for (int i = threadIdx.x; i < kJsTableSize; i += kThreads) s_js[i] = kJsTable[i];
-    JsPair J;
-    J.Q = fuzzy_row(a, true, b, j, T);
-    J.P = fuzzy_row(a, false, b, j, T);
-    J.dL = (float)(log2((double)J.Q.inv_s) - log2((double)J.P.inv_s));
-    const DrawRow &Q = J.Q, &P = J.P;
+    __shared__ JsPair s_J;
+    if (threadIdx.x == 0) {   // the rows' parameters once per block (their float64 parts are not per thread)
+        JsPair J;
+        J.Q = fuzzy_row(a, true, b, j, T);
+        J.P = fuzzy_row(a, false, b, j, T);
+        J.dL = (float)(log2((double)J.Q.inv_s) - log2((double)J.P.inv_s));
+        s_J = J;
+    }
     __syncthreads();
+    const JsPair J = s_J;
+    const DrawRow &Q = J.Q, &P = J.P;
     const int w0 = chunk * a.dv_words, w1 = min(a.n_vec, w0 + a.dv_words);
     const uint4 *vq = reinterpret_cast<const uint4 *>(Q.row);
     const uint4 *vp = reinterpret_cast<const uint4 *>(P.row);

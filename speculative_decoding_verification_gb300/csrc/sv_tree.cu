@@ -69,7 +69,18 @@ struct TreeShared {
     int owner;                 // draw: first segment of this block past u R (kThreads: none)
     int result;
     float2 c_at, c_before;     // draw: cumulative sums at t* and before it (owner block)
+    DrawRow q, p;              // the current node's rows (set by thread 0)
+    int flag;                  // a decision taken by thread 0, read by every thread
 };
+
+// Thread 0's value of v for every thread of the block (decisions carry float64 bounds: one
+// thread evaluates them, the FP64 pipe is narrow on this GPU).
+__device__ __forceinline__ int block_bcast(int v, TreeShared &S) {
+    __syncthreads();
+    if (threadIdx.x == 0) S.flag = v;
+    __syncthreads();
+    return S.flag;
+}
 
 struct TreeCtx {
     cooperative_groups::cluster_group cl;
@@ -162,8 +173,11 @@ __device__ __forceinline__ float tree_R(TreeCtx &X, const DrawRow &Q, const Draw
     });
     const ff R = cluster_sum_ff(X, acc, S);
     // the positive part is 1-Lipschitz: sum_v |dq_v| + c |dp_v| + |dc| p_v, plus the sums
-    err = (base_err(Q) + kTreeKappa * Q.ay) + (double)c * (base_err(P) + kTreeKappa * P.ay) + dc +
-          8.0 * kU32 * (1.0 + (double)c) + 1e-12;
+    // (evaluated by thread 0 only, which takes the decisions)
+    err = 0.0;
+    if (threadIdx.x == 0)
+        err = (base_err(Q) + kTreeKappa * Q.ay) + (double)c * (base_err(P) + kTreeKappa * P.ay) + dc +
+              8.0 * kU32 * (1.0 + (double)c) + 1e-12;
     return R.hi + R.lo;
 }
 
@@ -303,19 +317,23 @@ __device__ __forceinline__ int tree_draw(TreeCtx &X, const DrawRow &Q, const Dra
         c_bf = O->c_before;
     }
     X.cl.sync();   // the owner's results are read before any block moves on
-    const double Xd = ff_to_double(Xu), Rd = ff_to_double(R);
-    const double ca = (double)c_at.x + c_at.y, cb = (double)c_bf.x + c_bf.y;
-    if (owner_rank < 0 || t_star < 0) {   // rounding left u R at or beyond the total
-        certain = false;
-        t_star = -1;
-    } else if (EXACT) {
-        certain = !(fabs(ca - Xd) < 1e-11 * Rd || fabs(Xd - cb) < 1e-11 * Rd);
-    } else {
-        // max(u, 1-u) times the summed per-token errors, the float32 word sums and the scans
-        const double tok = (base_err(Q) + kTreeKappa * Q.ay) + (double)c * (base_err(P) + kTreeKappa * P.ay) + dc;
-        const double E = fmax(u, 1.0 - u) * tok + 8.1 * kU32 * (ca + u * Rd) + 1e-9 * Rd + 1e-30;
-        certain = (ca - Xd) > E && (Xd - cb) > E;
+    int ok = 0;
+    if (threadIdx.x == 0) {
+        const double Xd = ff_to_double(Xu), Rd = ff_to_double(R);
+        const double ca = (double)c_at.x + c_at.y, cb = (double)c_bf.x + c_bf.y;
+        if (owner_rank < 0 || t_star < 0) {   // rounding left u R at or beyond the total
+            ok = 0;
+        } else if (EXACT) {
+            ok = !(fabs(ca - Xd) < 1e-11 * Rd || fabs(Xd - cb) < 1e-11 * Rd);
+        } else {
+            // max(u, 1-u) times the summed per-token errors, the float32 word sums and the scans
+            const double tok = (base_err(Q) + kTreeKappa * Q.ay) + (double)c * (base_err(P) + kTreeKappa * P.ay) + dc;
+            const double E = fmax(u, 1.0 - u) * tok + 8.1 * kU32 * (ca + u * Rd) + 1e-9 * Rd + 1e-30;
+            ok = (ca - Xd) > E && (Xd - cb) > E;
+        }
     }
+    certain = block_bcast(ok, S) != 0;
+    if (owner_rank < 0) t_star = -1;
     return t_star;
 }
 
@@ -417,8 +435,12 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kThreads)
             const char *rowq = a.tgt.base + ((long long)b * a.tgt.rows_per_seq + node) * a.tgt.pitch_bytes;
             const char *rowp = a.drf.base + ((long long)b * a.drf.rows_per_seq + node) * a.drf.pitch_bytes;
             const bool has_children = s_first[node] >= 0;
-            const DrawRow Q = draw_row(rowq, T, a.rowstat[rt], nullptr, nullptr, 1.0f);
-            DrawRow P = has_children ? draw_row(rowp, T, a.rowstat[rd], nullptr, nullptr, 1.0f) : Q;
+            if (threadIdx.x == 0) {
+                S.q = draw_row(rowq, T, a.rowstat[rt], nullptr, nullptr, 1.0f);
+                S.p = has_children ? draw_row(rowp, T, a.rowstat[rd], nullptr, nullptr, 1.0f) : S.q;
+            }
+            __syncthreads();
+            const DrawRow Q = S.q, P = S.p;
             // ---- float32 tier ----
             float c = 0.f, R = 1.f;
             double dc = 0.0, dR = 0.0;
@@ -426,30 +448,37 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kThreads)
             int nxt = -1;
             for (int ch = s_first[node]; ch >= 0 && !exact; ch = s_next[ch]) {
                 ++tests;
-                const int t = s_tok[ch];
-                const double ut = ub[ch];
-                float yq, yp;
-                const float qt = tw(Q, load_elem<ES>(rowq, t), yq), pt = tw(P, load_elem<ES>(rowp, t), yp);
-                const double eq = base_err(Q) + kTreeKappa * fabsf(yq), ep = base_err(P) + kTreeKappa * fabsf(yp);
-                const double num = (double)qt - (double)c * (double)pt;
-                const double lhs = ut * (double)R * (double)pt;
-                const double E = ut * ((double)R * pt * ep + pt * dR) + qt * eq + (double)c * pt * ep + pt * dc +
-                                 4.0 * kU32 * (qt + (double)c * pt + lhs) + 1e-40;
-                const double rhs = fmax(num, 0.0);
-                if (fabs(lhs - rhs) <= E || (pt == 0.f && fabs(num) <= E)) {
+                // the test, by thread 0: 0 reject, 1 accept, 2 too close to call
+                int dec = 0;
+                if (threadIdx.x == 0) {
+                    const int t = s_tok[ch];
+                    const double ut = ub[ch];
+                    float yq, yp;
+                    const float qt = tw(Q, load_elem<ES>(rowq, t), yq), pt = tw(P, load_elem<ES>(rowp, t), yp);
+                    const double eq = base_err(Q) + kTreeKappa * fabsf(yq), ep = base_err(P) + kTreeKappa * fabsf(yp);
+                    const double num = (double)qt - (double)c * (double)pt;
+                    const double lhs = ut * (double)R * (double)pt;
+                    const double E = ut * ((double)R * pt * ep + pt * dR) + qt * eq + (double)c * pt * ep + pt * dc +
+                                     4.0 * kU32 * (qt + (double)c * pt + lhs) + 1e-40;
+                    const double rhs = fmax(num, 0.0);
+                    if (fabs(lhs - rhs) <= E || (pt == 0.f && fabs(num) <= E)) dec = 2;
+                    else dec = lhs < rhs ? 1 : 0;
+                }
+                dec = block_bcast(dec, S);
+                if (dec == 2) {
                     exact = true;
                     break;
                 }
-                if (lhs < rhs) {
+                if (dec == 1) {
                     nxt = ch;
                     break;
                 }
                 // rejected: c <- c + R(c); R <- R(c)
                 const float c_new = c + R;
-                const double dc_new = dc + dR + kU32 * (double)c_new;
+                const double dc_new = threadIdx.x == 0 ? dc + dR + kU32 * (double)c_new : 0.0;
                 double eR;
                 const float R_new = tree_R<ES>(X, Q, P, c_new, dc_new, S, eR);
-                if (!((double)R_new > eR)) {   // cannot tell the residual from empty
+                if (!block_bcast((double)R_new > eR, S)) {   // cannot tell the residual from empty
                     exact = true;
                     break;
                 }

@@ -196,7 +196,7 @@ __device__ __forceinline__ void load_vec(const char *row, int vi, float (&x)[16 
 }
 
 template <int ES>
-__global__ void __launch_bounds__(kThreads) k_exact(const ExactArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) k_exact(const ExactArgs a) {
     constexpr int EPV = 16 / ES;
     __shared__ float2 tab[256];
     __shared__ double s_red[3][kWarps];

@@ -377,6 +377,127 @@ def tree_rates(sv, dev, world, n):
     return out
 
 
+def _timed_calls(call, n, world):
+    """Mean ms of n back-to-back calls on the current stream (5 untimed calls first)."""
+    import torch
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    start.record()
+    for _ in range(n):
+        call()
+    end.record()
+    torch.cuda.synchronize()
+    return max_over_ranks(start.elapsed_time(end) / n, world)
+
+
+def config_rates(sv, dev, world, n):
+    """Rounds/s of the other stated workloads, each as the library calls one round makes (inputs
+    resident; config 2 is in `filters`):
+      1: B=1, K=4, V=32000 f32 — one sv_verify call, launched on the stream and replayed from a
+         CUDA graph of one call (launch-bound);
+      3: SSD / Saguaro, B=16, K=5, V=128256 bf16 — sv_saguaro_sample (sigma_{8,0.3} draft
+         tokens), sv_verify with sigma, sv_cache_keys (fan-out 64), sv_cache_lookup;
+      4: Mirror, B=4, kappa=8, gamma=7, V=151936 bf16 — sv_topk_rows (roots from the early-exit
+         row), sv_verify of branch 0 against the early-exit rows, sv_mirror_reuse."""
+    import torch
+    from synth import workloads as W
+    r = int(os.environ.get("RANK", "0"))
+    out = {}
+    # ---- 1 ----
+    w = W.scaled(W.PLAIN, seed=rank_seed(W.PLAIN.seed, r))
+    tgt, drf = W.logits(w, 0, device=dev)
+    u_draft, u, _ = W.round_uniforms(w, 0)
+    T_d = torch.as_tensor(W.temperatures(w), device=dev)
+    u_d = torch.as_tensor(u, device=dev)
+    toks, _, _ = sv.sv_saguaro_sample(drf, torch.as_tensor(u_draft[:, :w.K].copy(), device=dev), T_d, n_rows=w.K)
+    ws, stats = sv.Workspace(), sv.new_stats(dev)
+    al = torch.empty(w.B, dtype=torch.int32, device=dev)
+    ot = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
+
+    def call1():
+        sv.sv_verify(tgt, drf, toks, u_d, T_d, accept_len=al, out_tokens=ot, stats=stats, workspace=ws)
+    ms = _timed_calls(call1, n, world)
+    c1 = {"workload": w.name, "value": whole_job_rate(1.0, world, ms), "unit": "rounds/s", "us_per_round": ms * 1e3,
+          "steps": n}
+    try:   # one call captured in a CUDA graph, replayed
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            call1()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call1()
+        msg = _timed_calls(g.replay, n, world)
+        c1["graph"] = {"value": whole_job_rate(1.0, world, msg), "unit": "rounds/s", "us_per_round": msg * 1e3}
+    except Exception as e:   # noqa: BLE001 - report, do not fail the bench
+        c1["graph"] = {"unavailable": str(e).splitlines()[0][:160]}
+    if sv.read_stats(stats)["status"] != 0:
+        raise RuntimeError(f"config 1 failed: {sv.read_stats(stats)}")
+    out["plain_b1"] = c1
+    # ---- 3 ----
+    w = W.scaled(W.SAGUARO, seed=rank_seed(W.SAGUARO.seed, r))
+    tgt, drf = W.logits(w, 0, device=dev)
+    u_draft, u, _ = W.round_uniforms(w, 0)
+    T_d = torch.as_tensor(W.temperatures(w), device=dev)
+    u_d = torch.as_tensor(u, device=dev)
+    ud_d = torch.as_tensor(u_draft[:, :w.K].copy(), device=dev)
+    _, f_int = sv.sv_fanout(w.budget, w.accept_rate, w.power_r, w.K)
+    ws, ws2, ws3, stats = sv.Workspace(), sv.Workspace(), sv.Workspace(), sv.new_stats(dev)
+    toks = torch.empty((w.B, w.K), dtype=torch.int32, device=dev)
+    al = torch.empty(w.B, dtype=torch.int32, device=dev)
+    ot = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
+    keys = torch.empty((w.B, int(sum(f_int))), dtype=torch.int32, device=dev)
+    hit = torch.empty(w.B, dtype=torch.uint8, device=dev)
+
+    def call3():
+        sv.sv_saguaro_sample(drf, ud_d, T_d, F=w.saguaro_F, C=w.saguaro_C, n_rows=w.K, tokens=toks, workspace=ws2)
+        sv.sv_verify(tgt, drf, toks, u_d, T_d, saguaro_F=w.saguaro_F, saguaro_C=w.saguaro_C, accept_len=al,
+                     out_tokens=ot, stats=stats, workspace=ws)
+        sv.sv_cache_keys(drf, toks, f_int, keys=keys, workspace=ws3)
+        sv.sv_cache_lookup(al, ot, keys, f_int, hit=hit)
+    ms = _timed_calls(call3, n, world)
+    if sv.read_stats(stats)["status"] != 0:
+        raise RuntimeError(f"config 3 failed: {sv.read_stats(stats)}")
+    out["saguaro_b16"] = {"workload": w.name, "value": whole_job_rate(1.0, world, ms), "unit": "rounds/s",
+                          "us_per_round": ms * 1e3, "steps": n, "calls": "sample, verify, cache keys, lookup"}
+    # ---- 4 ----
+    w = W.scaled(W.MIRROR, seed=rank_seed(W.MIRROR.seed, r))
+    tgt, ee = W.logits(w, 0, device=dev)
+    _, u, u_branch = W.round_uniforms(w, 0)
+    T_d = torch.as_tensor(W.temperatures(w), device=dev)
+    u_d = torch.as_tensor(u, device=dev)
+    kappa, gamma = w.kappa, w.K
+    ee0 = ee[:, 0].contiguous()
+    ids, lps, _ = sv.sv_topk_rows(ee0, kappa, T_d)
+    branches = torch.zeros((w.B, kappa, gamma), dtype=torch.int32, device=dev)
+    branches[:, :, 0] = ids
+    for i in range(kappa):   # deeper branch tokens: draws from the early-exit rows (the draft's job)
+        ub = torch.as_tensor(u_branch[:, i * gamma + 1:(i + 1) * gamma].copy(), device=dev)
+        t_i, _, _ = sv.sv_saguaro_sample(ee[:, 1:].contiguous(), ub, T_d, n_rows=gamma - 1)
+        branches[:, i, 1:] = t_i
+    toks0 = branches[:, 0, :].contiguous()
+    ws, ws2, stats = sv.Workspace(), sv.Workspace(), sv.new_stats(dev)
+    al = torch.empty(w.B, dtype=torch.int32, device=dev)
+    ot = torch.empty((w.B, w.K + 1), dtype=torch.int32, device=dev)
+    reuse = torch.empty(w.B, dtype=torch.uint8, device=dev)
+
+    def call4():
+        sv.sv_topk_rows(ee0, kappa, T_d, ids=ids, logprobs=lps, workspace=ws2)
+        sv.sv_verify(tgt, ee, toks0, u_d, T_d, accept_len=al, out_tokens=ot, stats=stats, workspace=ws)
+        sv.sv_mirror_reuse(branches, al, ot, reuse=reuse)
+    ms = _timed_calls(call4, n, world)
+    if sv.read_stats(stats)["status"] != 0:
+        raise RuntimeError(f"config 4 failed: {sv.read_stats(stats)}")
+    out["mirror_b4"] = {"workload": w.name, "value": whole_job_rate(1.0, world, ms), "unit": "rounds/s",
+                        "us_per_round": ms * 1e3, "steps": n, "calls": "top-kappa roots, verify, reuse"}
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import speculative_decoding_verification_gb300 as sv
@@ -476,6 +597,7 @@ def run_ours(args, rank, world, local_rank):
     line["filters"] = filter_rates(sv, dev, world, min(n, 200))
     line["pyramid"] = pyramid_rates(sv, dev, world, min(n, 200), peak)
     line["tree"] = tree_rates(sv, dev, world, min(n, 200))
+    line["configs"] = config_rates(sv, dev, world, min(n, 200))
     if args.kernel_only:
         return line if rank == 0 else None
 

@@ -149,9 +149,12 @@ extern "C" sv_status sv_cache_keys(const void *draft_logits, int64_t row_pitch, 
     ta.list = list;
     ta.list_x = nullptr;
     ta.list_stride = stride;
-    if (es == 4) k_topn<4><<<(unsigned)ta.n_rows, kThreads, 0, stream>>>(ta);
-    else k_topn<2><<<(unsigned)ta.n_rows, kThreads, 0, stream>>>(ta);
-    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    ta.stats = stats;
+    DeviceInfo di;
+    if (!device_info(di)) return SV_ERR_CUDA;
+    if ((es == 4 ? launch_topn<4>(ta, stride, di.sms, stream) : launch_topn<2>(ta, stride, di.sms, stream)) !=
+        cudaSuccess)
+        return SV_ERR_CUDA;
     ka.list = list;
     ka.stride = stride;
     ka.tokens = draft_tokens;
@@ -236,9 +239,10 @@ extern "C" sv_status sv_topk_rows(const void *logits, int64_t row_pitch, sv_dtyp
     ta.list = reinterpret_cast<int32_t *>(w + tp.off_list);
     ta.list_x = reinterpret_cast<float *>(w + tp.off_list_x);
     ta.list_stride = kappa;
-    if (es == 4) k_topn<4><<<(unsigned)n_rows, kThreads, 0, stream>>>(ta);
-    else k_topn<2><<<(unsigned)n_rows, kThreads, 0, stream>>>(ta);
-    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    ta.stats = stats;
+    if ((es == 4 ? launch_topn<4>(ta, kappa, di.sms, stream) : launch_topn<2>(ta, kappa, di.sms, stream)) !=
+        cudaSuccess)
+        return SV_ERR_CUDA;
     TopKArgs ka{};
     ka.list = ta.list;
     ka.list_x = ta.list_x;

@@ -216,6 +216,7 @@ struct TopNArgs {
     int32_t *list;          // [row][list_stride] sorted ids (output)
     float *list_x;          // [row][list_stride] their logits (output, may be null)
     int list_stride;
+    sv_stats *stats;        // timeouts of the cluster path (may be null)
 };
 
 template <int ES>
@@ -266,6 +267,420 @@ __global__ void __launch_bounds__(kThreads) k_topn(const TopNArgs a) {
         __threadfence_block();
         for (int i = threadIdx.x; i < N; i += blockDim.x) a.list_x[(size_t)r * a.list_stride + i] = load_elem<ES>(row, out[i]);
     }
+}
+
+// ------------------------------------------------------------------------------------------
+// Top-N of one row by a cluster of S <= 8 blocks (N <= kTopNFast).
+//
+// Elements are ranked by a 64-bit code: the order key above the complemented id, so that codes
+// are distinct and larger codes come first in (key desc, id asc) order.  Each block streams its
+// contiguous share of the row through a ring of bulk copies; in a first pass every thread keeps
+// the largest code of the vectors it sees.  The N-th largest of any N of those maxima is a
+// lower bound tau on the row's N-th largest code (N distinct elements reach it), so the row's
+// first N are all among the codes >= tau.  A second pass over the share (from the ring when
+// the share fits in it, else streamed again) collects those candidates, skipping every vector
+// whose largest key is below tau's; each block ranks its candidates, and its first N go to
+// block 0, which ranks the union: an element of the row's first N has all elements above it in
+// the union, so its rank there is its rank in the row.  A block whose candidates overflow
+// kTopNCand marks the row, and block 0 then takes it alone by the radix select.
+// ------------------------------------------------------------------------------------------
+constexpr int kTopNFast = 128;            // largest N of the cluster path
+constexpr int kTopNCluster = 8;           // largest cluster
+constexpr int kTopNCand = kMaxTopN;       // candidates one block holds
+constexpr int kTopNStageVecs = 1024;      // 16-byte vectors per stage of the bulk-copy ring
+constexpr int kTopNStages = 4;
+constexpr size_t kTopNRingBytes = (size_t)kTopNStages * kTopNStageVecs * 16;   // dynamic shared memory
+static_assert(kTopNFast <= kThreads, "one thread per rank of the block's maxima");
+
+__device__ __forceinline__ uint64_t rank_code(uint32_t key, int id) {
+    return ((uint64_t)key << 32) | (uint64_t)(~(uint32_t)id);
+}
+__device__ __forceinline__ uint32_t code_key(uint64_t c) { return (uint32_t)(c >> 32); }
+__device__ __forceinline__ int code_id(uint64_t c) { return (int)(~(uint32_t)c); }
+
+struct TopNCl {
+    uint64_t cand[kTopNCand];                  // this block's candidates (radix path: keys, ids)
+    uint64_t gath[kTopNCluster * kTopNFast];   // block 0: block q's sorted first N at q * N
+    uint64_t res[kTopNFast];                   // block 0: the row's first N, sorted
+    uint64_t mx[kThreads];
+    uint64_t taus[kTopNCluster];               // block q's bound, written by block q
+    uint64_t tau_b;
+    uint64_t bar[kTopNStages];                 // ring stages
+    int n_top[kTopNCluster], over[kTopNCluster];
+    int n_cand, fail;
+    uint32_t nth_key;                          // block 0: the row's N-th element
+    int nth_id;
+    unsigned hist[256];                        // radix path
+    int dig[2], warp_tot[kWarps], last, cnt;
+};
+
+// Elements g, g + G, ... of the row in 16-byte vectors (four loads in flight per thread), then
+// the scalar tail.
+template <int ES, class Fn>
+__device__ __forceinline__ void for_strided(const char *row, int V, int g, int G, Fn fn) {
+    constexpr int EPV = 16 / ES;
+    const int n_vec = (V * ES) / 16;
+    const uint4 *p = reinterpret_cast<const uint4 *>(row);
+    int vi = g;
+    for (; vi + 3 * G < n_vec; vi += 4 * G) {
+        uint4 w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) w[u] = __ldg(p + vi + u * G);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float x[EPV];
+            unpack<ES>(w[u], x);
+#pragma unroll
+            for (int k = 0; k < EPV; ++k) fn(x[k], (vi + u * G) * EPV + k);
+        }
+    }
+    for (; vi < n_vec; vi += G) {
+        float x[EPV];
+        unpack<ES>(__ldg(p + vi), x);
+#pragma unroll
+        for (int k = 0; k < EPV; ++k) fn(x[k], vi * EPV + k);
+    }
+    for (int v = n_vec * EPV + g; v < V; v += G) fn(load_elem<ES>(row, v), v);
+}
+
+// The largest order key of a 16-byte vector, or above it: the maximum propagates NaN (whose
+// canonical pattern has the largest key of its sign), and -0 and +0 share a key.
+template <int ES>
+__device__ __forceinline__ uint32_t vec_max_key(uint4 w) {
+    if constexpr (ES == 2) {
+        uint32_t m = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+        m = bmax2(m, __byte_perm(m, 0u, 0x1032));
+        return f32_key(bf16_lo(m));
+    } else {
+        float a, b;
+        asm("max.NaN.f32 %0, %1, %2;" : "=f"(a) : "f"(__uint_as_float(w.x)), "f"(__uint_as_float(w.y)));
+        asm("max.NaN.f32 %0, %1, %2;" : "=f"(b) : "f"(__uint_as_float(w.z)), "f"(__uint_as_float(w.w)));
+        asm("max.NaN.f32 %0, %1, %2;" : "=f"(a) : "f"(a), "f"(b));
+        return f32_key(a);
+    }
+}
+
+// The 32 values of a warp in descending order across lanes (bitonic network).
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, v, j);
+            const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+            v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
+        }
+    return v;
+}
+
+// Rank of (k, id) among n (key, id) pairs in (key desc, id asc) order.
+__device__ __forceinline__ int pair_rank(const uint32_t *keys, const int *ids, int n, uint32_t k, int id) {
+    int r = 0;
+    for (int j = 0; j < n; ++j) {
+        const uint32_t o = keys[j];
+        r += (o > k || (o == k && ids[j] < id)) ? 1 : 0;
+    }
+    return r;
+}
+
+// Single-block radix select: the N-th element into nth_key / nth_id and, in list mode
+// (N <= kTopNFast), the sorted first N as codes in res.
+template <int ES>
+__device__ void topn_exact_block(const char *row, int V, int N, bool list, TopNCl &s) {
+    uint32_t *xkey = reinterpret_cast<uint32_t *>(s.cand);
+    int *xid = reinterpret_cast<int *>(s.cand) + kTopNCand;
+    int *tie = reinterpret_cast<int *>(s.gath);
+    int n_above;
+    const uint32_t kstar = radix_select_count<ES>(row, V, N, n_above, s.hist, s.dig);
+    if (!list) {
+        const int last = ordered_ties<ES>(row, V, kstar, N - n_above, nullptr, s.warp_tot, &s.last);
+        if (threadIdx.x == 0) {
+            s.nth_key = kstar;
+            s.nth_id = last;
+        }
+        __syncthreads();
+        return;
+    }
+    if (threadIdx.x == 0) s.cnt = 0;
+    __syncthreads();
+    for_each_elem<ES>(row, V, [&](float x, int v) {
+        const uint32_t k = f32_key(x);
+        if (k > kstar) {
+            const int slot = atomicAdd(&s.cnt, 1);
+            if (slot < kTopNCand) {
+                xkey[slot] = k;
+                xid[slot] = v;
+            }
+        }
+    });
+    __syncthreads();
+    const int na = min(s.cnt, kTopNCand);   // = n_above < N
+    for (int i = threadIdx.x; i < na; i += blockDim.x)
+        s.res[pair_rank(xkey, xid, na, xkey[i], xid[i])] = rank_code(xkey[i], xid[i]);
+    ordered_ties<ES>(row, V, kstar, N - na, tie, s.warp_tot, &s.last);
+    for (int i = threadIdx.x; i < N - na; i += blockDim.x) s.res[na + i] = rank_code(kstar, tie[i]);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        s.nth_key = code_key(s.res[N - 1]);
+        s.nth_id = code_id(s.res[N - 1]);
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+// The cluster part of the top-N of one row, called by every block of the cluster (1 <= N <=
+// min(V, kTopNFast)).  Block `rank` takes the contiguous share [v0, v1) of the row's 16-byte
+// vectors, streamed by bulk copies through `ring` (kTopNRingBytes of dynamic shared memory); its
+// thread tid sees vectors v0 + tid + k kThreads, in increasing order.  `each_vec(w, vi)` sees
+// every vector of the share once and `each_elem(x, v)` every scalar-tail element; `publish()`
+// runs in every block just before the last barrier (to write per-block results into block 0).
+// Returns true in block 0 when the row needs the radix path (a block's candidates overflowed);
+// otherwise block 0 holds the row's first N in res and the N-th element in nth_key / nth_id.
+// Other blocks return false and must not touch block 0 after.  s.fail is set in a block whose
+// copies did not arrive in time (its results are then meaningless; the caller reports it).
+template <int ES, class EachVec, class EachElem, class Publish>
+__device__ bool cluster_topn(const cooperative_groups::cluster_group &cl, const char *row, int V, int N, TopNCl &s,
+                             char *ring, long long wait_limit, EachVec each_vec, EachElem each_elem,
+                             Publish publish) {
+    constexpr int EPV = 16 / ES;
+    const int S = (int)cl.num_blocks(), rank = (int)cl.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int g = rank * kThreads + tid, G = S * kThreads;
+    const int n_vec = (V * ES) / 16;
+    const int per = (n_vec + S - 1) / S;
+    const int v0 = min(rank * per, n_vec), v1 = min(v0 + per, n_vec);
+    const int n_chunks = (v1 - v0 + kTopNStageVecs - 1) / kTopNStageVecs;
+    // the ring carries chunk j of the sequence: the share once (j < n_chunks) and, unless the
+    // whole share stays in the ring, once more for the second pass (chunk j - n_chunks)
+    const bool resident = n_chunks <= kTopNStages;
+    const int total = resident ? n_chunks : 2 * n_chunks;
+    auto chunk_vecs = [&](int c) { return min(kTopNStageVecs, v1 - v0 - c * kTopNStageVecs); };
+    auto issue = [&](int j) {   // thread 0
+        const int c = j < n_chunks ? j : j - n_chunks, st = j % kTopNStages;
+        const uint32_t bytes = (uint32_t)chunk_vecs(c) * 16u;
+        mbar_arrive_expect_tx(&s.bar[st], bytes);
+        bulk_load(ring + (size_t)st * kTopNStageVecs * 16, row + (size_t)(v0 + c * kTopNStageVecs) * 16, bytes,
+                  &s.bar[st]);
+    };
+    cluster_arrive_relaxed();   // completes once every block has started (before any DSMEM access)
+    if (tid == 0) {
+        s.tau_b = 0ull;
+        s.n_cand = 0;
+        s.fail = 0;
+        for (int i = 0; i < kTopNStages; ++i) mbar_init(&s.bar[i], 1);
+        fence_barrier_init();
+        for (int j = 0; j < min(kTopNStages, total); ++j) issue(j);
+    }
+    __syncthreads();
+    // consumes ring chunks j0 .. j1-1 with fn(w, vi); refills each stage once every thread is
+    // done with it.  A copy late beyond wait_limit ends the streaming (s.fail) after the copies
+    // still in flight have landed (bounded).
+    bool failed = false;
+    auto stream = [&](int j0, int j1, auto fn) {
+        if (failed) return;
+        for (int j = j0; j < j1; ++j) {
+            const int st = j % kTopNStages, c = j < n_chunks ? j : j - n_chunks;
+            const bool ok = mbar_wait_bounded(&s.bar[st], (uint32_t)(j / kTopNStages) & 1u, wait_limit);
+            if (ok) {
+                const int nv = chunk_vecs(c);
+                const char *base = ring + (size_t)st * kTopNStageVecs * 16;
+                for (int i = tid; i < nv; i += kThreads) fn(lds128(base + i * 16), v0 + c * kTopNStageVecs + i);
+            }
+            if (__syncthreads_or(!ok)) {
+                const int issued = min(j + kTopNStages, total);
+                for (int d = j; d < issued; ++d)
+                    mbar_wait_bounded(&s.bar[d % kTopNStages], (uint32_t)(d / kTopNStages) & 1u, wait_limit);
+                if (tid == 0) s.fail = 1;
+                failed = true;
+                return;
+            }
+            if (tid == 0 && j + kTopNStages < total) issue(j + kTopNStages);
+        }
+    };
+    // ---- pass 1: each thread's largest code ----
+    uint32_t mk = 0u;   // largest key seen and the first id holding it (mk = 0: none yet)
+    int mi = 0x7FFFFFFF;
+    auto see = [&](uint32_t k, int v) {
+        if (k > mk || (k == mk && v < mi)) {
+            mk = k;
+            mi = v;
+        }
+    };
+    stream(0, n_chunks, [&](uint4 w, int vi) {
+        each_vec(w, vi);
+        if (vec_max_key<ES>(w) >= mk) {   // a new maximum may be here: the exact keys, in order
+            float x[EPV];
+            unpack<ES>(w, x);
+#pragma unroll
+            for (int k = 0; k < EPV; ++k) see(f32_key(x[k]), vi * EPV + k);
+        }
+    });
+    for (int v = n_vec * EPV + g; v < V; v += G) {
+        const float x = load_elem<ES>(row, v);
+        each_elem(x, v);
+        see(f32_key(x), v);
+    }
+    const uint64_t m = mi == 0x7FFFFFFF ? 0ull : rank_code(mk, mi);   // 0: no element
+    if (N <= 32) {
+        const uint64_t w = __shfl_sync(0xFFFFFFFFu, warp_sort_desc(m), N - 1);
+        if (lane == 0) atomicMax(reinterpret_cast<unsigned long long *>(&s.tau_b), (unsigned long long)w);
+    } else {
+        s.mx[tid] = m;
+        __syncthreads();
+        int r = 0;
+        for (int j = 0; j < kThreads; ++j) r += s.mx[j] > m ? 1 : 0;
+        if (r == N - 1) s.tau_b = m;
+    }
+    __syncthreads();
+    cluster_wait();
+    if (tid < S) *cl.map_shared_rank(&s.taus[rank], tid) = s.tau_b;
+    cl.sync();   // (1) every block's bound is in every block
+    uint64_t tau = 0ull;
+    for (int q = 0; q < S; ++q) tau = s.taus[q] > tau ? s.taus[q] : tau;
+    // ---- pass 2: the codes >= tau ----
+    const uint32_t tau_key = code_key(tau);
+    auto add = [&](uint64_t c) {
+        const int slot = atomicAdd(&s.n_cand, 1);
+        if (slot < kTopNCand) s.cand[slot] = c;
+    };
+    auto collect = [&](uint4 w, int vi) {
+        if (vec_max_key<ES>(w) < tau_key) return;
+        float x[EPV];
+        unpack<ES>(w, x);
+#pragma unroll
+        for (int k = 0; k < EPV; ++k) {
+            const uint64_t c = rank_code(f32_key(x[k]), vi * EPV + k);
+            if (c >= tau) add(c);
+        }
+    };
+    if (resident) {
+        if (!failed)
+            for (int c = 0; c < n_chunks; ++c) {
+                const char *base = ring + (size_t)c * kTopNStageVecs * 16;
+                const int nv = chunk_vecs(c);
+                for (int i = tid; i < nv; i += kThreads) collect(lds128(base + i * 16), v0 + c * kTopNStageVecs + i);
+            }
+    } else {
+        stream(n_chunks, total, collect);
+    }
+    for (int v = n_vec * EPV + g; v < V; v += G) {
+        const uint64_t c = rank_code(f32_key(load_elem<ES>(row, v)), v);
+        if (c >= tau) add(c);
+    }
+    __syncthreads();
+    const int nc = s.n_cand;
+    if (nc <= kTopNCand) {
+        uint64_t *dst = cl.map_shared_rank(s.gath, 0) + rank * N;
+        for (int i = tid; i < nc; i += kThreads) {
+            const uint64_t c = s.cand[i];
+            int r = 0;
+#pragma unroll 8
+            for (int j = 0; j < nc; ++j) r += s.cand[j] > c ? 1 : 0;
+            if (r < N) dst[r] = c;
+        }
+    }
+    if (tid == 0) {
+        *cl.map_shared_rank(&s.n_top[rank], 0) = min(nc, N);
+        *cl.map_shared_rank(&s.over[rank], 0) = nc > kTopNCand ? 1 : 0;
+    }
+    publish();
+    cl.sync();   // (2) every block's list and results are in block 0
+    if (rank != 0) return false;
+    int over = 0;
+    for (int q = 0; q < S; ++q) over |= s.over[q];
+    if (over) return true;
+    for (int idx = tid; idx < S * N; idx += kThreads) {
+        const int q = idx / N, i = idx - q * N;
+        if (i >= s.n_top[q]) continue;
+        const uint64_t c = s.gath[idx];
+        int r = 0;
+        for (int q2 = 0; q2 < S; ++q2) {
+            const uint64_t *l = s.gath + q2 * N;
+            const int n = s.n_top[q2];
+            for (int j = 0; j < n; ++j) r += l[j] > c ? 1 : 0;
+        }
+        if (r < N) s.res[r] = c;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        s.nth_key = code_key(s.res[N - 1]);
+        s.nth_id = code_id(s.res[N - 1]);
+    }
+    __syncthreads();
+    return false;
+}
+
+// Top-N lists by clusters: cluster c of the grid takes row c.
+template <int ES>
+__global__ void __launch_bounds__(kThreads) k_topn_cl(const TopNArgs a) {
+    __shared__ TopNCl s;
+    extern __shared__ __align__(128) char ring[];
+    const cooperative_groups::cluster_group cl = cooperative_groups::this_cluster();
+    const long long r = blockIdx.x / cl.num_blocks();
+    if (r >= a.n_rows) return;
+    const long long b = r / a.rows_used, j = r - b * a.rows_used;
+    const char *row = a.base + (b * a.rows_per_seq + j) * a.pitch_bytes;
+    int N = a.n_all > 0 ? a.n_all : a.n_of_j[j];
+    if (N > a.V) N = a.V;
+    if (N <= 0) return;   // the same in every block of the cluster
+    const bool radix = cluster_topn<ES>(cl, row, a.V, N, s, ring, kWaitLimitCycles, [](uint4, int) {},
+                                        [](float, int) {}, [] {});
+    if (s.fail && threadIdx.x == 0) report_error(a.stats, SV_ERR_TIMEOUT, (int)r);
+    if (cl.block_rank() != 0) return;
+    if (radix) topn_exact_block<ES>(row, a.V, N, true, s);
+    int32_t *out = a.list + (size_t)r * a.list_stride;
+    for (int i = threadIdx.x; i < N; i += blockDim.x) {
+        const int id = code_id(s.res[i]);
+        out[i] = id;
+        if (a.list_x) a.list_x[(size_t)r * a.list_stride + i] = load_elem<ES>(row, id);
+    }
+}
+
+// Cluster size for n_rows rows: a block for every SM when the rows are few (each block streams
+// its share through a 64 KB ring, two blocks to an SM), at most kTopNCluster per row.
+inline int topn_cluster_size(long long n_rows, int sms) {
+    int S = 1;
+    while (S < kTopNCluster && n_rows * S < sms) S *= 2;
+    return S;
+}
+
+// Launch of a row-per-cluster kernel: grid = n_rows * S blocks, clusters of S.
+template <class Args>
+cudaError_t launch_row_clusters(void (*kern)(Args), const Args &args, long long n_rows, int S, size_t smem,
+                                cudaStream_t stream) {
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(n_rows * S));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
+// Top-N lists of TopNArgs rows: the cluster path when every N fits it, else one block per row.
+template <int ES>
+cudaError_t launch_topn(const TopNArgs &ta, int max_n, int sms, cudaStream_t stream) {
+    if (ta.n_rows < 1) return cudaSuccess;
+    if (max_n <= kTopNFast)
+        return launch_row_clusters(k_topn_cl<ES>, ta, ta.n_rows, topn_cluster_size(ta.n_rows, sms), kTopNRingBytes,
+                                   stream);
+    k_topn<ES><<<(unsigned)ta.n_rows, kThreads, 0, stream>>>(ta);
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1164,13 +1579,46 @@ struct TopSetArgs {
     sv_stats *stats;
 };
 
+// Masses of the kept tokens inside and outside D (the elements at or above (xstar, last) in
+// (logit desc, id asc) order), by one block over the whole row: (E, A, count) of each side.
+template <int ES, class Kept, class Mass>
+__device__ void topset_split_block(const char *row, int V, float xstar, int last, Kept kept, Mass mass, double *s_red,
+                                   double3 &t_in, double3 &t_out) {
+    ff e_in = {0.f, 0.f}, e_out = {0.f, 0.f};
+    float a_in = 0.f, a_out = 0.f;
+    int n_in = 0, n_out = 0;
+    for_strided<ES>(row, V, threadIdx.x, kThreads, [&](float x, int v) {
+        if (!kept(x, v)) return;
+        float y;
+        const float e = mass(x, y);
+        if (x > xstar || (x == xstar && v <= last)) {
+            e_in = ff_add_f(e_in, e);
+            a_in += e * fabsf(y);
+            ++n_in;
+        } else {
+            e_out = ff_add_f(e_out, e);
+            a_out += e * fabsf(y);
+            ++n_out;
+        }
+    });
+    t_in = block_sum_d3(ff_to_double(e_in), (double)a_in, (double)n_in, s_red);
+    t_out = block_sum_d3(ff_to_double(e_out), (double)a_out, (double)n_out, s_red);
+}
+
+// One cluster per row.  The pass of the cluster top-N also sums, per block, the masses of the
+// kept tokens (float-float per thread); block 0 takes the F-th element, the masses of the first
+// F from its list, and the rest as the row total less those (or, when a block's candidates
+// overflowed or that difference is too small to trust, one pass of its own over the row).
 template <int ES>
 __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
-    __shared__ unsigned hist[256];
-    __shared__ int s_dig[2], s_warp[kWarps], s_last;
+    __shared__ TopNCl s;
+    extern __shared__ __align__(128) char ring[];
     __shared__ double s_red[3 * kWarps];
     __shared__ RowStat s_rs;
-    const long long lr = blockIdx.x;
+    __shared__ double s_tot[kTopNCluster][4];   // block 0: each block's (E, A, count) of kept tokens
+    const cooperative_groups::cluster_group cl = cooperative_groups::this_cluster();
+    const int S = (int)cl.num_blocks(), rank = (int)cl.block_rank();
+    const long long lr = blockIdx.x / S;
     if (lr >= a.n_rows) return;
     const long long rid = a.rid0 + lr;
     const long long b = lr / a.rows.rows_used, j = lr - b * a.rows.rows_used;
@@ -1184,7 +1632,7 @@ __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
     none.z_f = 1.0f;
     none.z_err_f = 0.0f;
     if (!(T >= 1e-3f && T <= 1e3f)) {   // greedy or invalid: no transform
-        if (threadIdx.x == 0) a.top[rid] = none;
+        if (threadIdx.x == 0 && rank == 0) a.top[rid] = none;
         return;
     }
     const char *row = a.rows.base + (b * a.rows.rows_per_seq + j) * a.rows.pitch_bytes;
@@ -1194,16 +1642,11 @@ __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
     }
     __syncthreads();
     const RowStat st = s_rs;
-    if (!rs_sampled_ok(st) || st.flags) {
-        if (threadIdx.x == 0) a.top[rid] = none;
+    if (!rs_sampled_ok(st) || st.flags) {   // the same in every block of the cluster
+        if (threadIdx.x == 0 && rank == 0) a.top[rid] = none;
         return;
     }
     const int N = min(a.F, a.V);
-    int n_above;
-    const uint32_t kstar = radix_select_count<ES>(row, a.V, N, n_above, hist, s_dig);
-    const int last = ordered_ties<ES>(row, a.V, kstar, N - n_above, nullptr, s_warp, &s_last);
-    const float xstar = key_value(kstar);
-    // masses inside and outside D among the tokens the top-k / top-p filters keep
     float c_hi, c_lo;
     log2e_over(T, c_hi, c_lo);
     const float rf = (float)st.r;
@@ -1213,59 +1656,152 @@ __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
         cut_x = a.nuc[rid].cut_x;
         cut_id = a.nuc[rid].cut_id;
     }
-    double e_in = 0.0, e_out = 0.0, a_in = 0.0, a_out = 0.0;
-    int n_out = 0;
-    for_each_elem<ES>(row, a.V, [&](float x, int v) {
-        if (x == -INFINITY || !(x > cut_x || (x == cut_x && v <= cut_id))) return;
-        const float y = fmaf(x, c_lo, fmaf(x, c_hi, -rf));
-        const float e = ex2_fast(y);
-        if (x > xstar || (x == xstar && v <= last)) {
-            e_in += (double)e;
-            a_in += (double)(e * fabsf(y));
+    // tokens the top-k / top-p filters keep, and their float32 masses 2^y, y = x c - r
+    auto kept = [&](float x, int v) { return x != -INFINITY && (x > cut_x || (x == cut_x && v <= cut_id)); };
+    auto mass = [&](float x, float &y) {
+        y = fmaf(x, c_lo, fmaf(x, c_hi, -rf));
+        return ex2_fast(y);
+    };
+    double3 t_in, t_out;
+    float xstar;
+    int last;
+    bool direct = true;
+    double sub_err = 0.0;   // absolute error of an outside mass taken as a difference
+    if (N > kTopNFast) {   // a single-block cluster (the launch sees to it): radix select, split pass
+        topn_exact_block<ES>(row, a.V, N, false, s);
+        xstar = key_value(s.nth_key);
+        last = s.nth_id;
+        topset_split_block<ES>(row, a.V, xstar, last, kept, mass, s_red, t_in, t_out);
+    } else {
+        // rows under a top-k / top-p cut sum their kept masses in the pass; the others take the
+        // row total S from the statistics pass (the same masses, with a certified bound)
+        const bool filtered = a.nuc != nullptr && !(cut_x == -INFINITY && cut_id == 0x7FFFFFFF);
+        ff e_t = {0.f, 0.f};
+        float a_t = 0.f;
+        int n_t = 0;
+        auto add_mass = [&](float x, int v) {
+            if (!kept(x, v)) return;
+            float y;
+            const float e = mass(x, y);
+            e_t = ff_add_f(e_t, e);
+            a_t = fmaf(e, fabsf(y), a_t);
+            ++n_t;
+        };
+        const bool radix = cluster_topn<ES>(
+            cl, row, a.V, N, s, ring, kWaitLimitCycles,
+            [&](uint4 w, int vi) {
+                if (!filtered) return;
+                float x[16 / ES];
+                unpack<ES>(w, x);
+#pragma unroll
+                for (int k = 0; k < 16 / ES; ++k) add_mass(x[k], vi * (16 / ES) + k);
+            },
+            [&](float x, int v) {
+                if (filtered) add_mass(x, v);
+            },
+            [&] {
+                if (!filtered) return;
+                const double3 t = block_sum_d3(ff_to_double(e_t), (double)a_t, (double)n_t, s_red);
+                if (threadIdx.x == 0) {
+                    double *d = cl.map_shared_rank(&s_tot[0][0], 0) + 4 * rank;
+                    d[0] = t.x;
+                    d[1] = t.y;
+                    d[2] = t.z;
+                }
+            });
+        if (s.fail && threadIdx.x == 0) report_error(a.stats, SV_ERR_TIMEOUT, (int)b);
+        if (rank != 0) return;
+        if (radix) topn_exact_block<ES>(row, a.V, N, false, s);
+        xstar = key_value(s.nth_key);
+        last = s.nth_id;
+        if (radix) {
+            topset_split_block<ES>(row, a.V, xstar, last, kept, mass, s_red, t_in, t_out);
         } else {
-            e_out += (double)e;
-            a_out += (double)(e * fabsf(y));
-            ++n_out;
+            double e_i = 0.0, a_i = 0.0, n_i = 0.0;
+            if (threadIdx.x < N) {
+                const uint64_t c = s.res[threadIdx.x];
+                const float x = key_value(code_key(c));
+                const int v = code_id(c);
+                if (kept(x, v)) {
+                    float y;
+                    const float e = mass(x, y);
+                    e_i = (double)e;
+                    a_i = (double)(e * fabsf(y));
+                    n_i = 1.0;
+                }
+            }
+            t_in = block_sum_d3(e_i, a_i, n_i, s_red);
+            direct = false;
+            bool trust;
+            if (filtered) {
+                double E = 0.0, A = 0.0, n = 0.0;
+                for (int q = 0; q < S; ++q) {
+                    E += s_tot[q][0];
+                    A += s_tot[q][1];
+                    n += s_tot[q][2];
+                }
+                // E - E_in: the masses of D cancel exactly (the same float32 values on both
+                // sides); each float-float addition errs by at most 2^-47 of its sum, so a
+                // thread's share of n elements leaves at most n 2^-47 E.  A enters the bound only.
+                t_out.x = E - t_in.x;
+                t_out.y = fmax(A - t_in.y, 0.0) + 1e-4 * A;
+                t_out.z = n - t_in.z;
+                if (t_out.z == 0.0) t_out.x = t_out.y = 0.0;   // nothing kept outside D
+                const double r_rel = (double)(a.V / (S * kThreads) + 16) * 0x1p-46;
+                sub_err = r_rel * E;
+                trust = t_out.z == 0.0 || t_out.x > 0x1p17 * sub_err;
+            } else {
+                // S - E_in, off by at most err S + r_in E_in; A S bounds the outside sum of e |y|
+                const double Srow = (double)st.s_hi + (double)st.s_lo;
+                const double r_in = kEx2RelErr + 1.02 * kYRound * (t_in.x > 0.0 ? t_in.y / t_in.x : 0.0) + 4.0 * kU32;
+                t_out.x = Srow - t_in.x;
+                t_out.y = 1.01 * (double)st.ay * Srow + 1e-30;
+                t_out.z = 1.0;   // a positive outside mass (checked below) means a kept token outside D
+                sub_err = (double)st.err * Srow + r_in * t_in.x;
+                trust = t_out.x > 16.0 * sub_err && t_out.x > 0x1p-4 * Srow;
+            }
+            if (!trust) {   // too small to take as a difference
+                topset_split_block<ES>(row, a.V, xstar, last, kept, mass, s_red, t_in, t_out);
+                direct = true;
+            }
         }
-    });
-    const double3 t_in = block_sum_d3(e_in, a_in, (double)n_out, s_red);
-    const double3 t_out = block_sum_d3(e_out, a_out, 0.0, s_red);
-    if (threadIdx.x == 0) {
-        const double C = (double)a.C, Ein = t_in.x, Eout = t_out.x;
-        const double num = C * Ein + Eout, den = Ein + Eout;
-        TopSet t = none;
-        if (C == 0.0 && t_in.z == 0.0) {
-            // every kept token lies in D and C = 0: no transform (the row is used unchanged)
-            t.p_d = 1.0;
-        } else if (!(num > 0.0)) {
-            // the mass left outside D underflows float32: no transform, reported as unresolved
-            stats_add(a.stats, &a.stats->unresolved, 1);
-        } else {
-            t.top_x = xstar;
-            t.top_id = last;
-            t.p_d = Ein / den;
-            t.z = num / den;
-            // each part is a sum of float32 masses: relative error kEx2RelErr + ln2 u |y| per
-            // token (A / E is the mass-weighted mean |y|) plus rounding; masses that flush to
-            // zero below 2^-126 are at most V 2^-126 in all
-            const double r_in = kEx2RelErr + 1.02 * kYRound * (Ein > 0.0 ? t_in.y / Ein : 0.0) + 4.0 * kU32;
-            const double r_out = kEx2RelErr + 1.02 * kYRound * (Eout > 0.0 ? t_out.y / Eout : 0.0) + 4.0 * kU32;
-            const double uf = (double)a.V * 0x1p-126;
-            const double rel_num = (C * Ein * r_in + Eout * r_out + uf) / num;
-            const double rel_den = (Ein * r_in + Eout * r_out + uf) / den;
-            t.z_err = rel_num + rel_den + 1e-12;
-            t.z_f = (float)t.z;
-            t.z_err_f = (float)t.z_err * (1.0f + 0x1p-20f);
-        }
-        a.top[rid] = t;
     }
+    if (threadIdx.x != 0) return;
+    const double C = (double)a.C, Ein = t_in.x, Eout = t_out.x;
+    const double num = C * Ein + Eout, den = Ein + Eout;
+    TopSet t = none;
+    if (C == 0.0 && t_out.z == 0.0) {
+        // every kept token lies in D and C = 0: no transform (the row is used unchanged)
+        t.p_d = 1.0;
+    } else if (!(num > 0.0)) {
+        // the mass left outside D underflows float32: no transform, reported as unresolved
+        stats_add(a.stats, &a.stats->unresolved, 1);
+    } else {
+        t.top_x = xstar;
+        t.top_id = last;
+        t.p_d = Ein / den;
+        t.z = num / den;
+        // each part is a sum of float32 masses: relative error kEx2RelErr + ln2 u |y| per token
+        // (A / E is the mass-weighted mean |y|; the float32 sums of e |y| are within 1% of it)
+        // plus rounding; masses that flush to zero below 2^-126 are at most V 2^-126 in all; an
+        // outside mass taken as a difference adds its own error sub_err
+        const double r_in = kEx2RelErr + 1.02 * kYRound * (Ein > 0.0 ? t_in.y / Ein : 0.0) + 4.0 * kU32;
+        const double r_out = kEx2RelErr + 1.02 * kYRound * (Eout > 0.0 ? t_out.y / Eout : 0.0) + 4.0 * kU32 +
+                             (direct || !(Eout > 0.0) ? 0.0 : sub_err / Eout);
+        const double uf = (double)a.V * 0x1p-126;
+        const double rel_num = (C * Ein * r_in + Eout * r_out + uf) / num;
+        const double rel_den = (Ein * r_in + Eout * r_out + uf) / den;
+        t.z_err = rel_num + rel_den + 1e-12;
+        t.z_f = (float)t.z;
+        t.z_err_f = (float)t.z_err * (1.0f + 0x1p-20f);
+    }
+    a.top[rid] = t;
 }
 
 template <int ES>
 sv_status launch_topset(const RowSet &drf, long long rid0, int B, int rows_used, int V, const float *temperature,
                         int F, float C, const WarpPartial *part, int n_split, const NucleusCut *nuc, TopSet *top,
                         sv_stats *stats, const DeviceInfo &di, cudaStream_t stream) {
-    (void)di;
     TopSetArgs a;
     a.rows = drf;
     a.rows.rows_used = rows_used;
@@ -1281,8 +1817,8 @@ sv_status launch_topset(const RowSet &drf, long long rid0, int B, int rows_used,
     a.top = top;
     a.stats = stats;
     if (a.n_rows < 1) return SV_OK;
-    k_topset<ES><<<(unsigned)a.n_rows, kThreads, 0, stream>>>(a);
-    return cuda_status(cudaGetLastError());
+    const int S = F > kTopNFast ? 1 : topn_cluster_size(a.n_rows, di.sms);
+    return cuda_status(launch_row_clusters(k_topset<ES>, a, a.n_rows, S, kTopNRingBytes, stream));
 }
 
 }  // namespace sv

@@ -149,7 +149,7 @@ def test_top_k_on_the_lazy_and_static_entry_points():
 # --------------------------------------------------------------------------------------
 # Saguaro: verification with p' and the draft sampler
 # --------------------------------------------------------------------------------------
-@pytest.mark.parametrize("F,C", [(8, 0.3), (8, 0.0), (1, 0.5), (300, 0.1)])
+@pytest.mark.parametrize("F,C", [(8, 0.3), (8, 0.0), (1, 0.5), (100, 0.5), (300, 0.1)])
 def test_saguaro_verify_parity(F, C):
     w = W.scaled(W.SAGUARO, B=16, saguaro_F=F, saguaro_C=C)
     inp = make_inputs(w, 0)
@@ -160,7 +160,8 @@ def test_saguaro_verify_parity(F, C):
 
 @pytest.mark.parametrize("F,C,top_p,top_k", [(0, 1.0, None, None), (8, 0.3, None, None), (8, 0.0, None, None),
                                              (8, 0.3, 0.9, None), (0, 1.0, None, 20), (8, 0.3, 0.9, 20),
-                                             (8, 0.0, None, 5)])
+                                             (8, 0.0, None, 5), (48, 0.3, None, None), (128, 0.2, 0.9, None),
+                                             (129, 0.2, None, None)])
 def test_saguaro_sample_parity(F, C, top_p, top_k):
     w = W.scaled(W.SAGUARO, B=16)
     tgt, drf = W.logits(w, 1, device="cuda")
@@ -242,6 +243,51 @@ def test_topn_against_sorting(N, V):
     xs = to_f64(t)
     want = np.argsort(-xs, axis=1, kind="stable")[:, :N]
     np.testing.assert_array_equal(ids.cpu().numpy(), want)
+
+
+def overflow_rows(rng, n, V, S=8):
+    """Rows whose largest values fill seven threads of every warp of the first block of a row's
+    cluster (16-byte vectors dealt round-robin to S * 256 threads).  Every warp's 8th-largest
+    thread maximum stays low, so thousands of elements clear the candidate bound, the first
+    block's buffer overflows and the selection takes the single-block radix path.  The high
+    values are bf16 steps of 1/32 above 5: many equal values, ordered by id."""
+    x = rng.normal(0, 1, (n, V))
+    t = (np.arange(V) // 8) % (S * 256)
+    hot = (t < 256) & ((t % 32) < 7)
+    x[:, hot] = 5.0 + rng.random((n, int(hot.sum())))
+    return x
+
+
+def test_topn_candidate_overflow():
+    rng = np.random.default_rng(17)
+    V = 151936
+    x = overflow_rows(rng, 2, V)
+    t = torch.as_tensor(x, dtype=torch.bfloat16, device="cuda")
+    for kappa in (8, 16):
+        ids, _, st = sv.sv_topk_rows(t, kappa)
+        torch.cuda.synchronize()
+        assert sv.read_stats(st)["status"] == 0
+        want = np.argsort(-to_f64(t), axis=1, kind="stable")[:, :kappa]
+        np.testing.assert_array_equal(ids.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("C", [0.3, 0.0])
+def test_saguaro_sample_candidate_overflow(C):
+    """The Saguaro top-F set on rows that overflow the cluster's candidate buffer."""
+    rng = np.random.default_rng(18)
+    B, R, V = 2, 3, 151936
+    drf = torch.as_tensor(overflow_rows(rng, B * R, V).reshape(B, R, V), dtype=torch.bfloat16, device="cuda")
+    u = rng.random((B, R))
+    T = np.ones(B, np.float32)
+    toks, dbg, st = sv.sv_saguaro_sample(drf, torch.as_tensor(u, device="cuda"), torch.as_tensor(T, device="cuda"),
+                                         F=8, C=C, debug=True)
+    torch.cuda.synchronize()
+    assert sv.read_stats(st)["status"] == 0
+    ref = oracle.draft_sample(to_f64(drf), u, T, np.ones(B), 8, C)
+    np.testing.assert_array_equal(toks.cpu().numpy(), ref["tokens"])
+    d = dbg.cpu().numpy()
+    np.testing.assert_allclose(d[:, :, 1], ref["p_top"], atol=1e-6)
+    np.testing.assert_allclose(d[:, :, 2], ref["z_prime"], atol=1e-6)
 
 
 def test_mirror_round_parity():

@@ -217,6 +217,7 @@ struct TopNArgs {
     float *list_x;          // [row][list_stride] their logits (output, may be null)
     int list_stride;
     sv_stats *stats;        // timeouts of the cluster path (may be null)
+    int ring_stages;        // cluster path: stages of each block's bulk-copy ring
 };
 
 template <int ES>
@@ -275,21 +276,21 @@ __global__ void __launch_bounds__(kThreads) k_topn(const TopNArgs a) {
 // Elements are ranked by a 64-bit code: the order key above the complemented id, so that codes
 // are distinct and larger codes come first in (key desc, id asc) order.  Each block streams its
 // contiguous share of the row through a ring of bulk copies; in a first pass every thread keeps
-// the largest code of the vectors it sees.  The N-th largest of any N of those maxima is a
-// lower bound tau on the row's N-th largest code (N distinct elements reach it), so the row's
-// first N are all among the codes >= tau.  A second pass over the share (from the ring when
-// the share fits in it, else streamed again) collects those candidates, skipping every vector
-// whose largest key is below tau's; each block ranks its candidates, and its first N go to
+// the largest key of the vectors it sees.  A key that at least N of those maxima reach is a
+// lower bound tau on the row's N-th largest key (N distinct elements reach it), so the row's
+// first N are all among the elements of key >= tau.  A second pass over the share (from the
+// ring when the share fits in it, else streamed again) collects their codes, skipping every
+// vector whose largest key is below tau; each block ranks its candidates, and its first N go to
 // block 0, which ranks the union: an element of the row's first N has all elements above it in
 // the union, so its rank there is its rank in the row.  A block whose candidates overflow
 // kTopNCand marks the row, and block 0 then takes it alone by the radix select.
 // ------------------------------------------------------------------------------------------
 constexpr int kTopNFast = 128;            // largest N of the cluster path
 constexpr int kTopNCluster = 8;           // largest cluster
-constexpr int kTopNCand = kMaxTopN;       // candidates one block holds
+constexpr int kTopNCand = 512;            // candidates one block holds
 constexpr int kTopNStageVecs = 1024;      // 16-byte vectors per stage of the bulk-copy ring
-constexpr int kTopNStages = 4;
-constexpr size_t kTopNRingBytes = (size_t)kTopNStages * kTopNStageVecs * 16;   // dynamic shared memory
+constexpr int kTopNStages = 4;            // most ring stages
+constexpr size_t kTopNStageBytes = (size_t)kTopNStageVecs * 16;
 static_assert(kTopNFast <= kThreads, "one thread per rank of the block's maxima");
 
 __device__ __forceinline__ uint64_t rank_code(uint32_t key, int id) {
@@ -298,16 +299,21 @@ __device__ __forceinline__ uint64_t rank_code(uint32_t key, int id) {
 __device__ __forceinline__ uint32_t code_key(uint64_t c) { return (uint32_t)(c >> 32); }
 __device__ __forceinline__ int code_id(uint64_t c) { return (int)(~(uint32_t)c); }
 
+// Dynamic shared memory of a row-cluster kernel: the ring (stages x kTopNStageBytes), then
+// block 0's gather area (block q's sorted first N at q * N: S * N codes).
+inline size_t topn_dyn_bytes(int stages, int S, int n_max) {
+    return (size_t)stages * kTopNStageBytes + (size_t)S * n_max * sizeof(uint64_t);
+}
+
 struct TopNCl {
     uint64_t cand[kTopNCand];                  // this block's candidates (radix path: keys, ids)
-    uint64_t gath[kTopNCluster * kTopNFast];   // block 0: block q's sorted first N at q * N
     uint64_t res[kTopNFast];                   // block 0: the row's first N, sorted
-    uint64_t mx[kThreads];
-    uint64_t taus[kTopNCluster];               // block q's bound, written by block q
-    uint64_t tau_b;
+    uint32_t mx[2 * kThreads];                 // thread maxima; the marked vectors; radix path: tie ids
+    uint32_t taus[kTopNCluster];               // block q's bound, written by block q
+    uint32_t tau_b;
     uint64_t bar[kTopNStages];                 // ring stages
     int n_top[kTopNCluster], over[kTopNCluster];
-    int n_cand, fail;
+    int n_cand, n_mark, fail;
     uint32_t nth_key;                          // block 0: the row's N-th element
     int nth_id;
     unsigned hist[256];                        // radix path
@@ -343,33 +349,88 @@ __device__ __forceinline__ void for_strided(const char *row, int V, int g, int G
     for (int v = n_vec * EPV + g; v < V; v += G) fn(load_elem<ES>(row, v), v);
 }
 
-// The largest order key of a 16-byte vector, or above it: the maximum propagates NaN (whose
-// canonical pattern has the largest key of its sign), and -0 and +0 share a key.
+// The largest order key of a 16-byte vector, exactly: the maximum ignores NaN (an all-NaN
+// result sends the vector to the per-element keys), and -0 shares +0's key.
 template <int ES>
-__device__ __forceinline__ uint32_t vec_max_key(uint4 w) {
+__device__ __forceinline__ uint32_t vec_key_max(uint4 w) {
+    float m;
     if constexpr (ES == 2) {
-        uint32_t m = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
-        m = bmax2(m, __byte_perm(m, 0u, 0x1032));
-        return f32_key(bf16_lo(m));
+        uint32_t h;
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(h) : "r"(w.x), "r"(w.y));
+        uint32_t h2;
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(h2) : "r"(w.z), "r"(w.w));
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(h) : "r"(h), "r"(h2));
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(h) : "r"(h), "r"(__byte_perm(h, 0u, 0x1032)));
+        m = bf16_lo(h);
     } else {
-        float a, b;
-        asm("max.NaN.f32 %0, %1, %2;" : "=f"(a) : "f"(__uint_as_float(w.x)), "f"(__uint_as_float(w.y)));
-        asm("max.NaN.f32 %0, %1, %2;" : "=f"(b) : "f"(__uint_as_float(w.z)), "f"(__uint_as_float(w.w)));
-        asm("max.NaN.f32 %0, %1, %2;" : "=f"(a) : "f"(a), "f"(b));
-        return f32_key(a);
+        m = fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)), fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
     }
+    uint32_t k = f32_key(m);
+    if (__any_sync(__activemask(), m != m)) {   // never on finite rows: a uniform branch
+        if (m != m) {                            // every element NaN
+            float x[16 / ES];
+            unpack<ES>(w, x);
+            k = 0u;
+#pragma unroll
+            for (int i = 0; i < 16 / ES; ++i) k = max(k, f32_key(x[i]));
+        }
+    }
+    return k;
+}
+
+// The largest order key of four 16-byte vectors (one packed maximum tree, then one key), exactly
+// as vec_key_max.
+template <int ES>
+__device__ __forceinline__ uint32_t group_key_max(const uint4 (&w)[4]) {
+    float m;
+    if constexpr (ES == 2) {
+        uint32_t a[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t h0, h1;
+            asm("max.bf16x2 %0, %1, %2;" : "=r"(h0) : "r"(w[k].x), "r"(w[k].y));
+            asm("max.bf16x2 %0, %1, %2;" : "=r"(h1) : "r"(w[k].z), "r"(w[k].w));
+            asm("max.bf16x2 %0, %1, %2;" : "=r"(a[k]) : "r"(h0), "r"(h1));
+        }
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(a[0]) : "r"(a[0]), "r"(a[1]));
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(a[2]) : "r"(a[2]), "r"(a[3]));
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(a[0]) : "r"(a[0]), "r"(a[2]));
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(a[0]) : "r"(a[0]), "r"(__byte_perm(a[0], 0u, 0x1032)));
+        m = bf16_lo(a[0]);
+    } else {
+        float a[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            a[k] = fmaxf(fmaxf(__uint_as_float(w[k].x), __uint_as_float(w[k].y)),
+                         fmaxf(__uint_as_float(w[k].z), __uint_as_float(w[k].w)));
+        m = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
+    }
+    uint32_t k = f32_key(m);
+    if (__any_sync(__activemask(), m != m)) {   // never on finite rows: a uniform branch
+        if (m != m) {                            // every element NaN
+            k = 0u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float x[16 / ES];
+                unpack<ES>(w[j], x);
+#pragma unroll
+                for (int i = 0; i < 16 / ES; ++i) k = max(k, f32_key(x[i]));
+            }
+        }
+    }
+    return k;
 }
 
 // The 32 values of a warp in descending order across lanes (bitonic network).
-__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v) {
+__device__ __forceinline__ uint32_t warp_sort_desc(uint32_t v) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int k = 2; k <= 32; k <<= 1)
 #pragma unroll
         for (int j = k >> 1; j > 0; j >>= 1) {
-            const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, v, j);
+            const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, v, j);
             const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
-            v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
+            v = keep_max ? max(v, o) : min(v, o);
         }
     return v;
 }
@@ -390,7 +451,7 @@ template <int ES>
 __device__ void topn_exact_block(const char *row, int V, int N, bool list, TopNCl &s) {
     uint32_t *xkey = reinterpret_cast<uint32_t *>(s.cand);
     int *xid = reinterpret_cast<int *>(s.cand) + kTopNCand;
-    int *tie = reinterpret_cast<int *>(s.gath);
+    int *tie = reinterpret_cast<int *>(s.mx);
     int n_above;
     const uint32_t kstar = radix_select_count<ES>(row, V, N, n_above, s.hist, s.dig);
     if (!list) {
@@ -435,7 +496,8 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 
 // The cluster part of the top-N of one row, called by every block of the cluster (1 <= N <=
 // min(V, kTopNFast)).  Block `rank` takes the contiguous share [v0, v1) of the row's 16-byte
-// vectors, streamed by bulk copies through `ring` (kTopNRingBytes of dynamic shared memory); its
+// vectors, streamed by bulk copies through `ring` (`stages` x kTopNStageBytes of dynamic
+// shared memory, followed by S * N codes of block 0's gather area); its
 // thread tid sees vectors v0 + tid + k kThreads, in increasing order.  `each_vec(w, vi)` sees
 // every vector of the share once and `each_elem(x, v)` every scalar-tail element; `publish()`
 // runs in every block just before the last barrier (to write per-block results into block 0).
@@ -445,7 +507,7 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 // copies did not arrive in time (its results are then meaningless; the caller reports it).
 template <int ES, class EachVec, class EachElem, class Publish>
 __device__ bool cluster_topn(const cooperative_groups::cluster_group &cl, const char *row, int V, int N, TopNCl &s,
-                             char *ring, long long wait_limit, EachVec each_vec, EachElem each_elem,
+                             char *ring, int stages, long long wait_limit, EachVec each_vec, EachElem each_elem,
                              Publish publish) {
     constexpr int EPV = 16 / ES;
     const int S = (int)cl.num_blocks(), rank = (int)cl.block_rank();
@@ -457,125 +519,145 @@ __device__ bool cluster_topn(const cooperative_groups::cluster_group &cl, const 
     const int n_chunks = (v1 - v0 + kTopNStageVecs - 1) / kTopNStageVecs;
     // the ring carries chunk j of the sequence: the share once (j < n_chunks) and, unless the
     // whole share stays in the ring, once more for the second pass (chunk j - n_chunks)
-    const bool resident = n_chunks <= kTopNStages;
+    uint64_t *gath = reinterpret_cast<uint64_t *>(ring + (size_t)stages * kTopNStageBytes);
+    const bool resident = n_chunks <= stages;
     const int total = resident ? n_chunks : 2 * n_chunks;
     auto chunk_vecs = [&](int c) { return min(kTopNStageVecs, v1 - v0 - c * kTopNStageVecs); };
     auto issue = [&](int j) {   // thread 0
-        const int c = j < n_chunks ? j : j - n_chunks, st = j % kTopNStages;
+        const int c = j < n_chunks ? j : j - n_chunks, st = j % stages;
         const uint32_t bytes = (uint32_t)chunk_vecs(c) * 16u;
         mbar_arrive_expect_tx(&s.bar[st], bytes);
-        bulk_load(ring + (size_t)st * kTopNStageVecs * 16, row + (size_t)(v0 + c * kTopNStageVecs) * 16, bytes,
+        bulk_load(ring + (size_t)st * kTopNStageBytes, row + (size_t)(v0 + c * kTopNStageVecs) * 16, bytes,
                   &s.bar[st]);
     };
     cluster_arrive_relaxed();   // completes once every block has started (before any DSMEM access)
     if (tid == 0) {
-        s.tau_b = 0ull;
+        s.tau_b = 0u;
         s.n_cand = 0;
+        s.n_mark = 0;
         s.fail = 0;
-        for (int i = 0; i < kTopNStages; ++i) mbar_init(&s.bar[i], 1);
+        for (int i = 0; i < stages; ++i) mbar_init(&s.bar[i], 1);
         fence_barrier_init();
-        for (int j = 0; j < min(kTopNStages, total); ++j) issue(j);
+        for (int j = 0; j < min(stages, total); ++j) issue(j);
     }
     __syncthreads();
-    // consumes ring chunks j0 .. j1-1 with fn(w, vi); refills each stage once every thread is
-    // done with it.  A copy late beyond wait_limit ends the streaming (s.fail) after the copies
-    // still in flight have landed (bounded).
+    // A thread's vectors of a chunk: tid + k kThreads for k < n (n <= 4, as kTopNStageVecs = 4
+    // kThreads); absent ones repeat the first, so a group's maximum is the maximum of its vectors.
+    auto group = [&](const char *base, int nv, int vbase, auto fn4) {
+        if (tid >= nv) return;
+        uint4 w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = tid + k * kThreads;
+            w[k] = (k == 0 || i < nv) ? lds128(base + i * 16) : w[0];
+        }
+        fn4(w, min(4, (nv - tid + kThreads - 1) / kThreads), vbase + tid);
+    };
+    static_assert(kTopNStageVecs == 4 * kThreads, "a thread's vectors of a chunk form one group");
+    // consumes ring chunks j0 .. j1-1 with fn4(w[4], n, vi0); refills each stage once every
+    // thread is done with it.  A copy late beyond wait_limit ends the streaming (s.fail) after
+    // the copies still in flight have landed (bounded).
     bool failed = false;
     auto stream = [&](int j0, int j1, auto fn) {
         if (failed) return;
         for (int j = j0; j < j1; ++j) {
-            const int st = j % kTopNStages, c = j < n_chunks ? j : j - n_chunks;
-            const bool ok = mbar_wait_bounded(&s.bar[st], (uint32_t)(j / kTopNStages) & 1u, wait_limit);
-            if (ok) {
-                const int nv = chunk_vecs(c);
-                const char *base = ring + (size_t)st * kTopNStageVecs * 16;
-                for (int i = tid; i < nv; i += kThreads) fn(lds128(base + i * 16), v0 + c * kTopNStageVecs + i);
-            }
+            const int st = j % stages, c = j < n_chunks ? j : j - n_chunks;
+            const bool ok = mbar_wait_bounded(&s.bar[st], (uint32_t)(j / stages) & 1u, wait_limit);
+            if (ok) group(ring + (size_t)st * kTopNStageBytes, chunk_vecs(c), v0 + c * kTopNStageVecs, fn);
             if (__syncthreads_or(!ok)) {
-                const int issued = min(j + kTopNStages, total);
+                const int issued = min(j + stages, total);
                 for (int d = j; d < issued; ++d)
-                    mbar_wait_bounded(&s.bar[d % kTopNStages], (uint32_t)(d / kTopNStages) & 1u, wait_limit);
+                    mbar_wait_bounded(&s.bar[d % stages], (uint32_t)(d / stages) & 1u, wait_limit);
                 if (tid == 0) s.fail = 1;
                 failed = true;
                 return;
             }
-            if (tid == 0 && j + kTopNStages < total) issue(j + kTopNStages);
+            if (tid == 0 && j + stages < total) issue(j + stages);
         }
     };
-    // ---- pass 1: each thread's largest code ----
-    uint32_t mk = 0u;   // largest key seen and the first id holding it (mk = 0: none yet)
-    int mi = 0x7FFFFFFF;
-    auto see = [&](uint32_t k, int v) {
-        if (k > mk || (k == mk && v < mi)) {
-            mk = k;
-            mi = v;
-        }
-    };
-    stream(0, n_chunks, [&](uint4 w, int vi) {
-        each_vec(w, vi);
-        if (vec_max_key<ES>(w) >= mk) {   // a new maximum may be here: the exact keys, in order
-            float x[EPV];
-            unpack<ES>(w, x);
+    // ---- pass 1: each thread's largest key ----
+    uint32_t mk = 0u;
+    stream(0, n_chunks, [&](const uint4 (&w)[4], int n, int vi0) {
 #pragma unroll
-            for (int k = 0; k < EPV; ++k) see(f32_key(x[k]), vi * EPV + k);
-        }
+        for (int k = 0; k < 4; ++k)
+            if (k < n) each_vec(w[k], vi0 + k * kThreads);
+        mk = max(mk, group_key_max<ES>(w));
     });
     for (int v = n_vec * EPV + g; v < V; v += G) {
         const float x = load_elem<ES>(row, v);
         each_elem(x, v);
-        see(f32_key(x), v);
+        mk = max(mk, f32_key(x));
     }
-    const uint64_t m = mi == 0x7FFFFFFF ? 0ull : rank_code(mk, mi);   // 0: no element
+    // the block's bound: the largest key that N thread maxima reach (0: none, below every key)
     if (N <= 32) {
-        const uint64_t w = __shfl_sync(0xFFFFFFFFu, warp_sort_desc(m), N - 1);
-        if (lane == 0) atomicMax(reinterpret_cast<unsigned long long *>(&s.tau_b), (unsigned long long)w);
+        const uint32_t w = __shfl_sync(0xFFFFFFFFu, warp_sort_desc(mk), N - 1);
+        if (lane == 0) atomicMax(&s.tau_b, w);
     } else {
-        s.mx[tid] = m;
+        s.mx[tid] = mk;
         __syncthreads();
         int r = 0;
-        for (int j = 0; j < kThreads; ++j) r += s.mx[j] > m ? 1 : 0;
-        if (r == N - 1) s.tau_b = m;
+        for (int j = 0; j < kThreads; ++j) r += s.mx[j] >= mk ? 1 : 0;
+        if (r >= N) atomicMax(&s.tau_b, mk);
     }
     __syncthreads();
     cluster_wait();
     if (tid < S) *cl.map_shared_rank(&s.taus[rank], tid) = s.tau_b;
     cl.sync();   // (1) every block's bound is in every block
-    uint64_t tau = 0ull;
-    for (int q = 0; q < S; ++q) tau = s.taus[q] > tau ? s.taus[q] : tau;
-    // ---- pass 2: the codes >= tau ----
-    const uint32_t tau_key = code_key(tau);
+    uint32_t tau = 0u;
+    for (int q = 0; q < S; ++q) tau = max(tau, s.taus[q]);
+    // ---- pass 2: the codes of the elements of key >= tau ----
+    // A cheap sweep marks the groups whose largest key reaches tau (few); their elements are
+    // then expanded, one group per thread.
     auto add = [&](uint64_t c) {
         const int slot = atomicAdd(&s.n_cand, 1);
         if (slot < kTopNCand) s.cand[slot] = c;
     };
-    auto collect = [&](uint4 w, int vi) {
-        if (vec_max_key<ES>(w) < tau_key) return;
-        float x[EPV];
-        unpack<ES>(w, x);
-#pragma unroll
-        for (int k = 0; k < EPV; ++k) {
-            const uint64_t c = rank_code(f32_key(x[k]), vi * EPV + k);
-            if (c >= tau) add(c);
+    constexpr int kMarkCap = 2 * kThreads;
+    auto mark = [&](const uint4 (&w)[4], int, int vi0) {
+        if (group_key_max<ES>(w) >= tau) {
+            const int slot = atomicAdd(&s.n_mark, 1);
+            if (slot < kMarkCap) s.mx[slot] = (uint32_t)vi0;
         }
     };
     if (resident) {
         if (!failed)
-            for (int c = 0; c < n_chunks; ++c) {
-                const char *base = ring + (size_t)c * kTopNStageVecs * 16;
-                const int nv = chunk_vecs(c);
-                for (int i = tid; i < nv; i += kThreads) collect(lds128(base + i * 16), v0 + c * kTopNStageVecs + i);
-            }
+            for (int c = 0; c < n_chunks; ++c)
+                group(ring + (size_t)c * kTopNStageBytes, chunk_vecs(c), v0 + c * kTopNStageVecs, mark);
     } else {
-        stream(n_chunks, total, collect);
+        stream(n_chunks, total, mark);
     }
     for (int v = n_vec * EPV + g; v < V; v += G) {
-        const uint64_t c = rank_code(f32_key(load_elem<ES>(row, v)), v);
-        if (c >= tau) add(c);
+        const uint32_t key = f32_key(load_elem<ES>(row, v));
+        if (key >= tau) add(rank_code(key, v));
+    }
+    __syncthreads();
+    const int n_mark = s.n_mark;
+    if (n_mark > kMarkCap) {
+        if (tid == 0) s.n_cand = kTopNCand + 1;   // overflow: the radix path
+    } else {
+        // one warp per marked group: lane l takes element l % EPV of vector l / EPV of the group
+        // (lanes 0 .. 4 EPV - 1)
+        const int warp = tid >> 5;
+        for (int i = warp; i < n_mark; i += kWarps) {
+            const int vi0 = (int)s.mx[i];
+            const int c = (vi0 - v0) / kTopNStageVecs;
+            const int vend = v0 + c * kTopNStageVecs + chunk_vecs(c);   // end of the group's chunk
+            const int vi = vi0 + (lane / EPV) * kThreads, e = vi * EPV + lane % EPV;
+            if (lane < 4 * EPV && vi < vend) {
+                const float x = resident ? (ES == 2 ? bf16_lo((uint32_t)*reinterpret_cast<const unsigned short *>(
+                                                          ring + (size_t)(vi - v0) * 16 + (lane % EPV) * 2))
+                                                    : *reinterpret_cast<const float *>(ring + (size_t)(vi - v0) * 16 +
+                                                                                       (lane % EPV) * 4))
+                                         : load_elem<ES>(row, e);
+                const uint32_t key = f32_key(x);
+                if (key >= tau) add(rank_code(key, e));
+            }
+        }
     }
     __syncthreads();
     const int nc = s.n_cand;
     if (nc <= kTopNCand) {
-        uint64_t *dst = cl.map_shared_rank(s.gath, 0) + rank * N;
+        uint64_t *dst = cl.map_shared_rank(gath, 0) + rank * N;
         for (int i = tid; i < nc; i += kThreads) {
             const uint64_t c = s.cand[i];
             int r = 0;
@@ -597,10 +679,10 @@ __device__ bool cluster_topn(const cooperative_groups::cluster_group &cl, const 
     for (int idx = tid; idx < S * N; idx += kThreads) {
         const int q = idx / N, i = idx - q * N;
         if (i >= s.n_top[q]) continue;
-        const uint64_t c = s.gath[idx];
+        const uint64_t c = gath[idx];
         int r = 0;
         for (int q2 = 0; q2 < S; ++q2) {
-            const uint64_t *l = s.gath + q2 * N;
+            const uint64_t *l = gath + q2 * N;
             const int n = s.n_top[q2];
             for (int j = 0; j < n; ++j) r += l[j] > c ? 1 : 0;
         }
@@ -628,7 +710,7 @@ __global__ void __launch_bounds__(kThreads) k_topn_cl(const TopNArgs a) {
     int N = a.n_all > 0 ? a.n_all : a.n_of_j[j];
     if (N > a.V) N = a.V;
     if (N <= 0) return;   // the same in every block of the cluster
-    const bool radix = cluster_topn<ES>(cl, row, a.V, N, s, ring, kWaitLimitCycles, [](uint4, int) {},
+    const bool radix = cluster_topn<ES>(cl, row, a.V, N, s, ring, a.ring_stages, kWaitLimitCycles, [](uint4, int) {},
                                         [](float, int) {}, [] {});
     if (s.fail && threadIdx.x == 0) report_error(a.stats, SV_ERR_TIMEOUT, (int)r);
     if (cl.block_rank() != 0) return;
@@ -641,12 +723,21 @@ __global__ void __launch_bounds__(kThreads) k_topn_cl(const TopNArgs a) {
     }
 }
 
-// Cluster size for n_rows rows: a block for every SM when the rows are few (each block streams
-// its share through a 64 KB ring, two blocks to an SM), at most kTopNCluster per row.
+// Cluster size for n_rows rows: two blocks for every SM when the rows are few (a block of a
+// 128256-token bf16 row then keeps its whole 64 KB share in its ring, three blocks to an SM),
+// at most kTopNCluster per row.
 inline int topn_cluster_size(long long n_rows, int sms) {
     int S = 1;
-    while (S < kTopNCluster && n_rows * S < sms) S *= 2;
+    while (S < kTopNCluster && n_rows * S < 2LL * sms) S *= 2;
     return S;
+}
+
+// Ring stages for shares of a row of n_vec vectors over S blocks: enough to hold a share (then
+// the second pass reads shared memory), at most kTopNStages.
+inline int topn_ring_stages(int n_vec, int S) {
+    const int share = (n_vec + S - 1) / S;
+    const int chunks = (share + kTopNStageVecs - 1) / kTopNStageVecs;
+    return chunks < 1 ? 1 : (chunks > kTopNStages ? kTopNStages : chunks);
 }
 
 // Launch of a row-per-cluster kernel: grid = n_rows * S blocks, clusters of S.
@@ -674,11 +765,15 @@ cudaError_t launch_row_clusters(void (*kern)(Args), const Args &args, long long 
 
 // Top-N lists of TopNArgs rows: the cluster path when every N fits it, else one block per row.
 template <int ES>
-cudaError_t launch_topn(const TopNArgs &ta, int max_n, int sms, cudaStream_t stream) {
-    if (ta.n_rows < 1) return cudaSuccess;
-    if (max_n <= kTopNFast)
-        return launch_row_clusters(k_topn_cl<ES>, ta, ta.n_rows, topn_cluster_size(ta.n_rows, sms), kTopNRingBytes,
-                                   stream);
+cudaError_t launch_topn(const TopNArgs &ta_in, int max_n, int sms, cudaStream_t stream) {
+    if (ta_in.n_rows < 1) return cudaSuccess;
+    if (max_n <= kTopNFast) {
+        TopNArgs ta = ta_in;
+        const int S = topn_cluster_size(ta.n_rows, sms);
+        ta.ring_stages = topn_ring_stages((int)((long long)ta.V * ES / 16), S);
+        return launch_row_clusters(k_topn_cl<ES>, ta, ta.n_rows, S, topn_dyn_bytes(ta.ring_stages, S, max_n), stream);
+    }
+    const TopNArgs &ta = ta_in;
     k_topn<ES><<<(unsigned)ta.n_rows, kThreads, 0, stream>>>(ta);
     return cudaGetLastError();
 }
@@ -1577,6 +1672,7 @@ struct TopSetArgs {
     const NucleusCut *nuc;   // indexed by candidate row, or null
     TopSet *top;             // indexed by candidate row
     sv_stats *stats;
+    int ring_stages;         // stages of each block's bulk-copy ring
 };
 
 // Masses of the kept tokens inside and outside D (the elements at or above (xstar, last) in
@@ -1616,6 +1712,8 @@ __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
     __shared__ double s_red[3 * kWarps];
     __shared__ RowStat s_rs;
     __shared__ double s_tot[kTopNCluster][4];   // block 0: each block's (E, A, count) of kept tokens
+    __shared__ float4 s_fin[kTopNFast / 32];     // block 0: the first N's (E hi, E lo, A, count) per warp
+    __shared__ int s_trust;
     const cooperative_groups::cluster_group cl = cooperative_groups::this_cluster();
     const int S = (int)cl.num_blocks(), rank = (int)cl.block_rank();
     const long long lr = blockIdx.x / S;
@@ -1688,7 +1786,7 @@ __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
             ++n_t;
         };
         const bool radix = cluster_topn<ES>(
-            cl, row, a.V, N, s, ring, kWaitLimitCycles,
+            cl, row, a.V, N, s, ring, a.ring_stages, kWaitLimitCycles,
             [&](uint4 w, int vi) {
                 if (!filtered) return;
                 float x[16 / ES];
@@ -1717,7 +1815,11 @@ __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
         if (radix) {
             topset_split_block<ES>(row, a.V, xstar, last, kept, mass, s_red, t_in, t_out);
         } else {
-            double e_i = 0.0, a_i = 0.0, n_i = 0.0;
+            // the first N (N <= kTopNFast: warps 0-3) in float-float, summed by thread 0
+            const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+            ff e_i = {0.f, 0.f};
+            float a_i = 0.f;
+            int n_i = 0;
             if (threadIdx.x < N) {
                 const uint64_t c = s.res[threadIdx.x];
                 const float x = key_value(code_key(c));
@@ -1725,42 +1827,67 @@ __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
                 if (kept(x, v)) {
                     float y;
                     const float e = mass(x, y);
-                    e_i = (double)e;
-                    a_i = (double)(e * fabsf(y));
-                    n_i = 1.0;
+                    e_i.hi = e;
+                    a_i = e * fabsf(y);
+                    n_i = 1;
                 }
             }
-            t_in = block_sum_d3(e_i, a_i, n_i, s_red);
-            direct = false;
-            bool trust;
-            if (filtered) {
-                double E = 0.0, A = 0.0, n = 0.0;
-                for (int q = 0; q < S; ++q) {
-                    E += s_tot[q][0];
-                    A += s_tot[q][1];
-                    n += s_tot[q][2];
-                }
-                // E - E_in: the masses of D cancel exactly (the same float32 values on both
-                // sides); each float-float addition errs by at most 2^-47 of its sum, so a
-                // thread's share of n elements leaves at most n 2^-47 E.  A enters the bound only.
-                t_out.x = E - t_in.x;
-                t_out.y = fmax(A - t_in.y, 0.0) + 1e-4 * A;
-                t_out.z = n - t_in.z;
-                if (t_out.z == 0.0) t_out.x = t_out.y = 0.0;   // nothing kept outside D
-                const double r_rel = (double)(a.V / (S * kThreads) + 16) * 0x1p-46;
-                sub_err = r_rel * E;
-                trust = t_out.z == 0.0 || t_out.x > 0x1p17 * sub_err;
-            } else {
-                // S - E_in, off by at most err S + r_in E_in; A S bounds the outside sum of e |y|
-                const double Srow = (double)st.s_hi + (double)st.s_lo;
-                const double r_in = kEx2RelErr + 1.02 * kYRound * (t_in.x > 0.0 ? t_in.y / t_in.x : 0.0) + 4.0 * kU32;
-                t_out.x = Srow - t_in.x;
-                t_out.y = 1.01 * (double)st.ay * Srow + 1e-30;
-                t_out.z = 1.0;   // a positive outside mass (checked below) means a kept token outside D
-                sub_err = (double)st.err * Srow + r_in * t_in.x;
-                trust = t_out.x > 16.0 * sub_err && t_out.x > 0x1p-4 * Srow;
+            if (warp * 32 < N) {
+                e_i = warp_sum_ff(e_i);
+                a_i = warp_sum_f(a_i);
+                n_i = __reduce_add_sync(0xFFFFFFFFu, n_i);
+                if (lane == 0) s_fin[warp] = make_float4(e_i.hi, e_i.lo, a_i, (float)n_i);
             }
-            if (!trust) {   // too small to take as a difference
+            __syncthreads();
+            // thread 0 alone forms the totals in float64 (this GPU's float64 pipe is narrow) and
+            // tells the block whether the difference can be trusted
+            bool trust = true;
+            if (threadIdx.x == 0) {
+                {
+                    ff E = {0.f, 0.f};
+                    float A = 0.f, n = 0.f;
+                    for (int w = 0; w * 32 < N; ++w) {
+                        E = ff_add(E, {s_fin[w].x, s_fin[w].y});
+                        A += s_fin[w].z;
+                        n += s_fin[w].w;
+                    }
+                    t_in = make_double3(ff_to_double(E), (double)A, (double)n);
+                }
+                direct = false;
+                if (filtered) {
+                    double E = 0.0, A = 0.0, n = 0.0;
+                    for (int q = 0; q < S; ++q) {
+                        E += s_tot[q][0];
+                        A += s_tot[q][1];
+                        n += s_tot[q][2];
+                    }
+                    // E - E_in: the masses of D cancel exactly (the same float32 values on both
+                    // sides); each float-float addition errs by at most 2^-47 of its sum, so a
+                    // thread's share of n elements leaves at most n 2^-47 E.  A enters the bound only.
+                    t_out.x = E - t_in.x;
+                    t_out.y = fmax(A - t_in.y, 0.0) + 1e-4 * A;
+                    t_out.z = n - t_in.z;
+                    if (t_out.z == 0.0) t_out.x = t_out.y = 0.0;   // nothing kept outside D
+                    const double r_rel = (double)(a.V / (S * kThreads) + 16) * 0x1p-46;
+                    sub_err = r_rel * E;
+                    trust = t_out.z == 0.0 || t_out.x > 0x1p17 * sub_err;
+                } else {
+                    // S - E_in, off by at most err S + r_in E_in; A S bounds the outside sum of e |y|
+                    const double Srow = (double)st.s_hi + (double)st.s_lo;
+                    const float fin = (float)t_in.x;
+                    const double r_in = (double)((float)(kEx2RelErr + 4.0 * kU32) +
+                                                 (float)(1.02 * kYRound) * (fin > 0.f ? __fdiv_ru((float)t_in.y, fin) : 0.f)) *
+                                        (1.0 + 0x1p-16);
+                    t_out.x = Srow - t_in.x;
+                    t_out.y = 1.01 * (double)st.ay * Srow + 1e-30;
+                    t_out.z = 1.0;   // a positive outside mass (checked below) means a kept token outside D
+                    sub_err = (double)st.err * Srow + r_in * t_in.x;
+                    trust = t_out.x > 16.0 * sub_err && t_out.x > 0x1p-4 * Srow;
+                }
+                s_trust = trust ? 1 : 0;
+            }
+            __syncthreads();
+            if (!s_trust) {   // too small to take as a difference: the block sums both sides
                 topset_split_block<ES>(row, a.V, xstar, last, kept, mass, s_red, t_in, t_out);
                 direct = true;
             }
@@ -1779,21 +1906,26 @@ __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
     } else {
         t.top_x = xstar;
         t.top_id = last;
-        t.p_d = Ein / den;
-        t.z = num / den;
-        // each part is a sum of float32 masses: relative error kEx2RelErr + ln2 u |y| per token
-        // (A / E is the mass-weighted mean |y|; the float32 sums of e |y| are within 1% of it)
-        // plus rounding; masses that flush to zero below 2^-126 are at most V 2^-126 in all; an
-        // outside mass taken as a difference adds its own error sub_err
-        const double r_in = kEx2RelErr + 1.02 * kYRound * (Ein > 0.0 ? t_in.y / Ein : 0.0) + 4.0 * kU32;
-        const double r_out = kEx2RelErr + 1.02 * kYRound * (Eout > 0.0 ? t_out.y / Eout : 0.0) + 4.0 * kU32 +
-                             (direct || !(Eout > 0.0) ? 0.0 : sub_err / Eout);
-        const double uf = (double)a.V * 0x1p-126;
-        const double rel_num = (C * Ein * r_in + Eout * r_out + uf) / num;
-        const double rel_den = (Ein * r_in + Eout * r_out + uf) / den;
-        t.z_err = rel_num + rel_den + 1e-12;
+        const double inv_den = 1.0 / den;   // the one float64 quotient (this GPU's float64 is slow)
+        t.p_d = Ein * inv_den;
+        t.z = num * inv_den;
+        // The bound, in float32 with every quotient and product rounded up.  Each part is a sum
+        // of float32 masses: relative error kEx2RelErr + ln2 u |y| per token (A / E is the
+        // mass-weighted mean |y|; the float32 sums of e |y| are within 1% of it) plus rounding;
+        // masses that flush to zero below 2^-126 are at most V 2^-126 in all; an outside mass
+        // taken as a difference adds its own error sub_err.
+        const float fEin = (float)Ein, fEout = (float)Eout, fnum = (float)num, fden = (float)den, fC = a.C;
+        const float base = (float)(kEx2RelErr + 4.0 * kU32), ky = (float)(1.02 * kYRound);
+        const float r_in = __fmaf_ru(ky, fEin > 0.f ? __fdiv_ru((float)t_in.y, fEin) : 0.f, base);
+        float r_out = __fmaf_ru(ky, fEout > 0.f ? __fdiv_ru((float)t_out.y, fEout) : 0.f, base);
+        if (!direct) r_out = __fadd_ru(r_out, fEout > 0.f ? __fdiv_ru((float)sub_err, fEout) : INFINITY);
+        const float uf = (float)a.V * 0x1p-126f;
+        const float e_in = __fmul_ru(fEin, r_in), e_out = __fmaf_ru(fEout, r_out, uf);
+        const float rel_num = __fdiv_ru(__fmaf_ru(fC, e_in, e_out), fnum);
+        const float rel_den = __fdiv_ru(__fadd_ru(e_in, e_out), fden);
+        t.z_err_f = __fmul_ru(__fadd_ru(__fadd_ru(rel_num, rel_den), 1e-12f), 1.0f + 0x1p-16f);
+        t.z_err = (double)t.z_err_f;
         t.z_f = (float)t.z;
-        t.z_err_f = (float)t.z_err * (1.0f + 0x1p-20f);
     }
     a.top[rid] = t;
 }
@@ -1818,7 +1950,10 @@ sv_status launch_topset(const RowSet &drf, long long rid0, int B, int rows_used,
     a.stats = stats;
     if (a.n_rows < 1) return SV_OK;
     const int S = F > kTopNFast ? 1 : topn_cluster_size(a.n_rows, di.sms);
-    return cuda_status(launch_row_clusters(k_topset<ES>, a, a.n_rows, S, kTopNRingBytes, stream));
+    a.ring_stages = topn_ring_stages((int)((long long)V * ES / 16), S);
+    const int n_max = F < V ? F : V;
+    return cuda_status(launch_row_clusters(k_topset<ES>, a, a.n_rows, S,
+                                           topn_dyn_bytes(a.ring_stages, S, n_max > kTopNFast ? 1 : n_max), stream));
 }
 
 }  // namespace sv

@@ -393,14 +393,39 @@ def _timed_calls(call, n, world):
     return max_over_ranks(start.elapsed_time(end) / n, world)
 
 
+def _graph_and_stream(call, n, world):
+    """(ms per round replayed from a CUDA graph of one round, ms per round as stream calls).
+    The graph holds exactly the library's launches of one round; the stream calls add the
+    Python binding's per-call host work."""
+    import torch
+    ms_stream = _timed_calls(call, n, world)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    return _timed_calls(g.replay, n, world), ms_stream
+
+
+def _round_line(w, n, world, ms_graph, ms_stream, **extra):
+    return dict(workload=w.name, value=whole_job_rate(1.0, world, ms_graph), unit="rounds/s",
+                us_per_round=ms_graph * 1e3, timing="CUDA graph of one round, replayed", steps=n,
+                stream_calls={"value": whole_job_rate(1.0, world, ms_stream), "unit": "rounds/s",
+                              "us_per_round": ms_stream * 1e3}, **extra)
+
+
 def config_rates(sv, dev, world, n):
     """Rounds/s of the other stated workloads, each as the library calls one round makes (inputs
-    resident; config 2 is in `filters`):
-      1: B=1, K=4, V=32000 f32 — one sv_verify call, launched on the stream and replayed from a
-         CUDA graph of one call (launch-bound);
-      3: SSD / Saguaro, B=16, K=5, V=128256 bf16 — sv_saguaro_sample (sigma_{8,0.3} draft
+    resident; config 2 is in `filters`), replayed from a CUDA graph of one round (and, beside it,
+    as plain stream calls through the Python binding):
+      1: B=1, K=4, V=32000 f32 -- one sv_verify call (launch-bound);
+      3: SSD / Saguaro, B=16, K=5, V=128256 bf16 -- sv_saguaro_sample (sigma_{8,0.3} draft
          tokens), sv_verify with sigma, sv_cache_keys (fan-out 64), sv_cache_lookup;
-      4: Mirror, B=4, kappa=8, gamma=7, V=151936 bf16 — sv_topk_rows (roots from the early-exit
+      4: Mirror, B=4, kappa=8, gamma=7, V=151936 bf16 -- sv_topk_rows (roots from the early-exit
          row), sv_verify of branch 0 against the early-exit rows, sv_mirror_reuse."""
     import torch
     from synth import workloads as W
@@ -419,26 +444,9 @@ def config_rates(sv, dev, world, n):
 
     def call1():
         sv.sv_verify(tgt, drf, toks, u_d, T_d, accept_len=al, out_tokens=ot, stats=stats, workspace=ws)
-    ms = _timed_calls(call1, n, world)
-    c1 = {"workload": w.name, "value": whole_job_rate(1.0, world, ms), "unit": "rounds/s", "us_per_round": ms * 1e3,
-          "steps": n}
-    try:   # one call captured in a CUDA graph, replayed
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            call1()
-        torch.cuda.current_stream().wait_stream(side)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            call1()
-        msg = _timed_calls(g.replay, n, world)
-        c1["graph"] = {"value": whole_job_rate(1.0, world, msg), "unit": "rounds/s", "us_per_round": msg * 1e3}
-    except Exception as e:   # noqa: BLE001 - report, do not fail the bench
-        c1["graph"] = {"unavailable": str(e).splitlines()[0][:160]}
+    out["plain_b1"] = _round_line(w, n, world, *_graph_and_stream(call1, n, world), calls="verify")
     if sv.read_stats(stats)["status"] != 0:
         raise RuntimeError(f"config 1 failed: {sv.read_stats(stats)}")
-    out["plain_b1"] = c1
     # ---- 3 ----
     w = W.scaled(W.SAGUARO, seed=rank_seed(W.SAGUARO.seed, r))
     tgt, drf = W.logits(w, 0, device=dev)
@@ -460,11 +468,10 @@ def config_rates(sv, dev, world, n):
                      out_tokens=ot, stats=stats, workspace=ws)
         sv.sv_cache_keys(drf, toks, f_int, keys=keys, workspace=ws3)
         sv.sv_cache_lookup(al, ot, keys, f_int, hit=hit)
-    ms = _timed_calls(call3, n, world)
+    out["saguaro_b16"] = _round_line(w, n, world, *_graph_and_stream(call3, n, world),
+                                     calls="sample, verify, cache keys, lookup")
     if sv.read_stats(stats)["status"] != 0:
         raise RuntimeError(f"config 3 failed: {sv.read_stats(stats)}")
-    out["saguaro_b16"] = {"workload": w.name, "value": whole_job_rate(1.0, world, ms), "unit": "rounds/s",
-                          "us_per_round": ms * 1e3, "steps": n, "calls": "sample, verify, cache keys, lookup"}
     # ---- 4 ----
     w = W.scaled(W.MIRROR, seed=rank_seed(W.MIRROR.seed, r))
     tgt, ee = W.logits(w, 0, device=dev)
@@ -490,11 +497,10 @@ def config_rates(sv, dev, world, n):
         sv.sv_topk_rows(ee0, kappa, T_d, ids=ids, logprobs=lps, workspace=ws2)
         sv.sv_verify(tgt, ee, toks0, u_d, T_d, accept_len=al, out_tokens=ot, stats=stats, workspace=ws)
         sv.sv_mirror_reuse(branches, al, ot, reuse=reuse)
-    ms = _timed_calls(call4, n, world)
+    out["mirror_b4"] = _round_line(w, n, world, *_graph_and_stream(call4, n, world),
+                                   calls="top-kappa roots, verify, reuse")
     if sv.read_stats(stats)["status"] != 0:
         raise RuntimeError(f"config 4 failed: {sv.read_stats(stats)}")
-    out["mirror_b4"] = {"workload": w.name, "value": whole_job_rate(1.0, world, ms), "unit": "rounds/s",
-                        "us_per_round": ms * 1e3, "steps": n, "calls": "top-kappa roots, verify, reuse"}
     return out
 
 

@@ -224,7 +224,8 @@ def run_reference(args, rank, world):
 def filter_rates(sv, dev, world, n):
     """Rounds/s of sv_verify on the two sampled workloads with filters (B=8, K=5, V=128256 bf16,
     T=0.8): top-p 0.9, and top-k 50 ahead of top-p 0.9.  Their inputs (22.6 MB) fit in L2, so a
-    256 MB buffer is written between timed calls and each call is timed alone."""
+    256 MB buffer is written between timed calls and each call is timed alone: replayed from a
+    CUDA graph of the call, and (stream_calls) through the Python binding."""
     import torch
     from synth import workloads as W
     out = {}
@@ -247,20 +248,36 @@ def filter_rates(sv, dev, world, n):
         for _ in range(5):
             call()
         torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-        barrier(world)
-        for b, e in ev:
-            flush.fill_(1)
-            b.record()
+
+        def timed(fn):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            barrier(world)
+            for b, e in ev:
+                flush.fill_(1)
+                b.record()
+                fn()
+                e.record()
+            torch.cuda.synchronize()
+            return max_over_ranks(statistics.mean(b.elapsed_time(e) for b, e in ev), world)
+        ms_stream = timed(call)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
             call()
-            e.record()
+        torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call()
+        ms = timed(g.replay)
         st = sv.read_stats(stats)
         if st["status"] != 0:
             raise RuntimeError(f"filtered verify failed: {st}")
-        ms = max_over_ranks(statistics.mean(b.elapsed_time(e) for b, e in ev), world)
         out[name] = {"workload": w.name, "value": whole_job_rate(1.0, world, ms), "unit": "rounds/s",
-                     "ms_per_round": ms, "steps": n, "l2": "256 MB written between calls",
+                     "ms_per_round": ms, "timing": "CUDA graph of one call, replayed", "steps": n,
+                     "l2": "256 MB written between calls",
+                     "stream_calls": {"value": whole_job_rate(1.0, world, ms_stream), "unit": "rounds/s",
+                                      "ms_per_round": ms_stream},
                      "reresolved": st["reresolved"], "unresolved": st["unresolved"]}
     del flush
     return out

@@ -120,6 +120,30 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start while the
+// previous kernel of the stream is still running; pdl_wait() returns once that kernel has
+// completed and its results are visible, so it comes before the first read of them.
+// pdl_trigger() lets the next kernel (if launched with launch_pdl) start early; its own
+// pdl_wait() still waits for this kernel's completion.  Both are no-ops without a dependent.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <class... Params, class... Args>
+inline cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 __device__ __forceinline__ uint4 lds128(const void *p) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -140,6 +140,8 @@ constexpr size_t kDrawSmemBytes = (size_t)kDrawCtlBytes + (size_t)2 * kDrawStage
 // consumer warps weight the tokens and write one float32 sum per 32-vector sub-chunk.
 template <int ES>
 __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + kDrawStages;
@@ -316,6 +318,7 @@ __device__ __forceinline__ float draw_error_bound(const DrawItem &it, float W, f
 // against draw_error_bound.
 template <int ES>
 __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
+    pdl_wait();
     constexpr int EPV = 16 / ES;
     __shared__ float2 s_scan[kThreads];
     __shared__ int s_sub;
@@ -510,10 +513,11 @@ static sv_status launch_draws(const DrawArgs &da, long long max_items, const Dev
     const long long maxu = max_items * da.n_split;
     if (grid > maxu) grid = maxu;
     if (grid < 1) grid = 1;
-    k_draw_sums<ES><<<(unsigned)grid, kStatsThreads, kDrawSmemBytes, stream>>>(da);
-    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
-    k_draw_finish<ES><<<(unsigned)max_items, kThreads, 0, stream>>>(da);
-    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    if (launch_pdl(k_draw_sums<ES>, dim3((unsigned)grid), dim3(kStatsThreads), kDrawSmemBytes, stream, da) !=
+        cudaSuccess)
+        return SV_ERR_CUDA;
+    if (launch_pdl(k_draw_finish<ES>, dim3((unsigned)max_items), dim3(kThreads), 0, stream, da) != cudaSuccess)
+        return SV_ERR_CUDA;
     return SV_OK;
 }
 

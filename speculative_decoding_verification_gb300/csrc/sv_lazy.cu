@@ -332,6 +332,7 @@ constexpr size_t kLazySmemBytes = (size_t)kLazyCtlBytes + (size_t)kStatsStages *
 // The statistics pass of k_stats with a work queue that grows while it runs.
 template <int ES>
 __global__ void __launch_bounds__(kLazyThreads, 2) k_lazy(const LazyArgs L) {
+    pdl_trigger();   // a dependent launch may be scheduled; it waits for this kernel
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + kStatsStages;

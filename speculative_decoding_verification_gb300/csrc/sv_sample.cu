@@ -36,6 +36,7 @@ struct SampleArgs {
 
 // One warp per row: combine the statistics, then either write the argmax (greedy) or queue a draw.
 __global__ void __launch_bounds__(kThreads) k_sample_items(const SampleArgs a, long long total) {
+    pdl_trigger();   // a dependent launch may be scheduled; it waits for this kernel
     const int lane = threadIdx.x & 31;
     const long long r = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
     if (r >= total) return;

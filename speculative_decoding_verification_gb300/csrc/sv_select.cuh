@@ -918,6 +918,7 @@ __device__ __forceinline__ double3 block_sum_d3(double x, double y, double z, do
 // cannot settle the nucleus cut.
 template <int ES>
 __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
+    pdl_trigger();   // a dependent launch may be scheduled; it waits for this kernel
     __shared__ double hm[256 + kWarps];
     __shared__ unsigned hc[256];
     __shared__ int s_dig[2], s_warp[kWarps], s_last;
@@ -1373,6 +1374,7 @@ __device__ int bf16_tie_id(Cluster &cl, int rank, const char *row, int V, uint32
 
 template <int ES>
 __global__ void __cluster_dims__(kNucSplit, 1, 1) __launch_bounds__(kThreads, 3) k_nucleus_hist(const NucleusArgs a) {
+    pdl_trigger();   // a dependent launch may be scheduled; it waits for this kernel
     static_assert(ES == 2, "value histogram: bf16 rows only");
     namespace cg = cooperative_groups;
     extern __shared__ __align__(16) unsigned s_cnt[];   // kNucKeys counters
@@ -1707,6 +1709,7 @@ __device__ void topset_split_block(const char *row, int V, float xstar, int last
 // overflowed or that difference is too small to trust, one pass of its own over the row).
 template <int ES>
 __global__ void __launch_bounds__(kThreads) k_topset(const TopSetArgs a) {
+    pdl_trigger();   // a dependent launch may be scheduled; it waits for this kernel
     __shared__ TopNCl s;
     extern __shared__ __align__(128) char ring[];
     __shared__ double s_red[3 * kWarps];

@@ -325,6 +325,7 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_stats(const StatsArgs a) {
     unsigned char *tiles = smem + kStatsCtlBytes;
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
+    pdl_trigger();   // the next kernel may be scheduled now; it waits for this one's results
 
     if (tid == 0) {
         for (int s = 0; s < kStatsStages; ++s) {

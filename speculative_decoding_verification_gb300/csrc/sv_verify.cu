@@ -29,6 +29,8 @@ template <int ES>
 __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
     __shared__ RowStat rs[2 * SV_MAX_K + 1];
     __shared__ int s_err;
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K = a.K, V = a.V;
@@ -303,7 +305,7 @@ static sv_status launch_verify(const VerifyPlan &pl, const AcceptArgs &acc_in, c
     acc.exact = reinterpret_cast<ExactItem *>(w + pl.off_exact);
     acc.exact_unc = reinterpret_cast<int *>(w + pl.off_xunc_n);
     acc.counters = counters;
-    k_accept<ES><<<B, kThreads, 0, stream>>>(acc);
+    if (launch_pdl(k_accept<ES>, dim3(B), dim3(kThreads), 0, stream, acc) != cudaSuccess) return SV_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
     // 4-5. draws and the float-float tier
     return launch_draw_tiers<ES>(pl, acc, nuc, top, w, B, di, stream);

@@ -164,6 +164,46 @@ sv_status sv_verify(const void *target_logits, int64_t t_row_pitch,
                     void *workspace, size_t workspace_bytes, sv_stream_t stream);
 
 /* ----------------------------------------------------------------------------------------
+ * sv_verify_host — sv_verify on inputs in host memory, outputs to host memory.
+ * [the same rule as sv_verify; the transfer is part of the call]
+ *
+ * The arguments mean what sv_verify's do, with these pointers in HOST memory (pinned memory,
+ * e.g. from cudaHostAlloc, makes the copies asynchronous and full-speed; pageable memory
+ * works through the driver's staging):
+ *   target_logits, draft_logits, draft_tokens, uniforms, temperature, top_p (or NULL),
+ *   top_k (or NULL), accept_len (written), out_tokens (written).
+ * stats and workspace stay in device memory; debug output is not offered.
+ *
+ * Copies: the call enqueues host-to-device copies, then the verification, then the
+ * device-to-host copies of accept_len and out_tokens, all on `stream`.
+ * - Inputs copied: every target row, and the draft rows j < K of each sequence with a nonzero
+ *   temperature (a greedy sequence's draft rows are never read, so they are not copied), plus
+ *   the tokens, uniforms, temperatures and filters.  The host reads the temperatures itself
+ *   to choose the rows.
+ * - Staging: the inputs land in device buffers carved from the workspace (rows padded to 16
+ *   bytes).  Copies are pitched, one per run of consecutive rows.
+ * - Completion: the host outputs are valid, and the host inputs may change, once the stream
+ *   has synchronised.
+ * - h2d_bytes: (host, may be NULL) receives the bytes copied to the device.
+ *
+ *  workspace  dev, >= sv_verify_host_workspace_size(B, K, V, dtype) bytes, 256-byte aligned.
+ * Returns sv_verify's argument errors, SV_ERR_WORKSPACE for a short workspace, SV_ERR_CUDA if
+ * a copy cannot be enqueued.
+ * -------------------------------------------------------------------------------------- */
+size_t sv_verify_host_workspace_size(int B, int K, int V, sv_dtype dtype);
+
+sv_status sv_verify_host(const void *target_logits, int64_t t_row_pitch,
+                         const void *draft_logits, int64_t d_row_pitch, int d_rows_per_seq,
+                         sv_dtype dtype,
+                         const int32_t *draft_tokens, const double *uniforms,
+                         int B, int K, int V,
+                         const float *temperature, const float *top_p, const int32_t *top_k,
+                         int saguaro_F, float saguaro_C,
+                         int32_t *accept_len, int32_t *out_tokens,
+                         sv_stats *stats, void *workspace, size_t workspace_bytes,
+                         size_t *h2d_bytes, sv_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
  * sv_verify_lazy — sv_verify that reads each sequence's rows position by position and stops at
  * its first rejection.
  * [SpS notes §3: after the first rejection the draft tokens to its right are discarded, so

@@ -134,6 +134,58 @@ def sv_verify(target, draft, draft_tokens, uniforms, temperature, top_p=None, sa
     return accept_len, out_tokens, dbg, stats
 
 
+def sv_verify_host(target, draft, draft_tokens, uniforms, temperature, top_p=None, saguaro_F=0, saguaro_C=1.0,
+                   accept_len=None, out_tokens=None, stats=None, workspace=None, stream=None, top_k=None,
+                   device=None):
+    """sv_verify_host on host (CPU) tensors: the library copies the rows the verification reads
+    (every target row; the draft rows of sequences with a nonzero temperature) and the small
+    inputs to the device, verifies there, and copies the outputs back, all on `stream`.
+
+    Pinned tensors (tensor.pin_memory()) make the copies asynchronous and full-speed.  target
+    [B, K+1, V] and draft [B, R>=K, V] (float32 or bfloat16); draft_tokens int32 [B, K]; uniforms
+    float64 [B, K+1]; temperature float32 [B]; top_p float32 [B] or None; top_k int32 [B] or
+    None.  Returns (accept_len int32 [B], out_tokens int32 [B, K+1]) as CPU tensors, valid once
+    the stream has synchronised, the stats block (device) and the bytes copied to the device."""
+    lib = load()
+    for name, t in (("target", target), ("draft", draft), ("draft_tokens", draft_tokens), ("uniforms", uniforms),
+                    ("temperature", temperature), ("top_p", top_p), ("top_k", top_k)):
+        if t is not None and t.is_cuda:
+            raise TypeError(f"sv_verify_host: {name} must be a host tensor")
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    B, K1, V = target.shape
+    K = K1 - 1
+    t_pitch, _ = _rows(target, "target")
+    if K > 0:
+        if draft.dtype != target.dtype:
+            raise TypeError("target and draft logits must share a dtype")
+        d_pitch, d_rows = _rows(draft, "draft")
+        d_ptr = _ptr(draft)
+    else:
+        d_pitch, d_rows, d_ptr = t_pitch, 1, ctypes.c_void_p(0)
+    for name, t, dt in (("draft_tokens", draft_tokens if K > 0 else None, torch.int32), ("uniforms", uniforms, torch.float64),
+                        ("temperature", temperature, torch.float32), ("top_p", top_p, torch.float32),
+                        ("top_k", top_k, torch.int32)):
+        if t is not None and (t.dtype != dt or not t.is_contiguous()):
+            raise TypeError(f"sv_verify_host: {name} must be a contiguous {dt} tensor")
+    pin = target.is_pinned()
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, pin_memory=pin)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, pin_memory=pin)
+    if stats is None:
+        stats = new_stats(dev)
+    ws_bytes = lib.sv_verify_host_workspace_size(B, K, V, _dtype_code(target))
+    ws = (workspace or _default_ws).get(ws_bytes, dev)
+    moved = ctypes.c_size_t(0)
+    code = lib.sv_verify_host(_ptr(target), t_pitch, d_ptr, d_pitch, d_rows, _dtype_code(target),
+                              _ptr(draft_tokens if K > 0 else None), _ptr(uniforms), B, K, V, _ptr(temperature),
+                              _ptr(top_p), _ptr(top_k), int(saguaro_F), float(saguaro_C), _ptr(accept_len),
+                              _ptr(out_tokens), _ptr(stats), _ptr(ws), ws.numel(), ctypes.c_void_p(ctypes.addressof(moved)),
+                              _stream(stream))
+    _abi.check("sv_verify_host", code)
+    return accept_len, out_tokens, stats, moved.value
+
+
 def sv_verify_static(target, draft, draft_tokens, uniforms, temperature, top_p=None, saguaro_F=0, saguaro_C=1.0,
                      accept_len=None, out_tokens=None, debug=None, stats=None, stream=None, top_k=None):
     """sv_verify without a workspace, for callers that cannot allocate device memory (a server

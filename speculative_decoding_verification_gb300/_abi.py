@@ -38,6 +38,9 @@ SIGNATURES = {
     "sv_verify_workspace_size": (c_size, [c_int, c_int, c_int]),
     "sv_verify": (c_int, [c_vp, c_i64, c_vp, c_i64, c_int, c_int, c_vp, c_vp, c_int, c_int, c_int, c_vp, c_vp,
                           c_vp, c_int, c_f32, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
+    "sv_verify_host_workspace_size": (c_size, [c_int, c_int, c_int, c_int]),
+    "sv_verify_host": (c_int, [c_vp, c_i64, c_vp, c_i64, c_int, c_int, c_vp, c_vp, c_int, c_int, c_int, c_vp, c_vp,
+                               c_vp, c_int, c_f32, c_vp, c_vp, c_vp, c_vp, c_size, c_vp, c_vp]),
     "sv_verify_lazy": (c_int, [c_vp, c_i64, c_vp, c_i64, c_int, c_int, c_vp, c_vp, c_int, c_int, c_int, c_vp, c_vp,
                                c_vp, c_int, c_f32, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
     "sv_verify_static": (c_int, [c_vp, c_i64, c_vp, c_i64, c_int, c_int, c_vp, c_vp, c_int, c_int, c_int, c_vp,

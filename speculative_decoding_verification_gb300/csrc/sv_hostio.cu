@@ -9,6 +9,28 @@ using namespace sv;
 
 namespace {
 
+// Copies the first K rows of every sequence with a nonzero temperature from pinned host memory
+// (read through its device mapping) into the staging rows: sequence b's row j goes to staging
+// row b * K + j.  16-byte words when both sides allow it, else 4-byte words, else bytes; a
+// grid-stride loop over (row, word).  One launch replaces one copy per run of rows.
+__global__ void k_gather_rows(const char *__restrict__ src, long long src_seq_bytes, long long src_pitch,
+                              const float *__restrict__ temperature, int B, int K, char *__restrict__ dst,
+                              long long dst_pitch, long long row_bytes, int wb) {
+    const long long words = row_bytes / wb;
+    const long long total = (long long)B * K * words;
+    const long long G = (long long)gridDim.x * blockDim.x;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += G) {
+        const long long r = i / words, w = i - r * words;
+        const int s = (int)(r / K), j = (int)(r % K);
+        if (temperature[s] == 0.0f) continue;   // a greedy sequence's draft rows are never read
+        const char *a = src + s * src_seq_bytes + j * src_pitch + w * wb;
+        char *d = dst + ((long long)s * K + j) * dst_pitch + w * wb;
+        if (wb == 16) *reinterpret_cast<uint4 *>(d) = *reinterpret_cast<const uint4 *>(a);
+        else if (wb == 4) *reinterpret_cast<uint32_t *>(d) = *reinterpret_cast<const uint32_t *>(a);
+        else *d = *a;
+    }
+}
+
 struct HostPlan {
     int64_t pitch;   // staging row pitch in elements (16-byte rows)
     size_t off_t, off_d, off_tok, off_u, off_T, off_tp, off_tk, off_al, off_ot, off_ws, ws_bytes, bytes;
@@ -70,16 +92,38 @@ extern "C" sv_status sv_verify_host(const void *target_logits, int64_t t_row_pit
         moved += bytes;
         return cudaMemcpyAsync(w + off, src, bytes, cudaMemcpyHostToDevice, stream) == cudaSuccess;
     };
+    // the temperatures first: the draft gather below reads them on the device
+    if (!copy(h.off_T, temperature, (size_t)B * sizeof(float))) return SV_ERR_CUDA;
     // every target row
     if (!copy_rows(w + h.off_t, static_cast<const char *>(target_logits), (size_t)t_row_pitch * es,
                    (size_t)B * (K + 1)))
         return SV_ERR_CUDA;
-    // draft rows j < K of the sampled sequences, one copy per run of consecutive ones (one per
-    // sequence when the host rows hold more than K rows per sequence)
+    // draft rows j < K of the sampled sequences: from pinned memory one gather launch, else one
+    // copy per run of consecutive sequences (one per sequence when the host rows hold more than
+    // K rows per sequence)
     if (K > 0) {
         const char *drf = static_cast<const char *>(draft_logits);
         const size_t spitch = (size_t)d_row_pitch * es;
-        for (int b0 = 0; b0 < B;) {
+        cudaPointerAttributes pa;
+        const bool pinned = cudaPointerGetAttributes(&pa, drf) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+                            pa.devicePointer != nullptr;
+        cudaGetLastError();   // a pageable pointer leaves no error behind
+        int n_seq = 0;
+        for (int b = 0; b < B; ++b) n_seq += temperature[b] != 0.0f ? 1 : 0;
+        if (pinned && n_seq > 0) {
+            DeviceInfo di;
+            if (!device_info(di)) return SV_ERR_CUDA;
+            const char *src = static_cast<const char *>(pa.devicePointer);
+            const uintptr_t al = (uintptr_t)src | (uintptr_t)spitch | (uintptr_t)row_bytes | (uintptr_t)dst_pitch;
+            const int wb = (al % 16 == 0) ? 16 : (al % 4 == 0) ? 4 : 1;
+            k_gather_rows<<<(unsigned)(di.sms * 8), 256, 0, stream>>>(
+                src, (long long)d_rows_per_seq * spitch, (long long)spitch,
+                reinterpret_cast<const float *>(w + h.off_T), B, K, w + h.off_d, (long long)dst_pitch,
+                (long long)row_bytes, wb);
+            if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+            moved += (size_t)n_seq * K * row_bytes;
+        }
+        for (int b0 = 0; b0 < B && !pinned;) {
             if (temperature[b0] == 0.0f) {
                 ++b0;
                 continue;
@@ -95,7 +139,6 @@ extern "C" sv_status sv_verify_host(const void *target_logits, int64_t t_row_pit
         if (!copy(h.off_tok, draft_tokens, (size_t)B * K * sizeof(int32_t))) return SV_ERR_CUDA;
     }
     if (!copy(h.off_u, uniforms, (size_t)B * (K + 1) * sizeof(double))) return SV_ERR_CUDA;
-    if (!copy(h.off_T, temperature, (size_t)B * sizeof(float))) return SV_ERR_CUDA;
     if (top_p && !copy(h.off_tp, top_p, (size_t)B * sizeof(float))) return SV_ERR_CUDA;
     if (top_k && !copy(h.off_tk, top_k, (size_t)B * sizeof(int32_t))) return SV_ERR_CUDA;
     if (h2d_bytes) *h2d_bytes = moved;

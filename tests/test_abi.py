@@ -96,6 +96,39 @@ def test_verify_rejects_bad_arguments_before_launch(lib):
     assert call(ws=fake + 8) == 5                # workspace not 256-byte aligned
 
 
+def test_verify_host_rejects_bad_arguments_before_any_copy(lib):
+    """sv_verify_host: argument and workspace errors come back before any copy is enqueued."""
+    fake = 1 << 20
+    ws = lib.sv_verify_host_workspace_size(4, 3, 1000, 1)
+    assert ws > lib.sv_verify_workspace_size(4, 3, 1000)          # staging on top of the verify workspace
+    assert lib.sv_verify_host_workspace_size(0, 3, 1000, 1) == 0
+    assert lib.sv_verify_host_workspace_size(4, 3, 1000, 7) == 0
+
+    def call(**kw):
+        args = dict(t=fake, tp=1000, d=fake, dp=1000, dr=3, dtype=1, tok=fake, u=fake, B=4, K=3, V=1000, T=fake,
+                    al=fake, ot=fake, ws=fake, wsb=ws)
+        kw = {**args, **kw}
+        return lib.sv_verify_host(kw["t"], kw["tp"], kw["d"], kw["dp"], kw["dr"], kw["dtype"], kw["tok"], kw["u"],
+                                  kw["B"], kw["K"], kw["V"], kw["T"], None, None, 0, 1.0, kw["al"], kw["ot"], None,
+                                  kw["ws"], kw["wsb"], None, None)
+    assert call(B=0) == 1
+    assert call(K=33) == 1
+    assert call(V=0) == 1
+    assert call(dtype=7) == 1
+    assert call(t=None) == 1
+    assert call(tp=999) == 1                     # pitch < V (host rows need no alignment)
+    assert call(tok=None) == 1
+    assert call(d=None) == 1
+    assert call(dr=2) == 1
+    assert call(u=None) == 1
+    assert call(T=None) == 1
+    assert call(al=None) == 1
+    assert call(ot=None) == 1
+    assert call(ws=None) == 5
+    assert call(wsb=ws - 1) == 5
+    assert call(ws=fake + 8) == 5
+
+
 def test_lookup_and_reuse_reject_bad_arguments(lib):
     f = (ctypes.c_int32 * 3)(1, 2, 3)
     fp = ctypes.cast(f, ctypes.c_void_p)

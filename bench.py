@@ -462,6 +462,15 @@ def config_rates(sv, dev, world, n):
     def call1():
         sv.sv_verify(tgt, drf, toks, u_d, T_d, accept_len=al, out_tokens=ot, stats=stats, workspace=ws)
     out["plain_b1"] = _round_line(w, n, world, *_graph_and_stream(call1, n, world), calls="verify")
+    # a graph of 100 consecutive calls, replayed: the per-call device time with no launch gaps
+    # between graph replays
+    g100 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g100):
+        for _ in range(100):
+            call1()
+    ms100 = _timed_calls(g100.replay, max(1, n // 10), world) / 100
+    out["plain_b1"]["graph_of_100_calls"] = {"value": whole_job_rate(1.0, world, ms100), "unit": "rounds/s",
+                                             "us_per_round": ms100 * 1e3}
     if sv.read_stats(stats)["status"] != 0:
         raise RuntimeError(f"config 1 failed: {sv.read_stats(stats)}")
     # ---- 3 ----
@@ -602,6 +611,11 @@ def run_ours(args, rank, world, local_rank):
             "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": dict(cfg, path=args.path, bytes_read_per_round=k1_bytes),
             "hbm_gbs_per_step": k1_bytes / (ms_max * 1e-3) / 1e9,
+            # the whole step against the nominal 8 TB/s, on all B (K+1) + B K logit rows and on
+            # the nominal count with the draft at K+1 rows
+            "step_roofline": {"bytes": B * (2 * K + 1) * V * 2, "nominal_bytes": B * (2 * K + 2) * V * 2,
+                              "of_8tbs": B * (2 * K + 1) * V * 2 / (ms_max * 1e-3) / 8e12,
+                              "nominal_of_8tbs": B * (2 * K + 2) * V * 2 / (ms_max * 1e-3) / 8e12},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": stats_traffic(w.B) if not lazy else None,
                          "kernel": "k_lazy" if lazy else "k_stats",

@@ -279,8 +279,9 @@ __global__ void __launch_bounds__(kThreads) k_topn(const TopNArgs a) {
 // the largest key of the vectors it sees.  A key that at least N of those maxima reach is a
 // lower bound tau on the row's N-th largest key (N distinct elements reach it), so the row's
 // first N are all among the elements of key >= tau.  A second pass over the share (from the
-// ring when the share fits in it, else streamed again) collects their codes, skipping every
-// vector whose largest key is below tau; each block ranks its candidates, and its first N go to
+// ring when the share fits in it, else streamed again) marks each thread's group of four
+// vectors whose largest key reaches tau, and one warp per marked group turns the elements of
+// key >= tau into codes; each block ranks its candidates, and its first N go to
 // block 0, which ranks the union: an element of the row's first N has all elements above it in
 // the union, so its rank there is its rank in the row.  A block whose candidates overflow
 // kTopNCand marks the row, and block 0 then takes it alone by the radix select.
@@ -517,8 +518,9 @@ __device__ bool cluster_topn(const cooperative_groups::cluster_group &cl, const 
     const int per = (n_vec + S - 1) / S;
     const int v0 = min(rank * per, n_vec), v1 = min(v0 + per, n_vec);
     const int n_chunks = (v1 - v0 + kTopNStageVecs - 1) / kTopNStageVecs;
-    // the ring carries chunk j of the sequence: the share once (j < n_chunks) and, unless the
-    // whole share stays in the ring, once more for the second pass (chunk j - n_chunks)
+    // the ring carries a sequence of chunks j: the share once (j < n_chunks) and, unless the
+    // whole share stays in the ring, once more for the second pass (chunk j - n_chunks of the
+    // share)
     uint64_t *gath = reinterpret_cast<uint64_t *>(ring + (size_t)stages * kTopNStageBytes);
     const bool resident = n_chunks <= stages;
     const int total = resident ? n_chunks : 2 * n_chunks;

@@ -1028,17 +1028,25 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
     // certification: cum and target come from the same per-element masses; the kept set is an
     // upper set, so its error per unit mass is at most the row's (weighted mean of |y|).  A
     // top-k cut alone involves no rounding.
-    const double cum_hi = above_m + jt * estar, cum_lo = above_m + (jt - 1) * estar;
-    const double rel = kEx2RelErr + 1.02 * kYRound * (A_row / S_fast) + 4.0 * kU32 + 1e-12;
-    const double E = rel * (cum_hi + target) + 1e-15 * S_fast;
-    const bool ambiguous = p_on && ((target - cum_lo) <= E || (cum_hi - target) <= E);
+    // the float64 certification by thread 0 alone (this GPU's float64 pipe is narrow)
+    __shared__ int s_amb;
+    if (threadIdx.x == 0) {
+        const double cum_hi = above_m + jt * estar, cum_lo = above_m + (jt - 1) * estar;
+        const double rel = kEx2RelErr + 1.02 * kYRound * (A_row / S_fast) + 4.0 * kU32 + 1e-12;
+        const double E = rel * (cum_hi + target) + 1e-15 * S_fast;
+        s_amb = p_on && ((target - cum_lo) <= E || (cum_hi - target) <= E) ? 1 : 0;
+    }
+    __syncthreads();
+    const bool ambiguous = s_amb != 0;
+    double m_num = 0.0, m_den = 1.0;   // the kept mass num / den, formed by thread 0 below
     NucleusCut out;
     out.ambiguous = ambiguous ? 1 : 0;
     out.mass_f = 1.0f;
     if (!ambiguous) {
         out.cut_x = xstar;
         out.cut_id = ordered_ties<ES>(row, a.V, kstar, jt, nullptr, s_warp, &s_last);
-        out.mass = cum_hi / S_fast;
+        m_num = above_m + jt * estar;
+        m_den = S_fast;
     } else {
         // ---- float-float tier: the same selects on exact masses ----
         tab[threadIdx.x] = kExp2Table[threadIdx.x];
@@ -1083,15 +1091,18 @@ __global__ void __launch_bounds__(kThreads) k_nucleus(const NucleusArgs a) {
         const bool unres = fabs(jr - rint(jr)) < 1e-9 * fmax(1.0, fabs(jr));
         out.cut_x = xx;
         out.cut_id = ordered_ties<ES>(row, a.V, kx, jx, nullptr, s_warp, &s_last);
-        out.mass = (A_x + jx * e_x) / S_x;
+        m_num = A_x + jx * e_x;
+        m_den = S_x;
         if (threadIdx.x == 0) {
             stats_add(a.stats, &a.stats->reresolved, 1);
             if (unres) stats_add(a.stats, &a.stats->unresolved, 1);
         }
     }
+    if (threadIdx.x != 0) return;
+    out.mass = m_num / m_den;
     out.log2_mass = log2(out.mass);
     out.mass_f = (float)out.mass;
-    if (threadIdx.x == 0) a.nuc[rid] = out;
+    a.nuc[rid] = out;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1611,7 +1622,7 @@ __global__ void __cluster_dims__(kNucSplit, 1, 1) __launch_bounds__(kThreads, 3)
     const int cut_id = pc.pos >= pc.count ? 0x7FFFFFFF
                                           : bf16_tie_id(cl, rank, row, a.V, (uint32_t)pc.key, pc.pos, s_wc, s_own, &s_res);
     cl.sync();   // no block leaves while another may still read its shared memory
-    if (rank != 0) return;
+    if (rank != 0 || threadIdx.x != 0) return;   // float64 on one thread: this GPU's float64 pipe is narrow
 
     const double above = ff_to_double(pc.mass), each = ff_to_double(pc.each), Sd = ff_to_double(S);
     const double cum_hi = above + pc.pos * each;
@@ -1622,15 +1633,13 @@ __global__ void __cluster_dims__(kNucSplit, 1, 1) __launch_bounds__(kThreads, 3)
     out.mass = cum_hi / Sd;
     out.log2_mass = log2(out.mass);
     out.mass_f = (float)out.mass;
-    if (threadIdx.x == 0) {
-        if (p_on) {
-            // each mass carries ~2^-44 and the float-float sums add ~2^-44 per level
-            const double tg = ff_to_double(target), cum_lo = above + (pc.pos - 1) * each;
-            const double E = 2e-11 * (cum_hi + tg);
-            if ((tg - cum_lo) <= E || (cum_hi - tg) <= E) stats_add(a.stats, &a.stats->unresolved, 1);
-        }
-        a.nuc[rid] = out;
+    if (p_on) {
+        // each mass carries ~2^-44 and the float-float sums add ~2^-44 per level
+        const double tg = ff_to_double(target), cum_lo = above + (pc.pos - 1) * each;
+        const double E = 2e-11 * (cum_hi + tg);
+        if ((tg - cum_lo) <= E || (cum_hi - tg) <= E) stats_add(a.stats, &a.stats->unresolved, 1);
     }
+    a.nuc[rid] = out;
 }
 
 template <int ES>

@@ -324,6 +324,7 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
     __shared__ int s_sub;
     __shared__ float2 s_pre;
     __shared__ int s_last_sub;
+    __shared__ float2 s_u;   // u as float-float, split once (float64 on one thread)
 
     const int d = blockIdx.x;
     const int n_items = *reinterpret_cast<volatile int *>(&a.counters->n_draws);
@@ -348,6 +349,8 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
     if (tid == 0) {
         s_sub = -1;
         s_last_sub = -1;
+        const float u_hi = __double2float_rn(it.u);
+        s_u = make_float2(u_hi, __double2float_rn(it.u - (double)u_hi));
     }
     __syncthreads();
     for (int off = 1; off < kThreads; off <<= 1) {
@@ -366,9 +369,7 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
     __syncthreads();
     // sum_v (q_v |y_q,v| + p_v |y_p,v|) over the normalised rows, from the statistics pass
     const float A = it.q.ay + (it.has_p ? it.p.ay : 0.f);
-    const float u_hi = __double2float_rn(it.u);
-    const float u_lo = __double2float_rn(it.u - (double)u_hi);
-    const ff thr = ff_mul(R, {u_hi, u_lo});
+    const ff thr = ff_mul(R, {s_u.x, s_u.y});
     // 3. the thread whose range holds thr finds the sub-chunk
     if (wsum.hi > 0.f && ff_diff(thr, excl) >= 0.f && ff_diff(thr, incl) < 0.f) {
         ff run = excl, pre = excl;

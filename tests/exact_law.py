@@ -114,3 +114,26 @@ def position_marginals(law, K, V):
         for i, t in enumerate(toks):
             joint[i, t] += pr
     return joint, joint.sum(axis=1)
+
+
+def sample_law(sample, V):
+    """Law of a one-uniform sampler u -> token id that is non-decreasing in u (an inverse-CDF
+    draw in id order), found by bisection on u: {token: probability} as a length-V array."""
+    law = np.zeros(V)
+    lo_u = 0.0
+    top = np.nextafter(1.0, 0.0)
+    cur = sample(0.0)
+    while True:
+        if sample(top) == cur:
+            law[cur] += 1.0 - lo_u
+            return law
+        lo, hi = lo_u, top
+        for _ in range(_ITERS):
+            mid = 0.5 * (lo + hi)
+            if sample(mid) == cur:
+                lo = mid
+            else:
+                hi = mid
+        law[cur] += hi - lo_u
+        lo_u = hi
+        cur = sample(hi)

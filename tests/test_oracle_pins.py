@@ -14,7 +14,7 @@ import scipy.stats
 
 import oracle
 from synth import philox
-from tests.exact_law import outcome_law, position_marginals
+from tests.exact_law import outcome_law, position_marginals, sample_law
 
 
 def softmax(x, T=1.0):
@@ -172,6 +172,33 @@ def test_saguaro_under_top_k_hand_example():
         assert r["tokens"][0, 0] == want and r["z_prime"][0, 0] == 1.0
 
 
+def test_saguaro_under_top_p_hand_example():
+    """sigma_{F,C} acts on the nucleus of the draft row (SSD notes §4.4 with SpS notes §3).  At
+    top_p = 0.75 the row (0.1, 0.4, 0.2, 0.2, 0.1) keeps {1, 2, 3}, cumulative 0.4, 0.6, 0.8, at
+    (1/2, 1/4, 1/4).  F=1, C=1/4 quarters the top token: (1/8, 1/4, 1/4) / (5/8) = (0.2, 0.4, 0.4),
+    P_D = 1/2, Z' = 5/8.  Scaling first and filtering after would give a different row: the scaled
+    row (1, 1, 2, 2, 1) / 7 reaches 0.75 only with token 0 as well, keeping (1, 1, 2, 2, 0) / 6.
+    F=2, C=0 zeroes tokens 1 and 2 and leaves token 3 alone (P_D = 3/4, Z' = 1/4)."""
+    x = np.log(np.array([[[0.1, 0.4, 0.2, 0.2, 0.1]]]))
+    one, tp = np.ones(1), np.array([0.75])
+    for u, want in [(0.0, 1), (0.19, 1), (0.21, 2), (0.59, 2), (0.61, 3), (0.99, 3)]:
+        r = oracle.draft_sample(x, np.array([[u]]), one, tp, 1, 0.25)
+        assert r["tokens"][0, 0] == want, (u, r["tokens"])
+        assert r["p_top"][0, 0] == pytest.approx(0.5, abs=1e-15)
+        assert r["z_prime"][0, 0] == pytest.approx(0.625, abs=1e-15)
+    for u in (0.0, 0.5, 0.99):
+        r = oracle.draft_sample(x, np.array([[u]]), one, tp, 2, 0.0)
+        assert r["tokens"][0, 0] == 3
+        assert r["p_top"][0, 0] == pytest.approx(0.75, abs=1e-15)
+        assert r["z_prime"][0, 0] == pytest.approx(0.25, abs=1e-15)
+    # verification divides by the same p': p'(s) for s = 1, 2, 3 and the nucleus mass of p
+    tgt = np.zeros((1, 2, 5))
+    for s, want in [(1, 0.2), (2, 0.4), (3, 0.4)]:
+        r = oracle.verify(tgt, x, np.array([[s]]), np.array([[0.5, 0.5]]), one, tp, 1, 0.25)
+        assert r["p_s"][0, 0] == pytest.approx(want, abs=1e-15)
+        assert r["mass_p"][0, 0] == pytest.approx(0.8, abs=1e-15)
+
+
 def test_inverse_cdf_hand_example():
     w = np.array([0.1, 0.0, 0.3, 0.6])
     for u, want in [(0.0, 0), (0.0999, 0), (0.1, 2), (0.3999, 2), (0.4, 3), (0.999, 3)]:
@@ -278,6 +305,43 @@ def test_exact_law_under_top_k_V4_K2(seed):
     np.testing.assert_allclose(joint[0], q2[0], atol=1e-12)
     for i in (1, 2):
         np.testing.assert_allclose(joint[i], exists[i] * q2[i], atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_exact_law_under_top_p_and_saguaro_V4_K2(seed):
+    """Brute force on V=4, K=2 with top-p on both models and sigma_{F,C} on the draft: draft
+    tokens drawn by draft_sample (its law read off by bisection on its uniform) and verified
+    with the same p' commit tokens whose law, position by position, is that of sampling the
+    target with the same nucleus and no transform (SSD notes §3.2: losslessness needs the
+    verifier to use p')."""
+    import functools
+    rng = np.random.default_rng(80 + seed)
+    tgt = rng.normal(0, 1.5, size=(3, 4))
+    drf = 0.5 * tgt[:2] + rng.normal(0, 1.0, size=(2, 4))
+    tp, F, C = 0.8, 1, 0.3
+    one, tpa = np.ones(1), np.array([tp])
+
+    def law_of(rows, F, C):
+        return np.stack([sample_law(lambda u, row=row: int(oracle.draft_sample(
+            row[None, None], np.array([[u]]), one, tpa, F, C)["tokens"][0, 0]), 4) for row in rows])
+
+    p_draw = law_of(drf, F, C)
+    q_want = law_of(tgt, 0, 1.0)
+    # the nucleus really cuts and sigma really moves mass, on at least one row each
+    assert np.any(q_want == 0.0) and np.any(p_draw == 0.0)
+    assert not np.allclose(p_draw, law_of(drf, 0, 1.0), atol=1e-6)
+    law = outcome_law(oracle.verify, tgt, drf, p_draw, top_p=tp, F=F, C=C)
+    assert sum(law.values()) == pytest.approx(1.0, abs=1e-12)
+    joint, exists = position_marginals(law, 2, 4)
+    np.testing.assert_allclose(joint[0], q_want[0], atol=1e-12)
+    for i in (1, 2):
+        np.testing.assert_allclose(joint[i], exists[i] * q_want[i], atol=1e-12)
+    # a verifier that divides by the untransformed nucleus is not lossless for these drafts
+    plain = functools.partial(oracle.verify, saguaro_F=0, saguaro_C=1.0)
+    bad = outcome_law(lambda t, d, s, u, T, p, F_, C_: plain(t, d, s, u, T, p), tgt, drf, p_draw,
+                      top_p=tp)
+    jb, _ = position_marginals(bad, 2, 4)
+    assert np.abs(jb[0] - q_want[0]).max() > 1e-3
 
 
 def test_mass_identities_single_position():

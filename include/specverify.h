@@ -207,7 +207,7 @@ sv_status sv_verify_host(const void *target_logits, int64_t t_row_pitch,
  * sv_verify_lazy — sv_verify that reads each sequence's rows position by position and stops at
  * its first rejection.
  * [SpS notes §3: after the first rejection the draft tokens to its right are discarded, so
- *  their rows decide nothing; SURVEY's "lazy positions"]
+ *  their rows decide nothing]
  *
  * Arguments, workspace (sv_verify_workspace_size) and outputs are those of sv_verify, and the
  * outputs are identical.  Rows after a sequence's first rejection (after its first greedy

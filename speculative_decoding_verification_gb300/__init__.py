@@ -85,11 +85,70 @@ def read_stats(t: torch.Tensor) -> dict:
     return out
 
 
-def _top_k(top_k):
-    """top_k must be a contiguous int32 CUDA tensor (or None): the library reads it as int32."""
-    if top_k is not None and (top_k.dtype != torch.int32 or not top_k.is_contiguous() or not top_k.is_cuda):
-        raise TypeError("top_k must be a contiguous int32 CUDA tensor")
-    return top_k
+def _cuda(t, name):
+    """The CUDA device of a logit tensor: the device entry points read device memory only."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor (host buffers go through sv_verify_host)")
+    return t.device
+
+
+def _arr(t, name, dtype, n, dev):
+    """t as the library reads or writes it: a contiguous `dtype` tensor on `dev` holding at least
+    n elements.  Anything else would be read with the wrong layout or past its end, so it is
+    refused here, before any work is queued."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != dev:
+        raise ValueError(f"{name} must be on {dev}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() < n:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs {n}")
+    return t
+
+
+def _opt(t, name, dtype, n, dev):
+    return None if t is None else _arr(t, name, dtype, n, dev)
+
+
+def _out(t, name, dtype, shape, dev):
+    """An output array: allocated when the caller passes none, else checked like an input."""
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=dev)
+    n = 1
+    for d in shape:
+        n *= d
+    return _arr(t, name, dtype, n, dev)
+
+
+def _pair(first, second, names, K, dev):
+    """Row pitch and rows of the first logit tensor and, when K > 0, of the second (same dtype and
+    device); with K = 0 the second is not read and its pointer is null."""
+    f_pitch, _ = _rows(first, names[0])
+    if K == 0:
+        return f_pitch, f_pitch, 1, ctypes.c_void_p(0)
+    if _cuda(second, names[1]) != dev:
+        raise ValueError(f"{names[0]} and {names[1]} must be on one device")
+    if second.dtype != first.dtype:
+        raise TypeError(f"{names[0]} and {names[1]} logits must share a dtype")
+    s_pitch, s_rows = _rows(second, names[1])
+    return f_pitch, s_pitch, s_rows, _ptr(second)
+
+
+def _seq_inputs(draft_tokens, uniforms, temperature, top_p, top_k, B, K, dev):
+    """The per-sequence inputs of the verify entry points, checked (draft tokens only when K > 0)."""
+    if K > 0:
+        _arr(draft_tokens, "draft_tokens", torch.int32, B * K, dev)
+    _arr(uniforms, "uniforms", torch.float64, B * (K + 1), dev)
+    _arr(temperature, "temperature", torch.float32, B, dev)
+    _opt(top_p, "top_p", torch.float32, B, dev)
+    _opt(top_k, "top_k", torch.int32, B, dev)
+
+
+def _stats(stats, dev):
+    return new_stats(dev) if stats is None else _arr(stats, "stats", torch.uint8, STATS_BYTES, dev)
 
 
 def sv_verify(target, draft, draft_tokens, uniforms, temperature, top_p=None, saguaro_F=0, saguaro_C=1.0,
@@ -107,28 +166,19 @@ def sv_verify(target, draft, draft_tokens, uniforms, temperature, top_p=None, sa
     lib = load()
     B, K1, V = target.shape
     K = K1 - 1
-    dev = target.device
-    t_pitch, _ = _rows(target, "target")
-    if K > 0:
-        if draft.dtype != target.dtype:
-            raise TypeError("target and draft logits must share a dtype")
-        d_pitch, d_rows = _rows(draft, "draft")
-        d_ptr = _ptr(draft)
-    else:
-        d_pitch, d_rows, d_ptr = t_pitch, 1, ctypes.c_void_p(0)
-    if accept_len is None:
-        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    dev = _cuda(target, "target")
+    t_pitch, d_pitch, d_rows, d_ptr = _pair(target, draft, ("target", "draft"), K, dev)
+    _seq_inputs(draft_tokens, uniforms, temperature, top_p, top_k, B, K, dev)
+    accept_len = _out(accept_len, "accept_len", torch.int32, (B,), dev)
+    out_tokens = _out(out_tokens, "out_tokens", torch.int32, (B, K + 1), dev)
     dbg = torch.empty((B, K + 1, _abi.SV_DEBUG_FIELDS), dtype=torch.float64, device=dev) if debug else None
-    if stats is None:
-        stats = new_stats(dev)
+    stats = _stats(stats, dev)
     ws_bytes = lib.sv_verify_workspace_size(B, K, V)
     ws = (workspace or _default_ws).get(ws_bytes, dev)
     fn = lib.sv_verify_lazy if lazy else lib.sv_verify
     code = fn(_ptr(target), t_pitch, d_ptr, d_pitch, d_rows, _dtype_code(target),
               _ptr(draft_tokens if K > 0 else None), _ptr(uniforms), B, K, V, _ptr(temperature),
-              _ptr(top_p), _ptr(_top_k(top_k)), int(saguaro_F), float(saguaro_C), _ptr(accept_len),
+              _ptr(top_p), _ptr(top_k), int(saguaro_F), float(saguaro_C), _ptr(accept_len),
               _ptr(out_tokens), _ptr(dbg), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream))
     _abi.check("sv_verify_lazy" if lazy else "sv_verify", code)
     return accept_len, out_tokens, dbg, stats
@@ -151,7 +201,9 @@ def sv_verify_host(target, draft, draft_tokens, uniforms, temperature, top_p=Non
                     ("temperature", temperature), ("top_p", top_p), ("top_k", top_k)):
         if t is not None and t.is_cuda:
             raise TypeError(f"sv_verify_host: {name} must be a host tensor")
-    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    dev = torch.device(device if device is not None else "cuda")
+    if dev.index is None:
+        dev = torch.device(dev.type, torch.cuda.current_device())
     B, K1, V = target.shape
     K = K1 - 1
     t_pitch, _ = _rows(target, "target")
@@ -162,18 +214,19 @@ def sv_verify_host(target, draft, draft_tokens, uniforms, temperature, top_p=Non
         d_ptr = _ptr(draft)
     else:
         d_pitch, d_rows, d_ptr = t_pitch, 1, ctypes.c_void_p(0)
-    for name, t, dt in (("draft_tokens", draft_tokens if K > 0 else None, torch.int32), ("uniforms", uniforms, torch.float64),
-                        ("temperature", temperature, torch.float32), ("top_p", top_p, torch.float32),
-                        ("top_k", top_k, torch.int32)):
-        if t is not None and (t.dtype != dt or not t.is_contiguous()):
-            raise TypeError(f"sv_verify_host: {name} must be a contiguous {dt} tensor")
     pin = target.is_pinned()
     if accept_len is None:
         accept_len = torch.empty(B, dtype=torch.int32, pin_memory=pin)
     if out_tokens is None:
         out_tokens = torch.empty((B, K + 1), dtype=torch.int32, pin_memory=pin)
-    if stats is None:
-        stats = new_stats(dev)
+    host = torch.device("cpu")
+    for name, t, dt, n in (("draft_tokens", draft_tokens if K > 0 else None, torch.int32, B * K),
+                           ("uniforms", uniforms, torch.float64, B * (K + 1)),
+                           ("temperature", temperature, torch.float32, B), ("top_p", top_p, torch.float32, B),
+                           ("top_k", top_k, torch.int32, B), ("accept_len", accept_len, torch.int32, B),
+                           ("out_tokens", out_tokens, torch.int32, B * (K + 1))):
+        _opt(t, name, dt, n, host)
+    stats = _stats(stats, dev)
     ws_bytes = lib.sv_verify_host_workspace_size(B, K, V, _dtype_code(target))
     ws = (workspace or _default_ws).get(ws_bytes, dev)
     moved = ctypes.c_size_t(0)
@@ -201,28 +254,20 @@ def sv_verify_static(target, draft, draft_tokens, uniforms, temperature, top_p=N
     lib = load()
     B, K1, V = target.shape
     K = K1 - 1
-    dev = target.device
-    t_pitch, _ = _rows(target, "target")
-    if K > 0:
-        if draft.dtype != target.dtype:
-            raise TypeError("target and draft logits must share a dtype")
-        d_pitch, d_rows = _rows(draft, "draft")
-        d_ptr = _ptr(draft)
-    else:
-        d_pitch, d_rows, d_ptr = t_pitch, 1, ctypes.c_void_p(0)
-    if accept_len is None:
-        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    dev = _cuda(target, "target")
+    t_pitch, d_pitch, d_rows, d_ptr = _pair(target, draft, ("target", "draft"), K, dev)
+    _seq_inputs(draft_tokens, uniforms, temperature, top_p, top_k, B, K, dev)
+    accept_len = _out(accept_len, "accept_len", torch.int32, (B,), dev)
+    out_tokens = _out(out_tokens, "out_tokens", torch.int32, (B, K + 1), dev)
     if debug is True:
         debug = torch.empty((B, K + 1, _abi.SV_DEBUG_FIELDS), dtype=torch.float64, device=dev)
     elif debug is False:
         debug = None
-    if stats is None:
-        stats = new_stats(dev)
+    _opt(debug, "debug", torch.float64, B * (K + 1) * _abi.SV_DEBUG_FIELDS, dev)
+    stats = _stats(stats, dev)
     code = lib.sv_verify_static(_ptr(target), t_pitch, d_ptr, d_pitch, d_rows, _dtype_code(target),
                                 _ptr(draft_tokens if K > 0 else None), _ptr(uniforms), B, K, V, _ptr(temperature),
-                                _ptr(top_p), _ptr(_top_k(top_k)), int(saguaro_F), float(saguaro_C), _ptr(accept_len),
+                                _ptr(top_p), _ptr(top_k), int(saguaro_F), float(saguaro_C), _ptr(accept_len),
                                 _ptr(out_tokens), _ptr(debug), _ptr(stats), _stream(stream))
     if code == _abi.SV_ERR_WORKSPACE:
         raise ValueError(f"sv_verify_static: B={B}, K={K}, V={V} needs more scratch than the "
@@ -243,23 +288,14 @@ def sv_fuzzy_verify(verifier, drafter, draft_tokens, uniforms, temperature, tau=
     lib = load()
     B, K1, V = verifier.shape
     K = K1 - 1
-    dev = verifier.device
-    v_pitch, _ = _rows(verifier, "verifier")
-    if K > 0:
-        if drafter.dtype != verifier.dtype:
-            raise TypeError("verifier and drafter logits must share a dtype")
-        d_pitch, d_rows = _rows(drafter, "drafter")
-        d_ptr = _ptr(drafter)
-    else:
-        d_pitch, d_rows, d_ptr = v_pitch, 1, ctypes.c_void_p(0)
+    dev = _cuda(verifier, "verifier")
+    v_pitch, d_pitch, d_rows, d_ptr = _pair(verifier, drafter, ("verifier", "drafter"), K, dev)
+    _seq_inputs(draft_tokens, uniforms, temperature, None, None, B, K, dev)
     code_mode = {"divergence": _abi.SV_ACCEPT_DIVERGENCE, "assisted": _abi.SV_ACCEPT_ASSISTED}[mode]
-    if accept_len is None:
-        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    accept_len = _out(accept_len, "accept_len", torch.int32, (B,), dev)
+    out_tokens = _out(out_tokens, "out_tokens", torch.int32, (B, K + 1), dev)
     div = torch.full((B, max(K, 1)), float("nan"), dtype=torch.float64, device=dev) if divergence else None
-    if stats is None:
-        stats = new_stats(dev)
+    stats = _stats(stats, dev)
     ws_bytes = lib.sv_fuzzy_verify_workspace_size(B, K, V)
     ws = (workspace or _default_ws).get(ws_bytes, dev)
     code = lib.sv_fuzzy_verify(_ptr(verifier), v_pitch, d_ptr, d_pitch, d_rows, _dtype_code(verifier),
@@ -278,21 +314,26 @@ def sv_tree_verify(target, draft, parents, tokens, uniforms, temperature, accept
     lib = load()
     B, N1, V = target.shape
     N = N1 - 1
-    dev = target.device
+    dev = _cuda(target, "target")
+    if _cuda(draft, "draft") != dev:
+        raise ValueError("target and draft must be on one device")
     if draft.dtype != target.dtype or draft.shape[1] < N1:
         raise TypeError("draft must share the target's dtype and hold N+1 rows per sequence")
     t_pitch, _ = _rows(target, "target")
     d_pitch, _ = _rows(draft, "draft")
-    if accept_len is None:
-        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty((B, N + 1), dtype=torch.int32, device=dev)
+    if N > 0:
+        _arr(parents, "parents", torch.int32, B * N, dev)
+        _arr(tokens, "tokens", torch.int32, B * N, dev)
+    _arr(uniforms, "uniforms", torch.float64, B * (N + 1), dev)
+    _arr(temperature, "temperature", torch.float32, B, dev)
+    accept_len = _out(accept_len, "accept_len", torch.int32, (B,), dev)
+    out_tokens = _out(out_tokens, "out_tokens", torch.int32, (B, N + 1), dev)
     if path is True:
         path = torch.empty((B, max(N, 1)), dtype=torch.int32, device=dev)
     elif path is False:
         path = None
-    if stats is None:
-        stats = new_stats(dev)
+    _opt(path, "path", torch.int32, B * N, dev)
+    stats = _stats(stats, dev)
     ws = (workspace or _default_ws).get(lib.sv_tree_verify_workspace_size(B, N, V), dev)
     code = lib.sv_tree_verify(_ptr(target), t_pitch, _ptr(draft), d_pitch, _dtype_code(target),
                               _ptr(parents if N > 0 else None), _ptr(tokens if N > 0 else None), _ptr(uniforms), B, N,
@@ -308,8 +349,12 @@ def sv_tree_reuse(parents, tokens, accept_len, out_tokens, reuse_node=None, stre
     lib = load()
     B, N = parents.shape
     K = out_tokens.shape[1] - 1
-    if reuse_node is None:
-        reuse_node = torch.empty(B, dtype=torch.int32, device=parents.device)
+    dev = _cuda(parents, "parents")
+    _arr(parents, "parents", torch.int32, B * N, dev)
+    _arr(tokens, "tokens", torch.int32, B * N, dev)
+    _arr(accept_len, "accept_len", torch.int32, B, dev)
+    _arr(out_tokens, "out_tokens", torch.int32, B * (K + 1), dev)
+    reuse_node = _out(reuse_node, "reuse_node", torch.int32, (B,), dev)
     code = lib.sv_tree_reuse(_ptr(parents), _ptr(tokens), N, _ptr(accept_len), _ptr(out_tokens), K, B,
                              _ptr(reuse_node), _stream(stream))
     _abi.check("sv_tree_reuse", code)
@@ -325,17 +370,19 @@ def sv_saguaro_sample(draft, uniforms, temperature, top_p=None, F=0, C=1.0, n_ro
     lib = load()
     B, R, V = draft.shape
     n_rows = R if n_rows is None else n_rows
-    dev = draft.device
+    dev = _cuda(draft, "draft")
     pitch, rows = _rows(draft, "draft")
-    if tokens is None:
-        tokens = torch.empty((B, n_rows), dtype=torch.int32, device=dev)
+    _arr(uniforms, "uniforms", torch.float64, B * n_rows, dev)
+    _arr(temperature, "temperature", torch.float32, B, dev)
+    _opt(top_p, "top_p", torch.float32, B, dev)
+    _opt(top_k, "top_k", torch.int32, B, dev)
+    tokens = _out(tokens, "tokens", torch.int32, (B, n_rows), dev)
     dbg = torch.empty((B, n_rows, 4), dtype=torch.float64, device=dev) if debug else None
-    if stats is None:
-        stats = new_stats(dev)
+    stats = _stats(stats, dev)
     ws_bytes = lib.sv_saguaro_sample_workspace_size(B, n_rows, V)
     ws = (workspace or _default_ws).get(ws_bytes, dev)
     code = lib.sv_saguaro_sample(_ptr(draft), pitch, rows, _dtype_code(draft), B, n_rows, V, _ptr(temperature),
-                                 _ptr(top_p), _ptr(_top_k(top_k)), int(F), float(C), _ptr(uniforms), _ptr(tokens),
+                                 _ptr(top_p), _ptr(top_k), int(F), float(C), _ptr(uniforms), _ptr(tokens),
                                  _ptr(dbg), _ptr(stats),
                                  _ptr(ws), ws.numel(), _stream(stream))
     _abi.check("sv_saguaro_sample", code)
@@ -364,12 +411,12 @@ def sv_cache_keys(draft, draft_tokens, F_int, keys=None, stats=None, workspace=N
     lib = load()
     B, R, V = draft.shape
     K = len(F_int) - 1
-    dev = draft.device
+    dev = _cuda(draft, "draft")
     pitch, rows = _rows(draft, "draft")
-    if keys is None:
-        keys = torch.empty((B, int(sum(F_int))), dtype=torch.int32, device=dev)
-    if stats is None:
-        stats = new_stats(dev)
+    if K > 0:
+        _arr(draft_tokens, "draft_tokens", torch.int32, B * K, dev)
+    keys = _out(keys, "keys", torch.int32, (B, int(sum(F_int))), dev)
+    stats = _stats(stats, dev)
     f_arr, f_ptr = _host_i32(F_int)
     ws_bytes = lib.sv_cache_keys_workspace_size(B, K, V)
     ws = (workspace or _default_ws).get(ws_bytes, dev)
@@ -383,8 +430,11 @@ def sv_cache_lookup(accept_len, out_tokens, keys, F_int, hit=None, stream=None):
     lib = load()
     B = accept_len.shape[0]
     K = len(F_int) - 1
-    if hit is None:
-        hit = torch.empty(B, dtype=torch.uint8, device=accept_len.device)
+    dev = _cuda(accept_len, "accept_len")
+    _arr(accept_len, "accept_len", torch.int32, B, dev)
+    _arr(out_tokens, "out_tokens", torch.int32, B * (K + 1), dev)
+    _arr(keys, "keys", torch.int32, B * int(sum(F_int)), dev)
+    hit = _out(hit, "hit", torch.uint8, (B,), dev)
     f_arr, f_ptr = _host_i32(F_int)
     code = lib.sv_cache_lookup(_ptr(accept_len), _ptr(out_tokens), _ptr(keys), f_ptr, B, K, _ptr(hit),
                                _stream(stream))
@@ -396,14 +446,12 @@ def sv_topk_rows(logits, kappa, temperature=None, ids=None, logprobs=None, stats
     """sv_topk_rows: logits [N, V]; returns (ids int32 [N, kappa], logprobs float64 [N, kappa], stats)."""
     lib = load()
     N, V = logits.shape
-    dev = logits.device
+    dev = _cuda(logits, "logits")
     pitch, _ = _rows(logits, "logits")
-    if ids is None:
-        ids = torch.empty((N, kappa), dtype=torch.int32, device=dev)
-    if logprobs is None:
-        logprobs = torch.empty((N, kappa), dtype=torch.float64, device=dev)
-    if stats is None:
-        stats = new_stats(dev)
+    _opt(temperature, "temperature", torch.float32, N, dev)
+    ids = _out(ids, "ids", torch.int32, (N, kappa), dev)
+    logprobs = _out(logprobs, "logprobs", torch.float64, (N, kappa), dev)
+    stats = _stats(stats, dev)
     ws_bytes = lib.sv_topk_rows_workspace_size(N, V)
     ws = (workspace or _default_ws).get(ws_bytes, dev)
     code = lib.sv_topk_rows(_ptr(logits), pitch, _dtype_code(logits), N, V, int(kappa), _ptr(temperature), _ptr(ids),
@@ -415,8 +463,11 @@ def sv_topk_rows(logits, kappa, temperature=None, ids=None, logprobs=None, stats
 def sv_mirror_reuse(branches, accept_len, out_tokens, reuse=None, stream=None):
     lib = load()
     B, kappa, gamma = branches.shape
-    if reuse is None:
-        reuse = torch.empty(B, dtype=torch.uint8, device=branches.device)
+    dev = _cuda(branches, "branches")
+    _arr(branches, "branches", torch.int32, B * kappa * gamma, dev)
+    _arr(accept_len, "accept_len", torch.int32, B, dev)
+    _arr(out_tokens, "out_tokens", torch.int32, B * (gamma + 1), dev)
+    reuse = _out(reuse, "reuse", torch.uint8, (B,), dev)
     code = lib.sv_mirror_reuse(_ptr(branches), _ptr(accept_len), _ptr(out_tokens), B, kappa, gamma, _ptr(reuse),
                                _stream(stream))
     _abi.check("sv_mirror_reuse", code)

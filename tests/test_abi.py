@@ -209,3 +209,54 @@ def test_js_table_header_values():
         p /= p.sum()
         terms = [max(a, b) * g_exact(abs(np.log2(a / b))) for a, b in zip(q, p)]
         assert sum(terms) == pytest.approx(oracle.jensen_shannon(q, p), rel=1e-12, abs=1e-15)
+
+
+def test_binding_refuses_bad_tensors_before_any_call(lib):
+    """The Python binding checks each array's dtype, device, contiguity and size before the library
+    sees its pointer: a float32 uniforms block, for one, would be read past its end as float64."""
+    import torch
+    import speculative_decoding_verification_gb300 as sv
+    B, K, V = 4, 3, 64
+    cpu = torch.device("cpu")
+    t = torch.zeros((B, K + 1, V))
+    tok = torch.zeros((B, K), dtype=torch.int32)
+    u = torch.zeros((B, K + 1), dtype=torch.float64)
+    T = torch.ones(B)
+    # the device entry points take CUDA tensors only: host memory goes through sv_verify_host
+    host_calls = [
+        lambda: sv.sv_verify(t, t[:, :K], tok, u, T),
+        lambda: sv.sv_verify(t, t[:, :K], tok, u, T, lazy=True),
+        lambda: sv.sv_verify_static(t, t[:, :K], tok, u, T),
+        lambda: sv.sv_fuzzy_verify(t, t[:, :K], tok, u, T),
+        lambda: sv.sv_tree_verify(t, t, tok, tok, u, T),
+        lambda: sv.sv_tree_reuse(tok, tok, T.int(), tok),
+        lambda: sv.sv_saguaro_sample(t, u, T),
+        lambda: sv.sv_cache_keys(t, tok, [1, 1, 1, 1]),
+        lambda: sv.sv_cache_lookup(T.int(), u.int(), tok, [1, 1, 1, 1]),
+        lambda: sv.sv_topk_rows(t[:, 0], 2),
+        lambda: sv.sv_mirror_reuse(tok[:, None, :], T.int(), u.int()),
+    ]
+    for call in host_calls:
+        with pytest.raises(TypeError, match="CUDA tensor"):
+            call()
+    # each refusal of the array check
+    sv._arr(u, "uniforms", torch.float64, B * (K + 1), cpu)
+    with pytest.raises(TypeError, match="float64"):
+        sv._arr(u.float(), "uniforms", torch.float64, B * (K + 1), cpu)
+    with pytest.raises(ValueError, match="contiguous"):
+        sv._arr(torch.zeros((K + 1, B), dtype=torch.float64).t(), "uniforms", torch.float64, B * (K + 1), cpu)
+    with pytest.raises(ValueError, match="elements"):
+        sv._arr(u[:2], "uniforms", torch.float64, B * (K + 1), cpu)
+    with pytest.raises(ValueError, match="must be on"):
+        sv._arr(torch.empty(B * (K + 1), dtype=torch.float64, device="meta"), "uniforms", torch.float64,
+                B * (K + 1), cpu)
+    with pytest.raises(TypeError, match="torch tensor"):
+        sv._arr(np.zeros(B * (K + 1)), "uniforms", torch.float64, B * (K + 1), cpu)
+    # the host entry: input sizes and the host buffers its copies write into
+    d = t[:, :K].contiguous()
+    with pytest.raises(ValueError, match="uniforms"):
+        sv.sv_verify_host(t, d, tok, u[:, :K].contiguous(), T, device="cuda:0")
+    with pytest.raises(TypeError, match="accept_len"):
+        sv.sv_verify_host(t, d, tok, u, T, accept_len=torch.zeros(B, dtype=torch.int64), device="cuda:0")
+    with pytest.raises(ValueError, match="out_tokens"):
+        sv.sv_verify_host(t, d, tok, u, T, out_tokens=torch.zeros((B, K), dtype=torch.int32), device="cuda:0")

@@ -275,6 +275,7 @@ def filter_rates(sv, dev, world, n):
             raise RuntimeError(f"filtered verify failed: {st}")
         out[name] = {"workload": w.name, "value": whole_job_rate(1.0, world, ms), "unit": "rounds/s",
                      "ms_per_round": ms, "timing": "CUDA graph of one call, replayed", "steps": n,
+                     "logit_bytes_per_round": round_logit_bytes(w),
                      "l2": "256 MB written between calls",
                      "stream_calls": {"value": whole_job_rate(1.0, world, ms_stream), "unit": "rounds/s",
                                       "ms_per_round": ms_stream},
@@ -325,7 +326,7 @@ def pyramid_rates(sv, dev, world, n, peak):
         rows = w.B * (2 * w.K + 1)
         byts = rows * w.V * 2
         out[name] = {"workload": w.name, "mode": mode, "value": whole_job_rate(1.0, world, ms), "unit": "rounds/s",
-                     "ms_per_round": ms, "steps": n, "rows_per_round": rows,
+                     "ms_per_round": ms, "steps": n, "rows_per_round": rows, "logit_bytes_per_round": byts,
                      "logit_gbs": byts / (ms * 1e-3) / 1e9, "mean_accept_len": float(al.float().mean().item()),
                      "reresolved": st["reresolved"], "unresolved": st["unresolved"]}
     return out
@@ -387,7 +388,8 @@ def tree_rates(sv, dev, world, n):
         ms = max_over_ranks(start.elapsed_time(end) / n, world)
         out[f"mirror_tree_B{B}"] = {"workload": f"branch-complete tree kappa=8 gamma=7 (56 nodes), B={B}, V={w.V} bf16",
                                     "value": whole_job_rate(1.0, world, ms), "unit": "rounds/s", "ms_per_round": ms,
-                                    "steps": n, "mean_accept_len": float(al.float().mean().item()),
+                                    "steps": n, "logit_bytes_per_round": round_logit_bytes(w),
+                                    "mean_accept_len": float(al.float().mean().item()),
                                     "child_tests": st["accept_tests"], "reresolved": st["reresolved"],
                                     "unresolved": st["unresolved"],
                                     "l2": "inputs of B=64 exceed L2; B=4 (0.14 GB) fits: no flush"}
@@ -428,9 +430,27 @@ def _graph_and_stream(call, n, world):
     return _timed_calls(g.replay, n, world), ms_stream
 
 
+def round_logit_bytes(w) -> int:
+    """Bytes of the logits one round of workload w takes as input: the K+1 target rows and the
+    draft rows of every sequence, each read once (the round's HBM floor)."""
+    return w.B * (w.K + 1 + w.rows_draft) * w.V * w.elem_bytes
+
+
+def add_hbm(line, peak):
+    """Give each filter, PyramidSD, tree and config line an "hbm" object: its input logit bytes
+    per round over its time per round, against the copy bandwidth `peak` (GB/s).  Rounds whose
+    inputs sit in L2 and whose time is launch-bound read far below it."""
+    for sec in ("filters", "pyramid", "tree", "configs"):
+        for v in line.get(sec, {}).values():
+            ms = v["ms_per_round"] if "ms_per_round" in v else v["us_per_round"] * 1e-3
+            gbs = v["logit_bytes_per_round"] / (ms * 1e-3) / 1e9
+            v["hbm"] = {"achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak}
+
+
 def _round_line(w, n, world, ms_graph, ms_stream, **extra):
     return dict(workload=w.name, value=whole_job_rate(1.0, world, ms_graph), unit="rounds/s",
                 us_per_round=ms_graph * 1e3, timing="CUDA graph of one round, replayed", steps=n,
+                logit_bytes_per_round=round_logit_bytes(w),
                 stream_calls={"value": whole_job_rate(1.0, world, ms_stream), "unit": "rounds/s",
                               "us_per_round": ms_stream * 1e3}, **extra)
 
@@ -635,6 +655,7 @@ def run_ours(args, rank, world, local_rank):
     line["pyramid"] = pyramid_rates(sv, dev, world, min(n, 200), peak)
     line["tree"] = tree_rates(sv, dev, world, min(n, 200))
     line["configs"] = config_rates(sv, dev, world, min(n, 200))
+    add_hbm(line, peak)
     if args.kernel_only:
         return line if rank == 0 else None
 

@@ -102,12 +102,9 @@ __global__ void k_selftest_exp2(double lo, double hi, long long n, unsigned long
     atomicMax(&out_bits[1], (unsigned long long)__double_as_longlong(e_ff));
 }
 
-// Every float32 x with key(lo) <= key(x) <= key(hi), key an order-preserving map of the bit
-// patterns: the same two errors as k_selftest_exp2, over all inputs instead of a sample.
-__device__ __forceinline__ unsigned f32_order_key(float x) {
-    const unsigned b = __float_as_uint(x);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
+// Every float32 x with key(lo) <= key(x) <= key(hi), key the order-preserving map of the bit
+// patterns that host_order_key computes: the same two errors as k_selftest_exp2, over all
+// inputs instead of a sample.  The kernel walks the keys and maps each back to its float.
 __device__ __forceinline__ float f32_from_order_key(unsigned k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }

@@ -1160,19 +1160,6 @@ __device__ __forceinline__ ff ff_shfl_up(ff v, int o) {
 __device__ __forceinline__ ff ff_shfl(ff v, int l) {
     return {__shfl_sync(0xFFFFFFFFu, v.hi, l), __shfl_sync(0xFFFFFFFFu, v.lo, l)};
 }
-// 32-bit shared::cluster address of a shared variable in block `rank` of the cluster.
-__device__ __forceinline__ uint32_t dsmem_map(const void *p, uint32_t rank) {
-    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-    return r;
-}
-
-// Atomic add to a shared::cluster address, no result.
-__device__ __forceinline__ void dsmem_red_add(uint32_t addr, uint32_t v) {
-    asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ bool ff_ge(ff a, ff b) { return a.hi > b.hi || (a.hi == b.hi && a.lo >= b.lo); }
 __device__ __forceinline__ ff ff_times(ff m, unsigned n) { return ff_mul(m, {(float)n, 0.f}); }
 

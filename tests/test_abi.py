@@ -46,7 +46,7 @@ def test_status_strings(lib):
 
 
 @pytest.mark.parametrize("budget,a,r,K", [(64, 0.7, 1.0, 5), (23, 0.8, 1.0, 5), (100, 0.5, 2.0, 3), (7.5, 0.3, 0.0, 0),
-                                          (1000, 0.95, 0.25, 12)])
+                                          (1000, 0.95, 0.25, 12), (3, 0.5, 0.0, 1), (6, 0.5, 0.0, 2)])
 def test_fanout_matches_oracle(lib, budget, a, r, K):
     import speculative_decoding_verification_gb300 as sv
     fr, fi = sv.sv_fanout(budget, a, r, K)

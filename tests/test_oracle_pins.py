@@ -501,6 +501,18 @@ def test_fanout_is_the_optimum_of_the_power_law_model(budget, a, r, K):
     assert np.all(np.abs(f_int - f_real) < 1.0)
 
 
+def test_fanout_remainder_ties_go_to_the_smaller_depth():
+    """a = 1/2, r = 0: the shape is (1, 1/2^k ..., 1/2^K * 2), so budget 3 at K = 1 splits
+    (1.5, 1.5) and budget 6 at K = 2 splits (3, 1.5, 1.5).  The floors leave one slot, and
+    equal remainders hand it to the smaller depth."""
+    f_real, f_int = oracle.fanout(3.0, 0.5, 0.0, 1)
+    np.testing.assert_array_equal(f_real, [1.5, 1.5])
+    assert list(f_int) == [2, 1]
+    f_real, f_int = oracle.fanout(6.0, 0.5, 0.0, 2)
+    np.testing.assert_array_equal(f_real, [3.0, 1.5, 1.5])
+    assert list(f_int) == [3, 2, 1]
+
+
 def test_fanout_budget64_values():
     f_real, f_int = oracle.fanout(64.0, 0.7, 1.0, 5)
     np.testing.assert_allclose(f_real, [14.676, 12.279, 10.273, 8.595, 7.191, 10.985], atol=5e-4)
@@ -546,6 +558,8 @@ def test_cache_keys_and_lookup_hand_example():
     hit = oracle.cache_lookup([0, 1, 0], np.array([[4, -1], [1, 3], [1, -1]]),
                               np.repeat(keys, 3, axis=0), [2, 3])
     assert list(hit) == [1, 1, 0]
+    # k = 0 and t* = 0, the first depth-1 key: the depth-0 keys (2, 4) decide, so no hit
+    assert oracle.cache_lookup([0], np.array([[0, -1]]), keys, [2, 3])[0] == 0
 
 
 def test_topk_rows_and_reuse_hand_example():
@@ -558,6 +572,12 @@ def test_topk_rows_and_reuse_hand_example():
     assert oracle.mirror_reuse(br, [1], np.array([[5, 2, -1, -1]]))[0] == 0
     assert oracle.mirror_reuse(br, [0], np.array([[3, -1, -1, -1]]))[0] == 1
     assert oracle.mirror_reuse(br, [3], np.array([[5, 6, 7, 1]]))[0] == 0    # k = gamma
+    assert oracle.mirror_reuse(br, [2], np.array([[5, 8, 9, -1]]))[0] == 1   # k = gamma - 1: a whole branch
+    # temperature first: at T = 1/2 the probabilities go as the squares (.01, .16, .04, .04, .01) / .26
+    y = np.log(np.array([[0.1, 0.4, 0.2, 0.2, 0.1]]))
+    ids, logp = oracle.topk_rows(y, 0.5, 3)
+    assert list(ids[0]) == [1, 2, 3]
+    np.testing.assert_allclose(logp[0], np.log(np.array([0.16, 0.04, 0.04]) / 0.26), atol=1e-14)
 
 
 # --------------------------------------------------------------------------------------
@@ -774,6 +794,25 @@ def test_tree_greedy_hand_example():
                            np.full((1, 5), 0.5), np.zeros(1))
     assert r["accept_len"][0] == 2 and list(r["path"][0]) == [2, 4, -1, -1]
     assert list(r["out_tokens"][0]) == [5, 4, 0, -1, -1]
+
+
+def test_tree_greedy_takes_the_first_of_equal_siblings():
+    """Root children 1 and 2 both hold token 5, the target's argmax at the root; the walk takes
+    node 1 (the lower index).  After node 1 the argmax is 1 (its child 3), after node 3 it is 0
+    (no child): path 1 -> 3, then 0.  Through node 2 it would have gone to node 4 (token 4)."""
+    V = 6
+    tgt = np.full((1, 5, V), -1.0)
+    for row, a in [(0, 5), (1, 1), (2, 4), (3, 0), (4, 3)]:
+        tgt[0, row, a] = 2.0
+    par, tok = np.array([[0, 0, 1, 2]]), np.array([[5, 5, 1, 4]])
+    r = oracle.tree_verify(tgt, np.zeros((1, 5, V)), par, tok, np.full((1, 5), 0.5), np.zeros(1))
+    assert r["accept_len"][0] == 2 and list(r["path"][0]) == [1, 3, -1, -1]
+    assert list(r["out_tokens"][0]) == [5, 1, 0, -1, -1]
+    # reuse walks the same way: (5, 1) ends at node 3; (5, 4) follows node 1 too, which has no
+    # child 4, so node 4 below the equal sibling 2 is not found (the reading that the walk and
+    # the reuse check both take)
+    assert list(oracle.tree_reuse(np.repeat(par, 2, 0), np.repeat(tok, 2, 0), [1, 1],
+                                  np.array([[5, 1, -1, -1, -1], [5, 4, -1, -1, -1]]))) == [3, -1]
 
 
 def test_tree_reuse_depth2_branching():

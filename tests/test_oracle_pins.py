@@ -84,6 +84,20 @@ def test_nucleus_hand_examples():
     np.testing.assert_array_equal(a, oracle.softmax_t(y, np.full(3, 0.7))[0])
 
 
+def test_nucleus_stops_at_the_prefix_that_reaches_top_p_exactly():
+    """SpS notes §6: the nucleus is the shortest prefix whose mass reaches top_p.  With the dyadic
+    masses (1/4, 1/2, 1/4) the prefix {1, 0} holds exactly 3/4, so top_p = 3/4 keeps those two
+    tokens (2/3 and 1/3) and not the third; a hair above 3/4 needs all three."""
+    q = np.array([[0.25, 0.5, 0.25]])
+    x = np.log(q)
+    d, m, n = oracle.nucleus(q, x, np.array([0.75]))
+    np.testing.assert_array_equal(d, [[1 / 3, 2 / 3, 0.0]])
+    assert m[0] == 0.75 and n[0] == 2
+    d, m, n = oracle.nucleus(q, x, np.array([np.nextafter(0.75, 1.0)]))
+    np.testing.assert_array_equal(d, q)
+    assert m[0] == 1.0 and n[0] == 3
+
+
 def test_top_k_hand_examples():
     """SpS notes §3: top-k acts on each distribution before the correction.  Probabilities
     (0.1, 0.4, 0.2, 0.2, 0.1): the plateaus at 0.2 and 0.1 are cut at the lowest ids."""

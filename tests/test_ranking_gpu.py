@@ -332,3 +332,11 @@ def test_reuse_and_lookup_hand_cases():
     hit = sv.sv_cache_lookup(torch.as_tensor([0, 1, 0], dtype=torch.int32, device="cuda"),
                              torch.as_tensor([[4, -1], [1, 3], [1, -1]], dtype=torch.int32, device="cuda"), keys, [2, 3])
     assert hit.cpu().tolist() == [1, 1, 0]
+    # k = gamma - 1: the whole of branch 1 is the committed prefix
+    one = torch.as_tensor([2], dtype=torch.int32, device="cuda")
+    assert sv.sv_mirror_reuse(br[:1], one, torch.as_tensor([[5, 8, 9, -1]], dtype=torch.int32,
+                                                         device="cuda")).cpu().tolist() == [1]
+    # t* = 0 is the first depth-1 key, not a depth-0 key: no hit at k = 0
+    hit0 = sv.sv_cache_lookup(torch.as_tensor([0], dtype=torch.int32, device="cuda"),
+                              torch.as_tensor([[0, -1]], dtype=torch.int32, device="cuda"), keys[:1], [2, 3])
+    assert hit0.cpu().tolist() == [0]

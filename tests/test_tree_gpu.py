@@ -135,6 +135,28 @@ def test_tree_reuse_matches_oracle():
     assert (want > 0).sum() >= 8
 
 
+def test_tree_greedy_equal_siblings():
+    """Root children 1 and 2 both hold token 5, the target's argmax at the root: the walk takes
+    node 1, then its child 3 (the argmax after node 1 is 1), then stops with 0; reuse follows the
+    same first child, so (5, 4) below node 2 is not found.  Outputs equal the oracle's."""
+    V = 8
+    x = np.full((1, 5, V), -1.0)
+    for row, am in [(0, 5), (1, 1), (2, 4), (3, 0), (4, 3)]:
+        x[0, row, am] = 2.0
+    par, tok = np.array([[0, 0, 1, 2]]), np.array([[5, 5, 1, 4]])
+    u, T = np.full((1, 5), 0.5), np.zeros(1, np.float32)
+    tgt = torch.as_tensor(x, dtype=torch.float32, device="cuda")
+    al, ot, path, st = run(tgt, torch.zeros_like(tgt), par, tok, u, T)
+    assert st["status"] == 0, st
+    ref = oracle.tree_verify(x, np.zeros_like(x), par, tok, u, T)
+    assert al[0] == 2 and list(path[0]) == [1, 3, -1, -1] and list(ot[0]) == [5, 1, 0, -1, -1]
+    np.testing.assert_array_equal(ot, ref["out_tokens"])
+    i32 = dict(dtype=torch.int32, device="cuda")
+    got = sv.sv_tree_reuse(torch.as_tensor(np.repeat(par, 2, 0), **i32), torch.as_tensor(np.repeat(tok, 2, 0), **i32),
+                           torch.as_tensor([1, 1], **i32), torch.as_tensor([[5, 1, -1, -1, -1], [5, 4, -1, -1, -1]], **i32))
+    assert got.cpu().tolist() == [3, -1]
+
+
 def test_tree_errors():
     rng = np.random.default_rng(41)
     w, tgt, drf, par, toks, u, T = tree_inputs(W.scaled(W.PLAIN, B=6, V=1000), 6, rng)

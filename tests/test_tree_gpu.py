@@ -139,7 +139,7 @@ def test_tree_greedy_equal_siblings():
     """Root children 1 and 2 both hold token 5, the target's argmax at the root: the walk takes
     node 1, then its child 3 (the argmax after node 1 is 1), then stops with 0; reuse follows the
     same first child, so (5, 4) below node 2 is not found.  Outputs equal the oracle's."""
-    V = 8
+    V = 1024
     x = np.full((1, 5, V), -1.0)
     for row, am in [(0, 5), (1, 1), (2, 4), (3, 0), (4, 3)]:
         x[0, row, am] = 2.0

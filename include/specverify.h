@@ -114,8 +114,10 @@ enum {
 /* Most drafted nodes in one tree of sv_tree_verify. */
 #define SV_MAX_TREE 128
 
+/* Library utilities (no counterpart on the pages): the text of a status code (a static string,
+ * never freed), and the version as major * 10000 + minor * 100 + patch. */
 const char *sv_status_string(sv_status s);
-int sv_version(void);   /* major * 10000 + minor * 100 + patch */
+int sv_version(void);
 
 /* ----------------------------------------------------------------------------------------
  * sv_verify — modified rejection sampling over the vocabulary for B sequences.

@@ -260,3 +260,19 @@ def test_binding_refuses_bad_tensors_before_any_call(lib):
         sv.sv_verify_host(t, d, tok, u, T, accept_len=torch.zeros(B, dtype=torch.int64), device="cuda:0")
     with pytest.raises(ValueError, match="out_tokens"):
         sv.sv_verify_host(t, d, tok, u, T, out_tokens=torch.zeros((B, K), dtype=torch.int32), device="cuda:0")
+
+
+def test_every_entry_point_cites_its_passage():
+    """Each declaration in the header follows a comment (the nearest one above it) that cites
+    the passage defining the operation (a bracketed page and section) or says that the pages
+    have no counterpart."""
+    text = open(os.path.join(ROOT, "include", "specverify.h")).read()
+    seen = set()
+    for m in re.finditer(r"^(?:[A-Za-z_0-9]+\s+)+\**\s*(sv_[a-z0-9_]+)\s*\(", text, re.M):
+        name = m.group(1)
+        before = text[: m.start()]
+        com = before[before.rindex("/*"): before.rindex("*/")]
+        seen.add(name)
+        assert "[" in com or "no counterpart" in com, name
+    assert {"sv_verify", "sv_saguaro_sample", "sv_fanout", "sv_cache_lookup", "sv_tree_verify"} <= seen
+    assert seen == set(declared_symbols())

@@ -37,6 +37,9 @@
  *    whose size comes from the matching *_workspace_size() function.  A workspace may be reused
  *    by consecutive calls on one stream; concurrent calls need distinct workspaces.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *    Every call works on the current device (cudaGetDevice): the stream and the device arrays
+ *    it names (the logits; for the integer calls their outputs) must belong to it, else the
+ *    call returns SV_ERR_INVALID_ARG after the size and workspace checks, before any launch.
  *    Argument errors are returned synchronously, before anything is launched.  Conditions only
  *    the GPU can see (non-finite logits, out-of-range tokens, a wait that timed out) are written
  *    to the optional device-side sv_stats block, which the caller reads after synchronising.
@@ -250,7 +253,10 @@ sv_status sv_verify_lazy(const void *target_logits, int64_t t_row_pitch,
  *    28.7 MiB and fits).  sv_verify_workspace_size(B, K, V) bounds the need from above.
  *  - Set-up: the first call on a device, with that device current, looks up the array's
  *    device address (cudaGetSymbolAddress) and caches it for that device; a failure there
- *    returns SV_ERR_CUDA.  Make that first call before any stream capture.
+ *    returns SV_ERR_CUDA.  Make that first call before any stream capture.  The cached
+ *    address belongs to the device's context at that time: after cudaDeviceReset, or after
+ *    the primary context is released and created again, it is stale, so a process that
+ *    resets a device must not call sv_verify_static on it afterwards.
  *  - Contents: every call shares the array, and it keeps the last call's contents.  Nothing
  *    in it has to start at zero: each call clears its counters (queued draws, queued
  *    float-float items, grid-barrier count, next unit of the statistics pass) with one

@@ -25,9 +25,23 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
-def _stream(stream):
-    s = stream if stream is not None else torch.cuda.current_stream()
+def _stream(stream, dev):
+    """The stream a call runs on: the caller's, which must belong to `dev`, or dev's current one.
+    The library launches on this stream and plans for the current device, so the two agree."""
+    if stream is None:
+        s = torch.cuda.current_stream(dev)
+    else:
+        s = stream
+        if s.device != dev:
+            raise ValueError(f"the stream is on {s.device}, the call's arrays on {dev}")
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _on(dev, fn, *args):
+    """Call the library with `dev` current: it takes the device of its workspace plan, static
+    scratch and SM count from the current device."""
+    with torch.cuda.device(dev):
+        return fn(*args)
 
 
 def _dtype_code(t):
@@ -176,10 +190,10 @@ def sv_verify(target, draft, draft_tokens, uniforms, temperature, top_p=None, sa
     ws_bytes = lib.sv_verify_workspace_size(B, K, V)
     ws = (workspace or _default_ws).get(ws_bytes, dev)
     fn = lib.sv_verify_lazy if lazy else lib.sv_verify
-    code = fn(_ptr(target), t_pitch, d_ptr, d_pitch, d_rows, _dtype_code(target),
+    code = _on(dev, fn, _ptr(target), t_pitch, d_ptr, d_pitch, d_rows, _dtype_code(target),
               _ptr(draft_tokens if K > 0 else None), _ptr(uniforms), B, K, V, _ptr(temperature),
               _ptr(top_p), _ptr(top_k), int(saguaro_F), float(saguaro_C), _ptr(accept_len),
-              _ptr(out_tokens), _ptr(dbg), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream))
+              _ptr(out_tokens), _ptr(dbg), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream, dev))
     _abi.check("sv_verify_lazy" if lazy else "sv_verify", code)
     return accept_len, out_tokens, dbg, stats
 
@@ -230,11 +244,11 @@ def sv_verify_host(target, draft, draft_tokens, uniforms, temperature, top_p=Non
     ws_bytes = lib.sv_verify_host_workspace_size(B, K, V, _dtype_code(target))
     ws = (workspace or _default_ws).get(ws_bytes, dev)
     moved = ctypes.c_size_t(0)
-    code = lib.sv_verify_host(_ptr(target), t_pitch, d_ptr, d_pitch, d_rows, _dtype_code(target),
+    code = _on(dev, lib.sv_verify_host, _ptr(target), t_pitch, d_ptr, d_pitch, d_rows, _dtype_code(target),
                               _ptr(draft_tokens if K > 0 else None), _ptr(uniforms), B, K, V, _ptr(temperature),
                               _ptr(top_p), _ptr(top_k), int(saguaro_F), float(saguaro_C), _ptr(accept_len),
                               _ptr(out_tokens), _ptr(stats), _ptr(ws), ws.numel(), ctypes.c_void_p(ctypes.addressof(moved)),
-                              _stream(stream))
+                              _stream(stream, dev))
     _abi.check("sv_verify_host", code)
     return accept_len, out_tokens, stats, moved.value
 
@@ -265,10 +279,10 @@ def sv_verify_static(target, draft, draft_tokens, uniforms, temperature, top_p=N
         debug = None
     _opt(debug, "debug", torch.float64, B * (K + 1) * _abi.SV_DEBUG_FIELDS, dev)
     stats = _stats(stats, dev)
-    code = lib.sv_verify_static(_ptr(target), t_pitch, d_ptr, d_pitch, d_rows, _dtype_code(target),
+    code = _on(dev, lib.sv_verify_static, _ptr(target), t_pitch, d_ptr, d_pitch, d_rows, _dtype_code(target),
                                 _ptr(draft_tokens if K > 0 else None), _ptr(uniforms), B, K, V, _ptr(temperature),
                                 _ptr(top_p), _ptr(top_k), int(saguaro_F), float(saguaro_C), _ptr(accept_len),
-                                _ptr(out_tokens), _ptr(debug), _ptr(stats), _stream(stream))
+                                _ptr(out_tokens), _ptr(debug), _ptr(stats), _stream(stream, dev))
     if code == _abi.SV_ERR_WORKSPACE:
         raise ValueError(f"sv_verify_static: B={B}, K={K}, V={V} needs more scratch than the "
                          f"{_abi.SV_STATIC_SCRATCH_BYTES >> 20} MiB static array; use sv_verify with a workspace")
@@ -298,10 +312,10 @@ def sv_fuzzy_verify(verifier, drafter, draft_tokens, uniforms, temperature, tau=
     stats = _stats(stats, dev)
     ws_bytes = lib.sv_fuzzy_verify_workspace_size(B, K, V)
     ws = (workspace or _default_ws).get(ws_bytes, dev)
-    code = lib.sv_fuzzy_verify(_ptr(verifier), v_pitch, d_ptr, d_pitch, d_rows, _dtype_code(verifier),
+    code = _on(dev, lib.sv_fuzzy_verify, _ptr(verifier), v_pitch, d_ptr, d_pitch, d_rows, _dtype_code(verifier),
                                _ptr(draft_tokens if K > 0 else None), _ptr(uniforms), B, K, V, _ptr(temperature),
                                float(tau), code_mode, _ptr(accept_len), _ptr(out_tokens), _ptr(div), _ptr(stats),
-                               _ptr(ws), ws.numel(), _stream(stream))
+                               _ptr(ws), ws.numel(), _stream(stream, dev))
     _abi.check("sv_fuzzy_verify", code)
     return accept_len, out_tokens, (div[:, :K] if div is not None else None), stats
 
@@ -335,10 +349,10 @@ def sv_tree_verify(target, draft, parents, tokens, uniforms, temperature, accept
     _opt(path, "path", torch.int32, B * N, dev)
     stats = _stats(stats, dev)
     ws = (workspace or _default_ws).get(lib.sv_tree_verify_workspace_size(B, N, V), dev)
-    code = lib.sv_tree_verify(_ptr(target), t_pitch, _ptr(draft), d_pitch, _dtype_code(target),
+    code = _on(dev, lib.sv_tree_verify, _ptr(target), t_pitch, _ptr(draft), d_pitch, _dtype_code(target),
                               _ptr(parents if N > 0 else None), _ptr(tokens if N > 0 else None), _ptr(uniforms), B, N,
                               V, _ptr(temperature), _ptr(accept_len), _ptr(out_tokens), _ptr(path), _ptr(stats),
-                              _ptr(ws), ws.numel(), _stream(stream))
+                              _ptr(ws), ws.numel(), _stream(stream, dev))
     _abi.check("sv_tree_verify", code)
     return accept_len, out_tokens, (path[:, :N] if path is not None else None), stats
 
@@ -355,8 +369,8 @@ def sv_tree_reuse(parents, tokens, accept_len, out_tokens, reuse_node=None, stre
     _arr(accept_len, "accept_len", torch.int32, B, dev)
     _arr(out_tokens, "out_tokens", torch.int32, B * (K + 1), dev)
     reuse_node = _out(reuse_node, "reuse_node", torch.int32, (B,), dev)
-    code = lib.sv_tree_reuse(_ptr(parents), _ptr(tokens), N, _ptr(accept_len), _ptr(out_tokens), K, B,
-                             _ptr(reuse_node), _stream(stream))
+    code = _on(dev, lib.sv_tree_reuse, _ptr(parents), _ptr(tokens), N, _ptr(accept_len), _ptr(out_tokens), K, B,
+                             _ptr(reuse_node), _stream(stream, dev))
     _abi.check("sv_tree_reuse", code)
     return reuse_node
 
@@ -381,10 +395,10 @@ def sv_saguaro_sample(draft, uniforms, temperature, top_p=None, F=0, C=1.0, n_ro
     stats = _stats(stats, dev)
     ws_bytes = lib.sv_saguaro_sample_workspace_size(B, n_rows, V)
     ws = (workspace or _default_ws).get(ws_bytes, dev)
-    code = lib.sv_saguaro_sample(_ptr(draft), pitch, rows, _dtype_code(draft), B, n_rows, V, _ptr(temperature),
+    code = _on(dev, lib.sv_saguaro_sample, _ptr(draft), pitch, rows, _dtype_code(draft), B, n_rows, V, _ptr(temperature),
                                  _ptr(top_p), _ptr(top_k), int(F), float(C), _ptr(uniforms), _ptr(tokens),
                                  _ptr(dbg), _ptr(stats),
-                                 _ptr(ws), ws.numel(), _stream(stream))
+                                 _ptr(ws), ws.numel(), _stream(stream, dev))
     _abi.check("sv_saguaro_sample", code)
     return tokens, dbg, stats
 
@@ -420,8 +434,8 @@ def sv_cache_keys(draft, draft_tokens, F_int, keys=None, stats=None, workspace=N
     f_arr, f_ptr = _host_i32(F_int)
     ws_bytes = lib.sv_cache_keys_workspace_size(B, K, V)
     ws = (workspace or _default_ws).get(ws_bytes, dev)
-    code = lib.sv_cache_keys(_ptr(draft), pitch, rows, _dtype_code(draft), _ptr(draft_tokens), f_ptr, B, K, V,
-                             _ptr(keys), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream))
+    code = _on(dev, lib.sv_cache_keys, _ptr(draft), pitch, rows, _dtype_code(draft), _ptr(draft_tokens), f_ptr, B, K, V,
+                             _ptr(keys), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream, dev))
     _abi.check("sv_cache_keys", code)
     return keys, stats
 
@@ -436,8 +450,8 @@ def sv_cache_lookup(accept_len, out_tokens, keys, F_int, hit=None, stream=None):
     _arr(keys, "keys", torch.int32, B * int(sum(F_int)), dev)
     hit = _out(hit, "hit", torch.uint8, (B,), dev)
     f_arr, f_ptr = _host_i32(F_int)
-    code = lib.sv_cache_lookup(_ptr(accept_len), _ptr(out_tokens), _ptr(keys), f_ptr, B, K, _ptr(hit),
-                               _stream(stream))
+    code = _on(dev, lib.sv_cache_lookup, _ptr(accept_len), _ptr(out_tokens), _ptr(keys), f_ptr, B, K, _ptr(hit),
+                               _stream(stream, dev))
     _abi.check("sv_cache_lookup", code)
     return hit
 
@@ -454,8 +468,8 @@ def sv_topk_rows(logits, kappa, temperature=None, ids=None, logprobs=None, stats
     stats = _stats(stats, dev)
     ws_bytes = lib.sv_topk_rows_workspace_size(N, V)
     ws = (workspace or _default_ws).get(ws_bytes, dev)
-    code = lib.sv_topk_rows(_ptr(logits), pitch, _dtype_code(logits), N, V, int(kappa), _ptr(temperature), _ptr(ids),
-                            _ptr(logprobs), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream))
+    code = _on(dev, lib.sv_topk_rows, _ptr(logits), pitch, _dtype_code(logits), N, V, int(kappa), _ptr(temperature), _ptr(ids),
+                            _ptr(logprobs), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream, dev))
     _abi.check("sv_topk_rows", code)
     return ids, logprobs, stats
 
@@ -468,24 +482,26 @@ def sv_mirror_reuse(branches, accept_len, out_tokens, reuse=None, stream=None):
     _arr(accept_len, "accept_len", torch.int32, B, dev)
     _arr(out_tokens, "out_tokens", torch.int32, B * (gamma + 1), dev)
     reuse = _out(reuse, "reuse", torch.uint8, (B,), dev)
-    code = lib.sv_mirror_reuse(_ptr(branches), _ptr(accept_len), _ptr(out_tokens), B, kappa, gamma, _ptr(reuse),
-                               _stream(stream))
+    code = _on(dev, lib.sv_mirror_reuse, _ptr(branches), _ptr(accept_len), _ptr(out_tokens), B, kappa, gamma, _ptr(reuse),
+                               _stream(stream, dev))
     _abi.check("sv_mirror_reuse", code)
     return reuse
 
 
 def sv_selftest_timeout(limit_cycles: int, stats=None, stream=None):
     lib = load()
+    dev = torch.device("cuda", torch.cuda.current_device())
     if stats is None:
-        stats = new_stats("cuda")
-    _abi.check("sv_selftest_timeout", lib.sv_selftest_timeout(int(limit_cycles), _ptr(stats), _stream(stream)))
+        stats = new_stats(dev)
+    _abi.check("sv_selftest_timeout", lib.sv_selftest_timeout(int(limit_cycles), _ptr(stats), _stream(stream, dev)))
     return stats
 
 
 def sv_selftest_exp2(lo: float, hi: float, n: int, stream=None):
     lib = load()
-    out = torch.zeros(2, dtype=torch.float64, device="cuda")
-    _abi.check("sv_selftest_exp2", lib.sv_selftest_exp2(float(lo), float(hi), int(n), _ptr(out), _stream(stream)))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    out = torch.zeros(2, dtype=torch.float64, device=dev)
+    _abi.check("sv_selftest_exp2", lib.sv_selftest_exp2(float(lo), float(hi), int(n), _ptr(out), _stream(stream, dev)))
     return out
 
 
@@ -493,8 +509,9 @@ def sv_selftest_exp2_all(lo: float, hi: float, stream=None):
     """Largest relative errors (fast, float-float) of the library's exponentials over every
     float32 input in [lo, hi], and the number of inputs evaluated."""
     lib = load()
-    out = torch.zeros(3, dtype=torch.float64, device="cuda")
-    _abi.check("sv_selftest_exp2_all", lib.sv_selftest_exp2_all(float(lo), float(hi), _ptr(out), _stream(stream)))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    out = torch.zeros(3, dtype=torch.float64, device=dev)
+    _abi.check("sv_selftest_exp2_all", lib.sv_selftest_exp2_all(float(lo), float(hi), _ptr(out), _stream(stream, dev)))
     torch.cuda.synchronize()
     r = out.cpu().tolist()
     return r[0], r[1], int(r[2])

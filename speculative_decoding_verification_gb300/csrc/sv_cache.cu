@@ -60,6 +60,7 @@ extern "C" sv_status sv_cache_lookup(const int32_t *accept_len, const int32_t *o
     }
     ko.off[K + 1] = (int)tot;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!on_current_device(s, keys, hit)) return SV_ERR_INVALID_ARG;
     k_cache_lookup<<<div_up(B, 256), 256, 0, s>>>(accept_len, out_tokens, keys, ko, B, K, hit);
     return cuda_status(cudaGetLastError());
 }
@@ -69,6 +70,7 @@ extern "C" sv_status sv_mirror_reuse(const int32_t *branches, const int32_t *acc
     if (!branches || !accept_len || !out_tokens || !reuse || B < 1 || kappa < 1 || gamma < 1)
         return SV_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!on_current_device(s, branches, reuse)) return SV_ERR_INVALID_ARG;
     k_mirror_reuse<<<div_up(B, 256), 256, 0, s>>>(branches, accept_len, out_tokens, B, kappa, gamma, reuse);
     return cuda_status(cudaGetLastError());
 }

@@ -521,6 +521,7 @@ extern "C" sv_status sv_fuzzy_verify(const void *verifier_logits, int64_t v_row_
     const int es = elem_size(dtype);
     const VerifyPlan pl = plan_verify(B, K, V, es);
     if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < pl.bytes) return SV_ERR_WORKSPACE;
+    if (!on_current_device(stream, verifier_logits, K > 0 ? drafter_logits : nullptr)) return SV_ERR_INVALID_ARG;
     if (stats && cudaMemsetAsync(stats, 0, sizeof(sv_stats), stream) != cudaSuccess) return SV_ERR_CUDA;
     FuzzyArgs fa{};
     // every row of both models is streamed (greedy sequences compare the two argmaxes)

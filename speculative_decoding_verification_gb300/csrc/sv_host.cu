@@ -34,6 +34,30 @@ bool device_info(DeviceInfo &out) {
     return true;
 }
 
+bool on_current_device(cudaStream_t s, const void *p0, const void *p1) {
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess) return false;
+    if (s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread) {
+        int sd = -1;
+        if (cudaStreamGetDevice(s, &sd) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        if (sd != cur) return false;
+    }
+    const void *ps[2] = {p0, p1};
+    for (const void *p : ps) {
+        if (p == nullptr) continue;
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (at.type == cudaMemoryTypeDevice && at.device != cur) return false;
+    }
+    return true;
+}
+
 namespace {
 thread_local cudaEvent_t t_prof_begin = nullptr, t_prof_end = nullptr;
 }
@@ -155,6 +179,7 @@ static unsigned host_order_key(float x) {
 extern "C" sv_status sv_selftest_exp2_all(float lo, float hi, double *out, sv_stream_t stream) {
     if (out == nullptr || !(lo <= hi) || lo < -125.0f || hi > 100.0f) return SV_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!on_current_device(s, out)) return SV_ERR_INVALID_ARG;
     if (cudaMemsetAsync(out, 0, 3 * sizeof(double), s) != cudaSuccess) return SV_ERR_CUDA;
     const unsigned k0 = host_order_key(lo), k1 = host_order_key(hi);
     const long long count = (long long)k1 - (long long)k0 + 1;
@@ -230,6 +255,7 @@ extern "C" sv_status sv_fanout(double budget, double a, double r, int K, double 
 extern "C" sv_status sv_selftest_timeout(int64_t limit_cycles, sv_stats *stats, sv_stream_t stream) {
     if (stats == nullptr || limit_cycles < 0) return SV_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!on_current_device(s, stats)) return SV_ERR_INVALID_ARG;
     if (cudaMemsetAsync(stats, 0, sizeof(sv_stats), s) != cudaSuccess) return SV_ERR_CUDA;
     k_selftest_timeout<<<1, 64, 0, s>>>(limit_cycles, stats);
     return cuda_status(cudaGetLastError());
@@ -238,6 +264,7 @@ extern "C" sv_status sv_selftest_timeout(int64_t limit_cycles, sv_stats *stats, 
 extern "C" sv_status sv_selftest_exp2(double lo, double hi, int64_t n, double *out, sv_stream_t stream) {
     if (out == nullptr || n < 1 || !(lo <= hi) || lo < -125.0 || hi > 100.0) return SV_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!on_current_device(s, out)) return SV_ERR_INVALID_ARG;
     if (cudaMemsetAsync(out, 0, 2 * sizeof(double), s) != cudaSuccess) return SV_ERR_CUDA;
     k_selftest_exp2<<<1024, 256, 0, s>>>(lo, hi, n, reinterpret_cast<unsigned long long *>(out));
     return cuda_status(cudaGetLastError());

@@ -80,6 +80,7 @@ extern "C" sv_status sv_verify_host(const void *target_logits, int64_t t_row_pit
     const int es = elem_size(dtype);
     const HostPlan h = plan_host(B, K, V, es);
     if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < h.bytes) return SV_ERR_WORKSPACE;
+    if (!on_current_device(stream, workspace)) return SV_ERR_INVALID_ARG;
     char *w = static_cast<char *>(workspace);
     const size_t row_bytes = (size_t)V * es, dst_pitch = (size_t)h.pitch * es;
     size_t moved = 0;

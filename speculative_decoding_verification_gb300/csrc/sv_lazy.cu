@@ -725,6 +725,7 @@ extern "C" sv_status sv_verify_lazy(const void *target_logits, int64_t t_row_pit
     const VerifyPlan pl = plan_verify(B, K, V, es);
     if (pl.lz_cap >= (1LL << 31)) return SV_ERR_INVALID_ARG;
     if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < pl.bytes) return SV_ERR_WORKSPACE;
+    if (!on_current_device(stream, target_logits, K > 0 ? draft_logits : nullptr)) return SV_ERR_INVALID_ARG;
     if (stats && cudaMemsetAsync(stats, 0, sizeof(sv_stats), stream) != cudaSuccess) return SV_ERR_CUDA;
     AcceptArgs acc{};
     acc.tgt = {static_cast<const char *>(target_logits), t_row_pitch * es, K + 1, K + 1, 0};

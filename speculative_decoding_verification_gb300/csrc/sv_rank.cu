@@ -137,6 +137,7 @@ extern "C" sv_status sv_cache_keys(const void *draft_logits, int64_t row_pitch, 
     const int es = elem_size(dtype);
     const size_t need = keys_ws(B, K, stride);
     if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need) return SV_ERR_WORKSPACE;
+    if (!on_current_device(stream, draft_logits, keys)) return SV_ERR_INVALID_ARG;
     if (stats && cudaMemsetAsync(stats, 0, sizeof(sv_stats), stream) != cudaSuccess) return SV_ERR_CUDA;
     int32_t *list = static_cast<int32_t *>(workspace);
     ta.base = static_cast<const char *>(draft_logits);
@@ -205,6 +206,7 @@ extern "C" sv_status sv_topk_rows(const void *logits, int64_t row_pitch, sv_dtyp
     const int es = elem_size(dtype);
     const TopKPlan tp = plan_topk(n_rows, V, es, kappa);
     if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < tp.bytes) return SV_ERR_WORKSPACE;
+    if (!on_current_device(stream, logits, ids)) return SV_ERR_INVALID_ARG;
     DeviceInfo di;
     if (!device_info(di)) return SV_ERR_CUDA;
     if (stats && cudaMemsetAsync(stats, 0, sizeof(sv_stats), stream) != cudaSuccess) return SV_ERR_CUDA;

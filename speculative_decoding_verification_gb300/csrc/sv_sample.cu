@@ -283,6 +283,7 @@ extern "C" sv_status sv_saguaro_sample(const void *draft_logits, int64_t row_pit
     const int es = elem_size(dtype);
     const SamplePlan sp = plan_sample(B, n_rows, V, es);
     if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < sp.bytes) return SV_ERR_WORKSPACE;
+    if (!on_current_device(stream, draft_logits)) return SV_ERR_INVALID_ARG;
     if (stats && cudaMemsetAsync(stats, 0, sizeof(sv_stats), stream) != cudaSuccess) return SV_ERR_CUDA;
     SampleArgs a{};
     a.rows = {static_cast<const char *>(draft_logits), row_pitch * es, rows_per_seq, n_rows, 0};

@@ -21,7 +21,9 @@ constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 void *g_scratch_addr[kMaxDevices] = {};
 
-// Set-up, once per device: look up the array's device address with that device current.
+// Set-up, once per device: look up the array's device address with that device current.  The
+// address is kept for the life of the process; it does not survive a reset of the device's
+// context (cudaDeviceReset), after which the module is loaded again elsewhere.
 sv_status scratch_address(void **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;

@@ -675,6 +675,7 @@ extern "C" sv_status sv_tree_verify(const void *target_logits, int64_t t_row_pit
     const int es = elem_size(dtype);
     const TreePlan pl = plan_tree(B, N, V, es);
     if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < pl.bytes) return SV_ERR_WORKSPACE;
+    if (!on_current_device(stream, target_logits, draft_logits)) return SV_ERR_INVALID_ARG;
     if (stats && cudaMemsetAsync(stats, 0, sizeof(sv_stats), stream) != cudaSuccess) return SV_ERR_CUDA;
     TreeArgs ta{};
     ta.tgt = {static_cast<const char *>(target_logits), t_row_pitch * es, N + 1, N + 1, 0};
@@ -700,6 +701,7 @@ extern "C" sv_status sv_tree_reuse(const int32_t *parents, const int32_t *tokens
     if (B < 1 || N < 0 || K < 0 || accept_len == nullptr || out_tokens == nullptr || reuse_node == nullptr)
         return SV_ERR_INVALID_ARG;
     if (N > 0 && (parents == nullptr || tokens == nullptr)) return SV_ERR_INVALID_ARG;
+    if (!on_current_device(stream, accept_len, reuse_node)) return SV_ERR_INVALID_ARG;
     k_tree_reuse<<<(unsigned)div_up(B, 128), 128, 0, stream>>>(parents, tokens, N, accept_len, out_tokens, K, B,
                                                                reuse_node);
     return cuda_status(cudaGetLastError());

@@ -337,6 +337,7 @@ sv_status sv::verify_entry(const void *target_logits, int64_t t_row_pitch, const
     const int es = elem_size(dtype);
     const VerifyPlan pl = plan_verify(B, K, V, es);
     if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < pl.bytes) return SV_ERR_WORKSPACE;
+    if (!on_current_device(stream, target_logits, K > 0 ? draft_logits : nullptr)) return SV_ERR_INVALID_ARG;
     if (stats && cudaMemsetAsync(stats, 0, sizeof(sv_stats), stream) != cudaSuccess) return SV_ERR_CUDA;
 
     AcceptArgs acc{};

@@ -276,3 +276,19 @@ def test_every_entry_point_cites_its_passage():
         assert "[" in com or "no counterpart" in com, name
     assert {"sv_verify", "sv_saguaro_sample", "sv_fanout", "sv_cache_lookup", "sv_tree_verify"} <= seen
     assert seen == set(declared_symbols())
+
+
+def test_binding_refuses_a_stream_of_another_device():
+    """The library plans for the current device and launches on the stream it is given, so the
+    binding runs each call with the arrays' device current and refuses a stream that belongs to
+    another device before the library is called (a fake stream object stands in: no GPU)."""
+    import types
+
+    import torch
+
+    import speculative_decoding_verification_gb300 as sv
+    other = types.SimpleNamespace(device=torch.device("cuda", 1), cuda_stream=0)
+    with pytest.raises(ValueError, match="stream is on cuda:1"):
+        sv._stream(other, torch.device("cuda", 0))
+    same = types.SimpleNamespace(device=torch.device("cuda", 0), cuda_stream=1234)
+    assert sv._stream(same, torch.device("cuda", 0)).value == 1234

@@ -126,8 +126,14 @@ __device__ __forceinline__ AcceptOutcome accept_test(const AcceptArgs &a, int b,
         const ff yp = ff_affine(xd, c, {(float)rp.r, 0.f});
         const ff dy = ff_sub(yq, yp);
         delta += 1e-12f * (fabsf(yq.hi) + fabsf(yp.hi));   // float-float y and c
-        const float e = ex2_fast(dy.hi) * fmaf(dy.lo, (float)kLn2, 1.0f);
-        ratio = e * __fdiv_rn(num, den);
+        // dy is about log2(den / num) wherever the test is close, i.e. up to +-log2 V and more:
+        // split it into an integer n and a fraction f in [-1/2, 1/2] (exact), so the fast
+        // exponential sees only f, inside the range its error bound was measured on, and 2^n
+        // scales the quotient exactly (to inf or 0 where it leaves the float32 range).
+        const float n = rintf(fminf(fmaxf(dy.hi, -512.0f), 512.0f));
+        const float f = __fsub_rn(dy.hi, n);
+        const float e = ex2_fast(f) * fmaf(dy.lo, (float)kLn2, 1.0f);
+        ratio = ldexpf(e * __fdiv_rn(num, den), (int)n);
     }
     delta *= 1.01f;
     const float rr = fminf(1.0f, ratio);

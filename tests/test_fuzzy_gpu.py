@@ -135,3 +135,15 @@ def test_k0_and_errors():
     T2[5] = -2.0
     _, _, _, st = run(ver, drf, toks, u, T2, 0.5)
     assert st["status"] == sv._abi.SV_ERR_INVALID_ARG and st["error_index"] == 5
+
+
+@pytest.mark.parametrize("greedy_every", [0, 4])
+def test_assisted_mode_full_stage_k25(greedy_every):
+    """The assisted mode at the qualifier -> target stage's full size (B=64, K=25, V=128256 bf16),
+    as the benchmark runs it: every sequence against the oracle.  With greedy_every=4 a quarter of
+    the sequences are greedy."""
+    w = W.PYRAMID_QT
+    ver, drf, toks, u, T = stage_inputs(w, 7, greedy_every=greedy_every)
+    out = run(ver, drf, toks, u, T, 0.0, mode="assisted")
+    check(out, reference(ver, drf, toks, u, T, 0.0, mode="assisted", chunk=4))
+    assert out[0].max() >= 3                           # positions deep into the 25 are reached

@@ -169,3 +169,56 @@ def test_tree_errors():
     bt[4, 0] = 5000
     _, _, _, st = run(tgt, drf, par, bt, u, T)
     assert st["status"] == sv._abi.SV_ERR_BAD_TOKEN and st["error_index"] == 4
+
+
+def branch_complete_parents(B, kappa, gamma):
+    """parents [B, kappa * gamma] of the branch-complete tree the benchmark verifies: kappa roots
+    below the context, each heading a chain of gamma drafted tokens (node = branch * gamma + depth)."""
+    par = np.zeros((B, kappa * gamma), dtype=np.int64)
+    for i in range(kappa):
+        for d in range(1, gamma + 1):
+            node = i * gamma + d
+            par[:, node - 1] = 0 if d == 1 else node - 1
+    return par
+
+
+def branch_complete_inputs(B, rng, round_idx):
+    """The benchmark's tree workload (Mirror recipe, kappa = 8 roots x depth gamma = 7, 56 nodes,
+    V = 151936 bf16, T = 1): each node's token drawn by the oracle's sampler from its parent's draft
+    row, the uniforms from rng."""
+    base = W.MIRROR
+    N = base.kappa * base.K
+    w = W.scaled(base, B=B, K=N, draft_rows_extra=1)
+    tgt, drf = W.logits(w, round_idx, device="cuda")
+    T = W.temperatures(w)
+    par = branch_complete_parents(B, base.kappa, base.K)
+    toks = np.zeros((B, N), dtype=np.int64)
+    ud = rng.random((B, N))
+    for b0 in range(0, B, 4):
+        d64 = to_f64(drf[b0:b0 + 4])
+        rows = np.take_along_axis(d64, par[b0:b0 + 4, :, None], axis=1)
+        toks[b0:b0 + 4] = oracle.draft_sample(rows, ud[b0:b0 + 4], T[b0:b0 + 4], np.ones(len(rows)))["tokens"]
+    u = rng.random((B, N + 1))
+    return tgt, drf, par, toks, u, T
+
+
+def _tree_reference(tgt, drf, par, toks, u, T, chunk=4):
+    parts = []
+    for b0 in range(0, tgt.shape[0], chunk):
+        s = slice(b0, b0 + chunk)
+        parts.append(oracle.tree_verify(to_f64(tgt[s]), to_f64(drf[s]), par[s], toks[s], u[s], T[s]))
+    return {k: np.concatenate([p[k] for p in parts]) for k in ("accept_len", "out_tokens", "path")}
+
+
+@pytest.mark.parametrize("B,round_idx", [(4, 0), (64, 1)])
+def test_branch_complete_tree(B, round_idx):
+    """The benchmark's branch-complete tree (eight roots under the context, depth 7, V = 151936) at
+    B = 4 and B = 64, every sequence against the oracle.  At B = 64 the residuals after several
+    rejected roots cancel often enough that some sequences need the float-float redo; those must
+    match too."""
+    rng = np.random.default_rng(500 + B)
+    tgt, drf, par, toks, u, T = branch_complete_inputs(B, rng, round_idx)
+    out = run(tgt, drf, par, toks, u, T)
+    check(out, _tree_reference(tgt, drf, par, toks, u, T))
+    if B == 64:
+        assert out[3]["reresolved"] > 0, out[3]

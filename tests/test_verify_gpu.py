@@ -249,3 +249,31 @@ def test_chi_square_committed_tokens_V8_gpu(K):
     a = np.minimum(pd, qf[:K]).sum(axis=1)
     want = np.array([np.prod(a[:j]) * (1 - a[j]) for j in range(K)] + [np.prod(a)])
     assert scipy.stats.chisquare(np.bincount(al, minlength=K + 1), n * want).pvalue > 0.01
+
+
+@pytest.mark.parametrize("K", [13, 25, 31, 32])
+@pytest.mark.parametrize("lazy", [False, True])
+@pytest.mark.parametrize("close", [False, True])
+def test_long_drafts(K, lazy, close):
+    """K up to the library's maximum (32), greedy and sampled sequences mixed (the large-batch
+    recipe at B=16, V=128256 bf16).  With close=True the draft is nearly the target, so runs of
+    accepted tokens reach deep positions and whole drafts are accepted; with close=False most
+    sequences stop early.  sv_verify and sv_verify_lazy (which reads positions 0 and 1 one at a
+    time and the rest in one batch) both against the oracle."""
+    extra = dict(draft_scale=0.98, draft_sigma=0.12) if close else {}
+    w = W.scaled(W.LARGE_BATCH, B=16, K=K, **extra)
+    inp = make_inputs(w, 3 + K, chunk=4)
+    ref = oracle_verify(inp, w, chunk=2)
+    a = gpu_args(inp)
+    al, ot, dbg, st = sv.sv_verify(inp["target"], inp["draft"], a["draft_tokens"], a["uniforms"], a["temperature"],
+                                   debug=not lazy, lazy=lazy)
+    torch.cuda.synchronize()
+    al, ot, st = al.cpu().numpy(), ot.cpu().numpy(), sv.read_stats(st)
+    if lazy:
+        assert st["status"] == 0, st
+        np.testing.assert_array_equal(al, ref["accept_len"])
+        np.testing.assert_array_equal(ot, ref["out_tokens"])
+    else:
+        compare(w, inp, ref, al, ot, dbg.cpu().numpy(), st)
+    if close:
+        assert (al == K).any() and al.max() == K

@@ -147,22 +147,40 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def oracle_seconds(tgt, drf, K, seqs, T, u, toks, chunk=32):
-    """Seconds the float64 oracle spends verifying the given sequences one by one.  The exact
-    float64 copies of their logits are made chunk by chunk outside the timed region."""
-    import oracle
+def _round_parts(w, r, parts, dev):
+    """Round r of workload w as the oracle workers' shares of its sequences: raw bf16 rows,
+    uniforms, temperatures (generated on `dev`, copied to the host outside any timing)."""
     import torch
-    total = 0.0
-    for i in range(0, len(seqs), chunk):
-        sel = seqs[i:i + chunk]
-        idx = torch.as_tensor(sel, device=tgt.device)
-        t64 = tgt.index_select(0, idx).double().cpu().numpy()
-        d64 = drf.index_select(0, idx)[:, :K].double().cpu().numpy()
-        t0 = time.perf_counter()
-        for j, b in enumerate(sel):
-            oracle.verify(t64[j:j + 1], d64[j:j + 1], toks[b:b + 1], u[b:b + 1], T[b:b + 1], np.ones(1), 0, 1.0)
-        total += time.perf_counter() - t0
-    return total
+    from oracle.parallel import split_ranges
+    from synth import workloads as W
+    tgt, drf = W.logits(w, r, device=dev)
+    u_draft, u, _ = W.round_uniforms(w, r)
+    T = W.temperatures(w)
+    tp = W.top_ps(w).astype(np.float64)
+    t_raw = tgt.view(torch.int16).cpu().numpy().view(np.uint16)
+    d_raw = drf.view(torch.int16).cpu().numpy().view(np.uint16)
+    del tgt, drf
+    return [{"target": (t_raw[lo:hi], "bf16"), "draft": (d_raw[lo:hi], "bf16"), "u": (u[lo:hi], None),
+             "u_draft": (u_draft[lo:hi], None), "T": (T[lo:hi], None), "top_p": (tp[lo:hi], None)}
+            for lo, hi in split_ranges(w.B, parts)]
+
+
+def oracle_round_seconds(w, rounds, workers, dev, repeats=1):
+    """Wall seconds of the float64 oracle's verification of whole rounds of workload w on
+    `workers` spawned processes (the sequences split evenly, one oracle call per sequence).
+    For each round index in `rounds` the rows are loaded into the workers, widened to float64
+    and the draft tokens drawn by the oracle's own sampler, all untimed; then verification of
+    the whole round is timed `repeats` times.  Returns one time per timed run."""
+    from oracle.parallel import OraclePool
+    times = []
+    with OraclePool(workers) as pool:
+        for r in rounds:
+            pool.load(_round_parts(w, r, pool.n, dev))
+            pool.run("oracle.parallel:draft_tokens", {"K": w.K})
+            for _ in range(repeats):
+                _, sec = pool.run("oracle.parallel:verify_chunk", {"K": w.K})
+                times.append(sec)
+    return times
 
 
 # ------------------------------------------------------------------------------------------
@@ -184,40 +202,26 @@ def config_block(w):
 
 
 def run_reference(args, rank, world):
-    """The float64 oracle on the host cores (rank 0 only): every step verifies a bounded sample
-    of the round's sequences; the rate is extrapolated to whole 512-sequence rounds."""
+    """The float64 oracle on all host cores (rank 0 only): every step verifies one whole round of
+    the workload (512 sequences, the same round each step, as the library's steps do) on one
+    spawned process per core."""
     if rank != 0:
         return None
     import torch
-    import oracle
-    from synth import workloads as W
+    from oracle.parallel import host_cores
     w = workload(0)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    tgt, drf = W.logits(w, 0, device=dev)
-    u_draft, u, _ = W.round_uniforms(w, 0)
-    T = W.temperatures(w)
-    # sequences per step: at most 16, and about 4096 over the whole run (~40 s of one core)
-    per_step = int(os.environ.get("SV_ORACLE_SEQS", "0")) or max(1, min(16, 4096 // max(1, args.warmup + args.steps)))
-    seqs_all = [s % w.B for s in range(per_step * (args.warmup + args.steps))]
-    toks = np.zeros((w.B, w.K), dtype=np.int64)
-    for b0 in range(0, w.B, 64):
-        d64 = drf[b0:b0 + 64, : w.K].double().cpu().numpy()
-        toks[b0:b0 + 64] = oracle.draft_sample(d64, u_draft[b0:b0 + 64, : w.K], T[b0:b0 + 64],
-                                               np.ones(len(d64)))["tokens"]
-    times = []
-    for i in range(args.warmup + args.steps):
-        sel = seqs_all[i * per_step:(i + 1) * per_step]
-        dt = oracle_seconds(tgt, drf, w.K, sel, T, u, toks)
-        if i >= args.warmup:
-            times.append(dt / len(sel) * w.B)        # seconds per full round
+    cores = host_cores()
+    times = oracle_round_seconds(w, [0], cores, dev, repeats=args.warmup + args.steps)[args.warmup:]
     sec = statistics.mean(times)
     value = 1.0 / sec
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1000.0, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_block(w),
-            "cpu_baseline": {"value": value, "unit": "rounds/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{per_step} of 512 sequences per step, single-thread float64 numpy "
-                                       f"oracle, extrapolated to whole rounds"},
+            "cpu_baseline": {"value": value, "unit": "rounds/s", "cores": cores, "kind": "oracle",
+                             "sample": f"whole rounds: all 512 sequences of round 0 per step on {cores} spawned "
+                                       "processes, float64 numpy oracle, one call per sequence; widening the rows "
+                                       "and drawing the draft tokens untimed"},
             "e2e": {"value": value, "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -430,6 +434,15 @@ def _graph_and_stream(call, n, world):
     return _timed_calls(g.replay, n, world), ms_stream
 
 
+def whole_call_roofline(bytes_read, ms, peak, peak_kind):
+    """The whole verification call as a fraction of the HBM roofline, on the logit bytes it
+    actually reads (every target row and the draft rows of sampled sequences for sv_verify; the
+    rows up to each first rejection for sv_verify_lazy), over the call's own time."""
+    gbs = bytes_read / (ms * 1e-3) / 1e9
+    return {"bytes": int(bytes_read), "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak,
+            "peak_source": f"{peak_kind} copy bandwidth", "of_8tbs": gbs / 8000.0}
+
+
 def round_logit_bytes(w) -> int:
     """Bytes of the logits one round of workload w takes as input: the K+1 target rows and the
     draft rows of every sequence, each read once (the round's HBM floor)."""
@@ -631,11 +644,9 @@ def run_ours(args, rank, world, local_rank):
             "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": dict(cfg, path=args.path, bytes_read_per_round=k1_bytes),
             "hbm_gbs_per_step": k1_bytes / (ms_max * 1e-3) / 1e9,
-            # the whole step against the nominal 8 TB/s, on all B (K+1) + B K logit rows and on
-            # the nominal count with the draft at K+1 rows
-            "step_roofline": {"bytes": B * (2 * K + 1) * V * 2, "nominal_bytes": B * (2 * K + 2) * V * 2,
-                              "of_8tbs": B * (2 * K + 1) * V * 2 / (ms_max * 1e-3) / 8e12,
-                              "nominal_of_8tbs": B * (2 * K + 2) * V * 2 / (ms_max * 1e-3) / 8e12},
+            # the whole call on the logit bytes it reads, against the measured copy bandwidth and
+            # the nominal 8 TB/s
+            "step_roofline": whole_call_roofline(k1_bytes, ms_max, peak, peak_kind),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": stats_traffic(w.B) if not lazy else None,
                          "kernel": "k_lazy" if lazy else "k_stats",
@@ -650,7 +661,8 @@ def run_ours(args, rank, world, local_rank):
     b_o = st_o["rows"] * V * 2
     line[other] = {"value": whole_job_rate(1.0, world, ms_o), "unit": "rounds/s", "ms_per_step": ms_o,
                    "bytes_read_per_round": b_o, "kernel": "k_stats" if lazy else "k_lazy", "kernel_ms": k_o,
-                   "kernel_gbs": b_o / (k_o * 1e-3) / 1e9, "frac": b_o / (k_o * 1e-3) / 1e9 / peak}
+                   "kernel_gbs": b_o / (k_o * 1e-3) / 1e9, "frac": b_o / (k_o * 1e-3) / 1e9 / peak,
+                   "step_roofline": whole_call_roofline(b_o, ms_o, peak, peak_kind)}
     line["filters"] = filter_rates(sv, dev, world, min(n, 200))
     line["pyramid"] = pyramid_rates(sv, dev, world, min(n, 200), peak)
     line["tree"] = tree_rates(sv, dev, world, min(n, 200))
@@ -709,15 +721,20 @@ def run_ours(args, rank, world, local_rank):
     line["e2e"] = {"value": whole_job_rate(1.0, world, e2e_ms), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                    "call": "sv_verify_lazy after host copies" if lazy else "sv_verify_host (host buffers)"}
-    # ---- CPU baseline: the oracle on one whole round (rank 0) ----
-    if rank == 0:
-        n_seq = B
-        seqs = list(range(min(n_seq, B)))
-        toks = toks_d.cpu().numpy().astype(np.int64)
-        dt = oracle_seconds(tgt, drf, K, seqs, T, u, toks)
-        line["cpu_baseline"] = {"value": len(seqs) / dt / B, "unit": "rounds/s", "cores": 1, "kind": "oracle",
-                                "sample": f"{len(seqs)} of {B} sequences of the round (half greedy), "
-                                          f"{dt:.1f} s single-thread float64 numpy"}
+    # ---- CPU baseline: the float64 oracle on whole rounds, all host cores and one (rank 0) ----
+    if rank == 0 and world == 1:
+        from oracle.parallel import host_cores
+        cores = host_cores()
+        many = oracle_round_seconds(w, [0, 1, 2, 3, 4], cores, dev)
+        one = oracle_round_seconds(w, [0, 1, 2], 1, dev)
+        line["cpu_baseline"] = {"value": len(many) / sum(many), "unit": "rounds/s", "cores": cores, "kind": "oracle",
+                                "sample": f"5 whole rounds (rounds 0-4, 512 sequences each, half greedy) on {cores} "
+                                          "spawned processes; float64 numpy oracle, one call per sequence; widening "
+                                          "the rows and drawing the draft tokens untimed",
+                                "seconds_per_round": many,
+                                "single_thread": {"value": len(one) / sum(one), "unit": "rounds/s", "cores": 1,
+                                                  "sample": "3 whole rounds (rounds 0-2) on one process",
+                                                  "seconds_per_round": one}}
     return line if rank == 0 else None
 
 

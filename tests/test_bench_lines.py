@@ -38,3 +38,17 @@ def test_add_hbm_on_both_time_keys():
     assert t["achieved_gbs"] == pytest.approx(500.0) and t["frac"] == pytest.approx(0.0625)
     assert c["achieved_gbs"] == pytest.approx(4000.0) and c["frac"] == pytest.approx(0.5)
     assert c["peak_gbs"] == 8000.0
+
+
+def test_whole_call_roofline_divides_the_bytes_read_by_the_call_time():
+    r = bench.whole_call_roofline(1_116_340_224, 0.25, 6693.8, "measured")
+    assert r["achieved_gbs"] == pytest.approx(1_116_340_224 / 0.25e-3 / 1e9)
+    assert r["frac"] == pytest.approx(r["achieved_gbs"] / 6693.8)
+    assert r["of_8tbs"] == pytest.approx(r["achieved_gbs"] / 8000.0)
+
+
+def test_oracle_round_seconds_times_whole_rounds_on_the_pool():
+    """The CPU baseline's timing: whole rounds through spawned workers, one time per timed run."""
+    w = W.scaled(W.LARGE_BATCH, B=6, V=300)
+    t = bench.oracle_round_seconds(w, [0, 1], 2, "cpu", repeats=2)
+    assert len(t) == 4 and all(x > 0 for x in t)

@@ -663,11 +663,12 @@ def run_ours(args, rank, world, local_rank):
                    "bytes_read_per_round": b_o, "kernel": "k_stats" if lazy else "k_lazy", "kernel_ms": k_o,
                    "kernel_gbs": b_o / (k_o * 1e-3) / 1e9, "frac": b_o / (k_o * 1e-3) / 1e9 / peak,
                    "step_roofline": whole_call_roofline(b_o, ms_o, peak, peak_kind)}
-    line["filters"] = filter_rates(sv, dev, world, min(n, 200))
-    line["pyramid"] = pyramid_rates(sv, dev, world, min(n, 200), peak)
-    line["tree"] = tree_rates(sv, dev, world, min(n, 200))
-    line["configs"] = config_rates(sv, dev, world, min(n, 200))
-    add_hbm(line, peak)
+    if not args.headline_only:
+        line["filters"] = filter_rates(sv, dev, world, min(n, 200))
+        line["pyramid"] = pyramid_rates(sv, dev, world, min(n, 200), peak)
+        line["tree"] = tree_rates(sv, dev, world, min(n, 200))
+        line["configs"] = config_rates(sv, dev, world, min(n, 200))
+        add_hbm(line, peak)
     if args.kernel_only:
         return line if rank == 0 else None
 
@@ -749,6 +750,9 @@ def main():
                     help="sv_verify (every candidate row) or sv_verify_lazy (rows up to each first rejection)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="report the device-timed steps only (no end-to-end or CPU-baseline measurement)")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time the headline workload (and the other verification path) only: no filter, "
+                         "PyramidSD, tree or other-workload lines (for profiling runs)")
     args = ap.parse_args()
     rank, world, local_rank = rank_env()
     if args.impl == "reference":

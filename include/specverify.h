@@ -40,6 +40,7 @@
  *    Every call works on the current device (cudaGetDevice): the stream and the device arrays
  *    it names (the logits; for the integer calls their outputs) must belong to it, else the
  *    call returns SV_ERR_INVALID_ARG after the size and workspace checks, before any launch.
+ *    The check is skipped while `stream` is being captured into a CUDA graph.
  *    Argument errors are returned synchronously, before anything is launched.  Conditions only
  *    the GPU can see (non-finite logits, out-of-range tokens, a wait that timed out) are written
  *    to the optional device-side sv_stats block, which the caller reads after synchronising.

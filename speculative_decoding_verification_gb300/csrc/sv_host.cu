@@ -37,6 +37,14 @@ bool device_info(DeviceInfo &out) {
 bool on_current_device(cudaStream_t s, const void *p0, const void *p1) {
     int cur = 0;
     if (cudaGetDevice(&cur) != cudaSuccess) return false;
+    // While the stream is being captured into a graph the queries below would end the capture,
+    // so they are skipped; the same call made outside a capture is checked.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return true;
     if (s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread) {
         int sd = -1;
         if (cudaStreamGetDevice(s, &sd) != cudaSuccess) {

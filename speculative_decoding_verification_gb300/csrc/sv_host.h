@@ -43,7 +43,8 @@ inline bool rows_ok(const void *base, int64_t pitch, int V, sv_dtype dtype) {
 // The call's stream and the device arrays p0, p1 (either may be null) belong to the current
 // device.  A stream of another device would run the kernels there while the workspace plan and
 // the SM count come from the current one, and an array on another device would be read without
-// peer access.  Host and managed memory pass.  One stream query and two pointer queries.
+// peer access.  Host and managed memory pass.  One stream query and two pointer queries, none
+// while the stream is being captured into a CUDA graph (they would end the capture).
 bool on_current_device(cudaStream_t s, const void *p0, const void *p1 = nullptr);
 
 inline sv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }

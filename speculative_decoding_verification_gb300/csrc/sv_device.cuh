@@ -196,6 +196,61 @@ __device__ __forceinline__ float ex2_fast(float y) {
     return r;
 }
 
+// ------------------------------------------------------------------------------------------
+// Packed float32 pairs: Blackwell's f32x2 add / multiply-add issue one instruction for two
+// IEEE round-to-nearest operations, each rounded exactly as its scalar form.  A pair lives in
+// one 64-bit register (lo in the low word).
+// ------------------------------------------------------------------------------------------
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 f2_pack(float lo, float hi) {
+    f32x2 d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+
+__device__ __forceinline__ void f2_unpack(f32x2 v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// The two bfloat16 values of a 32-bit word as a float pair (lo element first), exactly.
+__device__ __forceinline__ f32x2 f2_from_bf16x2(uint32_t w) {
+    f32x2 d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(w << 16), "r"(w & 0xFFFF0000u));
+    return d;
+}
+
+__device__ __forceinline__ f32x2 f2_from_u32x2(uint32_t lo, uint32_t hi) {
+    f32x2 d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// 2^y of both lanes with the fast exponential.
+__device__ __forceinline__ f32x2 f2_ex2(f32x2 y) {
+    float lo, hi;
+    f2_unpack(y, lo, hi);
+    return f2_pack(ex2_fast(lo), ex2_fast(hi));
+}
+
+__device__ __forceinline__ float f2_sum(f32x2 v) {
+    float lo, hi;
+    f2_unpack(v, lo, hi);
+    return __fadd_rn(lo, hi);
+}
+
 // Exact power of two for an integer exponent (0 below the normal range).
 __device__ __forceinline__ float pow2i(int e) {
     if (e < -126) return 0.0f;

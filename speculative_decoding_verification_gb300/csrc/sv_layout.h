@@ -9,8 +9,9 @@ namespace sv {
 // ---- launch geometry ---------------------------------------------------------------------
 constexpr int kThreads = 256;               // threads per streaming block
 constexpr int kWarps = kThreads / 32;
-constexpr int kTileBytes = 16384;           // one bulk copy (one pipeline stage per row)
-constexpr int kStatsStages = 6;             // pipeline depth of the statistics pass
+constexpr int kTileBytes = 16384;           // one bulk copy (a draw-pass or selection stage per row)
+constexpr int kStatsTileBytes = 32768;      // one stage of the statistics pass (two 16 KB halves)
+constexpr int kStatsStages = 3;             // pipeline depth of the statistics pass
 constexpr int kStatsThreads = kThreads + 32;   // eight consumer warps and one producer warp
 constexpr int kUnitTiles = 4;               // aim for (row, chunk) units of about this many tiles
 constexpr int kDrawStages = 3;              // pipeline depth of the draw pass (two rows per stage)
@@ -170,15 +171,15 @@ inline int choose_split(long long n_rows, long long row_bytes) {
     return (int)s;
 }
 
-// 16-byte vectors per chunk: whole tiles where the row has them, so only a row's last chunk
-// ends in a partial tile.  n_split may shrink; both are returned.
+// 16-byte vectors per chunk: whole statistics-pass tiles where the row has them, so only a
+// row's last chunk ends in a partial tile.  n_split may shrink; both are returned.
 inline void chunk_geometry(long long n_vec, int &n_split, int &chunk_vecs) {
     if (n_vec <= 0) {
         n_split = 1;
         chunk_vecs = 1;
         return;
     }
-    const long long tv = kTileBytes / 16;
+    const long long tv = kStatsTileBytes / 16;
     long long cv = (n_vec + n_split - 1) / n_split;
     if (cv > tv) cv = (cv + tv - 1) / tv * tv;
     chunk_vecs = (int)cv;

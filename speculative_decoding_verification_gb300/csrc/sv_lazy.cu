@@ -327,7 +327,7 @@ constexpr int kLazyRing = 64;                 // finish requests in flight per b
 constexpr int kLazyTCache = 2048;             // temperatures cached in shared memory
 constexpr int kLazyCtlBytes = 1024 + kLazyRing * 16 + kLazyTCache * 4;   // + request ring + cache
 static_assert(2 * kStatsStages * 8 + 16 + kStatsStages * (int)sizeof(TileMeta) <= 1024, "control block");
-constexpr size_t kLazySmemBytes = (size_t)kLazyCtlBytes + (size_t)kStatsStages * kTileBytes;
+constexpr size_t kLazySmemBytes = (size_t)kLazyCtlBytes + (size_t)kStatsStages * kStatsTileBytes;
 
 // The statistics pass of k_stats with a work queue that grows while it runs.
 template <int ES>
@@ -480,8 +480,8 @@ __global__ void __launch_bounds__(kLazyThreads, 2) k_lazy(const LazyArgs L) {
                         ok = false;
                         break;
                     }
-                    const int fv = ui.v0 + t * (kTileBytes / 16);
-                    const int nv = max(0, min(kTileBytes / 16, ui.v1 - fv));
+                    const int fv = ui.v0 + t * (kStatsTileBytes / 16);
+                    const int nv = max(0, min(kStatsTileBytes / 16, ui.v1 - fv));
                     m.row = ui.row;
                     m.rid = ui.rid;
                     m.c_hi = ui.c_hi;
@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(kLazyThreads, 2) k_lazy(const LazyArgs L) {
                     meta[st] = m;
                     if (nv > 0) {
                         mbar_arrive_expect_tx(&full[st], (uint32_t)nv * 16u);
-                        bulk_load_stream(tiles + st * kTileBytes, ui.row + (size_t)fv * 16, (uint32_t)nv * 16u,
+                        bulk_load_stream(tiles + st * kStatsTileBytes, ui.row + (size_t)fv * 16, (uint32_t)nv * 16u,
                                          &full[st], policy);
                         in_flight[st] = it;
                     } else {
@@ -538,7 +538,7 @@ __global__ void __launch_bounds__(kLazyThreads, 2) k_lazy(const LazyArgs L) {
         if (m.flags & kTileEnd) break;
         const bool greedy = (m.flags & kTileGreedy) != 0;
         if (m.flags & kTileFirst) acc_init(A);
-        if (m.nv > 0) acc_tile<ES>(A, tiles + st * kTileBytes, m.nv, m.fv, greedy, m.c_hi);
+        if (m.nv > 0) acc_tile<ES>(A, tiles + st * kStatsTileBytes, m.nv, m.fv, greedy, m.c_hi);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
         if (m.flags & kTileLast) {

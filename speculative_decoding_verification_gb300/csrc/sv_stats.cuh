@@ -7,7 +7,7 @@
 // (T == 0) it finds the maximum and its lowest index.  Both track NaN / +inf.
 //
 // Work is handed out as (row, chunk) units from a global counter to a persistent grid.  In each
-// block a producer warp streams the units' 16 KB tiles into shared memory with 1-D bulk copies
+// block a producer warp streams the units' 32 KB tiles into shared memory with 1-D bulk copies
 // (cp.async.bulk) and eight consumer warps read them with 128-bit shared loads.  Each consumer
 // warp writes one WarpPartial per unit; partials are combined per row by the accept kernel.
 #pragma once
@@ -74,7 +74,7 @@ __device__ __forceinline__ UnitInfo stats_unit(const StatsArgs &a, long long u, 
 }
 
 __device__ __forceinline__ int unit_tiles(const UnitInfo &ui) {
-    return (ui.v1 - ui.v0 + (kTileBytes / 16) - 1) / (kTileBytes / 16);
+    return (ui.v1 - ui.v0 + (kStatsTileBytes / 16) - 1) / (kStatsTileBytes / 16);
 }
 
 // Per-thread accumulator.
@@ -164,17 +164,43 @@ __device__ __forceinline__ void acc_scalar(StatAcc &A, float x, int idx, bool gr
     acc_add(A, e);
 }
 
-// A thread's share of one shared-memory tile: its NV vectors (vi = tid + i * kThreads) are
+// The error weight A = sum 2^y (-y) of a thread's share of a tile with every logit clamped at
+// the floor first.  The fast path leaves the clamp out; a -inf logit (a masked token) or one
+// whose x c_hi overflows gives y = -inf there, and 2^y y = 0 * inf = NaN, so the tile's weight
+// is taken again here.  The row sum needs no second pass: those elements weigh 0 either way.
+template <int ES>
+__device__ __noinline__ float acc_tile_weight_clamped(const unsigned char *buf, int nv, float c_hi, float rf) {
+    constexpr int EPV = 16 / ES;
+    constexpr int NV = kTileBytes / 16 / kThreads;
+    float a = 0.f;
+    for (int i = 0; i < NV; ++i) {
+        const int vi = threadIdx.x + i * kThreads;
+        if (vi >= nv) break;
+        float x[EPV];
+        unpack<ES>(lds128(buf + vi * 16), x);
+        for (int k = 0; k < EPV; ++k) {
+            const float y = fmaf(fmax_nan(x[k], kF32Floor), c_hi, -rf);
+            a = fmaf(ex2_fast(y), -y, a);
+        }
+    }
+    return a;
+}
+
+// A thread's share of one 16 KB half of a stage: its NV vectors (vi = tid + i * kThreads) are
 // loaded together, checked against the reference with one combined maximum, and their
 // 8 * NV (bf16) exponentials are independent, so the SFU work overlaps.  Vectors past the
-// end of a partial tile read as -inf.  Sampled rows accumulate S = sum 2^y and
+// end of a partial tile hold no element.  Sampled rows accumulate S = sum 2^y and
 // A = sum 2^y (-y) with y = x c_hi - r <= 0 rounded once (c = c_hi + c_lo); combine_row
 // applies the x c_lo part to the row sum to first order.  One compensated addition per tile.
 template <int ES>
-__device__ __forceinline__ void acc_tile(StatAcc &A, const unsigned char *buf, int nv, int fv, bool greedy, float c_hi) {
+__device__ __forceinline__ void acc_half(StatAcc &A, const unsigned char *buf, int nv, int fv, bool greedy, float c_hi) {
     constexpr int EPV = 16 / ES;
     constexpr int NV = kTileBytes / 16 / kThreads;
-    const uint32_t ninf = ES == 2 ? 0xFF80FF80u : 0xFF800000u;
+    // vectors past the end of a partial tile: -inf for greedy rows (they can never hold the
+    // argmax), the floor for sampled rows (weight 0, and no -inf to send the tile's error weight
+    // down the clamped path)
+    const uint32_t ninf = greedy ? (ES == 2 ? 0xFF80FF80u : 0xFF800000u)
+                                 : (ES == 2 ? kBf16Floor2 : __float_as_uint(kF32Floor));
     const int tid = threadIdx.x;
     uint4 w[NV];
     if (nv == kTileBytes / 16) {
@@ -221,41 +247,60 @@ __device__ __forceinline__ void acc_tile(StatAcc &A, const unsigned char *buf, i
         return;
     }
     if (!(vmax <= A.thr)) acc_reference(A, vmax, c_hi);
-    float sv[NV], av[NV];
+    // Both elements of a pair go through one f32x2 instruction, each rounded as its scalar form:
+    // y = x c_hi - r (one rounding), e = 2^y, and the error weight accumulates e y (= -A).  The
+    // row sum's tree keeps its depth: two pair additions inside a vector (bf16: 4 pairs; f32: one
+    // addition of 2 pairs), two across the tile's vectors, and the final lo + hi, i.e. 3 + 2
+    // rounding levels for bf16 (2 + 2 for f32) as the error bound counts them.
+    const f32x2 c2 = f2_pack(c_hi, c_hi), nr2 = f2_pack(-A.rf, -A.rf);
+    f32x2 sv[NV];
+    f32x2 ay2[2] = {0ull, 0ull};
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
-        float x[EPV], e[EPV];
-        if constexpr (ES == 2) {
-            const uint4 c = make_uint4(bmax2(w[i].x, kBf16Floor2), bmax2(w[i].y, kBf16Floor2),
-                                       bmax2(w[i].z, kBf16Floor2), bmax2(w[i].w, kBf16Floor2));
-            unpack<ES>(c, x);
+        constexpr int PPV = 8 / ES;   // pairs per 16-byte vector
+        f32x2 e2[PPV];
+#pragma unroll
+        for (int k = 0; k < PPV; ++k) {
+            const uint32_t w0 = k == 0 ? w[i].x : k == 1 ? w[i].y : k == 2 ? w[i].z : w[i].w;
+            f32x2 x2;
+            if constexpr (ES == 2) {
+                x2 = f2_from_bf16x2(w0);
+            } else {
+                x2 = f2_from_u32x2(k == 0 ? w[i].x : w[i].z, k == 0 ? w[i].y : w[i].w);
+            }
+            const f32x2 y2 = f2_fma(x2, c2, nr2);
+            e2[k] = f2_ex2(y2);
+            ay2[i & 1] = f2_fma(e2[k], y2, ay2[i & 1]);
+        }
+        if constexpr (PPV == 4) {
+            sv[i] = f2_add(f2_add(e2[0], e2[1]), f2_add(e2[2], e2[3]));
         } else {
-            unpack<ES>(w[i], x);
-#pragma unroll
-            for (int k = 0; k < EPV; ++k) x[k] = fmax_nan(x[k], kF32Floor);
+            sv[i] = f2_add(e2[0], e2[1]);
         }
-        float a = 0.f;
-#pragma unroll
-        for (int k = 0; k < EPV; ++k) {
-            const float y = fmaf(x[k], c_hi, -A.rf);   // one rounding; x c_lo enters in combine_row
-            e[k] = ex2_fast(y);
-            a = fmaf(e[k], -y, a);
-        }
-        if constexpr (EPV == 8) {
-            sv[i] = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-        } else {
-            sv[i] = (e[0] + e[1]) + (e[2] + e[3]);
-        }
-        av[i] = a;
     }
-    float st = sv[0], at = av[0];
+    f32x2 s2;
+    if constexpr (NV == 4) {
+        s2 = f2_add(f2_add(sv[0], sv[1]), f2_add(sv[2], sv[3]));
+    } else {
+        s2 = sv[0];
 #pragma unroll
-    for (int i = 1; i < NV; ++i) {
-        st += sv[i];
-        at += av[i];
+        for (int i = 1; i < NV; ++i) s2 = f2_add(s2, sv[i]);
     }
+    const float st = f2_sum(s2);
+    float at = -f2_sum(f2_add(ay2[0], ay2[1]));
+    if (at != at) at = acc_tile_weight_clamped<ES>(buf, nv, c_hi, A.rf);
     acc_add(A, st);
     A.aerr += at;
+}
+
+// A thread's share of one 32 KB stage: its two 16 KB halves in order (each with its own maximum
+// check, tree sums and compensated addition), so a thread's elements are met in increasing id
+// order and the per-stage costs (barrier wait, stage description, release) are paid once.
+template <int ES>
+__device__ __forceinline__ void acc_tile(StatAcc &A, const unsigned char *buf, int nv, int fv, bool greedy, float c_hi) {
+    constexpr int HV = kTileBytes / 16;   // vectors per half
+    acc_half<ES>(A, buf, min(nv, HV), fv, greedy, c_hi);
+    if (nv > HV) acc_half<ES>(A, buf + kTileBytes, nv - HV, fv + HV, greedy, c_hi);
 }
 
 // Warp-combine and store this unit's partial (float32 / float-float arithmetic only).
@@ -305,11 +350,11 @@ constexpr int kTileFirst = 1, kTileLast = 2, kTileGreedy = 4, kTileEnd = 8;
 
 constexpr int kStatsCtlBytes = 1024;   // full[], empty[], abort flag, TileMeta[]
 static_assert(2 * kStatsStages * 8 + 16 + kStatsStages * (int)sizeof(TileMeta) <= kStatsCtlBytes, "control block");
-constexpr size_t kStatsSmemBytes = (size_t)kStatsCtlBytes + (size_t)kStatsStages * kTileBytes;
+constexpr size_t kStatsSmemBytes = (size_t)kStatsCtlBytes + (size_t)kStatsStages * kStatsTileBytes;
 
 // Warp-specialised pipeline.  The producer (lane 0 of the last warp) takes (row, chunk) units
 // from a global counter, skips units that are not needed, and streams each unit's tiles into a
-// kStatsStages-deep ring of 16 KB shared-memory tiles with 1-D bulk copies; per stage it first
+// kStatsStages-deep ring of 32 KB shared-memory tiles with 1-D bulk copies; per stage it first
 // waits until the eight consumer warps released the stage ("empty"), writes the TileMeta, then
 // issues the copy that completes the stage's "full" barrier.  Consumer warps wait on "full",
 // accumulate their share of the tile, and release it.  Waits sleep (suspend hint) instead of
@@ -378,8 +423,8 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_stats(const StatsArgs a) {
                         ok = false;
                         break;
                     }
-                    const int fv = ui.v0 + t * (kTileBytes / 16);
-                    const int nv = max(0, min(kTileBytes / 16, ui.v1 - fv));
+                    const int fv = ui.v0 + t * (kStatsTileBytes / 16);
+                    const int nv = max(0, min(kStatsTileBytes / 16, ui.v1 - fv));
                     m.row = ui.row;
                     m.rid = ui.rid;
                     m.c_hi = ui.c_hi;
@@ -394,7 +439,7 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_stats(const StatsArgs a) {
                     meta[st] = m;
                     if (nv > 0) {
                         mbar_arrive_expect_tx(&full[st], (uint32_t)nv * 16u);
-                        bulk_load_stream(tiles + st * kTileBytes, ui.row + (size_t)fv * 16, (uint32_t)nv * 16u,
+                        bulk_load_stream(tiles + st * kStatsTileBytes, ui.row + (size_t)fv * 16, (uint32_t)nv * 16u,
                                          &full[st], policy);
                         in_flight[st] = it;
                     } else {
@@ -430,7 +475,7 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_stats(const StatsArgs a) {
         if (m.flags & kTileEnd) break;
         const bool greedy = (m.flags & kTileGreedy) != 0;
         if (m.flags & kTileFirst) acc_init(A);
-        if (m.nv > 0) acc_tile<ES>(A, tiles + st * kTileBytes, m.nv, m.fv, greedy, m.c_hi);
+        if (m.nv > 0) acc_tile<ES>(A, tiles + st * kStatsTileBytes, m.nv, m.fv, greedy, m.c_hi);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
         if (m.flags & kTileLast) {

@@ -22,6 +22,9 @@ constexpr int kUnitTarget = 1024;           // at least about this many (row, ch
 constexpr int kExactSplit = 16;             // chunks per row in the float-float tier
 constexpr int kExactCap = 2048;             // most queued items per call in the float-float tier
 constexpr int kExactGroup = 1;              // draw sub-chunks per warp unit in the float-float tier
+constexpr int kFlowGroupSubs = 32;          // dataflow kernel: sub-chunks per float-float row-pass unit
+constexpr int kFlowSplitA = 4;              // dataflow kernel: float-float row-sum units per row
+constexpr int kFlowUncCap = 256;            // dataflow kernel: tokens of uncertain sign listed per item
 constexpr long long kWaitLimitCycles = 4000000000LL;   // ~2 s at 2 GHz: bounded barrier waits
 constexpr unsigned kSuspendHintNs = 100000;  // a waiting thread sleeps at most this long per try
 

@@ -180,20 +180,8 @@ __device__ void flow_enqueue(const FlowArgs &F, int type, long long first, int n
 
 __device__ __forceinline__ void flow_done(const FlowArgs &F) { atomicSub(&F.st.counters->n_pending, 1); }
 
-// Per sequence: validate, mark the debug fields undefined, queue its first rows.  Also clears
-// the appended part of the queue and the per-item counters (grid-stride).
-__global__ void __launch_bounds__(kThreads) k_flow_init(const FlowArgs F, int B) {
-    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long nthr = (long long)gridDim.x * blockDim.x;
-    for (long long i = F.q1_base + tid; i < F.cap; i += nthr) F.units[i] = 0ull;
-    for (long long i = tid; i < B; i += nthr) F.draw_cnt[i] = 0;
-    for (long long i = tid; i < F.cap_x; i += nthr) {
-        F.x_cnt[i] = 0;
-        F.a_cnt[i] = 0;
-        F.acc.exact_unc[i] = 0;
-    }
-    if (tid >= B) return;
-    const int b = (int)tid;
+// One sequence of the init kernel: validate, mark the debug fields undefined, queue its first rows.
+__device__ void flow_init_seq(const FlowArgs &F, int b) {
     F.pos_cnt[b] = 0;
     const AcceptArgs &a = F.acc;
     const int K = a.K;
@@ -222,6 +210,21 @@ __global__ void __launch_bounds__(kThreads) k_flow_init(const FlowArgs F, int B)
     const bool with_d = !greedy && K > 0;
     if (!F.lazy || kLazyTail <= 0) flow_enqueue_rows(F, b, 0, K, with_d, kBatchTail, 0, true);
     else flow_enqueue_rows(F, b, 0, 0, with_d, kBatchOne, 0, true);
+}
+
+// Every sequence's init (grid-stride over sequences), and the clearing of the appended part of
+// the queue and of the per-item counters.
+__global__ void __launch_bounds__(kThreads) k_flow_init(const FlowArgs F, int B) {
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long nthr = (long long)gridDim.x * blockDim.x;
+    for (long long i = F.q1_base + tid; i < F.cap; i += nthr) F.units[i] = 0ull;
+    for (long long i = tid; i < B; i += nthr) F.draw_cnt[i] = 0;
+    for (long long i = tid; i < F.cap_x; i += nthr) {
+        F.x_cnt[i] = 0;
+        F.a_cnt[i] = 0;
+        F.acc.exact_unc[i] = 0;
+    }
+    for (long long bb = tid; bb < B; bb += nthr) flow_init_seq(F, (int)bb);
 }
 
 // ------------------------------------------------------------------------------------------

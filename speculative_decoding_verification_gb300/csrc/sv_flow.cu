@@ -1092,44 +1092,18 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
             int st = 0;
             uint32_t epar = 0;
             bool ok = true;
-            // Two queues: the units appended during the pass (draws, float-float units, lazy
-            // mode's later rows) go first, so that a sequence's later work follows its rows
-            // closely; the units written by the init kernel fill the rest of the time.  An
-            // appended slot is claimed only while one is queued (compare-and-swap on the head);
-            // its word may still be on its way from the appender, so its valid bit is awaited.
-            const int q0_n = *reinterpret_cast<volatile int *>(&a.counters->q0_tail);
-            volatile int *q_tail_v = reinterpret_cast<volatile int *>(&a.counters->q_tail);
-            volatile int *q_head1_v = reinterpret_cast<volatile int *>(&a.counters->q_head1);
-            volatile int *q_head0_v = reinterpret_cast<volatile int *>(&a.counters->q_head);
-            // 1: a word claimed, 0: nothing queued now, -1: abort
-            auto claim_word = [&](unsigned long long &wd) -> int {
-                int h1 = *q_head1_v;
-                while (h1 < *q_tail_v) {
-                    const int prev = atomicCAS(&a.counters->q_head1, h1, h1 + 1);
-                    if (prev == h1) {
-                        const long long sl = F.q1_base + h1;
-                        if (sl >= F.cap) return 0;
-                        const long long t0 = clock64();
-                        while (!((wd = ld_relaxed_u64(&F.units[sl])) >> 63)) {
-                            if (*reinterpret_cast<volatile int *>(abort_flag) || clock64() - t0 > a.wait_limit) {
-                                if (atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
-                                return -1;
-                            }
-                            __nanosleep(32);
-                        }
-                        return 1;
-                    }
-                    h1 = prev;
-                }
-                if (*q_head0_v < q0_n) {
-                    const int c = atomicAdd(&a.counters->q_head, 1);
-                    if (c < q0_n) {
-                        wd = ld_relaxed_u64(&F.units[c]);
-                        return 1;
-                    }
-                }
-                return 0;
+            // One FIFO: the units written by the init kernel, then the units appended during the
+            // pass.  In the bulk of the pass each iteration claims the next slot and starts
+            // loading its word before issuing the current unit's stages; near the end it claims
+            // only when idle, so that queued units go to idle blocks.
+            const long long q0_n = *reinterpret_cast<volatile int *>(&a.counters->q0_tail);
+            auto slot_of = [&](long long c) { return c < q0_n ? c : F.q1_base + (c - q0_n); };
+            auto load_word = [&](long long c) {
+                const long long sl = slot_of(c);
+                return sl < F.cap ? ld_relaxed_u64(&F.units[sl]) : 0ull;
             };
+            long long claim = atomicAdd(&a.counters->q_head, 1);
+            unsigned long long word = load_word(claim);
             // stage one: wait for the stage to be free, then describe it
             auto next_stage = [&]() -> bool {
                 if (it >= kStatsStages) {
@@ -1148,35 +1122,13 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                     if (it >= 2 * kStatsStages) epar ^= 1u;   // round r >= 2 waits phase r - 1
                 }
             };
-            // The next unit is claimed while the current one's last stage waits for a free slot,
-            // so the claim's round trips overlap the copies in flight.
-            unsigned long long pf = 0;   // a claimed word not yet issued (bit 63 set), or 0
-            auto prefetch = [&]() {
-                if (pf >> 63) return;
-                unsigned long long wd = 0;
-                const int got = claim_word(wd);
-                if (got < 0) ok = false;
-                else if (got > 0) pf = wd;
-            };
             while (ok) {
                 long long unit = -1;
                 unsigned payload = 0;
                 int type = 0;
-                unsigned long long word = 0;
                 unsigned ns = 32;
                 const long long t_start = clock64();   // the wait is bounded by its own length
-                while (true) {
-                    if (pf >> 63) {
-                        word = pf;
-                        pf = 0;
-                        break;
-                    }
-                    const int got = claim_word(word);
-                    if (got < 0) {
-                        ok = false;
-                        break;
-                    }
-                    if (got > 0) break;
+                while (slot_of(claim) < F.cap && !(word >> 63)) {
                     if (ld_acquire(&a.counters->n_pending) == 0) break;   // no more work will appear
                     if (*reinterpret_cast<volatile int *>(abort_flag) || clock64() - t_start > a.wait_limit) {
                         if (atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
@@ -1185,14 +1137,21 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                     }
                     __nanosleep(ns);
                     ns = ns < 256 ? 2 * ns : 256;
+                    word = load_word(claim);
                 }
-                if (ok && (word >> 63)) {
+                if (word >> 63) {
                     unit = (long long)(unsigned)(word & 0xFFFFFFFFu);
                     type = (int)((word >> 60) & 7u);
                     payload = (unsigned)((word >> 32) & 0x0FFFFFFFu);
                     if (type != kUnitStats) __threadfence();   // acquire: the unit's data was written before it
                 }
                 const bool have = ok && unit >= 0;
+                long long next = -1;
+                unsigned long long next_word = 0;
+                if (have && q0_n + *reinterpret_cast<volatile int *>(&a.counters->q_tail) - claim > 2LL * gridDim.x) {
+                    next = atomicAdd(&a.counters->q_head, 1);
+                    next_word = load_word(next);
+                }
                 if (!have) {
                     if (next_stage()) {
                         TileMeta m;
@@ -1206,8 +1165,7 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                     const UnitInfo ui = stats_unit<ES>(a, unit, t_cache, n_cache);
                     const int nt = max(unit_tiles(ui), 1);
                     for (int t = 0; t < nt && ok; ++t) {
-                        if (t == nt - 1) prefetch();
-                        if (!ok || !next_stage()) {
+                        if (!next_stage()) {
                             ok = false;
                             break;
                         }
@@ -1247,8 +1205,7 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                     constexpr int HV = kTileBytes / 16;   // vectors per half stage
                     const int nt = max((v1 - v0 + HV - 1) / HV, 1);
                     for (int t = 0; t < nt && ok; ++t) {
-                        if (t == nt - 1) prefetch();
-                        if (!ok || !next_stage()) {
+                        if (!next_stage()) {
                             ok = false;
                             break;
                         }
@@ -1289,6 +1246,13 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                         mbar_arrive(&full[st]);
                         advance();
                     }
+                }
+                if (next >= 0) {
+                    claim = next;
+                    word = next_word;
+                } else {
+                    claim = atomicAdd(&a.counters->q_head, 1);
+                    word = load_word(claim);
                 }
             }
             // after an abort, copies still in flight land before shared memory is released

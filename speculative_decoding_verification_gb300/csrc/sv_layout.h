@@ -153,12 +153,11 @@ struct Counters {
     unsigned barrier;       // grid barrier of the exact tier
     int next_unit;          // statistics pass: next (row, chunk) unit to hand out
     int next_draw_unit;     // draw pass: next (item, chunk) unit to hand out
-    int q_head;             // dataflow kernel: next position of the init kernel's units to claim
-    int q0_tail, q_tail;    // dataflow kernel: units written by the init kernel / appended since
-    int n_pending;          // dataflow kernel: sequences whose last token is not written yet
+    int q_head;             // lazy verification: next queue position to claim (position 0, then later)
+    int q0_tail, q_tail;    // lazy verification: position-0 units / later units queued
+    int n_pending;          // lazy verification: sequences not finished yet
     int n_div_exact;        // fuzzy verification: divergences queued for the float-float pass
-    int q_head1;            // dataflow kernel: next appended queue position to claim
-    int pad[5];
+    int pad[6];
 };
 
 inline int div_up(long long a, long long b) { return (int)((a + b - 1) / b); }

@@ -49,8 +49,16 @@ namespace sv {
 // ---- geometry ------------------------------------------------------------------------------
 constexpr int kFlowThreads = kStatsThreads + 32;   // 8 consumer warps, producer, finisher
 constexpr int kFlowRing = 64;                      // finisher requests in flight per block
-constexpr int kFlowTCache = 2048;                  // temperatures cached in shared memory
-constexpr int kFlowCtlBytes = 1024 + kFlowRing * 16 + kFlowTCache * 4 + 256 * 8;   // + ring, cache, exp2 table
+constexpr int kFlowTCache = 1024;                  // temperatures cached in shared memory
+constexpr int kFlowWindow = 64;                    // eager mode: sequences queued ahead at a time
+// shared memory: control block (barriers, flags, stage descriptions), finisher ring, the eight
+// consumer warps' partials of each stage's unit and their arrival counts, temperatures, exp2 table
+constexpr int kFlowOffRing = 1024;
+constexpr int kFlowOffPart = kFlowOffRing + kFlowRing * 16;
+constexpr int kFlowOffPartCnt = kFlowOffPart + kStatsStages * kWarps * (int)sizeof(WarpPartial);
+constexpr int kFlowOffTCache = kFlowOffPartCnt + 64;
+constexpr int kFlowOffTab = kFlowOffTCache + kFlowTCache * 4;
+constexpr int kFlowCtlBytes = kFlowOffTab + 256 * 8;
 constexpr size_t kFlowSmemBytes = (size_t)kFlowCtlBytes + (size_t)kStatsStages * kStatsTileBytes;
 static_assert(2 * kStatsStages * 8 + 16 + kStatsStages * (int)sizeof(TileMeta) <= 1024, "control block");
 static_assert(kDrawUnitSubs * 32 == 2 * (kTileBytes / 16), "a draw unit is two stages of 16 KB per row");
@@ -74,9 +82,12 @@ struct FlowArgs {
     unsigned long long *units;   // [cap] the queue
     long long cap;
     long long q1_base;   // units[0, q1_base): written by the init kernel; units[q1_base, cap): appended
-    int *pos_cnt;        // [B] consumer warps done with the sequence's statistics units (cumulative)
+    FlowCounters *fc;    // the kernel's counters (one cache line each)
+    int *pos_cnt;        // [B] consumer warps done with the sequence's statistics units (cumulative);
+                         // -1 for a sequence the init kernel rejected
     int n_seq;
     int lazy;
+    int window;          // eager mode: sequences the init kernel queues; each finished one queues the next
     // draws
     int n_vec, n_sub, d_split;
     float *subs;         // [B][n_sub] float32 sum of the weights of each sub-chunk
@@ -129,7 +140,7 @@ __device__ __forceinline__ void seq_pos(const FlowArgs &F, long long rid, int &b
 // Claim n slots of the appended region (one thread).  Each unit is queued once, so the region
 // is sized for all of them; running out means a bug, reported rather than written past.
 __device__ __forceinline__ long long flow_claim(const FlowArgs &F, int n) {
-    const long long base = F.q1_base + atomicAdd(&F.st.counters->q_tail, n);
+    const long long base = F.q1_base + atomicAdd(&F.fc->q_tail.v, n);
     if (base + n > F.cap) {
         report_error(F.st.stats, SV_ERR_WORKSPACE, -1);
         return -1;
@@ -149,7 +160,7 @@ __device__ void flow_enqueue_rows(const FlowArgs &F, int b, int j0, int j1, bool
     const unsigned payload = ((unsigned)(cum + n * kWarps) << 8) | ((unsigned)j0 << 2) | (unsigned)kind;
     long long base;
     if (initial) {
-        base = atomicAdd(&F.st.counters->q0_tail, n);
+        base = atomicAdd(&F.fc->q0_tail.v, n);
         if (base + n > F.q1_base) {
             report_error(F.st.stats, SV_ERR_WORKSPACE, b);
             return;
@@ -178,11 +189,11 @@ __device__ void flow_enqueue(const FlowArgs &F, int type, long long first, int n
     for (int k = 0; k < n; ++k) st_relaxed_u64(&F.units[base + k], unit_word(type, 0, (unsigned)(first + k)));
 }
 
-__device__ __forceinline__ void flow_done(const FlowArgs &F) { atomicSub(&F.st.counters->n_pending, 1); }
+__device__ __forceinline__ void flow_done(const FlowArgs &F) { atomicSub(&F.fc->n_pending.v, 1); }
 
 // One sequence of the init kernel: validate, mark the debug fields undefined, queue its first rows.
 __device__ void flow_init_seq(const FlowArgs &F, int b) {
-    F.pos_cnt[b] = 0;
+    F.pos_cnt[b] = -1;   // rejected until validated
     const AcceptArgs &a = F.acc;
     const int K = a.K;
     const float T = a.temperature[b];
@@ -206,10 +217,30 @@ __device__ void flow_init_seq(const FlowArgs &F, int b) {
             return;
         }
     }
-    atomicAdd(&F.st.counters->n_pending, 1);
+    F.pos_cnt[b] = 0;
+    atomicAdd(&F.fc->n_pending.v, 1);
     const bool with_d = !greedy && K > 0;
-    if (!F.lazy || kLazyTail <= 0) flow_enqueue_rows(F, b, 0, K, with_d, kBatchTail, 0, true);
-    else flow_enqueue_rows(F, b, 0, 0, with_d, kBatchOne, 0, true);
+    if (!F.lazy) {
+        if (b < F.window) flow_enqueue_rows(F, b, 0, K, with_d, kBatchTail, 0, true);
+    } else if (kLazyTail <= 0) {
+        flow_enqueue_rows(F, b, 0, K, with_d, kBatchTail, 0, true);
+    } else {
+        flow_enqueue_rows(F, b, 0, 0, with_d, kBatchOne, 0, true);
+    }
+}
+
+// Eager mode: queue every row of the next sequence beyond the first window (one thread), skipping
+// sequences the init kernel rejected.
+__device__ void flow_queue_next(const FlowArgs &F) {
+    const int K = F.acc.K;
+    while (true) {
+        const int nb = F.window + atomicAdd(&F.fc->next_seq.v, 1);
+        if (nb >= F.n_seq) return;
+        if (F.pos_cnt[nb] < 0) continue;
+        const bool greedy = F.acc.temperature[nb] == 0.0f;
+        flow_enqueue_rows(F, nb, 0, K, !greedy && K > 0, kBatchTail, 0, false);
+        return;
+    }
 }
 
 // Every sequence's init (grid-stride over sequences), and the clearing of the appended part of
@@ -236,7 +267,7 @@ __global__ void __launch_bounds__(kThreads) k_flow_init(const FlowArgs F, int B)
 __device__ void flow_to_exact(const FlowArgs &F, int draw, int b) {
     const AcceptArgs &a = F.acc;
     stats_add(a.stats, &a.stats->reresolved, 1);
-    const int i = atomicAdd(&a.counters->n_exact, 1);
+    const int i = atomicAdd(&F.fc->n_exact.v, 1);
     if (i >= F.cap_x) {
         stats_add(a.stats, &a.stats->unresolved, 1);
         flow_done(F);
@@ -277,7 +308,7 @@ __device__ void flow_draw(const FlowArgs &F, int b, int k, float T, const RowSta
     it.dbg_r = a.debug ? a.debug + (size_t)b * (K + 1) * SV_DEBUG_FIELDS + SV_DBG_R : nullptr;
     it.seq = b;
     it.k = k;
-    const int d = atomicAdd(&a.counters->n_draws, 1);
+    const int d = atomicAdd(&F.fc->n_draws.v, 1);
     a.draws[d] = it;
     flow_enqueue(F, kUnitDraw, (long long)d * F.d_split, F.d_split);
 }
@@ -362,6 +393,7 @@ __device__ void flow_fin_seq(const FlowArgs &F, int b, int j0, int kind, int cum
     int bad = 0;
     const int j_last = kind == kBatchOne ? j0 : K;   // rows of positions j0..j_last were read
     if (lane == 0) {
+        if (all_read) flow_queue_next(F);   // this sequence's rows are read: the window moves on
         const int n_d = greedy ? 0 : max(0, min(j_last, K - 1) - j0 + 1);
         stats_add(a.stats, &a.stats->rows, j_last - j0 + 1 + n_d);
     }
@@ -1005,9 +1037,11 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
     volatile int *ring_head = abort_flag + 2;     // requests taken by the finisher warp
     volatile int *cons_done = abort_flag + 3;     // consumer warps that left their loop
     TileMeta *meta = reinterpret_cast<TileMeta *>(smem + 2 * kStatsStages * 8 + 16);
-    volatile int4 *ring = reinterpret_cast<volatile int4 *>(smem + 1024);   // (x, type << 24 | y, z, slot + 1)
-    float *t_cache = reinterpret_cast<float *>(smem + 1024 + kFlowRing * 16);
-    float2 *tab = reinterpret_cast<float2 *>(smem + 1024 + kFlowRing * 16 + kFlowTCache * 4);
+    volatile int4 *ring = reinterpret_cast<volatile int4 *>(smem + kFlowOffRing);   // (x, type << 24 | y, z, slot + 1)
+    WarpPartial *s_part = reinterpret_cast<WarpPartial *>(smem + kFlowOffPart);   // [stage][warp]
+    int *s_part_cnt = reinterpret_cast<int *>(smem + kFlowOffPartCnt);             // [stage]
+    float *t_cache = reinterpret_cast<float *>(smem + kFlowOffTCache);
+    float2 *tab = reinterpret_cast<float2 *>(smem + kFlowOffTab);
     unsigned char *tiles = smem + kFlowCtlBytes;
     const StatsArgs &a = F.st;
     const int tid = threadIdx.x;
@@ -1022,6 +1056,7 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
         *ring_tail = 0;
         *ring_head = 0;
         *cons_done = 0;
+        for (int st = 0; st < kStatsStages; ++st) s_part_cnt[st] = 0;
         fence_barrier_init();
     }
     const int n_cache = min(kFlowTCache, F.n_seq);
@@ -1096,13 +1131,13 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
             // pass.  In the bulk of the pass each iteration claims the next slot and starts
             // loading its word before issuing the current unit's stages; near the end it claims
             // only when idle, so that queued units go to idle blocks.
-            const long long q0_n = *reinterpret_cast<volatile int *>(&a.counters->q0_tail);
+            const long long q0_n = *reinterpret_cast<volatile int *>(&F.fc->q0_tail.v);
             auto slot_of = [&](long long c) { return c < q0_n ? c : F.q1_base + (c - q0_n); };
             auto load_word = [&](long long c) {
                 const long long sl = slot_of(c);
                 return sl < F.cap ? ld_relaxed_u64(&F.units[sl]) : 0ull;
             };
-            long long claim = atomicAdd(&a.counters->q_head, 1);
+            long long claim = atomicAdd(&F.fc->q_head.v, 1);
             unsigned long long word = load_word(claim);
             // stage one: wait for the stage to be free, then describe it
             auto next_stage = [&]() -> bool {
@@ -1127,9 +1162,11 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                 unsigned payload = 0;
                 int type = 0;
                 unsigned ns = 32;
+                int spins = 0;
                 const long long t_start = clock64();   // the wait is bounded by its own length
                 while (slot_of(claim) < F.cap && !(word >> 63)) {
-                    if (ld_acquire(&a.counters->n_pending) == 0) break;   // no more work will appear
+                    // no more work will appear (read every few tries: every idle producer polls it)
+                    if ((spins++ & 3) == 0 && ld_acquire(&F.fc->n_pending.v) == 0) break;
                     if (*reinterpret_cast<volatile int *>(abort_flag) || clock64() - t_start > a.wait_limit) {
                         if (atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
                         ok = false;
@@ -1148,8 +1185,8 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                 const bool have = ok && unit >= 0;
                 long long next = -1;
                 unsigned long long next_word = 0;
-                if (have && q0_n + *reinterpret_cast<volatile int *>(&a.counters->q_tail) - claim > 2LL * gridDim.x) {
-                    next = atomicAdd(&a.counters->q_head, 1);
+                if (have && q0_n + *reinterpret_cast<volatile int *>(&F.fc->q_tail.v) - claim > 2LL * gridDim.x) {
+                    next = atomicAdd(&F.fc->q_head.v, 1);
                     next_word = load_word(next);
                 }
                 if (!have) {
@@ -1251,7 +1288,7 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                     claim = next;
                     word = next_word;
                 } else {
-                    claim = atomicAdd(&a.counters->q_head, 1);
+                    claim = atomicAdd(&F.fc->q_head.v, 1);
                     word = load_word(claim);
                 }
             }
@@ -1365,25 +1402,45 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
             if (m.flags & kTileFirst) acc_init(A);
             if (m.nv > 0) acc_tile<ES>(A, stage, m.nv, m.fv, greedy, m.c_hi);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
             if (m.flags & kTileLast) {
                 if (tid < m.n_tail) {
                     const float x = load_elem<ES>(m.row, m.tail0 + tid);
                     acc_scalar(A, x, m.tail0 + tid, greedy, m.c_hi, m.c_lo);
                 }
-                acc_store(A, greedy, a.part + ((size_t)m.rid * a.n_split + m.chunk) * kWarps + warp);
-                // the warp that completes the batch of rows hands the sequence to the finisher
-                int b = 0, j = 0;
-                seq_pos(F, m.rid, b, j);
+                // The eight warps' partials of the unit meet in shared memory; the last warp to
+                // arrive stores all eight and makes them visible with one fence and one count, so
+                // a unit costs one global fence, not eight.  The stage is released only after
+                // this (its partial slots and count are reused by the stage's next unit).
+                acc_store(A, greedy, s_part + st * kWarps + warp);
+                __syncwarp();
+                int last = 0;
                 if (lane == 0) {
-                    __threadfence();
-                    if (atomicAdd(&F.pos_cnt[b], 1) == (m.aux >> 8) - 1) {
+                    __threadfence_block();
+                    last = atomicAdd(&s_part_cnt[st], 1) == kWarps - 1;
+                }
+                last = __shfl_sync(0xFFFFFFFFu, last, 0);
+                if (last) {
+                    __threadfence_block();
+                    const uint4 *src = reinterpret_cast<const uint4 *>(s_part + st * kWarps);
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.part + ((size_t)m.rid * a.n_split + m.chunk) * kWarps);
+                    static_assert(kWarps * sizeof(WarpPartial) == 16 * 16, "one 16-byte word per lane of half a warp");
+                    if (lane < 16) dst[lane] = src[lane];
+                    __syncwarp();
+                    // the batch's last unit hands the sequence to the finisher
+                    int b = 0, j = 0;
+                    seq_pos(F, m.rid, b, j);
+                    if (lane == 0) {
+                        s_part_cnt[st] = 0;
                         __threadfence();
-                        post(kReqSeq, b, m.aux & 0xFF, m.aux >> 8);
+                        if (atomicAdd(&F.pos_cnt[b], kWarps) == (m.aux >> 8) - kWarps) {
+                            __threadfence();
+                            post(kReqSeq, b, m.aux & 0xFF, m.aux >> 8);
+                        }
                     }
                 }
                 __syncwarp();
             }
+            if (lane == 0) mbar_arrive(&empty[st]);
         }
         if (++st == kStatsStages) {
             st = 0;
@@ -1451,7 +1508,9 @@ static sv_status launch_flow(const VerifyPlan &pl, const AcceptArgs &acc_in, int
     F.cap_x = pl.cap_x;
     F.x_groups = pl.x_groups;
     F.max_slots = pl.max_slots;
-    if (cudaMemsetAsync(counters, 0, sizeof(Counters), stream) != cudaSuccess) return SV_ERR_CUDA;
+    F.fc = reinterpret_cast<FlowCounters *>(w + pl.off_flow_ctr);
+    F.window = lazy ? B : (B < kFlowWindow ? B : kFlowWindow);
+    if (cudaMemsetAsync(F.fc, 0, sizeof(FlowCounters), stream) != cudaSuccess) return SV_ERR_CUDA;
     {
         const long long clear = F.cap - F.q1_base;
         long long grid = div_up(B, kThreads);

@@ -64,7 +64,7 @@ struct VerifyPlan {
     size_t off_lz_units = 0, off_lz_pos = 0;   // work queue of the dataflow kernel (sv_flow.cu)
     long long lz_cap = 0;                  // queue capacity: every unit of a call once
     long long n_flow_initial = 0;          // queue slots for the units the init kernel writes
-    size_t off_draw_cnt = 0, off_xcnt = 0, off_acnt = 0, off_xuncw = 0;
+    size_t off_draw_cnt = 0, off_xcnt = 0, off_acnt = 0, off_xuncw = 0, off_flow_ctr = 0;
     int cap_x = 1;                         // most float-float items per call
     int x_groups = 1;                      // float-float row-pass units per item
     int max_slots = 2;                     // rows per sequence (2K + 1, at least 2)

@@ -160,6 +160,23 @@ struct Counters {
     int pad[6];
 };
 
+// Counters of the dataflow kernel, each on its own 128-byte line: producers of every block claim
+// units, finishers append units and count finished sequences, and a line shared by all of them
+// would serialise those atomics.  Zeroed by the host before each call.
+struct FlowCounter {
+    int v;
+    int pad[31];
+};
+struct FlowCounters {
+    FlowCounter q_head;      // next queue position to claim
+    FlowCounter q0_tail;     // units written by the init kernel
+    FlowCounter q_tail;      // units appended since
+    FlowCounter n_pending;   // sequences whose last token is not written yet
+    FlowCounter n_draws;     // draw items
+    FlowCounter n_exact;     // float-float items
+    FlowCounter next_seq;    // eager mode: sequences queued after the first window
+};
+
 inline int div_up(long long a, long long b) { return (int)((a + b - 1) / b); }
 
 // Chunks per row: enough (row, chunk) units to balance ~kUnitTarget of them, chunks >= one tile.

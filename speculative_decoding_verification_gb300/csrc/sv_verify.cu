@@ -247,6 +247,7 @@ VerifyPlan plan_verify(int B, int K, int V, int es) {
     p.off_xcnt = cv.take<int>(cap);
     p.off_acnt = cv.take<int>(cap);
     p.off_xuncw = cv.take<float2>(cap * kFlowUncCap);
+    p.off_flow_ctr = cv.take<FlowCounters>(1);
     static_assert(kFlowSplitA * kWarps <= kExactSplit * 3, "the float-float row sums fit the tier's partial buffer");
     const long long n_pairs = (long long)B * K;
     long long want = n_pairs > 0 ? (2LL * kUnitTarget + n_pairs - 1) / n_pairs : 1;

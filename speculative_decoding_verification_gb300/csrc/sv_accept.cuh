@@ -84,19 +84,15 @@ struct AcceptOutcome {
 // and C_s = C on the top-F set; y_q - y_p is formed in float-float.  The exponential, the
 // products and the quotient carry kEx2RelErr + 8u, the row sums err_q + err_p, the masses
 // 2(err_q + err_p), the normaliser z_err; u < ratio is certain outside ratio (1 -+ delta).
-template <int ES>
-__device__ __forceinline__ AcceptOutcome accept_test(const AcceptArgs &a, int b, int j, int s, double u_acc,
-                                                     float c_hi, float c_lo, const RowStat &rq, const RowStat &rp) {
+// xt, xd: the target and draft logits of token s at position j (loaded by the caller).
+__device__ __forceinline__ AcceptOutcome accept_test_x(const AcceptArgs &a, int b, int j, int s, double u_acc,
+                                                       float c_hi, float c_lo, const RowStat &rq, const RowStat &rp,
+                                                       float xt, float xd) {
     bool acc = false, amb = false, near = false;
     bool keep_q = false, keep_p = false, in_top = false;
     float ratio = NAN;
     const long long rid_t = (long long)b * (a.K + 1) + j;
     const long long rid_d = a.n_rows0 + (long long)b * a.K + j;
-    const RowSet &ts = a.tgt, &ds = a.drf;
-    const char *trow = ts.base + ((long long)b * ts.rows_per_seq + j) * ts.pitch_bytes;
-    const char *drow = ds.base + ((long long)b * ds.rows_per_seq + j) * ds.pitch_bytes;
-    const float xt = load_elem<ES>(trow, s);
-    const float xd = load_elem<ES>(drow, s);
     float num = rp.s_hi, den = rq.s_hi;
     float delta = (float)(kEx2RelErr + 8.0 * kU32 + 1e-10) + rq.err + rp.err;
     keep_q = xt != -INFINITY;
@@ -146,6 +142,16 @@ __device__ __forceinline__ AcceptOutcome accept_test(const AcceptArgs &a, int b,
     amb = (u >= lo && u < hi) || (keep_q && keep_p && ratio < 0x1p-100f && u < 0x1p-90f);
     near = fabsf(u - rr) < 1e-6f;
     return {acc, amb, near, keep_q, keep_p, in_top, ratio};
+}
+
+// The accept test of position j with the two logits of s loaded here.
+template <int ES>
+__device__ __forceinline__ AcceptOutcome accept_test(const AcceptArgs &a, int b, int j, int s, double u_acc,
+                                                     float c_hi, float c_lo, const RowStat &rq, const RowStat &rp) {
+    const RowSet &ts = a.tgt, &ds = a.drf;
+    const char *trow = ts.base + ((long long)b * ts.rows_per_seq + j) * ts.pitch_bytes;
+    const char *drow = ds.base + ((long long)b * ds.rows_per_seq + j) * ds.pitch_bytes;
+    return accept_test_x(a, b, j, s, u_acc, c_hi, c_lo, rq, rp, load_elem<ES>(trow, s), load_elem<ES>(drow, s));
 }
 
 }  // namespace sv

@@ -50,7 +50,6 @@ namespace sv {
 constexpr int kFlowThreads = kStatsThreads + 32;   // 8 consumer warps, producer, finisher
 constexpr int kFlowRing = 64;                      // finisher requests in flight per block
 constexpr int kFlowTCache = 1024;                  // temperatures cached in shared memory
-constexpr int kFlowWindow = 64;                    // eager mode: sequences queued ahead at a time
 // shared memory: control block (barriers, flags, stage descriptions), finisher ring, the eight
 // consumer warps' partials of each stage's unit and their arrival counts, temperatures, exp2 table
 constexpr int kFlowOffRing = 1024;
@@ -83,11 +82,9 @@ struct FlowArgs {
     long long cap;
     long long q1_base;   // units[0, q1_base): written by the init kernel; units[q1_base, cap): appended
     FlowCounters *fc;    // the kernel's counters (one cache line each)
-    int *pos_cnt;        // [B] consumer warps done with the sequence's statistics units (cumulative);
-                         // -1 for a sequence the init kernel rejected
+    int *pos_cnt;        // [B] consumer warps done with the sequence's statistics units (cumulative)
     int n_seq;
     int lazy;
-    int window;          // eager mode: sequences the init kernel queues; each finished one queues the next
     // draws
     int n_vec, n_sub, d_split;
     float *subs;         // [B][n_sub] float32 sum of the weights of each sub-chunk
@@ -119,6 +116,11 @@ __device__ __forceinline__ int ld_acquire(const int *p) {
     asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+
+// Release / acquire fence at GPU scope: the thread's earlier writes (and those it has observed)
+// are visible to any thread that observes its later writes, and it sees what such writers wrote
+// before their own release.  Lighter than the sequentially consistent __threadfence().
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ unsigned long long unit_word(int type, unsigned payload, unsigned index) {
     return (1ull << 63) | ((unsigned long long)type << 60) | ((unsigned long long)(payload & 0x0FFFFFFFu) << 32) | index;
@@ -193,7 +195,7 @@ __device__ __forceinline__ void flow_done(const FlowArgs &F) { atomicSub(&F.fc->
 
 // One sequence of the init kernel: validate, mark the debug fields undefined, queue its first rows.
 __device__ void flow_init_seq(const FlowArgs &F, int b) {
-    F.pos_cnt[b] = -1;   // rejected until validated
+    F.pos_cnt[b] = 0;
     const AcceptArgs &a = F.acc;
     const int K = a.K;
     const float T = a.temperature[b];
@@ -217,30 +219,10 @@ __device__ void flow_init_seq(const FlowArgs &F, int b) {
             return;
         }
     }
-    F.pos_cnt[b] = 0;
     atomicAdd(&F.fc->n_pending.v, 1);
     const bool with_d = !greedy && K > 0;
-    if (!F.lazy) {
-        if (b < F.window) flow_enqueue_rows(F, b, 0, K, with_d, kBatchTail, 0, true);
-    } else if (kLazyTail <= 0) {
-        flow_enqueue_rows(F, b, 0, K, with_d, kBatchTail, 0, true);
-    } else {
-        flow_enqueue_rows(F, b, 0, 0, with_d, kBatchOne, 0, true);
-    }
-}
-
-// Eager mode: queue every row of the next sequence beyond the first window (one thread), skipping
-// sequences the init kernel rejected.
-__device__ void flow_queue_next(const FlowArgs &F) {
-    const int K = F.acc.K;
-    while (true) {
-        const int nb = F.window + atomicAdd(&F.fc->next_seq.v, 1);
-        if (nb >= F.n_seq) return;
-        if (F.pos_cnt[nb] < 0) continue;
-        const bool greedy = F.acc.temperature[nb] == 0.0f;
-        flow_enqueue_rows(F, nb, 0, K, !greedy && K > 0, kBatchTail, 0, false);
-        return;
-    }
+    if (!F.lazy || kLazyTail <= 0) flow_enqueue_rows(F, b, 0, K, with_d, kBatchTail, 0, true);
+    else flow_enqueue_rows(F, b, 0, 0, with_d, kBatchOne, 0, true);
 }
 
 // Every sequence's init (grid-stride over sequences), and the clearing of the appended part of
@@ -335,10 +317,30 @@ __device__ void flow_debug(const AcceptArgs &a, int b, int j, float T, const Row
     dbg[SV_DBG_MASS_P] = 1.0;
 }
 
+__device__ __forceinline__ RowStat shfl_rowstat(const RowStat &r, int src) {
+    RowStat o;
+    o.s_hi = __shfl_sync(0xFFFFFFFFu, r.s_hi, src);
+    o.s_lo = __shfl_sync(0xFFFFFFFFu, r.s_lo, src);
+    o.err = __shfl_sync(0xFFFFFFFFu, r.err, src);
+    o.maxv = __shfl_sync(0xFFFFFFFFu, r.maxv, src);
+    o.argmax = __shfl_sync(0xFFFFFFFFu, r.argmax, src);
+    o.r = __shfl_sync(0xFFFFFFFFu, r.r, src);
+    o.flags = __shfl_sync(0xFFFFFFFFu, r.flags, src);
+    o.ay = __shfl_sync(0xFFFFFFFFu, r.ay, src);
+    return o;
+}
+
+__device__ __forceinline__ bool rowstat_bad(const RowStat &r, bool greedy) {
+    return (r.flags != 0) || (greedy ? !isfinite(r.maxv) : !rs_sampled_ok(r));
+}
+
 // The batch of rows starting at position j0 of sequence b is complete (one warp).  In eager
-// mode the batch is every row of the sequence: all are combined first (a non-finite row anywhere
+// mode the batch is every row of the sequence: all are checked first (a non-finite row anywhere
 // fails the sequence, and every position's debug values are written), then the positions are
-// walked.  In lazy mode the batch's rows are combined as the walk reaches them.
+// walked.  When every row was one unit (large batches), the consumers combined the rows'
+// statistics already and lane j loads position j's statistics and the logits of its drafted
+// token, all at once; otherwise the rows are combined here from the chunks' partials, one after
+// another.  In lazy mode the batch's rows are combined as the walk reaches them.
 template <int ES>
 __device__ void flow_fin_seq(const FlowArgs &F, int b, int j0, int kind, int cum) {
     const AcceptArgs &a = F.acc;
@@ -349,6 +351,7 @@ __device__ void flow_fin_seq(const FlowArgs &F, int b, int j0, int kind, int cum
     const double u_l = lane <= K ? a.uniforms[(size_t)b * (K + 1) + lane] : 0.0;
     const bool greedy = (T == 0.0f);
     const bool all_read = !F.lazy;
+    const bool fast = all_read && ns == 1 && K < 32;
     auto token = [&](int j) {
         const int v = __shfl_sync(0xFFFFFFFFu, tok_l, j & 31);
         return j < 32 ? v : a.tokens[(size_t)b * K + j];
@@ -359,21 +362,29 @@ __device__ void flow_fin_seq(const FlowArgs &F, int b, int j0, int kind, int cum
             outs[j] = j < k ? (j < 32 ? tok_l : a.tokens[(size_t)b * K + j]) : (j == k ? tstar : -1);
         if (lane == 0) a.accept_len[b] = k;
     };
-    // combine a row's partials (valid in lane 0), keep it for the float-float tier, check it
+    auto row_t = [&](int j) { return a.tgt.base + ((long long)b * a.tgt.rows_per_seq + j) * a.tgt.pitch_bytes; };
+    auto row_d = [&](int j) { return a.drf.base + ((long long)b * a.drf.rows_per_seq + j) * a.drf.pitch_bytes; };
+    // a row's statistics (valid in lane 0): read when the consumers combined them, else combined
+    // here from the chunks' partials; kept for the float-float tier and checked
     auto combine = [&](long long rid, int &bad) {
-        const RowStat r = combine_row(a.part + (size_t)rid * ns * kWarps, ns * kWarps, greedy, T);
+        RowStat r{};
+        if (ns == 1) {
+            if (lane == 0) r = a.rowstat[rid];
+        } else {
+            r = combine_row(a.part + (size_t)rid * ns * kWarps, ns * kWarps, greedy, T);
+        }
         if (lane == 0) {
-            a.rowstat[rid] = r;
-            if ((r.flags != 0) || (greedy ? !isfinite(r.maxv) : !rs_sampled_ok(r))) {
+            if (ns != 1) a.rowstat[rid] = r;
+            if (rowstat_bad(r, greedy)) {
                 report_error(a.stats, SV_ERR_NONFINITE, (int)rid);
                 bad = 1;
             }
         }
         return r;
     };
-    // debug values of position j (lane 0; the rows' statistics in rq, rp)
-    auto debug_at = [&](int j, const RowStat &rq, const RowStat &rp) {
-        if (!a.debug || lane != 0) return;
+    // debug values of position j, written by the calling lane (rq, rp: its rows' statistics)
+    auto debug_own = [&](int j, const RowStat &rq, const RowStat &rp) {
+        if (!a.debug) return;
         if (greedy) {
             a.debug[((size_t)b * (K + 1) + j) * SV_DEBUG_FIELDS + SV_DBG_MASS_Q] = 1.0;
             if (j < K) a.debug[((size_t)b * (K + 1) + j) * SV_DEBUG_FIELDS + SV_DBG_MASS_P] = 1.0;
@@ -381,23 +392,52 @@ __device__ void flow_fin_seq(const FlowArgs &F, int b, int j0, int kind, int cum
             flow_debug<ES>(a, b, j, T, rq, j < K ? &rp : nullptr);
         }
     };
-    // every row of positions j_from..j_to, combined (lazy mode: rows the walk did not reach)
+    // every row of positions j_from..j_to, combined one after another
     auto combine_range = [&](int j_from, int j_to, int &bad) {
         for (int jj = j_from; jj <= j_to; ++jj) {
             const RowStat rq = combine((long long)b * (K + 1) + jj, bad);
             RowStat rp{};
             if (!greedy && jj < K) rp = combine(F.st.n_rows0 + (long long)b * K + jj, bad);
-            debug_at(jj, rq, rp);
+            if (lane == 0) debug_own(jj, rq, rp);
         }
     };
     int bad = 0;
     const int j_last = kind == kBatchOne ? j0 : K;   // rows of positions j0..j_last were read
     if (lane == 0) {
-        if (all_read) flow_queue_next(F);   // this sequence's rows are read: the window moves on
         const int n_d = greedy ? 0 : max(0, min(j_last, K - 1) - j0 + 1);
         stats_add(a.stats, &a.stats->rows, j_last - j0 + 1 + n_d);
     }
-    if (kind == kBatchComplete || all_read) {
+    // lane j's position: its rows' statistics and its drafted token's two logits (fast path)
+    RowStat rq_l{}, rp_l{};
+    float xt_l = 0.f, xd_l = 0.f;
+    if (fast) {
+        const int j = lane;
+        int badl = 0;
+        if (j <= K) {
+            const long long rid_q = (long long)b * (K + 1) + j, rid_p = F.st.n_rows0 + (long long)b * K + j;
+            rq_l = a.rowstat[rid_q];
+            if (!greedy && j < K) {
+                rp_l = a.rowstat[rid_p];
+                xt_l = load_elem<ES>(row_t(j), tok_l);
+                xd_l = load_elem<ES>(row_d(j), tok_l);
+            }
+            if (rowstat_bad(rq_l, greedy)) {
+                report_error(a.stats, SV_ERR_NONFINITE, (int)rid_q);
+                badl = 1;
+            }
+            if (!greedy && j < K && rowstat_bad(rp_l, greedy)) {
+                report_error(a.stats, SV_ERR_NONFINITE, (int)rid_p);
+                badl = 1;
+            }
+        }
+        bad = __any_sync(0xFFFFFFFFu, badl);
+        if (bad) {
+            outputs(0, -1);
+            if (lane == 0) flow_done(F);
+            return;
+        }
+        if (j <= K) debug_own(j, rq_l, rp_l);
+    } else if (kind == kBatchComplete || all_read) {
         combine_range(j0, K, bad);
         bad = __shfl_sync(0xFFFFFFFFu, bad, 0);
         if (bad) {
@@ -415,18 +455,30 @@ __device__ void flow_fin_seq(const FlowArgs &F, int b, int j0, int kind, int cum
     for (int j = j0; j <= j_last; ++j) {
         const long long rid_q = (long long)b * (K + 1) + j, rid_p = F.st.n_rows0 + (long long)b * K + j;
         const bool with_p = !greedy && j < K;
+        const int s = j < K ? token(j) : -1;   // every lane: token() shuffles
         RowStat rq{}, rp{};
-        if (all_read) {
-            if (lane == 0) {
-                rq = a.rowstat[rid_q];
-                if (with_p) rp = a.rowstat[rid_p];
-            }
+        float xt = 0.f, xd = 0.f;
+        if (fast) {
+            rq = shfl_rowstat(rq_l, j);
+            rp = shfl_rowstat(rp_l, j);
+            xt = __shfl_sync(0xFFFFFFFFu, xt_l, j);
+            xd = __shfl_sync(0xFFFFFFFFu, xd_l, j);
         } else {
-            rq = combine(rid_q, bad);
-            if (with_p) rp = combine(rid_p, bad);
-            debug_at(j, rq, rp);
+            if (all_read) {
+                if (lane == 0) {
+                    rq = a.rowstat[rid_q];
+                    if (with_p) rp = a.rowstat[rid_p];
+                }
+            } else {
+                rq = combine(rid_q, bad);
+                if (with_p) rp = combine(rid_p, bad);
+                if (lane == 0) debug_own(j, rq, rp);
+            }
+            if (with_p && lane == 0) {
+                xt = load_elem<ES>(row_t(j), s);
+                xd = load_elem<ES>(row_d(j), s);
+            }
         }
-        const int s = j < K ? token(j) : -1;
         const double u_j = __shfl_sync(0xFFFFFFFFu, u_l, j & 31);
         // lane 0 decides: 0 finished (k, tstar), 1 accepted, 2 float-float tier, 3 a draw is queued
         int verdict = 0, k = 0, tstar = -1;
@@ -441,8 +493,8 @@ __device__ void flow_fin_seq(const FlowArgs &F, int b, int j0, int kind, int cum
                     tstar = rq.argmax;
                 }
             } else if (with_p) {
-                const AcceptOutcome o =
-                    accept_test<ES>(a, b, j, s, j < 32 ? u_j : a.uniforms[(size_t)b * (K + 1) + j], c_hi, c_lo, rq, rp);
+                const AcceptOutcome o = accept_test_x(a, b, j, s, j < 32 ? u_j : a.uniforms[(size_t)b * (K + 1) + j],
+                                                      c_hi, c_lo, rq, rp, xt, xd);
                 stats_add(a.stats, &a.stats->accept_tests, 1);
                 if (o.near) stats_add(a.stats, &a.stats->near_boundary, 1);
                 if (o.amb) {
@@ -511,10 +563,17 @@ __device__ void flow_finish(const FlowArgs &F, int d) {
     const int s0 = min(lane * per, n_sub), s1 = min(s0 + per, n_sub);
     ff wsum = {0.f, 0.f};
     int last_pos = -1;
-    for (int s = s0; s < s1; ++s) {
-        const float v = subs[s];
-        wsum = ff_add_f(wsum, v);
-        if (v > 0.f) last_pos = s;
+    for (int sb = s0; sb < s1; sb += 8) {   // eight loads in flight, then their sums
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = sb + e < s1 ? subs[sb + e] : 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if (sb + e < s1) {
+                wsum = ff_add_f(wsum, v[e]);
+                if (v[e] > 0.f) last_pos = sb + e;
+            }
+        }
     }
     ff incl = wsum;
 #pragma unroll
@@ -540,15 +599,23 @@ __device__ void flow_finish(const FlowArgs &F, int d) {
     ff pre = excl;
     if (wsum.hi > 0.f && ff_diff(thr, excl) >= 0.f && ff_diff(thr, incl) < 0.f) {
         ff run = excl;
-        for (int s = s0; s < s1; ++s) {
-            const float wv = subs[s];
-            const ff nx = ff_add_f(run, wv);
-            if (wv > 0.f) {
-                found = s;
-                pre = run;
-                if (ff_diff(thr, nx) < 0.f) break;
+        bool done = false;
+        for (int sb = s0; sb < s1 && !done; sb += 8) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = sb + e < s1 ? subs[sb + e] : 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (!done && sb + e < s1) {
+                    const ff nx = ff_add_f(run, v[e]);
+                    if (v[e] > 0.f) {
+                        found = sb + e;
+                        pre = run;
+                        if (ff_diff(thr, nx) < 0.f) done = true;
+                    }
+                    run = nx;
+                }
             }
-            run = nx;
         }
     }
     const unsigned fm = __ballot_sync(0xFFFFFFFFu, found >= 0);
@@ -763,10 +830,15 @@ __device__ void flow_exact_d(const FlowArgs &F, int i, const float2 *tab) {
     const float4 *xn = F.xnorm + (size_t)i * F.n_sub;
     const int n_sub = F.n_sub, n_vsub = n_sub - 1, n_vec = F.n_vec;
     ff sq = {0.f, 0.f}, sp = {0.f, 0.f};
-    for (int s = lane; s < n_sub; s += 32) {
-        const float4 v = xn[s];
-        sq = ff_add(sq, {v.x, v.y});
-        sp = ff_add(sp, {v.z, v.w});
+    for (int s8 = lane; s8 < n_sub; s8 += 8 * 32) {   // eight loads in flight, then their sums
+        float4 v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = s8 + e * 32 < n_sub ? xn[s8 + e * 32] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            sq = ff_add(sq, {v[e].x, v[e].y});
+            sp = ff_add(sp, {v[e].z, v[e].w});
+        }
     }
     sq = warp_sum_ff(sq);
     sp = warp_sum_ff(sp);
@@ -785,24 +857,52 @@ __device__ void flow_exact_d(const FlowArgs &F, int i, const float2 *tab) {
     }
     __syncwarp();
     __threadfence_block();
-    auto W = [&](int s) {
-        const float4 v = xs[s];
-        ff w = ff_sub(ff_mul({v.x, v.y}, iq), ff_mul({v.z, v.w}, ip));
-        for (int k = 0; k < n_unc; ++k) {
-            const int t = unc[k];
-            const int ts = t < n_vec * (16 / ES) ? t / (32 * (16 / ES)) : n_vsub;
-            if (ts == s) w = ff_add(w, {uncw[k].x, uncw[k].y});
-        }
-        return w;
-    };
+    // W(s) = A_q(s) / S_q - A_p(s) / S_p (+ the exact residuals of its uncertain tokens) for the
+    // lane's own sub-chunks, written over the item's sums in place (read back below), so that the
+    // uncertain list is walked once per lane
+    float4 *xw = F.xsubs + (size_t)i * F.n_sub;
     const int per = (n_sub + 31) / 32;
     const int s0 = min(lane * per, n_sub), s1 = min(s0 + per, n_sub);
+    for (int sb = s0; sb < s1; sb += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = sb + e < s1 ? xs[sb + e] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (sb + e < s1) {
+                const ff w = ff_sub(ff_mul({v[e].x, v[e].y}, iq), ff_mul({v[e].z, v[e].w}, ip));
+                xw[sb + e] = make_float4(w.hi, w.lo, 0.f, 0.f);
+            }
+        }
+    }
+    for (int k = 0; k < n_unc; ++k) {
+        const int t = unc[k];
+        const int ts = t < n_vec * (16 / ES) ? t / (32 * (16 / ES)) : n_vsub;
+        if (ts >= s0 && ts < s1) {
+            const float4 v = xw[ts];
+            const ff w = ff_add({v.x, v.y}, {uncw[k].x, uncw[k].y});
+            xw[ts] = make_float4(w.hi, w.lo, 0.f, 0.f);
+        }
+    }
+    __syncwarp();
+    __threadfence_block();   // the fallback below reads other lanes' sub-chunks
+    auto W = [&](int s) {
+        const float4 v = xw[s];
+        return ff{v.x, v.y};
+    };
     ff mine = {0.f, 0.f};
     int last_pos = -1;
-    for (int s = s0; s < s1; ++s) {
-        const ff w = W(s);
-        mine = ff_add(mine, w);
-        if (w.hi > 0.f) last_pos = s;
+    for (int sb = s0; sb < s1; sb += 4) {
+        ff v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = sb + e < s1 ? W(sb + e) : ff{0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (sb + e < s1) {
+                mine = ff_add(mine, v[e]);
+                if (v[e].hi > 0.f) last_pos = sb + e;
+            }
+        }
     }
     ff incl = mine;
 #pragma unroll
@@ -827,15 +927,23 @@ __device__ void flow_exact_d(const FlowArgs &F, int i, const float2 *tab) {
     ff pre = excl;
     if (mine.hi > 0.f && ff_diff(thr, excl) >= 0.f && ff_diff(thr, incl) < 0.f) {
         ff run = excl;
-        for (int s = s0; s < s1; ++s) {
-            const ff w = W(s);
-            const ff nx = ff_add(run, w);
-            if (w.hi > 0.f && ff_diff(thr, nx) < 0.f) {
-                found = s;
-                pre = run;
-                break;
+        bool done = false;
+        for (int sb = s0; sb < s1 && !done; sb += 4) {
+            ff v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = sb + e < s1 ? W(sb + e) : ff{0.f, 0.f};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (!done && sb + e < s1) {
+                    const ff nx = ff_add(run, v[e]);
+                    if (v[e].hi > 0.f && ff_diff(thr, nx) < 0.f) {
+                        found = sb + e;
+                        pre = run;
+                        done = true;
+                    }
+                    run = nx;
+                }
             }
-            run = nx;
         }
     }
     const unsigned fm = __ballot_sync(0xFFFFFFFFu, found >= 0);
@@ -859,18 +967,23 @@ __device__ void flow_exact_d(const FlowArgs &F, int i, const float2 *tab) {
         const int t0 = sub < n_vsub ? sub * 32 * EPV : n_vec * EPV;
         const int ntok = sub < n_vsub ? min(32 * EPV, (n_vec - sub * 32) * EPV) : a.V - n_vec * EPV;
         ff wt[EPV];
+        float xq[EPV], xp[EPV];
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {   // the lane's logits first, all loads in flight
+            const int idx = lane * EPV + e;   // lane-major: the lane's tokens are consecutive
+            xq[e] = idx < ntok ? load_elem<ES>(d.q.row, t0 + idx) : -INFINITY;
+            xp[e] = (idx < ntok && d.has_p) ? load_elem<ES>(d.p.row, t0 + idx) : -INFINITY;
+        }
         ff lt = {0.f, 0.f};
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
-            const int idx = lane * EPV + e;   // lane-major: the lane's tokens are consecutive
+            const int idx = lane * EPV + e;
             wt[e] = {0.f, 0.f};
             if (idx < ntok) {
                 const int t = t0 + idx;
-                const float xq = load_elem<ES>(d.q.row, t);
-                const ff q = ff_mul(exact_w(d.q, xq, t, tab), iq);
+                const ff q = ff_mul(exact_w(d.q, xq[e], t, tab), iq);
                 if (d.has_p) {
-                    const float xp = load_elem<ES>(d.p.row, t);
-                    const ff w = ff_sub(q, ff_mul(exact_w(d.p, xp, t, tab), ip));
+                    const ff w = ff_sub(q, ff_mul(exact_w(d.p, xp[e], t, tab), ip));
                     wt[e] = w.hi > 0.f ? w : ff{0.f, 0.f};
                 } else {
                     wt[e] = q;
@@ -968,7 +1081,7 @@ __device__ void flow_exact_c(const FlowArgs &F, long long unit, const float2 *ta
             if (vi < n_vec) {
                 const uint4 wq = __ldg(reinterpret_cast<const uint4 *>(d.q.row) + vi);
                 const uint4 wp = d.has_p ? __ldg(reinterpret_cast<const uint4 *>(d.p.row) + vi) : wq;
-#pragma unroll 1
+#pragma unroll 2
                 for (int k = 0; k < EPV; ++k) token(elem_of<ES>(wq, k), elem_of<ES>(wp, k), vi * EPV + k);
             }
         } else {
@@ -1127,18 +1240,47 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
             int st = 0;
             uint32_t epar = 0;
             bool ok = true;
-            // One FIFO: the units written by the init kernel, then the units appended during the
-            // pass.  In the bulk of the pass each iteration claims the next slot and starts
-            // loading its word before issuing the current unit's stages; near the end it claims
-            // only when idle, so that queued units go to idle blocks.
-            const long long q0_n = *reinterpret_cast<volatile int *>(&F.fc->q0_tail.v);
-            auto slot_of = [&](long long c) { return c < q0_n ? c : F.q1_base + (c - q0_n); };
-            auto load_word = [&](long long c) {
-                const long long sl = slot_of(c);
-                return sl < F.cap ? ld_relaxed_u64(&F.units[sl]) : 0ull;
+            // Two queues.  The units appended during the pass (draws, float-float units, lazy
+            // mode's later rows) go first while some are visibly queued, so that a sequence's
+            // later work follows its rows closely; the units the init kernel wrote fill the
+            // rest.  An appended slot is claimed by compare-and-swap only while the tail is past
+            // the head (a few tries, then the other queue), so no producer waits on a slot that
+            // may never be filled; the slot's word may still be on its way from the appender, so
+            // its valid bit is awaited (briefly).
+            const int q0_n = *reinterpret_cast<volatile int *>(&F.fc->q0_tail.v);
+            volatile int *q_tail_v = reinterpret_cast<volatile int *>(&F.fc->q_tail.v);
+            volatile int *q_head1_v = reinterpret_cast<volatile int *>(&F.fc->q_head1.v);
+            volatile int *q_head0_v = reinterpret_cast<volatile int *>(&F.fc->q_head.v);
+            // 1: a word claimed, 0: nothing queued now, -1: abort
+            auto claim_word = [&](unsigned long long &wd) -> int {
+                int h1 = *q_head1_v;
+                for (int tries = 0; tries < 3 && h1 < *q_tail_v; ++tries) {
+                    const int prev = atomicCAS(&F.fc->q_head1.v, h1, h1 + 1);
+                    if (prev != h1) {
+                        h1 = prev;
+                        continue;
+                    }
+                    const long long sl = F.q1_base + h1;
+                    if (sl >= F.cap) return 0;
+                    const long long t0 = clock64();
+                    while (!((wd = ld_relaxed_u64(&F.units[sl])) >> 63)) {
+                        if (*reinterpret_cast<volatile int *>(abort_flag) || clock64() - t0 > a.wait_limit) {
+                            if (atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
+                            return -1;
+                        }
+                        __nanosleep(32);
+                    }
+                    return 1;
+                }
+                if (*q_head0_v < q0_n) {
+                    const int c = atomicAdd(&F.fc->q_head.v, 1);
+                    if (c < q0_n) {
+                        wd = ld_relaxed_u64(&F.units[c]);
+                        return 1;
+                    }
+                }
+                return 0;
             };
-            long long claim = atomicAdd(&F.fc->q_head.v, 1);
-            unsigned long long word = load_word(claim);
             // stage one: wait for the stage to be free, then describe it
             auto next_stage = [&]() -> bool {
                 if (it >= kStatsStages) {
@@ -1157,15 +1299,38 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                     if (it >= 2 * kStatsStages) epar ^= 1u;   // round r >= 2 waits phase r - 1
                 }
             };
+            // The next unit is claimed while the current one's last stage waits for a free slot,
+            // so the claim's round trips overlap the copies in flight.
+            unsigned long long pf = 0;   // a claimed word not yet issued (bit 63 set), or 0
+            auto prefetch = [&]() {
+                if (pf >> 63) return;
+                unsigned long long wd = 0;
+                const int got = claim_word(wd);
+                if (got < 0) ok = false;
+                else if (got > 0) pf = wd;
+            };
             while (ok) {
                 long long unit = -1;
                 unsigned payload = 0;
                 int type = 0;
-                unsigned ns = 32;
+                unsigned long long word = 0;
+                unsigned ns = 64;
                 int spins = 0;
                 const long long t_start = clock64();   // the wait is bounded by its own length
-                while (slot_of(claim) < F.cap && !(word >> 63)) {
-                    // no more work will appear (read every few tries: every idle producer polls it)
+                while (true) {
+                    if (pf >> 63) {
+                        word = pf;
+                        pf = 0;
+                        break;
+                    }
+                    const int got = claim_word(word);
+                    if (got < 0) {
+                        ok = false;
+                        break;
+                    }
+                    if (got > 0) break;
+                    // nothing queued: has every sequence finished?  (read every few tries: every
+                    // idle producer polls it; the sleeps grow so idle producers stay quiet)
                     if ((spins++ & 3) == 0 && ld_acquire(&F.fc->n_pending.v) == 0) break;
                     if (*reinterpret_cast<volatile int *>(abort_flag) || clock64() - t_start > a.wait_limit) {
                         if (atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
@@ -1173,22 +1338,15 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                         break;
                     }
                     __nanosleep(ns);
-                    ns = ns < 256 ? 2 * ns : 256;
-                    word = load_word(claim);
+                    ns = ns < 1024 ? 2 * ns : 1024;
                 }
-                if (word >> 63) {
+                if (ok && (word >> 63)) {
                     unit = (long long)(unsigned)(word & 0xFFFFFFFFu);
                     type = (int)((word >> 60) & 7u);
                     payload = (unsigned)((word >> 32) & 0x0FFFFFFFu);
                     if (type != kUnitStats) __threadfence();   // acquire: the unit's data was written before it
                 }
                 const bool have = ok && unit >= 0;
-                long long next = -1;
-                unsigned long long next_word = 0;
-                if (have && q0_n + *reinterpret_cast<volatile int *>(&F.fc->q_tail.v) - claim > 2LL * gridDim.x) {
-                    next = atomicAdd(&F.fc->q_head.v, 1);
-                    next_word = load_word(next);
-                }
                 if (!have) {
                     if (next_stage()) {
                         TileMeta m;
@@ -1202,7 +1360,8 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                     const UnitInfo ui = stats_unit<ES>(a, unit, t_cache, n_cache);
                     const int nt = max(unit_tiles(ui), 1);
                     for (int t = 0; t < nt && ok; ++t) {
-                        if (!next_stage()) {
+                        if (t == nt - 1) prefetch();
+                        if (!ok || !next_stage()) {
                             ok = false;
                             break;
                         }
@@ -1242,7 +1401,8 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                     constexpr int HV = kTileBytes / 16;   // vectors per half stage
                     const int nt = max((v1 - v0 + HV - 1) / HV, 1);
                     for (int t = 0; t < nt && ok; ++t) {
-                        if (!next_stage()) {
+                        if (t == nt - 1) prefetch();
+                        if (!ok || !next_stage()) {
                             ok = false;
                             break;
                         }
@@ -1283,13 +1443,6 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                         mbar_arrive(&full[st]);
                         advance();
                     }
-                }
-                if (next >= 0) {
-                    claim = next;
-                    word = next_word;
-                } else {
-                    claim = atomicAdd(&F.fc->q_head.v, 1);
-                    word = load_word(claim);
                 }
             }
             // after an abort, copies still in flight land before shared memory is released
@@ -1424,23 +1577,45 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                     const uint4 *src = reinterpret_cast<const uint4 *>(s_part + st * kWarps);
                     uint4 *dst = reinterpret_cast<uint4 *>(a.part + ((size_t)m.rid * a.n_split + m.chunk) * kWarps);
                     static_assert(kWarps * sizeof(WarpPartial) == 16 * 16, "one 16-byte word per lane of half a warp");
-                    if (lane < 16) dst[lane] = src[lane];
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (lane < 16) v = src[lane];
                     __syncwarp();
+                    // the stage's partial slots are read: free the stage before the fence, so that
+                    // the fence's wait holds up this warp only, not the block's pipeline
+                    if (lane == 0) {
+                        s_part_cnt[st] = 0;
+                        mbar_arrive(&empty[st]);
+                    }
                     // the batch's last unit hands the sequence to the finisher
                     int b = 0, j = 0;
                     seq_pos(F, m.rid, b, j);
+                    if (a.n_split == 1) {
+                        // the unit is the whole row: its statistics are combined here, off the
+                        // finisher's path (the partials are read from the registers of lanes 0-15)
+                        __shared__ __align__(16) WarpPartial s_row[kWarps][kWarps];   // per warp: the 8 partials
+                        if (lane < 16) reinterpret_cast<uint4 *>(s_row[warp])[lane] = v;
+                        __syncwarp();
+                        const float Tb = b < n_cache ? t_cache[b] : F.acc.temperature[b];
+                        const RowStat r = combine_row(s_row[warp], kWarps, greedy, Tb);
+                        if (lane == 0) F.acc.rowstat[m.rid] = r;
+                    } else if (lane < 16) {
+                        dst[lane] = v;
+                    }
+                    __syncwarp();
                     if (lane == 0) {
-                        s_part_cnt[st] = 0;
-                        __threadfence();
+                        fence_acq_rel_gpu();
                         if (atomicAdd(&F.pos_cnt[b], kWarps) == (m.aux >> 8) - kWarps) {
-                            __threadfence();
+                            fence_acq_rel_gpu();
                             post(kReqSeq, b, m.aux & 0xFF, m.aux >> 8);
                         }
                     }
+                } else if (lane == 0) {
+                    mbar_arrive(&empty[st]);
                 }
                 __syncwarp();
+            } else if (lane == 0) {
+                mbar_arrive(&empty[st]);
             }
-            if (lane == 0) mbar_arrive(&empty[st]);
         }
         if (++st == kStatsStages) {
             st = 0;
@@ -1509,7 +1684,6 @@ static sv_status launch_flow(const VerifyPlan &pl, const AcceptArgs &acc_in, int
     F.x_groups = pl.x_groups;
     F.max_slots = pl.max_slots;
     F.fc = reinterpret_cast<FlowCounters *>(w + pl.off_flow_ctr);
-    F.window = lazy ? B : (B < kFlowWindow ? B : kFlowWindow);
     if (cudaMemsetAsync(F.fc, 0, sizeof(FlowCounters), stream) != cudaSuccess) return SV_ERR_CUDA;
     {
         const long long clear = F.cap - F.q1_base;

@@ -13,7 +13,7 @@ constexpr int kTileBytes = 16384;           // one bulk copy (a draw-pass or sel
 constexpr int kStatsTileBytes = 32768;      // one stage of the statistics pass (two 16 KB halves)
 constexpr int kStatsStages = 3;             // pipeline depth of the statistics pass
 constexpr int kStatsThreads = kThreads + 32;   // eight consumer warps and one producer warp
-constexpr int kUnitTiles = 4;               // aim for (row, chunk) units of about this many tiles
+constexpr int kUnitTiles = 16;              // aim for (row, chunk) units of about this many tiles
 constexpr int kDrawStages = 3;              // pipeline depth of the draw pass (two rows per stage)
 constexpr int kDrawUnitSubs = 64;           // draw-pass units: 64 sub-chunks (2 tiles) of a row pair
 constexpr int kSubBytes = 512;              // bytes of one row per draw sub-chunk (32 x 16 B)
@@ -22,7 +22,7 @@ constexpr int kUnitTarget = 1024;           // at least about this many (row, ch
 constexpr int kExactSplit = 16;             // chunks per row in the float-float tier
 constexpr int kExactCap = 2048;             // most queued items per call in the float-float tier
 constexpr int kExactGroup = 1;              // draw sub-chunks per warp unit in the float-float tier
-constexpr int kFlowGroupSubs = 32;          // dataflow kernel: sub-chunks per float-float row-pass unit
+constexpr int kFlowGroupSubs = 16;          // dataflow kernel: sub-chunks per float-float row-pass unit
 constexpr int kFlowSplitA = 4;              // dataflow kernel: float-float row-sum units per row
 constexpr int kFlowUncCap = 256;            // dataflow kernel: tokens of uncertain sign listed per item
 constexpr long long kWaitLimitCycles = 4000000000LL;   // ~2 s at 2 GHz: bounded barrier waits
@@ -168,13 +168,13 @@ struct FlowCounter {
     int pad[31];
 };
 struct FlowCounters {
-    FlowCounter q_head;      // next queue position to claim
+    FlowCounter q_head;      // next position of the init kernel's units to claim
+    FlowCounter q_head1;     // next position of the appended units to claim
     FlowCounter q0_tail;     // units written by the init kernel
     FlowCounter q_tail;      // units appended since
     FlowCounter n_pending;   // sequences whose last token is not written yet
     FlowCounter n_draws;     // draw items
     FlowCounter n_exact;     // float-float items
-    FlowCounter next_seq;    // eager mode: sequences queued after the first window
 };
 
 inline int div_up(long long a, long long b) { return (int)((a + b - 1) / b); }

@@ -1240,42 +1240,33 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
             int st = 0;
             uint32_t epar = 0;
             bool ok = true;
-            // Two queues.  The units appended during the pass (draws, float-float units, lazy
-            // mode's later rows) go first while some are visibly queued, so that a sequence's
-            // later work follows its rows closely; the units the init kernel wrote fill the
-            // rest.  An appended slot is claimed by compare-and-swap only while the tail is past
-            // the head (a few tries, then the other queue), so no producer waits on a slot that
-            // may never be filled; the slot's word may still be on its way from the appender, so
-            // its valid bit is awaited (briefly).
+            // Two queues, taken in order: the units the init kernel wrote (every sequence's
+            // first rows), then the units appended during the pass (draws, float-float units,
+            // lazy mode's later rows), so that the bandwidth-bound row statistics stream without
+            // interruption.  Claims are plain atomic increments, which scale to every producer at
+            // once.  A producer that drew an appended position past the tail keeps it as a
+            // reservation and takes the unit as soon as its word is written; every position below
+            // the head is reserved by exactly one producer, so no unit is left unclaimed.
             const int q0_n = *reinterpret_cast<volatile int *>(&F.fc->q0_tail.v);
             volatile int *q_tail_v = reinterpret_cast<volatile int *>(&F.fc->q_tail.v);
             volatile int *q_head1_v = reinterpret_cast<volatile int *>(&F.fc->q_head1.v);
             volatile int *q_head0_v = reinterpret_cast<volatile int *>(&F.fc->q_head.v);
-            // 1: a word claimed, 0: nothing queued now, -1: abort
+            long long resv = -1;   // a reserved appended position, not yet written
+            // 1: a word claimed, 0: nothing available now
             auto claim_word = [&](unsigned long long &wd) -> int {
-                int h1 = *q_head1_v;
-                for (int tries = 0; tries < 3 && h1 < *q_tail_v; ++tries) {
-                    const int prev = atomicCAS(&F.fc->q_head1.v, h1, h1 + 1);
-                    if (prev != h1) {
-                        h1 = prev;
-                        continue;
-                    }
-                    const long long sl = F.q1_base + h1;
-                    if (sl >= F.cap) return 0;
-                    const long long t0 = clock64();
-                    while (!((wd = ld_relaxed_u64(&F.units[sl])) >> 63)) {
-                        if (*reinterpret_cast<volatile int *>(abort_flag) || clock64() - t0 > a.wait_limit) {
-                            if (atomicExch(abort_flag, 1) == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);
-                            return -1;
-                        }
-                        __nanosleep(32);
-                    }
-                    return 1;
-                }
-                if (*q_head0_v < q0_n) {
+                if (resv < 0 && *q_head0_v < q0_n) {
                     const int c = atomicAdd(&F.fc->q_head.v, 1);
                     if (c < q0_n) {
                         wd = ld_relaxed_u64(&F.units[c]);
+                        return 1;
+                    }
+                }
+                if (resv < 0 && *q_head1_v < *q_tail_v) resv = F.q1_base + atomicAdd(&F.fc->q_head1.v, 1);
+                if (resv >= F.cap) resv = -1;   // cannot happen: the queue holds every unit of the call
+                if (resv >= 0) {
+                    wd = ld_relaxed_u64(&F.units[resv]);
+                    if (wd >> 63) {
+                        resv = -1;
                         return 1;
                     }
                 }
@@ -1306,8 +1297,7 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                 if (pf >> 63) return;
                 unsigned long long wd = 0;
                 const int got = claim_word(wd);
-                if (got < 0) ok = false;
-                else if (got > 0) pf = wd;
+                if (got > 0) pf = wd;
             };
             while (ok) {
                 long long unit = -1;
@@ -1323,12 +1313,7 @@ __global__ void __launch_bounds__(kFlowThreads, 2) k_flow(const FlowArgs F) {
                         pf = 0;
                         break;
                     }
-                    const int got = claim_word(word);
-                    if (got < 0) {
-                        ok = false;
-                        break;
-                    }
-                    if (got > 0) break;
+                    if (claim_word(word) > 0) break;
                     // nothing queued: has every sequence finished?  (read every few tries: every
                     // idle producer polls it; the sleeps grow so idle producers stay quiet)
                     if ((spins++ & 3) == 0 && ld_acquire(&F.fc->n_pending.v) == 0) break;

@@ -508,7 +508,7 @@ extern "C" sv_status sv_fuzzy_verify(const void *verifier_logits, int64_t v_row_
     if (mode == SV_ACCEPT_ASSISTED) {
         if (divergence != nullptr) return SV_ERR_INVALID_ARG;
         return verify_entry(verifier_logits, v_row_pitch, drafter_logits, d_row_pitch, d_rows_per_seq, dtype,
-                            draft_tokens, uniforms, B, K, V, temperature, nullptr, nullptr, 0, 1.0f, 1, 0, accept_len,
+                            draft_tokens, uniforms, B, K, V, temperature, nullptr, nullptr, 0, 1.0f, 1, accept_len,
                             out_tokens, nullptr, stats, workspace, workspace_bytes, stream);
     }
     if (mode != SV_ACCEPT_DIVERGENCE || !isfinite(tau)) return SV_ERR_INVALID_ARG;

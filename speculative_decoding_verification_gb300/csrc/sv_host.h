@@ -61,13 +61,8 @@ struct VerifyPlan {
     size_t off_nuc = 0, off_top = 0;
     size_t off_xpart = 0, off_xdraw = 0, off_xsubs = 0, off_xnorm = 0, off_xunc_n = 0, off_xunc = 0;
     int x_split = 1;                       // chunks per row in the float-float pass
-    size_t off_lz_units = 0, off_lz_pos = 0;   // work queue of the dataflow kernel (sv_flow.cu)
-    long long lz_cap = 0;                  // queue capacity: every unit of a call once
-    long long n_flow_initial = 0;          // queue slots for the units the init kernel writes
-    size_t off_draw_cnt = 0, off_xcnt = 0, off_acnt = 0, off_xuncw = 0, off_flow_ctr = 0;
-    int cap_x = 1;                         // most float-float items per call
-    int x_groups = 1;                      // float-float row-pass units per item
-    int max_slots = 2;                     // rows per sequence (2K + 1, at least 2)
+    size_t off_lz_units = 0, off_lz_pos = 0;   // lazy verification queue
+    long long lz_cap = 0;                  // queue capacity: every (row, chunk) unit once
     int dv_chunks = 1, dv_words = 1;       // fuzzy verification: chunks per row pair, words per chunk
     size_t off_dpart = 0, off_ditem = 0, off_dq = 0, off_deferred = 0;
     size_t bytes = 0;
@@ -75,19 +70,12 @@ struct VerifyPlan {
 
 VerifyPlan plan_verify(int B, int K, int V, int es);
 
-// The verification path of sv_verify and sv_verify_lazy; draw_from_q = 1 replaces the residual
-// draw after a rejection by a draw from the target row itself (the assisted acceptance of
-// three-model speculative decoding); lazy = 1 reads each sequence's rows only up to its first
-// rejection.  Calls without top-k, top-p or sigma_{F,C} run the dataflow kernel of sv_flow.cu,
-// the others the staged pipeline of sv_verify.cu.
+// The sv_verify pipeline; draw_from_q = 1 replaces the residual draw after a rejection by a draw
+// from the target row itself (the assisted acceptance of three-model speculative decoding).
 sv_status verify_entry(const void *target_logits, int64_t t_row_pitch, const void *draft_logits, int64_t d_row_pitch,
                        int d_rows_per_seq, sv_dtype dtype, const int32_t *draft_tokens, const double *uniforms, int B,
                        int K, int V, const float *temperature, const float *top_p, const int32_t *top_k, int saguaro_F,
-                       float saguaro_C, int draw_from_q, int lazy, int32_t *accept_len, int32_t *out_tokens,
-                       double *debug, sv_stats *stats, void *workspace, size_t workspace_bytes, cudaStream_t stream);
-
-struct AcceptArgs;
-// The dataflow kernel (sv_flow.cu) on a planned workspace.
-sv_status flow_verify(const VerifyPlan &pl, const AcceptArgs &acc, int B, int lazy, void *ws, cudaStream_t stream);
+                       float saguaro_C, int draw_from_q, int32_t *accept_len, int32_t *out_tokens, double *debug,
+                       sv_stats *stats, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 }  // namespace sv

@@ -147,7 +147,7 @@ extern "C" sv_status sv_verify_host(const void *target_logits, int64_t t_row_pit
         w + h.off_t, h.pitch, K > 0 ? w + h.off_d : nullptr, h.pitch, K > 0 ? K : 1, dtype,
         K > 0 ? reinterpret_cast<const int32_t *>(w + h.off_tok) : nullptr, reinterpret_cast<const double *>(w + h.off_u),
         B, K, V, reinterpret_cast<const float *>(w + h.off_T), top_p ? reinterpret_cast<const float *>(w + h.off_tp) : nullptr,
-        top_k ? reinterpret_cast<const int32_t *>(w + h.off_tk) : nullptr, saguaro_F, saguaro_C, 0, 0,
+        top_k ? reinterpret_cast<const int32_t *>(w + h.off_tk) : nullptr, saguaro_F, saguaro_C, 0,
         reinterpret_cast<int32_t *>(w + h.off_al), reinterpret_cast<int32_t *>(w + h.off_ot), nullptr, stats,
         w + h.off_ws, h.ws_bytes, stream);
     if (st != SV_OK) return st;

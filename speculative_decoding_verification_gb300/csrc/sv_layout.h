@@ -22,9 +22,6 @@ constexpr int kUnitTarget = 1024;           // at least about this many (row, ch
 constexpr int kExactSplit = 16;             // chunks per row in the float-float tier
 constexpr int kExactCap = 2048;             // most queued items per call in the float-float tier
 constexpr int kExactGroup = 1;              // draw sub-chunks per warp unit in the float-float tier
-constexpr int kFlowGroupSubs = 16;          // dataflow kernel: sub-chunks per float-float row-pass unit
-constexpr int kFlowSplitA = 4;              // dataflow kernel: float-float row-sum units per row
-constexpr int kFlowUncCap = 256;            // dataflow kernel: tokens of uncertain sign listed per item
 constexpr long long kWaitLimitCycles = 4000000000LL;   // ~2 s at 2 GHz: bounded barrier waits
 constexpr unsigned kSuspendHintNs = 100000;  // a waiting thread sleeps at most this long per try
 
@@ -158,23 +155,6 @@ struct Counters {
     int n_pending;          // lazy verification: sequences not finished yet
     int n_div_exact;        // fuzzy verification: divergences queued for the float-float pass
     int pad[6];
-};
-
-// Counters of the dataflow kernel, each on its own 128-byte line: producers of every block claim
-// units, finishers append units and count finished sequences, and a line shared by all of them
-// would serialise those atomics.  Zeroed by the host before each call.
-struct FlowCounter {
-    int v;
-    int pad[31];
-};
-struct FlowCounters {
-    FlowCounter q_head;      // next position of the init kernel's units to claim
-    FlowCounter q_head1;     // next position of the appended units to claim
-    FlowCounter q0_tail;     // units written by the init kernel
-    FlowCounter q_tail;      // units appended since
-    FlowCounter n_pending;   // sequences whose last token is not written yet
-    FlowCounter n_draws;     // draw items
-    FlowCounter n_exact;     // float-float items
 };
 
 inline int div_up(long long a, long long b) { return (int)((a + b - 1) / b); }

@@ -232,23 +232,9 @@ VerifyPlan plan_verify(int B, int K, int V, int es) {
     p.off_xnorm = cv.take<float4>(cap * p.x_split);
     p.off_xunc_n = cv.take<int>(cap);
     p.off_xunc = cv.take<int>(cap * kExactUncCap);
-    // the dataflow kernel's queue: every statistics unit of the call once (written by the init
-    // kernel in eager mode), room for lazy mode's later rows, every draw unit, every float-float
-    // unit; its per-item counters; the exact residuals of tokens of uncertain sign
-    p.cap_x = (int)cap;
-    p.max_slots = max_slots;
-    p.x_groups = div_up(p.n_sub, kFlowGroupSubs);
-    p.n_flow_initial = n_cand * p.n_split;
-    p.lz_cap = 2 * n_cand * p.n_split + (long long)B * p.d_split +
-               (long long)cap * (p.x_groups + (long long)max_slots * kFlowSplitA);
+    p.lz_cap = n_cand * p.n_split;
     p.off_lz_units = cv.take<unsigned long long>((size_t)p.lz_cap);
     p.off_lz_pos = cv.take<int>((size_t)B);
-    p.off_draw_cnt = cv.take<int>((size_t)B);
-    p.off_xcnt = cv.take<int>(cap);
-    p.off_acnt = cv.take<int>(cap);
-    p.off_xuncw = cv.take<float2>(cap * kFlowUncCap);
-    p.off_flow_ctr = cv.take<FlowCounters>(1);
-    static_assert(kFlowSplitA * kWarps <= kExactSplit * 3, "the float-float row sums fit the tier's partial buffer");
     const long long n_pairs = (long long)B * K;
     long long want = n_pairs > 0 ? (2LL * kUnitTarget + n_pairs - 1) / n_pairs : 1;
     if (want > kMaxSplit) want = kMaxSplit;
@@ -338,8 +324,7 @@ extern "C" size_t sv_verify_workspace_size(int B, int K, int V) {
 sv_status sv::verify_entry(const void *target_logits, int64_t t_row_pitch, const void *draft_logits,
                            int64_t d_row_pitch, int d_rows_per_seq, sv_dtype dtype, const int32_t *draft_tokens,
                            const double *uniforms, int B, int K, int V, const float *temperature, const float *top_p,
-                           const int32_t *top_k, int saguaro_F, float saguaro_C, int draw_from_q, int lazy,
-                           int32_t *accept_len,
+                           const int32_t *top_k, int saguaro_F, float saguaro_C, int draw_from_q, int32_t *accept_len,
                            int32_t *out_tokens, double *debug, sv_stats *stats, void *workspace,
                            size_t workspace_bytes, cudaStream_t stream) {
     if (B < 1 || K < 0 || K > SV_MAX_K || V < 1) return SV_ERR_INVALID_ARG;
@@ -372,10 +357,6 @@ sv_status sv::verify_entry(const void *target_logits, int64_t t_row_pitch, const
     acc.debug = debug;
     acc.stats = stats;
     acc.draw_from_q = draw_from_q;
-    if (top_p == nullptr && top_k == nullptr && !acc.sag_on) {
-        if (pl.lz_cap >= (1LL << 31)) return SV_ERR_INVALID_ARG;   // queue positions are 32-bit
-        return flow_verify(pl, acc, B, lazy, workspace, stream);
-    }
     if (es == 4) return launch_verify<4>(pl, acc, top_p, top_k, saguaro_F, saguaro_C, B, workspace, stream);
     return launch_verify<2>(pl, acc, top_p, top_k, saguaro_F, saguaro_C, B, workspace, stream);
 }
@@ -387,7 +368,7 @@ extern "C" sv_status sv_verify(const void *target_logits, int64_t t_row_pitch, c
                                int32_t *accept_len, int32_t *out_tokens, double *debug, sv_stats *stats,
                                void *workspace, size_t workspace_bytes, sv_stream_t stream) {
     return sv::verify_entry(target_logits, t_row_pitch, draft_logits, d_row_pitch, d_rows_per_seq, dtype, draft_tokens,
-                            uniforms, B, K, V, temperature, top_p, top_k, saguaro_F, saguaro_C, 0, 0, accept_len,
+                            uniforms, B, K, V, temperature, top_p, top_k, saguaro_F, saguaro_C, 0, accept_len,
                             out_tokens, debug, stats, workspace, workspace_bytes,
                             reinterpret_cast<cudaStream_t>(stream));
 }

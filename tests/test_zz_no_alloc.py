@@ -19,13 +19,14 @@ from synth import workloads as W
 from tests.helpers import gpu_args, make_inputs
 
 def test_oversize_call_is_refused_before_device_work():
-    """B=1024, K=5, V=128256 needs about 54 MiB of scratch: refused with SV_ERR_WORKSPACE, on any
-    machine, before the library touches a device (the pointers below are never dereferenced)."""
+    """B=4096, K=5, V=128256 bf16 needs more scratch than the library's fixed array holds: refused
+    with SV_ERR_WORKSPACE, on any machine, before the library touches a device (the pointers
+    below are never dereferenced)."""
     from speculative_decoding_verification_gb300 import build
     build.build()
     lib = sv.load()
     fake = 1 << 20
-    B, K, V = 1024, 5, 128256
+    B, K, V = 4096, 5, 128256
     assert lib.sv_verify_workspace_size(B, K, V) > _abi.SV_STATIC_SCRATCH_BYTES
     code = lib.sv_verify_static(fake, V, fake, V, K, _abi.SV_BF16, fake, fake, B, K, V, fake, None, None, 0, 1.0,
                                 fake, fake, None, None, None)

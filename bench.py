@@ -147,6 +147,20 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+CLOCK_LEAD_S = 0.8   # untimed load before the timed region, so that clock samples cover it
+CLOCK_TAIL_S = 0.3
+
+
+def keep_busy(step, seconds: float):
+    """Runs step() (untimed) in batches until `seconds` of wall time have passed."""
+    import torch
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+
+
 def _round_parts(w, r, parts, dev):
     """Round r of workload w as the oracle workers' shares of its sequences: raw bf16 rows,
     uniforms, temperatures (generated on `dev`, copied to the host outside any timing)."""
@@ -595,12 +609,15 @@ def run_ours(args, rank, world, local_rank):
     def step():
         sv.sv_verify(tgt, drf, toks_d, u_d, T_d, accept_len=al, out_tokens=ot, stats=stats, workspace=ws, lazy=lazy)
 
-    # clocks are sampled from before the warm-up (GPU under load) to the end of the timed region
+    # clocks are sampled over one loaded window around the timed region: nvidia-smi needs a few
+    # hundred ms to give its first sample, and K steps take milliseconds, so untimed steps of the
+    # same call keep the GPU busy before (after the warm-up) and after the timed region
     clocks = ClockSampler(local_rank)
     clocks.start()
     for _ in range(max(args.warmup, 0)):
         step()
     torch.cuda.synchronize()
+    keep_busy(step, CLOCK_LEAD_S)
     if sv.read_stats(stats)["status"] != 0:
         raise RuntimeError(f"verify failed: {sv.read_stats(stats)}")
 
@@ -631,7 +648,10 @@ def run_ours(args, rank, world, local_rank):
         return max_over_ranks(ms, world), k_ms, st
 
     ms_max, k1_ms, final = timed(step)
+    keep_busy(step, CLOCK_TAIL_S)
     clk = clocks.stop()
+    clk["window"] = (f"samples every 100 ms from the warm-up to {CLOCK_TAIL_S} s after the timed region; "
+                     f"untimed steps keep the GPU busy {CLOCK_LEAD_S} s before and {CLOCK_TAIL_S} s after it")
     value = whole_job_rate(1.0, world, ms_max)
 
     cfg = config_block(w)

@@ -195,8 +195,126 @@ __device__ __forceinline__ void load_vec(const char *row, int vi, float (&x)[16 
     unpack<ES>(w, x);
 }
 
+// Adds b to the float-float sum s without renormalising: TwoSum of the high parts, then the
+// rounding error and b's low part into s.lo (the cascaded summation of Ogita, Rump and Oishi,
+// "Accurate sum and dot product", 2005).  For n nonnegative terms the result is within about
+// n^2 u^2 of the sum, far below the tier's 2e-11 tolerance for the n <= 8 terms a lane adds
+// per sub-chunk.
+__device__ __forceinline__ void ff_acc(ff &s, ff b) {
+    const float t = __fadd_rn(s.hi, b.hi);
+    const float bb = __fsub_rn(t, s.hi);
+    const float e = __fadd_rn(__fsub_rn(s.hi, __fsub_rn(t, bb)), __fsub_rn(b.hi, bb));
+    s.lo = __fadd_rn(s.lo, __fadd_rn(e, b.lo));
+    s.hi = t;
+}
+
+// 2^(x c - r) in float-float for rows whose r satisfies |r| < 2^19, without branches: the same
+// steps as ff_exp2_xc, with results below 2^-140 (and -inf logits) selected to zero at the end.
+// For such rows every token with x c_hi - r >= -140 has |x c_hi| < 2^20, so ff_exp2_xc's
+// wide-argument path is never needed; arguments that select zero are replaced by 0 first, so
+// every intermediate stays finite.
+__device__ __forceinline__ ff ff_exp2_nf(float x, ff c, int r, float rf, const float2 *tab) {
+    const ff p0 = two_prod(x, c.hi);
+    const bool zero = !(__fsub_rn(p0.hi, rf) >= -140.0f);
+    const float xs = zero ? 0.f : x;
+    const float ph = zero ? 0.f : p0.hi, pl = zero ? 0.f : p0.lo;
+    const float yl = __fmaf_rn(xs, c.lo, pl);
+    const float kf = rintf(__fmul_rn(ph, 256.0f));
+    const int k = static_cast<int>(kf);
+    const float rh = __fsub_rn(ph, __fmul_rn(kf, 0.00390625f));   // exact
+    const float L_HI = 0.693147182464599609375f;
+    const float L_LO = -1.9046542999577520e-09f;
+    ff s = two_prod(rh, L_HI);
+    s.lo = __fmaf_rn(rh, L_LO, __fmaf_rn(yl, L_HI, s.lo));
+    s = fast_two_sum(s.hi, s.lo);
+    const ff s2 = two_prod(s.hi, s.hi);
+    const float half_s2 = __fmul_rn(0.5f, s2.hi);
+    const float cubic = __fmul_rn(__fmul_rn(s2.hi, s.hi), __fmaf_rn(s.hi, 1.0f / 24.0f, 1.0f / 6.0f));
+    const float small = __fadd_rn(__fmaf_rn(s.hi, s.lo, __fmul_rn(0.5f, s2.lo)), cubic);
+    ff t = fast_two_sum(s.hi, half_s2);
+    t.lo = __fadd_rn(t.lo, __fadd_rn(s.lo, small));
+    const int j = k & 255;
+    const int n = (k >> 8) - r;
+    const float2 T = tab[j];
+    const ff P = two_prod(T.x, t.hi);
+    ff e = fast_two_sum(T.x, P.hi);
+    const float tail = __fadd_rn(T.y, __fadd_rn(P.lo, __fmaf_rn(T.x, t.lo, __fmul_rn(T.y, t.hi))));
+    e = fast_two_sum(e.hi, __fadd_rn(e.lo, tail));
+    const float sc = zero ? 0.f : pow2i(n);
+    return {__fmul_rn(e.hi, sc), __fmul_rn(e.lo, sc)};
+}
+
+// Phase C of the float-float tier on vector sub-chunks [g0, g1) of item i when neither row has
+// a filter and both rows' r satisfy |r| < 2^19: the same sums as the general path (normaliser
+// partials per unit, sign-split A_q, A_p per sub-chunk, tokens of uncertain sign listed), with
+// the sub-chunk's tokens unrolled without branches and the next sub-chunk's logits loaded
+// ahead.
+template <int ES, bool HAS_P>
+__device__ __forceinline__ void exact_run_nf(const ExactArgs &a, const ExactDraw &d, int i, int g0, int g1, int lane,
+                                             const float2 *tab, float4 *xs) {
+    static_assert(kExactGroup == 1, "one sub-chunk per unit");
+    constexpr int EPV = 16 / ES;
+    const uint4 *qrow = reinterpret_cast<const uint4 *>(d.q.row);
+    const uint4 *prow = reinterpret_cast<const uint4 *>(d.p.row);
+    const int rq = (int)d.q.rf, rp = (int)d.p.rf;
+    auto load = [&](int sb, uint4 &wq, uint4 &wp) {
+        const int vi = sb * 32 + lane;
+        wq = wp = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);   // -inf: weight 0
+        if (ES == 4) wq = wp = make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+        if (sb < g1 && vi < a.n_vec) {
+            wq = __ldg(qrow + vi);
+            if (HAS_P) wp = __ldg(prow + vi);
+        }
+    };
+    uint4 nq_w, np_w;
+    load(g0, nq_w, np_w);
+    for (int sb = g0; sb < g1; ++sb) {
+        const uint4 wq = nq_w, wp = np_w;
+        load(sb + 1, nq_w, np_w);
+        const int vi = sb * 32 + lane;
+        ff nq = {0.f, 0.f}, np = {0.f, 0.f}, aq = {0.f, 0.f}, ap = {0.f, 0.f};
+        unsigned unc = 0;   // tokens of this lane whose sign the float32 test cannot settle
+        float xq[EPV], xp[EPV];
+        unpack<ES>(wq, xq);
+        if (HAS_P) unpack<ES>(wp, xp);
+#pragma unroll
+        for (int k = 0; k < EPV; ++k) {
+            const ff eq = ff_exp2_nf(xq[k], d.q.c, rq, d.q.rf, tab);
+            ff_acc(nq, eq);
+            if (HAS_P) {
+                const ff ep = ff_exp2_nf(xp[k], d.p.c, rp, d.p.rf, tab);
+                ff_acc(np, ep);
+                const float wq1 = eq.hi * d.inv_q, wp1 = ep.hi * d.inv_p;
+                const float diff = wq1 - wp1, tol = d.sign_tol * (wq1 + wp1);
+                const bool pos = diff > tol;
+                unc |= (!pos && diff >= -tol && wq1 > 0.f) ? (1u << k) : 0u;
+                ff_acc(aq, pos ? eq : ff{0.f, 0.f});
+                ff_acc(ap, pos ? ep : ff{0.f, 0.f});
+            } else {
+                ff_acc(aq, eq);
+            }
+        }
+        if (HAS_P && __any_sync(0xFFFFFFFFu, unc != 0)) {
+            for (int k = 0; k < EPV; ++k) {
+                if (unc & (1u << k)) {
+                    const int slot = atomicAdd(&a.xunc_n[i], 1);
+                    if (slot < kExactUncCap) a.xunc[(size_t)i * kExactUncCap + slot] = vi * EPV + k;
+                }
+            }
+        }
+        aq = warp_sum_ff(fast_two_sum(aq.hi, aq.lo));
+        ap = warp_sum_ff(fast_two_sum(ap.hi, ap.lo));
+        nq = warp_sum_ff(fast_two_sum(nq.hi, nq.lo));
+        np = warp_sum_ff(fast_two_sum(np.hi, np.lo));
+        if (lane == 0) {
+            xs[sb] = make_float4(aq.hi, aq.lo, ap.hi, ap.lo);
+            a.xnorm[(size_t)i * a.xsplit + sb] = make_float4(nq.hi, nq.lo, np.hi, np.lo);
+        }
+    }
+}
+
 template <int ES>
-__global__ void __launch_bounds__(kThreads, 4) k_exact(const ExactArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) k_exact(const ExactArgs a) {
     constexpr int EPV = 16 / ES;
     __shared__ float2 tab[256];
     __shared__ double s_red[3][kWarps];
@@ -361,63 +479,84 @@ __global__ void __launch_bounds__(kThreads, 4) k_exact(const ExactArgs a) {
     // ---- phase C: one float-float pass over the draw rows, one warp per unit ----------------
     // A unit is kExactGroup sub-chunks of one item (or its scalar tail): per sub-chunk the
     // sign-split sums (A_q, A_p), per unit the two normaliser partials.  No block barriers.
+    // Each warp takes a contiguous range of units, so that an item's parameters are read once
+    // per run of its units and the next sub-chunk's logits are in flight while one is summed.
     const int n_grp = a.xsplit;   // exact_groups(n_sub)
     const long long units_c = (long long)n_items * n_grp;
-    for (long long u = gwarp; u < units_c; u += nwarps) {
-        const int i = (int)(u / n_grp), g = (int)(u - (long long)i * n_grp);
+    const long long per_warp = (units_c + nwarps - 1) / nwarps;
+    const long long uc0 = min((long long)gwarp * per_warp, units_c), uc1 = min(uc0 + per_warp, units_c);
+    for (long long u = uc0; u < uc1;) {
+        const int i = (int)(u / n_grp);
+        const long long u_end = min(uc1, (long long)(i + 1) * n_grp);
+        int g = (int)(u - (long long)i * n_grp);
+        const int g_end = (int)(u_end - (long long)i * n_grp);
+        u = u_end;
         const ExactItem itm = a.items[i];
         const ExactDraw d = itm.draw >= 0 ? exact_draw_from(a.draws[itm.draw]) : a.xdraw[i];
         float4 *xs = a.xsubs + (size_t)i * a.n_sub;
-        ff nq = {0.f, 0.f}, np = {0.f, 0.f};
-        // one token: its contributions to the normalisers and, by the sign test, to (A_q, A_p)
-        auto token = [&](float xq, float xp, int v, ff &aq, ff &ap) {
-            const ff eq = exact_w(d.q, xq, v, tab);
-            nq = ff_add(nq, eq);
-            if (!d.has_p) {
-                aq = ff_add(aq, eq);
-                return;
+        if (kExactGroup == 1 && !d.q.filt && !(d.has_p && d.p.filt) && fabsf(d.q.rf) < 0x1p19f &&
+            (!d.has_p || fabsf(d.p.rf) < 0x1p19f)) {
+            // rows without filters: the vector sub-chunks on the unrolled path
+            const int gv_end = min(g_end, n_grp - 1);
+            if (g < gv_end) {
+                if (d.has_p) exact_run_nf<ES, true>(a, d, i, g, gv_end, lane, tab, xs);
+                else exact_run_nf<ES, false>(a, d, i, g, gv_end, lane, tab, xs);
+                g = gv_end;
             }
-            const ff ep = exact_w(d.p, xp, v, tab);
-            np = ff_add(np, ep);
-            const float wq = eq.hi * d.inv_q, wp = ep.hi * d.inv_p;
-            const float diff = wq - wp, tol = d.sign_tol * (wq + wp);
-            if (diff > tol) {
-                aq = ff_add(aq, eq);
-                ap = ff_add(ap, ep);
-            } else if (diff >= -tol && wq > 0.f) {
-                const int slot = atomicAdd(&a.xunc_n[i], 1);
-                if (slot < kExactUncCap) a.xunc[(size_t)i * kExactUncCap + slot] = v;
-            }
-        };
-        if (g < n_grp - 1) {
-            const int sb0 = g * kExactGroup, sb1 = min(sb0 + kExactGroup, n_vsub);
-            for (int sb = sb0; sb < sb1; ++sb) {
-                const int vi = sb * 32 + lane;
-                ff aq = {0.f, 0.f}, ap = {0.f, 0.f};
-                if (vi < n_vec) {
-                    const uint4 wq = __ldg(reinterpret_cast<const uint4 *>(d.q.row) + vi);
-                    const uint4 wp = d.has_p ? __ldg(reinterpret_cast<const uint4 *>(d.p.row) + vi) : wq;
+        }
+        for (; g < g_end; ++g) {
+            ff nq = {0.f, 0.f}, np = {0.f, 0.f};
+            // one token: its contributions to the normalisers and, by the sign test, to (A_q, A_p)
+            auto token = [&](float xq, float xp, int v, ff &aq, ff &ap) {
+                const ff eq = exact_w(d.q, xq, v, tab);
+                nq = ff_add(nq, eq);
+                if (!d.has_p) {
+                    aq = ff_add(aq, eq);
+                    return;
+                }
+                const ff ep = exact_w(d.p, xp, v, tab);
+                np = ff_add(np, ep);
+                const float wq = eq.hi * d.inv_q, wp = ep.hi * d.inv_p;
+                const float diff = wq - wp, tol = d.sign_tol * (wq + wp);
+                if (diff > tol) {
+                    aq = ff_add(aq, eq);
+                    ap = ff_add(ap, ep);
+                } else if (diff >= -tol && wq > 0.f) {
+                    const int slot = atomicAdd(&a.xunc_n[i], 1);
+                    if (slot < kExactUncCap) a.xunc[(size_t)i * kExactUncCap + slot] = v;
+                }
+            };
+            if (g < n_grp - 1) {
+                const int sb0 = g * kExactGroup, sb1 = min(sb0 + kExactGroup, n_vsub);
+                for (int sb = sb0; sb < sb1; ++sb) {
+                    const int vi = sb * 32 + lane;
+                    ff aq = {0.f, 0.f}, ap = {0.f, 0.f};
+                    if (vi < n_vec) {
+                        const uint4 wq = __ldg(reinterpret_cast<const uint4 *>(d.q.row) + vi);
+                        const uint4 wp = d.has_p ? __ldg(reinterpret_cast<const uint4 *>(d.p.row) + vi) : wq;
 #pragma unroll 1
-                    for (int k = 0; k < EPV; ++k) token(elem_of<ES>(wq, k), elem_of<ES>(wp, k), vi * EPV + k, aq, ap);
+                        for (int k = 0; k < EPV; ++k)
+                            token(elem_of<ES>(wq, k), elem_of<ES>(wp, k), vi * EPV + k, aq, ap);
+                    }
+                    aq = warp_sum_ff(aq);
+                    ap = warp_sum_ff(ap);
+                    if (lane == 0) xs[sb] = make_float4(aq.hi, aq.lo, ap.hi, ap.lo);
+                }
+            } else {
+                const int t = n_vec * EPV + lane;
+                ff aq = {0.f, 0.f}, ap = {0.f, 0.f};
+                if (t < a.V) {
+                    const float xq = load_elem<ES>(d.q.row, t);
+                    token(xq, d.has_p ? load_elem<ES>(d.p.row, t) : xq, t, aq, ap);
                 }
                 aq = warp_sum_ff(aq);
                 ap = warp_sum_ff(ap);
-                if (lane == 0) xs[sb] = make_float4(aq.hi, aq.lo, ap.hi, ap.lo);
+                if (lane == 0) xs[n_vsub] = make_float4(aq.hi, aq.lo, ap.hi, ap.lo);
             }
-        } else {
-            const int t = n_vec * EPV + lane;
-            ff aq = {0.f, 0.f}, ap = {0.f, 0.f};
-            if (t < a.V) {
-                const float xq = load_elem<ES>(d.q.row, t);
-                token(xq, d.has_p ? load_elem<ES>(d.p.row, t) : xq, t, aq, ap);
-            }
-            aq = warp_sum_ff(aq);
-            ap = warp_sum_ff(ap);
-            if (lane == 0) xs[n_vsub] = make_float4(aq.hi, aq.lo, ap.hi, ap.lo);
+            nq = warp_sum_ff(nq);
+            np = warp_sum_ff(np);
+            if (lane == 0) a.xnorm[(size_t)i * n_grp + g] = make_float4(nq.hi, nq.lo, np.hi, np.lo);
         }
-        nq = warp_sum_ff(nq);
-        np = warp_sum_ff(np);
-        if (lane == 0) a.xnorm[(size_t)i * n_grp + g] = make_float4(nq.hi, nq.lo, np.hi, np.lo);
     }
     if (!grid_barrier(&a.counters->barrier, bar_target, a.wait_limit)) {
         if (tid == 0 && blockIdx.x == 0) report_error(a.stats, SV_ERR_TIMEOUT, -1);

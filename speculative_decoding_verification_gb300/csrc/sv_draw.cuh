@@ -66,10 +66,43 @@ __device__ __forceinline__ float draw_weight(const DrawItem &it, float xq, float
 constexpr uint32_t kDrawFloor2 = 0xF149F149u;   // bf16 pair (-9.95e29, -9.95e29)
 constexpr float kDrawFloor = -9.95e29f;
 
-// Weights of one vector (EPV tokens from element e0); returns their tree sum.
+// Weights of one vector (EPV tokens from element e0); returns their tree sum.  bf16 rows
+// without filters take the packed path: two tokens per f32x2 instruction, each rounded exactly
+// as draw_weight rounds it (fma.rn.f32x2 is two IEEE fmas; x k_lo + inv_s and ep tp are formed
+// negated for p, which round-to-nearest mirrors exactly), so both passes see the same weights.
 template <int ES, bool HAS_P, bool FILT>
 __device__ __forceinline__ float vec_weights(const DrawItem &it, uint4 wq, uint4 wp, int e0, float (&wv)[16 / ES]) {
     constexpr int EPV = 16 / ES;
+    if constexpr (ES == 2 && !FILT) {
+        const f32x2 chq = f2_pack(it.q.c_hi, it.q.c_hi), nrq = f2_pack(-it.q.rf, -it.q.rf);
+        const f32x2 klq = f2_pack(it.q.k_lo, it.q.k_lo), isq = f2_pack(it.q.inv_s, it.q.inv_s);
+        const f32x2 chp = f2_pack(it.p.c_hi, it.p.c_hi), nrp = f2_pack(-it.p.rf, -it.p.rf);
+        const f32x2 nklp = f2_pack(-it.p.k_lo, -it.p.k_lo), nisp = f2_pack(-it.p.inv_s, -it.p.inv_s);
+        const f32x2 zero2 = f2_pack(0.f, 0.f);
+        const uint32_t qw[4] = {wq.x, wq.y, wq.z, wq.w};
+        const uint32_t pw[4] = {wp.x, wp.y, wp.z, wp.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const f32x2 xq = f2_from_bf16x2(bmax2(qw[h], kDrawFloor2));
+            const f32x2 eq = f2_ex2(f2_fma(xq, chq, nrq));
+            const f32x2 tq = f2_fma(xq, klq, isq);
+            float w0, w1;
+            if (HAS_P) {
+                const f32x2 xp = f2_from_bf16x2(bmax2(pw[h], kDrawFloor2));
+                const f32x2 ep = f2_ex2(f2_fma(xp, chp, nrp));
+                const f32x2 ntp = f2_fma(xp, nklp, nisp);   // -(x k_lo + inv_s)
+                const f32x2 npv = f2_fma(ep, ntp, zero2);   // -(ep tp)
+                f2_unpack(f2_fma(eq, tq, npv), w0, w1);
+                w0 = fmaxf(w0, 0.0f);
+                w1 = fmaxf(w1, 0.0f);
+            } else {
+                f2_unpack(f2_fma(eq, tq, zero2), w0, w1);
+            }
+            wv[2 * h] = w0;
+            wv[2 * h + 1] = w1;
+        }
+        return ((wv[0] + wv[1]) + (wv[2] + wv[3])) + ((wv[4] + wv[5]) + (wv[6] + wv[7]));
+    }
     float xq[EPV], xp[EPV];
     if constexpr (ES == 2) {
         unpack<ES>(make_uint4(bmax2(wq.x, kDrawFloor2), bmax2(wq.y, kDrawFloor2), bmax2(wq.z, kDrawFloor2),
@@ -131,13 +164,16 @@ struct DrawMeta {
     int fv, nv;       // first vector of the tile within the row, vectors in the tile
     int flags;        // kTileLast (last tile of the item's last chunk: also the scalar tail) | kTileEnd
 };
-constexpr int kDrawCtlBytes = 512;
-static_assert(2 * kDrawStages * 8 + 16 + kDrawStages * (int)sizeof(DrawMeta) <= kDrawCtlBytes, "control block");
+constexpr int kDrawItemOff = 256;   // per stage: a copy of its item, bulk-copied with the tiles
+constexpr int kDrawCtlBytes = 1024;
+static_assert(2 * kDrawStages * 8 + 16 + kDrawStages * (int)sizeof(DrawMeta) <= kDrawItemOff, "control block");
+static_assert(kDrawItemOff + kDrawStages * (int)sizeof(DrawItem) <= kDrawCtlBytes, "item copies");
 constexpr size_t kDrawSmemBytes = (size_t)kDrawCtlBytes + (size_t)2 * kDrawStages * kTileBytes;
 
 // Pass 1, warp-specialised like the statistics pass: the producer warp takes (item, chunk)
-// units from a global counter and streams each unit's q and p tiles into shared memory; eight
-// consumer warps weight the tokens and write one float32 sum per 32-vector sub-chunk.
+// units from a global counter and streams each unit's q and p tiles into shared memory, with a
+// copy of the item itself in the same stage; eight consumer warps weight the tokens and write
+// one float32 sum per 32-vector sub-chunk.
 template <int ES>
 __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a) {
     pdl_wait();
@@ -147,6 +183,7 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a
     uint64_t *empty = full + kDrawStages;
     int *abort_flag = reinterpret_cast<int *>(smem + 2 * kDrawStages * 8);
     DrawMeta *meta = reinterpret_cast<DrawMeta *>(smem + 2 * kDrawStages * 8 + 16);
+    DrawItem *stage_item = reinterpret_cast<DrawItem *>(smem + kDrawItemOff);
     unsigned char *tiles = smem + kDrawCtlBytes;   // stage s: q tile at 2s, p tile at 2s+1
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -174,9 +211,13 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a
             int st = 0;                 // it % kDrawStages
             uint32_t epar = 0;          // parity of the "empty" phase to wait for at stage st
             bool ok = true;
+            // the next unit is claimed as soon as the current one is known, so that the claim's
+            // round trip overlaps the current unit's copies
+            long long u_next = atomicAdd(&a.counters->next_draw_unit, 1);
             while (ok) {
-                const long long u = atomicAdd(&a.counters->next_draw_unit, 1);
+                const long long u = u_next;
                 const bool have = u < n_units;
+                if (have) u_next = atomicAdd(&a.counters->next_draw_unit, 1);
                 int d = 0, c = 0, v0 = 0, v1 = 0;
                 const DrawItem *item = nullptr;
                 if (have) {
@@ -212,19 +253,19 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a
                     m.nv = nv;
                     m.flags = (t == nt - 1 && c == a.n_split - 1) ? kTileLast : 0;
                     meta[st] = m;
+                    const uint32_t bytes = (uint32_t)nv * 16u;
+                    const bool has_p = item->has_p != 0;
+                    const uint32_t tile_bytes = nv > 0 ? (has_p ? 2u * bytes : bytes) : 0u;
+                    mbar_arrive_expect_tx(&full[st], tile_bytes + (uint32_t)sizeof(DrawItem));
+                    bulk_load(stage_item + st, item, (uint32_t)sizeof(DrawItem), &full[st]);
                     if (nv > 0) {
-                        const uint32_t bytes = (uint32_t)nv * 16u;
-                        const bool has_p = item->has_p != 0;
-                        mbar_arrive_expect_tx(&full[st], has_p ? 2u * bytes : bytes);
                         bulk_load_stream(tiles + (2 * st) * kTileBytes, item->q.row + (size_t)fv * 16, bytes, &full[st],
                                          policy);
                         if (has_p)
                             bulk_load_stream(tiles + (2 * st + 1) * kTileBytes, item->p.row + (size_t)fv * 16, bytes,
                                              &full[st], policy);
-                        in_flight[st] = it;
-                    } else {
-                        mbar_arrive(&full[st]);
                     }
+                    in_flight[st] = it;
                     if (++st == kDrawStages) {
                         st = 0;
                         if (it >= 2 * kDrawStages - 1) epar ^= 1u;   // round r >= 2 waits phase r - 1
@@ -241,8 +282,6 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a
     }
 
     // ---------------- consumers ----------------
-    int cur = -1;
-    DrawItem item;
     int st = 0;
     uint32_t par = 0;
     for (;;) {
@@ -252,10 +291,7 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a
         }
         const DrawMeta m = meta[st];
         if (m.flags & kTileEnd) break;
-        if (m.d != cur) {
-            item = a.items[m.d];
-            cur = m.d;
-        }
+        const DrawItem item = stage_item[st];   // read before the stage is released below
         float *subs_item = a.subs + (size_t)m.d * a.n_sub;
         const unsigned char *bq = tiles + (2 * st) * kTileBytes;
         const unsigned char *bp = bq + kTileBytes;
@@ -266,8 +302,6 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a
             if (item.filt) draw_tile<ES, false, true>(item, bq, bp, m.fv, m.nv, subs_item);
             else draw_tile<ES, false, false>(item, bq, bp, m.fv, m.nv, subs_item);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
         // the scalar tail of the row forms the last sub-chunk
         if ((m.flags & kTileLast) && warp == 0) {
             constexpr int EPV = 16 / ES;
@@ -276,6 +310,8 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a
             const float W = warp_sum_f(w);
             if (lane == 0) subs_item[n_vsub] = W;
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
         if (++st == kDrawStages) {
             st = 0;
             par ^= 1u;

@@ -245,10 +245,10 @@ __device__ __forceinline__ ff ff_exp2_nf(float x, ff c, int r, float rf, const f
 }
 
 // Phase C of the float-float tier on vector sub-chunks [g0, g1) of item i when neither row has
-// a filter and both rows' r satisfy |r| < 2^19: the same sums as the general path (normaliser
-// partials per unit, sign-split A_q, A_p per sub-chunk, tokens of uncertain sign listed), with
-// the sub-chunk's tokens unrolled without branches and the next sub-chunk's logits loaded
-// ahead.
+// a filter and both rows' r satisfy |r| < 2^19: the same sums as the general path (sign-split
+// A_q, A_p per sub-chunk, tokens of uncertain sign listed; the normaliser partial of the whole
+// run in unit g0's slot and zero in the others, which phase D adds up all the same), with the
+// sub-chunk's tokens unrolled without branches and the next sub-chunk's logits loaded ahead.
 template <int ES, bool HAS_P>
 __device__ __forceinline__ void exact_run_nf(const ExactArgs &a, const ExactDraw &d, int i, int g0, int g1, int lane,
                                              const float2 *tab, float4 *xs) {
@@ -268,30 +268,46 @@ __device__ __forceinline__ void exact_run_nf(const ExactArgs &a, const ExactDraw
     };
     uint4 nq_w, np_w;
     load(g0, nq_w, np_w);
+    // the normaliser partials of the whole run, reduced across the warp once at its end
+    ff nq_run = {0.f, 0.f}, np_run = {0.f, 0.f};
     for (int sb = g0; sb < g1; ++sb) {
         const uint4 wq = nq_w, wp = np_w;
         load(sb + 1, nq_w, np_w);
         const int vi = sb * 32 + lane;
         ff nq = {0.f, 0.f}, np = {0.f, 0.f}, aq = {0.f, 0.f}, ap = {0.f, 0.f};
         unsigned unc = 0;   // tokens of this lane whose sign the float32 test cannot settle
-        float xq[EPV], xp[EPV];
-        unpack<ES>(wq, xq);
-        if (HAS_P) unpack<ES>(wp, xp);
-#pragma unroll
-        for (int k = 0; k < EPV; ++k) {
-            const ff eq = ff_exp2_nf(xq[k], d.q.c, rq, d.q.rf, tab);
-            ff_acc(nq, eq);
-            if (HAS_P) {
-                const ff ep = ff_exp2_nf(xp[k], d.p.c, rp, d.p.rf, tab);
-                ff_acc(np, ep);
-                const float wq1 = eq.hi * d.inv_q, wp1 = ep.hi * d.inv_p;
-                const float diff = wq1 - wp1, tol = d.sign_tol * (wq1 + wp1);
-                const bool pos = diff > tol;
-                unc |= (!pos && diff >= -tol && wq1 > 0.f) ? (1u << k) : 0u;
-                ff_acc(aq, pos ? eq : ff{0.f, 0.f});
-                ff_acc(ap, pos ? ep : ff{0.f, 0.f});
+        // four tokens at a time (a loop of two for bf16), which keeps the unrolled code small
+        // enough for the instruction cache
+#pragma unroll 1
+        for (int h = 0; h < EPV / 4; ++h) {
+            float xq[4], xp[4];
+            if constexpr (ES == 2) {
+                const uint32_t q0 = h ? wq.z : wq.x, q1 = h ? wq.w : wq.y;
+                const uint32_t p0 = h ? wp.z : wp.x, p1 = h ? wp.w : wp.y;
+                xq[0] = bf16_lo(q0); xq[1] = bf16_hi(q0); xq[2] = bf16_lo(q1); xq[3] = bf16_hi(q1);
+                xp[0] = bf16_lo(p0); xp[1] = bf16_hi(p0); xp[2] = bf16_lo(p1); xp[3] = bf16_hi(p1);
             } else {
-                ff_acc(aq, eq);
+                xq[0] = __uint_as_float(wq.x); xq[1] = __uint_as_float(wq.y);
+                xq[2] = __uint_as_float(wq.z); xq[3] = __uint_as_float(wq.w);
+                xp[0] = __uint_as_float(wp.x); xp[1] = __uint_as_float(wp.y);
+                xp[2] = __uint_as_float(wp.z); xp[3] = __uint_as_float(wp.w);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const ff eq = ff_exp2_nf(xq[k], d.q.c, rq, d.q.rf, tab);
+                ff_acc(nq, eq);
+                if (HAS_P) {
+                    const ff ep = ff_exp2_nf(xp[k], d.p.c, rp, d.p.rf, tab);
+                    ff_acc(np, ep);
+                    const float wq1 = eq.hi * d.inv_q, wp1 = ep.hi * d.inv_p;
+                    const float diff = wq1 - wp1, tol = d.sign_tol * (wq1 + wp1);
+                    const bool pos = diff > tol;
+                    unc |= (!pos && diff >= -tol && wq1 > 0.f) ? (1u << (4 * h + k)) : 0u;
+                    ff_acc(aq, pos ? eq : ff{0.f, 0.f});
+                    ff_acc(ap, pos ? ep : ff{0.f, 0.f});
+                } else {
+                    ff_acc(aq, eq);
+                }
             }
         }
         if (HAS_P && __any_sync(0xFFFFFFFFu, unc != 0)) {
@@ -302,15 +318,18 @@ __device__ __forceinline__ void exact_run_nf(const ExactArgs &a, const ExactDraw
                 }
             }
         }
+        nq_run = ff_add(nq_run, fast_two_sum(nq.hi, nq.lo));
+        np_run = ff_add(np_run, fast_two_sum(np.hi, np.lo));
         aq = warp_sum_ff(fast_two_sum(aq.hi, aq.lo));
         ap = warp_sum_ff(fast_two_sum(ap.hi, ap.lo));
-        nq = warp_sum_ff(fast_two_sum(nq.hi, nq.lo));
-        np = warp_sum_ff(fast_two_sum(np.hi, np.lo));
         if (lane == 0) {
             xs[sb] = make_float4(aq.hi, aq.lo, ap.hi, ap.lo);
-            a.xnorm[(size_t)i * a.xsplit + sb] = make_float4(nq.hi, nq.lo, np.hi, np.lo);
+            if (sb > g0) a.xnorm[(size_t)i * a.xsplit + sb] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
+    nq_run = warp_sum_ff(nq_run);
+    np_run = warp_sum_ff(np_run);
+    if (lane == 0) a.xnorm[(size_t)i * a.xsplit + g0] = make_float4(nq_run.hi, nq_run.lo, np_run.hi, np_run.lo);
 }
 
 template <int ES>
@@ -483,8 +502,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_exact(const ExactArgs a) {
     // per run of its units and the next sub-chunk's logits are in flight while one is summed.
     const int n_grp = a.xsplit;   // exact_groups(n_sub)
     const long long units_c = (long long)n_items * n_grp;
-    const long long per_warp = (units_c + nwarps - 1) / nwarps;
-    const long long uc0 = min((long long)gwarp * per_warp, units_c), uc1 = min(uc0 + per_warp, units_c);
+    // balanced ranges: every warp gets floor or ceil of units_c / nwarps
+    const long long uc0 = units_c * gwarp / nwarps, uc1 = units_c * (gwarp + 1) / nwarps;
     for (long long u = uc0; u < uc1;) {
         const int i = (int)(u / n_grp);
         const long long u_end = min(uc1, (long long)(i + 1) * n_grp);

@@ -119,7 +119,9 @@ struct DrawItem {
     int filt;               // nucleus cut or top-F set in use
     int seq;
     int k;                  // draw position (accepted count for sv_verify)
+    int pad[2];             // a multiple of 16 bytes: the draw pass bulk-copies items
 };
+static_assert(sizeof(DrawItem) % 16 == 0, "draw items are copied with cp.async.bulk");
 
 // Fuzzy verification: per (pair, chunk) partial of the divergence pass, and per pair its
 // float32 divergence, error bound and (when the bound could not settle it) float-float value.

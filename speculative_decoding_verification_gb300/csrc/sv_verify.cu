@@ -49,6 +49,21 @@ __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
         return;
     }
     const int n_t = K + 1, n_d = greedy ? 0 : K;
+    // warp 0 loads its lane's draft token, uniform and the two logits at that token now, so
+    // that those loads overlap the row combination below
+    int s = -1;
+    float xt = 0.f, xd = 0.f;
+    double u_acc = 0.0;
+    if (warp == 0 && lane < K) {
+        s = a.tokens[(size_t)b * K + lane];
+        if (!greedy && s >= 0 && s < V) {
+            const char *trow = a.tgt.base + ((long long)b * a.tgt.rows_per_seq + lane) * a.tgt.pitch_bytes;
+            const char *drow = a.drf.base + ((long long)b * a.drf.rows_per_seq + lane) * a.drf.pitch_bytes;
+            xt = load_elem<ES>(trow, s);
+            xd = load_elem<ES>(drow, s);
+            u_acc = a.uniforms[(size_t)b * (K + 1) + lane];
+        }
+    }
     for (int i = warp; i < n_t + n_d; i += kWarps) {
         const long long rid = i < n_t ? (long long)b * n_t + i : a.n_rows0 + (long long)b * K + (i - n_t);
         const RowStat r = combine_row(a.part + (size_t)rid * a.n_split * kWarps, a.n_split * kWarps, greedy, T);
@@ -79,19 +94,16 @@ __global__ void __launch_bounds__(kThreads) k_accept(const AcceptArgs a) {
     // and the normaliser z_err; u < ratio is certain outside ratio (1 -+ delta).
     float c_hi = 0.f, c_lo = 0.f;
     if (!greedy) log2e_over(T, c_hi, c_lo);
-    int s = -1;
     bool acc = false, amb = false, near = false, badtok = false;
     bool keep_q = false, keep_p = false, in_top = false;
     float ratio = NAN;
     if (lane < K) {
-        s = a.tokens[(size_t)b * K + lane];
         badtok = s < 0 || s >= V;
         if (!badtok) {
             if (greedy) {
                 acc = (s == rs[lane].argmax);
             } else {
-                const AcceptOutcome o = accept_test<ES>(a, b, lane, s, a.uniforms[(size_t)b * (K + 1) + lane], c_hi,
-                                                        c_lo, rs[lane], rs[n_t + lane]);
+                const AcceptOutcome o = accept_test_x(a, b, lane, s, u_acc, c_hi, c_lo, rs[lane], rs[n_t + lane], xt, xd);
                 acc = o.acc;
                 amb = o.amb;
                 near = o.near;

@@ -319,6 +319,40 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_draw_sums(const DrawArgs a
     }
 }
 
+// Block-wide scan of one float-float value per thread (kThreads threads, all of them calling):
+// inclusive and exclusive prefix sums in thread order and the block total.  Warp scans by
+// shuffles, then one warp scans the warp totals: three barriers.  s_w holds kWarps entries.
+__device__ __forceinline__ void block_scan_ff(ff v, ff &incl, ff &excl, ff &total, float2 *s_w) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    ff inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float h = __shfl_up_sync(0xFFFFFFFFu, inc.hi, o);
+        const float l = __shfl_up_sync(0xFFFFFFFFu, inc.lo, o);
+        if (lane >= o) inc = ff_add(inc, {h, l});
+    }
+    if (lane == 31) s_w[warp] = make_float2(inc.hi, inc.lo);
+    __syncthreads();
+    if (warp == 0) {
+        ff t = lane < kWarps ? ff{s_w[lane].x, s_w[lane].y} : ff{0.f, 0.f};
+#pragma unroll
+        for (int o = 1; o < kWarps; o <<= 1) {
+            const float h = __shfl_up_sync(0xFFFFFFFFu, t.hi, o);
+            const float l = __shfl_up_sync(0xFFFFFFFFu, t.lo, o);
+            if (lane >= o) t = ff_add(t, {h, l});
+        }
+        __syncwarp();
+        if (lane < kWarps) s_w[lane] = make_float2(t.hi, t.lo);   // inclusive warp prefixes
+    }
+    __syncthreads();
+    const ff base = warp > 0 ? ff{s_w[warp - 1].x, s_w[warp - 1].y} : ff{0.f, 0.f};
+    const float ph = __shfl_up_sync(0xFFFFFFFFu, inc.hi, 1), pl = __shfl_up_sync(0xFFFFFFFFu, inc.lo, 1);
+    incl = ff_add(base, inc);
+    excl = lane > 0 ? ff_add(base, {ph, pl}) : base;
+    total = {s_w[kWarps - 1].x, s_w[kWarps - 1].y};
+    __syncthreads();   // s_w may be reused by the caller
+}
+
 // Bound on |(u R~ - C~(v)) - (u R - C(v))| for any v, where ~ marks the computed prefix sums.
 // With per-token errors d_v = |w~_v - w_v| the difference is (1-u) sum_{i<=v} d_i and
 // u sum_{i>v} d_i of opposite signs at worst, so it is at most max(u, 1-u) sum_v d_v.  Each
@@ -356,7 +390,7 @@ template <int ES>
 __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
     pdl_wait();
     constexpr int EPV = 16 / ES;
-    __shared__ float2 s_scan[kThreads];
+    __shared__ float2 s_w[kWarps];
     __shared__ int s_sub;
     __shared__ float2 s_pre;
     __shared__ int s_last_sub;
@@ -380,27 +414,15 @@ __global__ void __launch_bounds__(kThreads) k_draw_finish(const DrawArgs a) {
         wsum = ff_add_f(wsum, v);
         if (v > 0.f) last_pos = s;
     }
-    // 2. block inclusive scan of wsum in float-float
-    s_scan[tid] = make_float2(wsum.hi, wsum.lo);
+    // 2. block scan of wsum in float-float
     if (tid == 0) {
         s_sub = -1;
         s_last_sub = -1;
         const float u_hi = __double2float_rn(it.u);
         s_u = make_float2(u_hi, __double2float_rn(it.u - (double)u_hi));
     }
-    __syncthreads();
-    for (int off = 1; off < kThreads; off <<= 1) {
-        const float2 v = tid >= off ? s_scan[tid - off] : make_float2(0.f, 0.f);
-        __syncthreads();
-        const float2 m = s_scan[tid];
-        const ff t = ff_add({m.x, m.y}, {v.x, v.y});
-        s_scan[tid] = make_float2(t.hi, t.lo);
-        __syncthreads();
-    }
-    const float2 in2 = s_scan[tid];
-    const float2 ex2v = tid > 0 ? s_scan[tid - 1] : make_float2(0.f, 0.f);
-    const float2 r2 = s_scan[kThreads - 1];
-    const ff incl = {in2.x, in2.y}, excl = {ex2v.x, ex2v.y}, R = {r2.x, r2.y};
+    ff incl, excl, R;
+    block_scan_ff(wsum, incl, excl, R, s_w);
     atomicMax(&s_last_sub, last_pos);
     __syncthreads();
     // sum_v (q_v |y_q,v| + p_v |y_p,v|) over the normalised rows, from the statistics pass

@@ -337,20 +337,15 @@ __global__ void __launch_bounds__(kThreads, 3) k_exact(const ExactArgs a) {
     constexpr int EPV = 16 / ES;
     __shared__ float2 tab[256];
     __shared__ double s_red[3][kWarps];
-    __shared__ int s_flag;
     const int n_items = min(*reinterpret_cast<volatile int *>(&a.counters->n_exact), kExactCap);
     if (n_items == 0) return;   // uniform across the grid
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     {
         tab[tid] = kExp2Table[tid];
     }
-    if (tid == 0) {
-        int acc = 0;
-        for (int i = 0; i < n_items; ++i) acc |= a.items[i].draw < 0;
-        s_flag = acc;
-    }
-    __syncthreads();
-    const bool any_accept = s_flag != 0;
+    int acc_here = 0;
+    for (int i = tid; i < n_items; i += kThreads) acc_here |= a.items[i].draw < 0;
+    const bool any_accept = __syncthreads_or(acc_here) != 0;
     unsigned bar_target = 0;
     const int n_vsub = a.n_sub - 1;
     const int n_vec = a.n_vec;
@@ -586,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_exact(const ExactArgs a) {
     // Float-float throughout (the float64 pipe of this GPU would set the latency of the block).
     __shared__ float2 s_unc_w[kExactUncCap];
     __shared__ int s_unc_sub[kExactUncCap];
-    __shared__ float2 s_scan[kThreads];
+    __shared__ float2 s_scan[kWarps];
     __shared__ float4 s_norm[kWarps];
     __shared__ int s_sub;
     __shared__ float2 s_pre;
@@ -595,6 +590,12 @@ __global__ void __launch_bounds__(kThreads, 3) k_exact(const ExactArgs a) {
         const ExactItem itm = a.items[i];
         const ExactDraw d = itm.draw >= 0 ? exact_draw_from(a.draws[itm.draw]) : a.xdraw[i];
         const float4 *xs = a.xsubs + (size_t)i * a.n_sub;
+        // this thread's contiguous range of sub-chunks; its first two masses are loaded now so
+        // that the loads overlap the normaliser reduction
+        const int per = (a.n_sub + kThreads - 1) / kThreads;
+        const int s0 = min(tid * per, a.n_sub), s1 = min(s0 + per, a.n_sub);
+        const float4 xs0 = s0 < s1 ? xs[s0] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 xs1 = s0 + 1 < s1 ? xs[s0 + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
         // normalisers
         ff sq = {0.f, 0.f}, sp = {0.f, 0.f};
         for (int k = tid; k < n_grp; k += kThreads) {
@@ -631,15 +632,13 @@ __global__ void __launch_bounds__(kThreads, 3) k_exact(const ExactArgs a) {
         }
         __syncthreads();
         auto W = [&](int s) {
-            const float4 v = xs[s];
+            const float4 v = s == s0 ? xs0 : s == s0 + 1 ? xs1 : xs[s];
             ff w = ff_sub(ff_mul({v.x, v.y}, iq), ff_mul({v.z, v.w}, ip));
             for (int k = 0; k < n_unc; ++k)
                 if (s_unc_sub[k] == s) w = ff_add(w, {s_unc_w[k].x, s_unc_w[k].y});
             return w;
         };
-        // per-thread contiguous ranges of sub-chunks, block scan of their sums
-        const int per = (a.n_sub + kThreads - 1) / kThreads;
-        const int s0 = min(tid * per, a.n_sub), s1 = min(s0 + per, a.n_sub);
+        // block scan of the per-thread range sums
         ff mine = {0.f, 0.f};
         int last_pos = -1;
         for (int s = s0; s < s1; ++s) {
@@ -647,21 +646,9 @@ __global__ void __launch_bounds__(kThreads, 3) k_exact(const ExactArgs a) {
             mine = ff_add(mine, w);
             if (w.hi > 0.f) last_pos = s;
         }
-        s_scan[tid] = make_float2(mine.hi, mine.lo);
         atomicMax(&s_last, last_pos);
-        __syncthreads();
-        for (int off = 1; off < kThreads; off <<= 1) {
-            const float2 v = tid >= off ? s_scan[tid - off] : make_float2(0.f, 0.f);
-            __syncthreads();
-            const float2 m = s_scan[tid];
-            const ff t = ff_add({m.x, m.y}, {v.x, v.y});
-            s_scan[tid] = make_float2(t.hi, t.lo);
-            __syncthreads();
-        }
-        const float2 in2 = s_scan[tid];
-        const float2 ex2v = tid > 0 ? s_scan[tid - 1] : make_float2(0.f, 0.f);
-        const float2 r2 = s_scan[kThreads - 1];
-        const ff incl = {in2.x, in2.y}, excl = {ex2v.x, ex2v.y}, R = {r2.x, r2.y};
+        ff incl, excl, R;
+        block_scan_ff(mine, incl, excl, R, s_scan);
         const float u_hi = __double2float_rn(d.u);
         const float u_lo = __double2float_rn(d.u - (double)u_hi);
         const ff thr = ff_mul(R, {u_hi, u_lo});

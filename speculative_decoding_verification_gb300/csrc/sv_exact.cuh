@@ -335,6 +335,7 @@ __device__ __forceinline__ void exact_run_nf(const ExactArgs &a, const ExactDraw
 template <int ES>
 __global__ void __launch_bounds__(kThreads, 3) k_exact(const ExactArgs a) {
     constexpr int EPV = 16 / ES;
+    pdl_trigger();   // the stream's next kernel may be scheduled; it waits for this one to finish
     __shared__ float2 tab[256];
     __shared__ double s_red[3][kWarps];
     const int n_items = min(*reinterpret_cast<volatile int *>(&a.counters->n_exact), kExactCap);

@@ -29,6 +29,7 @@ struct StatsArgs {
     WarpPartial *part;          // [candidate row][chunk][warp]
     Counters *counters;         // zeroed by the host before the pass (work counter; later kernels)
     sv_stats *stats;
+    bool zero_stats = false;    // the counter reset also clears *stats (the call's first launch)
     long long wait_limit;
 };
 
@@ -370,6 +371,7 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_stats(const StatsArgs a) {
     unsigned char *tiles = smem + kStatsCtlBytes;
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
+    pdl_wait();      // the counters are zeroed by the kernel before this one
     pdl_trigger();   // the next kernel may be scheduled now; it waits for this one's results
 
     if (tid == 0) {
@@ -494,17 +496,34 @@ __global__ void __launch_bounds__(kStatsThreads, 2) k_stats(const StatsArgs a) {
 }
 
 // Host side: clear the call's counters, then run the statistics pass on a persistent grid.
+// Zeroes a call's counters (and, when given, its sv_stats block) once the stream's previous
+// kernel has finished with them.
+static __global__ void k_zero_counters(Counters *c, sv_stats *st) {
+    pdl_wait();
+    pdl_trigger();
+    int *w = reinterpret_cast<int *>(c);
+    for (int i = threadIdx.x; i < (int)(sizeof(Counters) / sizeof(int)); i += blockDim.x) w[i] = 0;
+    if (st != nullptr) {
+        int *v = reinterpret_cast<int *>(st);
+        for (int i = threadIdx.x; i < (int)(sizeof(sv_stats) / sizeof(int)); i += blockDim.x) v[i] = 0;
+    }
+}
+
 template <int ES>
 static sv_status launch_stats(const StatsArgs &sa, const DeviceInfo &di, cudaStream_t stream) {
-    if (cudaMemsetAsync(sa.counters, 0, sizeof(Counters), stream) != cudaSuccess) return SV_ERR_CUDA;
+    // the counters are zeroed by a kernel rather than a memset, so that the launches of the
+    // whole call (and of the next call) form one chain of programmatic dependent launches
+    if (launch_pdl(k_zero_counters, dim3(1), dim3(64), 0, stream, sa.counters, sa.zero_stats ? sa.stats : nullptr) !=
+        cudaSuccess)
+        return SV_ERR_CUDA;
     const int occ = prepare_kernel((const void *)k_stats<ES>, kStatsThreads, kStatsSmemBytes);
     if (occ < 1) return SV_ERR_CUDA;
     long long grid = (long long)di.sms * occ;
     if (grid > sa.n_units) grid = sa.n_units;
     if (grid < 1) grid = 1;
     profile_begin(stream);
-    k_stats<ES><<<(unsigned)grid, kStatsThreads, kStatsSmemBytes, stream>>>(sa);
-    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    if (launch_pdl(k_stats<ES>, dim3((unsigned)grid), dim3(kStatsThreads), kStatsSmemBytes, stream, sa) != cudaSuccess)
+        return SV_ERR_CUDA;
     profile_end(stream);
     return SV_OK;
 }

@@ -286,6 +286,7 @@ static sv_status launch_verify(const VerifyPlan &pl, const AcceptArgs &acc_in, c
     sa.part = part;
     sa.counters = counters;
     sa.stats = acc.stats;
+    sa.zero_stats = true;
     sa.wait_limit = wait;
     {
         const sv_status st = launch_stats<ES>(sa, di, stream);
@@ -350,7 +351,7 @@ sv_status sv::verify_entry(const void *target_logits, int64_t t_row_pitch, const
     const VerifyPlan pl = plan_verify(B, K, V, es);
     if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < pl.bytes) return SV_ERR_WORKSPACE;
     if (!on_current_device(stream, target_logits, K > 0 ? draft_logits : nullptr)) return SV_ERR_INVALID_ARG;
-    if (stats && cudaMemsetAsync(stats, 0, sizeof(sv_stats), stream) != cudaSuccess) return SV_ERR_CUDA;
+    // stats is cleared by the call's first kernel (launch_stats)
 
     AcceptArgs acc{};
     acc.tgt = {static_cast<const char *>(target_logits), t_row_pitch * es, K + 1, K + 1, 0};

@@ -77,7 +77,7 @@ typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 
 /*
  * Device-written status and counters.  Each call that takes a stats pointer overwrites the
- * block (it is cleared on the call's stream before the first kernel).  status holds the first
+ * block (it is cleared on the call's stream before any kernel of the call writes to it).  status holds the first
  * device-detected error and error_index the row (or sequence) it concerns, -1 if none.
  *
  * Decisions (accept tests and draws) are first taken in float32 with a proven error bound.
@@ -251,7 +251,7 @@ sv_status sv_verify_lazy(const void *target_logits, int64_t t_row_pitch,
  *
  *  - Limit: a call whose scratch need for (B, K, V, dtype) exceeds SV_STATIC_SCRATCH_BYTES
  *    returns SV_ERR_WORKSPACE before any device work (B = 512, K = 5, V = 128256 needs about
- *    28.7 MiB and fits).  sv_verify_workspace_size(B, K, V) bounds the need from above.
+ *    23.9 MiB and fits).  sv_verify_workspace_size(B, K, V) bounds the need from above.
  *  - Set-up: the first call on a device, with that device current, looks up the array's
  *    device address (cudaGetSymbolAddress) and caches it for that device; a failure there
  *    returns SV_ERR_CUDA.  Make that first call before any stream capture.  The cached
@@ -259,10 +259,10 @@ sv_status sv_verify_lazy(const void *target_logits, int64_t t_row_pitch,
  *    the primary context is released and created again, it is stale, so a process that
  *    resets a device must not call sv_verify_static on it afterwards.
  *  - Contents: every call shares the array, and it keeps the last call's contents.  Nothing
- *    in it has to start at zero: each call clears its counters (queued draws, queued
- *    float-float items, grid-barrier count, next unit of the statistics pass) with one
- *    memset on its stream before its first kernel, and every other byte is written before it
- *    is read within the same call.
+ *    in it has to start at zero: each call's first kernel clears its counters (queued draws,
+ *    queued float-float items, grid-barrier count, next unit of the statistics pass) on its
+ *    stream once the stream's previous kernel has finished, and every other byte is written
+ *    before it is read within the same call.
  *  - Races: calls whose kernels overlap on the GPU (other streams, other host threads on the
  *    same device) use the same scratch and race.  Order them, e.g. on one stream.
  * -------------------------------------------------------------------------------------- */

@@ -20,8 +20,9 @@
 //   k_div            per (row pair, chunk): float32 partial sums of s h(d), and of the error weight
 //   k_fuzzy_accept   per sequence: divergences with a certified error bound, the first position
 //                    above tau; positions too close to tau are queued for...
-//   k_div_exact      ...a float-float evaluation of their divergence (one block per pair), after
-//                    which k_fuzzy_accept runs again for the deferred sequences
+//   k_div_exact_sums, k_div_exact_terms  ...a float-float evaluation of their divergence, each pair
+//                    split into chunks over the grid, after which k_fuzzy_accept runs again for
+//                    the deferred sequences
 //   k_draw_sums, k_draw_finish, k_exact   the draw from the verifier's row at the first failure
 // The assisted mode is the sv_verify pipeline with the residual draw replaced by a draw from q.
 #include <math.h>
@@ -35,6 +36,8 @@
 #include "sv_tiers.cuh"
 
 namespace sv {
+
+constexpr int kDivExactChunks = 128;   // most chunks per pair in the float-float divergence pass
 
 struct FuzzyArgs {
     RowSet ver, drf;
@@ -54,6 +57,10 @@ struct FuzzyArgs {
     int dv_chunks, dv_words, n_vec;
     DivItem *ditem;
     int *dq;
+    float4 *dxa;               // [entry]: a chunk's float-float row sums (S_q, S_p)
+    float2 *dxb;               // [entry]: a chunk's float-float divergence sum
+    int *dxcnt;                // [queue slot]: chunks done, zeroed when the pair is queued
+    int dx_cap;
     int *deferred;
     Counters *counters;
     DrawItem *draws;
@@ -212,95 +219,188 @@ __device__ __forceinline__ ff ff_log2(ff x, const float2 *tab) {
     return ff_add({y0, 0.f}, ff_mul(ln, inv_ln2));
 }
 
-// The divergence of one queued pair in float-float (one block per pair).
+// The divergences of the queued pairs in float-float.  Each pair is split into ch chunks of
+// its row pair (ch from the number queued, so that their (pair, chunk) entries fit the
+// workspace), and two persistent passes run over all (pair, chunk) units: the first sums the
+// chunk's q and p masses, the second takes the pair's exact row sums from those partials, sums
+// its chunk's divergence terms, and the last chunk of a pair to finish adds the pair's
+// partials and records the divergence.
+__device__ __forceinline__ int div_exact_chunks(int n, int cap) {
+    const int ch = n > 0 ? cap / n : 1;
+    return ch < 1 ? 1 : (ch > kDivExactChunks ? kDivExactChunks : ch);
+}
+
+struct DivExactUnit {
+    long long pair;
+    int slot, chunk, v0, v1;   // tokens [v0, v1) of the pair's rows
+};
+
+__device__ __forceinline__ DivExactUnit div_exact_unit(const FuzzyArgs &a, long long u, int ch) {
+    DivExactUnit x;
+    x.slot = (int)(u / ch);
+    x.chunk = (int)(u - (long long)x.slot * ch);
+    x.pair = a.dq[x.slot];
+    const int per = (a.V + ch - 1) / ch;
+    x.v0 = min(x.chunk * per, a.V);
+    x.v1 = min(x.v0 + per, a.V);
+    return x;
+}
+
+// Block sum of two float-float values (every thread of the block calls; s_h.. hold kWarps).
+__device__ __forceinline__ void block_ff2(ff u, ff v, ff &U, ff &W, float *s_h, float *s_l, float *s_h2,
+                                          float *s_l2) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        u = ff_add(u, {__shfl_xor_sync(0xFFFFFFFFu, u.hi, o), __shfl_xor_sync(0xFFFFFFFFu, u.lo, o)});
+        v = ff_add(v, {__shfl_xor_sync(0xFFFFFFFFu, v.hi, o), __shfl_xor_sync(0xFFFFFFFFu, v.lo, o)});
+    }
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        s_h[w] = u.hi;
+        s_l[w] = u.lo;
+        s_h2[w] = v.hi;
+        s_l2[w] = v.lo;
+    }
+    __syncthreads();
+    U = {0.f, 0.f};
+    W = {0.f, 0.f};
+    for (int i = 0; i < kWarps; ++i) {
+        U = ff_add(U, {s_h[i], s_l[i]});
+        W = ff_add(W, {s_h2[i], s_l2[i]});
+    }
+    __syncthreads();
+}
+
+// Pass 1: per (pair, chunk), the float-float sums of 2^(x c - r) over the chunk's tokens of
+// the verifier row (q) and the drafter row (p).
 template <int ES>
-__global__ void __launch_bounds__(kThreads) k_div_exact(const FuzzyArgs a) {
+__global__ void __launch_bounds__(kThreads) k_div_exact_sums(const FuzzyArgs a) {
+    __shared__ float2 tab[256];
+    __shared__ float s_h[kWarps], s_l[kWarps], s_h2[kWarps], s_l2[kWarps];
+    const int n = *reinterpret_cast<volatile int *>(&a.counters->n_div_exact);
+    if (n == 0) return;   // uniform across the grid
+    const int ch = div_exact_chunks(n, a.dx_cap);
+    tab[threadIdx.x] = kExp2Table[threadIdx.x];
+    __syncthreads();
+    for (long long u = blockIdx.x; u < (long long)n * ch; u += gridDim.x) {
+        const DivExactUnit x = div_exact_unit(a, u, ch);
+        const long long b = x.pair / a.K;
+        const int j = (int)(x.pair - b * a.K);
+        const float T = a.temperature[b];
+        const RowStat rq = a.rowstat[b * (a.K + 1) + j], rp = a.rowstat[a.n_rows0 + b * a.K + j];
+        float c_hi, c_lo;
+        log2e_over(T, c_hi, c_lo);
+        const ff c = {c_hi, c_lo};
+        const char *qrow = a.ver.base + (b * a.ver.rows_per_seq + j) * a.ver.pitch_bytes;
+        const char *prow = a.drf.base + (b * a.drf.rows_per_seq + j) * a.drf.pitch_bytes;
+        auto mass = [&](float xv, int r) -> ff { return xv == -INFINITY ? ff{0.f, 0.f} : ff_exp2_xc(xv, c, r, tab); };
+        ff sq = {0.f, 0.f}, sp = {0.f, 0.f};
+        for (int v = x.v0 + threadIdx.x; v < x.v1; v += kThreads) {
+            sq = ff_add(sq, mass(load_elem<ES>(qrow, v), rq.r));
+            sp = ff_add(sp, mass(load_elem<ES>(prow, v), rp.r));
+        }
+        ff Sq, Sp;
+        block_ff2(sq, sp, Sq, Sp, s_h, s_l, s_h2, s_l2);
+        if (threadIdx.x == 0) a.dxa[(size_t)x.slot * ch + x.chunk] = make_float4(Sq.hi, Sq.lo, Sp.hi, Sp.lo);
+    }
+}
+
+// Pass 2: per (pair, chunk), the float-float divergence terms of the chunk's tokens with the
+// pair's exact row sums; the last chunk of a pair adds the partials and records the divergence.
+template <int ES>
+__global__ void __launch_bounds__(kThreads) k_div_exact_terms(const FuzzyArgs a) {
     __shared__ float2 tab[256];
     __shared__ ff s_c[12];
     __shared__ float s_h[kWarps], s_l[kWarps], s_h2[kWarps], s_l2[kWarps];
     __shared__ ff s_inv[2];
-    const int n = a.counters->n_div_exact;
-    if ((int)blockIdx.x >= n) return;
-    const long long pair = a.dq[blockIdx.x];
-    const long long b = pair / a.K;
-    const int j = (int)(pair - b * a.K);
-    const float T = a.temperature[b];
+    __shared__ int s_last;
+    const int n = *reinterpret_cast<volatile int *>(&a.counters->n_div_exact);
+    if (n == 0) return;   // uniform across the grid
+    const int ch = div_exact_chunks(n, a.dx_cap);
     tab[threadIdx.x] = kExp2Table[threadIdx.x];
     if (threadIdx.x < 12) {
         const float k = (float)(threadIdx.x + 1);
         s_c[threadIdx.x] = ff_recip({k * (2.0f * k - 1.0f), 0.f});   // 1 / (k (2k - 1))
     }
-    const RowStat rq = a.rowstat[b * (a.K + 1) + j], rp = a.rowstat[a.n_rows0 + b * a.K + j];
-    float c_hi, c_lo;
-    log2e_over(T, c_hi, c_lo);
-    const ff c = {c_hi, c_lo};
-    const char *qrow = a.ver.base + (b * a.ver.rows_per_seq + j) * a.ver.pitch_bytes;
-    const char *prow = a.drf.base + (b * a.drf.rows_per_seq + j) * a.drf.pitch_bytes;
     __syncthreads();
-    auto mass = [&](float x, int r) -> ff { return x == -INFINITY ? ff{0.f, 0.f} : ff_exp2_xc(x, c, r, tab); };
-    auto block_ff2 = [&](ff u, ff v, ff &U, ff &W) {
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            u = ff_add(u, {__shfl_xor_sync(0xFFFFFFFFu, u.hi, o), __shfl_xor_sync(0xFFFFFFFFu, u.lo, o)});
-            v = ff_add(v, {__shfl_xor_sync(0xFFFFFFFFu, v.hi, o), __shfl_xor_sync(0xFFFFFFFFu, v.lo, o)});
-        }
-        const int w = threadIdx.x >> 5;
-        if ((threadIdx.x & 31) == 0) {
-            s_h[w] = u.hi;
-            s_l[w] = u.lo;
-            s_h2[w] = v.hi;
-            s_l2[w] = v.lo;
-        }
-        __syncthreads();
-        U = {0.f, 0.f};
-        W = {0.f, 0.f};
-        for (int i = 0; i < kWarps; ++i) {
-            U = ff_add(U, {s_h[i], s_l[i]});
-            W = ff_add(W, {s_h2[i], s_l2[i]});
-        }
-        __syncthreads();
-    };
-    // exact row sums
-    ff sq = {0.f, 0.f}, sp = {0.f, 0.f};
-    for (int v = threadIdx.x; v < a.V; v += kThreads) {
-        sq = ff_add(sq, mass(load_elem<ES>(qrow, v), rq.r));
-        sp = ff_add(sp, mass(load_elem<ES>(prow, v), rp.r));
-    }
-    ff Sq, Sp;
-    block_ff2(sq, sp, Sq, Sp);
-    const ff iq = ff_recip(Sq), ip = ff_recip(Sp);
     const ff inv_ln2 = {1.44269502162933349609375f, 1.925963033500011e-08f};
-    ff acc = {0.f, 0.f};
-    for (int v = threadIdx.x; v < a.V; v += kThreads) {
-        const ff q = ff_mul(mass(load_elem<ES>(qrow, v), rq.r), iq);
-        const ff p = ff_mul(mass(load_elem<ES>(prow, v), rp.r), ip);
-        const ff s = ff_add(q, p);
-        if (!(s.hi > 0.f)) continue;
-        const ff rs = ff_recip(s);
-        const ff d = ff_mul(ff_sub(q, p), rs);
-        ff h;
-        if (fabsf(d.hi) < 0.25f) {
-            const ff d2 = ff_mul(d, d);
-            ff poly = s_c[11];
-            for (int k = 10; k >= 0; --k) poly = ff_add(s_c[k], ff_mul(d2, poly));
-            h = ff_mul(ff_mul(d2, poly), inv_ln2);
-        } else {
-            const ff qa = ff_mul(ff_add(q, q), rs), pb = ff_mul(ff_add(p, p), rs);
-            h = {0.f, 0.f};
-            if (qa.hi > 0x1p-100f) h = ff_add(h, ff_mul(qa, ff_log2(qa, tab)));
-            else if (qa.hi > 0.f) h = ff_add_f(h, qa.hi * log2f(qa.hi));
-            if (pb.hi > 0x1p-100f) h = ff_add(h, ff_mul(pb, ff_log2(pb, tab)));
-            else if (pb.hi > 0.f) h = ff_add_f(h, pb.hi * log2f(pb.hi));
+    for (long long u = blockIdx.x; u < (long long)n * ch; u += gridDim.x) {
+        const DivExactUnit x = div_exact_unit(a, u, ch);
+        const long long b = x.pair / a.K;
+        const int j = (int)(x.pair - b * a.K);
+        const float T = a.temperature[b];
+        const RowStat rq = a.rowstat[b * (a.K + 1) + j], rp = a.rowstat[a.n_rows0 + b * a.K + j];
+        float c_hi, c_lo;
+        log2e_over(T, c_hi, c_lo);
+        const ff c = {c_hi, c_lo};
+        const char *qrow = a.ver.base + (b * a.ver.rows_per_seq + j) * a.ver.pitch_bytes;
+        const char *prow = a.drf.base + (b * a.drf.rows_per_seq + j) * a.drf.pitch_bytes;
+        auto mass = [&](float xv, int r) -> ff { return xv == -INFINITY ? ff{0.f, 0.f} : ff_exp2_xc(xv, c, r, tab); };
+        // the pair's exact row sums from the chunks' partials (one warp)
+        if (threadIdx.x < 32) {
+            ff sq = {0.f, 0.f}, sp = {0.f, 0.f};
+            for (int k = threadIdx.x; k < ch; k += 32) {
+                const float4 pv = a.dxa[(size_t)x.slot * ch + k];
+                sq = ff_add(sq, {pv.x, pv.y});
+                sp = ff_add(sp, {pv.z, pv.w});
+            }
+            sq = warp_sum_ff(sq);
+            sp = warp_sum_ff(sp);
+            if (threadIdx.x == 0) {
+                s_inv[0] = ff_recip(sq);
+                s_inv[1] = ff_recip(sp);
+            }
         }
-        acc = ff_add(acc, ff_mul(s, h));
-    }
-    ff F, unused;
-    block_ff2(acc, {0.f, 0.f}, F, unused);
-    if (threadIdx.x == 0) {
-        const double dv = 0.25 * ff_to_double(F);
-        a.ditem[pair].exact = dv;
-        a.ditem[pair].state = 2;
-        if (fabs(dv - (double)a.tau) < 1e-10) stats_add(a.stats, &a.stats->unresolved, 1);
+        __syncthreads();
+        const ff iq = s_inv[0], ip = s_inv[1];
+        ff acc = {0.f, 0.f};
+        for (int v = x.v0 + threadIdx.x; v < x.v1; v += kThreads) {
+            const ff q = ff_mul(mass(load_elem<ES>(qrow, v), rq.r), iq);
+            const ff p = ff_mul(mass(load_elem<ES>(prow, v), rp.r), ip);
+            const ff s = ff_add(q, p);
+            if (!(s.hi > 0.f)) continue;
+            const ff rs = ff_recip(s);
+            const ff d = ff_mul(ff_sub(q, p), rs);
+            ff h;
+            if (fabsf(d.hi) < 0.25f) {
+                const ff d2 = ff_mul(d, d);
+                ff poly = s_c[11];
+                for (int k = 10; k >= 0; --k) poly = ff_add(s_c[k], ff_mul(d2, poly));
+                h = ff_mul(ff_mul(d2, poly), inv_ln2);
+            } else {
+                const ff qa = ff_mul(ff_add(q, q), rs), pb = ff_mul(ff_add(p, p), rs);
+                h = {0.f, 0.f};
+                if (qa.hi > 0x1p-100f) h = ff_add(h, ff_mul(qa, ff_log2(qa, tab)));
+                else if (qa.hi > 0.f) h = ff_add_f(h, qa.hi * log2f(qa.hi));
+                if (pb.hi > 0x1p-100f) h = ff_add(h, ff_mul(pb, ff_log2(pb, tab)));
+                else if (pb.hi > 0.f) h = ff_add_f(h, pb.hi * log2f(pb.hi));
+            }
+            acc = ff_add(acc, ff_mul(s, h));
+        }
+        ff F, unused;
+        block_ff2(acc, {0.f, 0.f}, F, unused, s_h, s_l, s_h2, s_l2);
+        if (threadIdx.x == 0) {
+            a.dxb[(size_t)x.slot * ch + x.chunk] = make_float2(F.hi, F.lo);
+            __threadfence();
+            s_last = atomicAdd(&a.dxcnt[x.slot], 1) == ch - 1;
+        }
+        __syncthreads();
+        if (s_last && threadIdx.x < 32) {
+            __threadfence();
+            ff t = {0.f, 0.f};
+            for (int k = threadIdx.x; k < ch; k += 32) {
+                const float2 pv = __ldcg(&a.dxb[(size_t)x.slot * ch + k]);   // written by other blocks: L2
+                t = ff_add(t, {pv.x, pv.y});
+            }
+            t = warp_sum_ff(t);
+            if (threadIdx.x == 0) {
+                const double dv = 0.25 * ff_to_double(t);
+                a.ditem[x.pair].exact = dv;
+                a.ditem[x.pair].state = 2;
+                if (fabs(dv - (double)a.tau) < 1e-10) stats_add(a.stats, &a.stats->unresolved, 1);
+            }
+        }
+        __syncthreads();   // s_inv and s_last are rewritten by the next unit
     }
 }
 
@@ -392,6 +492,7 @@ __global__ void __launch_bounds__(32) k_fuzzy_accept(const FuzzyArgs a, int pass
             const long long pair = (long long)b * K + lane;
             a.ditem[pair].state = 1;
             const int slot = atomicAdd(&a.counters->n_div_exact, 1);
+            a.dxcnt[slot] = 0;
             a.dq[slot] = (int)pair;
         }
         if (lane == 0) {
@@ -464,6 +565,10 @@ static sv_status launch_fuzzy(const VerifyPlan &pl, FuzzyArgs fa, AcceptArgs acc
     fa.n_vec = pl.n_vec;
     fa.ditem = reinterpret_cast<DivItem *>(w + pl.off_ditem);
     fa.dq = reinterpret_cast<int *>(w + pl.off_dq);
+    fa.dxa = reinterpret_cast<float4 *>(w + pl.off_dxa);
+    fa.dxb = reinterpret_cast<float2 *>(w + pl.off_dxb);
+    fa.dxcnt = reinterpret_cast<int *>(w + pl.off_dxcnt);
+    fa.dx_cap = pl.dx_cap;
     fa.deferred = reinterpret_cast<int *>(w + pl.off_deferred);
     fa.counters = counters;
     fa.draws = reinterpret_cast<DrawItem *>(w + pl.off_draws);
@@ -475,7 +580,10 @@ static sv_status launch_fuzzy(const VerifyPlan &pl, FuzzyArgs fa, AcceptArgs acc
     if (n_pairs > 0) k_div<ES><<<(unsigned)(n_pairs * fa.dv_chunks), kThreads, 0, stream>>>(fa);
     k_fuzzy_accept<ES><<<fa.B, 32, 0, stream>>>(fa, 0);
     if (n_pairs > 0) {
-        k_div_exact<ES><<<(unsigned)n_pairs, kThreads, 0, stream>>>(fa);
+        // persistent passes over the queued pairs' chunks (the queue length is on the device)
+        const unsigned gx = (unsigned)(di.sms * 4);
+        k_div_exact_sums<ES><<<gx, kThreads, 0, stream>>>(fa);
+        k_div_exact_terms<ES><<<gx, kThreads, 0, stream>>>(fa);
         k_fuzzy_accept<ES><<<fa.B, 32, 0, stream>>>(fa, 1);
     }
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;

@@ -65,6 +65,8 @@ struct VerifyPlan {
     long long lz_cap = 0;                  // queue capacity: every (row, chunk) unit once
     int dv_chunks = 1, dv_words = 1;       // fuzzy verification: chunks per row pair, words per chunk
     size_t off_dpart = 0, off_ditem = 0, off_dq = 0, off_deferred = 0;
+    size_t off_dxa = 0, off_dxb = 0, off_dxcnt = 0;   // float-float divergences: per (queued pair, chunk)
+    int dx_cap = 1;                        // (pair, chunk) entries of off_dxa / off_dxb
     size_t bytes = 0;
 };
 

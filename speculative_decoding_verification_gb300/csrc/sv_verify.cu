@@ -257,6 +257,13 @@ VerifyPlan plan_verify(int B, int K, int V, int es) {
     p.off_ditem = cv.take<DivItem>((size_t)(n_pairs > 0 ? n_pairs : 1));
     p.off_dq = cv.take<int>((size_t)(n_pairs > 0 ? n_pairs : 1));
     p.off_deferred = cv.take<int>((size_t)B);
+    // the float-float divergence pass splits each queued pair over up to kDivExactChunks chunks;
+    // the entries are shared by the queued pairs, so fewer chunks each when many are queued
+    const long long np1 = n_pairs > 0 ? n_pairs : 1;
+    p.dx_cap = (int)(4 * np1 > 4096 ? 4 * np1 : 4096);
+    p.off_dxa = cv.take<float4>((size_t)p.dx_cap);
+    p.off_dxb = cv.take<float2>((size_t)p.dx_cap);
+    p.off_dxcnt = cv.take<int>((size_t)np1);
     p.bytes = cv.off + 256;
     return p;
 }

@@ -688,7 +688,9 @@ def run_ours(args, rank, world, local_rank):
                          "peak_source": f"{peak_kind} copy bandwidth", "kernel_ms": k1_ms,
                          "timing": "CUDA events around the kernel on its stream, in a second pass of the K steps",
                          "ms_per_step_with_events": ms_instr},
-            "gpu_launches": 5 * n, "clocks": clk,
+            # per call: k_zero_counters, k_stats, k_accept, k_draw_sums, k_draw_finish, k_exact (eager);
+            # k_lazy_init, k_lazy, k_draw_sums, k_draw_finish, k_exact (lazy)
+            "gpu_launches": (5 if lazy else 6) * n, "clocks": clk,
             "decisions": {k: final[k] for k in ("accept_tests", "draws", "reresolved", "near_boundary",
                                                 "unresolved")}}
     # the other verification path on the same inputs (same outputs; see config.path)

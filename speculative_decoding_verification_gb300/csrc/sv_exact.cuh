@@ -244,14 +244,95 @@ __device__ __forceinline__ ff ff_exp2_nf(float x, ff c, int r, float rf, const f
     return {__fmul_rn(e.hi, sc), __fmul_rn(e.lo, sc)};
 }
 
+// Factored weights for bf16 rows.  A bf16 logit is x = s 2^(E-127) (1 + (8 m_h + m_l)/128),
+// m_h its top three and m_l its low four mantissa bits, so 2^(x c - r) = 2^(v1 c - r) 2^(v2 c)
+// exactly, with v1 = s 2^(E-127) (1 + m_h/8) and v2 = s 2^(E-127) m_l/128 both floats.  A
+// table of the first factor per row over (s, E, m_h) and one of the second per temperature
+// over (s, E, m_l), each entry a float-float exponential, turn a token's weight into two
+// shared-memory loads and a float-float product: the relative error stays a few times 2^-44,
+// like the direct exponential's.  Exponents outside the tables, entries whose factor could
+// leave [2^-100, 2^64] (first) or [2^-32, 2^32] (second, so that a product neither overflows
+// nor leaves the normal range), and -inf or zero logits take the direct exponential.
+constexpr int kTabE0 = 118;                   // |x| in [2^-9, 2^7)
+constexpr int kTabNE = 16;
+constexpr int kTabGroups = 2 * kTabNE;        // (s, E)
+constexpr int kTab1 = kTabGroups * 8;         // first-factor entries
+constexpr int kTab2 = kTabGroups * 16;        // second-factor entries
+constexpr int kTabSlots = 2;                  // items whose tables one block holds
+static_assert(kTab1 == kThreads, "one first-factor entry per thread");
+
+__device__ __forceinline__ float tab_scale(int g) {   // s 2^(E-127) of group g
+    const float p = __int_as_float((kTabE0 + (g & (kTabNE - 1))) << 23);
+    return g >= kTabNE ? -p : p;
+}
+
+__device__ __forceinline__ float2 tab_first(float v, const ExactRow &r, const float2 *tab) {
+    const float y = __fmaf_rn(v, r.c.hi, -r.rf);
+    if (!(y >= -100.0f && y <= 64.0f)) return make_float2(__int_as_float(0x7FC00000), 0.f);
+    const ff e = ff_exp2_nf(v, r.c, (int)r.rf, r.rf, tab);
+    return make_float2(e.hi, e.lo);
+}
+
+__device__ __forceinline__ float2 tab_second(float v, ff c, const float2 *tab) {
+    if (!(fabsf(__fmul_rn(v, c.hi)) <= 32.0f)) return make_float2(__int_as_float(0x7FC00000), 0.f);
+    const ff e = ff_exp2_nf(v, c, 0, 0.f, tab);
+    return make_float2(e.hi, e.lo);
+}
+
+// Rows without filters whose r satisfies |r| < 2^19: the unrolled row pass applies.
+__device__ __forceinline__ bool nf_rows(const ExactDraw &d) {
+    return !d.q.filt && !(d.has_p && d.p.filt) && fabsf(d.q.rf) < 0x1p19f && (!d.has_p || fabsf(d.p.rf) < 0x1p19f);
+}
+
+__device__ __forceinline__ bool same_c(const ExactDraw &d) {
+    return !d.has_p || (d.q.c.hi == d.p.c.hi && d.q.c.lo == d.p.c.lo);
+}
+
+// Tables of one item, by the whole block: t1q / t1p per row, t2q for q's temperature (and
+// t2p for p's when it differs).
+__device__ __forceinline__ void build_tables(const ExactDraw &d, float2 *t1q, float2 *t1p, float2 *t2q, float2 *t2p,
+                                             const float2 *tab, int tid) {
+    const float v1 = tab_scale(tid >> 3) * (1.0f + 0.125f * (float)(tid & 7));
+    t1q[tid] = tab_first(v1, d.q, tab);
+    if (d.has_p) t1p[tid] = tab_first(v1, d.p, tab);
+    const bool same = same_c(d);
+    for (int j = tid; j < kTab2; j += kThreads) {
+        const float v2 = tab_scale(j >> 4) * (0.0078125f * (float)(j & 15));
+        t2q[j] = tab_second(v2, d.q.c, tab);
+        if (!same) t2p[j] = tab_second(v2, d.p.c, tab);
+    }
+}
+
+// Weight of the bf16 logit with bit pattern b (16 bits) from the tables; ok is false where
+// the tables cannot give it.
+__device__ __forceinline__ ff tab_w(uint32_t b, const float2 *t1, const float2 *t2, bool &ok) {
+    const int e = (int)((b >> 7) & 0xFFu) - kTabE0;
+    const bool inr = (unsigned)e < (unsigned)kTabNE;
+    const int g = (inr ? e : 0) + (int)(b >> 15) * kTabNE;
+    const float2 f1 = t1[g * 8 + (int)((b >> 4) & 7u)];
+    const float2 f2 = t2[g * 16 + (int)(b & 15u)];
+    const float h = __fmul_rn(f1.x, f2.x);
+    const float l = __fmaf_rn(f1.x, f2.y, __fmaf_rn(f1.y, f2.x, __fmaf_rn(f1.x, f2.x, -h)));
+    ok = inr && h >= 0.f;
+    return {h, l};
+}
+
+// The direct exponential for the few tokens the tables leave out, kept out of line so that
+// the unrolled token loop stays small.
+static __device__ __noinline__ ff exp2_direct(float x, ff c, int r, float rf, const float2 *tab) {
+    return ff_exp2_nf(x, c, r, rf, tab);
+}
+
 // Phase C of the float-float tier on vector sub-chunks [g0, g1) of item i when neither row has
 // a filter and both rows' r satisfy |r| < 2^19: the same sums as the general path (sign-split
 // A_q, A_p per sub-chunk, tokens of uncertain sign listed; the normaliser partial of the whole
 // run in unit g0's slot and zero in the others, which phase D adds up all the same), with the
 // sub-chunk's tokens unrolled without branches and the next sub-chunk's logits loaded ahead.
-template <int ES, bool HAS_P>
+template <int ES, bool HAS_P, bool TAB>
 __device__ __forceinline__ void exact_run_nf(const ExactArgs &a, const ExactDraw &d, int i, int g0, int g1, int lane,
-                                             const float2 *tab, float4 *xs) {
+                                             const float2 *tab, float4 *xs, const float2 *t1q, const float2 *t2q,
+                                             const float2 *t1p, const float2 *t2p) {
+    static_assert(!TAB || ES == 2, "tables for bf16 rows");
     static_assert(kExactGroup == 1, "one sub-chunk per unit");
     constexpr int EPV = 16 / ES;
     const uint4 *qrow = reinterpret_cast<const uint4 *>(d.q.row);
@@ -294,10 +375,25 @@ __device__ __forceinline__ void exact_run_nf(const ExactArgs &a, const ExactDraw
             }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const ff eq = ff_exp2_nf(xq[k], d.q.c, rq, d.q.rf, tab);
+                ff eq, ep;
+                if constexpr (TAB) {
+                    const uint32_t wq2 = (k < 2) ? (h ? wq.z : wq.x) : (h ? wq.w : wq.y);
+                    const uint32_t bq = (k & 1) ? (wq2 >> 16) : (wq2 & 0xFFFFu);
+                    bool ok;
+                    eq = tab_w(bq, t1q, t2q, ok);
+                    if (!ok) eq = exp2_direct(xq[k], d.q.c, rq, d.q.rf, tab);
+                    if (HAS_P) {
+                        const uint32_t wp2 = (k < 2) ? (h ? wp.z : wp.x) : (h ? wp.w : wp.y);
+                        const uint32_t bp = (k & 1) ? (wp2 >> 16) : (wp2 & 0xFFFFu);
+                        ep = tab_w(bp, t1p, t2p, ok);
+                        if (!ok) ep = exp2_direct(xp[k], d.p.c, rp, d.p.rf, tab);
+                    }
+                } else {
+                    eq = ff_exp2_nf(xq[k], d.q.c, rq, d.q.rf, tab);
+                    if (HAS_P) ep = ff_exp2_nf(xp[k], d.p.c, rp, d.p.rf, tab);
+                }
                 ff_acc(nq, eq);
                 if (HAS_P) {
-                    const ff ep = ff_exp2_nf(xp[k], d.p.c, rp, d.p.rf, tab);
                     ff_acc(np, ep);
                     const float wq1 = eq.hi * d.inv_q, wp1 = ep.hi * d.inv_p;
                     const float diff = wq1 - wp1, tol = d.sign_tol * (wq1 + wp1);
@@ -500,6 +596,25 @@ __global__ void __launch_bounds__(kThreads, 3) k_exact(const ExactArgs a) {
     const long long units_c = (long long)n_items * n_grp;
     // balanced ranges: every warp gets floor or ceil of units_c / nwarps
     const long long uc0 = units_c * gwarp / nwarps, uc1 = units_c * (gwarp + 1) / nwarps;
+    // bf16: the factored-weight tables of the (at most kTabSlots) items this block's units touch
+    __shared__ float2 s_t1[kTabSlots][2][kTab1];
+    __shared__ float2 s_t2[kTabSlots][2][kTab2];
+    int tab_i0 = 0, tab_n = 0;   // block-uniform
+    if constexpr (ES == 2) {
+        const long long ub0 = units_c * (blockIdx.x * kWarps) / nwarps;
+        const long long ub1 = units_c * ((blockIdx.x + 1) * kWarps) / nwarps;
+        if (ub1 > ub0 && (ub1 - 1) / n_grp - ub0 / n_grp < kTabSlots) {
+            tab_i0 = (int)(ub0 / n_grp);
+            tab_n = (int)((ub1 - 1) / n_grp) - tab_i0 + 1;
+            for (int ts = 0; ts < tab_n; ++ts) {
+                const ExactItem itm = a.items[tab_i0 + ts];
+                const ExactDraw d = itm.draw >= 0 ? exact_draw_from(a.draws[itm.draw]) : a.xdraw[tab_i0 + ts];
+                if (nf_rows(d))
+                    build_tables(d, s_t1[ts][0], s_t1[ts][1], s_t2[ts][0], s_t2[ts][1], tab, tid);
+            }
+            __syncthreads();
+        }
+    }
     for (long long u = uc0; u < uc1;) {
         const int i = (int)(u / n_grp);
         const long long u_end = min(uc1, (long long)(i + 1) * n_grp);
@@ -509,13 +624,25 @@ __global__ void __launch_bounds__(kThreads, 3) k_exact(const ExactArgs a) {
         const ExactItem itm = a.items[i];
         const ExactDraw d = itm.draw >= 0 ? exact_draw_from(a.draws[itm.draw]) : a.xdraw[i];
         float4 *xs = a.xsubs + (size_t)i * a.n_sub;
-        if (kExactGroup == 1 && !d.q.filt && !(d.has_p && d.p.filt) && fabsf(d.q.rf) < 0x1p19f &&
-            (!d.has_p || fabsf(d.p.rf) < 0x1p19f)) {
-            // rows without filters: the vector sub-chunks on the unrolled path
+        const int ts = i - tab_i0;
+        if (kExactGroup == 1 && nf_rows(d) && (ES == 4 || (ts >= 0 && ts < tab_n))) {
+            // rows without filters: the vector sub-chunks on the unrolled path (bf16: from the tables)
             const int gv_end = min(g_end, n_grp - 1);
             if (g < gv_end) {
-                if (d.has_p) exact_run_nf<ES, true>(a, d, i, g, gv_end, lane, tab, xs);
-                else exact_run_nf<ES, false>(a, d, i, g, gv_end, lane, tab, xs);
+                if constexpr (ES == 2) {
+                    const float2 *t2p = same_c(d) ? s_t2[ts][0] : s_t2[ts][1];
+                    if (d.has_p)
+                        exact_run_nf<ES, true, true>(a, d, i, g, gv_end, lane, tab, xs, s_t1[ts][0], s_t2[ts][0],
+                                                     s_t1[ts][1], t2p);
+                    else
+                        exact_run_nf<ES, false, true>(a, d, i, g, gv_end, lane, tab, xs, s_t1[ts][0], s_t2[ts][0],
+                                                      nullptr, nullptr);
+                } else {
+                    if (d.has_p) exact_run_nf<ES, true, false>(a, d, i, g, gv_end, lane, tab, xs, nullptr, nullptr,
+                                                              nullptr, nullptr);
+                    else exact_run_nf<ES, false, false>(a, d, i, g, gv_end, lane, tab, xs, nullptr, nullptr, nullptr,
+                                                        nullptr);
+                }
                 g = gv_end;
             }
         }

@@ -309,3 +309,76 @@ def test_accept_test_too_close_goes_float_float(lazy):
     else:
         compare(w, inp, ref, al, ot, dbg.cpu().numpy(), st)
         assert st["unresolved"] == 0, st
+
+
+def _inject_special_logits(x, rng):
+    """Logits the float-float tier's bf16 weight tables do not cover (zero, |x| < 2^-9, |x| >=
+    128, -inf) and large negative ones inside them, at a few random ids of every row."""
+    B, R, V = x.shape
+    for val in (0.0, 1e-4, -3e-4, -60.0, -100.0, -150.0, -300.0, float("-inf")):
+        ids = torch.as_tensor(rng.integers(0, V, size=(B, R, 3)), device=x.device)
+        x.scatter_(2, ids, torch.full(ids.shape, val, dtype=x.dtype, device=x.device))
+
+
+@pytest.mark.parametrize("lazy", [False, True])
+def test_draw_near_boundary_goes_float_float(lazy):
+    """u of the residual draw set 1e-8 (relative) above or below a boundary of the oracle's
+    own cumulative residual sum, so that the float32 tier cannot certify the draw and the
+    float-float tier decides it, at temperatures from 0.15 to 3 (bf16 rows without filters:
+    the tier's factored weight tables, with the direct exponential for the logits and
+    temperatures they leave out).  Every output equals the oracle's."""
+    w = W.scaled(W.LARGE_BATCH, B=30, K=3, V=20000, greedy_even_rows=False)
+    inp = make_inputs(w, 2)
+    rng = np.random.default_rng(7)
+    _inject_special_logits(inp["target"], rng)
+    _inject_special_logits(inp["draft"], rng)
+    temps = np.array([0.0, 0.15, 0.3, 0.6, 1.0, 1.7, 3.0], np.float32)
+    inp["T"] = temps[np.arange(w.B) % len(temps)]
+    ref0 = oracle_verify(inp, w)
+    K = w.K
+    moved = 0
+    drawn = {}
+    for b in range(w.B):
+        if inp["T"][b] == 0:
+            continue
+        k = int(ref0["accept_len"][b])
+        T = float(inp["T"][b])
+        q, _, _ = oracle.row_distribution(to_f64(inp["target"][b, k]), T, 1.0)
+        if k < K:
+            p, _, _ = oracle.row_distribution(to_f64(inp["draft"][b, k]), T, 1.0)
+            wr = np.maximum(q - p, 0.0)
+        else:
+            wr = q
+        c = np.cumsum(wr)
+        R = c[-1]
+        # a boundary C(t) between 5% and 95% of R, the one nearest the middle id whose draw
+        # (t just below it, the next id whose sum passes u R just above it) lies at least
+        # 5e-10 R from every boundary: the float-float tier resolves 2e-11
+        cand = np.nonzero((c > 0.05 * R) & (c < 0.95 * R) & (wr > 0))[0]
+        if R <= 0 or len(cand) == 0:
+            continue
+        found = None
+        for t in cand[np.argsort(np.abs(cand - cand[len(cand) // 2]), kind="stable")][:400]:
+            u_b = c[t] / R * (1.0 + (1e-8 if b % 2 else -1e-8))
+            thr = u_b * R
+            v = int(np.searchsorted(c, thr, side="right"))
+            if v < len(c) and min(c[v] - thr, thr - (c[v - 1] if v > 0 else 0.0)) >= 5e-10 * R:
+                found = (u_b, v)
+                break
+        if found is None:
+            continue
+        inp["u"][b, K], drawn[b] = found
+        moved += 1
+    assert moved >= 12, moved
+    ref = oracle_verify(inp, w)
+    for b, t in drawn.items():
+        assert ref["out_tokens"][b, ref["accept_len"][b]] == t, (b, t)
+    a = gpu_args(inp)
+    al, ot, dbg, st = sv.sv_verify(inp["target"], inp["draft"], a["draft_tokens"], a["uniforms"], a["temperature"],
+                                   debug=not lazy, lazy=lazy)
+    torch.cuda.synchronize()
+    al, ot, st = al.cpu().numpy(), ot.cpu().numpy(), sv.read_stats(st)
+    assert st["reresolved"] >= moved, st
+    assert st["status"] == 0 and st["unresolved"] == 0, st
+    np.testing.assert_array_equal(al, ref["accept_len"])
+    np.testing.assert_array_equal(ot, ref["out_tokens"])

@@ -15,7 +15,9 @@
 //      float-float rescan, t*.
 // Results agree with a float64 evaluation except when u R lies within 2e-11 relative of a
 // boundary; such decisions are counted in sv_stats.unresolved.  Element exponentials use
-// Tang's table method in float-float (sv_device.cuh); no float64 work runs per element.
+// Tang's table method in float-float (sv_device.cuh); in phase C the weights of bf16 rows
+// without filters come from per-block tables of two exact factors (see tab_w); no float64
+// work runs per element.
 #pragma once
 
 #include "sv_device.cuh"

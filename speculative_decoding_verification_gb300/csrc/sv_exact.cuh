@@ -253,8 +253,10 @@ __device__ __forceinline__ ff ff_exp2_nf(float x, ff c, int r, float rf, const f
 // over (s, E, m_l), each entry a float-float exponential, turn a token's weight into two
 // shared-memory loads and a float-float product: the relative error stays a few times 2^-44,
 // like the direct exponential's.  Exponents outside the tables, entries whose factor could
-// leave [2^-100, 2^64] (first) or [2^-32, 2^32] (second, so that a product neither overflows
-// nor leaves the normal range), and -inf or zero logits take the direct exponential.
+// leave [2^-100, 2^64] (first) or [2^-32, 2^32] (second), and -inf or zero logits take the
+// direct exponential, so a product stays in [2^-132, 2^96]: it cannot overflow, and below
+// 2^-126, where the direct exponential flushes to zero, the two differ by less than 2^-126
+// of a row sum that is at least 1/2.
 constexpr int kTabE0 = 118;                   // |x| in [2^-9, 2^7)
 constexpr int kTabNE = 16;
 constexpr int kTabGroups = 2 * kTabNE;        // (s, E)
